@@ -1,0 +1,222 @@
+"""Python face of the fp64 oracle (ctypes over ring_attn_oracle.c).
+
+TEST INFRASTRUCTURE ONLY.  Only tests, the smoke check and the benchmark's
+CPU-baseline leg may call it.
+
+Citations name the web page "Large-scale distributed AI model training
+series: sequence parallelism" (the "SP series") and its sections:
+  * section 2.3 (Ring Self-Attention): attention is Q K^T then Score V; each
+    of N devices holds L/N tokens and the key/value blocks travel round a
+    ring, N-1 transfers and N block computations per device;
+  * section 6.2 (Ring Attention): one ring carries K and V together and the
+    per-step partial results are merged with the online-softmax correction;
+  * section 8.2 (USP): for a causal model the sequence is split by folding
+    it, so that every device gets the same amount of work.
+
+Inputs are numpy float64 arrays holding the bf16 values (the caller widens
+them); layout q/o/dO [B,Hq,L,d], k/v [B,Hkv,L,d], lse [B,Hq,L].
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ring_attn_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lib = None
+
+_dp = ctypes.POINTER(ctypes.c_double)
+_ip = ctypes.POINTER(ctypes.c_int)
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle into oracle/_build/liboracle.so (plain gcc)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["gcc", "-O2", "-std=c11", "-shared", "-fPIC", "-o", tmp, _SRC, "-lm", "-lpthread"]
+        )
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _bind(lib):
+    I = ctypes.c_int
+    lib.oracle_fwd.argtypes = [_dp, _dp, _dp, I, I, I, I, I, I, _dp, _dp, I]
+    lib.oracle_fwd_rows.argtypes = [_dp, _dp, _dp, I, I, I, I, I, I, _ip, I, _dp, _dp, I]
+    lib.oracle_bwd.argtypes = [_dp, _dp, _dp, _dp, I, I, I, I, I, I, _dp, _dp, _dp, _dp, _dp, I]
+    lib.oracle_bwd_rows.argtypes = [_dp, _dp, _dp, _dp, I, I, I, I, I, I, _ip, I, _ip, I,
+                                    _dp, _dp, _dp, I]
+    lib.oracle_ring_fwd.argtypes = [_dp, _dp, _dp, I, I, I, I, I, I, I, _dp, _dp, I]
+    lib.oracle_owner_rank.argtypes = [I, I, I, I]
+    for f in (lib.oracle_fwd, lib.oracle_fwd_rows, lib.oracle_bwd, lib.oracle_bwd_rows,
+              lib.oracle_ring_fwd, lib.oracle_owner_rank):
+        f.restype = ctypes.c_int
+    return lib
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        _lib = _bind(ctypes.CDLL(build()))
+    return _lib
+
+
+def _swap_library(path):
+    """Point this module at another build of the oracle source (used by the
+    mutation test, which plants mistakes in a copy); returns the previous
+    handle so the caller can restore it."""
+    global _lib
+    prev = _lib
+    _lib = _bind(ctypes.CDLL(path)) if path else None
+    return prev
+
+
+def _restore_library(handle):
+    global _lib
+    _lib = handle
+
+
+def _f64(a) -> np.ndarray:
+    a = np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+    return a
+
+
+def _p(a: np.ndarray):
+    return a.ctypes.data_as(_dp)
+
+
+def _shape(q, k):
+    B, Hq, L, d = q.shape
+    Bk, Hkv, Lk, dk = k.shape
+    if (B, L, d) != (Bk, Lk, dk) or Hq % Hkv:
+        raise ValueError(f"incompatible shapes q{q.shape} k{k.shape}")
+    return B, Hq, Hkv, L, d
+
+
+def _threads(n):
+    if n:
+        return int(n)
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def _check(rc):
+    if rc < 0:
+        raise ValueError(f"oracle rejected its arguments (rc={rc})")
+    return rc
+
+
+def fwd(q, k, v, causal: bool, threads: int = 0):
+    """Plain definition of softmax(Q K^T / sqrt(d)) V (SP series section 2.3).
+
+    Returns (o [B,Hq,L,d], lse [B,Hq,L]); lse is the natural log-sum-exp of
+    the scaled scores."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, Hq, Hkv, L, d = _shape(q, k)
+    o = np.zeros((B, Hq, L, d))
+    lse = np.zeros((B, Hq, L))
+    _check(_load().oracle_fwd(_p(q), _p(k), _p(v), B, Hq, Hkv, L, d, int(causal), _p(o), _p(lse),
+                              _threads(threads)))
+    return o, lse
+
+
+def fwd_rows(q, k, v, causal: bool, rows, threads: int = 0):
+    """The plain definition on selected query rows (same rows for every head).
+
+    Returns (o_rows [B,Hq,R,d], lse_rows [B,Hq,R]) and the thread count used."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, Hq, Hkv, L, d = _shape(q, k)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int32))
+    R = rows.size
+    o = np.zeros((B, Hq, R, d))
+    lse = np.zeros((B, Hq, R))
+    nt = _check(_load().oracle_fwd_rows(_p(q), _p(k), _p(v), B, Hq, Hkv, L, d, int(causal),
+                                        rows.ctypes.data_as(_ip), R, _p(o), _p(lse),
+                                        _threads(threads)))
+    return o, lse, nt
+
+
+def bwd(q, k, v, dO, causal: bool, threads: int = 0):
+    """Hand-derived backward of l = sum(dO * O).
+
+    Returns (dq, dk, dv, lse, D) in fp64; D_i = dO_i . o_i."""
+    q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
+    B, Hq, Hkv, L, d = _shape(q, k)
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    lse = np.zeros((B, Hq, L))
+    D = np.zeros((B, Hq, L))
+    _check(_load().oracle_bwd(_p(q), _p(k), _p(v), _p(dO), B, Hq, Hkv, L, d, int(causal), _p(dq),
+                              _p(dk), _p(dv), _p(lse), _p(D), _threads(threads)))
+    return dq, dk, dv, lse, D
+
+
+def bwd_rows(q, k, v, dO, causal: bool, q_rows, k_rows, threads: int = 0):
+    """Backward on sampled rows: dq on q_rows, dk/dv on k_rows.
+
+    Returns (dq_rows [B,Hq,Rq,d], dk_rows [B,Hkv,Rk,d], dv_rows [B,Hkv,Rk,d])."""
+    q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
+    B, Hq, Hkv, L, d = _shape(q, k)
+    qr = np.ascontiguousarray(np.asarray(q_rows, dtype=np.int32))
+    kr = np.ascontiguousarray(np.asarray(k_rows, dtype=np.int32))
+    dq = np.zeros((B, Hq, qr.size, d))
+    dk = np.zeros((B, Hkv, kr.size, d))
+    dv = np.zeros((B, Hkv, kr.size, d))
+    _check(_load().oracle_bwd_rows(_p(q), _p(k), _p(v), _p(dO), B, Hq, Hkv, L, d, int(causal),
+                                   qr.ctypes.data_as(_ip), qr.size, kr.ctypes.data_as(_ip), kr.size,
+                                   _p(dq), _p(dk), _p(dv), _threads(threads)))
+    return dq, dk, dv
+
+
+def ring_fwd(q, k, v, causal: bool, n_chunks: int, threads: int = 0):
+    """Ring form: per ring step partial (o_s, lse_s) merged by log-sum-exp
+    (SP series sections 2.3 and 6.2; causal ranks own folded sub-chunks,
+    section 8.2)."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, Hq, Hkv, L, d = _shape(q, k)
+    o = np.zeros((B, Hq, L, d))
+    lse = np.zeros((B, Hq, L))
+    _check(_load().oracle_ring_fwd(_p(q), _p(k), _p(v), B, Hq, Hkv, L, d, int(causal), int(n_chunks),
+                                   _p(o), _p(lse), _threads(threads)))
+    return o, lse
+
+
+# ------------------------------------------------------------ chunk map (host)
+
+def owner_rank(L: int, n_chunks: int, causal: bool, p: int) -> int:
+    """Rank owning sequence position p: chunk p // (L/N) for the encoder;
+    for causal the folded pair {r, 2N-1-r} of sub-chunks of length L/(2N)
+    (SP series section 8.2)."""
+    r = _load().oracle_owner_rank(int(L), int(n_chunks), int(causal), int(p))
+    if r < 0:
+        raise ValueError("bad chunk map arguments")
+    return r
+
+
+def ring_sources(r: int, n_chunks: int):
+    """Ring visiting order of rank r: at step s it holds the key/value block of
+    rank (r - s) mod N, starting with its own (SP series section 2.3)."""
+    return [(r - s) % n_chunks for s in range(n_chunks)]
+
+
+def visible_pairs(L: int, causal: bool, tile: int):
+    """Set of (query tile, key tile) pairs that hold at least one visible
+    (i, j) position: all pairs for the encoder, key tile <= query tile for a
+    causal model (position j <= i)."""
+    nt = (L + tile - 1) // tile
+    out = set()
+    for a in range(nt):
+        for b in range(nt):
+            if not causal or b * tile <= min((a + 1) * tile, L) - 1:
+                out.add((a, b))
+    return out

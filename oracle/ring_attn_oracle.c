@@ -1,0 +1,442 @@
+/*
+ * ring_attn_oracle.c -- plain fp64 CPU oracle for blockwise Ring Self-Attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
+ * call this file; only the test suite, the smoke check and the CPU-baseline
+ * leg of the benchmark use it.  It shares no code, header or constant with
+ * the CUDA library.
+ *
+ * What it computes (all arithmetic in double precision on the bf16 input
+ * values, which the caller passes already widened to double):
+ *
+ *   Self-attention as two matrix products, softmax(Q K^T / sqrt(d)) V
+ *   ("Sequence parallelism" series, section 2.3 Ring Self-Attention: the
+ *   computation is Q*K^T followed by AttentionScore*V).  For batch b, query
+ *   head h and query row i, with kv head g = floor(h / (Hq/Hkv)) (grouped
+ *   query attention with consecutive grouping) and scale = 1/sqrt(d):
+ *
+ *     s_ij  = scale * sum_c q[b,h,i,c] * k[b,g,j,c]     for j in V(i)
+ *     V(i)  = {0..L-1} (encoder, no mask)  or  {0..i} (causal decoder)
+ *     lse_i = log sum_{j in V(i)} exp(s_ij)   (natural log, max-subtracted)
+ *     P_ij  = exp(s_ij - lse_i)
+ *     o_i   = sum_j P_ij v[b,g,j,:]
+ *
+ *   Backward of the loss l = sum(dO * O), derived by hand (the pages only
+ *   say that the backward pass recomputes the attention; Ring Attention
+ *   section 6.2 and the BPT section 4.3 use activation recomputation):
+ *
+ *     D_i   = sum_c dO_ic * o_ic          (o from this oracle, in fp64)
+ *     dP_ij = dO_i . v_j
+ *     dS_ij = P_ij * (dP_ij - D_i)
+ *     dq_i  = scale * sum_j dS_ij k_j
+ *     dk_j  = scale * sum_{h in group(g)} sum_i dS_ij q_i
+ *     dv_j  =         sum_{h in group(g)} sum_i P_ij dO_i
+ *
+ *   Ring form (Ring Self-Attention, section 2.3; Ring Attention, section
+ *   6.2): the sequence is cut into N chunks, rank r owns chunk r (encoder)
+ *   or the folded pair of sub-chunks {r, 2N-1-r} of length L/(2N) (causal,
+ *   the fold of the USP section 8.2).  At ring step s = 0..N-1 rank r holds
+ *   the keys/values of rank (r - s) mod N, computes the partial result of
+ *   that block (o_s, lse_s) and merges it into its running result with the
+ *   log-sum-exp rule (the online-softmax correction of section 6.2):
+ *
+ *     lse <- log(exp(lse) + exp(lse_s)),
+ *     o   <- exp(lse_old - lse) * o + exp(lse_s - lse) * o_s.
+ *
+ * Layout: q, o, dO, dq are [B][Hq][L][d]; k, v, dk, dv are [B][Hkv][L][d];
+ * lse and D are [B][Hq][L]; all contiguous, row-major.
+ *
+ * Parallelism: plain pthreads over independent rows; no blocking, fusion
+ * or reordering of the arithmetic of one row.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+typedef struct {
+  const double *q, *k, *v, *dO;
+  int B, Hq, Hkv, L, d, causal;
+  double scale;
+} problem_t;
+
+static const double *q_row(const problem_t *P, int b, int h, int i) {
+  return P->q + (((size_t)b * P->Hq + h) * P->L + i) * (size_t)P->d;
+}
+static const double *do_row(const problem_t *P, int b, int h, int i) {
+  return P->dO + (((size_t)b * P->Hq + h) * P->L + i) * (size_t)P->d;
+}
+static const double *k_row(const problem_t *P, int b, int g, int j) {
+  return P->k + (((size_t)b * P->Hkv + g) * P->L + j) * (size_t)P->d;
+}
+static const double *v_row(const problem_t *P, int b, int g, int j) {
+  return P->v + (((size_t)b * P->Hkv + g) * P->L + j) * (size_t)P->d;
+}
+static double dot(const double *a, const double *b, int n) {
+  double s = 0.0;
+  for (int c = 0; c < n; ++c) s += a[c] * b[c];
+  return s;
+}
+/* Number of keys row i may attend to: j in [0, n_visible). */
+static int n_visible(const problem_t *P, int i) { return P->causal ? i + 1 : P->L; }
+
+/* ---------------------------------------------------------------- forward */
+
+/* One query row of the plain definition.  s is scratch of length L. */
+static void fwd_row(const problem_t *P, int b, int h, int i, double *s, double *o, double *lse_out) {
+  const int g = h / (P->Hq / P->Hkv);
+  const double *qi = q_row(P, b, h, i);
+  const int n = n_visible(P, i);
+  double m = -INFINITY;
+  for (int j = 0; j < n; ++j) {
+    s[j] = P->scale * dot(qi, k_row(P, b, g, j), P->d);
+    if (s[j] > m) m = s[j];
+  }
+  double sum = 0.0;
+  for (int j = 0; j < n; ++j) sum += exp(s[j] - m);
+  const double lse = m + log(sum);
+  for (int c = 0; c < P->d; ++c) o[c] = 0.0;
+  for (int j = 0; j < n; ++j) {
+    const double p = exp(s[j] - lse);
+    const double *vj = v_row(P, b, g, j);
+    for (int c = 0; c < P->d; ++c) o[c] += p * vj[c];
+  }
+  *lse_out = lse;
+}
+
+/* ------------------------------------------------------------ thread pool */
+
+typedef struct task_s task_t;
+typedef void (*task_fn)(task_t *t, long item, double *scratch);
+struct task_s {
+  const problem_t *P;
+  long n_items;
+  long next; /* atomic work counter */
+  task_fn fn;
+  size_t scratch_len;
+  /* per-task arguments */
+  const int *rows; int n_rows;
+  double *o, *lse, *D, *dq, *dk, *dv;
+  int n_chunks;
+  const int *stat_lo; /* per (b,h): first query row whose stats exist (rows mode) */
+};
+
+static void *worker(void *arg) {
+  task_t *t = (task_t *)arg;
+  double *scratch = (double *)malloc(sizeof(double) * (t->scratch_len ? t->scratch_len : 1));
+  for (;;) {
+    long it = __atomic_fetch_add(&t->next, 1, __ATOMIC_RELAXED);
+    if (it >= t->n_items) break;
+    t->fn(t, it, scratch);
+  }
+  free(scratch);
+  return NULL;
+}
+
+static int run_parallel(task_t *t, int n_threads) {
+  if (n_threads <= 0) n_threads = (int)sysconf(_SC_NPROCESSORS_ONLN);
+  if (n_threads < 1) n_threads = 1;
+  if (n_threads > 256) n_threads = 256;
+  if ((long)n_threads > t->n_items) n_threads = (int)(t->n_items > 0 ? t->n_items : 1);
+  t->next = 0;
+  pthread_t th[256];
+  int started = 0;
+  for (int i = 1; i < n_threads; ++i)
+    if (pthread_create(&th[i], NULL, worker, t) == 0) started = i; else break;
+  worker(t);
+  for (int i = 1; i <= started; ++i) pthread_join(th[i], NULL);
+  return n_threads;
+}
+
+static problem_t make_problem(const double *q, const double *k, const double *v, const double *dO,
+                              int B, int Hq, int Hkv, int L, int d, int causal) {
+  problem_t P;
+  P.q = q; P.k = k; P.v = v; P.dO = dO;
+  P.B = B; P.Hq = Hq; P.Hkv = Hkv; P.L = L; P.d = d; P.causal = causal;
+  P.scale = 1.0 / sqrt((double)d);
+  return P;
+}
+
+static int bad_shape(int B, int Hq, int Hkv, int L, int d) {
+  return B < 0 || Hq <= 0 || Hkv <= 0 || L < 0 || d <= 0 || Hq % Hkv != 0;
+}
+
+/* Full forward: every row of every (b, h). */
+static void fwd_full_item(task_t *t, long item, double *s) {
+  const problem_t *P = t->P;
+  const int i = (int)(item % P->L);
+  const long bh = item / P->L;
+  const int h = (int)(bh % P->Hq), b = (int)(bh / P->Hq);
+  const size_t r = (size_t)bh * P->L + i;
+  fwd_row(P, b, h, i, s, t->o + r * P->d, t->lse + r);
+}
+
+int oracle_fwd(const double *q, const double *k, const double *v, int B, int Hq, int Hkv, int L, int d,
+               int causal, double *o, double *lse, int n_threads) {
+  if (bad_shape(B, Hq, Hkv, L, d)) return -1;
+  problem_t P = make_problem(q, k, v, NULL, B, Hq, Hkv, L, d, causal);
+  task_t t; memset(&t, 0, sizeof t);
+  t.P = &P; t.n_items = (long)B * Hq * L; t.fn = fwd_full_item; t.scratch_len = (size_t)L;
+  t.o = o; t.lse = lse;
+  return run_parallel(&t, n_threads);
+}
+
+/* Forward on a list of query rows, the same list for every (b, h).
+ * o_rows is [B][Hq][n_rows][d], lse_rows is [B][Hq][n_rows]. */
+static void fwd_rows_item(task_t *t, long item, double *s) {
+  const problem_t *P = t->P;
+  const int ri = (int)(item % t->n_rows);
+  const long bh = item / t->n_rows;
+  const int h = (int)(bh % P->Hq), b = (int)(bh / P->Hq);
+  const size_t r = (size_t)bh * t->n_rows + ri;
+  fwd_row(P, b, h, t->rows[ri], s, t->o + r * P->d, t->lse + r);
+}
+
+int oracle_fwd_rows(const double *q, const double *k, const double *v, int B, int Hq, int Hkv, int L, int d,
+                    int causal, const int *rows, int n_rows, double *o_rows, double *lse_rows,
+                    int n_threads) {
+  if (bad_shape(B, Hq, Hkv, L, d) || n_rows < 0) return -1;
+  for (int i = 0; i < n_rows; ++i) if (rows[i] < 0 || rows[i] >= L) return -1;
+  problem_t P = make_problem(q, k, v, NULL, B, Hq, Hkv, L, d, causal);
+  task_t t; memset(&t, 0, sizeof t);
+  t.P = &P; t.n_items = (long)B * Hq * n_rows; t.fn = fwd_rows_item; t.scratch_len = (size_t)L;
+  t.rows = rows; t.n_rows = n_rows; t.o = o_rows; t.lse = lse_rows;
+  return run_parallel(&t, n_threads);
+}
+
+/* --------------------------------------------------------------- backward */
+
+/* Statistics of one query row needed by the backward: lse_i and D_i. */
+static void stats_row(const problem_t *P, int b, int h, int i, double *s, double *lse, double *D) {
+  double *o = s + P->L; /* scratch holds L + d doubles */
+  fwd_row(P, b, h, i, s, o, lse);
+  *D = dot(do_row(P, b, h, i), o, P->d);
+}
+
+/* dq for one query row, given its lse and D. */
+static void dq_row(const problem_t *P, int b, int h, int i, double lse, double D, double *dq) {
+  const int g = h / (P->Hq / P->Hkv);
+  const double *qi = q_row(P, b, h, i), *doi = do_row(P, b, h, i);
+  for (int c = 0; c < P->d; ++c) dq[c] = 0.0;
+  const int n = n_visible(P, i);
+  for (int j = 0; j < n; ++j) {
+    const double sij = P->scale * dot(qi, k_row(P, b, g, j), P->d);
+    const double pij = exp(sij - lse);
+    const double dpij = dot(doi, v_row(P, b, g, j), P->d);
+    const double dsij = pij * (dpij - D);
+    const double *kj = k_row(P, b, g, j);
+    for (int c = 0; c < P->d; ++c) dq[c] += P->scale * dsij * kj[c];
+  }
+}
+
+/* dk and dv for one key row j of kv head g.  lse and D are indexed
+ * [(b*Hq + h)*L + i] and must be valid for every query row that sees j. */
+static void dkdv_row(const problem_t *P, int b, int g, int j, const double *lse, const double *D,
+                     double *dk, double *dv) {
+  const int G = P->Hq / P->Hkv;
+  const double *kj = k_row(P, b, g, j), *vj = v_row(P, b, g, j);
+  for (int c = 0; c < P->d; ++c) { dk[c] = 0.0; dv[c] = 0.0; }
+  for (int h = g * G; h < (g + 1) * G; ++h) {
+    const size_t base = ((size_t)b * P->Hq + h) * P->L;
+    for (int i = P->causal ? j : 0; i < P->L; ++i) {
+      const double *qi = q_row(P, b, h, i), *doi = do_row(P, b, h, i);
+      const double sij = P->scale * dot(qi, kj, P->d);
+      const double pij = exp(sij - lse[base + i]);
+      const double dpij = dot(doi, vj, P->d);
+      const double dsij = pij * (dpij - D[base + i]);
+      for (int c = 0; c < P->d; ++c) {
+        dv[c] += pij * doi[c];
+        dk[c] += P->scale * dsij * qi[c];
+      }
+    }
+  }
+}
+
+static void stats_item(task_t *t, long item, double *s) {
+  const problem_t *P = t->P;
+  const long bh = item / P->L;
+  const int i = (int)(item % P->L);
+  const int h = (int)(bh % P->Hq), b = (int)(bh / P->Hq);
+  if (t->stat_lo && i < t->stat_lo[bh]) return;
+  const size_t r = (size_t)bh * P->L + i;
+  stats_row(P, b, h, i, s, t->lse + r, t->D + r);
+}
+static void dq_full_item(task_t *t, long item, double *s) {
+  (void)s;
+  const problem_t *P = t->P;
+  const long bh = item / P->L;
+  const int i = (int)(item % P->L);
+  const int h = (int)(bh % P->Hq), b = (int)(bh / P->Hq);
+  const size_t r = (size_t)bh * P->L + i;
+  dq_row(P, b, h, i, t->lse[r], t->D[r], t->dq + r * P->d);
+}
+static void dkdv_full_item(task_t *t, long item, double *s) {
+  (void)s;
+  const problem_t *P = t->P;
+  const long bg = item / P->L;
+  const int j = (int)(item % P->L);
+  const int g = (int)(bg % P->Hkv), b = (int)(bg / P->Hkv);
+  const size_t r = (size_t)bg * P->L + j;
+  dkdv_row(P, b, g, j, t->lse, t->D, t->dk + r * P->d, t->dv + r * P->d);
+}
+
+/* Full backward.  Also returns the oracle's own lse and D ([B][Hq][L]). */
+int oracle_bwd(const double *q, const double *k, const double *v, const double *dO, int B, int Hq,
+               int Hkv, int L, int d, int causal, double *dq, double *dk, double *dv, double *lse,
+               double *D, int n_threads) {
+  if (bad_shape(B, Hq, Hkv, L, d)) return -1;
+  problem_t P = make_problem(q, k, v, dO, B, Hq, Hkv, L, d, causal);
+  task_t t; memset(&t, 0, sizeof t);
+  t.P = &P; t.lse = lse; t.D = D; t.dq = dq; t.dk = dk; t.dv = dv;
+  t.scratch_len = (size_t)L + d;
+  t.n_items = (long)B * Hq * L; t.fn = stats_item; run_parallel(&t, n_threads);
+  t.n_items = (long)B * Hq * L; t.fn = dq_full_item; run_parallel(&t, n_threads);
+  t.n_items = (long)B * Hkv * L; t.fn = dkdv_full_item;
+  return run_parallel(&t, n_threads);
+}
+
+/* Sampled backward: dq on query rows q_rows (same list for every (b, h)),
+ * dk/dv on key rows k_rows (same list for every (b, g)).  The statistics
+ * are computed for every query row that can see one of the sampled keys
+ * (for causal: rows >= min(k_rows); otherwise all rows) and for q_rows.
+ * Outputs: dq_rows [B][Hq][n_q][d], dk_rows/dv_rows [B][Hkv][n_k][d]. */
+static void dq_rows_item(task_t *t, long item, double *s) {
+  const problem_t *P = t->P;
+  const int ri = (int)(item % t->n_rows);
+  const long bh = item / t->n_rows;
+  const int h = (int)(bh % P->Hq), b = (int)(bh / P->Hq);
+  double lse, D;
+  stats_row(P, b, h, t->rows[ri], s, &lse, &D);
+  dq_row(P, b, h, t->rows[ri], lse, D, t->dq + ((size_t)bh * t->n_rows + ri) * P->d);
+}
+static void dkdv_rows_item(task_t *t, long item, double *s) {
+  (void)s;
+  const problem_t *P = t->P;
+  const int ri = (int)(item % t->n_rows);
+  const long bg = item / t->n_rows;
+  const int g = (int)(bg % P->Hkv), b = (int)(bg / P->Hkv);
+  const size_t r = (size_t)bg * t->n_rows + ri;
+  dkdv_row(P, b, g, t->rows[ri], t->lse, t->D, t->dk + r * P->d, t->dv + r * P->d);
+}
+
+int oracle_bwd_rows(const double *q, const double *k, const double *v, const double *dO, int B, int Hq,
+                    int Hkv, int L, int d, int causal, const int *q_rows, int n_q, const int *k_rows,
+                    int n_k, double *dq_rows, double *dk_rows, double *dv_rows, int n_threads) {
+  if (bad_shape(B, Hq, Hkv, L, d) || n_q < 0 || n_k < 0) return -1;
+  for (int i = 0; i < n_q; ++i) if (q_rows[i] < 0 || q_rows[i] >= L) return -1;
+  int kmin = L;
+  for (int i = 0; i < n_k; ++i) {
+    if (k_rows[i] < 0 || k_rows[i] >= L) return -1;
+    if (k_rows[i] < kmin) kmin = k_rows[i];
+  }
+  problem_t P = make_problem(q, k, v, dO, B, Hq, Hkv, L, d, causal);
+  task_t t; memset(&t, 0, sizeof t);
+  t.P = &P; t.scratch_len = (size_t)L + d;
+  int nt = 1;
+  if (n_q > 0) {
+    t.rows = q_rows; t.n_rows = n_q; t.dq = dq_rows;
+    t.n_items = (long)B * Hq * n_q; t.fn = dq_rows_item;
+    nt = run_parallel(&t, n_threads);
+  }
+  if (n_k > 0) {
+    const size_t nrow = (size_t)B * Hq * L;
+    double *lse = (double *)malloc(sizeof(double) * nrow);
+    double *D = (double *)malloc(sizeof(double) * nrow);
+    int *lo = (int *)malloc(sizeof(int) * (size_t)B * Hq);
+    if (!lse || !D || !lo) { free(lse); free(D); free(lo); return -2; }
+    for (size_t r = 0; r < nrow; ++r) { lse[r] = NAN; D[r] = NAN; }
+    for (long bh = 0; bh < (long)B * Hq; ++bh) lo[bh] = causal ? kmin : 0;
+    t.lse = lse; t.D = D; t.stat_lo = lo;
+    t.n_items = (long)B * Hq * L; t.fn = stats_item; run_parallel(&t, n_threads);
+    t.stat_lo = NULL;
+    t.rows = k_rows; t.n_rows = n_k; t.dk = dk_rows; t.dv = dv_rows;
+    t.n_items = (long)B * Hkv * n_k; t.fn = dkdv_rows_item;
+    nt = run_parallel(&t, n_threads);
+    free(lse); free(D); free(lo);
+  }
+  return nt;
+}
+
+/* --------------------------------------------------------------- ring form */
+
+/* Rank that owns sequence position p. */
+static int owner_rank(int L, int N, int causal, int p) {
+  if (!causal) return p / (L / N);
+  const int sub = p / (L / (2 * N));
+  return sub < N ? sub : 2 * N - 1 - sub;
+}
+
+/* Partial attention of query row i against the keys of rank src that i may
+ * see.  Returns 0 if there is none; otherwise writes (o_s, lse_s). */
+static int ring_block(const problem_t *P, int N, int b, int h, int i, int src, double *s, double *o_s,
+                      double *lse_s) {
+  const int g = h / (P->Hq / P->Hkv);
+  const double *qi = q_row(P, b, h, i);
+  double m = -INFINITY;
+  int cnt = 0;
+  for (int j = 0; j < P->L; ++j) {
+    s[j] = -INFINITY;
+    if (owner_rank(P->L, N, P->causal, j) != src) continue;
+    if (P->causal && j > i) continue;
+    s[j] = P->scale * dot(qi, k_row(P, b, g, j), P->d);
+    if (s[j] > m) m = s[j];
+    ++cnt;
+  }
+  if (cnt == 0) return 0;
+  double sum = 0.0;
+  for (int j = 0; j < P->L; ++j) if (s[j] != -INFINITY) sum += exp(s[j] - m);
+  *lse_s = m + log(sum);
+  for (int c = 0; c < P->d; ++c) o_s[c] = 0.0;
+  for (int j = 0; j < P->L; ++j) {
+    if (s[j] == -INFINITY) continue;
+    const double p = exp(s[j] - *lse_s);
+    const double *vj = v_row(P, b, g, j);
+    for (int c = 0; c < P->d; ++c) o_s[c] += p * vj[c];
+  }
+  return 1;
+}
+
+static void ring_item(task_t *t, long item, double *s) {
+  const problem_t *P = t->P;
+  const int N = t->n_chunks;
+  const int i = (int)(item % P->L);
+  const long bh = item / P->L;
+  const int h = (int)(bh % P->Hq), b = (int)(bh / P->Hq);
+  const int r = owner_rank(P->L, N, P->causal, i);
+  double *o_s = s + P->L;
+  double *o = t->o + ((size_t)bh * P->L + i) * P->d;
+  double lse = -INFINITY;
+  for (int c = 0; c < P->d; ++c) o[c] = 0.0;
+  for (int step = 0; step < N; ++step) {
+    const int src = ((r - step) % N + N) % N;
+    double lse_s;
+    if (!ring_block(P, N, b, h, i, src, s, o_s, &lse_s)) continue;
+    const double hi = lse > lse_s ? lse : lse_s;
+    const double merged = hi + log(exp(lse - hi) + exp(lse_s - hi));
+    const double a = exp(lse - merged), w = exp(lse_s - merged);
+    for (int c = 0; c < P->d; ++c) o[c] = a * o[c] + w * o_s[c];
+    lse = merged;
+  }
+  t->lse[(size_t)bh * P->L + i] = lse;
+}
+
+/* Ring form of the forward with n_chunks ranks.  Requires L % n_chunks == 0
+ * (encoder) or L % (2 n_chunks) == 0 (causal, folded sub-chunks). */
+int oracle_ring_fwd(const double *q, const double *k, const double *v, int B, int Hq, int Hkv, int L,
+                    int d, int causal, int n_chunks, double *o, double *lse, int n_threads) {
+  if (bad_shape(B, Hq, Hkv, L, d) || n_chunks <= 0) return -1;
+  if (L % (causal ? 2 * n_chunks : n_chunks) != 0) return -1;
+  problem_t P = make_problem(q, k, v, NULL, B, Hq, Hkv, L, d, causal);
+  task_t t; memset(&t, 0, sizeof t);
+  t.P = &P; t.n_items = (long)B * Hq * L; t.fn = ring_item; t.scratch_len = (size_t)L + d;
+  t.o = o; t.lse = lse; t.n_chunks = n_chunks;
+  return run_parallel(&t, n_threads);
+}
+
+int oracle_owner_rank(int L, int n_chunks, int causal, int p) {
+  if (n_chunks <= 0 || p < 0 || p >= L) return -1;
+  if (L % (causal ? 2 * n_chunks : n_chunks) != 0) return -1;
+  return owner_rank(L, n_chunks, causal, p);
+}

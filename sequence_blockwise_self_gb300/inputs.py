@@ -1,0 +1,98 @@
+"""Seeded synthetic inputs and row samplers.
+
+Shared by the tests, the benchmark and the smoke check, and by both sides of
+every parity comparison (the CUDA library and the fp64 oracle).  This module
+holds no attention arithmetic: it only draws numbers and picks row indices.
+
+Recipe: q, k, v and dO are drawn as float32 N(0, 1) from a CPU
+``torch.Generator`` seeded with ``seed``, in the order q, k, v, dO, and then
+rounded to bfloat16 (round to nearest even).  Layout is [B, H, L, d].
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    L: int
+    d: int
+    n_chunks: int
+    causal: bool
+
+    def fwd_flops(self) -> float:
+        """4 B Hq L^2 d, halved when causal (the benchmark's FLOP count)."""
+        f = 4.0 * self.B * self.Hq * self.L * self.L * self.d
+        return f / 2 if self.causal else f
+
+    def bwd_flops(self) -> float:
+        return 2.5 * self.fwd_flops()
+
+
+# The five synthetic workloads: shapes of a BERT-large encoder, a causal MHA
+# decoder and the Qwen2-7B attention (28 query heads, 4 kv heads, d = 128).
+WORKLOADS = {
+    "tiny": Workload("tiny", 1, 2, 2, 256, 64, 4, False),
+    "encoder": Workload("encoder", 8, 16, 16, 4096, 64, 8, False),
+    "decoder_mha": Workload("decoder_mha", 4, 32, 32, 8192, 128, 8, True),
+    "gqa_32k": Workload("gqa_32k", 1, 28, 4, 32768, 128, 16, True),
+    "gqa_128k": Workload("gqa_128k", 1, 28, 4, 131072, 128, 32, True),
+}
+WORKLOAD_SEEDS = {"tiny": 0, "encoder": 1, "decoder_mha": 2, "gqa_32k": 3, "gqa_128k": 4}
+
+
+def make_inputs(B, Hq, Hkv, L, d, seed, with_grad=True):
+    """Return bf16 CPU tensors (q, k, v, dO); dO is None if with_grad is False."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    q = torch.randn((B, Hq, L, d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    k = torch.randn((B, Hkv, L, d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    v = torch.randn((B, Hkv, L, d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    dO = None
+    if with_grad:
+        dO = torch.randn((B, Hq, L, d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    return q, k, v, dO
+
+
+def workload_inputs(w: Workload, seed=None, with_grad=True):
+    s = WORKLOAD_SEEDS.get(w.name, 0) if seed is None else seed
+    return make_inputs(w.B, w.Hq, w.Hkv, w.L, w.d, s, with_grad)
+
+
+def boundary_rows(L: int, n_chunks: int, causal: bool):
+    """First and last row of every chunk (encoder) or sub-chunk (causal, 2N
+    sub-chunks of length L/(2N)), plus rows 0 and L-1."""
+    parts = 2 * n_chunks if causal else n_chunks
+    c = L // parts
+    rows = {0, L - 1}
+    for i in range(parts):
+        rows.add(i * c)
+        rows.add(min(L - 1, (i + 1) * c - 1))
+    return rows
+
+
+def sample_rows(L: int, n_chunks: int, causal: bool, n: int, seed: int):
+    """Sorted sample of n distinct query rows: all chunk boundary rows, then
+    uniform draws without replacement from numpy's default_rng(seed + 1000)."""
+    rows = boundary_rows(L, n_chunks, causal)
+    if len(rows) >= n or n >= L:
+        base = sorted(rows) if n < L else list(range(L))
+        return np.array(base[:max(n, len(rows))] if n < L else base, dtype=np.int32)
+    rng = np.random.default_rng(seed + 1000)
+    rest = np.setdiff1d(np.arange(L), np.array(sorted(rows)))
+    extra = rng.choice(rest, size=n - len(rows), replace=False)
+    return np.array(sorted(rows | set(int(x) for x in extra)), dtype=np.int32)
+
+
+def tail_rows(L: int, n: int):
+    """The last n rows: for a causal model a key row j is seen only by
+    queries i >= j, so the fp64 statistics needed for its gradient stay cheap."""
+    n = min(n, L)
+    return np.arange(L - n, L, dtype=np.int32)

@@ -1,0 +1,81 @@
+"""The oracle's pins must catch plausible mistakes.
+
+Each case plants one mistake in a copy of the oracle's C source (on the CPU,
+in a temporary directory), builds it, points the oracle module at the mutant
+and runs a quick set of pins; at least one pin must fail.
+"""
+import os
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import oracle as _oracle_mod
+
+import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(pins.__file__), "..", "oracle", "ring_attn_oracle.c")
+
+MUTANTS = {
+    "causal_off_by_one": ("static int n_visible(const problem_t *P, int i) { return P->causal ? i + 1 : P->L; }",
+                          "static int n_visible(const problem_t *P, int i) { return P->causal ? i + 2 - (i + 1 >= P->L) : P->L; }"),
+    "gqa_head_map": ("const int g = h / (P->Hq / P->Hkv);\n  const double *qi = q_row(P, b, h, i);\n  const int n",
+                     "const int g = h % P->Hkv;\n  const double *qi = q_row(P, b, h, i);\n  const int n"),
+    "lse_drops_max": ("const double lse = m + log(sum);", "const double lse = log(sum) + (m > 0 ? 0 : m);"),
+    "dq_missing_scale": ("dq[c] += P->scale * dsij * kj[c];", "dq[c] += dsij * kj[c];"),
+    "ds_missing_D": ("const double dsij = pij * (dpij - D);", "const double dsij = pij * dpij;"),
+    "dk_wrong_operand": ("dk[c] += P->scale * dsij * qi[c];", "dk[c] += P->scale * dsij * doi[c];"),
+    "dv_uses_ds": ("dv[c] += pij * doi[c];", "dv[c] += dsij * doi[c];"),
+    "merge_wrong_sign": ("const double a = exp(lse - merged), w = exp(lse_s - merged);",
+                         "const double a = exp(lse - merged), w = exp(merged - lse_s);"),
+    "fold_wrong_pair": ("return sub < N ? sub : 2 * N - 1 - sub;", "return sub < N ? sub : sub - N;"),
+    "transposed_score": ("s[j] = P->scale * dot(qi, k_row(P, b, g, j), P->d);\n    if (s[j] > m) m = s[j];\n  }\n  double sum",
+                         "s[j] = P->scale * dot(q_row(P, b, h, j), k_row(P, b, g, i), P->d);\n    if (s[j] > m) m = s[j];\n  }\n  double sum"),
+}
+
+
+def _quick_pins():
+    """Run a fast subset of the pins; return the names of those that fail."""
+    checks = [
+        ("sdpa_fwd", lambda: [pins.test_fwd_matches_torch_sdpa(s, c) for s in pins.SHAPES[:2] for c in (False, True)]),
+        ("sdpa_bwd", lambda: [pins.test_bwd_matches_torch_autograd(s, c) for s in pins.SHAPES[:2] for c in (False, True)]),
+        ("rows_sum", lambda: [pins.test_softmax_rows_sum_to_one(c) for c in (False, True)]),
+        ("ring", lambda: [pins.test_ring_form_invariant_in_chunk_count(48, c) for c in (False, True)]),
+        ("row0", pins.test_causal_row_zero_closed_form),
+        ("gqa", lambda: [pins.test_gqa_equals_repeated_mha(c) for c in (False, True)]),
+        ("fold", lambda: [pins.test_fold_gives_every_rank_equal_causal_work(n) for n in (2, 4)]),
+        ("hand", lambda: [pins.test_hand_worked_example(m) for m in ("enc", "cau")]),
+    ]
+    failed = []
+    for name, fn in checks:
+        try:
+            with np.errstate(all="ignore"):
+                fn()
+        except Exception:  # any failure or error counts as a caught mutant
+            failed.append(name)
+    return failed
+
+
+def test_unmutated_source_passes_quick_pins():
+    assert _quick_pins() == []
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not unique"
+    mut = tmp_path / "mutant.c"
+    mut.write_text(src.replace(old, new))
+    so = tmp_path / "libmutant.so"
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-shared", "-fPIC", "-o", str(so), str(mut),
+                           "-lm", "-lpthread"])
+    prev = _oracle_mod._swap_library(str(so))
+    try:
+        failed = _quick_pins()
+    finally:
+        _oracle_mod._restore_library(prev)
+    assert failed, f"mutant {name} passed every pin"
+    # the real oracle is back in place
+    assert oracle.owner_rank(8, 2, True, 7) == 0
