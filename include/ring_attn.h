@@ -1,0 +1,131 @@
+/*
+ * ring_attn.h -- C ABI of the GB300 (sm_103a) blockwise Ring Self-Attention
+ * library.
+ *
+ * The operation (web page "Large-scale distributed AI model training series:
+ * sequence parallelism", section 2.3 Ring Self-Attention and section 6.2 Ring
+ * Attention): self-attention softmax(Q K^T / sqrt(d)) V, computed block by
+ * block.  The sequence of length L is cut into n_chunks chunks; the queries of
+ * each chunk visit the key/value chunks in ring order, starting with their own
+ * chunk and then (r - 1), (r - 2), ... mod n_chunks, and the partial results
+ * are merged with a running maximum and log-sum-exp (the online-softmax
+ * correction of section 6.2).  With causal = 1 (decoder), position i sees
+ * keys j <= i and every rank r owns the folded pair of sub-chunks
+ * {r, 2 n_chunks - 1 - r} of length L / (2 n_chunks) (the fold of section 8.2,
+ * USP), which gives every rank the same amount of work.  On one GPU the ring
+ * is emulated: all ranks' blocks run in one launch, each in its ring order.
+ * The result is exact attention; chunking only changes the order of fp32
+ * additions.
+ *
+ * Tensors (all contiguous, row-major, device memory, caller-owned):
+ *   q, o, dO, dq : bf16 [B][Hq][L][d]
+ *   k, v, dk, dv : bf16 [B][Hkv][L][d]
+ *   lse          : fp32 [B][Hq][L], natural log of sum_j exp(q_i.k_j/sqrt(d))
+ * Grouped-query attention: query head h uses kv head h / (Hq / Hkv).
+ * Scale is fixed at 1/sqrt(d).  Supported: d in {64, 128}; Hq % Hkv == 0;
+ * L % n_chunks == 0 (encoder) or L % (2 n_chunks) == 0 (causal); every base
+ * pointer 16-byte aligned; B * Hq and B * Hkv below 65536.
+ *
+ * Errors: argument errors are returned before anything is launched.  Calls
+ * are asynchronous on `stream`; a kernel that gives up on a bounded wait
+ * records a device status, read (and cleared) by ring_attn_device_status().
+ * Thread safety: calls from several host threads are serialised internally.
+ */
+#ifndef RING_ATTN_H
+#define RING_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  RING_ATTN_OK = 0,
+  RING_ATTN_ERR_NULL = -1,          /* a required pointer is NULL */
+  RING_ATTN_ERR_SHAPE = -2,         /* negative size, Hq % Hkv != 0, bad chunking */
+  RING_ATTN_ERR_UNSUPPORTED = -3,   /* d not in {64,128}, misaligned pointer, too many heads */
+  RING_ATTN_ERR_WORKSPACE = -4,     /* backward workspace missing or too small */
+  RING_ATTN_ERR_CUDA = -5,          /* a CUDA runtime/driver call failed */
+  RING_ATTN_ERR_DEVICE_TIMEOUT = -6 /* a kernel gave up on a bounded wait */
+};
+
+/*
+ * Forward pass.  Writes o (bf16) and lse (fp32).
+ * Inputs q, k, v are read only.  n_chunks >= 1 is the ring size N.
+ * Returns RING_ATTN_OK or a negative error code.  B == 0 or L == 0 is a
+ * no-op returning RING_ATTN_OK.
+ */
+int ring_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                  int L, int d, int n_chunks, int causal, cudaStream_t stream);
+
+/*
+ * Bytes of device workspace ring_attn_bwd needs for this shape (fp32 dq
+ * accumulator plus per-row statistics), or 0 for an invalid shape.
+ */
+size_t ring_attn_bwd_workspace_size(int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal);
+
+/*
+ * Backward pass of l = sum(dO * o): writes dq, dk, dv (bf16).  o and lse
+ * must be the forward outputs for the same q, k, v.  The probabilities are
+ * recomputed from lse (no score matrix is stored).  `workspace` is caller
+ * owned device memory of at least ring_attn_bwd_workspace_size() bytes,
+ * 256-byte aligned; its contents on entry do not matter.
+ */
+int ring_attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                  void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal,
+                  void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Static description of a status code. */
+const char* ring_attn_strerror(int status);
+
+/*
+ * Synchronises `stream`, then returns and clears the device status of the
+ * current device: RING_ATTN_OK, or RING_ATTN_ERR_DEVICE_TIMEOUT if a kernel
+ * aborted a bounded wait since the last call (the site code is written to
+ * *site if site is not NULL), or RING_ATTN_ERR_CUDA.
+ */
+int ring_attn_device_status(cudaStream_t stream, int* site);
+
+/* Frees cached launch plans (device copies of schedules). Optional. */
+void ring_attn_release(void);
+
+/* ---------------------------------------------------------------------
+ * Host-only scheduling queries (no GPU needed).  They expose the chunk map
+ * and the ring visiting order the kernels follow, at the granularity of the
+ * kernels' 128-row tiles.
+ * ------------------------------------------------------------------- */
+
+/* Rank (0..n_chunks-1) that owns sequence position pos, or a negative code. */
+int ring_attn_owner_rank(int L, int n_chunks, int causal, int pos);
+
+/*
+ * Forward plan.  The queries are processed in blocks of two 128-row tiles
+ * (256 rows); block u covers rows [256 u, 256 u + 256).  For each block the
+ * plan lists the 128-row key/value tiles it visits, in ring order, as
+ * half-open ranges [begin, end) of tile indices.
+ *   n_blocks, n_ranges : out, sizes (always written if non-NULL)
+ *   block_order        : [n_blocks] launch order (longest work first)
+ *   range_offsets      : [n_blocks + 1] offsets into ranges
+ *   ranges             : [2 * n_ranges] (begin, end) pairs
+ * Pass NULL arrays to query sizes only.  Returns RING_ATTN_OK or an error.
+ */
+int ring_attn_fwd_plan(int L, int n_chunks, int causal, int* n_blocks, int* n_ranges, int32_t* block_order,
+                       int32_t* range_offsets, int32_t* ranges);
+
+/*
+ * Backward plan: for each 128-row key/value tile t, the 128-row query tiles
+ * that see it, in the order the key/value block meets them travelling round
+ * the ring (its own rank first, then r + 1, r + 2, ... mod n_chunks).
+ * Same array conventions as ring_attn_fwd_plan, with n_blocks = key tiles.
+ */
+int ring_attn_bwd_plan(int L, int n_chunks, int causal, int* n_blocks, int* n_ranges, int32_t* block_order,
+                       int32_t* range_offsets, int32_t* ranges);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RING_ATTN_H */

@@ -1,0 +1,190 @@
+"""ctypes binding of the C ABI in include/ring_attn.h.
+
+Argument marshalling only: every step of the attention runs in the sm_103a
+kernels of libring_attn.so.  There is no fallback: if the library is not
+built, every call raises.  torch is used for device memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+OK = 0
+ERR_NULL = -1
+ERR_SHAPE = -2
+ERR_UNSUPPORTED = -3
+ERR_WORKSPACE = -4
+ERR_CUDA = -5
+ERR_DEVICE_TIMEOUT = -6
+
+_lib = None
+
+
+class RingAttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {strerror(status)} ({status})")
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load():
+    """Load libring_attn.so (it must have been built; see build.build())."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library not built: {path} is missing (call sequence_blockwise_self_gb300.build.build())")
+    lib = ctypes.CDLL(path)
+    I, P, S = ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
+    IP = ctypes.POINTER(ctypes.c_int)
+    I32P = ctypes.POINTER(ctypes.c_int32)
+    lib.ring_attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, P]
+    lib.ring_attn_fwd.restype = I
+    lib.ring_attn_bwd_workspace_size.argtypes = [I, I, I, I, I, I, I]
+    lib.ring_attn_bwd_workspace_size.restype = S
+    lib.ring_attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, S, P]
+    lib.ring_attn_bwd.restype = I
+    lib.ring_attn_strerror.argtypes = [I]
+    lib.ring_attn_strerror.restype = ctypes.c_char_p
+    lib.ring_attn_device_status.argtypes = [P, IP]
+    lib.ring_attn_device_status.restype = I
+    lib.ring_attn_release.argtypes = []
+    lib.ring_attn_release.restype = None
+    lib.ring_attn_owner_rank.argtypes = [I, I, I, I]
+    lib.ring_attn_owner_rank.restype = I
+    for f in (lib.ring_attn_fwd_plan, lib.ring_attn_bwd_plan):
+        f.argtypes = [I, I, I, IP, IP, I32P, I32P, I32P]
+        f.restype = I
+    _lib = lib
+    return lib
+
+
+def strerror(status: int) -> str:
+    return load().ring_attn_strerror(int(status)).decode()
+
+
+# ------------------------------------------------------------- host queries
+
+def owner_rank(L: int, n_chunks: int, causal: bool, pos: int) -> int:
+    return load().ring_attn_owner_rank(int(L), int(n_chunks), int(bool(causal)), int(pos))
+
+
+def _plan(fn, L, n_chunks, causal):
+    lib = load()
+    nb, nr = ctypes.c_int(0), ctypes.c_int(0)
+    rc = fn(int(L), int(n_chunks), int(bool(causal)), ctypes.byref(nb), ctypes.byref(nr), None, None, None)
+    if rc != OK:
+        raise RingAttnError(rc, "plan")
+    order = np.zeros(nb.value, dtype=np.int32)
+    offsets = np.zeros(nb.value + 1, dtype=np.int32)
+    ranges = np.zeros(2 * nr.value, dtype=np.int32)
+    p32 = lambda a: a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))  # noqa: E731
+    rc = fn(int(L), int(n_chunks), int(bool(causal)), None, None, p32(order), p32(offsets), p32(ranges))
+    if rc != OK:
+        raise RingAttnError(rc, "plan")
+    visits = [[(int(ranges[2 * r]), int(ranges[2 * r + 1])) for r in range(offsets[u], offsets[u + 1])]
+              for u in range(nb.value)]
+    return {"order": order, "offsets": offsets, "ranges": ranges, "visits": visits}
+
+
+def fwd_plan(L: int, n_chunks: int, causal: bool):
+    """Per 256-row query block: its key/value tile ranges in ring order."""
+    return _plan(load().ring_attn_fwd_plan, L, n_chunks, causal)
+
+
+def bwd_plan(L: int, n_chunks: int, causal: bool):
+    """Per key/value tile: its query tile ranges in ring order."""
+    return _plan(load().ring_attn_bwd_plan, L, n_chunks, causal)
+
+
+# --------------------------------------------------------------- device calls
+
+def _ptr(t) -> ctypes.c_void_p:
+    return ctypes.c_void_p(t.data_ptr() if t is not None else 0)
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check_tensor(t, name, dtype, shape):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def ring_attn_fwd(q, k, v, n_chunks: int, causal: bool, o=None, lse=None, stream=None):
+    """softmax(q k^T / sqrt(d)) v by ring-ordered blocks; returns (o, lse)."""
+    import torch
+    B, Hq, L, d = q.shape
+    Hkv = k.shape[1]
+    _check_tensor(q, "q", torch.bfloat16, (B, Hq, L, d))
+    _check_tensor(k, "k", torch.bfloat16, (B, Hkv, L, d))
+    _check_tensor(v, "v", torch.bfloat16, (B, Hkv, L, d))
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, L), dtype=torch.float32, device=q.device)
+    _check_tensor(o, "o", torch.bfloat16, (B, Hq, L, d))
+    _check_tensor(lse, "lse", torch.float32, (B, Hq, L))
+    rc = load().ring_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, L, d, int(n_chunks),
+                              int(bool(causal)), _stream(stream))
+    if rc != OK:
+        raise RingAttnError(rc, "ring_attn_fwd")
+    return o, lse
+
+
+def bwd_workspace_size(B, Hq, Hkv, L, d, n_chunks, causal) -> int:
+    return int(load().ring_attn_bwd_workspace_size(B, Hq, Hkv, L, d, int(n_chunks), int(bool(causal))))
+
+
+def ring_attn_bwd(q, k, v, o, lse, dO, n_chunks: int, causal: bool, dq=None, dk=None, dv=None, workspace=None,
+                  stream=None):
+    """Gradients of sum(dO * o) with respect to q, k, v; returns (dq, dk, dv)."""
+    import torch
+    B, Hq, L, d = q.shape
+    Hkv = k.shape[1]
+    for t, n, s in ((q, "q", (B, Hq, L, d)), (k, "k", (B, Hkv, L, d)), (v, "v", (B, Hkv, L, d)),
+                    (o, "o", (B, Hq, L, d)), (dO, "dO", (B, Hq, L, d))):
+        _check_tensor(t, n, torch.bfloat16, s)
+    _check_tensor(lse, "lse", torch.float32, (B, Hq, L))
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    ws_bytes = bwd_workspace_size(B, Hq, Hkv, L, d, n_chunks, causal)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
+    rc = load().ring_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk),
+                              _ptr(dv), B, Hq, Hkv, L, d, int(n_chunks), int(bool(causal)), _ptr(workspace),
+                              int(workspace.numel() * workspace.element_size()), _stream(stream))
+    if rc != OK:
+        raise RingAttnError(rc, "ring_attn_bwd")
+    return dq, dk, dv
+
+
+def device_status(stream=None):
+    """Synchronise and return (status, site) of the device status word."""
+    site = ctypes.c_int(0)
+    rc = load().ring_attn_device_status(_stream(stream), ctypes.byref(site))
+    return rc, site.value
+
+
+def release():
+    load().ring_attn_release()

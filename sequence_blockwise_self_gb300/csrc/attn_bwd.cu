@@ -1,0 +1,519 @@
+// attn_bwd.cu -- backward kernels of blockwise Ring Self-Attention, sm_103a.
+//
+// The backward pass recomputes the attention probabilities from the saved
+// log-sum-exp instead of storing them (activation recomputation, as the
+// BPT section 4.3 and the Ring Attention section 6.2 of "Large-scale
+// distributed AI model training series: sequence parallelism" use).  For
+// l = sum(dO * o), with P_ij = exp(s_ij - lse_i):
+//   D_i   = sum_c dO_ic o_ic
+//   dV_j += sum_i P_ij dO_i
+//   dS_ij = P_ij (dO_i . v_j - D_i)
+//   dK_j += scale sum_i dS_ij q_i
+//   dQ_i += scale sum_j dS_ij k_j
+//
+// Three launches:
+//   bwd_pre   per row: D_i, lse_i in log2 units (padded rows get +inf, so
+//             their probabilities are 0), and zero the fp32 dQ accumulator.
+//   bwd_main  one CTA per (key/value tile, batch, kv head).  K_j and V_j
+//             stay in shared memory; the CTA loops over the query heads of
+//             the group and over the query tiles that see the tile, in the
+//             order the key/value block meets them going round the ring.
+//             Per query tile, five tcgen05 GEMMs:
+//               S^T  = K Q^T      (TMEM)      dP^T = V dO^T   (TMEM)
+//               dV  += P^T dO     (TMEM)      dK  += dS^T Q   (TMEM)
+//               dQ   = dS K       (TMEM, then TMA reduce-add into fp32)
+//             P^T and dS^T (bf16) go through shared memory.
+//   bwd_post  dq = bf16(scale * dQ_acc).
+//
+// Warp roles of bwd_main (256 threads): warp 0 TMA producer, warp 1
+// tcgen05 issuer, warp 2 TMEM allocator, warps 4-7 one thread per key row:
+// probabilities, dS, the dQ drain, and the dK/dV epilogue.
+//
+// Tensor memory (fp32 columns): S^T [0,128) dP^T [128,256) dV [256,256+d)
+// dK [256+d, 256+2d); dQ at [384,448) for d = 64, and over S^T for d = 128
+// (S^T has been read by then; the next S^T waits for the dQ drain).
+#include <cfloat>
+
+#include "kernels.h"
+#include "sm103_ptx.cuh"
+
+namespace ra {
+
+namespace {
+
+constexpr int kBwdThreads = 256;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct BwdSmem {
+  static constexpr int kSub = D / 64;
+  static constexpr int kTile = 128 * D * 2;
+  alignas(1024) uint8_t k[kTile];
+  alignas(1024) uint8_t v[kTile];
+  alignas(1024) uint8_t q[2][kTile];
+  alignas(1024) uint8_t dO[kTile];
+  alignas(1024) uint8_t pT[128 * 128 * 2];   // also the fp32 staging of the dQ drain
+  alignas(1024) uint8_t dsT[128 * 128 * 2];
+  alignas(16) float lse2[2][128];
+  alignas(16) float dvec[2][128];
+  alignas(8) uint64_t kv_full;
+  alignas(8) uint64_t q_full[2];
+  alignas(8) uint64_t q_empty[2];
+  alignas(8) uint64_t do_full;
+  alignas(8) uint64_t do_empty;
+  alignas(8) uint64_t s_full;
+  alignas(8) uint64_t ds_full;
+  alignas(8) uint64_t dq_full;
+  alignas(8) uint64_t dq_free;
+  alignas(8) uint64_t kv_final;
+  alignas(8) uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+struct BwdDev {
+  int B, Hq, Hkv, L, Lpad, causal;
+  float scale, scale_log2;
+  const int32_t* order;
+  const int32_t* offsets;
+  const int32_t* ranges;
+  const float* lse2;
+  const float* dvec;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int* err;
+};
+
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, int* err) {
+  int local = 0;
+  mbar_wait(bar, parity, &local, err, kSiteBwdDrain);
+}
+
+// Visits (head offset hh, query tile it) of the CTA's list, in order.
+struct QIter {
+  const int32_t* rg;
+  int nr, G;
+  int hh = 0, ri = 0, it = 0;
+  __device__ QIter(const int32_t* rg_, int nr_, int G_) : rg(rg_), nr(nr_), G(G_) { it = nr > 0 ? rg[0] : 0; }
+  __device__ bool valid() const { return hh < G && nr > 0; }
+  __device__ void next() {
+    if (++it < rg[2 * ri + 1]) return;
+    if (++ri < nr) { it = rg[2 * ri]; return; }
+    ri = 0;
+    it = rg[0];
+    ++hh;
+  }
+};
+
+template <int D>
+__device__ void bwd_producer(BwdSmem<D>& sm, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+                             const CUtensorMap* tm_v, const CUtensorMap* tm_do, const BwdDev& p, int b, int g,
+                             int kv_tile, const int32_t* rg, int nr, volatile int* ab, int* err) {
+  using S = BwdSmem<D>;
+  const int G = p.Hq / p.Hkv;
+  const int kv_z = b * p.Hkv + g;
+  const uint32_t kvb = smem_u32(&sm.kv_full);
+  mbar_arrive_expect_tx(kvb, 2 * S::kTile);
+  for (int sub = 0; sub < S::kSub; ++sub) {
+    tma_load_3d(smem_u32(sm.k) + sub * 16384, tm_k, kvb, sub * 64, kv_tile * 128, kv_z);
+    tma_load_3d(smem_u32(sm.v) + sub * 16384, tm_v, kvb, sub * 64, kv_tile * 128, kv_z);
+  }
+  bool ok = true;
+  uint32_t nq = 0, ndo = 0;  // Q and dO fills issued
+  for (QIter qi(rg, nr, G); qi.valid() && ok; qi.next()) {
+    const uint32_t i = nq;
+    const int q_z = b * p.Hq + g * G + qi.hh;
+    const uint32_t slot = i & 1;
+    if (i >= 2) ok = mbar_wait(smem_u32(&sm.q_empty[slot]), ((i >> 1) - 1) & 1, ab, err, kSiteBwdProducer);
+    if (!ok) break;
+    const uint32_t qb = smem_u32(&sm.q_full[slot]);
+    mbar_arrive_expect_tx(qb, S::kTile + 1024);
+    for (int sub = 0; sub < S::kSub; ++sub)
+      tma_load_3d(smem_u32(sm.q[slot]) + sub * 16384, tm_q, qb, sub * 64, qi.it * 128, q_z);
+    const size_t roff = static_cast<size_t>(q_z) * p.Lpad + qi.it * 128;
+    bulk_load_1d(smem_u32(sm.lse2[slot]), p.lse2 + roff, 512, qb);
+    bulk_load_1d(smem_u32(sm.dvec[slot]), p.dvec + roff, 512, qb);
+    ++nq;
+    if (i >= 1) ok = mbar_wait(smem_u32(&sm.do_empty), (i - 1) & 1, ab, err, kSiteBwdProducer);
+    if (!ok) break;
+    const uint32_t db = smem_u32(&sm.do_full);
+    mbar_arrive_expect_tx(db, S::kTile);
+    for (int sub = 0; sub < S::kSub; ++sub)
+      tma_load_3d(smem_u32(sm.dO) + sub * 16384, tm_do, db, sub * 64, qi.it * 128, q_z);
+    ++ndo;
+  }
+  if (!ok) {
+    // Let every copy this thread issued land before the CTA exits.
+    wait_drain(kvb, 0, err);
+    for (uint32_t s = 0; s < 2 && s < nq; ++s) {
+      const uint32_t last = s + 2 * ((nq - 1 - s) / 2);
+      wait_drain(smem_u32(&sm.q_full[s]), (last >> 1) & 1, err);
+    }
+    if (ndo > 0) wait_drain(smem_u32(&sm.do_full), (ndo - 1) & 1, err);
+  }
+}
+
+template <int D>
+__device__ void bwd_mma(BwdSmem<D>& sm, uint32_t tmem, uint32_t n_total, volatile int* ab, int* err) {
+  constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
+  constexpr uint32_t kIdKV = idesc_bf16(128, D, false, true);
+  constexpr uint32_t kIdQ = idesc_bf16(128, D, true, true);
+  const uint32_t t_s = tmem, t_dp = tmem + 128, t_dv = tmem + 256, t_dk = tmem + 256 + D;
+  const uint32_t t_dq = (D == 128) ? tmem : tmem + 384;
+  const uint32_t ka = smem_u32(sm.k), va = smem_u32(sm.v), da = smem_u32(sm.dO);
+  const uint32_t pa = smem_u32(sm.pT), sa = smem_u32(sm.dsT);
+
+  bool ok = mbar_wait(smem_u32(&sm.kv_full), 0, ab, err, kSiteBwdMma);
+  for (uint32_t i = 0; i < n_total && ok; ++i) {
+    const uint32_t slot = i & 1;
+    const uint32_t qa = smem_u32(sm.q[slot]);
+    ok = mbar_wait(smem_u32(&sm.q_full[slot]), (i >> 1) & 1, ab, err, kSiteBwdMma) &&
+         mbar_wait(smem_u32(&sm.do_full), i & 1, ab, err, kSiteBwdMma) &&
+         (i == 0 || mbar_wait(smem_u32(&sm.dq_free), (i - 1) & 1, ab, err, kSiteBwdMma));
+    if (!ok) break;
+    tc_fence_after();
+    // S^T = K Q^T and dP^T = V dO^T (both operands K-major)
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+      umma_ss(t_s, sdesc_sw128(ka + off, 16, 1024), sdesc_sw128(qa + off, 16, 1024), kIdS, kk > 0);
+    }
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+      umma_ss(t_dp, sdesc_sw128(va + off, 16, 1024), sdesc_sw128(da + off, 16, 1024), kIdS, kk > 0);
+    }
+    umma_commit(smem_u32(&sm.s_full));
+    ok = mbar_wait(smem_u32(&sm.ds_full), i & 1, ab, err, kSiteBwdMma);
+    if (!ok) break;
+    tc_fence_after();
+    // dV += P^T dO : A = P^T (K-major over queries), B = dO (MN-major)
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+      umma_ss(t_dv, sdesc_sw128(pa + off, 16, 1024), sdesc_sw128(da + kk * 2048, 16384, 1024), kIdKV,
+              (i > 0 || kk > 0) ? 1u : 0u);
+    }
+    if (i + 1 < n_total) umma_commit(smem_u32(&sm.do_empty));
+    // dK += dS^T Q : A = dS^T (K-major), B = Q (MN-major)
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+      umma_ss(t_dk, sdesc_sw128(sa + off, 16, 1024), sdesc_sw128(qa + kk * 2048, 16384, 1024), kIdKV,
+              (i > 0 || kk > 0) ? 1u : 0u);
+    }
+    if (i + 2 < n_total) umma_commit(smem_u32(&sm.q_empty[slot]));
+    // dQ = dS K : A = dS (MN-major view of dS^T), B = K (MN-major)
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+      umma_ss(t_dq, sdesc_sw128(sa + kk * 2048, 16384, 1024), sdesc_sw128(ka + kk * 2048, 16384, 1024), kIdQ,
+              kk > 0);
+    umma_commit(smem_u32(&sm.dq_full));
+  }
+  if (ok) {
+    umma_commit(smem_u32(&sm.kv_final));
+  } else {
+    umma_commit(smem_u32(&sm.drain));
+    wait_drain(smem_u32(&sm.drain), 0, err);
+  }
+}
+
+template <int D>
+__device__ void bwd_compute(BwdSmem<D>& sm, uint32_t tmem, const BwdDev& p, const CUtensorMap* tm_dqacc, int b,
+                            int g, int kv_tile, const int32_t* rg, int nr, volatile int* ab, int* err) {
+  const int wq = (threadIdx.x >> 5) & 3;
+  const int lane = threadIdx.x & 31;
+  const int row = wq * 32 + lane;  // key row (S^T lane) and also dQ query row
+  const int kv_pos = kv_tile * 128 + row;
+  const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+  const uint32_t t_s = tmem + lane_off, t_dp = tmem + 128 + lane_off;
+  const uint32_t t_dv = tmem + 256 + lane_off, t_dk = tmem + 256 + D + lane_off;
+  const uint32_t t_dq = ((D == 128) ? tmem : tmem + 384) + lane_off;
+  const uint32_t pa = smem_u32(sm.pT), sa = smem_u32(sm.dsT);
+  const uint32_t stage = pa + wq * 8192;  // two 4 KB fp32 staging boxes per warp
+  const int G = p.Hq / p.Hkv;
+  const float c = p.scale_log2;
+  bool ok = true;
+  uint32_t i = 0;
+  for (QIter qi(rg, nr, G); qi.valid() && ok; qi.next(), ++i) {
+    const uint32_t slot = i & 1;
+    ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.q_full[slot]), (i >> 1) & 1, ab, err, kSiteBwdSoftmax));
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.s_full), i & 1, ab, err, kSiteBwdSoftmax));
+    if (!ok) break;
+    tc_fence_after();
+    const int q0 = qi.it * 128;
+    // Probabilities are zero where the key is after the query (causal) or
+    // past the end; padded query rows have lse2 = +inf, hence P = 0.
+    const int first_valid_q = p.causal ? kv_pos - q0 : 0;  // local query index
+    const bool row_dead = kv_pos >= p.L;
+    const float* lse2 = sm.lse2[slot];
+    const float* dvec = sm.dvec[slot];
+#pragma unroll
+    for (int c0 = 0; c0 < 4; ++c0) {
+      uint32_t rs[32], rp[32];
+      tmem_ld32(t_s + c0 * 32, rs);
+      tmem_ld32(t_dp + c0 * 32, rp);
+      float pv[32], ds[32];
+#pragma unroll
+      for (int x = 0; x < 32; ++x) {
+        const int qq = c0 * 32 + x;
+        float pr = ex2(fmaf(__uint_as_float(rs[x]), c, -lse2[qq]));
+        if (row_dead || qq < first_valid_q) pr = 0.f;
+        pv[x] = pr;
+        ds[x] = pr * (__uint_as_float(rp[x]) - dvec[qq]);
+      }
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const int ch = c0 * 4 + q4;
+        const uint32_t off = (ch >> 3) * 16384 + sw128_offset(row, ch & 7);
+        st_shared_v4(pa + off, pack_bf16(pv[q4 * 8], pv[q4 * 8 + 1]), pack_bf16(pv[q4 * 8 + 2], pv[q4 * 8 + 3]),
+                     pack_bf16(pv[q4 * 8 + 4], pv[q4 * 8 + 5]), pack_bf16(pv[q4 * 8 + 6], pv[q4 * 8 + 7]));
+        st_shared_v4(sa + off, pack_bf16(ds[q4 * 8], ds[q4 * 8 + 1]), pack_bf16(ds[q4 * 8 + 2], ds[q4 * 8 + 3]),
+                     pack_bf16(ds[q4 * 8 + 4], ds[q4 * 8 + 5]), pack_bf16(ds[q4 * 8 + 6], ds[q4 * 8 + 7]));
+      }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    mbar_arrive(smem_u32(&sm.ds_full));
+    // dQ drain: rows of dQ (query rows) -> fp32 staging -> TMA reduce-add.
+    ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.dq_full), i & 1, ab, err, kSiteBwdSoftmax));
+    if (!ok) break;
+    tc_fence_after();
+    const int q_z = b * p.Hq + g * G + qi.hh;
+#pragma unroll
+    for (int c0 = 0; c0 < D / 32; ++c0) {
+      const uint32_t box = stage + (c0 & 1) * 4096;
+      if (c0 >= 2) {
+        if (lane == 0) bulk_wait_group_read<1>();
+        __syncwarp();
+      }
+      uint32_t r[32];
+      tmem_ld32(t_dq + c0 * 32, r);
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch)
+        st_shared_v4(box + sw128_offset(lane, ch), r[ch * 4], r[ch * 4 + 1], r[ch * 4 + 2], r[ch * 4 + 3]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_reduce_add_3d(tm_dqacc, box, c0 * 32, q0 + wq * 32, q_z);
+        bulk_commit_group();
+      }
+    }
+    if (lane == 0) bulk_wait_group_read<0>();
+    __syncwarp();
+    tc_fence_before();
+    mbar_arrive(smem_u32(&sm.dq_free));
+  }
+  if (lane == 0) bulk_wait_group<0>();
+  if (ok) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.kv_final), 0, ab, err, kSiteBwdEpilogue));
+  if (ok) {
+    tc_fence_after();
+    const bool store = kv_pos < p.L;
+    const int kv_z = b * p.Hkv + g;
+    const size_t base = (static_cast<size_t>(kv_z) * p.L + (store ? kv_pos : 0)) * D;
+    const float s = p.scale;
+#pragma unroll
+    for (int c0 = 0; c0 < D / 32; ++c0) {
+      uint32_t r[32];
+      tmem_ld32(t_dv + c0 * 32, r);  // warp-collective: every lane loads
+      if (store) {
+        uint4* dst = reinterpret_cast<uint4*>(p.dv + base + c0 * 32);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const float* f = reinterpret_cast<const float*>(r) + q4 * 8;
+          dst[q4] = make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]),
+                               pack_bf16(f[6], f[7]));
+        }
+      }
+      tmem_ld32(t_dk + c0 * 32, r);
+      if (store) {
+        uint4* dst = reinterpret_cast<uint4*>(p.dk + base + c0 * 32);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const float* f = reinterpret_cast<const float*>(r) + q4 * 8;
+          dst[q4] = make_uint4(pack_bf16(f[0] * s, f[1] * s), pack_bf16(f[2] * s, f[3] * s),
+                               pack_bf16(f[4] * s, f[5] * s), pack_bf16(f[6] * s, f[7] * s));
+        }
+      }
+    }
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    ring_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                         const __grid_constant__ CUtensorMap tm_dqacc, const BwdDev p) {
+  using S = BwdSmem<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (smem_u32(smem_raw) & 1023u) {  // the swizzled layouts need a 1024-byte aligned base
+    if (threadIdx.x == 0) atomicCAS(p.err, 0, kSiteBwdMisaligned);
+    return;
+  }
+  S& sm = *reinterpret_cast<S*>(smem_raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int BG = p.B * p.Hkv;
+  const int kv_tile = p.order[blockIdx.x / BG];
+  const int bg = blockIdx.x % BG;
+  const int b = bg / p.Hkv, g = bg % p.Hkv;
+  const int32_t* rg = p.ranges + 2 * p.offsets[kv_tile];
+  const int nr = p.offsets[kv_tile + 1] - p.offsets[kv_tile];
+  volatile int* ab = &sm.abort_flag;
+
+  if (threadIdx.x == 0) {
+    sm.abort_flag = 0;
+    mbar_init(smem_u32(&sm.kv_full), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&sm.q_full[s]), 1);
+      mbar_init(smem_u32(&sm.q_empty[s]), 1);
+    }
+    mbar_init(smem_u32(&sm.do_full), 1);
+    mbar_init(smem_u32(&sm.do_empty), 1);
+    mbar_init(smem_u32(&sm.s_full), 1);
+    mbar_init(smem_u32(&sm.ds_full), 128);
+    mbar_init(smem_u32(&sm.dq_full), 1);
+    mbar_init(smem_u32(&sm.dq_free), 128);
+    mbar_init(smem_u32(&sm.kv_final), 1);
+    mbar_init(smem_u32(&sm.drain), 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_do);
+    tma_prefetch_desc(&tm_dqacc);
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_u32(&sm.tmem_base), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  if (warp == 0) {
+    if (lane == 0) bwd_producer<D>(sm, &tm_q, &tm_k, &tm_v, &tm_do, p, b, g, kv_tile, rg, nr, ab, p.err);
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int nq = 0;
+      for (int ri = 0; ri < nr; ++ri) nq += rg[2 * ri + 1] - rg[2 * ri];
+      bwd_mma<D>(sm, tmem, static_cast<uint32_t>(nq) * (p.Hq / p.Hkv), ab, p.err);
+    }
+  } else if (warp >= 4) {
+    bwd_compute<D>(sm, tmem, p, &tm_dqacc, b, g, kv_tile, rg, nr, ab, p.err);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 2) tmem_dealloc(tmem, 512);
+}
+
+// One warp per row: D_i = sum_c dO_ic o_ic, lse2_i = lse_i log2(e) (or +inf
+// / 0 for padded rows), and zero the row of the fp32 dQ accumulator.
+template <int D>
+__global__ void __launch_bounds__(256) ring_attn_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
+                                                                const __nv_bfloat16* __restrict__ dO,
+                                                                const float* __restrict__ lse, float* lse2,
+                                                                float* dvec, float* dq_acc, int L, int Lpad,
+                                                                long long n_rows) {
+  const long long r = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (r >= n_rows) return;
+  const long long bh = r / Lpad;
+  const int i = static_cast<int>(r % Lpad);
+  constexpr int kPer = D / 32;  // elements per lane
+  float acc = 0.f;
+  if (i < L) {
+    const size_t off = (static_cast<size_t>(bh) * L + i) * D + lane * kPer;
+    if constexpr (kPer == 4) {
+      const uint2 a = *reinterpret_cast<const uint2*>(o + off);
+      const uint2 bb = *reinterpret_cast<const uint2*>(dO + off);
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&bb);
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        const float2 fa = __bfloat1622float2(a2[x]), fb = __bfloat1622float2(b2[x]);
+        acc = fmaf(fa.x, fb.x, acc);
+        acc = fmaf(fa.y, fb.y, acc);
+      }
+    } else {
+      const uint32_t a = *reinterpret_cast<const uint32_t*>(o + off);
+      const uint32_t bb = *reinterpret_cast<const uint32_t*>(dO + off);
+      const float2 fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a));
+      const float2 fb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bb));
+      acc = fmaf(fa.x, fb.x, fa.y * fb.y);
+    }
+  }
+#pragma unroll
+  for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+  if (lane == 0) {
+    dvec[r] = (i < L) ? acc : 0.f;
+    lse2[r] = (i < L) ? lse[static_cast<size_t>(bh) * L + i] * kLog2e : INFINITY;
+  }
+  float4* z = reinterpret_cast<float4*>(dq_acc + static_cast<size_t>(r) * D);
+#pragma unroll
+  for (int x = lane; x < D / 4; x += 32) z[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// dq = bf16(scale * dQ_acc) for rows < L; 8 elements per thread.
+template <int D>
+__global__ void __launch_bounds__(256) ring_attn_bwd_post_kernel(const float* __restrict__ dq_acc,
+                                                                 __nv_bfloat16* __restrict__ dq, float scale, int L,
+                                                                 int Lpad, long long n_out8) {
+  const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= n_out8) return;
+  const long long e = t * 8;                      // element index in [B*Hq*L*D)
+  const long long row = e / D;                    // (bh, i) flattened over L
+  const int col = static_cast<int>(e % D);
+  const long long bh = row / L;
+  const int i = static_cast<int>(row % L);
+  const float4* src = reinterpret_cast<const float4*>(dq_acc + (static_cast<size_t>(bh) * Lpad + i) * D + col);
+  const float4 a = src[0], bq = src[1];
+  uint4 out = make_uint4(pack_bf16(a.x * scale, a.y * scale), pack_bf16(a.z * scale, a.w * scale),
+                         pack_bf16(bq.x * scale, bq.y * scale), pack_bf16(bq.z * scale, bq.w * scale));
+  *reinterpret_cast<uint4*>(dq + e) = out;
+}
+
+template <int D>
+cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(a.B) * a.Hq * a.Lpad;
+  const unsigned pre_blocks = static_cast<unsigned>((rows * 32 + 255) / 256);
+  ring_attn_bwd_pre_kernel<D><<<pre_blocks, 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dO), a.lse, a.lse2, a.Dvec,
+      a.dq_acc, a.L, a.Lpad, rows);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  BwdDev p;
+  p.B = a.B; p.Hq = a.Hq; p.Hkv = a.Hkv; p.L = a.L; p.Lpad = a.Lpad; p.causal = a.causal;
+  p.scale = 1.0f / sqrtf(static_cast<float>(D));
+  p.scale_log2 = p.scale * kLog2e;
+  p.order = a.order; p.offsets = a.offsets; p.ranges = a.ranges;
+  p.lse2 = a.lse2; p.dvec = a.Dvec;
+  p.dk = static_cast<__nv_bfloat16*>(a.dk);
+  p.dv = static_cast<__nv_bfloat16*>(a.dv);
+  p.err = a.err;
+  const size_t smem = sizeof(BwdSmem<D>);
+  e = cudaFuncSetAttribute(ring_attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const dim3 grid(static_cast<unsigned>(a.n_blocks) * a.B * a.Hkv);
+  ring_attn_bwd_kernel<D><<<grid, kBwdThreads, smem, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dqacc, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  const long long n8 = static_cast<long long>(a.B) * a.Hq * a.L * D / 8;
+  ring_attn_bwd_post_kernel<D><<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, stream>>>(
+      a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), p.scale, a.L, a.Lpad, n8);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t bwd_smem_bytes(int d) {
+  return d == 128 ? sizeof(BwdSmem<128>) : sizeof(BwdSmem<64>);
+}
+
+cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream) {
+  return a.d == 128 ? launch_bwd_d<128>(a, stream) : launch_bwd_d<64>(a, stream);
+}
+
+}  // namespace ra

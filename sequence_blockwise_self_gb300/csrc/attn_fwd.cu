@@ -1,0 +1,400 @@
+// attn_fwd.cu -- forward kernel of blockwise Ring Self-Attention on sm_103a.
+//
+// What it computes ("Large-scale distributed AI model training series:
+// sequence parallelism", section 2.3 Ring Self-Attention, section 4.2 BPT
+// and section 6.2 Ring Attention): for a block of query rows, the two
+// products S = Q K^T and O = P V are formed tile by tile over the key/value
+// tiles the block may see, visited in ring order (the host plan), and the
+// softmax is corrected online with a running maximum and row sum, so the
+// partial results of successive ring steps merge into exact attention.
+//
+// One CTA = one 256-row query block of one (batch, head): two 128-row query
+// tiles that share every key/value tile.  Warp roles (384 threads):
+//   warp 0      TMA producer: Q once, then K_j, V_j into a ring of slots
+//   warp 1      tcgen05 issuer (one thread): S_t = Q_t K_j^T, O_t += P_t V_j
+//   warp 2      tensor-memory allocator
+//   warps 4-7   softmax of query tile 0 (one thread per row = TMEM lane)
+//   warps 8-11  softmax of query tile 1
+// Tensor memory (512 columns, fp32): S_0 [0,128) S_1 [128,256)
+// O_0 [256,256+d) O_1 [384,384+d).  P (bf16) goes through shared memory in
+// the 128-byte-swizzled K-major layout the tensor core reads.
+//
+// Issue order per key/value tile j (as in FlashAttention-4 style pipelines):
+//   PV_0(j), S_0(j+1), PV_1(j), S_1(j+1)
+// and one commit after each S_t(j+1) covers PV_t(j) as well, so when the
+// softmax of tile t sees S_t(j+1) the accumulator O_t is quiescent and P_t
+// may be overwritten.  The running maximum is in log2 units; O and l are
+// rescaled only when the maximum grew by more than 8 (a factor 256), which
+// keeps the result exact while skipping most rescales.
+#include <cfloat>
+#include <climits>
+
+#include "kernels.h"
+#include "sm103_ptx.cuh"
+
+namespace ra {
+
+namespace {
+
+constexpr int kFwdThreads = 384;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct FwdSmem {
+  static constexpr int kSub = D / 64;                // 64-column sub-tiles per row
+  static constexpr int kTile = 128 * D * 2;          // bytes of a Q, K or V tile
+  static constexpr int kSlots = (D == 128) ? 3 : 6;  // key/value ring slots
+  alignas(1024) uint8_t q[2][kTile];
+  alignas(1024) uint8_t p[2][128 * 128 * 2];
+  alignas(1024) uint8_t kv[kSlots][kTile];
+  alignas(8) uint64_t q_full;
+  alignas(8) uint64_t kv_full[kSlots];
+  alignas(8) uint64_t kv_empty[kSlots];
+  alignas(8) uint64_t s_full[2];
+  alignas(8) uint64_t p_full[2];
+  alignas(8) uint64_t o_final[2];
+  alignas(8) uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+struct FwdDev {
+  int B, Hq, Hkv, L, causal;
+  float scale_log2;
+  const int32_t* order;
+  const int32_t* offsets;
+  const int32_t* ranges;
+  float* lse;
+  int* err;
+};
+
+// Wait that ignores the abort flag (used to drain in-flight copies/MMAs
+// after an abort), still bounded in time.
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, int* err) {
+  int local = 0;
+  mbar_wait(bar, parity, &local, err, kSiteFwdDrain);
+}
+
+template <int D>
+__device__ void fwd_producer(FwdSmem<D>& sm, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+                             const CUtensorMap* tm_v, int q0, int q_z, int kv_z, const int32_t* rg, int nr,
+                             volatile int* ab, int* err) {
+  using S = FwdSmem<D>;
+  const uint32_t qbar = smem_u32(&sm.q_full);
+  mbar_arrive_expect_tx(qbar, 2 * S::kTile);
+  for (int t = 0; t < 2; ++t)
+    for (int sub = 0; sub < S::kSub; ++sub)
+      tma_load_3d(smem_u32(sm.q[t]) + sub * 16384, tm_q, qbar, sub * 64, q0 + 128 * t, q_z);
+  uint32_t n = 0;
+  bool ok = true;
+  for (int ri = 0; ri < nr && ok; ++ri) {
+    for (int jt = rg[2 * ri]; jt < rg[2 * ri + 1] && ok; ++jt) {
+      for (int sel = 0; sel < 2 && ok; ++sel) {
+        const uint32_t slot = n % S::kSlots, use = n / S::kSlots;
+        if (use > 0) ok = mbar_wait(smem_u32(&sm.kv_empty[slot]), (use - 1) & 1, ab, err, kSiteFwdProducer);
+        if (!ok) break;
+        const uint32_t fb = smem_u32(&sm.kv_full[slot]);
+        mbar_arrive_expect_tx(fb, S::kTile);
+        const CUtensorMap* m = sel ? tm_v : tm_k;
+        for (int sub = 0; sub < S::kSub; ++sub)
+          tma_load_3d(smem_u32(sm.kv[slot]) + sub * 16384, m, fb, sub * 64, jt * 128, kv_z);
+        ++n;
+      }
+    }
+  }
+  if (!ok) {
+    // Let every copy this thread issued land before the CTA exits.
+    wait_drain(qbar, 0, err);
+    for (uint32_t i = 0; i < S::kSlots && i < n; ++i) {
+      const uint32_t last = i + S::kSlots * ((n - 1 - i) / S::kSlots);
+      wait_drain(smem_u32(&sm.kv_full[i]), (last / S::kSlots) & 1, err);
+    }
+  }
+}
+
+template <int D>
+__device__ void fwd_mma(FwdSmem<D>& sm, uint32_t tmem, int nkv, volatile int* ab, int* err) {
+  using S = FwdSmem<D>;
+  constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
+  constexpr uint32_t kIdO = idesc_bf16(128, D, false, true);
+  const uint32_t total_uses = 2u * nkv;
+
+  auto issue_s = [&](int t, uint32_t kslot) {
+    const uint32_t qa = smem_u32(sm.q[t]), ka = smem_u32(sm.kv[kslot]);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+      umma_ss(tmem + 128 * t, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), kIdS, kk > 0);
+    }
+  };
+  auto issue_pv = [&](int t, uint32_t vslot, bool acc) {
+    const uint32_t pa = smem_u32(sm.p[t]), va = smem_u32(sm.kv[vslot]);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const uint32_t poff = (kk >> 2) * 16384 + (kk & 3) * 32;
+      umma_ss(tmem + 256 + 128 * t, sdesc_sw128(pa + poff, 16, 1024), sdesc_sw128(va + kk * 2048, 16384, 1024), kIdO,
+              (acc || kk > 0) ? 1u : 0u);
+    }
+  };
+  uint32_t n = 0;
+  auto wait_full = [&](uint32_t& slot, uint32_t& use_idx) -> bool {
+    slot = n % S::kSlots;
+    use_idx = n;
+    const bool r = mbar_wait(smem_u32(&sm.kv_full[slot]), (n / S::kSlots) & 1, ab, err, kSiteFwdMma);
+    ++n;
+    return r;
+  };
+  // Release a slot only if the producer will refill it: every commit is
+  // then awaited by someone before the CTA exits.
+  auto release = [&](uint32_t slot, uint32_t use_idx) {
+    if (use_idx + S::kSlots < total_uses) umma_commit(smem_u32(&sm.kv_empty[slot]));
+  };
+
+  bool ok = mbar_wait(smem_u32(&sm.q_full), 0, ab, err, kSiteFwdMma);
+  if (ok) {
+    uint32_t ks, ku;
+    ok = wait_full(ks, ku);
+    if (ok) {
+      tc_fence_after();
+      issue_s(0, ks);
+      umma_commit(smem_u32(&sm.s_full[0]));
+      issue_s(1, ks);
+      umma_commit(smem_u32(&sm.s_full[1]));
+      release(ks, ku);
+    }
+  }
+  for (int j = 0; j < nkv && ok; ++j) {
+    uint32_t vs, vu, ks = 0, ku = 0;
+    ok = wait_full(vs, vu);
+    const bool has_next = j + 1 < nkv;
+    for (int t = 0; t < 2 && ok; ++t) {
+      ok = mbar_wait(smem_u32(&sm.p_full[t]), j & 1, ab, err, kSiteFwdMma);
+      if (!ok) break;
+      tc_fence_after();
+      issue_pv(t, vs, j > 0);
+      if (has_next) {
+        if (t == 0) {
+          ok = wait_full(ks, ku);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        issue_s(t, ks);
+        umma_commit(smem_u32(&sm.s_full[t]));
+      } else {
+        umma_commit(smem_u32(&sm.o_final[t]));
+      }
+    }
+    if (!ok) break;
+    if (has_next) release(ks, ku);
+    release(vs, vu);
+  }
+  if (!ok) {
+    umma_commit(smem_u32(&sm.drain));
+    wait_drain(smem_u32(&sm.drain), 0, err);
+  }
+}
+
+template <int D>
+__device__ void fwd_softmax(FwdSmem<D>& sm, uint32_t tmem, int t, const FwdDev& p, const CUtensorMap* tm_o,
+                            int q0, int q_z, const int32_t* rg, int nr, volatile int* ab, int* err) {
+  const int wq = (threadIdx.x >> 5) & 3;  // TMEM lane quadrant of this warp
+  const int lane = threadIdx.x & 31;
+  const int row = wq * 32 + lane;
+  const int qpos = q0 + 128 * t + row;
+  const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+  const uint32_t t_s = tmem + 128 * t + lane_off;
+  const uint32_t t_o = tmem + 256 + 128 * t + lane_off;
+  const uint32_t pbase = smem_u32(sm.p[t]);
+  const float c = p.scale_log2;
+  float m = -INFINITY, l = 0.f;
+  bool ok = true;
+  int j = 0;
+  for (int ri = 0; ri < nr && ok; ++ri) {
+    for (int jt = rg[2 * ri]; jt < rg[2 * ri + 1]; ++jt, ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.s_full[t]), j & 1, ab, err, kSiteFwdSoftmax));
+      if (!ok) break;
+      tc_fence_after();
+      float s[128];
+#pragma unroll
+      for (int c0 = 0; c0 < 4; ++c0) {
+        uint32_t r[32];
+        tmem_ld32(t_s + c0 * 32, r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[c0 * 32 + i] = __uint_as_float(r[i]);
+      }
+      const int kv0 = jt * 128;
+      if (kv0 + 128 > p.L || (p.causal && kv0 + 127 > qpos)) {
+        const int lim = min(p.L - 1, p.causal ? qpos : INT_MAX) - kv0;  // valid columns: i <= lim
+#pragma unroll
+        for (int i = 0; i < 128; ++i)
+          if (i > lim) s[i] = -INFINITY;
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int i = 1; i < 128; ++i) mx = fmaxf(mx, s[i]);
+      const float m_new = fmaxf(m, mx * c);
+      const bool resc = m_new > m + kRescaleThreshold;
+      if (j > 0 && __any_sync(0xffffffffu, resc)) {
+        // O_t is quiescent: the commit that signalled S_t(j) covers PV_t(j-1).
+        const float f = resc ? ex2(m - m_new) : 1.f;
+#pragma unroll
+        for (int c0 = 0; c0 < D / 32; ++c0) {
+          uint32_t r[32];
+          tmem_ld32(t_o + c0 * 32, r);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * f);
+          tmem_st32(t_o + c0 * 32, r);
+        }
+      }
+      if (resc) {
+        l *= ex2(m - m_new);
+        m = m_new;
+      }
+      const float ms = (m == -INFINITY) ? 0.f : m;
+      float rs = 0.f;
+#pragma unroll
+      for (int i = 0; i < 128; ++i) {
+        s[i] = ex2(fmaf(s[i], c, -ms));
+        rs += s[i];
+      }
+      l += rs;
+#pragma unroll
+      for (int ch = 0; ch < 16; ++ch) {
+        st_shared_v4(pbase + (ch >> 3) * 16384 + sw128_offset(row, ch & 7), pack_bf16(s[ch * 8], s[ch * 8 + 1]),
+                     pack_bf16(s[ch * 8 + 2], s[ch * 8 + 3]), pack_bf16(s[ch * 8 + 4], s[ch * 8 + 5]),
+                     pack_bf16(s[ch * 8 + 6], s[ch * 8 + 7]));
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sm.p_full[t]));
+    }
+  }
+  if (ok) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.o_final[t]), 0, ab, err, kSiteFwdEpilogue));
+  if (ok) {
+    tc_fence_after();
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    // Normalised O row -> bf16 -> the P buffer (free: the last PV_t is done),
+    // laid out as the 128-byte-swizzled boxes of the output tensor map.
+#pragma unroll
+    for (int c0 = 0; c0 < D / 32; ++c0) {
+      uint32_t r[32];
+      tmem_ld32(t_o + c0 * 32, r);
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const int ch = c0 * 4 + q4;
+        const float* f = reinterpret_cast<const float*>(r) + q4 * 8;
+        st_shared_v4(pbase + (ch >> 3) * 16384 + sw128_offset(row, ch & 7), pack_bf16(f[0] * inv, f[1] * inv),
+                     pack_bf16(f[2] * inv, f[3] * inv), pack_bf16(f[4] * inv, f[5] * inv),
+                     pack_bf16(f[6] * inv, f[7] * inv));
+      }
+    }
+    if (qpos < p.L) p.lse[static_cast<size_t>(q_z) * p.L + qpos] = (m + log2f(l)) * kLn2;
+    fence_proxy_async_smem();
+  }
+  tc_fence_before();
+  named_bar_sync(1 + t, 128);
+  if (ok && row == 0 && q0 + 128 * t < p.L) {  // no store for a tile wholly past the end
+    for (int sub = 0; sub < FwdSmem<D>::kSub; ++sub) tma_store_3d(tm_o, pbase + sub * 16384, sub * 64, q0 + 128 * t, q_z);
+    bulk_commit_group();
+    bulk_wait_group<0>();
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kFwdThreads, 1)
+    ring_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                         const FwdDev p) {
+  using S = FwdSmem<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (smem_u32(smem_raw) & 1023u) {  // the swizzled layouts need a 1024-byte aligned base
+    if (threadIdx.x == 0) atomicCAS(p.err, 0, kSiteFwdMisaligned);
+    return;
+  }
+  S& sm = *reinterpret_cast<S*>(smem_raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int BH = p.B * p.Hq;
+  const int u = p.order[blockIdx.x / BH];
+  const int bh = blockIdx.x % BH;
+  const int b = bh / p.Hq, h = bh % p.Hq;
+  const int kv_z = b * p.Hkv + h / (p.Hq / p.Hkv);
+  const int q0 = u * 256;
+  const int32_t* rg = p.ranges + 2 * p.offsets[u];
+  const int nr = p.offsets[u + 1] - p.offsets[u];
+  volatile int* ab = &sm.abort_flag;
+
+  if (threadIdx.x == 0) {
+    sm.abort_flag = 0;
+    mbar_init(smem_u32(&sm.q_full), 1);
+    for (int i = 0; i < S::kSlots; ++i) {
+      mbar_init(smem_u32(&sm.kv_full[i]), 1);
+      mbar_init(smem_u32(&sm.kv_empty[i]), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(smem_u32(&sm.s_full[t]), 1);
+      mbar_init(smem_u32(&sm.p_full[t]), 128);
+      mbar_init(smem_u32(&sm.o_final[t]), 1);
+    }
+    mbar_init(smem_u32(&sm.drain), 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_o);
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_u32(&sm.tmem_base), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) fwd_producer<D>(sm, &tm_q, &tm_k, &tm_v, q0, bh, kv_z, rg, nr, ab, p.err);
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int nkv = 0;
+      for (int ri = 0; ri < nr; ++ri) nkv += rg[2 * ri + 1] - rg[2 * ri];
+      fwd_mma<D>(sm, tmem, nkv, ab, p.err);
+    }
+  } else if (warp >= 4) {
+    fwd_softmax<D>(sm, tmem, (warp - 4) >> 2, p, &tm_o, q0, bh, rg, nr, ab, p.err);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 2) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+size_t fwd_smem_bytes(int d) {
+  return d == 128 ? sizeof(FwdSmem<128>) : sizeof(FwdSmem<64>);
+}
+
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
+  FwdDev p;
+  p.B = a.B; p.Hq = a.Hq; p.Hkv = a.Hkv; p.L = a.L; p.causal = a.causal;
+  p.scale_log2 = kLog2e / sqrtf(static_cast<float>(a.d));
+  p.order = a.order; p.offsets = a.offsets; p.ranges = a.ranges;
+  p.lse = a.lse; p.err = a.err;
+  const size_t smem = fwd_smem_bytes(a.d);
+  const dim3 grid(static_cast<unsigned>(a.n_blocks) * a.B * a.Hq);
+  cudaError_t e;
+  if (a.d == 128) {
+    e = cudaFuncSetAttribute(ring_attn_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    ring_attn_fwd_kernel<128><<<grid, kFwdThreads, smem, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, p);
+  } else {
+    e = cudaFuncSetAttribute(ring_attn_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    ring_attn_fwd_kernel<64><<<grid, kFwdThreads, smem, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, p);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace ra

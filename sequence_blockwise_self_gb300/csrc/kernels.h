@@ -1,0 +1,63 @@
+// kernels.h -- launch interface between the C ABI and the sm_103a kernels.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace ra {
+
+// Device-side error sites (recorded when a bounded wait gives up).
+enum ErrSite : int {
+  kSiteFwdProducer = 0x101,
+  kSiteFwdMma = 0x102,
+  kSiteFwdSoftmax = 0x103,
+  kSiteFwdEpilogue = 0x104,
+  kSiteFwdDrain = 0x105,
+  kSiteFwdMisaligned = 0x1FF,
+  kSiteBwdProducer = 0x201,
+  kSiteBwdMma = 0x202,
+  kSiteBwdSoftmax = 0x203,
+  kSiteBwdEpilogue = 0x204,
+  kSiteBwdDrain = 0x205,
+  kSiteBwdMisaligned = 0x2FF,
+};
+
+struct FwdArgs {
+  CUtensorMap tm_q, tm_k, tm_v, tm_o;
+  int B, Hq, Hkv, L, d, causal;
+  int n_blocks;             // 256-row query blocks per (b, h)
+  const int32_t* order;     // device [n_blocks]
+  const int32_t* offsets;   // device [n_blocks + 1]
+  const int32_t* ranges;    // device [2 * n_ranges]
+  float* lse;               // device [B*Hq*L]
+  int* err;                 // device status word
+};
+
+struct BwdArgs {
+  CUtensorMap tm_q, tm_k, tm_v, tm_do, tm_dqacc;
+  int B, Hq, Hkv, L, Lpad, d, causal;
+  int n_blocks;             // key/value tiles per (b, kv head)
+  const int32_t* order;
+  const int32_t* offsets;
+  const int32_t* ranges;
+  const void* o;            // bf16 [B*Hq*L*d]
+  const void* dO;           // bf16 [B*Hq*L*d]
+  const float* lse;         // fp32 [B*Hq*L]
+  float* lse2;              // workspace fp32 [B*Hq*Lpad]: lse * log2(e), +inf padding
+  float* Dvec;              // workspace fp32 [B*Hq*Lpad]: rowsum(dO * o), 0 padding
+  float* dq_acc;            // workspace fp32 [B*Hq*Lpad*d]
+  void* dq;                 // bf16 [B*Hq*L*d]
+  void* dk;                 // bf16 [B*Hkv*L*d]
+  void* dv;                 // bf16 [B*Hkv*L*d]
+  int* err;
+};
+
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
+
+// Dynamic shared memory each kernel needs (bytes), for the C ABI's checks.
+size_t fwd_smem_bytes(int d);
+size_t bwd_smem_bytes(int d);
+
+}  // namespace ra

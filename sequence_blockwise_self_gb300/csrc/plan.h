@@ -1,0 +1,56 @@
+// plan.h -- host-side chunk scheduler: chunk map, ring visiting order and
+// launch order of the attention kernels' work items.
+//
+// Citations name the web page "Large-scale distributed AI model training
+// series: sequence parallelism" and its sections:
+//   section 2.3  Ring Self-Attention: L tokens over N devices, L/N each; the
+//                key/value blocks move round a ring, N-1 transfers and N
+//                block computations per device.
+//   section 6.2  Ring Attention: K and V travel together; one ring suffices
+//                once the per-step results are merged (online softmax).
+//   section 7.2  DistFlashAttention, and section 8.2 USP: a causal model
+//                leaves the ring unbalanced; splitting the sequence by
+//                folding it gives every device about the same work.
+#pragma once
+#include <cstdint>
+#include <vector>
+
+namespace ra {
+
+constexpr int kTileRows = 128;      // rows per query / key-value tile
+constexpr int kQBlockRows = 256;    // forward work item: two query tiles
+
+// Rank owning sequence position pos.  Encoder: chunk pos / (L/N).  Causal:
+// the folded pair of sub-chunks {r, 2N-1-r}, each of length L/(2N).
+inline int owner_rank(int L, int N, bool causal, int pos) {
+  if (!causal) return pos / (L / N);
+  const int sub = pos / (L / (2 * N));
+  return sub < N ? sub : 2 * N - 1 - sub;
+}
+
+// True if the chunking is valid for this length.
+inline bool chunking_ok(int L, int N, bool causal) {
+  if (N < 1 || L < 1) return false;
+  const long parts = causal ? 2L * N : N;
+  return parts <= L && L % parts == 0;
+}
+
+struct Plan {
+  int n_blocks = 0;                  // work items per (batch, head)
+  std::vector<int32_t> order;        // [n_blocks] launch order, longest first
+  std::vector<int32_t> offsets;      // [n_blocks + 1] into ranges
+  std::vector<int32_t> ranges;       // (begin, end) tile-index pairs
+  std::vector<int64_t> work;         // [n_blocks] tile pairs per item
+};
+
+// Forward: item u = query rows [256u, 256u+256).  Lists the key/value tiles
+// it visits in the ring order of the rank owning its first row: step s
+// brings the block of rank (r - s) mod N; tiles of one step ascending.
+Plan build_fwd_plan(int L, int N, bool causal);
+
+// Backward: item t = key/value tile t.  Lists the query tiles that see it in
+// the order the block meets them going round the ring: its own rank first,
+// then ranks r + 1, r + 2, ... mod N.
+Plan build_bwd_plan(int L, int N, bool causal);
+
+}  // namespace ra

@@ -1,0 +1,283 @@
+// ring_attn_capi.cu -- the C ABI declared in include/ring_attn.h: argument
+// checks, tensor-map encoding, cached launch plans and kernel launches.
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <map>
+#include <memory>
+#include <mutex>
+#include <tuple>
+
+#include "../../include/ring_attn.h"
+#include "kernels.h"
+#include "plan.h"
+
+namespace ra {
+namespace {
+
+// Status word the kernels write when a bounded wait gives up (one per
+// device: a __device__ variable is instantiated in every device context).
+__device__ int g_device_status;
+
+std::mutex g_mutex;
+
+struct DevicePlan {
+  int n_blocks = 0;
+  int32_t* dev = nullptr;  // order | offsets | ranges
+  const int32_t* order() const { return dev; }
+  const int32_t* offsets() const { return dev + n_blocks; }
+  const int32_t* ranges() const { return dev + 2 * n_blocks + 1; }
+};
+
+std::map<std::tuple<int, int, int, int, int>, DevicePlan> g_plans;  // (device, kind, L, N, causal)
+std::map<int, int*> g_status_ptr;                                   // device -> &g_device_status
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 3-D map over a [z][L][d] tensor, box (box_cols, box_rows, 1) with a
+// 128-byte swizzle; box_cols * element size is 128 bytes, so the shared
+// memory image of a box is box_rows rows of 128 bytes.
+bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_bytes, int d, int L, int Z,
+              int box_cols, int box_rows = 128) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(Z)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * elem_bytes, static_cast<cuuint64_t>(d) * L * elem_bytes};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1u};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_shape(int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || L < 0 || n_chunks <= 0) return RING_ATTN_ERR_SHAPE;
+  if (Hq % Hkv != 0) return RING_ATTN_ERR_SHAPE;
+  if (d != 64 && d != 128) return RING_ATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * Hq >= 65536) return RING_ATTN_ERR_UNSUPPORTED;
+  if (L > 0 && !chunking_ok(L, n_chunks, causal != 0)) return RING_ATTN_ERR_SHAPE;
+  if (L > (1 << 30) / 2) return RING_ATTN_ERR_UNSUPPORTED;
+  return RING_ATTN_OK;
+}
+
+int current_device(int* dev) { return cudaGetDevice(dev) == cudaSuccess ? RING_ATTN_OK : RING_ATTN_ERR_CUDA; }
+
+// Device copy of a plan, built and uploaded on first use of a shape.
+int get_plan(int dev, int kind, int L, int N, int causal, DevicePlan* out) {
+  auto key = std::make_tuple(dev, kind, L, N, causal);
+  auto it = g_plans.find(key);
+  if (it != g_plans.end()) {
+    *out = it->second;
+    return RING_ATTN_OK;
+  }
+  Plan p = kind == 0 ? build_fwd_plan(L, N, causal != 0) : build_bwd_plan(L, N, causal != 0);
+  std::vector<int32_t> flat;
+  flat.insert(flat.end(), p.order.begin(), p.order.end());
+  flat.insert(flat.end(), p.offsets.begin(), p.offsets.end());
+  flat.insert(flat.end(), p.ranges.begin(), p.ranges.end());
+  DevicePlan dp;
+  dp.n_blocks = p.n_blocks;
+  if (cudaMalloc(&dp.dev, flat.size() * sizeof(int32_t)) != cudaSuccess) return RING_ATTN_ERR_CUDA;
+  if (cudaMemcpy(dp.dev, flat.data(), flat.size() * sizeof(int32_t), cudaMemcpyHostToDevice) != cudaSuccess) {
+    cudaFree(dp.dev);
+    return RING_ATTN_ERR_CUDA;
+  }
+  g_plans[key] = dp;
+  *out = dp;
+  return RING_ATTN_OK;
+}
+
+int status_ptr(int dev, int** out) {
+  auto it = g_status_ptr.find(dev);
+  if (it != g_status_ptr.end()) {
+    *out = it->second;
+    return RING_ATTN_OK;
+  }
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return RING_ATTN_ERR_CUDA;
+  g_status_ptr[dev] = static_cast<int*>(p);
+  *out = static_cast<int*>(p);
+  return RING_ATTN_OK;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct BwdLayout {
+  size_t lse2 = 0, dvec = 0, dq = 0, total = 0;
+};
+
+BwdLayout bwd_layout(int B, int Hq, int L, int d) {
+  BwdLayout w;
+  const size_t Lpad = round_up(static_cast<size_t>(L), 128);
+  const size_t rows = static_cast<size_t>(B) * Hq * Lpad;
+  w.lse2 = 0;
+  w.dvec = round_up(rows * sizeof(float), 256);
+  w.dq = w.dvec + round_up(rows * sizeof(float), 256);
+  w.total = w.dq + round_up(rows * d * sizeof(float), 256);
+  return w;
+}
+
+int plan_query(int kind, int L, int n_chunks, int causal, int* n_blocks, int* n_ranges, int32_t* order,
+               int32_t* offsets, int32_t* ranges) {
+  if (L <= 0 || n_chunks <= 0 || !chunking_ok(L, n_chunks, causal != 0)) return RING_ATTN_ERR_SHAPE;
+  Plan p = kind == 0 ? build_fwd_plan(L, n_chunks, causal != 0) : build_bwd_plan(L, n_chunks, causal != 0);
+  if (n_blocks) *n_blocks = p.n_blocks;
+  if (n_ranges) *n_ranges = static_cast<int>(p.ranges.size() / 2);
+  if (order) std::memcpy(order, p.order.data(), p.order.size() * sizeof(int32_t));
+  if (offsets) std::memcpy(offsets, p.offsets.data(), p.offsets.size() * sizeof(int32_t));
+  if (ranges) std::memcpy(ranges, p.ranges.data(), p.ranges.size() * sizeof(int32_t));
+  return RING_ATTN_OK;
+}
+
+}  // namespace
+}  // namespace ra
+
+using namespace ra;
+
+extern "C" {
+
+const char* ring_attn_strerror(int status) {
+  switch (status) {
+    case RING_ATTN_OK: return "ok";
+    case RING_ATTN_ERR_NULL: return "a required pointer is NULL";
+    case RING_ATTN_ERR_SHAPE: return "invalid shape or chunking";
+    case RING_ATTN_ERR_UNSUPPORTED: return "unsupported head dimension, alignment or size";
+    case RING_ATTN_ERR_WORKSPACE: return "backward workspace missing or too small";
+    case RING_ATTN_ERR_CUDA: return "CUDA runtime or driver call failed";
+    case RING_ATTN_ERR_DEVICE_TIMEOUT: return "a kernel aborted a bounded wait";
+    default: return "unknown status";
+  }
+}
+
+int ring_attn_owner_rank(int L, int n_chunks, int causal, int pos) {
+  if (L <= 0 || n_chunks <= 0 || !chunking_ok(L, n_chunks, causal != 0)) return RING_ATTN_ERR_SHAPE;
+  if (pos < 0 || pos >= L) return RING_ATTN_ERR_SHAPE;
+  return owner_rank(L, n_chunks, causal != 0, pos);
+}
+
+int ring_attn_fwd_plan(int L, int n_chunks, int causal, int* n_blocks, int* n_ranges, int32_t* block_order,
+                       int32_t* range_offsets, int32_t* ranges) {
+  return plan_query(0, L, n_chunks, causal, n_blocks, n_ranges, block_order, range_offsets, ranges);
+}
+
+int ring_attn_bwd_plan(int L, int n_chunks, int causal, int* n_blocks, int* n_ranges, int32_t* block_order,
+                       int32_t* range_offsets, int32_t* ranges) {
+  return plan_query(1, L, n_chunks, causal, n_blocks, n_ranges, block_order, range_offsets, ranges);
+}
+
+int ring_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int L,
+                  int d, int n_chunks, int causal, cudaStream_t stream) {
+  int rc = check_shape(B, Hq, Hkv, L, d, n_chunks, causal);
+  if (rc != RING_ATTN_OK) return rc;
+  if (B == 0 || L == 0) return RING_ATTN_OK;
+  if (!q || !k || !v || !o || !lse) return RING_ATTN_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return RING_ATTN_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  int dev;
+  if ((rc = current_device(&dev)) != RING_ATTN_OK) return rc;
+  FwdArgs a;
+  std::memset(&a, 0, sizeof a);
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (!make_map(&a.tm_q, q, bf, 2, d, L, B * Hq, 64) || !make_map(&a.tm_k, k, bf, 2, d, L, B * Hkv, 64) ||
+      !make_map(&a.tm_v, v, bf, 2, d, L, B * Hkv, 64) || !make_map(&a.tm_o, o, bf, 2, d, L, B * Hq, 64))
+    return RING_ATTN_ERR_CUDA;
+  DevicePlan plan;
+  if ((rc = get_plan(dev, 0, L, n_chunks, causal != 0, &plan)) != RING_ATTN_OK) return rc;
+  int* err;
+  if ((rc = status_ptr(dev, &err)) != RING_ATTN_OK) return rc;
+  a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.L = L; a.d = d; a.causal = causal != 0;
+  a.n_blocks = plan.n_blocks;
+  a.order = plan.order(); a.offsets = plan.offsets(); a.ranges = plan.ranges();
+  a.lse = lse; a.err = err;
+  return launch_fwd(a, stream) == cudaSuccess ? RING_ATTN_OK : RING_ATTN_ERR_CUDA;
+}
+
+size_t ring_attn_bwd_workspace_size(int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal) {
+  if (check_shape(B, Hq, Hkv, L, d, n_chunks, causal) != RING_ATTN_OK) return 0;
+  return bwd_layout(B, Hq, L, d).total;
+}
+
+int ring_attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                  void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal,
+                  void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  int rc = check_shape(B, Hq, Hkv, L, d, n_chunks, causal);
+  if (rc != RING_ATTN_OK) return rc;
+  if (B == 0 || L == 0) return RING_ATTN_OK;
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return RING_ATTN_ERR_NULL;
+  const void* ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return RING_ATTN_ERR_UNSUPPORTED;
+  const BwdLayout w = bwd_layout(B, Hq, L, d);
+  if (!workspace || workspace_bytes < w.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return RING_ATTN_ERR_WORKSPACE;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  int dev;
+  if ((rc = current_device(&dev)) != RING_ATTN_OK) return rc;
+  BwdArgs a;
+  std::memset(&a, 0, sizeof a);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const int Lpad = static_cast<int>(round_up(static_cast<size_t>(L), 128));
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (!make_map(&a.tm_q, q, bf, 2, d, L, B * Hq, 64) || !make_map(&a.tm_k, k, bf, 2, d, L, B * Hkv, 64) ||
+      !make_map(&a.tm_v, v, bf, 2, d, L, B * Hkv, 64) || !make_map(&a.tm_do, dO, bf, 2, d, L, B * Hq, 64) ||
+      !make_map(&a.tm_dqacc, ws + w.dq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, Lpad, B * Hq, 32, 32))
+    return RING_ATTN_ERR_CUDA;
+  DevicePlan plan;
+  if ((rc = get_plan(dev, 1, L, n_chunks, causal != 0, &plan)) != RING_ATTN_OK) return rc;
+  int* err;
+  if ((rc = status_ptr(dev, &err)) != RING_ATTN_OK) return rc;
+  a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.L = L; a.Lpad = Lpad; a.d = d; a.causal = causal != 0;
+  a.n_blocks = plan.n_blocks;
+  a.order = plan.order(); a.offsets = plan.offsets(); a.ranges = plan.ranges();
+  a.o = o; a.dO = dO; a.lse = lse;
+  a.lse2 = reinterpret_cast<float*>(ws + w.lse2);
+  a.Dvec = reinterpret_cast<float*>(ws + w.dvec);
+  a.dq_acc = reinterpret_cast<float*>(ws + w.dq);
+  a.dq = dq; a.dk = dk; a.dv = dv; a.err = err;
+  return launch_bwd(a, stream) == cudaSuccess ? RING_ATTN_OK : RING_ATTN_ERR_CUDA;
+}
+
+int ring_attn_device_status(cudaStream_t stream, int* site) {
+  if (site) *site = 0;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  int dev;
+  if (current_device(&dev) != RING_ATTN_OK) return RING_ATTN_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return RING_ATTN_ERR_CUDA;
+  int* p;
+  if (status_ptr(dev, &p) != RING_ATTN_OK) return RING_ATTN_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, p, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return RING_ATTN_ERR_CUDA;
+  if (v == 0) return RING_ATTN_OK;
+  if (site) *site = v;
+  const int zero = 0;
+  if (cudaMemcpy(p, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) return RING_ATTN_ERR_CUDA;
+  return RING_ATTN_ERR_DEVICE_TIMEOUT;
+}
+
+void ring_attn_release(void) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  int cur = 0;
+  cudaGetDevice(&cur);
+  for (auto& kv : g_plans) {
+    cudaSetDevice(std::get<0>(kv.first));
+    cudaFree(kv.second.dev);
+  }
+  cudaSetDevice(cur);
+  g_plans.clear();
+}
+
+}  // extern "C"

@@ -1,0 +1,155 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle.
+
+Tolerances (bf16 outputs and gradients, fp32 accumulation): max-abs error
+<= 2e-2 and mean-abs error <= 2e-3 on o, dq, dk, dv; lse within 1e-3.
+Small shapes are compared element by element on every output; the large
+workloads on sampled rows (256 query rows per head; key rows for dk/dv).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sequence_blockwise_self_gb300 as ra
+from sequence_blockwise_self_gb300 import build as lib_build
+from sequence_blockwise_self_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+TOL_MAX, TOL_MEAN, TOL_LSE = 2e-2, 2e-3, 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    lib_build.build()
+    ra.load()
+
+
+def f64(t):
+    return t.detach().float().cpu().double().numpy()
+
+
+def assert_close(name, got, want, tol_max=TOL_MAX, tol_mean=TOL_MEAN):
+    err = np.abs(np.asarray(got, dtype=np.float64) - want)
+    assert np.all(np.isfinite(got)), f"{name}: non-finite values"
+    assert err.max() <= tol_max and err.mean() <= tol_mean, \
+        f"{name}: max-abs {err.max():.3e} (tol {tol_max}), mean-abs {err.mean():.3e} (tol {tol_mean})"
+
+
+def assert_status_ok():
+    st, site = ra.device_status()
+    assert st == 0, f"device status {st} at site {site:#x}"
+
+
+def gpu_fwd_bwd(q, k, v, dO, n_chunks, causal):
+    qd, kd, vd, dOd = (x.cuda() for x in (q, k, v, dO))
+    o, lse = ra.ring_attn_fwd(qd, kd, vd, n_chunks, causal)
+    dq, dk, dv = ra.ring_attn_bwd(qd, kd, vd, o, lse, dOd, n_chunks, causal)
+    torch.cuda.synchronize()
+    assert_status_ok()
+    return o, lse, dq, dk, dv
+
+
+# (B, Hq, Hkv, L, d, n_chunks, causal)
+SMALL = [
+    (1, 2, 2, 256, 64, 1, False),     # the tiny workload, every chunk count
+    (1, 2, 2, 256, 64, 2, False),
+    (1, 2, 2, 256, 64, 4, False),
+    (1, 4, 2, 512, 128, 1, True),     # GQA causal, sub-chunks of 256 / 128 / 64
+    (1, 4, 2, 512, 128, 2, True),
+    (1, 4, 2, 512, 128, 4, True),
+    (2, 2, 1, 384, 64, 3, True),      # MQA, odd tile count, c = 64
+    (2, 8, 2, 768, 128, 3, False),    # GQA G = 4, N = 3
+    (1, 2, 2, 200, 128, 2, False),    # ragged: L not a multiple of the tile
+    (1, 2, 2, 200, 64, 2, True),
+    (1, 3, 1, 1000, 128, 5, True),    # ragged, chunks of 100 rows
+    (1, 2, 2, 1024, 128, 8, True),
+    (1, 2, 2, 128, 128, 1, True),     # a single tile
+    (1, 1, 1, 2, 64, 1, True),        # degenerate: two tokens
+]
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: "B{}H{}-{}L{}d{}N{}{}".format(*s[:6], "c" if s[6] else "e"))
+def test_small_shapes_full_parity(shape):
+    B, Hq, Hkv, L, d, N, causal = shape
+    q, k, v, dO = inputs.make_inputs(B, Hq, Hkv, L, d, seed=1000 + SMALL.index(shape))
+    o, lse, dq, dk, dv = gpu_fwd_bwd(q, k, v, dO, N, causal)
+    o_ref, lse_ref = oracle.fwd(f64(q), f64(k), f64(v), causal)
+    dq_ref, dk_ref, dv_ref, _, _ = oracle.bwd(f64(q), f64(k), f64(v), f64(dO), causal)
+    assert_close("o", f64(o), o_ref)
+    assert_close("lse", f64(lse), lse_ref, TOL_LSE, TOL_LSE)
+    assert_close("dq", f64(dq), dq_ref)
+    assert_close("dk", f64(dk), dk_ref)
+    assert_close("dv", f64(dv), dv_ref)
+
+
+def test_chunk_count_changes_only_rounding():
+    """The same inputs through N = 1, 2, 4, 8: outputs agree to fp32
+    summation-order differences (well inside the bf16 tolerance)."""
+    B, Hq, Hkv, L, d = 1, 4, 2, 1024, 128
+    q, k, v, dO = inputs.make_inputs(B, Hq, Hkv, L, d, seed=77)
+    outs = [gpu_fwd_bwd(q, k, v, dO, N, True) for N in (1, 2, 4, 8)]
+    for other in outs[1:]:
+        for a, b, name in zip(outs[0], other, ("o", "lse", "dq", "dk", "dv")):
+            assert_close(name, f64(b), f64(a), 1e-2, 1e-3)
+
+
+def test_repeat_calls_are_deterministic_in_forward():
+    q, k, v, dO = inputs.make_inputs(1, 2, 2, 512, 128, seed=5)
+    o1, l1, *_ = gpu_fwd_bwd(q, k, v, dO, 2, True)
+    o2, l2, *_ = gpu_fwd_bwd(q, k, v, dO, 2, True)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_empty_problem_is_a_no_op():
+    q = torch.empty((0, 2, 128, 64), dtype=torch.bfloat16, device="cuda")
+    o, lse = ra.ring_attn_fwd(q, q[:, :2], q[:, :2], 1, False)
+    assert o.numel() == 0 and lse.numel() == 0
+
+
+# ------------------------------------------------------------ full workloads
+
+def _sampled_parity(w: inputs.Workload, chunk_counts):
+    q, k, v, dO = inputs.workload_inputs(w)
+    seed = inputs.WORKLOAD_SEEDS[w.name]
+    rows = inputs.sample_rows(w.L, w.n_chunks, w.causal, 256, seed)
+    k_rows = inputs.tail_rows(w.L, 256) if w.causal else inputs.sample_rows(w.L, w.n_chunks, False, 256, seed + 1)
+    qf, kf, vf, dOf = f64(q), f64(k), f64(v), f64(dO)
+    o_ref, lse_ref, _ = oracle.fwd_rows(qf, kf, vf, w.causal, rows)
+    dq_ref, dk_ref, dv_ref = oracle.bwd_rows(qf, kf, vf, dOf, w.causal, rows, k_rows)
+    del qf, dOf
+    for N in chunk_counts:
+        o, lse, dq, dk, dv = gpu_fwd_bwd(q, k, v, dO, N, w.causal)
+        ri = torch.from_numpy(rows).long().cuda()
+        ki = torch.from_numpy(k_rows).long().cuda()
+        assert_close(f"o N={N}", f64(o[:, :, ri]), o_ref)
+        assert_close(f"lse N={N}", f64(lse[:, :, ri]), lse_ref, TOL_LSE, TOL_LSE)
+        assert_close(f"dq N={N}", f64(dq[:, :, ri]), dq_ref)
+        assert_close(f"dk N={N}", f64(dk[:, :, ki]), dk_ref)
+        assert_close(f"dv N={N}", f64(dv[:, :, ki]), dv_ref)
+        del o, lse, dq, dk, dv
+        torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name", ["encoder", "decoder_mha", "gqa_32k"])
+def test_workload_sampled_parity(name):
+    w = inputs.WORKLOADS[name]
+    _sampled_parity(w, sorted({1, 2, 4, w.n_chunks}))
+
+
+def test_workload_128k_sampled_parity():
+    """The long-context workload at full size, in the benchmark's launch
+    configuration (same entry points, same shapes, same chunk count)."""
+    w = inputs.WORKLOADS["gqa_128k"]
+    _sampled_parity(w, [w.n_chunks])
+
+
+def test_tiny_workload_full_parity():
+    w = inputs.WORKLOADS["tiny"]
+    q, k, v, dO = inputs.workload_inputs(w)
+    o, lse, dq, dk, dv = gpu_fwd_bwd(q, k, v, dO, w.n_chunks, w.causal)
+    o_ref, lse_ref = oracle.fwd(f64(q), f64(k), f64(v), w.causal)
+    dq_ref, dk_ref, dv_ref, _, _ = oracle.bwd(f64(q), f64(k), f64(v), f64(dO), w.causal)
+    for name, g, r in (("o", o, o_ref), ("dq", dq, dq_ref), ("dk", dk, dk_ref), ("dv", dv, dv_ref)):
+        assert_close(name, f64(g), r)
+    assert_close("lse", f64(lse), lse_ref, TOL_LSE, TOL_LSE)
