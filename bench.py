@@ -1,0 +1,367 @@
+#!/usr/bin/env python
+"""Benchmark of blockwise Ring Self-Attention (forward + backward) on GB300.
+
+One step = one forward and one backward pass (all steps of the hot path)
+over one batch of the long-context causal GQA workload (B=1, Hq=28, Hkv=4,
+L=131072, d=128, 32 ring chunks, folded causal assignment).  FLOPs follow
+the usual accounting: forward 4 B Hq L^2 d, halved when causal; backward
+2.5 x forward.  Inputs (q, k, v, dO: 0.94 + 0.13 + 0.13 + 0.94 GB) are far
+larger than L2, so no cache flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 (torchrun) every rank runs an independent replica of the step
+(the ring is emulated on one GPU; nothing is exchanged), and `value` is the
+sum of all ranks' FLOPs over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention TFLOP/s fwd & fwd+bwd at 1 GB300; % of dense BF16 tensor peak"
+DEFAULT_WORKLOAD = "gqa_128k"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return {"burst": float(p["bf16_tflops"]), "sustained": float(p["bf16_tflops_sustained"]),
+                "hbm_gbs": float(p["hbm_gbs"]), "source": "measured"}
+    except Exception:
+        return {"burst": 1900.0, "sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def _describe(w):
+    kind = "causal GQA" if w.causal and w.Hq != w.Hkv else ("causal MHA" if w.causal else "encoder")
+    return (f"{w.name}: {kind}, B={w.B} Hq={w.Hq} Hkv={w.Hkv} L={w.L} d={w.d}, N={w.n_chunks} ring chunks"
+            + (", folded (zig-zag) causal assignment" if w.causal else ""))
+
+
+# --------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.tmp = None
+
+    def __enter__(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.tmp is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.tmp.flush()
+        with open(self.tmp.name) as f:
+            lines = [ln.strip() for ln in f if ln.strip()]
+        os.unlink(self.tmp.name)
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _gpu_id(torch, dev):
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        return vis.split(",")[dev] if vis else str(dev)
+
+
+# ------------------------------------------------------------ CPU oracle
+
+def oracle_sample(w, q, k, v, dO, seconds_target: float, seed: int):
+    """Time the fp64 oracle on a bounded sample of the workload: forward and
+    dq (the oracle's backward for a query row, which recomputes the row's
+    statistics) for sampled query rows of the first kv-head group of batch 0.
+    Returns (TFLOP/s by the workload's accounting, details)."""
+    import numpy as np
+
+    import oracle
+
+    G = w.Hq // w.Hkv
+    q64 = q[:1, :G].double().numpy()
+    k64 = k[:1, :1].double().numpy()
+    v64 = v[:1, :1].double().numpy()
+    dO64 = dO[:1, :G].double().numpy()
+    rng = np.random.default_rng(seed)
+    threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+
+    def run(n_rows):
+        rows = np.sort(rng.choice(w.L, size=n_rows, replace=False)).astype(np.int32)
+        t0 = time.perf_counter()
+        oracle.fwd_rows(q64, k64, v64, w.causal, rows, threads=threads)
+        oracle.bwd_rows(q64, k64, v64, dO64, w.causal, rows, np.zeros(0, dtype=np.int32), threads=threads)
+        dt = time.perf_counter() - t0
+        keys = (rows.astype(np.float64) + 1).sum() if w.causal else float(w.L) * n_rows
+        flops = 3.5 * 4.0 * w.d * keys * G  # fwd + bwd accounting of the sampled rows
+        return flops, dt, rows
+
+    # calibrate on a few rows, then size the sample to the time target
+    f0, t0, _ = run(max(4, threads))
+    per_row = t0 / max(4, threads)
+    n = int(min(w.L, max(threads, seconds_target / max(per_row, 1e-9))))
+    flops, dt, rows = run(n)
+    return flops / dt / 1e12, {"rows": int(n), "heads": G, "seconds": dt, "flops": flops, "cores": threads}
+
+
+# ---------------------------------------------------------------- arms
+
+def run_reference(args, w):
+    """The oracle as it stands, timed on the host cores (rank 0 only)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from sequence_blockwise_self_gb300 import inputs
+    import oracle
+
+    oracle.build()
+    q, k, v, dO = inputs.workload_inputs(w)
+    per_step = []
+    details = None
+    for i in range(args.warmup + args.steps):
+        tf, det = oracle_sample(w, q, k, v, dO, seconds_target=3.0, seed=100 + i)
+        if i >= args.warmup:
+            per_step.append((tf, det))
+            details = det
+    value = statistics.median([t for t, _ in per_step])
+    sec = sum(d["seconds"] for _, d in per_step)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec / max(1, len(per_step)),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic: q,k,v,dO ~ N(0,1) rounded to bf16, seeded",
+        "config": {"workload": _describe(w)},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": details["cores"], "kind": "oracle",
+                         "sample": f"fp64 oracle forward + dq on {details['rows']} random query rows x "
+                                   f"{details['heads']} heads (one kv group) per step; FLOPs by the workload's "
+                                   f"fwd+bwd accounting of those rows"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+
+    import sequence_blockwise_self_gb300 as ra
+    from sequence_blockwise_self_gb300 import build as lib_build
+    from sequence_blockwise_self_gb300 import inputs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    lib_build.build()
+    ra.load()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    # inputs: seeded on the CPU (rank-dependent seed), pinned for the e2e leg
+    q, k, v, dO = inputs.workload_inputs(w, seed=inputs.WORKLOAD_SEEDS[w.name] + 1000 * rank)
+    host_in = [t.pin_memory() for t in (q, k, v, dO)]
+    qd, kd, vd, dOd = (t.to(dev) for t in host_in)
+    o = torch.empty_like(qd)
+    lse = torch.empty((w.B, w.Hq, w.L), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    ws = torch.empty(ra.bwd_workspace_size(w.B, w.Hq, w.Hkv, w.L, w.d, w.n_chunks, w.causal), dtype=torch.uint8,
+                     device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(qx, kx, vx, dOx):
+        ra.ring_attn_fwd(qx, kx, vx, w.n_chunks, w.causal, o=o, lse=lse, stream=stream)
+        ra.ring_attn_bwd(qx, kx, vx, o, lse, dOx, w.n_chunks, w.causal, dq=dq, dk=dk, dv=dv, workspace=ws,
+                         stream=stream)
+
+    for _ in range(args.warmup):
+        step(qd, kd, vd, dOd)
+    torch.cuda.synchronize(dev)
+    st, site = ra.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} at site {site:#x} during warm-up")
+
+    def max_over_ranks(x: float) -> float:
+        if world == 1:
+            return x
+        t = torch.tensor([x], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    # (1) device-resident timed region
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(_gpu_id(torch, local)) as clk:
+        barrier()
+        torch.cuda.synchronize(dev)
+        start.record(stream)
+        for _ in range(args.steps):
+            step(qd, kd, vd, dOd)
+        stop.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+    ms_total = max_over_ranks(start.elapsed_time(stop))
+    clocks = clk.summary()
+    st, site = ra.device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} at site {site:#x}")
+    ms_step = ms_total / args.steps
+    F = w.fwd_flops()
+    step_flops = 3.5 * F
+    value = world * step_flops * args.steps / (ms_total * 1e-3) / 1e12
+
+    # (2) per-kernel durations (events around each launch, same stream)
+    ra.profile_enable(True)
+    for _ in range(args.steps):
+        step(qd, kd, vd, dOd)
+    torch.cuda.synchronize(dev)
+    prof = ra.profile_read()
+    ra.profile_enable(False)
+    per_kernel = {k: {"ms_avg": (ms / n if n else None), "launches": n} for k, (ms, n) in prof.items()}
+    t_fwd = per_kernel["fwd"]["ms_avg"]
+    t_bwd_main = per_kernel["bwd_main"]["ms_avg"]
+    t_bwd = sum(per_kernel[k]["ms_avg"] or 0.0 for k in ("bwd_pre", "bwd_main", "bwd_post"))
+    peaks = _peaks()
+    bwd_main_tflops = 2.5 * F / (t_bwd_main * 1e-3) / 1e12
+    fwd_tflops = F / (t_fwd * 1e-3) / 1e12
+    dominant = "bwd_main" if t_bwd_main >= t_fwd else "fwd"
+    dom_tflops = bwd_main_tflops if dominant == "bwd_main" else fwd_tflops
+    roofline = {
+        "kernel": "ring_attn_bwd_kernel" if dominant == "bwd_main" else "ring_attn_fwd_kernel",
+        "bound": "tensor", "achieved": dom_tflops, "peak": peaks["sustained"], "unit": "TFLOP/s",
+        "frac": dom_tflops / peaks["sustained"], "traffic": None,
+        "peak_kind": f"bf16_tflops_sustained ({peaks['source']})",
+        "frac_of_burst_peak": dom_tflops / peaks["burst"],
+        "flops_per_launch": 2.5 * F if dominant == "bwd_main" else F,
+    }
+
+    # (3) end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, lse, dq, dk, dv)]
+        h2d = sum(t.numel() * t.element_size() for t in host_in)
+        d2h = sum(t.numel() * t.element_size() for t in host_out)
+        qe, ke, ve, dOe = (torch.empty_like(x) for x in (qd, kd, vd, dOd))
+        barrier()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            for dst, src in zip((qe, ke, ve, dOe), host_in):
+                dst.copy_(src, non_blocking=True)
+            step(qe, ke, ve, dOe)
+            for dst, src in zip(host_out, (o, lse, dq, dk, dv)):
+                dst.copy_(src, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        ms_e2e = max_over_ranks(e0.elapsed_time(e1))
+        e2e = {"value": world * step_flops * args.steps / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e / args.steps}
+        del qe, ke, ve, dOe
+
+    # (4) CPU oracle baseline (rank 0, one GPU only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tf, det = oracle_sample(w, q, k, v, dO, seconds_target=15.0, seed=7)
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": det["cores"], "kind": "oracle",
+               "sample": f"fp64 oracle forward + dq on {det['rows']} random query rows x {det['heads']} heads "
+                         f"(one kv group) of this workload, {det['seconds']:.1f} s; FLOPs by the workload's "
+                         f"fwd+bwd accounting of those rows"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic: q,k,v,dO ~ N(0,1) drawn in fp32 and rounded to bf16, seeded per rank",
+            "config": {"workload": _describe(w), "global_batch": w.B * world, "seq_len": w.L,
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": "inputs larger than L2 (q and dO 0.94 GB each); no flush"},
+            "fwd": {"ms": t_fwd, "tflops": fwd_tflops, "frac_of_sustained_peak": fwd_tflops / peaks["sustained"],
+                    "frac_of_burst_peak": fwd_tflops / peaks["burst"]},
+            "bwd": {"ms": t_bwd, "tflops": 2.5 * F / (t_bwd * 1e-3) / 1e12,
+                    "frac_of_sustained_peak": 2.5 * F / (t_bwd * 1e-3) / 1e12 / peaks["sustained"]},
+            "per_kernel": per_kernel,
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": 4 * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    from sequence_blockwise_self_gb300 import inputs
+
+    w = inputs.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

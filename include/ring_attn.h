@@ -89,6 +89,23 @@ const char* ring_attn_strerror(int status);
  */
 int ring_attn_device_status(cudaStream_t stream, int* site);
 
+/* ---------------------------------------------------------------------
+ * Per-kernel timing, for measurement.  While enabled, every kernel launch
+ * of the library is bracketed by two CUDA events recorded on the launch
+ * stream.  ring_attn_profile_read() waits for those events and returns,
+ * per kernel kind, the summed milliseconds and the number of launches since
+ * the last read (arrays of RING_ATTN_N_KERNELS entries), then forgets them.
+ * ------------------------------------------------------------------- */
+enum {
+  RING_ATTN_KERNEL_FWD = 0,      /* forward attention kernel */
+  RING_ATTN_KERNEL_BWD_PRE = 1,  /* backward pre-pass: D, log2 lse, zero dq accumulator */
+  RING_ATTN_KERNEL_BWD_MAIN = 2, /* fused backward kernel */
+  RING_ATTN_KERNEL_BWD_POST = 3, /* dq accumulator -> bf16 */
+  RING_ATTN_N_KERNELS = 4
+};
+int ring_attn_profile_enable(int on);
+int ring_attn_profile_read(double* ms, long long* launches);
+
 /* Frees cached launch plans (device copies of schedules). Optional. */
 void ring_attn_release(void);
 

@@ -14,6 +14,8 @@ from .capi import (  # noqa: F401
     fwd_plan,
     load,
     owner_rank,
+    profile_enable,
+    profile_read,
     release,
     ring_attn_bwd,
     ring_attn_fwd,

@@ -60,6 +60,10 @@ def load():
     lib.ring_attn_release.restype = None
     lib.ring_attn_owner_rank.argtypes = [I, I, I, I]
     lib.ring_attn_owner_rank.restype = I
+    lib.ring_attn_profile_enable.argtypes = [I]
+    lib.ring_attn_profile_enable.restype = I
+    lib.ring_attn_profile_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_longlong)]
+    lib.ring_attn_profile_read.restype = I
     for f in (lib.ring_attn_fwd_plan, lib.ring_attn_bwd_plan):
         f.argtypes = [I, I, I, IP, IP, I32P, I32P, I32P]
         f.restype = I
@@ -184,6 +188,23 @@ def device_status(stream=None):
     site = ctypes.c_int(0)
     rc = load().ring_attn_device_status(_stream(stream), ctypes.byref(site))
     return rc, site.value
+
+
+KERNEL_NAMES = ("fwd", "bwd_pre", "bwd_main", "bwd_post")
+
+
+def profile_enable(on: bool = True):
+    load().ring_attn_profile_enable(int(bool(on)))
+
+
+def profile_read():
+    """{kernel: (summed ms, launches)} since the last read (waits for them)."""
+    ms = (ctypes.c_double * 4)()
+    n = (ctypes.c_longlong * 4)()
+    rc = load().ring_attn_profile_read(ms, n)
+    if rc != OK:
+        raise RingAttnError(rc, "ring_attn_profile_read")
+    return {k: (ms[i], int(n[i])) for i, k in enumerate(KERNEL_NAMES)}
 
 
 def release():

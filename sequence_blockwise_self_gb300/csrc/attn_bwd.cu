@@ -477,10 +477,12 @@ template <int D>
 cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
   const long long rows = static_cast<long long>(a.B) * a.Hq * a.Lpad;
   const unsigned pre_blocks = static_cast<unsigned>((rows * 32 + 255) / 256);
+  if (a.timer) a.timer->mark(1, false, stream);
   ring_attn_bwd_pre_kernel<D><<<pre_blocks, 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dO), a.lse, a.lse2, a.Dvec,
       a.dq_acc, a.L, a.Lpad, rows);
   cudaError_t e = cudaGetLastError();
+  if (a.timer) a.timer->mark(1, true, stream);
   if (e != cudaSuccess) return e;
 
   BwdDev p;
@@ -496,14 +498,19 @@ cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
   e = cudaFuncSetAttribute(ring_attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const dim3 grid(static_cast<unsigned>(a.n_blocks) * a.B * a.Hkv);
+  if (a.timer) a.timer->mark(2, false, stream);
   ring_attn_bwd_kernel<D><<<grid, kBwdThreads, smem, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dqacc, p);
   e = cudaGetLastError();
+  if (a.timer) a.timer->mark(2, true, stream);
   if (e != cudaSuccess) return e;
 
   const long long n8 = static_cast<long long>(a.B) * a.Hq * a.L * D / 8;
+  if (a.timer) a.timer->mark(3, false, stream);
   ring_attn_bwd_post_kernel<D><<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, stream>>>(
       a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), p.scale, a.L, a.Lpad, n8);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (a.timer) a.timer->mark(3, true, stream);
+  return e;
 }
 
 }  // namespace

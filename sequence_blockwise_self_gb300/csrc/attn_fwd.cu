@@ -385,16 +385,14 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
   const size_t smem = fwd_smem_bytes(a.d);
   const dim3 grid(static_cast<unsigned>(a.n_blocks) * a.B * a.Hq);
   cudaError_t e;
-  if (a.d == 128) {
-    e = cudaFuncSetAttribute(ring_attn_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    ring_attn_fwd_kernel<128><<<grid, kFwdThreads, smem, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, p);
-  } else {
-    e = cudaFuncSetAttribute(ring_attn_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    ring_attn_fwd_kernel<64><<<grid, kFwdThreads, smem, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, p);
-  }
-  return cudaGetLastError();
+  auto kernel = a.d == 128 ? ring_attn_fwd_kernel<128> : ring_attn_fwd_kernel<64>;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  if (a.timer) a.timer->mark(0, false, stream);
+  kernel<<<grid, kFwdThreads, smem, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, p);
+  e = cudaGetLastError();
+  if (a.timer) a.timer->mark(0, true, stream);
+  return e;
 }
 
 }  // namespace ra

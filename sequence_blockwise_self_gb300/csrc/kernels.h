@@ -23,6 +23,11 @@ enum ErrSite : int {
   kSiteBwdMisaligned = 0x2FF,
 };
 
+// Optional hook that brackets each launch with events (measurement only).
+struct LaunchTimer {
+  virtual void mark(int kind, bool end, cudaStream_t stream) = 0;
+};
+
 struct FwdArgs {
   CUtensorMap tm_q, tm_k, tm_v, tm_o;
   int B, Hq, Hkv, L, d, causal;
@@ -32,6 +37,7 @@ struct FwdArgs {
   const int32_t* ranges;    // device [2 * n_ranges]
   float* lse;               // device [B*Hq*L]
   int* err;                 // device status word
+  LaunchTimer* timer;       // nullptr unless profiling
 };
 
 struct BwdArgs {
@@ -51,6 +57,7 @@ struct BwdArgs {
   void* dk;                 // bf16 [B*Hkv*L*d]
   void* dv;                 // bf16 [B*Hkv*L*d]
   int* err;
+  LaunchTimer* timer;       // nullptr unless profiling
 };
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);

@@ -32,6 +32,30 @@ struct DevicePlan {
 std::map<std::tuple<int, int, int, int, int>, DevicePlan> g_plans;  // (device, kind, L, N, causal)
 std::map<int, int*> g_status_ptr;                                   // device -> &g_device_status
 
+// Event pairs around launches while profiling is on.
+struct EventTimer : LaunchTimer {
+  bool on = false;
+  struct Rec { int kind; cudaEvent_t start, stop; };
+  std::vector<Rec> recs;
+  cudaEvent_t pending[RING_ATTN_N_KERNELS] = {};
+  void mark(int kind, bool end, cudaStream_t stream) override {
+    if (!end) {
+      cudaEvent_t ev;
+      if (cudaEventCreate(&ev) != cudaSuccess) return;
+      cudaEventRecord(ev, stream);
+      pending[kind] = ev;
+    } else if (pending[kind]) {
+      cudaEvent_t ev;
+      if (cudaEventCreate(&ev) != cudaSuccess) return;
+      cudaEventRecord(ev, stream);
+      recs.push_back({kind, pending[kind], ev});
+      pending[kind] = nullptr;
+    }
+  }
+};
+EventTimer g_timer;
+LaunchTimer* active_timer() { return g_timer.on ? &g_timer : nullptr; }
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (!fn) {
@@ -202,7 +226,7 @@ int ring_attn_fwd(const void* q, const void* k, const void* v, void* o, float* l
   a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.L = L; a.d = d; a.causal = causal != 0;
   a.n_blocks = plan.n_blocks;
   a.order = plan.order(); a.offsets = plan.offsets(); a.ranges = plan.ranges();
-  a.lse = lse; a.err = err;
+  a.lse = lse; a.err = err; a.timer = active_timer();
   return launch_fwd(a, stream) == cudaSuccess ? RING_ATTN_OK : RING_ATTN_ERR_CUDA;
 }
 
@@ -247,7 +271,7 @@ int ring_attn_bwd(const void* q, const void* k, const void* v, const void* o, co
   a.lse2 = reinterpret_cast<float*>(ws + w.lse2);
   a.Dvec = reinterpret_cast<float*>(ws + w.dvec);
   a.dq_acc = reinterpret_cast<float*>(ws + w.dq);
-  a.dq = dq; a.dk = dk; a.dv = dv; a.err = err;
+  a.dq = dq; a.dk = dk; a.dv = dv; a.err = err; a.timer = active_timer();
   return launch_bwd(a, stream) == cudaSuccess ? RING_ATTN_OK : RING_ATTN_ERR_CUDA;
 }
 
@@ -266,6 +290,32 @@ int ring_attn_device_status(cudaStream_t stream, int* site) {
   const int zero = 0;
   if (cudaMemcpy(p, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) return RING_ATTN_ERR_CUDA;
   return RING_ATTN_ERR_DEVICE_TIMEOUT;
+}
+
+int ring_attn_profile_enable(int on) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  g_timer.on = on != 0;
+  return RING_ATTN_OK;
+}
+
+int ring_attn_profile_read(double* ms, long long* launches) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  for (int k = 0; k < RING_ATTN_N_KERNELS; ++k) {
+    if (ms) ms[k] = 0.0;
+    if (launches) launches[k] = 0;
+  }
+  int rc = RING_ATTN_OK;
+  for (auto& r : g_timer.recs) {
+    float t = 0.f;
+    if (cudaEventSynchronize(r.stop) != cudaSuccess || cudaEventElapsedTime(&t, r.start, r.stop) != cudaSuccess)
+      rc = RING_ATTN_ERR_CUDA;
+    if (ms) ms[r.kind] += t;
+    if (launches) launches[r.kind] += 1;
+    cudaEventDestroy(r.start);
+    cudaEventDestroy(r.stop);
+  }
+  g_timer.recs.clear();
+  return rc;
 }
 
 void ring_attn_release(void) {
