@@ -78,6 +78,33 @@ int ring_attn_bwd(const void* q, const void* k, const void* v, const void* o, co
                   void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal,
                   void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * Size in bytes of the static device array ring_attn_bwd_noalloc works in
+ * (64 MiB per GPU that loads the library, held until the process exits).
+ */
+#define RING_ATTN_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+/*
+ * ring_attn_bwd without any device allocation.  The pages describe no such
+ * call; it serves callers that cannot call cudaMalloc: code whose device
+ * memory is owned by another allocator (a framework's caching pool, a fixed
+ * memory budget) and latency-critical code that cannot accept the device
+ * synchronisation cudaMalloc/cudaFree may cause.  Arguments and results are
+ * those of ring_attn_bwd minus the workspace: the statistics, the fp32 dq
+ * accumulator and the launch plan live in a static device array of
+ * RING_ATTN_NOALLOC_SCRATCH_BYTES.  A problem whose workspace
+ * (ring_attn_bwd_workspace_size) plus plan does not fit is rejected with
+ * RING_ATTN_ERR_WORKSPACE before anything is launched.  The first call on
+ * each device looks up the array's device address (cudaGetSymbolAddress);
+ * make that first call before any stream capture.  All calls share the one
+ * array and it keeps the last call's contents (each call rewrites what it
+ * needs): calls whose work may overlap on the GPU race and must be ordered
+ * by the caller, e.g. by issuing them on one stream.
+ */
+int ring_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                          const void* dO, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int L, int d,
+                          int n_chunks, int causal, cudaStream_t stream);
+
 /* Static description of a status code. */
 const char* ring_attn_strerror(int status);
 

@@ -18,6 +18,7 @@ from .capi import (  # noqa: F401
     profile_read,
     release,
     ring_attn_bwd,
+    ring_attn_bwd_noalloc,
     ring_attn_fwd,
     strerror,
 )

@@ -52,6 +52,8 @@ def load():
     lib.ring_attn_bwd_workspace_size.restype = S
     lib.ring_attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, S, P]
     lib.ring_attn_bwd.restype = I
+    lib.ring_attn_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P]
+    lib.ring_attn_bwd_noalloc.restype = I
     lib.ring_attn_strerror.argtypes = [I]
     lib.ring_attn_strerror.restype = ctypes.c_char_p
     lib.ring_attn_device_status.argtypes = [P, IP]
@@ -180,6 +182,26 @@ def ring_attn_bwd(q, k, v, o, lse, dO, n_chunks: int, causal: bool, dq=None, dk=
                               int(workspace.numel() * workspace.element_size()), _stream(stream))
     if rc != OK:
         raise RingAttnError(rc, "ring_attn_bwd")
+    return dq, dk, dv
+
+
+def ring_attn_bwd_noalloc(q, k, v, o, lse, dO, n_chunks: int, causal: bool, dq, dk, dv, stream=None):
+    """ring_attn_bwd for callers that cannot allocate device memory: the
+    library works in its own static device array (see include/ring_attn.h)
+    instead of a workspace.  dq, dk, dv must be passed in (allocated by the
+    caller's own means); returns them."""
+    import torch
+    B, Hq, L, d = q.shape
+    Hkv = k.shape[1]
+    for t, n, s in ((q, "q", (B, Hq, L, d)), (k, "k", (B, Hkv, L, d)), (v, "v", (B, Hkv, L, d)),
+                    (o, "o", (B, Hq, L, d)), (dO, "dO", (B, Hq, L, d)), (dq, "dq", (B, Hq, L, d)),
+                    (dk, "dk", (B, Hkv, L, d)), (dv, "dv", (B, Hkv, L, d))):
+        _check_tensor(t, n, torch.bfloat16, s)
+    _check_tensor(lse, "lse", torch.float32, (B, Hq, L))
+    rc = load().ring_attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk),
+                                      _ptr(dv), B, Hq, Hkv, L, d, int(n_chunks), int(bool(causal)), _stream(stream))
+    if rc != OK:
+        raise RingAttnError(rc, "ring_attn_bwd_noalloc")
     return dq, dk, dv
 
 

@@ -167,6 +167,16 @@ int plan_query(int kind, int L, int n_chunks, int causal, int* n_blocks, int* n_
 }
 
 }  // namespace
+
+// Device status word of the current device, for the library's other entry
+// points (ring_attn_noalloc.cu).
+int status_word_for_current_device(int** out) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  int dev;
+  if (current_device(&dev) != RING_ATTN_OK) return RING_ATTN_ERR_CUDA;
+  return status_ptr(dev, out);
+}
+
 }  // namespace ra
 
 using namespace ra;

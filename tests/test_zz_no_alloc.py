@@ -1,0 +1,68 @@
+"""ring_attn_bwd_noalloc: the backward pass for callers that cannot call
+cudaMalloc -- code whose device memory is owned by another allocator, or
+that cannot accept the device synchronisation cudaMalloc/cudaFree may cause.
+It works in the library's static device array instead of a workspace, so its
+gradients must equal those of ring_attn_bwd, call after call (the array
+keeps the previous call's contents, which must not leak into the next).
+
+This file is named to be collected last.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import sequence_blockwise_self_gb300 as ra
+from sequence_blockwise_self_gb300 import build as lib_build
+from sequence_blockwise_self_gb300 import capi
+from sequence_blockwise_self_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+TOL_MAX, TOL_MEAN = 2e-2, 2e-3  # the parity tolerance of the other GPU tests
+
+
+def _close(name, got, want):
+    err = (got.float() - want.float()).abs()
+    assert torch.isfinite(got.float()).all(), name
+    assert err.max().item() <= TOL_MAX and err.mean().item() <= TOL_MEAN, \
+        f"{name}: max-abs {err.max().item():.3e}, mean-abs {err.mean().item():.3e}"
+
+
+def test_noalloc_backward_matches_workspace_backward_on_two_calls_in_a_row():
+    lib_build.build()
+    lib = ra.load()
+    # (B, Hq, Hkv, L, d, n_chunks, causal): the second call has another shape,
+    # head size and mask, so stale statistics or plan from the first would show.
+    shapes = [(1, 4, 2, 1024, 128, 4, True), (2, 2, 2, 640, 64, 5, False)]
+    cases = []
+    for i, (B, Hq, Hkv, L, d, N, causal) in enumerate(shapes):
+        q, k, v, dO = (t.cuda() for t in inputs.make_inputs(B, Hq, Hkv, L, d, seed=500 + i))
+        o, lse = ra.ring_attn_fwd(q, k, v, N, causal)
+        ref = ra.ring_attn_bwd(q, k, v, o, lse, dO, N, causal)
+        out = (torch.full_like(q, float("nan")), torch.full_like(k, float("nan")), torch.full_like(v, float("nan")))
+        cases.append(((q, k, v, o, lse, dO, N, causal), ref, out))
+    torch.cuda.synchronize()
+    # the two calls of the allocation-free entry point, back to back
+    for args, _, (dq, dk, dv) in cases:
+        ra.ring_attn_bwd_noalloc(*args, dq, dk, dv)
+    torch.cuda.synchronize()
+    st, site = ra.device_status()
+    assert st == 0, f"device status {st} at {site:#x}"
+    for (_, (dq_r, dk_r, dv_r), (dq, dk, dv)) in cases:
+        _close("dq", dq, dq_r)
+        _close("dk", dk, dk_r)
+        _close("dv", dv, dv_r)
+
+    # a problem whose workspace does not fit the static array is refused
+    # before anything is touched or launched
+    fake = [ctypes.c_void_p(1 << 20)] * 9
+    B, Hq, L, d = 1, 32, 8192, 128
+    assert ra.bwd_workspace_size(B, Hq, Hq, L, d, 8, True) > capi_limit()
+    rc = lib.ring_attn_bwd_noalloc(*fake, B, Hq, Hq, L, d, 8, 1, ctypes.c_void_p(0))
+    assert rc == capi.ERR_WORKSPACE
+
+
+def capi_limit():
+    return 64 * 1024 * 1024
