@@ -12,8 +12,8 @@
 //   dQ_i += scale sum_j dS_ij k_j
 //
 // Three launches:
-//   bwd_pre   per row: D_i, lse_i in log2 units (padded rows get +inf, so
-//             their probabilities are 0), and zero the fp32 dQ accumulator.
+//   bwd_pre   per row: -D_i and -lse_i in log2 units (padded rows get -inf,
+//             so their probabilities are 0), and zero the fp32 dQ accumulator.
 //   bwd_main  one CTA per (key/value tile, batch, kv head).  K_j and V_j
 //             stay in shared memory; the CTA loops over the query heads of
 //             the group and over the query tiles that see the tile, in the
@@ -230,9 +230,13 @@ __device__ void bwd_compute(BwdSmem<D>& sm, uint32_t tmem, const BwdDev& p, cons
   const uint32_t t_dv = tmem + 256 + lane_off, t_dk = tmem + 256 + D + lane_off;
   const uint32_t t_dq = ((D == 128) ? tmem : tmem + 384) + lane_off;
   const uint32_t pa = smem_u32(sm.pT), sa = smem_u32(sm.dsT);
-  const uint32_t stage = pa + wq * 8192;  // two 4 KB fp32 staging boxes per warp
+  // The dQ drain stages fp32 boxes (32 rows x 128 B) in the P^T buffer, in
+  // exactly the bytes this warp's rows of P^T occupy (rows 32wq.. of both
+  // 64-column halves), so only this warp's own copies must have been read
+  // before it writes P^T again.
+  const uint32_t stage0 = pa + wq * 4096, stage1 = pa + 16384 + wq * 4096;
   const int G = p.Hq / p.Hkv;
-  const float c = p.scale_log2;
+  const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
   bool ok = true;
   uint32_t i = 0;
   for (QIter qi(rg, nr, G); qi.valid() && ok; qi.next(), ++i) {
@@ -243,24 +247,42 @@ __device__ void bwd_compute(BwdSmem<D>& sm, uint32_t tmem, const BwdDev& p, cons
     tc_fence_after();
     const int q0 = qi.it * 128;
     // Probabilities are zero where the key is after the query (causal) or
-    // past the end; padded query rows have lse2 = +inf, hence P = 0.
+    // past the end; padded query rows have -lse2 = -inf, hence P = 0.
     const int first_valid_q = p.causal ? kv_pos - q0 : 0;  // local query index
     const bool row_dead = kv_pos >= p.L;
-    const float* lse2 = sm.lse2[slot];
-    const float* dvec = sm.dvec[slot];
-#pragma unroll
-    for (int c0 = 0; c0 < 4; ++c0) {
-      uint32_t rs[32], rp[32];
-      tmem_ld32(t_s + c0 * 32, rs);
-      tmem_ld32(t_dp + c0 * 32, rp);
+    const bool need_mask = row_dead || first_valid_q > 0;
+    const float* nlse2 = sm.lse2[slot];  // -lse * log2(e)
+    const float* ndvec = sm.dvec[slot];  // -D
+    // the previous dQ drain copies must have finished reading this warp's rows
+    if (lane == 0) bulk_wait_group_read<0>();
+    __syncwarp();
+
+    auto process = [&](int c0, uint32_t (&rs)[32], uint32_t (&rp)[32]) {
       float pv[32], ds[32];
 #pragma unroll
-      for (int x = 0; x < 32; ++x) {
+      for (int x = 0; x < 32; x += 4) {
         const int qq = c0 * 32 + x;
-        float pr = ex2(fmaf(__uint_as_float(rs[x]), c, -lse2[qq]));
-        if (row_dead || qq < first_valid_q) pr = 0.f;
-        pv[x] = pr;
-        ds[x] = pr * (__uint_as_float(rp[x]) - dvec[qq]);
+        const float4 nl = *reinterpret_cast<const float4*>(nlse2 + qq);
+        const float4 nd = *reinterpret_cast<const float4*>(ndvec + qq);
+        const float2 a0 = __ffma2_rn(make_float2(__uint_as_float(rs[x]), __uint_as_float(rs[x + 1])), c2,
+                                     make_float2(nl.x, nl.y));
+        const float2 a1 = __ffma2_rn(make_float2(__uint_as_float(rs[x + 2]), __uint_as_float(rs[x + 3])), c2,
+                                     make_float2(nl.z, nl.w));
+        float2 p0 = make_float2(ex2(a0.x), ex2(a0.y));
+        float2 p1 = make_float2(ex2(a1.x), ex2(a1.y));
+        if (need_mask) {
+          if (row_dead || qq < first_valid_q) p0.x = 0.f;
+          if (row_dead || qq + 1 < first_valid_q) p0.y = 0.f;
+          if (row_dead || qq + 2 < first_valid_q) p1.x = 0.f;
+          if (row_dead || qq + 3 < first_valid_q) p1.y = 0.f;
+        }
+        const float2 d0 = __fadd2_rn(make_float2(__uint_as_float(rp[x]), __uint_as_float(rp[x + 1])),
+                                     make_float2(nd.x, nd.y));
+        const float2 d1 = __fadd2_rn(make_float2(__uint_as_float(rp[x + 2]), __uint_as_float(rp[x + 3])),
+                                     make_float2(nd.z, nd.w));
+        const float2 s0 = __fmul2_rn(p0, d0), s1 = __fmul2_rn(p1, d1);
+        pv[x] = p0.x; pv[x + 1] = p0.y; pv[x + 2] = p1.x; pv[x + 3] = p1.y;
+        ds[x] = s0.x; ds[x + 1] = s0.y; ds[x + 2] = s1.x; ds[x + 3] = s1.y;
       }
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
@@ -271,24 +293,63 @@ __device__ void bwd_compute(BwdSmem<D>& sm, uint32_t tmem, const BwdDev& p, cons
         st_shared_v4(sa + off, pack_bf16(ds[q4 * 8], ds[q4 * 8 + 1]), pack_bf16(ds[q4 * 8 + 2], ds[q4 * 8 + 3]),
                      pack_bf16(ds[q4 * 8 + 4], ds[q4 * 8 + 5]), pack_bf16(ds[q4 * 8 + 6], ds[q4 * 8 + 7]));
       }
+    };
+    // S^T / dP^T columns in four chunks of 32, loads double-buffered so the
+    // next chunk's tensor-memory latency hides behind this chunk's math.
+    {
+      uint32_t sA[32], pA[32], sB[32], pB[32];
+      tmem_ld32_async(t_s, sA);
+      tmem_ld32_async(t_dp, pA);
+      tmem_wait_ld(sA);
+      reg_fence(pA);
+      tmem_ld32_async(t_s + 32, sB);
+      tmem_ld32_async(t_dp + 32, pB);
+      process(0, sA, pA);
+      tmem_wait_ld(sB);
+      reg_fence(pB);
+      tmem_ld32_async(t_s + 64, sA);
+      tmem_ld32_async(t_dp + 64, pA);
+      process(1, sB, pB);
+      tmem_wait_ld(sA);
+      reg_fence(pA);
+      tmem_ld32_async(t_s + 96, sB);
+      tmem_ld32_async(t_dp + 96, pB);
+      process(2, sA, pA);
+      tmem_wait_ld(sB);
+      reg_fence(pB);
+      process(3, sB, pB);
     }
     fence_proxy_async_smem();
     tc_fence_before();
     mbar_arrive(smem_u32(&sm.ds_full));
-    // dQ drain: rows of dQ (query rows) -> fp32 staging -> TMA reduce-add.
+    // dQ drain: this thread's dQ row (a query row) leaves tensor memory in
+    // one batched load; the columns are released at once, then the row goes
+    // through fp32 staging boxes into the global accumulator (TMA reduce-add).
     ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.dq_full), i & 1, ab, err, kSiteBwdSoftmax));
     if (!ok) break;
     tc_fence_after();
     const int q_z = b * p.Hq + g * G + qi.hh;
-#pragma unroll
-    for (int c0 = 0; c0 < D / 32; ++c0) {
-      const uint32_t box = stage + (c0 & 1) * 4096;
+    uint32_t d0[32], d1[32], d2[32], d3[32];
+    tmem_ld32_async(t_dq, d0);
+    tmem_ld32_async(t_dq + 32, d1);
+    if (D == 128) {
+      tmem_ld32_async(t_dq + 64, d2);
+      tmem_ld32_async(t_dq + 96, d3);
+    }
+    tmem_wait_ld(d0);
+    reg_fence(d1);
+    if (D == 128) {
+      reg_fence(d2);
+      reg_fence(d3);
+    }
+    tc_fence_before();
+    mbar_arrive(smem_u32(&sm.dq_free));
+    auto stage = [&](int c0, const uint32_t (&r)[32]) {
+      const uint32_t box = (c0 & 1) ? stage1 : stage0;
       if (c0 >= 2) {
         if (lane == 0) bulk_wait_group_read<1>();
         __syncwarp();
       }
-      uint32_t r[32];
-      tmem_ld32(t_dq + c0 * 32, r);
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch)
         st_shared_v4(box + sw128_offset(lane, ch), r[ch * 4], r[ch * 4 + 1], r[ch * 4 + 2], r[ch * 4 + 3]);
@@ -298,11 +359,13 @@ __device__ void bwd_compute(BwdSmem<D>& sm, uint32_t tmem, const BwdDev& p, cons
         tma_reduce_add_3d(tm_dqacc, box, c0 * 32, q0 + wq * 32, q_z);
         bulk_commit_group();
       }
+    };
+    stage(0, d0);
+    stage(1, d1);
+    if (D == 128) {
+      stage(2, d2);
+      stage(3, d3);
     }
-    if (lane == 0) bulk_wait_group_read<0>();
-    __syncwarp();
-    tc_fence_before();
-    mbar_arrive(smem_u32(&sm.dq_free));
   }
   if (lane == 0) bulk_wait_group<0>();
   if (ok) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.kv_final), 0, ab, err, kSiteBwdEpilogue));
@@ -407,8 +470,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (warp == 2) tmem_dealloc(tmem, 512);
 }
 
-// One warp per row: D_i = sum_c dO_ic o_ic, lse2_i = lse_i log2(e) (or +inf
-// / 0 for padded rows), and zero the row of the fp32 dQ accumulator.
+// One warp per row: stores -D_i = -sum_c dO_ic o_ic and -lse_i log2(e) (0 and
+// -inf for padded rows, whose probabilities are then 0), and zeroes the row
+// of the fp32 dQ accumulator.
 template <int D>
 __global__ void __launch_bounds__(256) ring_attn_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
                                                                 const __nv_bfloat16* __restrict__ dO,
@@ -446,8 +510,8 @@ __global__ void __launch_bounds__(256) ring_attn_bwd_pre_kernel(const __nv_bfloa
 #pragma unroll
   for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
   if (lane == 0) {
-    dvec[r] = (i < L) ? acc : 0.f;
-    lse2[r] = (i < L) ? lse[static_cast<size_t>(bh) * L + i] * kLog2e : INFINITY;
+    dvec[r] = (i < L) ? -acc : 0.f;
+    lse2[r] = (i < L) ? -lse[static_cast<size_t>(bh) * L + i] * kLog2e : -INFINITY;
   }
   float4* z = reinterpret_cast<float4*>(dq_acc + static_cast<size_t>(r) * D);
 #pragma unroll

@@ -216,13 +216,23 @@ __device__ void fwd_softmax(FwdSmem<D>& sm, uint32_t tmem, int t, const FwdDev& 
       ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.s_full[t]), j & 1, ab, err, kSiteFwdSoftmax));
       if (!ok) break;
       tc_fence_after();
+      // one batched load of the 128 scores of this row, one wait
+      uint32_t r0[32], r1[32], r2[32], r3[32];
+      tmem_ld32_async(t_s, r0);
+      tmem_ld32_async(t_s + 32, r1);
+      tmem_ld32_async(t_s + 64, r2);
+      tmem_ld32_async(t_s + 96, r3);
+      tmem_wait_ld(r0);
+      reg_fence(r1);
+      reg_fence(r2);
+      reg_fence(r3);
       float s[128];
 #pragma unroll
-      for (int c0 = 0; c0 < 4; ++c0) {
-        uint32_t r[32];
-        tmem_ld32(t_s + c0 * 32, r);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[c0 * 32 + i] = __uint_as_float(r[i]);
+      for (int i = 0; i < 32; ++i) {
+        s[i] = __uint_as_float(r0[i]);
+        s[32 + i] = __uint_as_float(r1[i]);
+        s[64 + i] = __uint_as_float(r2[i]);
+        s[96 + i] = __uint_as_float(r3[i]);
       }
       const int kv0 = jt * 128;
       if (kv0 + 128 > p.L || (p.causal && kv0 + 127 > qpos)) {
@@ -231,14 +241,52 @@ __device__ void fwd_softmax(FwdSmem<D>& sm, uint32_t tmem, int t, const FwdDev& 
         for (int i = 0; i < 128; ++i)
           if (i > lim) s[i] = -INFINITY;
       }
-      float mx = s[0];
+      // four independent max3 chains over s[0..127]: 4 seeds + 15 groups of 8 + 4
+      float m0 = s[0], m1 = s[1], m2 = s[2], m3 = s[3];
 #pragma unroll
-      for (int i = 1; i < 128; ++i) mx = fmaxf(mx, s[i]);
+      for (int i = 4; i < 124; i += 8) {
+        m0 = max3f(m0, s[i], s[i + 1]);
+        m1 = max3f(m1, s[i + 2], s[i + 3]);
+        m2 = max3f(m2, s[i + 4], s[i + 5]);
+        m3 = max3f(m3, s[i + 6], s[i + 7]);
+      }
+      m0 = max3f(m0, s[124], s[125]);
+      m1 = max3f(m1, s[126], s[127]);
+      const float mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
       const float m_new = fmaxf(m, mx * c);
       const bool resc = m_new > m + kRescaleThreshold;
+      const float m_old = m;
+      if (resc) {
+        l *= ex2(m - m_new);
+        m = m_new;
+      }
+      const float ms = (m == -INFINITY) ? 0.f : m;
+      const float2 c2 = make_float2(c, c), nm2 = make_float2(-ms, -ms);
+      float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int i = 0; i < 128; i += 4) {
+        const float2 x0 = __ffma2_rn(make_float2(s[i], s[i + 1]), c2, nm2);
+        const float2 x1 = __ffma2_rn(make_float2(s[i + 2], s[i + 3]), c2, nm2);
+        s[i] = ex2(x0.x);
+        s[i + 1] = ex2(x0.y);
+        s[i + 2] = ex2(x1.x);
+        s[i + 3] = ex2(x1.y);
+        acc0 = __fadd2_rn(acc0, make_float2(s[i], s[i + 1]));
+        acc1 = __fadd2_rn(acc1, make_float2(s[i + 2], s[i + 3]));
+      }
+      l += (acc0.x + acc0.y) + (acc1.x + acc1.y);
+#pragma unroll
+      for (int ch = 0; ch < 16; ++ch) {
+        st_shared_v4(pbase + (ch >> 3) * 16384 + sw128_offset(row, ch & 7), pack_bf16(s[ch * 8], s[ch * 8 + 1]),
+                     pack_bf16(s[ch * 8 + 2], s[ch * 8 + 3]), pack_bf16(s[ch * 8 + 4], s[ch * 8 + 5]),
+                     pack_bf16(s[ch * 8 + 6], s[ch * 8 + 7]));
+      }
+      // Rare: the row maximum grew by more than the threshold, so the O_t
+      // accumulated so far is rescaled to the new reference.  O_t is
+      // quiescent here (the commit that signalled S_t(j) covers PV_t(j-1)),
+      // and PV_t(j) is only issued after this thread arrives on p_full.
       if (j > 0 && __any_sync(0xffffffffu, resc)) {
-        // O_t is quiescent: the commit that signalled S_t(j) covers PV_t(j-1).
-        const float f = resc ? ex2(m - m_new) : 1.f;
+        const float f = resc ? ex2(m_old - m) : 1.f;
 #pragma unroll
         for (int c0 = 0; c0 < D / 32; ++c0) {
           uint32_t r[32];
@@ -247,24 +295,6 @@ __device__ void fwd_softmax(FwdSmem<D>& sm, uint32_t tmem, int t, const FwdDev& 
           for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * f);
           tmem_st32(t_o + c0 * 32, r);
         }
-      }
-      if (resc) {
-        l *= ex2(m - m_new);
-        m = m_new;
-      }
-      const float ms = (m == -INFINITY) ? 0.f : m;
-      float rs = 0.f;
-#pragma unroll
-      for (int i = 0; i < 128; ++i) {
-        s[i] = ex2(fmaf(s[i], c, -ms));
-        rs += s[i];
-      }
-      l += rs;
-#pragma unroll
-      for (int ch = 0; ch < 16; ++ch) {
-        st_shared_v4(pbase + (ch >> 3) * 16384 + sw128_offset(row, ch & 7), pack_bf16(s[ch * 8], s[ch * 8 + 1]),
-                     pack_bf16(s[ch * 8 + 2], s[ch * 8 + 3]), pack_bf16(s[ch * 8 + 4], s[ch * 8 + 5]),
-                     pack_bf16(s[ch * 8 + 6], s[ch * 8 + 7]));
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -277,10 +307,7 @@ __device__ void fwd_softmax(FwdSmem<D>& sm, uint32_t tmem, int t, const FwdDev& 
     const float inv = l > 0.f ? 1.f / l : 0.f;
     // Normalised O row -> bf16 -> the P buffer (free: the last PV_t is done),
     // laid out as the 128-byte-swizzled boxes of the output tensor map.
-#pragma unroll
-    for (int c0 = 0; c0 < D / 32; ++c0) {
-      uint32_t r[32];
-      tmem_ld32(t_o + c0 * 32, r);
+    auto emit = [&](int c0, const uint32_t (&r)[32]) {
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
         const int ch = c0 * 4 + q4;
@@ -289,6 +316,24 @@ __device__ void fwd_softmax(FwdSmem<D>& sm, uint32_t tmem, int t, const FwdDev& 
                      pack_bf16(f[2] * inv, f[3] * inv), pack_bf16(f[4] * inv, f[5] * inv),
                      pack_bf16(f[6] * inv, f[7] * inv));
       }
+    };
+    {
+      uint32_t r0[32], r1[32];
+      tmem_ld32_async(t_o, r0);
+      tmem_ld32_async(t_o + 32, r1);
+      tmem_wait_ld(r0);
+      reg_fence(r1);
+      emit(0, r0);
+      emit(1, r1);
+    }
+    if (D == 128) {
+      uint32_t r2[32], r3[32];
+      tmem_ld32_async(t_o + 64, r2);
+      tmem_ld32_async(t_o + 96, r3);
+      tmem_wait_ld(r2);
+      reg_fence(r3);
+      emit(2, r2);
+      emit(3, r3);
     }
     if (qpos < p.L) p.lse[static_cast<size_t>(q_z) * p.L + qpos] = (m + log2f(l)) * kLn2;
     fence_proxy_async_smem();

@@ -50,8 +50,8 @@ struct BwdArgs {
   const void* o;            // bf16 [B*Hq*L*d]
   const void* dO;           // bf16 [B*Hq*L*d]
   const float* lse;         // fp32 [B*Hq*L]
-  float* lse2;              // workspace fp32 [B*Hq*Lpad]: lse * log2(e), +inf padding
-  float* Dvec;              // workspace fp32 [B*Hq*Lpad]: rowsum(dO * o), 0 padding
+  float* lse2;              // workspace fp32 [B*Hq*Lpad]: -lse * log2(e), -inf padding
+  float* Dvec;              // workspace fp32 [B*Hq*Lpad]: -rowsum(dO * o), 0 padding
   float* dq_acc;            // workspace fp32 [B*Hq*Lpad*d]
   void* dq;                 // bf16 [B*Hq*L*d]
   void* dk;                 // bf16 [B*Hkv*L*d]
