@@ -22,16 +22,27 @@
 //               S^T  = K Q^T      (TMEM)      dP^T = V dO^T   (TMEM)
 //               dV  += P^T dO     (TMEM)      dK  += dS^T Q   (TMEM)
 //               dQ   = dS K       (TMEM, then TMA reduce-add into fp32)
-//             P^T and dS^T (bf16) go through shared memory.
+//             P^T (bf16) goes to tensor memory, packed over dP^T columns
+//             already read, and feeds dV as the A operand; dS^T (bf16) goes
+//             to shared memory (A operand of dK, MN-major A operand of dQ).
 //   bwd_post  dq = bf16(scale * dQ_acc).
 //
-// Warp roles of bwd_main (256 threads): warp 0 TMA producer, warp 1
-// tcgen05 issuer, warp 2 TMEM allocator, warps 4-7 one thread per key row:
-// probabilities, dS, the dQ drain, and the dK/dV epilogue.
+// Warp roles of bwd_main (384 threads): warp 0 TMA producer, warp 1
+// tcgen05 issuer, warp 2 TMEM allocator, warps 4-11 two compute warpgroups.
+// Both warpgroups work on the same 128 key rows (one thread per row = TMEM
+// lane); warpgroup h takes query columns [64h, 64h+64) of S^T / dP^T,
+// dQ columns [h d/2, (h+1) d/2) in the drain, and dV (h = 0) or dK (h = 1)
+// in the epilogue.
 //
 // Tensor memory (fp32 columns): S^T [0,128) dP^T [128,256) dV [256,256+d)
 // dK [256+d, 256+2d); dQ at [384,448) for d = 64, and over S^T for d = 128
-// (S^T has been read by then; the next S^T waits for the dQ drain).
+// (S^T has been read by then; the next S^T waits for the dQ drain).  Packed
+// P^T of warpgroup h occupies [128+64h, 128+64h+32).
+//
+// Buffers: K, V stationary; Q (with its rows' lse and D) and dO double
+// buffered; dS^T single.  The dQ drain stages fp32 boxes in the bytes of
+// dS^T that the draining warp itself writes, so it only waits for its own
+// copies before writing dS^T again.
 #include <cfloat>
 
 #include "kernels.h"
@@ -41,7 +52,7 @@ namespace ra {
 
 namespace {
 
-constexpr int kBwdThreads = 256;
+constexpr int kBwdThreads = 384;
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
@@ -51,16 +62,15 @@ struct BwdSmem {
   alignas(1024) uint8_t k[kTile];
   alignas(1024) uint8_t v[kTile];
   alignas(1024) uint8_t q[2][kTile];
-  alignas(1024) uint8_t dO[kTile];
-  alignas(1024) uint8_t pT[128 * 128 * 2];   // also the fp32 staging of the dQ drain
-  alignas(1024) uint8_t dsT[128 * 128 * 2];
+  alignas(1024) uint8_t dO[2][kTile];
+  alignas(1024) uint8_t dsT[128 * 128 * 2];  // also the fp32 staging of the dQ drain
   alignas(16) float lse2[2][128];
   alignas(16) float dvec[2][128];
   alignas(8) uint64_t kv_full;
   alignas(8) uint64_t q_full[2];
   alignas(8) uint64_t q_empty[2];
-  alignas(8) uint64_t do_full;
-  alignas(8) uint64_t do_empty;
+  alignas(8) uint64_t do_full[2];
+  alignas(8) uint64_t do_empty[2];
   alignas(8) uint64_t s_full;
   alignas(8) uint64_t ds_full;
   alignas(8) uint64_t dq_full;
@@ -134,12 +144,12 @@ __device__ void bwd_producer(BwdSmem<D>& sm, const CUtensorMap* tm_q, const CUte
     bulk_load_1d(smem_u32(sm.lse2[slot]), p.lse2 + roff, 512, qb);
     bulk_load_1d(smem_u32(sm.dvec[slot]), p.dvec + roff, 512, qb);
     ++nq;
-    if (i >= 1) ok = mbar_wait(smem_u32(&sm.do_empty), (i - 1) & 1, ab, err, kSiteBwdProducer);
+    if (i >= 2) ok = mbar_wait(smem_u32(&sm.do_empty[slot]), ((i >> 1) - 1) & 1, ab, err, kSiteBwdProducer);
     if (!ok) break;
-    const uint32_t db = smem_u32(&sm.do_full);
+    const uint32_t db = smem_u32(&sm.do_full[slot]);
     mbar_arrive_expect_tx(db, S::kTile);
     for (int sub = 0; sub < S::kSub; ++sub)
-      tma_load_3d(smem_u32(sm.dO) + sub * 16384, tm_do, db, sub * 64, qi.it * 128, q_z);
+      tma_load_3d(smem_u32(sm.dO[slot]) + sub * 16384, tm_do, db, sub * 64, qi.it * 128, q_z);
     ++ndo;
   }
   if (!ok) {
@@ -149,7 +159,10 @@ __device__ void bwd_producer(BwdSmem<D>& sm, const CUtensorMap* tm_q, const CUte
       const uint32_t last = s + 2 * ((nq - 1 - s) / 2);
       wait_drain(smem_u32(&sm.q_full[s]), (last >> 1) & 1, err);
     }
-    if (ndo > 0) wait_drain(smem_u32(&sm.do_full), (ndo - 1) & 1, err);
+    for (uint32_t s = 0; s < 2 && s < ndo; ++s) {
+      const uint32_t last = s + 2 * ((ndo - 1 - s) / 2);
+      wait_drain(smem_u32(&sm.do_full[s]), (last >> 1) & 1, err);
+    }
   }
 }
 
@@ -160,19 +173,20 @@ __device__ void bwd_mma(BwdSmem<D>& sm, uint32_t tmem, uint32_t n_total, volatil
   constexpr uint32_t kIdQ = idesc_bf16(128, D, true, true);
   const uint32_t t_s = tmem, t_dp = tmem + 128, t_dv = tmem + 256, t_dk = tmem + 256 + D;
   const uint32_t t_dq = (D == 128) ? tmem : tmem + 384;
-  const uint32_t ka = smem_u32(sm.k), va = smem_u32(sm.v), da = smem_u32(sm.dO);
-  const uint32_t pa = smem_u32(sm.pT), sa = smem_u32(sm.dsT);
+  const uint32_t ka = smem_u32(sm.k), va = smem_u32(sm.v), sa = smem_u32(sm.dsT);
 
   bool ok = mbar_wait(smem_u32(&sm.kv_full), 0, ab, err, kSiteBwdMma);
   for (uint32_t i = 0; i < n_total && ok; ++i) {
     const uint32_t slot = i & 1;
-    const uint32_t qa = smem_u32(sm.q[slot]);
+    const uint32_t qa = smem_u32(sm.q[slot]), da = smem_u32(sm.dO[slot]);
     ok = mbar_wait(smem_u32(&sm.q_full[slot]), (i >> 1) & 1, ab, err, kSiteBwdMma) &&
-         mbar_wait(smem_u32(&sm.do_full), i & 1, ab, err, kSiteBwdMma) &&
+         mbar_wait(smem_u32(&sm.do_full[slot]), (i >> 1) & 1, ab, err, kSiteBwdMma) &&
          (i == 0 || mbar_wait(smem_u32(&sm.dq_free), (i - 1) & 1, ab, err, kSiteBwdMma));
     if (!ok) break;
     tc_fence_after();
-    // S^T = K Q^T and dP^T = V dO^T (both operands K-major)
+    // S^T = K Q^T and dP^T = V dO^T (both operands K-major).  dP^T overwrites
+    // the packed P^T of the previous tile: dV(i-1) finished before dQ(i-1),
+    // whose drain released dq_free.
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -187,14 +201,13 @@ __device__ void bwd_mma(BwdSmem<D>& sm, uint32_t tmem, uint32_t n_total, volatil
     ok = mbar_wait(smem_u32(&sm.ds_full), i & 1, ab, err, kSiteBwdMma);
     if (!ok) break;
     tc_fence_after();
-    // dV += P^T dO : A = P^T (K-major over queries), B = dO (MN-major)
+    // dV += P^T dO : A = packed P^T in tensor memory (query k-step kk lives
+    // in warpgroup kk/4's columns), B = dO (MN-major)
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-      umma_ss(t_dv, sdesc_sw128(pa + off, 16, 1024), sdesc_sw128(da + kk * 2048, 16384, 1024), kIdKV,
+    for (int kk = 0; kk < 8; ++kk)
+      umma_ts(t_dv, tmem + 128 + 64 * (kk >> 2) + 8 * (kk & 3), sdesc_sw128(da + kk * 2048, 16384, 1024), kIdKV,
               (i > 0 || kk > 0) ? 1u : 0u);
-    }
-    if (i + 1 < n_total) umma_commit(smem_u32(&sm.do_empty));
+    if (i + 2 < n_total) umma_commit(smem_u32(&sm.do_empty[slot]));
     // dK += dS^T Q : A = dS^T (K-major), B = Q (MN-major)
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
@@ -221,20 +234,19 @@ __device__ void bwd_mma(BwdSmem<D>& sm, uint32_t tmem, uint32_t n_total, volatil
 template <int D>
 __device__ void bwd_compute(BwdSmem<D>& sm, uint32_t tmem, const BwdDev& p, const CUtensorMap* tm_dqacc, int b,
                             int g, int kv_tile, const int32_t* rg, int nr, volatile int* ab, int* err) {
-  const int wq = (threadIdx.x >> 5) & 3;
+  const int wg = ((threadIdx.x >> 5) - 4) >> 2;  // 0 or 1: which half of the query columns
+  const int wq = (threadIdx.x >> 5) & 3;         // TMEM lane quadrant
   const int lane = threadIdx.x & 31;
   const int row = wq * 32 + lane;  // key row (S^T lane) and also dQ query row
   const int kv_pos = kv_tile * 128 + row;
   const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-  const uint32_t t_s = tmem + lane_off, t_dp = tmem + 128 + lane_off;
-  const uint32_t t_dv = tmem + 256 + lane_off, t_dk = tmem + 256 + D + lane_off;
-  const uint32_t t_dq = ((D == 128) ? tmem : tmem + 384) + lane_off;
-  const uint32_t pa = smem_u32(sm.pT), sa = smem_u32(sm.dsT);
-  // The dQ drain stages fp32 boxes (32 rows x 128 B) in the P^T buffer, in
-  // exactly the bytes this warp's rows of P^T occupy (rows 32wq.. of both
-  // 64-column halves), so only this warp's own copies must have been read
-  // before it writes P^T again.
-  const uint32_t stage0 = pa + wq * 4096, stage1 = pa + 16384 + wq * 4096;
+  const uint32_t t_s = tmem + 64 * wg + lane_off;          // this half's S^T columns
+  const uint32_t t_dp = tmem + 128 + 64 * wg + lane_off;   // this half's dP^T columns
+  const uint32_t t_p = t_dp;                               // packed P^T over the first 32 of them
+  const uint32_t t_dq = ((D == 128) ? tmem : tmem + 384) + (D / 2) * wg + lane_off;
+  const uint32_t sa = smem_u32(sm.dsT);
+  // this warp's rows of dS^T (query half wg = sub-tile wg): its staging box
+  const uint32_t stage = sa + wg * 16384 + wq * 4096;
   const int G = p.Hq / p.Hkv;
   const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
   bool ok = true;
@@ -250,18 +262,19 @@ __device__ void bwd_compute(BwdSmem<D>& sm, uint32_t tmem, const BwdDev& p, cons
     // past the end; padded query rows have -lse2 = -inf, hence P = 0.
     const int first_valid_q = p.causal ? kv_pos - q0 : 0;  // local query index
     const bool row_dead = kv_pos >= p.L;
-    const bool need_mask = row_dead || first_valid_q > 0;
+    const bool need_mask = row_dead || first_valid_q > 64 * wg;
     const float* nlse2 = sm.lse2[slot];  // -lse * log2(e)
     const float* ndvec = sm.dvec[slot];  // -D
     // the previous dQ drain copies must have finished reading this warp's rows
     if (lane == 0) bulk_wait_group_read<0>();
     __syncwarp();
 
-    auto process = [&](int c0, uint32_t (&rs)[32], uint32_t (&rp)[32]) {
-      float pv[32], ds[32];
+    // 16 query columns: P^T packed into tensor memory, dS^T into shared memory
+    auto process = [&](int c, uint32_t (&rs)[16], uint32_t (&rp)[16]) {
+      uint32_t pk[8], dk8[8];
 #pragma unroll
-      for (int x = 0; x < 32; x += 4) {
-        const int qq = c0 * 32 + x;
+      for (int x = 0; x < 16; x += 4) {
+        const int qq = 64 * wg + 16 * c + x;
         const float4 nl = *reinterpret_cast<const float4*>(nlse2 + qq);
         const float4 nd = *reinterpret_cast<const float4*>(ndvec + qq);
         const float2 a0 = __ffma2_rn(make_float2(__uint_as_float(rs[x]), __uint_as_float(rs[x + 1])), c2,
@@ -281,119 +294,102 @@ __device__ void bwd_compute(BwdSmem<D>& sm, uint32_t tmem, const BwdDev& p, cons
         const float2 d1 = __fadd2_rn(make_float2(__uint_as_float(rp[x + 2]), __uint_as_float(rp[x + 3])),
                                      make_float2(nd.z, nd.w));
         const float2 s0 = __fmul2_rn(p0, d0), s1 = __fmul2_rn(p1, d1);
-        pv[x] = p0.x; pv[x + 1] = p0.y; pv[x + 2] = p1.x; pv[x + 3] = p1.y;
-        ds[x] = s0.x; ds[x + 1] = s0.y; ds[x + 2] = s1.x; ds[x + 3] = s1.y;
+        pk[x / 2] = pack_bf16(p0.x, p0.y);
+        pk[x / 2 + 1] = pack_bf16(p1.x, p1.y);
+        dk8[x / 2] = pack_bf16(s0.x, s0.y);
+        dk8[x / 2 + 1] = pack_bf16(s1.x, s1.y);
       }
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const int ch = c0 * 4 + q4;
-        const uint32_t off = (ch >> 3) * 16384 + sw128_offset(row, ch & 7);
-        st_shared_v4(pa + off, pack_bf16(pv[q4 * 8], pv[q4 * 8 + 1]), pack_bf16(pv[q4 * 8 + 2], pv[q4 * 8 + 3]),
-                     pack_bf16(pv[q4 * 8 + 4], pv[q4 * 8 + 5]), pack_bf16(pv[q4 * 8 + 6], pv[q4 * 8 + 7]));
-        st_shared_v4(sa + off, pack_bf16(ds[q4 * 8], ds[q4 * 8 + 1]), pack_bf16(ds[q4 * 8 + 2], ds[q4 * 8 + 3]),
-                     pack_bf16(ds[q4 * 8 + 4], ds[q4 * 8 + 5]), pack_bf16(ds[q4 * 8 + 6], ds[q4 * 8 + 7]));
-      }
+      // packed columns 8c..8c+7 of this half lie in dP^T columns 0..31 of the
+      // half, all read in chunks 0 and 1 (c <= 1 when c's own columns are
+      // written over, c's pending successor reads columns >= 16(c+1))
+      tmem_st8_async(t_p + 8 * c, pk);
+      const int ch = 2 * c;  // 16-byte chunk (8 queries) within the half's 128-byte row
+      st_shared_v4(sa + wg * 16384 + sw128_offset(row, ch), dk8[0], dk8[1], dk8[2], dk8[3]);
+      st_shared_v4(sa + wg * 16384 + sw128_offset(row, ch + 1), dk8[4], dk8[5], dk8[6], dk8[7]);
     };
-    // S^T / dP^T columns in four chunks of 32, loads double-buffered so the
-    // next chunk's tensor-memory latency hides behind this chunk's math.
     {
-      uint32_t sA[32], pA[32], sB[32], pB[32];
-      tmem_ld32_async(t_s, sA);
-      tmem_ld32_async(t_dp, pA);
+      uint32_t sA[16], pA[16], sB[16], pB[16];
+      tmem_ld16_async(t_s, sA);
+      tmem_ld16_async(t_dp, pA);
       tmem_wait_ld(sA);
       reg_fence(pA);
-      tmem_ld32_async(t_s + 32, sB);
-      tmem_ld32_async(t_dp + 32, pB);
+      tmem_ld16_async(t_s + 16, sB);
+      tmem_ld16_async(t_dp + 16, pB);
       process(0, sA, pA);
       tmem_wait_ld(sB);
       reg_fence(pB);
-      tmem_ld32_async(t_s + 64, sA);
-      tmem_ld32_async(t_dp + 64, pA);
+      tmem_ld16_async(t_s + 32, sA);
+      tmem_ld16_async(t_dp + 32, pA);
       process(1, sB, pB);
       tmem_wait_ld(sA);
       reg_fence(pA);
-      tmem_ld32_async(t_s + 96, sB);
-      tmem_ld32_async(t_dp + 96, pB);
+      tmem_ld16_async(t_s + 48, sB);
+      tmem_ld16_async(t_dp + 48, pB);
       process(2, sA, pA);
       tmem_wait_ld(sB);
       reg_fence(pB);
       process(3, sB, pB);
     }
+    tmem_wait_st();
     fence_proxy_async_smem();
     tc_fence_before();
     mbar_arrive(smem_u32(&sm.ds_full));
-    // dQ drain: this thread's dQ row (a query row) leaves tensor memory in
-    // one batched load; the columns are released at once, then the row goes
-    // through fp32 staging boxes into the global accumulator (TMA reduce-add).
+    // dQ drain: this thread's dQ row (a query row), this half's columns,
+    // leaves tensor memory in one batched load; the columns are released at
+    // once, then the row goes through an fp32 staging box into the global
+    // accumulator (TMA reduce-add).
     ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.dq_full), i & 1, ab, err, kSiteBwdSoftmax));
     if (!ok) break;
     tc_fence_after();
     const int q_z = b * p.Hq + g * G + qi.hh;
-    uint32_t d0[32], d1[32], d2[32], d3[32];
+    uint32_t d0[32], d1[32];
     tmem_ld32_async(t_dq, d0);
-    tmem_ld32_async(t_dq + 32, d1);
-    if (D == 128) {
-      tmem_ld32_async(t_dq + 64, d2);
-      tmem_ld32_async(t_dq + 96, d3);
-    }
+    if (D == 128) tmem_ld32_async(t_dq + 32, d1);
     tmem_wait_ld(d0);
-    reg_fence(d1);
-    if (D == 128) {
-      reg_fence(d2);
-      reg_fence(d3);
-    }
+    if (D == 128) reg_fence(d1);
     tc_fence_before();
     mbar_arrive(smem_u32(&sm.dq_free));
-    auto stage = [&](int c0, const uint32_t (&r)[32]) {
-      const uint32_t box = (c0 & 1) ? stage1 : stage0;
-      if (c0 >= 2) {
-        if (lane == 0) bulk_wait_group_read<1>();
+    auto stage_box = [&](int bx, const uint32_t (&r)[32]) {
+      if (bx > 0) {  // one box per warp: the previous copy must have read it
+        if (lane == 0) bulk_wait_group_read<0>();
         __syncwarp();
       }
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch)
-        st_shared_v4(box + sw128_offset(lane, ch), r[ch * 4], r[ch * 4 + 1], r[ch * 4 + 2], r[ch * 4 + 3]);
+      for (int c8 = 0; c8 < 8; ++c8)
+        st_shared_v4(stage + sw128_offset(lane, c8), r[c8 * 4], r[c8 * 4 + 1], r[c8 * 4 + 2], r[c8 * 4 + 3]);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        tma_reduce_add_3d(tm_dqacc, box, c0 * 32, q0 + wq * 32, q_z);
+        tma_reduce_add_3d(tm_dqacc, stage, (D / 2) * wg + 32 * bx, q0 + wq * 32, q_z);
         bulk_commit_group();
       }
     };
-    stage(0, d0);
-    stage(1, d1);
-    if (D == 128) {
-      stage(2, d2);
-      stage(3, d3);
-    }
+    stage_box(0, d0);
+    if (D == 128) stage_box(1, d1);
   }
   if (lane == 0) bulk_wait_group<0>();
   if (ok) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.kv_final), 0, ab, err, kSiteBwdEpilogue));
   if (ok) {
+    // epilogue: warpgroup 0 writes dV, warpgroup 1 writes dK (times scale)
     tc_fence_after();
     const bool store = kv_pos < p.L;
     const int kv_z = b * p.Hkv + g;
     const size_t base = (static_cast<size_t>(kv_z) * p.L + (store ? kv_pos : 0)) * D;
-    const float s = p.scale;
+    const uint32_t t_src = (wg == 0 ? tmem + 256 : tmem + 256 + D) + lane_off;
+    __nv_bfloat16* dst_row = (wg == 0 ? p.dv : p.dk) + base;
+    const float s = wg == 0 ? 1.f : p.scale;
 #pragma unroll
-    for (int c0 = 0; c0 < D / 32; ++c0) {
-      uint32_t r[32];
-      tmem_ld32(t_dv + c0 * 32, r);  // warp-collective: every lane loads
+    for (int c0 = 0; c0 < D / 32; c0 += 2) {
+      uint32_t r0[32], r1[32];
+      tmem_ld32_async(t_src + c0 * 32, r0);
+      tmem_ld32_async(t_src + c0 * 32 + 32, r1);
+      tmem_wait_ld(r0);
+      reg_fence(r1);
       if (store) {
-        uint4* dst = reinterpret_cast<uint4*>(p.dv + base + c0 * 32);
+        uint4* dst = reinterpret_cast<uint4*>(dst_row + c0 * 32);
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const float* f = reinterpret_cast<const float*>(r) + q4 * 8;
-          dst[q4] = make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]),
-                               pack_bf16(f[6], f[7]));
-        }
-      }
-      tmem_ld32(t_dk + c0 * 32, r);
-      if (store) {
-        uint4* dst = reinterpret_cast<uint4*>(p.dk + base + c0 * 32);
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const float* f = reinterpret_cast<const float*>(r) + q4 * 8;
+        for (int q4 = 0; q4 < 8; ++q4) {
+          const float* f = reinterpret_cast<const float*>(q4 < 4 ? r0 : r1) + (q4 & 3) * 8;
           dst[q4] = make_uint4(pack_bf16(f[0] * s, f[1] * s), pack_bf16(f[2] * s, f[3] * s),
                                pack_bf16(f[4] * s, f[5] * s), pack_bf16(f[6] * s, f[7] * s));
         }
@@ -429,13 +425,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&sm.q_full[s]), 1);
       mbar_init(smem_u32(&sm.q_empty[s]), 1);
+      mbar_init(smem_u32(&sm.do_full[s]), 1);
+      mbar_init(smem_u32(&sm.do_empty[s]), 1);
     }
-    mbar_init(smem_u32(&sm.do_full), 1);
-    mbar_init(smem_u32(&sm.do_empty), 1);
     mbar_init(smem_u32(&sm.s_full), 1);
-    mbar_init(smem_u32(&sm.ds_full), 128);
+    mbar_init(smem_u32(&sm.ds_full), 256);
     mbar_init(smem_u32(&sm.dq_full), 1);
-    mbar_init(smem_u32(&sm.dq_free), 128);
+    mbar_init(smem_u32(&sm.dq_free), 256);
     mbar_init(smem_u32(&sm.kv_final), 1);
     mbar_init(smem_u32(&sm.drain), 1);
     fence_mbar_init();
