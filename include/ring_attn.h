@@ -63,7 +63,8 @@ int ring_attn_fwd(const void* q, const void* k, const void* v, void* o, float* l
 
 /*
  * Bytes of device workspace ring_attn_bwd needs for this shape (fp32 dq
- * accumulator plus per-row statistics), or 0 for an invalid shape.
+ * accumulator plus per-row statistics, and fp32 dk/dv accumulators when
+ * Hq > Hkv), or 0 for an invalid shape.
  */
 size_t ring_attn_bwd_workspace_size(int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal);
 
@@ -90,8 +91,8 @@ int ring_attn_bwd(const void* q, const void* k, const void* v, const void* o, co
  * memory is owned by another allocator (a framework's caching pool, a fixed
  * memory budget) and latency-critical code that cannot accept the device
  * synchronisation cudaMalloc/cudaFree may cause.  Arguments and results are
- * those of ring_attn_bwd minus the workspace: the statistics, the fp32 dq
- * accumulator and the launch plan live in a static device array of
+ * those of ring_attn_bwd minus the workspace: the statistics, the fp32
+ * accumulators and the launch plan live in a static device array of
  * RING_ATTN_NOALLOC_SCRATCH_BYTES.  A problem whose workspace
  * (ring_attn_bwd_workspace_size) plus plan does not fit is rejected with
  * RING_ATTN_ERR_WORKSPACE before anything is launched.  The first call on

@@ -14,10 +14,14 @@
 // Three launches:
 //   bwd_pre   per row: -D_i and -lse_i in log2 units (padded rows get -inf,
 //             so their probabilities are 0), and zero the fp32 dQ accumulator.
-//   bwd_main  one CTA per (key/value tile, batch, kv head).  K_j and V_j
-//             stay in shared memory; the CTA loops over the query heads of
-//             the group and over the query tiles that see the tile, in the
-//             order the key/value block meets them going round the ring.
+//   bwd_main  one CTA per (key/value tile, batch, query head).  K_j and V_j
+//             stay in shared memory; the CTA loops over the query tiles of
+//             its head that see the tile, in the order the key/value block
+//             meets them going round the ring.  CTAs launch head by head
+//             (longest first within a head), so the CTAs running together
+//             add into the dQ rows of one or two heads, which stay in L2.
+//             With grouped-query attention the G query heads of a group add
+//             their dK/dV partials into fp32 accumulators (TMA reduce-add).
 //             Per query tile, five tcgen05 GEMMs:
 //               S^T  = K Q^T      (TMEM)      dP^T = V dO^T   (TMEM)
 //               dV  += P^T dO     (TMEM)      dK  += dS^T Q   (TMEM)
@@ -25,7 +29,8 @@
 //             P^T (bf16) goes to tensor memory, packed over dP^T columns
 //             already read, and feeds dV as the A operand; dS^T (bf16) goes
 //             to shared memory (A operand of dK, MN-major A operand of dQ).
-//   bwd_post  dq = bf16(scale * dQ_acc).
+//   bwd_post  dq = bf16(scale * dQ_acc); for grouped-query attention also
+//             dk = bf16(scale * dK_acc) and dv = bf16(dV_acc).
 //
 // Warp roles of bwd_main (384 threads): warp 0 TMA producer, warp 1
 // tcgen05 issuer, warp 2 TMEM allocator, warps 4-11 two compute warpgroups.
@@ -40,9 +45,14 @@
 // P^T of warpgroup h occupies [128+64h, 128+64h+32).
 //
 // Buffers: K, V stationary; Q (with its rows' lse and D) and dO double
-// buffered; dS^T single.  The dQ drain stages fp32 boxes in the bytes of
-// dS^T that the draining warp itself writes, so it only waits for its own
-// copies before writing dS^T again.
+// buffered; dS^T single.  The dQ drain of tile i stages fp32 boxes in the
+// Q and dO buffers of tile i, dead by then (dK(i) and dV(i) have finished):
+// 8 KB per compute warp, so a warp's boxes never wait on each other.  The
+// compute warps, not the tensor core, release those buffers to the producer
+// once their copies have read the boxes, at the start of tile i+1; the
+// refill (for tile i+2) has a whole tile of slack.  (Vector atomics from
+// registers instead of TMA reduce-adds doubled the L2 reduction sectors and
+// ran slower.)
 #include <cfloat>
 
 #include "kernels.h"
@@ -83,6 +93,8 @@ struct BwdSmem {
 
 struct BwdDev {
   int B, Hq, Hkv, L, Lpad, causal;
+  int n_blocks;        // key/value tiles per (batch, head)
+  int kv_accumulate;   // grouped-query attention: dK/dV partials reduce into fp32
   float scale, scale_log2;
   const int32_t* order;
   const int32_t* offsets;
@@ -99,29 +111,24 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, int* e
   mbar_wait(bar, parity, &local, err, kSiteBwdDrain);
 }
 
-// Visits (head offset hh, query tile it) of the CTA's list, in order.
+// Visits the query tiles `it` of the CTA's list (ranges of tile indices), in order.
 struct QIter {
   const int32_t* rg;
-  int nr, G;
-  int hh = 0, ri = 0, it = 0;
-  __device__ QIter(const int32_t* rg_, int nr_, int G_) : rg(rg_), nr(nr_), G(G_) { it = nr > 0 ? rg[0] : 0; }
-  __device__ bool valid() const { return hh < G && nr > 0; }
+  int nr;
+  int ri = 0, it = 0;
+  __device__ QIter(const int32_t* rg_, int nr_) : rg(rg_), nr(nr_) { it = nr > 0 ? rg[0] : 0; }
+  __device__ bool valid() const { return ri < nr; }
   __device__ void next() {
     if (++it < rg[2 * ri + 1]) return;
-    if (++ri < nr) { it = rg[2 * ri]; return; }
-    ri = 0;
-    it = rg[0];
-    ++hh;
+    if (++ri < nr) it = rg[2 * ri];
   }
 };
 
 template <int D>
 __device__ void bwd_producer(BwdSmem<D>& sm, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
-                             const CUtensorMap* tm_v, const CUtensorMap* tm_do, const BwdDev& p, int b, int g,
-                             int kv_tile, const int32_t* rg, int nr, volatile int* ab, int* err) {
+                             const CUtensorMap* tm_v, const CUtensorMap* tm_do, const BwdDev& p, int kv_z,
+                             int q_z, int kv_tile, const int32_t* rg, int nr, volatile int* ab, int* err) {
   using S = BwdSmem<D>;
-  const int G = p.Hq / p.Hkv;
-  const int kv_z = b * p.Hkv + g;
   const uint32_t kvb = smem_u32(&sm.kv_full);
   mbar_arrive_expect_tx(kvb, 2 * S::kTile);
   for (int sub = 0; sub < S::kSub; ++sub) {
@@ -130,9 +137,8 @@ __device__ void bwd_producer(BwdSmem<D>& sm, const CUtensorMap* tm_q, const CUte
   }
   bool ok = true;
   uint32_t nq = 0, ndo = 0;  // Q and dO fills issued
-  for (QIter qi(rg, nr, G); qi.valid() && ok; qi.next()) {
+  for (QIter qi(rg, nr); qi.valid() && ok; qi.next()) {
     const uint32_t i = nq;
-    const int q_z = b * p.Hq + g * G + qi.hh;
     const uint32_t slot = i & 1;
     if (i >= 2) ok = mbar_wait(smem_u32(&sm.q_empty[slot]), ((i >> 1) - 1) & 1, ab, err, kSiteBwdProducer);
     if (!ok) break;
@@ -207,7 +213,6 @@ __device__ void bwd_mma(BwdSmem<D>& sm, uint32_t tmem, uint32_t n_total, volatil
     for (int kk = 0; kk < 8; ++kk)
       umma_ts(t_dv, tmem + 128 + 64 * (kk >> 2) + 8 * (kk & 3), sdesc_sw128(da + kk * 2048, 16384, 1024), kIdKV,
               (i > 0 || kk > 0) ? 1u : 0u);
-    if (i + 2 < n_total) umma_commit(smem_u32(&sm.do_empty[slot]));
     // dK += dS^T Q : A = dS^T (K-major), B = Q (MN-major)
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
@@ -215,7 +220,6 @@ __device__ void bwd_mma(BwdSmem<D>& sm, uint32_t tmem, uint32_t n_total, volatil
       umma_ss(t_dk, sdesc_sw128(sa + off, 16, 1024), sdesc_sw128(qa + kk * 2048, 16384, 1024), kIdKV,
               (i > 0 || kk > 0) ? 1u : 0u);
     }
-    if (i + 2 < n_total) umma_commit(smem_u32(&sm.q_empty[slot]));
     // dQ = dS K : A = dS (MN-major view of dS^T), B = K (MN-major)
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
@@ -232,8 +236,9 @@ __device__ void bwd_mma(BwdSmem<D>& sm, uint32_t tmem, uint32_t n_total, volatil
 }
 
 template <int D>
-__device__ void bwd_compute(BwdSmem<D>& sm, uint32_t tmem, const BwdDev& p, const CUtensorMap* tm_dqacc, int b,
-                            int g, int kv_tile, const int32_t* rg, int nr, volatile int* ab, int* err) {
+__device__ void bwd_compute(BwdSmem<D>& sm, uint32_t tmem, const BwdDev& p, const CUtensorMap* tm_dqacc,
+                            const CUtensorMap* tm_dkacc, const CUtensorMap* tm_dvacc, int kv_z, int q_z, int kv_tile,
+                            const int32_t* rg, int nr, volatile int* ab, int* err) {
   const int wg = ((threadIdx.x >> 5) - 4) >> 2;  // 0 or 1: which half of the query columns
   const int wq = (threadIdx.x >> 5) & 3;         // TMEM lane quadrant
   const int lane = threadIdx.x & 31;
@@ -245,13 +250,14 @@ __device__ void bwd_compute(BwdSmem<D>& sm, uint32_t tmem, const BwdDev& p, cons
   const uint32_t t_p = t_dp;                               // packed P^T over the first 32 of them
   const uint32_t t_dq = ((D == 128) ? tmem : tmem + 384) + (D / 2) * wg + lane_off;
   const uint32_t sa = smem_u32(sm.dsT);
-  // this warp's rows of dS^T (query half wg = sub-tile wg): its staging box
-  const uint32_t stage = sa + wg * 16384 + wq * 4096;
-  const int G = p.Hq / p.Hkv;
+  // dQ staging of warp e = 4 wg + wq: (d/64) boxes of 4 KB at e * (d/64) * 4 KB
+  // of the tile's Q buffer (e < 4) or dO buffer (e >= 4)
+  const int e = 4 * wg + wq;
+  const uint32_t stage_off = static_cast<uint32_t>(e & 3) * (D / 64) * 4096;
   const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
   bool ok = true;
   uint32_t i = 0;
-  for (QIter qi(rg, nr, G); qi.valid() && ok; qi.next(), ++i) {
+  for (QIter qi(rg, nr); qi.valid() && ok; qi.next(), ++i) {
     const uint32_t slot = i & 1;
     ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.q_full[slot]), (i >> 1) & 1, ab, err, kSiteBwdSoftmax));
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.s_full), i & 1, ab, err, kSiteBwdSoftmax));
@@ -265,9 +271,6 @@ __device__ void bwd_compute(BwdSmem<D>& sm, uint32_t tmem, const BwdDev& p, cons
     const bool need_mask = row_dead || first_valid_q > 64 * wg;
     const float* nlse2 = sm.lse2[slot];  // -lse * log2(e)
     const float* ndvec = sm.dvec[slot];  // -D
-    // the previous dQ drain copies must have finished reading this warp's rows
-    if (lane == 0) bulk_wait_group_read<0>();
-    __syncwarp();
 
     // 16 query columns: P^T packed into tensor memory, dS^T into shared memory
     auto process = [&](int c, uint32_t (&rs)[16], uint32_t (&rp)[16]) {
@@ -334,6 +337,17 @@ __device__ void bwd_compute(BwdSmem<D>& sm, uint32_t tmem, const BwdDev& p, cons
     fence_proxy_async_smem();
     tc_fence_before();
     mbar_arrive(smem_u32(&sm.ds_full));
+    if (i > 0) {
+      // Off the critical path (the tensor core now runs dV/dK/dQ): the
+      // previous tile's dQ copies have read their boxes, so its Q and dO
+      // buffers go back to the producer (one arrival per compute warp).
+      if (lane == 0) {
+        bulk_wait_group_read<0>();
+        mbar_arrive(smem_u32(&sm.q_empty[slot ^ 1]));
+        mbar_arrive(smem_u32(&sm.do_empty[slot ^ 1]));
+      }
+      __syncwarp();
+    }
     // dQ drain: this thread's dQ row (a query row), this half's columns,
     // leaves tensor memory in one batched load; the columns are released at
     // once, then the row goes through an fp32 staging box into the global
@@ -341,7 +355,6 @@ __device__ void bwd_compute(BwdSmem<D>& sm, uint32_t tmem, const BwdDev& p, cons
     ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.dq_full), i & 1, ab, err, kSiteBwdSoftmax));
     if (!ok) break;
     tc_fence_after();
-    const int q_z = b * p.Hq + g * G + qi.hh;
     uint32_t d0[32], d1[32];
     tmem_ld32_async(t_dq, d0);
     if (D == 128) tmem_ld32_async(t_dq + 32, d1);
@@ -349,18 +362,16 @@ __device__ void bwd_compute(BwdSmem<D>& sm, uint32_t tmem, const BwdDev& p, cons
     if (D == 128) reg_fence(d1);
     tc_fence_before();
     mbar_arrive(smem_u32(&sm.dq_free));
+    const uint32_t stage = smem_u32(e < 4 ? sm.q[slot] : sm.dO[slot]) + stage_off;
     auto stage_box = [&](int bx, const uint32_t (&r)[32]) {
-      if (bx > 0) {  // one box per warp: the previous copy must have read it
-        if (lane == 0) bulk_wait_group_read<0>();
-        __syncwarp();
-      }
+      const uint32_t box = stage + bx * 4096;
 #pragma unroll
       for (int c8 = 0; c8 < 8; ++c8)
-        st_shared_v4(stage + sw128_offset(lane, c8), r[c8 * 4], r[c8 * 4 + 1], r[c8 * 4 + 2], r[c8 * 4 + 3]);
+        st_shared_v4(box + sw128_offset(lane, c8), r[c8 * 4], r[c8 * 4 + 1], r[c8 * 4 + 2], r[c8 * 4 + 3]);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        tma_reduce_add_3d(tm_dqacc, stage, (D / 2) * wg + 32 * bx, q0 + wq * 32, q_z);
+        tma_reduce_add_3d(tm_dqacc, box, (D / 2) * wg + 32 * bx, q0 + wq * 32, q_z);
         bulk_commit_group();
       }
     };
@@ -368,32 +379,72 @@ __device__ void bwd_compute(BwdSmem<D>& sm, uint32_t tmem, const BwdDev& p, cons
     if (D == 128) stage_box(1, d1);
   }
   if (lane == 0) bulk_wait_group<0>();
+  // Every compute warp's dQ copies have now read their staging boxes; the
+  // dK/dV epilogue below reuses the Q and dO buffers across warps, so all
+  // 256 compute threads meet here first.
+  named_bar_sync(1, 256);
   if (ok) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.kv_final), 0, ab, err, kSiteBwdEpilogue));
   if (ok) {
-    // epilogue: warpgroup 0 writes dV, warpgroup 1 writes dK (times scale)
+    // Epilogue: warpgroup 0 takes dV, warpgroup 1 takes dK.  Without grouped
+    // queries the CTA holds the whole gradient and writes bf16 (dK times
+    // scale); with them it adds its fp32 partial into the accumulator
+    // through staging boxes in the Q and dO buffers, free once kv_final
+    // arrived (every load was consumed by then).
     tc_fence_after();
-    const bool store = kv_pos < p.L;
-    const int kv_z = b * p.Hkv + g;
-    const size_t base = (static_cast<size_t>(kv_z) * p.L + (store ? kv_pos : 0)) * D;
     const uint32_t t_src = (wg == 0 ? tmem + 256 : tmem + 256 + D) + lane_off;
-    __nv_bfloat16* dst_row = (wg == 0 ? p.dv : p.dk) + base;
-    const float s = wg == 0 ? 1.f : p.scale;
+    if (!p.kv_accumulate) {
+      const bool store = kv_pos < p.L;
+      const size_t base = (static_cast<size_t>(kv_z) * p.L + (store ? kv_pos : 0)) * D;
+      __nv_bfloat16* dst_row = (wg == 0 ? p.dv : p.dk) + base;
+      const float s = wg == 0 ? 1.f : p.scale;
 #pragma unroll
-    for (int c0 = 0; c0 < D / 32; c0 += 2) {
-      uint32_t r0[32], r1[32];
-      tmem_ld32_async(t_src + c0 * 32, r0);
-      tmem_ld32_async(t_src + c0 * 32 + 32, r1);
-      tmem_wait_ld(r0);
-      reg_fence(r1);
-      if (store) {
-        uint4* dst = reinterpret_cast<uint4*>(dst_row + c0 * 32);
+      for (int c0 = 0; c0 < D / 32; c0 += 2) {
+        uint32_t r0[32], r1[32];
+        tmem_ld32_async(t_src + c0 * 32, r0);
+        tmem_ld32_async(t_src + c0 * 32 + 32, r1);
+        tmem_wait_ld(r0);
+        reg_fence(r1);
+        if (store) {
+          uint4* dst = reinterpret_cast<uint4*>(dst_row + c0 * 32);
 #pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4) {
-          const float* f = reinterpret_cast<const float*>(q4 < 4 ? r0 : r1) + (q4 & 3) * 8;
-          dst[q4] = make_uint4(pack_bf16(f[0] * s, f[1] * s), pack_bf16(f[2] * s, f[3] * s),
-                               pack_bf16(f[4] * s, f[5] * s), pack_bf16(f[6] * s, f[7] * s));
+          for (int q4 = 0; q4 < 8; ++q4) {
+            const float* f = reinterpret_cast<const float*>(q4 < 4 ? r0 : r1) + (q4 & 3) * 8;
+            dst[q4] = make_uint4(pack_bf16(f[0] * s, f[1] * s), pack_bf16(f[2] * s, f[3] * s),
+                                 pack_bf16(f[4] * s, f[5] * s), pack_bf16(f[6] * s, f[7] * s));
+          }
         }
       }
+    } else {
+      // warp e = 4 wg + wq stages its 32 rows x d fp32 (d/32 boxes of 4 KB) in
+      // half e % 2 of buffer e / 2 of {Q0, Q1, dO0, dO1}
+      const int e = 4 * wg + wq;
+      uint8_t* buf = e < 4 ? sm.q[e >> 1] : sm.dO[(e - 4) >> 1];
+      const uint32_t region = smem_u32(buf) + (e & 1) * (BwdSmem<D>::kTile / 2);
+      const CUtensorMap* tm = wg == 0 ? tm_dvacc : tm_dkacc;
+#pragma unroll
+      for (int c0 = 0; c0 < D / 32; c0 += 2) {
+        uint32_t r0[32], r1[32];
+        tmem_ld32_async(t_src + c0 * 32, r0);
+        tmem_ld32_async(t_src + c0 * 32 + 32, r1);
+        tmem_wait_ld(r0);
+        reg_fence(r1);
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) {
+          st_shared_v4(region + c0 * 4096 + sw128_offset(lane, c8), r0[c8 * 4], r0[c8 * 4 + 1], r0[c8 * 4 + 2],
+                       r0[c8 * 4 + 3]);
+          st_shared_v4(region + (c0 + 1) * 4096 + sw128_offset(lane, c8), r1[c8 * 4], r1[c8 * 4 + 1],
+                       r1[c8 * 4 + 2], r1[c8 * 4 + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        for (int c0 = 0; c0 < D / 32; ++c0)
+          tma_reduce_add_3d(tm, region + c0 * 4096, 32 * c0, kv_tile * 128 + wq * 32, kv_z);
+        bulk_commit_group();
+        bulk_wait_group<0>();
+      }
+      __syncwarp();
     }
   }
 }
@@ -402,7 +453,8 @@ template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     ring_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                         const __grid_constant__ CUtensorMap tm_dqacc, const BwdDev p) {
+                         const __grid_constant__ CUtensorMap tm_dqacc, const __grid_constant__ CUtensorMap tm_dkacc,
+                         const __grid_constant__ CUtensorMap tm_dvacc, const BwdDev p) {
   using S = BwdSmem<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (smem_u32(smem_raw) & 1023u) {  // the swizzled layouts need a 1024-byte aligned base
@@ -411,10 +463,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
   S& sm = *reinterpret_cast<S*>(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int BG = p.B * p.Hkv;
-  const int kv_tile = p.order[blockIdx.x / BG];
-  const int bg = blockIdx.x % BG;
-  const int b = bg / p.Hkv, g = bg % p.Hkv;
+  // items head-major: all key tiles of query head 0 (longest first), then head 1, ...
+  const int qh = blockIdx.x / p.n_blocks;  // b * Hq + h
+  const int kv_tile = p.order[blockIdx.x % p.n_blocks];
+  const int b = qh / p.Hq, h = qh % p.Hq;
+  const int kv_z = b * p.Hkv + h / (p.Hq / p.Hkv);
   const int32_t* rg = p.ranges + 2 * p.offsets[kv_tile];
   const int nr = p.offsets[kv_tile + 1] - p.offsets[kv_tile];
   volatile int* ab = &sm.abort_flag;
@@ -424,9 +477,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(smem_u32(&sm.kv_full), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&sm.q_full[s]), 1);
-      mbar_init(smem_u32(&sm.q_empty[s]), 1);
+      mbar_init(smem_u32(&sm.q_empty[s]), 8);  // released by the 8 compute warps
       mbar_init(smem_u32(&sm.do_full[s]), 1);
-      mbar_init(smem_u32(&sm.do_empty[s]), 1);
+      mbar_init(smem_u32(&sm.do_empty[s]), 8);
     }
     mbar_init(smem_u32(&sm.s_full), 1);
     mbar_init(smem_u32(&sm.ds_full), 256);
@@ -440,6 +493,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_do);
     tma_prefetch_desc(&tm_dqacc);
+    if (p.kv_accumulate) {
+      tma_prefetch_desc(&tm_dkacc);
+      tma_prefetch_desc(&tm_dvacc);
+    }
   }
   if (warp == 2) {
     tmem_alloc(smem_u32(&sm.tmem_base), 512);
@@ -450,15 +507,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   if (warp == 0) {
-    if (lane == 0) bwd_producer<D>(sm, &tm_q, &tm_k, &tm_v, &tm_do, p, b, g, kv_tile, rg, nr, ab, p.err);
+    if (lane == 0) bwd_producer<D>(sm, &tm_q, &tm_k, &tm_v, &tm_do, p, kv_z, qh, kv_tile, rg, nr, ab, p.err);
   } else if (warp == 1) {
     if (lane == 0) {
       int nq = 0;
       for (int ri = 0; ri < nr; ++ri) nq += rg[2 * ri + 1] - rg[2 * ri];
-      bwd_mma<D>(sm, tmem, static_cast<uint32_t>(nq) * (p.Hq / p.Hkv), ab, p.err);
+      bwd_mma<D>(sm, tmem, static_cast<uint32_t>(nq), ab, p.err);
     }
   } else if (warp >= 4) {
-    bwd_compute<D>(sm, tmem, p, &tm_dqacc, b, g, kv_tile, rg, nr, ab, p.err);
+    bwd_compute<D>(sm, tmem, p, &tm_dqacc, &tm_dkacc, &tm_dvacc, kv_z, qh, kv_tile, rg, nr, ab, p.err);
   }
   tc_fence_before();
   __syncthreads();
@@ -468,13 +525,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
 // One warp per row: stores -D_i = -sum_c dO_ic o_ic and -lse_i log2(e) (0 and
 // -inf for padded rows, whose probabilities are then 0), and zeroes the row
-// of the fp32 dQ accumulator.
+// of the fp32 dQ accumulator and, for rows below kv_rows, of the dK and dV
+// accumulators (grouped-query attention; null otherwise).
 template <int D>
 __global__ void __launch_bounds__(256) ring_attn_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
                                                                 const __nv_bfloat16* __restrict__ dO,
                                                                 const float* __restrict__ lse, float* lse2,
-                                                                float* dvec, float* dq_acc, int L, int Lpad,
-                                                                long long n_rows) {
+                                                                float* dvec, float* dq_acc, float* dk_acc,
+                                                                float* dv_acc, int L, int Lpad, long long n_rows,
+                                                                long long kv_rows) {
   const long long r = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (r >= n_rows) return;
@@ -509,12 +568,23 @@ __global__ void __launch_bounds__(256) ring_attn_bwd_pre_kernel(const __nv_bfloa
     dvec[r] = (i < L) ? -acc : 0.f;
     lse2[r] = (i < L) ? -lse[static_cast<size_t>(bh) * L + i] * kLog2e : -INFINITY;
   }
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
   float4* z = reinterpret_cast<float4*>(dq_acc + static_cast<size_t>(r) * D);
 #pragma unroll
-  for (int x = lane; x < D / 4; x += 32) z[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int x = lane; x < D / 4; x += 32) z[x] = zero;
+  if (dk_acc && r < kv_rows) {
+    float4* zk = reinterpret_cast<float4*>(dk_acc + static_cast<size_t>(r) * D);
+    float4* zv = reinterpret_cast<float4*>(dv_acc + static_cast<size_t>(r) * D);
+#pragma unroll
+    for (int x = lane; x < D / 4; x += 32) {
+      zk[x] = zero;
+      zv[x] = zero;
+    }
+  }
 }
 
-// dq = bf16(scale * dQ_acc) for rows < L; 8 elements per thread.
+// dst[z][i][:] = bf16(scale * src[z][i][:]) for rows i < L (src has Lpad
+// rows per z); 8 elements per thread.
 template <int D>
 __global__ void __launch_bounds__(256) ring_attn_bwd_post_kernel(const float* __restrict__ dq_acc,
                                                                  __nv_bfloat16* __restrict__ dq, float scale, int L,
@@ -540,13 +610,15 @@ cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
   if (a.timer) a.timer->mark(1, false, stream);
   ring_attn_bwd_pre_kernel<D><<<pre_blocks, 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dO), a.lse, a.lse2, a.Dvec,
-      a.dq_acc, a.L, a.Lpad, rows);
+      a.dq_acc, a.dk_acc, a.dv_acc, a.L, a.Lpad, rows, static_cast<long long>(a.B) * a.Hkv * a.Lpad);
   cudaError_t e = cudaGetLastError();
   if (a.timer) a.timer->mark(1, true, stream);
   if (e != cudaSuccess) return e;
 
   BwdDev p;
   p.B = a.B; p.Hq = a.Hq; p.Hkv = a.Hkv; p.L = a.L; p.Lpad = a.Lpad; p.causal = a.causal;
+  p.n_blocks = a.n_blocks;
+  p.kv_accumulate = a.dk_acc != nullptr;
   p.scale = 1.0f / sqrtf(static_cast<float>(D));
   p.scale_log2 = p.scale * kLog2e;
   p.order = a.order; p.offsets = a.offsets; p.ranges = a.ranges;
@@ -557,9 +629,10 @@ cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
   const size_t smem = sizeof(BwdSmem<D>);
   e = cudaFuncSetAttribute(ring_attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const dim3 grid(static_cast<unsigned>(a.n_blocks) * a.B * a.Hkv);
+  const dim3 grid(static_cast<unsigned>(a.n_blocks) * a.B * a.Hq);
   if (a.timer) a.timer->mark(2, false, stream);
-  ring_attn_bwd_kernel<D><<<grid, kBwdThreads, smem, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dqacc, p);
+  ring_attn_bwd_kernel<D><<<grid, kBwdThreads, smem, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dqacc,
+                                                               a.tm_dkacc, a.tm_dvacc, p);
   e = cudaGetLastError();
   if (a.timer) a.timer->mark(2, true, stream);
   if (e != cudaSuccess) return e;
@@ -568,6 +641,14 @@ cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
   if (a.timer) a.timer->mark(3, false, stream);
   ring_attn_bwd_post_kernel<D><<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, stream>>>(
       a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), p.scale, a.L, a.Lpad, n8);
+  if (p.kv_accumulate) {
+    const long long kv8 = static_cast<long long>(a.B) * a.Hkv * a.L * D / 8;
+    const unsigned blocks = static_cast<unsigned>((kv8 + 255) / 256);
+    ring_attn_bwd_post_kernel<D><<<blocks, 256, 0, stream>>>(a.dk_acc, static_cast<__nv_bfloat16*>(a.dk), p.scale,
+                                                             a.L, a.Lpad, kv8);
+    ring_attn_bwd_post_kernel<D><<<blocks, 256, 0, stream>>>(a.dv_acc, static_cast<__nv_bfloat16*>(a.dv), 1.f, a.L,
+                                                             a.Lpad, kv8);
+  }
   e = cudaGetLastError();
   if (a.timer) a.timer->mark(3, true, stream);
   return e;

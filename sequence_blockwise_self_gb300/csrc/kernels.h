@@ -40,8 +40,35 @@ struct FwdArgs {
   LaunchTimer* timer;       // nullptr unless profiling
 };
 
+// Backward workspace: byte offsets of its parts (each 256-byte aligned).
+//   lse2 [B*Hq][Lpad] fp32, D [B*Hq][Lpad] fp32, dQ accumulator
+//   [B*Hq][Lpad][d] fp32, and for grouped-query attention (Hq > Hkv) dK and
+//   dV accumulators [B*Hkv][Lpad][d] fp32 (each key tile receives one
+//   partial per query head of its group).
+struct BwdWorkspace {
+  size_t lse2 = 0, dvec = 0, dq = 0, dk = 0, dv = 0, total = 0;
+  int Lpad = 0;
+  bool kv_accumulate = false;
+};
+
+inline BwdWorkspace bwd_workspace(int B, int Hq, int Hkv, int L, int d) {
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  BwdWorkspace w;
+  w.Lpad = (L + 127) / 128 * 128;
+  const size_t rows = static_cast<size_t>(B) * Hq * w.Lpad;
+  const size_t kv_rows = static_cast<size_t>(B) * Hkv * w.Lpad;
+  w.kv_accumulate = Hq > Hkv;
+  w.lse2 = 0;
+  w.dvec = up(rows * sizeof(float));
+  w.dq = w.dvec + up(rows * sizeof(float));
+  w.dk = w.dq + up(rows * d * sizeof(float));
+  w.dv = w.dk + (w.kv_accumulate ? up(kv_rows * d * sizeof(float)) : 0);
+  w.total = w.dv + (w.kv_accumulate ? up(kv_rows * d * sizeof(float)) : 0);
+  return w;
+}
+
 struct BwdArgs {
-  CUtensorMap tm_q, tm_k, tm_v, tm_do, tm_dqacc;
+  CUtensorMap tm_q, tm_k, tm_v, tm_do, tm_dqacc, tm_dkacc, tm_dvacc;
   int B, Hq, Hkv, L, Lpad, d, causal;
   int n_blocks;             // key/value tiles per (b, kv head)
   const int32_t* order;
@@ -53,6 +80,8 @@ struct BwdArgs {
   float* lse2;              // workspace fp32 [B*Hq*Lpad]: -lse * log2(e), -inf padding
   float* Dvec;              // workspace fp32 [B*Hq*Lpad]: -rowsum(dO * o), 0 padding
   float* dq_acc;            // workspace fp32 [B*Hq*Lpad*d]
+  float* dk_acc;            // workspace fp32 [B*Hkv*Lpad*d] (grouped-query attention only, else null)
+  float* dv_acc;            // workspace fp32 [B*Hkv*Lpad*d] (grouped-query attention only, else null)
   void* dq;                 // bf16 [B*Hq*L*d]
   void* dk;                 // bf16 [B*Hkv*L*d]
   void* dv;                 // bf16 [B*Hkv*L*d]

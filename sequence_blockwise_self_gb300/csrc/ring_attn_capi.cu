@@ -139,21 +139,6 @@ int status_ptr(int dev, int** out) {
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-struct BwdLayout {
-  size_t lse2 = 0, dvec = 0, dq = 0, total = 0;
-};
-
-BwdLayout bwd_layout(int B, int Hq, int L, int d) {
-  BwdLayout w;
-  const size_t Lpad = round_up(static_cast<size_t>(L), 128);
-  const size_t rows = static_cast<size_t>(B) * Hq * Lpad;
-  w.lse2 = 0;
-  w.dvec = round_up(rows * sizeof(float), 256);
-  w.dq = w.dvec + round_up(rows * sizeof(float), 256);
-  w.total = w.dq + round_up(rows * d * sizeof(float), 256);
-  return w;
-}
-
 int plan_query(int kind, int L, int n_chunks, int causal, int* n_blocks, int* n_ranges, int32_t* order,
                int32_t* offsets, int32_t* ranges) {
   if (L <= 0 || n_chunks <= 0 || !chunking_ok(L, n_chunks, causal != 0)) return RING_ATTN_ERR_SHAPE;
@@ -242,7 +227,7 @@ int ring_attn_fwd(const void* q, const void* k, const void* v, void* o, float* l
 
 size_t ring_attn_bwd_workspace_size(int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal) {
   if (check_shape(B, Hq, Hkv, L, d, n_chunks, causal) != RING_ATTN_OK) return 0;
-  return bwd_layout(B, Hq, L, d).total;
+  return bwd_workspace(B, Hq, Hkv, L, d).total;
 }
 
 int ring_attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
@@ -255,7 +240,7 @@ int ring_attn_bwd(const void* q, const void* k, const void* v, const void* o, co
   const void* ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv};
   for (const void* p : ptrs)
     if (!aligned16(p)) return RING_ATTN_ERR_UNSUPPORTED;
-  const BwdLayout w = bwd_layout(B, Hq, L, d);
+  const BwdWorkspace w = bwd_workspace(B, Hq, Hkv, L, d);
   if (!workspace || workspace_bytes < w.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return RING_ATTN_ERR_WORKSPACE;
   std::lock_guard<std::mutex> lock(g_mutex);
@@ -270,6 +255,10 @@ int ring_attn_bwd(const void* q, const void* k, const void* v, const void* o, co
       !make_map(&a.tm_v, v, bf, 2, d, L, B * Hkv, 64) || !make_map(&a.tm_do, dO, bf, 2, d, L, B * Hq, 64) ||
       !make_map(&a.tm_dqacc, ws + w.dq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, Lpad, B * Hq, 32, 32))
     return RING_ATTN_ERR_CUDA;
+  if (w.kv_accumulate &&
+      (!make_map(&a.tm_dkacc, ws + w.dk, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, Lpad, B * Hkv, 32, 32) ||
+       !make_map(&a.tm_dvacc, ws + w.dv, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, Lpad, B * Hkv, 32, 32)))
+    return RING_ATTN_ERR_CUDA;
   DevicePlan plan;
   if ((rc = get_plan(dev, 1, L, n_chunks, causal != 0, &plan)) != RING_ATTN_OK) return rc;
   int* err;
@@ -281,6 +270,8 @@ int ring_attn_bwd(const void* q, const void* k, const void* v, const void* o, co
   a.lse2 = reinterpret_cast<float*>(ws + w.lse2);
   a.Dvec = reinterpret_cast<float*>(ws + w.dvec);
   a.dq_acc = reinterpret_cast<float*>(ws + w.dq);
+  a.dk_acc = w.kv_accumulate ? reinterpret_cast<float*>(ws + w.dk) : nullptr;
+  a.dv_acc = w.kv_accumulate ? reinterpret_cast<float*>(ws + w.dv) : nullptr;
   a.dq = dq; a.dk = dk; a.dv = dv; a.err = err; a.timer = active_timer();
   return launch_bwd(a, stream) == cudaSuccess ? RING_ATTN_OK : RING_ATTN_ERR_CUDA;
 }

@@ -9,7 +9,7 @@
 // and, on the first call for a shape, allocates a small device copy of the
 // launch plan; this entry point needs neither.
 //
-// How: the workspace (per-row statistics and the fp32 dq accumulator) and
+// How: the workspace (per-row statistics and the fp32 accumulators) and
 // the launch plan live in one file-scope static __device__ array of
 // kNoAllocScratchBytes.  Every GPU that loads the library holds that array
 // until the process exits.  Host code cannot pass the array's name to a
@@ -19,7 +19,7 @@
 // should therefore happen before any stream capture begins.
 //
 // All calls share the array and it keeps the previous call's contents: the
-// pre-pass kernel rewrites the statistics and zeroes the dq accumulator, and
+// pre-pass kernel rewrites the statistics and zeroes the accumulators, and
 // the plan is copied in again on every call.  Two calls whose work overlaps
 // on the GPU (different streams, no ordering) race on the array.
 #include <cudaTypedefs.h>
@@ -47,8 +47,6 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 std::mutex g_noalloc_mutex;
 std::map<int, unsigned char*> g_scratch_dev;                           // device -> address of the array
 std::map<std::tuple<int, int, int>, std::vector<int32_t>> g_host_plan;  // (L, N, causal) -> flat plan
-
-size_t up256(size_t x) { return (x + 255) / 256 * 256; }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -128,12 +126,10 @@ extern "C" int ring_attn_bwd_noalloc(const void* q, const void* k, const void* v
   for (const void* p : ptrs)
     if (reinterpret_cast<uintptr_t>(p) & 15u) return RING_ATTN_ERR_UNSUPPORTED;
 
-  // Scratch layout: lse2 | D | dq accumulator | plan, each 256-byte aligned.
-  const size_t Lpad = (static_cast<size_t>(L) + 127) / 128 * 128;
-  const size_t rows = static_cast<size_t>(B) * Hq * Lpad;
-  const size_t off_dvec = up256(rows * sizeof(float));
-  const size_t off_dq = off_dvec + up256(rows * sizeof(float));
-  const size_t off_plan = off_dq + up256(rows * d * sizeof(float));
+  // Scratch layout: the backward workspace (see kernels.h), then the plan.
+  const BwdWorkspace w = bwd_workspace(B, Hq, Hkv, L, d);
+  const size_t Lpad = static_cast<size_t>(w.Lpad);
+  const size_t off_plan = w.total;
   if (off_plan > kNoAllocScratchBytes) return RING_ATTN_ERR_WORKSPACE;  // beyond the static array
 
   std::lock_guard<std::mutex> lock(g_noalloc_mutex);
@@ -158,8 +154,14 @@ extern "C" int ring_attn_bwd_noalloc(const void* q, const void* k, const void* v
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   if (!map3d(&a.tm_q, q, bf, 2, d, L, B * Hq, 64, 128) || !map3d(&a.tm_k, k, bf, 2, d, L, B * Hkv, 64, 128) ||
       !map3d(&a.tm_v, v, bf, 2, d, L, B * Hkv, 64, 128) || !map3d(&a.tm_do, dO, bf, 2, d, L, B * Hq, 64, 128) ||
-      !map3d(&a.tm_dqacc, scratch + off_dq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, static_cast<int>(Lpad), B * Hq, 32,
+      !map3d(&a.tm_dqacc, scratch + w.dq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, static_cast<int>(Lpad), B * Hq, 32,
              32))
+    return RING_ATTN_ERR_CUDA;
+  if (w.kv_accumulate &&
+      (!map3d(&a.tm_dkacc, scratch + w.dk, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, static_cast<int>(Lpad), B * Hkv, 32,
+              32) ||
+       !map3d(&a.tm_dvacc, scratch + w.dv, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, static_cast<int>(Lpad), B * Hkv, 32,
+              32)))
     return RING_ATTN_ERR_CUDA;
   a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.L = L; a.Lpad = static_cast<int>(Lpad); a.d = d; a.causal = causal != 0;
   a.n_blocks = n_blocks;
@@ -167,9 +169,11 @@ extern "C" int ring_attn_bwd_noalloc(const void* q, const void* k, const void* v
   a.offsets = dplan + n_blocks;
   a.ranges = dplan + 2 * n_blocks + 1;
   a.o = o; a.dO = dO; a.lse = lse;
-  a.lse2 = reinterpret_cast<float*>(scratch);
-  a.Dvec = reinterpret_cast<float*>(scratch + off_dvec);
-  a.dq_acc = reinterpret_cast<float*>(scratch + off_dq);
+  a.lse2 = reinterpret_cast<float*>(scratch + w.lse2);
+  a.Dvec = reinterpret_cast<float*>(scratch + w.dvec);
+  a.dq_acc = reinterpret_cast<float*>(scratch + w.dq);
+  a.dk_acc = w.kv_accumulate ? reinterpret_cast<float*>(scratch + w.dk) : nullptr;
+  a.dv_acc = w.kv_accumulate ? reinterpret_cast<float*>(scratch + w.dv) : nullptr;
   a.dq = dq; a.dk = dk; a.dv = dv; a.err = err; a.timer = nullptr;
   return launch_bwd(a, stream) == cudaSuccess ? RING_ATTN_OK : RING_ATTN_ERR_CUDA;
 }
