@@ -16,8 +16,13 @@
 //   warps 4-7   softmax of query tile 0 (one thread per row = TMEM lane)
 //   warps 8-11  softmax of query tile 1
 // Tensor memory (512 columns, fp32): S_0 [0,128) S_1 [128,256)
-// O_0 [256,256+d) O_1 [384,384+d).  P (bf16) goes through shared memory in
-// the 128-byte-swizzled K-major layout the tensor core reads.
+// O_0 [256,256+d) O_1 [384,384+d).  P_t (bf16, two per 32-bit column) is
+// written over the first 64 columns of S_t once the softmax has the scores
+// in registers, and feeds O_t += P_t V as the tensor-memory A operand, so P
+// never touches shared memory (whose bandwidth the two SS products nearly
+// fill).  The next S_t is issued behind PV_t by the same thread; tcgen05
+// MMAs from one thread execute in issue order, so it cannot overwrite P_t
+// before PV_t has read it.
 //
 // Issue order per key/value tile j (as in FlashAttention-4 style pipelines):
 //   PV_0(j), S_0(j+1), PV_1(j), S_1(j+1)
@@ -45,9 +50,8 @@ template <int D>
 struct FwdSmem {
   static constexpr int kSub = D / 64;                // 64-column sub-tiles per row
   static constexpr int kTile = 128 * D * 2;          // bytes of a Q, K or V tile
-  static constexpr int kSlots = (D == 128) ? 3 : 6;  // key/value ring slots
+  static constexpr int kSlots = (D == 128) ? 5 : 10;  // key/value ring slots
   alignas(1024) uint8_t q[2][kTile];
-  alignas(1024) uint8_t p[2][128 * 128 * 2];
   alignas(1024) uint8_t kv[kSlots][kTile];
   alignas(8) uint64_t q_full;
   alignas(8) uint64_t kv_full[kSlots];
@@ -130,13 +134,11 @@ __device__ void fwd_mma(FwdSmem<D>& sm, uint32_t tmem, int nkv, volatile int* ab
     }
   };
   auto issue_pv = [&](int t, uint32_t vslot, bool acc) {
-    const uint32_t pa = smem_u32(sm.p[t]), va = smem_u32(sm.kv[vslot]);
+    const uint32_t va = smem_u32(sm.kv[vslot]);
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      const uint32_t poff = (kk >> 2) * 16384 + (kk & 3) * 32;
-      umma_ss(tmem + 256 + 128 * t, sdesc_sw128(pa + poff, 16, 1024), sdesc_sw128(va + kk * 2048, 16384, 1024), kIdO,
+    for (int kk = 0; kk < 8; ++kk)  // A = P_t packed in S_t's columns: 8 per 16 keys
+      umma_ts(tmem + 256 + 128 * t, tmem + 128 * t + 8 * kk, sdesc_sw128(va + kk * 2048, 16384, 1024), kIdO,
               (acc || kk > 0) ? 1u : 0u);
-    }
   };
   uint32_t n = 0;
   auto wait_full = [&](uint32_t& slot, uint32_t& use_idx) -> bool {
@@ -206,7 +208,6 @@ __device__ void fwd_softmax(FwdSmem<D>& sm, uint32_t tmem, int t, const FwdDev& 
   const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
   const uint32_t t_s = tmem + 128 * t + lane_off;
   const uint32_t t_o = tmem + 256 + 128 * t + lane_off;
-  const uint32_t pbase = smem_u32(sm.p[t]);
   const float c = p.scale_log2;
   float m = -INFINITY, l = 0.f;
   bool ok = true;
@@ -263,24 +264,24 @@ __device__ void fwd_softmax(FwdSmem<D>& sm, uint32_t tmem, int t, const FwdDev& 
       const float ms = (m == -INFINITY) ? 0.f : m;
       const float2 c2 = make_float2(c, c), nm2 = make_float2(-ms, -ms);
       float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+      // P = 2^(s c - m) in quarters; each quarter goes to tensor memory (two
+      // bf16 per column, over S_t's first 64 columns) as soon as it is packed.
 #pragma unroll
-      for (int i = 0; i < 128; i += 4) {
-        const float2 x0 = __ffma2_rn(make_float2(s[i], s[i + 1]), c2, nm2);
-        const float2 x1 = __ffma2_rn(make_float2(s[i + 2], s[i + 3]), c2, nm2);
-        s[i] = ex2(x0.x);
-        s[i + 1] = ex2(x0.y);
-        s[i + 2] = ex2(x1.x);
-        s[i + 3] = ex2(x1.y);
-        acc0 = __fadd2_rn(acc0, make_float2(s[i], s[i + 1]));
-        acc1 = __fadd2_rn(acc1, make_float2(s[i + 2], s[i + 3]));
+      for (int half = 0; half < 4; ++half) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 32 * half; i < 32 * half + 32; i += 4) {
+          const float2 x0 = __ffma2_rn(make_float2(s[i], s[i + 1]), c2, nm2);
+          const float2 x1 = __ffma2_rn(make_float2(s[i + 2], s[i + 3]), c2, nm2);
+          const float p0 = ex2(x0.x), p1 = ex2(x0.y), p2 = ex2(x1.x), p3 = ex2(x1.y);
+          acc0 = __fadd2_rn(acc0, make_float2(p0, p1));
+          acc1 = __fadd2_rn(acc1, make_float2(p2, p3));
+          pk[(i - 32 * half) / 2] = pack_bf16(p0, p1);
+          pk[(i - 32 * half) / 2 + 1] = pack_bf16(p2, p3);
+        }
+        tmem_st16_async(t_s + 16 * half, pk);
       }
       l += (acc0.x + acc0.y) + (acc1.x + acc1.y);
-#pragma unroll
-      for (int ch = 0; ch < 16; ++ch) {
-        st_shared_v4(pbase + (ch >> 3) * 16384 + sw128_offset(row, ch & 7), pack_bf16(s[ch * 8], s[ch * 8 + 1]),
-                     pack_bf16(s[ch * 8 + 2], s[ch * 8 + 3]), pack_bf16(s[ch * 8 + 4], s[ch * 8 + 5]),
-                     pack_bf16(s[ch * 8 + 6], s[ch * 8 + 7]));
-      }
       // Rare: the row maximum grew by more than the threshold, so the O_t
       // accumulated so far is rescaled to the new reference.  O_t is
       // quiescent here (the commit that signalled S_t(j) covers PV_t(j-1)),
@@ -296,17 +297,22 @@ __device__ void fwd_softmax(FwdSmem<D>& sm, uint32_t tmem, int t, const FwdDev& 
           tmem_st32(t_o + c0 * 32, r);
         }
       }
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(smem_u32(&sm.p_full[t]));
     }
   }
+  // Output staging: a key/value slot that neither of the last two loads (K
+  // and V of the last tile, which the other tile's final PV may still read)
+  // occupies; every earlier load was consumed before o_final.
+  const uint32_t last_v = (2u * static_cast<uint32_t>(j) - 1u) % FwdSmem<D>::kSlots;  // j == tiles visited
+  const uint32_t pbase = smem_u32(sm.kv[(last_v + 1 + t) % FwdSmem<D>::kSlots]);
   if (ok) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.o_final[t]), 0, ab, err, kSiteFwdEpilogue));
   if (ok) {
     tc_fence_after();
     const float inv = l > 0.f ? 1.f / l : 0.f;
-    // Normalised O row -> bf16 -> the P buffer (free: the last PV_t is done),
-    // laid out as the 128-byte-swizzled boxes of the output tensor map.
+    // Normalised O row -> bf16 -> the staging slot (see above), laid out as
+    // the 128-byte-swizzled boxes of the output tensor map.
     auto emit = [&](int c0, const uint32_t (&r)[32]) {
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
