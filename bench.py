@@ -114,6 +114,26 @@ def _gpu_id(torch, dev):
         return vis.split(",")[dev] if vis else str(dev)
 
 
+# ----------------------------------------------------------- multi-rank
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Slowest rank's value (all ranks get it); identity on one rank."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(step_flops: float, steps: int, world: int, ms_total_max: float) -> float:
+    """Every rank runs `steps` steps of `step_flops`; the job takes the
+    slowest rank's time."""
+    return world * step_flops * steps / (ms_total_max * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------ CPU oracle
 
 def oracle_sample(w, q, k, v, dO, seconds_target: float, seed: int):
@@ -232,13 +252,6 @@ def run_ours(args, w):
     if st != 0:
         raise RuntimeError(f"device status {st} at site {site:#x} during warm-up")
 
-    def max_over_ranks(x: float) -> float:
-        if world == 1:
-            return x
-        t = torch.tensor([x], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
     # (1) device-resident timed region
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(_gpu_id(torch, local)) as clk:
@@ -250,7 +263,7 @@ def run_ours(args, w):
         stop.record(stream)
         torch.cuda.synchronize(dev)
         barrier()
-    ms_total = max_over_ranks(start.elapsed_time(stop))
+    ms_total = max_over_ranks(start.elapsed_time(stop), world, dev)
     clocks = clk.summary()
     st, site = ra.device_status()
     if st != 0:
@@ -258,7 +271,7 @@ def run_ours(args, w):
     ms_step = ms_total / args.steps
     F = w.fwd_flops()
     step_flops = 3.5 * F
-    value = world * step_flops * args.steps / (ms_total * 1e-3) / 1e12
+    value = whole_job_tflops(step_flops, args.steps, world, ms_total)
 
     # (2) per-kernel durations (events around each launch, same stream)
     ra.profile_enable(True)
@@ -305,8 +318,8 @@ def run_ours(args, w):
         e1.record(stream)
         torch.cuda.synchronize(dev)
         barrier()
-        ms_e2e = max_over_ranks(e0.elapsed_time(e1))
-        e2e = {"value": world * step_flops * args.steps / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
+        ms_e2e = max_over_ranks(e0.elapsed_time(e1), world, dev)
+        e2e = {"value": whole_job_tflops(step_flops, args.steps, world, ms_e2e), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e / args.steps}
         del qe, ke, ve, dOe
 

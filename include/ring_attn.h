@@ -117,6 +117,16 @@ const char* ring_attn_strerror(int status);
  */
 int ring_attn_device_status(cudaStream_t stream, int* site);
 
+/*
+ * Failure-detection self-test.  Launches one small kernel whose bounded
+ * wait (the same wait the attention kernels use on their mbarriers) can
+ * never be satisfied: after timeout_us microseconds it gives up, records the
+ * self-test site code (0x301) in the device status word and returns, so the
+ * next ring_attn_device_status() reports RING_ATTN_ERR_DEVICE_TIMEOUT and the
+ * context stays usable.  timeout_us must be in (0, 10^7].
+ */
+int ring_attn_selftest_bounded_wait(unsigned timeout_us, cudaStream_t stream);
+
 /* ---------------------------------------------------------------------
  * Per-kernel timing, for measurement.  While enabled, every kernel launch
  * of the library is bracketed by two CUDA events recorded on the launch

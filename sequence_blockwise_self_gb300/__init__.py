@@ -17,6 +17,7 @@ from .capi import (  # noqa: F401
     profile_enable,
     profile_read,
     release,
+    selftest_bounded_wait,
     ring_attn_bwd,
     ring_attn_bwd_noalloc,
     ring_attn_fwd,

@@ -62,6 +62,8 @@ def load():
     lib.ring_attn_release.restype = None
     lib.ring_attn_owner_rank.argtypes = [I, I, I, I]
     lib.ring_attn_owner_rank.restype = I
+    lib.ring_attn_selftest_bounded_wait.argtypes = [ctypes.c_uint, P]
+    lib.ring_attn_selftest_bounded_wait.restype = I
     lib.ring_attn_profile_enable.argtypes = [I]
     lib.ring_attn_profile_enable.restype = I
     lib.ring_attn_profile_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_longlong)]
@@ -203,6 +205,13 @@ def ring_attn_bwd_noalloc(q, k, v, o, lse, dO, n_chunks: int, causal: bool, dq, 
     if rc != OK:
         raise RingAttnError(rc, "ring_attn_bwd_noalloc")
     return dq, dk, dv
+
+
+def selftest_bounded_wait(timeout_us: int, stream=None):
+    """Launch the failure-detection self-test (a wait that can only time out)."""
+    rc = load().ring_attn_selftest_bounded_wait(int(timeout_us), _stream(stream))
+    if rc != OK:
+        raise RingAttnError(rc, "ring_attn_selftest_bounded_wait")
 
 
 def device_status(stream=None):

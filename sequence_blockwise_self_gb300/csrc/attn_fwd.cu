@@ -423,6 +423,29 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
 }  // namespace
 
+// Failure-detection self-test: one warp waits on an mbarrier that nothing
+// will ever arrive at.  The bounded wait gives up after timeout_ns, raises
+// the abort flag and records kSiteSelfTest in the status word, exactly as a
+// lost arrival in the attention kernels would; the kernel then returns
+// normally, leaving the context usable.
+__global__ void ring_attn_selftest_wait_kernel(int* err, unsigned long long timeout_ns) {
+  __shared__ alignas(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const bool ok = mbar_wait(smem_u32(&bar), 0, &abort_flag, err, kSiteSelfTest, timeout_ns);
+  if (ok && threadIdx.x == 0) atomicCAS(err, 0, -1);  // cannot happen: nothing arrives
+}
+
+cudaError_t launch_selftest_wait(int* err, unsigned long long timeout_ns, cudaStream_t stream) {
+  ring_attn_selftest_wait_kernel<<<1, 32, 0, stream>>>(err, timeout_ns);
+  return cudaGetLastError();
+}
+
 size_t fwd_smem_bytes(int d) {
   return d == 128 ? sizeof(FwdSmem<128>) : sizeof(FwdSmem<64>);
 }

@@ -21,6 +21,7 @@ enum ErrSite : int {
   kSiteBwdEpilogue = 0x204,
   kSiteBwdDrain = 0x205,
   kSiteBwdMisaligned = 0x2FF,
+  kSiteSelfTest = 0x301,
 };
 
 // Optional hook that brackets each launch with events (measurement only).
@@ -90,6 +91,7 @@ struct BwdArgs {
 };
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
+cudaError_t launch_selftest_wait(int* err, unsigned long long timeout_ns, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
 
 // Dynamic shared memory each kernel needs (bytes), for the C ABI's checks.

@@ -293,6 +293,16 @@ int ring_attn_device_status(cudaStream_t stream, int* site) {
   return RING_ATTN_ERR_DEVICE_TIMEOUT;
 }
 
+int ring_attn_selftest_bounded_wait(unsigned timeout_us, cudaStream_t stream) {
+  if (timeout_us == 0 || timeout_us > 10000000u) return RING_ATTN_ERR_SHAPE;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  int dev;
+  if (current_device(&dev) != RING_ATTN_OK) return RING_ATTN_ERR_CUDA;
+  int* err;
+  if (status_ptr(dev, &err) != RING_ATTN_OK) return RING_ATTN_ERR_CUDA;
+  return launch_selftest_wait(err, 1000ull * timeout_us, stream) == cudaSuccess ? RING_ATTN_OK : RING_ATTN_ERR_CUDA;
+}
+
 int ring_attn_profile_enable(int on) {
   std::lock_guard<std::mutex> lock(g_mutex);
   g_timer.on = on != 0;

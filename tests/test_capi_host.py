@@ -76,6 +76,11 @@ def test_fwd_rejects_bad_arguments_without_launching(lib):
     assert _fwd(lib, ptr=ctypes.c_void_p(8)) == capi.ERR_UNSUPPORTED
 
 
+def test_selftest_rejects_bad_timeout_without_launching(lib):
+    assert lib.ring_attn_selftest_bounded_wait(0, NUL) == capi.ERR_SHAPE
+    assert lib.ring_attn_selftest_bounded_wait(10000001, NUL) == capi.ERR_SHAPE
+
+
 def test_bwd_rejects_bad_arguments_and_workspace(lib):
     args = [NUL] * 9
     ws = lib.ring_attn_bwd_workspace_size(1, 2, 2, 256, 64, 4, 0)
