@@ -42,6 +42,41 @@ def _peaks():
         return {"burst": 1900.0, "sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
 
 
+KERNEL_SOURCES = {
+    "ring_attn_fwd_kernel": ["attn_fwd.cu", "sm103_ptx.cuh", "kernels.h"],
+    "ring_attn_bwd_kernel": ["attn_bwd.cu", "sm103_ptx.cuh", "kernels.h"],
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """sha256 over the source files a kernel is compiled from."""
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "sequence_blockwise_self_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def measured_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch (read + write) from the ncu summary in
+    profiles/dram_traffic_<workload>_launch.md, or None if there is none or
+    the kernel's sources changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", f"dram_traffic_{workload}_launch.md")
+    try:
+        with open(path) as f:
+            for line in f:
+                cells = [c.strip() for c in line.strip().strip("|").split("|")]
+                if len(cells) >= 4 and cells[0] == kernel:
+                    if cells[3] != kernel_source_hash(kernel):
+                        return None
+                    return float(cells[1]) + float(cells[2])
+    except OSError:
+        pass
+    return None
+
+
 def _describe(w):
     kind = "causal GQA" if w.causal and w.Hq != w.Hkv else ("causal MHA" if w.causal else "encoder")
     return (f"{w.name}: {kind}, B={w.B} Hq={w.Hq} Hkv={w.Hkv} L={w.L} d={w.d}, N={w.n_chunks} ring chunks"
@@ -292,7 +327,9 @@ def run_ours(args, w):
     roofline = {
         "kernel": "ring_attn_bwd_kernel" if dominant == "bwd_main" else "ring_attn_fwd_kernel",
         "bound": "tensor", "achieved": dom_tflops, "peak": peaks["sustained"], "unit": "TFLOP/s",
-        "frac": dom_tflops / peaks["sustained"], "traffic": None,
+        "frac": dom_tflops / peaks["sustained"],
+        "traffic": measured_traffic("ring_attn_bwd_kernel" if dominant == "bwd_main" else "ring_attn_fwd_kernel",
+                                    w.name),
         "peak_kind": f"bf16_tflops_sustained ({peaks['source']})",
         "frac_of_burst_peak": dom_tflops / peaks["burst"],
         "flops_per_launch": 2.5 * F if dominant == "bwd_main" else F,
