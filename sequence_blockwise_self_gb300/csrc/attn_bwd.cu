@@ -33,7 +33,8 @@
 //             dk = bf16(scale * dK_acc) and dv = bf16(dV_acc).
 //
 // Warp roles of bwd_main (384 threads): warp 0 TMA producer, warp 1
-// tcgen05 issuer, warp 2 TMEM allocator, warps 4-11 two compute warpgroups.
+// tcgen05 issuer (converged; one elected lane issues), warp 2 TMEM
+// allocator, warps 4-11 two compute warpgroups.
 // Both warpgroups work on the same 128 key rows (one thread per row = TMEM
 // lane); warpgroup h takes query columns [64h, 64h+64) of S^T / dP^T,
 // dQ columns [h d/2, (h+1) d/2) in the drain, and dV (h = 0) or dK (h = 1)
@@ -181,13 +182,13 @@ __device__ void bwd_mma(BwdSmem<D>& sm, uint32_t tmem, uint32_t n_total, volatil
   const uint32_t t_dq = (D == 128) ? tmem : tmem + 384;
   const uint32_t ka = smem_u32(sm.k), va = smem_u32(sm.v), sa = smem_u32(sm.dsT);
 
-  bool ok = mbar_wait(smem_u32(&sm.kv_full), 0, ab, err, kSiteBwdMma);
+  bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.kv_full), 0, ab, err, kSiteBwdMma));
   for (uint32_t i = 0; i < n_total && ok; ++i) {
     const uint32_t slot = i & 1;
     const uint32_t qa = smem_u32(sm.q[slot]), da = smem_u32(sm.dO[slot]);
-    ok = mbar_wait(smem_u32(&sm.q_full[slot]), (i >> 1) & 1, ab, err, kSiteBwdMma) &&
-         mbar_wait(smem_u32(&sm.do_full[slot]), (i >> 1) & 1, ab, err, kSiteBwdMma) &&
-         (i == 0 || mbar_wait(smem_u32(&sm.dq_free), (i - 1) & 1, ab, err, kSiteBwdMma));
+    ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.q_full[slot]), (i >> 1) & 1, ab, err, kSiteBwdMma));
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.do_full[slot]), (i >> 1) & 1, ab, err, kSiteBwdMma));
+    if (ok && i > 0) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.dq_free), (i - 1) & 1, ab, err, kSiteBwdMma));
     if (!ok) break;
     tc_fence_after();
     // S^T = K Q^T and dP^T = V dO^T (both operands K-major).  dP^T overwrites
@@ -196,41 +197,41 @@ __device__ void bwd_mma(BwdSmem<D>& sm, uint32_t tmem, uint32_t n_total, volatil
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-      umma_ss(t_s, sdesc_sw128(ka + off, 16, 1024), sdesc_sw128(qa + off, 16, 1024), kIdS, kk > 0);
+      umma_ss_warp(t_s, sdesc_sw128(ka + off, 16, 1024), sdesc_sw128(qa + off, 16, 1024), kIdS, kk > 0);
     }
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-      umma_ss(t_dp, sdesc_sw128(va + off, 16, 1024), sdesc_sw128(da + off, 16, 1024), kIdS, kk > 0);
+      umma_ss_warp(t_dp, sdesc_sw128(va + off, 16, 1024), sdesc_sw128(da + off, 16, 1024), kIdS, kk > 0);
     }
-    umma_commit(smem_u32(&sm.s_full));
-    ok = mbar_wait(smem_u32(&sm.ds_full), i & 1, ab, err, kSiteBwdMma);
+    umma_commit_warp(smem_u32(&sm.s_full));
+    ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.ds_full), i & 1, ab, err, kSiteBwdMma));
     if (!ok) break;
     tc_fence_after();
     // dV += P^T dO : A = packed P^T in tensor memory (query k-step kk lives
     // in warpgroup kk/4's columns), B = dO (MN-major)
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
-      umma_ts(t_dv, tmem + 128 + 64 * (kk >> 2) + 8 * (kk & 3), sdesc_sw128(da + kk * 2048, 16384, 1024), kIdKV,
+      umma_ts_warp(t_dv, tmem + 128 + 64 * (kk >> 2) + 8 * (kk & 3), sdesc_sw128(da + kk * 2048, 16384, 1024), kIdKV,
               (i > 0 || kk > 0) ? 1u : 0u);
     // dK += dS^T Q : A = dS^T (K-major), B = Q (MN-major)
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
       const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-      umma_ss(t_dk, sdesc_sw128(sa + off, 16, 1024), sdesc_sw128(qa + kk * 2048, 16384, 1024), kIdKV,
+      umma_ss_warp(t_dk, sdesc_sw128(sa + off, 16, 1024), sdesc_sw128(qa + kk * 2048, 16384, 1024), kIdKV,
               (i > 0 || kk > 0) ? 1u : 0u);
     }
     // dQ = dS K : A = dS (MN-major view of dS^T), B = K (MN-major)
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
-      umma_ss(t_dq, sdesc_sw128(sa + kk * 2048, 16384, 1024), sdesc_sw128(ka + kk * 2048, 16384, 1024), kIdQ,
+      umma_ss_warp(t_dq, sdesc_sw128(sa + kk * 2048, 16384, 1024), sdesc_sw128(ka + kk * 2048, 16384, 1024), kIdQ,
               kk > 0);
-    umma_commit(smem_u32(&sm.dq_full));
+    umma_commit_warp(smem_u32(&sm.dq_full));
   }
   if (ok) {
-    umma_commit(smem_u32(&sm.kv_final));
+    umma_commit_warp(smem_u32(&sm.kv_final));
   } else {
-    umma_commit(smem_u32(&sm.drain));
+    umma_commit_warp(smem_u32(&sm.drain));
     wait_drain(smem_u32(&sm.drain), 0, err);
   }
 }
@@ -509,11 +510,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (warp == 0) {
     if (lane == 0) bwd_producer<D>(sm, &tm_q, &tm_k, &tm_v, &tm_do, p, kv_z, qh, kv_tile, rg, nr, ab, p.err);
   } else if (warp == 1) {
-    if (lane == 0) {
-      int nq = 0;
-      for (int ri = 0; ri < nr; ++ri) nq += rg[2 * ri + 1] - rg[2 * ri];
-      bwd_mma<D>(sm, tmem, static_cast<uint32_t>(nq), ab, p.err);
-    }
+    // the whole warp runs the issue loop; one elected lane issues
+    int nq = 0;
+    for (int ri = 0; ri < nr; ++ri) nq += rg[2 * ri + 1] - rg[2 * ri];
+    bwd_mma<D>(sm, tmem, static_cast<uint32_t>(nq), ab, p.err);
   } else if (warp >= 4) {
     bwd_compute<D>(sm, tmem, p, &tm_dqacc, &tm_dkacc, &tm_dvacc, kv_z, qh, kv_tile, rg, nr, ab, p.err);
   }

@@ -11,7 +11,8 @@
 // One CTA = one 256-row query block of one (batch, head): two 128-row query
 // tiles that share every key/value tile.  Warp roles (384 threads):
 //   warp 0      TMA producer: Q once, then K_j, V_j into a ring of slots
-//   warp 1      tcgen05 issuer (one thread): S_t = Q_t K_j^T, O_t += P_t V_j
+//   warp 1      tcgen05 issuer (converged warp, one elected lane issues):
+//               S_t = Q_t K_j^T, O_t += P_t V_j
 //   warp 2      tensor-memory allocator
 //   warps 4-7   softmax of query tile 0 (one thread per row = TMEM lane)
 //   warps 8-11  softmax of query tile 1
@@ -130,40 +131,40 @@ __device__ void fwd_mma(FwdSmem<D>& sm, uint32_t tmem, int nkv, volatile int* ab
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-      umma_ss(tmem + 128 * t, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), kIdS, kk > 0);
+      umma_ss_warp(tmem + 128 * t, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), kIdS, kk > 0);
     }
   };
   auto issue_pv = [&](int t, uint32_t vslot, bool acc) {
     const uint32_t va = smem_u32(sm.kv[vslot]);
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)  // A = P_t packed in S_t's columns: 8 per 16 keys
-      umma_ts(tmem + 256 + 128 * t, tmem + 128 * t + 8 * kk, sdesc_sw128(va + kk * 2048, 16384, 1024), kIdO,
+      umma_ts_warp(tmem + 256 + 128 * t, tmem + 128 * t + 8 * kk, sdesc_sw128(va + kk * 2048, 16384, 1024), kIdO,
               (acc || kk > 0) ? 1u : 0u);
   };
   uint32_t n = 0;
   auto wait_full = [&](uint32_t& slot, uint32_t& use_idx) -> bool {
     slot = n % S::kSlots;
     use_idx = n;
-    const bool r = mbar_wait(smem_u32(&sm.kv_full[slot]), (n / S::kSlots) & 1, ab, err, kSiteFwdMma);
+    const bool r = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.kv_full[slot]), (n / S::kSlots) & 1, ab, err, kSiteFwdMma));
     ++n;
     return r;
   };
   // Release a slot only if the producer will refill it: every commit is
   // then awaited by someone before the CTA exits.
   auto release = [&](uint32_t slot, uint32_t use_idx) {
-    if (use_idx + S::kSlots < total_uses) umma_commit(smem_u32(&sm.kv_empty[slot]));
+    if (use_idx + S::kSlots < total_uses) umma_commit_warp(smem_u32(&sm.kv_empty[slot]));
   };
 
-  bool ok = mbar_wait(smem_u32(&sm.q_full), 0, ab, err, kSiteFwdMma);
+  bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.q_full), 0, ab, err, kSiteFwdMma));
   if (ok) {
     uint32_t ks, ku;
     ok = wait_full(ks, ku);
     if (ok) {
       tc_fence_after();
       issue_s(0, ks);
-      umma_commit(smem_u32(&sm.s_full[0]));
+      umma_commit_warp(smem_u32(&sm.s_full[0]));
       issue_s(1, ks);
-      umma_commit(smem_u32(&sm.s_full[1]));
+      umma_commit_warp(smem_u32(&sm.s_full[1]));
       release(ks, ku);
     }
   }
@@ -172,7 +173,7 @@ __device__ void fwd_mma(FwdSmem<D>& sm, uint32_t tmem, int nkv, volatile int* ab
     ok = wait_full(vs, vu);
     const bool has_next = j + 1 < nkv;
     for (int t = 0; t < 2 && ok; ++t) {
-      ok = mbar_wait(smem_u32(&sm.p_full[t]), j & 1, ab, err, kSiteFwdMma);
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.p_full[t]), j & 1, ab, err, kSiteFwdMma));
       if (!ok) break;
       tc_fence_after();
       issue_pv(t, vs, j > 0);
@@ -183,9 +184,9 @@ __device__ void fwd_mma(FwdSmem<D>& sm, uint32_t tmem, int nkv, volatile int* ab
           tc_fence_after();
         }
         issue_s(t, ks);
-        umma_commit(smem_u32(&sm.s_full[t]));
+        umma_commit_warp(smem_u32(&sm.s_full[t]));
       } else {
-        umma_commit(smem_u32(&sm.o_final[t]));
+        umma_commit_warp(smem_u32(&sm.o_final[t]));
       }
     }
     if (!ok) break;
@@ -193,7 +194,7 @@ __device__ void fwd_mma(FwdSmem<D>& sm, uint32_t tmem, int nkv, volatile int* ab
     release(vs, vu);
   }
   if (!ok) {
-    umma_commit(smem_u32(&sm.drain));
+    umma_commit_warp(smem_u32(&sm.drain));
     wait_drain(smem_u32(&sm.drain), 0, err);
   }
 }
@@ -407,11 +408,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   if (warp == 0) {
     if (lane == 0) fwd_producer<D>(sm, &tm_q, &tm_k, &tm_v, q0, bh, kv_z, rg, nr, ab, p.err);
   } else if (warp == 1) {
-    if (lane == 0) {
-      int nkv = 0;
-      for (int ri = 0; ri < nr; ++ri) nkv += rg[2 * ri + 1] - rg[2 * ri];
-      fwd_mma<D>(sm, tmem, nkv, ab, p.err);
-    }
+    // the whole warp runs the issue loop; one elected lane issues
+    int nkv = 0;
+    for (int ri = 0; ri < nr; ++ri) nkv += rg[2 * ri + 1] - rg[2 * ri];
+    fwd_mma<D>(sm, tmem, nkv, ab, p.err);
   } else if (warp >= 4) {
     fwd_softmax<D>(sm, tmem, (warp - 4) >> 2, p, &tm_o, q0, bh, rg, nr, ab, p.err);
   }
