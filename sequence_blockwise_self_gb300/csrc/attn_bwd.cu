@@ -34,7 +34,7 @@
 //
 // Warp roles of bwd_main (384 threads): warp 0 TMA producer, warp 1
 // tcgen05 issuer (converged; one elected lane issues), warp 2 TMEM
-// allocator, warps 4-11 two compute warpgroups.
+// allocator, warp 3 dQ reduce issuer, warps 4-11 two compute warpgroups.
 // Both warpgroups work on the same 128 key rows (one thread per row = TMEM
 // lane); warpgroup h takes query columns [64h, 64h+64) of S^T / dP^T,
 // dQ columns [h d/2, (h+1) d/2) in the drain, and dV (h = 0) or dK (h = 1)
@@ -45,15 +45,20 @@
 // (S^T has been read by then; the next S^T waits for the dQ drain).  Packed
 // P^T of warpgroup h occupies [128+64h, 128+64h+32).
 //
+// Product order per query tile i: S^T(i), dP^T(i) | dQ(i), dV(i), dK(i).
+// dQ(i) is signalled on its own, so its drain from tensor memory overlaps
+// dV(i) and dK(i), and S^T(i+1) (over the drained dQ columns) follows dK(i)
+// on the tensor core without a gap.
+//
 // Buffers: K, V stationary; Q (with its rows' lse and D) and dO double
 // buffered; dS^T single.  The dQ drain of tile i stages fp32 boxes in the
-// Q and dO buffers of tile i, dead by then (dK(i) and dV(i) have finished):
-// 8 KB per compute warp, so a warp's boxes never wait on each other.  The
-// compute warps, not the tensor core, release those buffers to the producer
-// once their copies have read the boxes, at the start of tile i+1; the
-// refill (for tile i+2) has a whole tile of slack.  (Vector atomics from
-// registers instead of TMA reduce-adds doubled the L2 reduction sectors and
-// ran slower.)
+// Q and dO buffers of tile i once dV(i) and dK(i) have finished reading
+// them: 8 KB per compute warp, so a warp's boxes never wait on each other.
+// Warp 3 issues the TMA reduce-adds of every staged box, waits until they
+// have read shared memory and then hands the buffers back to the producer,
+// so no compute warp ever waits on a bulk copy.  (Vector atomics from
+// registers instead of TMA reduce-adds ran slower, with either row layout
+// of the accumulator.)
 #include <cfloat>
 
 #include "kernels.h"
@@ -86,6 +91,11 @@ struct BwdSmem {
   alignas(8) uint64_t ds_full;
   alignas(8) uint64_t dq_full;
   alignas(8) uint64_t dq_free;
+  alignas(8) uint64_t qdo_read;    // dV(i), dK(i) done: Q(i), dO(i) free for staging
+  // the 8 compute warps staged dQ(i) in slot i % 2; one barrier per slot,
+  // so its phases cannot run ahead of the reducer (staging tile i+2 in the
+  // slot needs the reducer to have released it after tile i)
+  alignas(8) uint64_t stage_full[2];
   alignas(8) uint64_t kv_final;
   alignas(8) uint64_t drain;
   uint32_t tmem_base;
@@ -191,9 +201,10 @@ __device__ void bwd_mma(BwdSmem<D>& sm, uint32_t tmem, uint32_t n_total, volatil
     if (ok && i > 0) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.dq_free), (i - 1) & 1, ab, err, kSiteBwdMma));
     if (!ok) break;
     tc_fence_after();
-    // S^T = K Q^T and dP^T = V dO^T (both operands K-major).  dP^T overwrites
-    // the packed P^T of the previous tile: dV(i-1) finished before dQ(i-1),
-    // whose drain released dq_free.
+    // S^T = K Q^T and dP^T = V dO^T (both operands K-major).  S^T overwrites
+    // dQ(i-1), whose drain released dq_free; dP^T overwrites the packed P^T
+    // of the previous tile, read by dV(i-1), which the tensor core ran
+    // before these.
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -208,25 +219,26 @@ __device__ void bwd_mma(BwdSmem<D>& sm, uint32_t tmem, uint32_t n_total, volatil
     ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.ds_full), i & 1, ab, err, kSiteBwdMma));
     if (!ok) break;
     tc_fence_after();
+    // dQ = dS K : A = dS (MN-major view of dS^T), B = K (MN-major)
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+      umma_ss_warp(t_dq, sdesc_sw128(sa + kk * 2048, 16384, 1024), sdesc_sw128(ka + kk * 2048, 16384, 1024), kIdQ,
+                   kk > 0);
+    umma_commit_warp(smem_u32(&sm.dq_full));
     // dV += P^T dO : A = packed P^T in tensor memory (query k-step kk lives
     // in warpgroup kk/4's columns), B = dO (MN-major)
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
       umma_ts_warp(t_dv, tmem + 128 + 64 * (kk >> 2) + 8 * (kk & 3), sdesc_sw128(da + kk * 2048, 16384, 1024), kIdKV,
-              (i > 0 || kk > 0) ? 1u : 0u);
+                   (i > 0 || kk > 0) ? 1u : 0u);
     // dK += dS^T Q : A = dS^T (K-major), B = Q (MN-major)
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
       const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
       umma_ss_warp(t_dk, sdesc_sw128(sa + off, 16, 1024), sdesc_sw128(qa + kk * 2048, 16384, 1024), kIdKV,
-              (i > 0 || kk > 0) ? 1u : 0u);
+                   (i > 0 || kk > 0) ? 1u : 0u);
     }
-    // dQ = dS K : A = dS (MN-major view of dS^T), B = K (MN-major)
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk)
-      umma_ss_warp(t_dq, sdesc_sw128(sa + kk * 2048, 16384, 1024), sdesc_sw128(ka + kk * 2048, 16384, 1024), kIdQ,
-              kk > 0);
-    umma_commit_warp(smem_u32(&sm.dq_full));
+    umma_commit_warp(smem_u32(&sm.qdo_read));
   }
   if (ok) {
     umma_commit_warp(smem_u32(&sm.kv_final));
@@ -236,9 +248,38 @@ __device__ void bwd_mma(BwdSmem<D>& sm, uint32_t tmem, uint32_t n_total, volatil
   }
 }
 
+// Warp 3, one lane: for each query tile, once the 8 compute warps have
+// staged dQ(i), issue the TMA reduce-adds of their boxes into the fp32
+// accumulator, wait until the copies have read shared memory and return
+// the tile's Q and dO buffers to the producer.  Joins the compute warps'
+// named barrier before their epilogue, all copies complete.
 template <int D>
-__device__ void bwd_compute(BwdSmem<D>& sm, uint32_t tmem, const BwdDev& p, const CUtensorMap* tm_dqacc,
-                            const CUtensorMap* tm_dkacc, const CUtensorMap* tm_dvacc, int kv_z, int q_z, int kv_tile,
+__device__ void bwd_dq_reducer(BwdSmem<D>& sm, const CUtensorMap* tm_dqacc, int q_z, const int32_t* rg, int nr,
+                               volatile int* ab, int* err) {
+  bool ok = true;
+  uint32_t i = 0;
+  for (QIter qi(rg, nr); qi.valid() && ok; qi.next(), ++i) {
+    const uint32_t slot = i & 1;
+    ok = mbar_wait(smem_u32(&sm.stage_full[slot]), (i >> 1) & 1, ab, err, kSiteBwdReducer);
+    if (!ok) break;
+    const int q0 = qi.it * 128;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {  // compute warp e = 4 wg + wq
+      const uint32_t stage = smem_u32(e < 4 ? sm.q[slot] : sm.dO[slot]) + static_cast<uint32_t>(e & 3) * (D / 64) * 4096;
+#pragma unroll
+      for (int bx = 0; bx < D / 64; ++bx)
+        tma_reduce_add_3d(tm_dqacc, stage + bx * 4096, (D / 2) * (e >> 2) + 32 * bx, q0 + (e & 3) * 32, q_z);
+    }
+    bulk_commit_group();
+    bulk_wait_group_read<0>();
+    mbar_arrive(smem_u32(&sm.q_empty[slot]));
+    mbar_arrive(smem_u32(&sm.do_empty[slot]));
+  }
+  bulk_wait_group<0>();
+}
+
+template <int D>
+__device__ void bwd_compute(BwdSmem<D>& sm, uint32_t tmem, const BwdDev& p, const CUtensorMap* tm_dkacc, const CUtensorMap* tm_dvacc, int kv_z, int q_z, int kv_tile,
                             const int32_t* rg, int nr, volatile int* ab, int* err) {
   const int wg = ((threadIdx.x >> 5) - 4) >> 2;  // 0 or 1: which half of the query columns
   const int wq = (threadIdx.x >> 5) & 3;         // TMEM lane quadrant
@@ -338,21 +379,11 @@ __device__ void bwd_compute(BwdSmem<D>& sm, uint32_t tmem, const BwdDev& p, cons
     fence_proxy_async_smem();
     tc_fence_before();
     mbar_arrive(smem_u32(&sm.ds_full));
-    if (i > 0) {
-      // Off the critical path (the tensor core now runs dV/dK/dQ): the
-      // previous tile's dQ copies have read their boxes, so its Q and dO
-      // buffers go back to the producer (one arrival per compute warp).
-      if (lane == 0) {
-        bulk_wait_group_read<0>();
-        mbar_arrive(smem_u32(&sm.q_empty[slot ^ 1]));
-        mbar_arrive(smem_u32(&sm.do_empty[slot ^ 1]));
-      }
-      __syncwarp();
-    }
     // dQ drain: this thread's dQ row (a query row), this half's columns,
     // leaves tensor memory in one batched load; the columns are released at
-    // once, then the row goes through an fp32 staging box into the global
-    // accumulator (TMA reduce-add).
+    // once, then the row is staged as fp32 boxes in the tile's Q and dO
+    // buffers (once dV and dK have read them) for warp 3's reduce-adds into
+    // the global accumulator.
     ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.dq_full), i & 1, ab, err, kSiteBwdSoftmax));
     if (!ok) break;
     tc_fence_after();
@@ -363,27 +394,24 @@ __device__ void bwd_compute(BwdSmem<D>& sm, uint32_t tmem, const BwdDev& p, cons
     if (D == 128) reg_fence(d1);
     tc_fence_before();
     mbar_arrive(smem_u32(&sm.dq_free));
+    ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.qdo_read), i & 1, ab, err, kSiteBwdSoftmax));
+    if (!ok) break;
     const uint32_t stage = smem_u32(e < 4 ? sm.q[slot] : sm.dO[slot]) + stage_off;
     auto stage_box = [&](int bx, const uint32_t (&r)[32]) {
       const uint32_t box = stage + bx * 4096;
 #pragma unroll
       for (int c8 = 0; c8 < 8; ++c8)
         st_shared_v4(box + sw128_offset(lane, c8), r[c8 * 4], r[c8 * 4 + 1], r[c8 * 4 + 2], r[c8 * 4 + 3]);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        tma_reduce_add_3d(tm_dqacc, box, (D / 2) * wg + 32 * bx, q0 + wq * 32, q_z);
-        bulk_commit_group();
-      }
     };
     stage_box(0, d0);
     if (D == 128) stage_box(1, d1);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&sm.stage_full[slot]));
   }
-  if (lane == 0) bulk_wait_group<0>();
-  // Every compute warp's dQ copies have now read their staging boxes; the
-  // dK/dV epilogue below reuses the Q and dO buffers across warps, so all
-  // 256 compute threads meet here first.
-  named_bar_sync(1, 256);
+  // Warp 3's reduce-adds have read every staging box once it joins here;
+  // the dK/dV epilogue below reuses the Q and dO buffers across warps.
+  named_bar_sync(1, 288);
   if (ok) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.kv_final), 0, ab, err, kSiteBwdEpilogue));
   if (ok) {
     // Epilogue: warpgroup 0 takes dV, warpgroup 1 takes dK.  Without grouped
@@ -478,14 +506,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(smem_u32(&sm.kv_full), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&sm.q_full[s]), 1);
-      mbar_init(smem_u32(&sm.q_empty[s]), 8);  // released by the 8 compute warps
+      mbar_init(smem_u32(&sm.q_empty[s]), 1);  // released by the dQ reduce issuer
       mbar_init(smem_u32(&sm.do_full[s]), 1);
-      mbar_init(smem_u32(&sm.do_empty[s]), 8);
+      mbar_init(smem_u32(&sm.do_empty[s]), 1);
     }
     mbar_init(smem_u32(&sm.s_full), 1);
     mbar_init(smem_u32(&sm.ds_full), 256);
     mbar_init(smem_u32(&sm.dq_full), 1);
     mbar_init(smem_u32(&sm.dq_free), 256);
+    mbar_init(smem_u32(&sm.qdo_read), 1);
+    mbar_init(smem_u32(&sm.stage_full[0]), 8);
+    mbar_init(smem_u32(&sm.stage_full[1]), 8);
     mbar_init(smem_u32(&sm.kv_final), 1);
     mbar_init(smem_u32(&sm.drain), 1);
     fence_mbar_init();
@@ -514,8 +545,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     int nq = 0;
     for (int ri = 0; ri < nr; ++ri) nq += rg[2 * ri + 1] - rg[2 * ri];
     bwd_mma<D>(sm, tmem, static_cast<uint32_t>(nq), ab, p.err);
+  } else if (warp == 3) {
+    if (lane == 0) bwd_dq_reducer<D>(sm, &tm_dqacc, qh, rg, nr, ab, p.err);
+    __syncwarp();
+    named_bar_sync(1, 288);
   } else if (warp >= 4) {
-    bwd_compute<D>(sm, tmem, p, &tm_dqacc, &tm_dkacc, &tm_dvacc, kv_z, qh, kv_tile, rg, nr, ab, p.err);
+    bwd_compute<D>(sm, tmem, p, &tm_dkacc, &tm_dvacc, kv_z, qh, kv_tile, rg, nr, ab, p.err);
   }
   tc_fence_before();
   __syncthreads();

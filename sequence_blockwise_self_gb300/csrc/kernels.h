@@ -20,6 +20,7 @@ enum ErrSite : int {
   kSiteBwdSoftmax = 0x203,
   kSiteBwdEpilogue = 0x204,
   kSiteBwdDrain = 0x205,
+  kSiteBwdReducer = 0x206,
   kSiteBwdMisaligned = 0x2FF,
   kSiteSelfTest = 0x301,
 };
