@@ -102,6 +102,17 @@ struct BwdSmem {
   int abort_flag;
 };
 
+// Offset of element (row i, column col) of the (batch, head) slice z of the
+// fp32 dQ accumulator: tiles of 128 query rows, each stored as d/4 column
+// quads of [128 rows][4 floats].  The half tile of one compute warpgroup
+// (d/2 columns) is then one contiguous block, both here and in its staging
+// buffer, and goes into the accumulator as a single bulk reduce-add.
+template <int D>
+__host__ __device__ __forceinline__ size_t dq_acc_offset(long long z, int Lpad, int i, int col) {
+  return static_cast<size_t>(z) * Lpad * D + static_cast<size_t>(i >> 7) * 128 * D + (col >> 2) * 512 +
+         (i & 127) * 4 + (col & 3);
+}
+
 struct BwdDev {
   int B, Hq, Hkv, L, Lpad, causal;
   int n_blocks;        // key/value tiles per (batch, head)
@@ -112,6 +123,7 @@ struct BwdDev {
   const int32_t* ranges;
   const float* lse2;
   const float* dvec;
+  float* dq_acc;       // fp32, tiled (dq_acc_offset)
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   int* err;
@@ -254,7 +266,7 @@ __device__ void bwd_mma(BwdSmem<D>& sm, uint32_t tmem, uint32_t n_total, volatil
 // the tile's Q and dO buffers to the producer.  Joins the compute warps'
 // named barrier before their epilogue, all copies complete.
 template <int D>
-__device__ void bwd_dq_reducer(BwdSmem<D>& sm, const CUtensorMap* tm_dqacc, int q_z, const int32_t* rg, int nr,
+__device__ void bwd_dq_reducer(BwdSmem<D>& sm, float* dq_acc, int Lpad, int q_z, const int32_t* rg, int nr,
                                volatile int* ab, int* err) {
   bool ok = true;
   uint32_t i = 0;
@@ -263,16 +275,18 @@ __device__ void bwd_dq_reducer(BwdSmem<D>& sm, const CUtensorMap* tm_dqacc, int 
     ok = mbar_wait(smem_u32(&sm.stage_full[slot]), (i >> 1) & 1, ab, err, kSiteBwdReducer);
     if (!ok) break;
     const int q0 = qi.it * 128;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {  // compute warp e = 4 wg + wq
-      const uint32_t stage = smem_u32(e < 4 ? sm.q[slot] : sm.dO[slot]) + static_cast<uint32_t>(e & 3) * (D / 64) * 4096;
-#pragma unroll
-      for (int bx = 0; bx < D / 64; ++bx)
-        tma_reduce_add_3d(tm_dqacc, stage + bx * 4096, (D / 2) * (e >> 2) + 32 * bx, q0 + (e & 3) * 32, q_z);
-    }
+    // warpgroup 0's half tile (staged in the Q buffer), then warpgroup 1's
+    // (in the dO buffer), as two groups: Q goes back to the producer (which
+    // refills it first) as soon as its half has been read
+    float* const dst = dq_acc + dq_acc_offset<D>(q_z, Lpad, q0, 0);
+    constexpr uint32_t kHalf = 128 * (D / 2) * 4;
+    bulk_reduce_add_f32(dst, smem_u32(sm.q[slot]), kHalf);
     bulk_commit_group();
-    bulk_wait_group_read<0>();
+    bulk_reduce_add_f32(dst + kHalf / 4, smem_u32(sm.dO[slot]), kHalf);
+    bulk_commit_group();
+    bulk_wait_group_read<1>();
     mbar_arrive(smem_u32(&sm.q_empty[slot]));
+    bulk_wait_group_read<0>();
     mbar_arrive(smem_u32(&sm.do_empty[slot]));
   }
   bulk_wait_group<0>();
@@ -292,10 +306,6 @@ __device__ void bwd_compute(BwdSmem<D>& sm, uint32_t tmem, const BwdDev& p, cons
   const uint32_t t_p = t_dp;                               // packed P^T over the first 32 of them
   const uint32_t t_dq = ((D == 128) ? tmem : tmem + 384) + (D / 2) * wg + lane_off;
   const uint32_t sa = smem_u32(sm.dsT);
-  // dQ staging of warp e = 4 wg + wq: (d/64) boxes of 4 KB at e * (d/64) * 4 KB
-  // of the tile's Q buffer (e < 4) or dO buffer (e >= 4)
-  const int e = 4 * wg + wq;
-  const uint32_t stage_off = static_cast<uint32_t>(e & 3) * (D / 64) * 4096;
   const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
   bool ok = true;
   uint32_t i = 0;
@@ -396,15 +406,16 @@ __device__ void bwd_compute(BwdSmem<D>& sm, uint32_t tmem, const BwdDev& p, cons
     mbar_arrive(smem_u32(&sm.dq_free));
     ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.qdo_read), i & 1, ab, err, kSiteBwdSoftmax));
     if (!ok) break;
-    const uint32_t stage = smem_u32(e < 4 ? sm.q[slot] : sm.dO[slot]) + stage_off;
-    auto stage_box = [&](int bx, const uint32_t (&r)[32]) {
-      const uint32_t box = stage + bx * 4096;
+    // staging in the accumulator's own layout: warpgroup wg's half tile in
+    // the tile's Q (wg 0) or dO (wg 1) buffer as [d/8 quads][128 rows][4]
+    const uint32_t stage = smem_u32(wg == 0 ? sm.q[slot] : sm.dO[slot]) + row * 16;
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8)
-        st_shared_v4(box + sw128_offset(lane, c8), r[c8 * 4], r[c8 * 4 + 1], r[c8 * 4 + 2], r[c8 * 4 + 3]);
-    };
-    stage_box(0, d0);
-    if (D == 128) stage_box(1, d1);
+    for (int k = 0; k < 8; ++k) st_shared_v4(stage + k * 2048, d0[4 * k], d0[4 * k + 1], d0[4 * k + 2], d0[4 * k + 3]);
+    if (D == 128) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        st_shared_v4(stage + (8 + k) * 2048, d1[4 * k], d1[4 * k + 1], d1[4 * k + 2], d1[4 * k + 3]);
+    }
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&sm.stage_full[slot]));
@@ -482,7 +493,7 @@ template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     ring_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                         const __grid_constant__ CUtensorMap tm_dqacc, const __grid_constant__ CUtensorMap tm_dkacc,
+                         const __grid_constant__ CUtensorMap tm_dkacc,
                          const __grid_constant__ CUtensorMap tm_dvacc, const BwdDev p) {
   using S = BwdSmem<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -524,7 +535,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_do);
-    tma_prefetch_desc(&tm_dqacc);
     if (p.kv_accumulate) {
       tma_prefetch_desc(&tm_dkacc);
       tma_prefetch_desc(&tm_dvacc);
@@ -546,7 +556,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int ri = 0; ri < nr; ++ri) nq += rg[2 * ri + 1] - rg[2 * ri];
     bwd_mma<D>(sm, tmem, static_cast<uint32_t>(nq), ab, p.err);
   } else if (warp == 3) {
-    if (lane == 0) bwd_dq_reducer<D>(sm, &tm_dqacc, qh, rg, nr, ab, p.err);
+    if (lane == 0) bwd_dq_reducer<D>(sm, p.dq_acc, p.Lpad, qh, rg, nr, ab, p.err);
     __syncwarp();
     named_bar_sync(1, 288);
   } else if (warp >= 4) {
@@ -559,9 +569,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // One warp per row: stores -D_i = -sum_c dO_ic o_ic and -lse_i log2(e) (0 and
-// -inf for padded rows, whose probabilities are then 0), and zeroes the row
-// of the fp32 dQ accumulator and, for rows below kv_rows, of the dK and dV
-// accumulators (grouped-query attention; null otherwise).
+// -inf for padded rows, whose probabilities are then 0), and zeroes the r-th
+// block of d floats of the fp32 dQ accumulator (whatever its layout, the
+// blocks of all rows cover it) and, for rows below kv_rows, the rows of the
+// dK and dV accumulators (grouped-query attention; null otherwise).
 template <int D>
 __global__ void __launch_bounds__(256) ring_attn_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
                                                                 const __nv_bfloat16* __restrict__ dO,
@@ -638,6 +649,31 @@ __global__ void __launch_bounds__(256) ring_attn_bwd_post_kernel(const float* __
   *reinterpret_cast<uint4*>(dq + e) = out;
 }
 
+// dq[z][i][:] = bf16(scale * dQ_acc) for rows i < L, reading the tiled
+// accumulator: thread t takes query row t % 128 of its tile and 8 columns,
+// so a warp reads two contiguous 512-byte runs.
+template <int D>
+__global__ void __launch_bounds__(256) ring_attn_bwd_dq_post_kernel(const float* __restrict__ dq_acc,
+                                                                    __nv_bfloat16* __restrict__ dq, float scale,
+                                                                    int L, int Lpad, long long n_threads) {
+  const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= n_threads) return;
+  const int r = static_cast<int>(t & 127);
+  const long long rest = t >> 7;
+  const int k8 = static_cast<int>(rest % (D / 8));  // 8-column group
+  const long long zt = rest / (D / 8);               // (z, tile)
+  const int tiles = Lpad / 128;
+  const long long z = zt / tiles;
+  const int i = static_cast<int>(zt % tiles) * 128 + r;
+  if (i >= L) return;
+  const float* src = dq_acc + dq_acc_offset<D>(z, Lpad, i, 8 * k8);
+  const float4 a = *reinterpret_cast<const float4*>(src);
+  const float4 bq = *reinterpret_cast<const float4*>(src + 512);
+  const uint4 out = make_uint4(pack_bf16(a.x * scale, a.y * scale), pack_bf16(a.z * scale, a.w * scale),
+                               pack_bf16(bq.x * scale, bq.y * scale), pack_bf16(bq.z * scale, bq.w * scale));
+  *reinterpret_cast<uint4*>(dq + (static_cast<size_t>(z) * L + i) * D + 8 * k8) = out;
+}
+
 template <int D>
 cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
   const long long rows = static_cast<long long>(a.B) * a.Hq * a.Lpad;
@@ -657,7 +693,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
   p.scale = 1.0f / sqrtf(static_cast<float>(D));
   p.scale_log2 = p.scale * kLog2e;
   p.order = a.order; p.offsets = a.offsets; p.ranges = a.ranges;
-  p.lse2 = a.lse2; p.dvec = a.Dvec;
+  p.lse2 = a.lse2; p.dvec = a.Dvec; p.dq_acc = a.dq_acc;
   p.dk = static_cast<__nv_bfloat16*>(a.dk);
   p.dv = static_cast<__nv_bfloat16*>(a.dv);
   p.err = a.err;
@@ -666,16 +702,16 @@ cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const dim3 grid(static_cast<unsigned>(a.n_blocks) * a.B * a.Hq);
   if (a.timer) a.timer->mark(2, false, stream);
-  ring_attn_bwd_kernel<D><<<grid, kBwdThreads, smem, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dqacc,
-                                                               a.tm_dkacc, a.tm_dvacc, p);
+  ring_attn_bwd_kernel<D><<<grid, kBwdThreads, smem, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dkacc,
+                                                               a.tm_dvacc, p);
   e = cudaGetLastError();
   if (a.timer) a.timer->mark(2, true, stream);
   if (e != cudaSuccess) return e;
 
-  const long long n8 = static_cast<long long>(a.B) * a.Hq * a.L * D / 8;
+  const long long nq8 = static_cast<long long>(a.B) * a.Hq * a.Lpad * D / 8;
   if (a.timer) a.timer->mark(3, false, stream);
-  ring_attn_bwd_post_kernel<D><<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, stream>>>(
-      a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), p.scale, a.L, a.Lpad, n8);
+  ring_attn_bwd_dq_post_kernel<D><<<static_cast<unsigned>((nq8 + 255) / 256), 256, 0, stream>>>(
+      a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), p.scale, a.L, a.Lpad, nq8);
   if (p.kv_accumulate) {
     const long long kv8 = static_cast<long long>(a.B) * a.Hkv * a.L * D / 8;
     const unsigned blocks = static_cast<unsigned>((kv8 + 255) / 256);

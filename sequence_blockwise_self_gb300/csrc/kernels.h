@@ -70,7 +70,7 @@ inline BwdWorkspace bwd_workspace(int B, int Hq, int Hkv, int L, int d) {
 }
 
 struct BwdArgs {
-  CUtensorMap tm_q, tm_k, tm_v, tm_do, tm_dqacc, tm_dkacc, tm_dvacc;
+  CUtensorMap tm_q, tm_k, tm_v, tm_do, tm_dkacc, tm_dvacc;
   int B, Hq, Hkv, L, Lpad, d, causal;
   int n_blocks;             // key/value tiles per (b, kv head)
   const int32_t* order;
@@ -81,7 +81,7 @@ struct BwdArgs {
   const float* lse;         // fp32 [B*Hq*L]
   float* lse2;              // workspace fp32 [B*Hq*Lpad]: -lse * log2(e), -inf padding
   float* Dvec;              // workspace fp32 [B*Hq*Lpad]: -rowsum(dO * o), 0 padding
-  float* dq_acc;            // workspace fp32 [B*Hq*Lpad*d]
+  float* dq_acc;            // workspace fp32, B*Hq*Lpad*d, tiled per 128 query rows
   float* dk_acc;            // workspace fp32 [B*Hkv*Lpad*d] (grouped-query attention only, else null)
   float* dv_acc;            // workspace fp32 [B*Hkv*Lpad*d] (grouped-query attention only, else null)
   void* dq;                 // bf16 [B*Hq*L*d]

@@ -252,8 +252,7 @@ int ring_attn_bwd(const void* q, const void* k, const void* v, const void* o, co
   const int Lpad = static_cast<int>(round_up(static_cast<size_t>(L), 128));
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   if (!make_map(&a.tm_q, q, bf, 2, d, L, B * Hq, 64) || !make_map(&a.tm_k, k, bf, 2, d, L, B * Hkv, 64) ||
-      !make_map(&a.tm_v, v, bf, 2, d, L, B * Hkv, 64) || !make_map(&a.tm_do, dO, bf, 2, d, L, B * Hq, 64) ||
-      !make_map(&a.tm_dqacc, ws + w.dq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, Lpad, B * Hq, 32, 32))
+      !make_map(&a.tm_v, v, bf, 2, d, L, B * Hkv, 64) || !make_map(&a.tm_do, dO, bf, 2, d, L, B * Hq, 64))
     return RING_ATTN_ERR_CUDA;
   if (w.kv_accumulate &&
       (!make_map(&a.tm_dkacc, ws + w.dk, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, Lpad, B * Hkv, 32, 32) ||

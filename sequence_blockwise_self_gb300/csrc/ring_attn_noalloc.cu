@@ -153,9 +153,7 @@ extern "C" int ring_attn_bwd_noalloc(const void* q, const void* k, const void* v
   std::memset(&a, 0, sizeof a);
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   if (!map3d(&a.tm_q, q, bf, 2, d, L, B * Hq, 64, 128) || !map3d(&a.tm_k, k, bf, 2, d, L, B * Hkv, 64, 128) ||
-      !map3d(&a.tm_v, v, bf, 2, d, L, B * Hkv, 64, 128) || !map3d(&a.tm_do, dO, bf, 2, d, L, B * Hq, 64, 128) ||
-      !map3d(&a.tm_dqacc, scratch + w.dq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, static_cast<int>(Lpad), B * Hq, 32,
-             32))
+      !map3d(&a.tm_v, v, bf, 2, d, L, B * Hkv, 64, 128) || !map3d(&a.tm_do, dO, bf, 2, d, L, B * Hq, 64, 128))
     return RING_ATTN_ERR_CUDA;
   if (w.kv_accumulate &&
       (!map3d(&a.tm_dkacc, scratch + w.dk, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, static_cast<int>(Lpad), B * Hkv, 32,
