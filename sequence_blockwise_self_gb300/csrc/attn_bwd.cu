@@ -208,8 +208,10 @@ __device__ void bwd_mma(BwdSmem<D>& sm, uint32_t tmem, uint32_t n_total, volatil
   for (uint32_t i = 0; i < n_total && ok; ++i) {
     const uint32_t slot = i & 1;
     const uint32_t qa = smem_u32(sm.q[slot]), da = smem_u32(sm.dO[slot]);
+    // Q(i) is refilled before dO(i) (the reduce warp returns the Q buffer
+    // first), so S^T(i) goes as soon as Q(i) and the dQ(i-1) columns are
+    // there, and dP^T(i) waits for dO(i) on its own.
     ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.q_full[slot]), (i >> 1) & 1, ab, err, kSiteBwdMma));
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.do_full[slot]), (i >> 1) & 1, ab, err, kSiteBwdMma));
     if (ok && i > 0) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.dq_free), (i - 1) & 1, ab, err, kSiteBwdMma));
     if (!ok) break;
     tc_fence_after();
@@ -222,6 +224,9 @@ __device__ void bwd_mma(BwdSmem<D>& sm, uint32_t tmem, uint32_t n_total, volatil
       const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
       umma_ss_warp(t_s, sdesc_sw128(ka + off, 16, 1024), sdesc_sw128(qa + off, 16, 1024), kIdS, kk > 0);
     }
+    ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.do_full[slot]), (i >> 1) & 1, ab, err, kSiteBwdMma));
+    if (!ok) break;
+    tc_fence_after();
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
