@@ -25,7 +25,7 @@
 //             Per query tile, five tcgen05 GEMMs:
 //               S^T  = K Q^T      (TMEM)      dP^T = V dO^T   (TMEM)
 //               dV  += P^T dO     (TMEM)      dK  += dS^T Q   (TMEM)
-//               dQ   = dS K       (TMEM, then TMA reduce-add into fp32)
+//               dQ   = dS K       (TMEM, then bulk reduce-add into fp32)
 //             P^T (bf16) goes to tensor memory, packed over dP^T columns
 //             already read, and feeds dV as the A operand; dS^T (bf16) goes
 //             to shared memory (A operand of dK, MN-major A operand of dQ).
@@ -51,14 +51,16 @@
 // on the tensor core without a gap.
 //
 // Buffers: K, V stationary; Q (with its rows' lse and D) and dO double
-// buffered; dS^T single.  The dQ drain of tile i stages fp32 boxes in the
-// Q and dO buffers of tile i once dV(i) and dK(i) have finished reading
-// them: 8 KB per compute warp, so a warp's boxes never wait on each other.
-// Warp 3 issues the TMA reduce-adds of every staged box, waits until they
-// have read shared memory and then hands the buffers back to the producer,
-// so no compute warp ever waits on a bulk copy.  (Vector atomics from
-// registers instead of TMA reduce-adds ran slower, with either row layout
-// of the accumulator.)
+// buffered; dS^T single.  The dQ drain of tile i stages fp32 in the Q and
+// dO buffers of tile i once dV(i) and dK(i) have finished reading them:
+// warpgroup 0's half tile in Q, warpgroup 1's in dO, each in the
+// accumulator's own layout.  Warp 3 adds each half into the accumulator
+// with one 1-D bulk reduce-add, waits until it has read shared memory and
+// then hands the buffer back to the producer (Q first: S^T(i+2) needs only
+// Q), so no compute warp ever waits on a bulk copy.  (Vector atomics from
+// registers instead of bulk reduce-adds ran slower, with either row layout
+// of the accumulator; both paths reduce at the same per-SM rate, ~21 B/clk
+// with every SM busy.)
 #include <cfloat>
 
 #include "kernels.h"
@@ -79,7 +81,7 @@ struct BwdSmem {
   alignas(1024) uint8_t v[kTile];
   alignas(1024) uint8_t q[2][kTile];
   alignas(1024) uint8_t dO[2][kTile];
-  alignas(1024) uint8_t dsT[128 * 128 * 2];  // also the fp32 staging of the dQ drain
+  alignas(1024) uint8_t dsT[128 * 128 * 2];
   alignas(16) float lse2[2][128];
   alignas(16) float dvec[2][128];
   alignas(8) uint64_t kv_full;
@@ -266,7 +268,7 @@ __device__ void bwd_mma(BwdSmem<D>& sm, uint32_t tmem, uint32_t n_total, volatil
 }
 
 // Warp 3, one lane: for each query tile, once the 8 compute warps have
-// staged dQ(i), issue the TMA reduce-adds of their boxes into the fp32
+// staged dQ(i), issue the bulk reduce-adds of their halves into the fp32
 // accumulator, wait until the copies have read shared memory and return
 // the tile's Q and dO buffers to the producer.  Joins the compute warps'
 // named barrier before their epilogue, all copies complete.
@@ -396,8 +398,8 @@ __device__ void bwd_compute(BwdSmem<D>& sm, uint32_t tmem, const BwdDev& p, cons
     mbar_arrive(smem_u32(&sm.ds_full));
     // dQ drain: this thread's dQ row (a query row), this half's columns,
     // leaves tensor memory in one batched load; the columns are released at
-    // once, then the row is staged as fp32 boxes in the tile's Q and dO
-    // buffers (once dV and dK have read them) for warp 3's reduce-adds into
+    // once, then the row is staged as fp32 in the tile's Q and dO buffers
+    // (once dV and dK have read them) for warp 3's reduce-adds into
     // the global accumulator.
     ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.dq_full), i & 1, ab, err, kSiteBwdSoftmax));
     if (!ok) break;
@@ -425,7 +427,7 @@ __device__ void bwd_compute(BwdSmem<D>& sm, uint32_t tmem, const BwdDev& p, cons
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&sm.stage_full[slot]));
   }
-  // Warp 3's reduce-adds have read every staging box once it joins here;
+  // Warp 3's reduce-adds have read every staged half once it joins here;
   // the dK/dV epilogue below reuses the Q and dO buffers across warps.
   named_bar_sync(1, 288);
   if (ok) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.kv_final), 0, ab, err, kSiteBwdEpilogue));
