@@ -345,9 +345,10 @@ def run_ours(args, w):
     # copies its inputs in from pinned host memory and its outputs out to
     # pinned host memory, as a training loop feeding the library would; the
     # copies run on a second stream and overlap the neighbouring steps'
-    # compute (inputs of step k+1 in, outputs of step k out), with device
-    # buffers doubled and events ordering each copy against the step that
-    # produces or consumes it.
+    # compute (inputs of step k+1 in, outputs of step k out), one stream per
+    # direction so that both copy engines work at once, with device buffers
+    # doubled and events ordering each copy against the step that produces
+    # or consumes it.
     e2e = None
     if not args.no_e2e:
         host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, lse, dq, dk, dv)]
@@ -355,19 +356,19 @@ def run_ours(args, w):
         d2h = sum(t.numel() * t.element_size() for t in host_out)
         dev_in = [[torch.empty_like(x) for x in (qd, kd, vd, dOd)] for _ in range(2)]
         dev_out = [[torch.empty_like(x) for x in (o, lse, dq, dk, dv)] for _ in range(2)]
-        copy_stream = torch.cuda.Stream(dev)
+        h2d_stream, d2h_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         ev = lambda: torch.cuda.Event()  # noqa: E731
         in_ready, in_free = [ev(), ev()], [ev(), ev()]
         out_ready, out_free = [ev(), ev()], [ev(), ev()]
 
         def copy_in(k):
             b = k % 2
-            with torch.cuda.stream(copy_stream):
+            with torch.cuda.stream(h2d_stream):
                 if k >= 2:
-                    copy_stream.wait_event(in_free[b])  # step k-2 has read these inputs
+                    h2d_stream.wait_event(in_free[b])  # step k-2 has read these inputs
                 for dst, src in zip(dev_in[b], host_in):
                     dst.copy_(src, non_blocking=True)
-                in_ready[b].record(copy_stream)
+                in_ready[b].record(h2d_stream)
 
         def run_step(k):
             b = k % 2
@@ -384,17 +385,18 @@ def run_ours(args, w):
 
         def copy_out(k):
             b = k % 2
-            with torch.cuda.stream(copy_stream):
-                copy_stream.wait_event(out_ready[b])
+            with torch.cuda.stream(d2h_stream):
+                d2h_stream.wait_event(out_ready[b])
                 for dst, src in zip(host_out, dev_out[b]):
                     dst.copy_(src, non_blocking=True)
-                out_free[b].record(copy_stream)
+                out_free[b].record(d2h_stream)
 
         barrier()
         torch.cuda.synchronize(dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        copy_stream.wait_event(e0)
+        h2d_stream.wait_event(e0)
+        d2h_stream.wait_event(e0)
         copy_in(0)
         for kstep in range(args.steps):
             if kstep + 1 < args.steps:
@@ -402,7 +404,7 @@ def run_ours(args, w):
             run_step(kstep)
             copy_out(kstep)
         done = torch.cuda.Event()
-        done.record(copy_stream)
+        done.record(d2h_stream)
         stream.wait_event(done)
         e1.record(stream)
         torch.cuda.synchronize(dev)
@@ -410,11 +412,24 @@ def run_ours(args, w):
         ms_e2e = max_over_ranks(e0.elapsed_time(e1), world, dev)
         e2e = {"value": whole_job_tflops(step_flops, args.steps, world, ms_e2e), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e / args.steps,
-               "copies": "pinned host <-> device on a second stream, overlapping the neighbouring steps"}
+               "copies": "pinned host <-> device, one stream per direction, overlapping the neighbouring steps"}
         # the last step's outputs came back intact
         if not (torch.equal(host_out[2], dev_out[(args.steps - 1) % 2][2].cpu())
                 and torch.equal(host_out[0], dev_out[(args.steps - 1) % 2][0].cpu())):
             raise RuntimeError("e2e: host copy of the last step's outputs does not match the device")
+        # link bandwidth of this machine, for reading the number: one 0.94 GB copy
+        # each way, alone
+        link = {}
+        for name, dst, src, strm in (("h2d_gbs", dev_in[0][0], host_in[0], h2d_stream),
+                                     ("d2h_gbs", host_out[2], dev_out[0][2], d2h_stream)):
+            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(strm):
+                c0.record(strm)
+                dst.copy_(src, non_blocking=True)
+                c1.record(strm)
+            c1.synchronize()
+            link[name] = src.numel() * src.element_size() / (c0.elapsed_time(c1) * 1e6)
+        e2e.update(link)
         del dev_in, dev_out
 
     # (4) CPU oracle baseline (rank 0, one GPU only)
