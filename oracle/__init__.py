@@ -12,6 +12,8 @@ from .oracle import (  # noqa: F401
     bwd,
     bwd_rows,
     ring_fwd,
+    ring_step,
+    merge,
     owner_rank,
     ring_sources,
     visible_pairs,

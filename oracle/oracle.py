@@ -54,9 +54,12 @@ def _bind(lib):
     lib.oracle_bwd_rows.argtypes = [_dp, _dp, _dp, _dp, I, I, I, I, I, I, _ip, I, _ip, I,
                                     _dp, _dp, _dp, I]
     lib.oracle_ring_fwd.argtypes = [_dp, _dp, _dp, I, I, I, I, I, I, I, _dp, _dp, I]
+    lib.oracle_ring_step.argtypes = [_dp, _dp, _dp, I, I, I, I, I, I, I, I, I, _dp, _dp, I]
+    lib.oracle_merge.argtypes = [_dp, _dp, _dp, _dp, ctypes.c_long, I]
+    lib.oracle_merge.restype = None
     lib.oracle_owner_rank.argtypes = [I, I, I, I]
     for f in (lib.oracle_fwd, lib.oracle_fwd_rows, lib.oracle_bwd, lib.oracle_bwd_rows,
-              lib.oracle_ring_fwd, lib.oracle_owner_rank):
+              lib.oracle_ring_fwd, lib.oracle_ring_step, lib.oracle_owner_rank):
         f.restype = ctypes.c_int
     return lib
 
@@ -188,6 +191,37 @@ def ring_fwd(q, k, v, causal: bool, n_chunks: int, threads: int = 0):
     lse = np.zeros((B, Hq, L))
     _check(_load().oracle_ring_fwd(_p(q), _p(k), _p(v), B, Hq, Hkv, L, d, int(causal), int(n_chunks),
                                    _p(o), _p(lse), _threads(threads)))
+    return o, lse
+
+
+def ring_step(q, k, v, causal: bool, n_chunks: int, rank: int, src: int, threads: int = 0):
+    """One ring step in isolation (SP series sections 2.3 and 6.2): the
+    partial result (o_s, lse_s) of rank `rank`'s query rows against the keys
+    and values of rank `src`.  Returned in global row order, [B,Hq,L,d] and
+    [B,Hq,L]; rows of other ranks are 0 and -inf, as are rows of `rank` that
+    see none of src's keys."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, Hq, Hkv, L, d = _shape(q, k)
+    o = np.zeros((B, Hq, L, d))
+    lse = np.full((B, Hq, L), -np.inf)
+    _check(_load().oracle_ring_step(_p(q), _p(k), _p(v), B, Hq, Hkv, L, d, int(causal), int(n_chunks),
+                                    int(rank), int(src), _p(o), _p(lse), _threads(threads)))
+    return o, lse
+
+
+def merge(o_a, lse_a, o_b, lse_b):
+    """Log-sum-exp merge of two partial results of the same rows (SP series
+    section 6.2): returns (o, lse) with lse = log(e^lse_a + e^lse_b) and
+    o = e^(lse_a - lse) o_a + e^(lse_b - lse) o_b; a side with lse = -inf
+    contributes nothing."""
+    o = np.array(o_a, dtype=np.float64, copy=True, order="C")
+    lse = np.array(lse_a, dtype=np.float64, copy=True, order="C")
+    ob = _f64(o_b)
+    lb = _f64(lse_b)
+    d = o.shape[-1]
+    if ob.shape != o.shape or lb.shape != lse.shape or o.shape[:-1] != lse.shape:
+        raise ValueError("merge: shape mismatch")
+    _load().oracle_merge(_p(o), _p(lse), _p(ob), _p(lb), int(lse.size), int(d))
     return o, lse
 
 

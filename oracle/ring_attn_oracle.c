@@ -120,6 +120,7 @@ struct task_s {
   const int *rows; int n_rows;
   double *o, *lse, *D, *dq, *dk, *dv;
   int n_chunks;
+  int rank, src;      /* ring step mode: query rank and key/value source rank */
   const int *stat_lo; /* per (b,h): first query row whose stats exist (rows mode) */
 };
 
@@ -433,6 +434,63 @@ int oracle_ring_fwd(const double *q, const double *k, const double *v, int B, in
   t.P = &P; t.n_items = (long)B * Hq * L; t.fn = ring_item; t.scratch_len = (size_t)L + d;
   t.o = o; t.lse = lse; t.n_chunks = n_chunks;
   return run_parallel(&t, n_threads);
+}
+
+/* One ring step in isolation: rank `rank`'s query rows against the keys and
+ * values rank `src` holds (at step s = (rank - src) mod N of its ring).  For
+ * every row i owned by `rank`, (o_s, lse_s) of that block; a row that sees
+ * none of src's keys (causal) gets lse_s = -inf and o_s = 0, the neutral
+ * element of the merge.  Rows of other ranks are left untouched. */
+static void step_item(task_t *t, long item, double *s) {
+  const problem_t *P = t->P;
+  const int i = (int)(item % P->L);
+  const long bh = item / P->L;
+  const int h = (int)(bh % P->Hq), b = (int)(bh / P->Hq);
+  if (owner_rank(P->L, t->n_chunks, P->causal, i) != t->rank) return;
+  double *o_s = t->o + ((size_t)bh * P->L + i) * P->d;
+  double lse_s;
+  if (!ring_block(P, t->n_chunks, b, h, i, t->src, s, o_s, &lse_s)) {
+    for (int c = 0; c < P->d; ++c) o_s[c] = 0.0;
+    lse_s = -INFINITY;
+  }
+  t->lse[(size_t)bh * P->L + i] = lse_s;
+}
+
+int oracle_ring_step(const double *q, const double *k, const double *v, int B, int Hq, int Hkv, int L, int d,
+                     int causal, int n_chunks, int rank, int src, double *o_s, double *lse_s, int n_threads) {
+  if (bad_shape(B, Hq, Hkv, L, d) || n_chunks <= 0) return -1;
+  if (L % (causal ? 2 * n_chunks : n_chunks) != 0) return -1;
+  if (rank < 0 || rank >= n_chunks || src < 0 || src >= n_chunks) return -1;
+  problem_t P = make_problem(q, k, v, NULL, B, Hq, Hkv, L, d, causal);
+  task_t t; memset(&t, 0, sizeof t);
+  t.P = &P; t.n_items = (long)B * Hq * L; t.fn = step_item; t.scratch_len = (size_t)L;
+  t.o = o_s; t.lse = lse_s; t.n_chunks = n_chunks; t.rank = rank; t.src = src;
+  return run_parallel(&t, n_threads);
+}
+
+/* The merge of two partial results of the same query rows (the log-sum-exp
+ * rule above), written out on its own: for each of n_rows rows of width d,
+ *   lse = log(exp(lse_a) + exp(lse_b)),
+ *   o   = exp(lse_a - lse) o_a + exp(lse_b - lse) o_b,
+ * into (o_a, lse_a).  A side with lse = -inf contributes nothing (both
+ * -inf: (o_a, lse_a) stay as they are). */
+void oracle_merge(double *o_a, double *lse_a, const double *o_b, const double *lse_b, long n_rows, int d) {
+  for (long r = 0; r < n_rows; ++r) {
+    double *oa = o_a + (size_t)r * d;
+    const double *ob = o_b + (size_t)r * d;
+    const double la = lse_a[r], lb = lse_b[r];
+    if (lb == -INFINITY) continue;
+    if (la == -INFINITY) {
+      for (int c = 0; c < d; ++c) oa[c] = ob[c];
+      lse_a[r] = lb;
+      continue;
+    }
+    const double hi = la > lb ? la : lb;
+    const double merged = hi + log(exp(la - hi) + exp(lb - hi));
+    const double wa = exp(la - merged), wb = exp(lb - merged);
+    for (int c = 0; c < d; ++c) oa[c] = wa * oa[c] + wb * ob[c];
+    lse_a[r] = merged;
+  }
 }
 
 int oracle_owner_rank(int L, int n_chunks, int causal, int p) {

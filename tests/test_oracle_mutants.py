@@ -14,6 +14,7 @@ import oracle
 from oracle import oracle as _oracle_mod
 
 import test_oracle_pins as pins
+import test_oracle_ring_step as steps
 
 SRC = os.path.join(os.path.dirname(pins.__file__), "..", "oracle", "ring_attn_oracle.c")
 
@@ -30,6 +31,10 @@ MUTANTS = {
     "merge_wrong_sign": ("const double a = exp(lse - merged), w = exp(lse_s - merged);",
                          "const double a = exp(lse - merged), w = exp(merged - lse_s);"),
     "fold_wrong_pair": ("return sub < N ? sub : 2 * N - 1 - sub;", "return sub < N ? sub : sub - N;"),
+    "merge_weights_swapped": ("for (int c = 0; c < d; ++c) oa[c] = wa * oa[c] + wb * ob[c];",
+                              "for (int c = 0; c < d; ++c) oa[c] = wb * oa[c] + wa * ob[c];"),
+    "step_wrong_source": ("if (!ring_block(P, t->n_chunks, b, h, i, t->src, s, o_s, &lse_s)) {",
+                          "if (!ring_block(P, t->n_chunks, b, h, i, t->rank, s, o_s, &lse_s)) {"),
     "transposed_score": ("s[j] = P->scale * dot(qi, k_row(P, b, g, j), P->d);\n    if (s[j] > m) m = s[j];\n  }\n  double sum",
                          "s[j] = P->scale * dot(q_row(P, b, h, j), k_row(P, b, g, i), P->d);\n    if (s[j] > m) m = s[j];\n  }\n  double sum"),
 }
@@ -46,6 +51,8 @@ def _quick_pins():
         ("gqa", lambda: [pins.test_gqa_equals_repeated_mha(c) for c in (False, True)]),
         ("fold", lambda: [pins.test_fold_gives_every_rank_equal_causal_work(n) for n in (2, 4)]),
         ("hand", lambda: [pins.test_hand_worked_example(m) for m in ("enc", "cau")]),
+        ("steps", lambda: [steps.test_steps_merged_in_ring_order_equal_plain(48, 3, c) for c in (False, True)]),
+        ("merge", steps.test_merge_weights_are_a_sigmoid_of_the_lse_gap),
     ]
     failed = []
     for name, fn in checks:

@@ -1,0 +1,127 @@
+"""Pins of the oracle's ring-step and merge routines (CPU).
+
+One ring step is rank r's query rows against the keys/values of rank src
+("Large-scale distributed AI model training series: sequence parallelism",
+section 2.3 Ring Self-Attention and section 6.2 Ring Attention); the merge
+is the log-sum-exp rule that combines partial results of the same rows
+(section 6.2).  They are pinned to the plain definition (every rank's steps
+merged in ring order give the full attention), to the structure of the
+fold (section 8.2) and to closed forms of the merge.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+
+
+def _problem(B, Hq, Hkv, L, d, seed):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((B, Hq, L, d))
+    k = rng.standard_normal((B, Hkv, L, d))
+    v = rng.standard_normal((B, Hkv, L, d))
+    return q, k, v
+
+
+def _rows_of(L, N, causal, r):
+    return np.array([p for p in range(L) if oracle.owner_rank(L, N, causal, p) == r])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("L,N", [(48, 2), (48, 3), (64, 4)])
+def test_steps_merged_in_ring_order_equal_plain(L, N, causal):
+    if causal and L % (2 * N):
+        pytest.skip("fold needs L % 2N == 0")
+    q, k, v = _problem(1, 4, 2, L, 8, seed=10 * L + N + causal)
+    o_ref, lse_ref = oracle.fwd(q, k, v, causal)
+    for r in range(N):
+        rows = _rows_of(L, N, causal, r)
+        o = np.zeros((1, 4, L, 8))
+        lse = np.full((1, 4, L), -np.inf)
+        for src in oracle.ring_sources(r, N):
+            o_s, lse_s = oracle.ring_step(q, k, v, causal, N, r, src)
+            o, lse = oracle.merge(o, lse, o_s, lse_s)
+        np.testing.assert_allclose(o[:, :, rows], o_ref[:, :, rows], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse[:, :, rows], lse_ref[:, :, rows], rtol=0, atol=1e-12)
+        others = np.setdiff1d(np.arange(L), rows)
+        assert np.all(lse[:, :, others] == -np.inf) and np.all(o[:, :, others] == 0)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_single_chunk_step_is_plain(causal):
+    q, k, v = _problem(2, 2, 1, 24, 16, seed=3 + causal)
+    o_ref, lse_ref = oracle.fwd(q, k, v, causal)
+    o, lse = oracle.ring_step(q, k, v, causal, 1, 0, 0)
+    np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_ref, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("N", [2, 3, 4])
+def test_causal_fold_visibility_per_step(N):
+    """With the fold, rank r's first sub-chunk (r) sees src's keys only if
+    src <= r; its second sub-chunk (2N-1-r) sees every rank's keys."""
+    c = 8
+    L = 2 * N * c
+    q, k, v = _problem(1, 1, 1, L, 4, seed=N)
+    for r in range(N):
+        first = np.arange(r * c, (r + 1) * c)
+        second = np.arange((2 * N - 1 - r) * c, (2 * N - r) * c)
+        for src in range(N):
+            _, lse = oracle.ring_step(q, k, v, True, N, r, src)
+            assert np.all(np.isfinite(lse[0, 0, second]))
+            if src <= r:
+                assert np.all(np.isfinite(lse[0, 0, first]))
+            else:
+                assert np.all(lse[0, 0, first] == -np.inf)
+
+
+def test_merge_with_itself_adds_log2():
+    rng = np.random.default_rng(0)
+    o = rng.standard_normal((5, 7))
+    lse = rng.standard_normal(5) * 10
+    o2, lse2 = oracle.merge(o, lse, o, lse)
+    np.testing.assert_allclose(o2, o, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lse2, lse + math.log(2.0), rtol=0, atol=1e-13)
+
+
+def test_merge_neutral_element():
+    rng = np.random.default_rng(1)
+    o = rng.standard_normal((4, 3))
+    lse = rng.standard_normal(4)
+    empty_o, empty_lse = np.zeros((4, 3)), np.full(4, -np.inf)
+    for a, b in (((o, lse), (empty_o, empty_lse)), ((empty_o, empty_lse), (o, lse))):
+        o2, lse2 = oracle.merge(*a, *b)
+        assert np.array_equal(o2, o) and np.array_equal(lse2, lse)
+
+
+def test_merge_weights_are_a_sigmoid_of_the_lse_gap():
+    """Merging the unit vectors e0 (weight of side a) and e1 (side b) exposes
+    the weights: 1 / (1 + e^(lse_b - lse_a)) and its complement."""
+    gaps = np.array([-30.0, -3.0, -0.5, 0.0, 0.25, 2.0, 40.0])
+    lse_a = np.full(gaps.size, 1.5)
+    lse_b = lse_a + gaps
+    o_a = np.tile([1.0, 0.0], (gaps.size, 1))
+    o_b = np.tile([0.0, 1.0], (gaps.size, 1))
+    o, lse = oracle.merge(o_a, lse_a, o_b, lse_b)
+    for n, g in enumerate(gaps):
+        wa = 1.0 / (1.0 + math.exp(g))
+        assert abs(o[n, 0] - wa) < 1e-14 and abs(o[n, 1] - (1.0 - wa)) < 1e-14
+        assert abs(lse[n] - (1.5 + math.log1p(math.exp(g)))) < 1e-12
+
+
+def test_merge_is_symmetric_and_order_free():
+    rng = np.random.default_rng(2)
+    parts = [(rng.standard_normal((6, 5)), rng.standard_normal(6) * 3) for _ in range(4)]
+    ab = oracle.merge(*parts[0], *parts[1])
+    ba = oracle.merge(*parts[1], *parts[0])
+    np.testing.assert_allclose(ab[0], ba[0], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(ab[1], ba[1], rtol=0, atol=1e-14)
+    acc = parts[0]
+    for p in parts[1:]:
+        acc = oracle.merge(*acc, *p)
+    acc2 = parts[3]
+    for p in (parts[1], parts[0], parts[2]):
+        acc2 = oracle.merge(*acc2, *p)
+    np.testing.assert_allclose(acc[0], acc2[0], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(acc[1], acc2[1], rtol=0, atol=1e-13)
