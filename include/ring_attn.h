@@ -106,6 +106,66 @@ int ring_attn_bwd_noalloc(const void* q, const void* k, const void* v, const voi
                           const void* dO, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int L, int d,
                           int n_chunks, int causal, cudaStream_t stream);
 
+/* ---------------------------------------------------------------------
+ * Ring mode: the ring run step by step, the way each rank of a multi-GPU
+ * ring runs it ("Large-scale distributed AI model training series: sequence
+ * parallelism", section 2.3 Ring Self-Attention: each device keeps its
+ * query chunk while the key/value blocks travel round the ring; section 6.2
+ * Ring Attention: each step's partial result is merged into the running one
+ * with the online-softmax correction).  Rank r holds chunk r of the
+ * sequence, in chunk order: rows [rC, (r+1)C), C = L / n_chunks, when
+ * causal == 0; sub-chunk r followed by sub-chunk 2N-1-r, each L/(2N) rows,
+ * when causal != 0 (the fold that balances causal work, section 8.2).
+ * Chunks must be whole 128-row tiles -- C (causal == 0) or L/(2N) (causal)
+ * a multiple of 128 -- else RING_ATTN_ERR_UNSUPPORTED.  Pointers are device
+ * pointers, 16-byte aligned and owned by the caller; calls are asynchronous
+ * on `stream`; argument errors return before anything is launched.
+ * ------------------------------------------------------------------- */
+
+/*
+ * One ring step of rank `rank`: the attention of its query chunk against the
+ * key/value chunk of rank `src` (the block it holds at step (rank - src) mod
+ * n_chunks), with the causal mask taken on the rows' sequence positions.
+ *   q_chunk           bf16 [B][Hq][C][d]    rank's query rows, chunk order
+ *   k_chunk, v_chunk  bf16 [B][Hkv][C][d]   src's key/value rows, chunk order
+ *   o_s               fp32 [B][Hq][C][d]    out: the partial result, normalised
+ *                                           over src's keys alone
+ *   lse_s             fp32 [B][Hq][C]       out: its log-sum-exp (natural log);
+ *                                           a row that sees none of src's keys
+ *                                           gets lse_s = -inf and o_s = 0
+ */
+int ring_attn_fwd_step(const void* q_chunk, const void* k_chunk, const void* v_chunk, float* o_s, float* lse_s,
+                       int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal, int rank, int src,
+                       cudaStream_t stream);
+
+/*
+ * Merge of two partial results of the same n_rows rows of width d (64 or
+ * 128), in place: lse <- log(e^lse + e^lse_s), o <- e^(lse_old - lse) o +
+ * e^(lse_s - lse) o_s; a side with lse = -inf contributes nothing.  o, o_s
+ * fp32 [n_rows][d], lse, lse_s fp32 [n_rows].  If o_out is not NULL, bf16(o)
+ * is written there as well ([n_rows][d]), e.g. after the last step.
+ */
+int ring_attn_merge(float* o, float* lse, const float* o_s, const float* lse_s, long long n_rows, int d,
+                    void* o_out, cudaStream_t stream);
+
+/* Workspace bytes ring_attn_ring_fwd needs for this shape, or 0 if invalid. */
+size_t ring_attn_ring_fwd_workspace_size(int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal);
+
+/*
+ * The whole ring on one GPU, every rank of it, the ring-mode way: q, k, v
+ * (sequence order, as for ring_attn_fwd) are gathered into chunk order; at
+ * each step s = 0..n_chunks-1 one launch runs every rank's step (rank r
+ * against rank (r - s) mod n_chunks) and the merge folds it into the running
+ * fp32 result; the result is scattered back to sequence order into o (bf16)
+ * and lse (fp32), as ring_attn_fwd writes them.  `workspace` (caller-owned
+ * device memory of ring_attn_ring_fwd_workspace_size() bytes, 256-byte
+ * aligned) holds the gathered chunks, the running result and one step's
+ * partial result.
+ */
+int ring_attn_ring_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                       int L, int d, int n_chunks, int causal, void* workspace, size_t workspace_bytes,
+                       cudaStream_t stream);
+
 /* Static description of a status code. */
 const char* ring_attn_strerror(int status);
 
@@ -139,7 +199,10 @@ enum {
   RING_ATTN_KERNEL_BWD_PRE = 1,  /* backward pre-pass: D, log2 lse, zero dq accumulator */
   RING_ATTN_KERNEL_BWD_MAIN = 2, /* fused backward kernel */
   RING_ATTN_KERNEL_BWD_POST = 3, /* dq accumulator -> bf16 */
-  RING_ATTN_N_KERNELS = 4
+  RING_ATTN_KERNEL_RING_STEP = 4,  /* ring mode: one step of attention (every rank or one) */
+  RING_ATTN_KERNEL_RING_MERGE = 5, /* ring mode: log-sum-exp merge */
+  RING_ATTN_KERNEL_RING_IO = 6,    /* ring mode: gather into / scatter out of chunk order */
+  RING_ATTN_N_KERNELS = 7
 };
 int ring_attn_profile_enable(int on);
 int ring_attn_profile_read(double* ms, long long* launches);
@@ -178,6 +241,18 @@ int ring_attn_fwd_plan(int L, int n_chunks, int causal, int* n_blocks, int* n_ra
  */
 int ring_attn_bwd_plan(int L, int n_chunks, int causal, int* n_blocks, int* n_ranges, int32_t* block_order,
                        int32_t* range_offsets, int32_t* ranges);
+
+/*
+ * Ring-mode step plan of rank `rank` at ring step `step` (it then holds the
+ * key/value chunk of rank (rank - step) mod n_chunks): for each 256-row
+ * block of the rank's chunk (chunk-order rows), the 128-row tiles of the
+ * source chunk (chunk-order indices, ascending) holding a key some row of
+ * the block may see; a block may list none.  Same array conventions as
+ * ring_attn_fwd_plan, with n_blocks = blocks of one chunk.  Chunks must be
+ * whole 128-row tiles (see ring mode above).
+ */
+int ring_attn_step_plan(int L, int n_chunks, int causal, int step, int rank, int* n_blocks, int* n_ranges,
+                        int32_t* block_order, int32_t* range_offsets, int32_t* ranges);
 
 #ifdef __cplusplus
 }

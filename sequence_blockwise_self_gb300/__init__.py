@@ -4,7 +4,9 @@ Public API (torch tensors in, torch tensors out; the arithmetic runs in the
 library's CUDA kernels):
     ring_attn_fwd(q, k, v, n_chunks, causal) -> (o, lse)
     ring_attn_bwd(q, k, v, o, lse, dO, n_chunks, causal) -> (dq, dk, dv)
-Host-only queries: owner_rank, fwd_plan, bwd_plan.
+Ring mode (the ring run step by step, as each rank of a multi-GPU ring
+would): ring_attn_fwd_step, ring_attn_merge, ring_attn_ring_fwd.
+Host-only queries: owner_rank, fwd_plan, bwd_plan, step_plan.
 """
 from .capi import (  # noqa: F401
     RingAttnError,
@@ -18,8 +20,13 @@ from .capi import (  # noqa: F401
     profile_read,
     release,
     selftest_bounded_wait,
+    step_plan,
     ring_attn_bwd,
     ring_attn_bwd_noalloc,
     ring_attn_fwd,
+    ring_attn_fwd_step,
+    ring_attn_merge,
+    ring_attn_ring_fwd,
+    ring_fwd_workspace_size,
     strerror,
 )

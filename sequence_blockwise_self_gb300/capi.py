@@ -71,6 +71,16 @@ def load():
     for f in (lib.ring_attn_fwd_plan, lib.ring_attn_bwd_plan):
         f.argtypes = [I, I, I, IP, IP, I32P, I32P, I32P]
         f.restype = I
+    lib.ring_attn_step_plan.argtypes = [I, I, I, I, I, IP, IP, I32P, I32P, I32P]
+    lib.ring_attn_step_plan.restype = I
+    lib.ring_attn_fwd_step.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, P]
+    lib.ring_attn_fwd_step.restype = I
+    lib.ring_attn_merge.argtypes = [P, P, P, P, ctypes.c_longlong, I, P, P]
+    lib.ring_attn_merge.restype = I
+    lib.ring_attn_ring_fwd_workspace_size.argtypes = [I, I, I, I, I, I, I]
+    lib.ring_attn_ring_fwd_workspace_size.restype = S
+    lib.ring_attn_ring_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, P, S, P]
+    lib.ring_attn_ring_fwd.restype = I
     _lib = lib
     return lib
 
@@ -101,6 +111,13 @@ def _plan(fn, L, n_chunks, causal):
     visits = [[(int(ranges[2 * r]), int(ranges[2 * r + 1])) for r in range(offsets[u], offsets[u + 1])]
               for u in range(nb.value)]
     return {"order": order, "offsets": offsets, "ranges": ranges, "visits": visits}
+
+
+def step_plan(L: int, n_chunks: int, causal: bool, step: int, rank: int):
+    """Ring mode: per 256-row block of rank's chunk, the source chunk's tile
+    ranges it visits at this step (chunk-local indices)."""
+    fn = load().ring_attn_step_plan
+    return _plan(lambda L_, N_, c_, *rest: fn(L_, N_, c_, int(step), int(rank), *rest), L, n_chunks, causal)
 
 
 def fwd_plan(L: int, n_chunks: int, causal: bool):
@@ -156,6 +173,77 @@ def ring_attn_fwd(q, k, v, n_chunks: int, causal: bool, o=None, lse=None, stream
                               int(bool(causal)), _stream(stream))
     if rc != OK:
         raise RingAttnError(rc, "ring_attn_fwd")
+    return o, lse
+
+
+# ------------------------------------------------------------------ ring mode
+
+def ring_attn_fwd_step(q_chunk, k_chunk, v_chunk, n_chunks: int, causal: bool, rank: int, src: int, o_s=None,
+                       lse_s=None, stream=None):
+    """One ring step of rank `rank` against the key/value chunk of rank `src`
+    (chunks in chunk order, see include/ring_attn.h); returns the fp32
+    partial result (o_s [B,Hq,C,d], lse_s [B,Hq,C])."""
+    import torch
+    B, Hq, C, d = q_chunk.shape
+    Hkv = k_chunk.shape[1]
+    _check_tensor(q_chunk, "q_chunk", torch.bfloat16, (B, Hq, C, d))
+    _check_tensor(k_chunk, "k_chunk", torch.bfloat16, (B, Hkv, C, d))
+    _check_tensor(v_chunk, "v_chunk", torch.bfloat16, (B, Hkv, C, d))
+    o_s = torch.empty((B, Hq, C, d), dtype=torch.float32, device=q_chunk.device) if o_s is None else o_s
+    lse_s = torch.empty((B, Hq, C), dtype=torch.float32, device=q_chunk.device) if lse_s is None else lse_s
+    _check_tensor(o_s, "o_s", torch.float32, (B, Hq, C, d))
+    _check_tensor(lse_s, "lse_s", torch.float32, (B, Hq, C))
+    rc = load().ring_attn_fwd_step(_ptr(q_chunk), _ptr(k_chunk), _ptr(v_chunk), _ptr(o_s), _ptr(lse_s), B, Hq, Hkv,
+                                   C * int(n_chunks), d, int(n_chunks), int(bool(causal)), int(rank), int(src),
+                                   _stream(stream))
+    if rc != OK:
+        raise RingAttnError(rc, "ring_attn_fwd_step")
+    return o_s, lse_s
+
+
+def ring_attn_merge(o, lse, o_s, lse_s, o_out=None, stream=None):
+    """In place: (o, lse) <- log-sum-exp merge of (o, lse) and (o_s, lse_s)
+    (fp32, [..., d] and [...]); optionally bf16(o) into o_out.  Returns (o, lse)."""
+    import torch
+    d = o.shape[-1]
+    rows = lse.numel()
+    _check_tensor(o, "o", torch.float32, tuple(lse.shape) + (d,))
+    _check_tensor(lse, "lse", torch.float32, tuple(lse.shape))
+    _check_tensor(o_s, "o_s", torch.float32, tuple(o.shape))
+    _check_tensor(lse_s, "lse_s", torch.float32, tuple(lse.shape))
+    if o_out is not None:
+        _check_tensor(o_out, "o_out", torch.bfloat16, tuple(o.shape))
+    rc = load().ring_attn_merge(_ptr(o), _ptr(lse), _ptr(o_s), _ptr(lse_s), rows, d, _ptr(o_out), _stream(stream))
+    if rc != OK:
+        raise RingAttnError(rc, "ring_attn_merge")
+    return o, lse
+
+
+def ring_fwd_workspace_size(B, Hq, Hkv, L, d, n_chunks, causal) -> int:
+    return int(load().ring_attn_ring_fwd_workspace_size(B, Hq, Hkv, L, d, int(n_chunks), int(bool(causal))))
+
+
+def ring_attn_ring_fwd(q, k, v, n_chunks: int, causal: bool, o=None, lse=None, workspace=None, stream=None):
+    """The forward of ring_attn_fwd computed the ring-mode way (every rank's
+    steps as separate launches, merged step by step); returns (o, lse)."""
+    import torch
+    B, Hq, L, d = q.shape
+    Hkv = k.shape[1]
+    _check_tensor(q, "q", torch.bfloat16, (B, Hq, L, d))
+    _check_tensor(k, "k", torch.bfloat16, (B, Hkv, L, d))
+    _check_tensor(v, "v", torch.bfloat16, (B, Hkv, L, d))
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, Hq, L), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check_tensor(o, "o", torch.bfloat16, (B, Hq, L, d))
+    _check_tensor(lse, "lse", torch.float32, (B, Hq, L))
+    ws_bytes = ring_fwd_workspace_size(B, Hq, Hkv, L, d, n_chunks, causal)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
+    rc = load().ring_attn_ring_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, L, d, int(n_chunks),
+                                   int(bool(causal)), _ptr(workspace),
+                                   int(workspace.numel() * workspace.element_size()), _stream(stream))
+    if rc != OK:
+        raise RingAttnError(rc, "ring_attn_ring_fwd")
     return o, lse
 
 
@@ -221,7 +309,7 @@ def device_status(stream=None):
     return rc, site.value
 
 
-KERNEL_NAMES = ("fwd", "bwd_pre", "bwd_main", "bwd_post")
+KERNEL_NAMES = ("fwd", "bwd_pre", "bwd_main", "bwd_post", "ring_step", "ring_merge", "ring_io")
 
 
 def profile_enable(on: bool = True):

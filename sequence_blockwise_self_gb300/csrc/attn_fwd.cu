@@ -66,14 +66,32 @@ struct FwdSmem {
 };
 
 struct FwdDev {
-  int B, Hq, Hkv, L, causal;
+  int B, Hq, Hkv, L, causal;  // L: rows of one (batch, head) slice (step mode: the chunk length C)
   float scale_log2;
   const int32_t* order;
   const int32_t* offsets;
   const int32_t* ranges;
   float* lse;
   int* err;
+  // Ring step mode (step_nb > 0): item k = 256-row block k % step_nb of rank
+  // rank_lo + k / step_nb's chunk, against the chunk of rank (r - step) mod
+  // n_chunks.  Slice z of q, o, lse is r * z_rank * B*Hq + (b, h), of k, v
+  // src * z_rank * B*Hkv + (b, kv head): z_rank = 1 for chunk-major buffers
+  // holding every rank, 0 for buffers holding one chunk.  The output is the
+  // normalised partial result in fp32 (o32 / the fp32 output map).
+  int step_nb, step, rank_lo, n_chunks, sub_len, z_rank;
+  float* o32;
 };
+
+// Sequence position of row `local` of rank `rank`'s chunk, as far as the
+// causal mask needs it (the fold: sub-chunks `rank` and 2N-1-rank of
+// sub_len rows); rows of the whole sequence are their own positions.
+template <bool kStep>
+__device__ __forceinline__ int seq_pos(const FwdDev& p, int rank, int local) {
+  if (!kStep || !p.causal) return local;
+  return local < p.sub_len ? rank * p.sub_len + local
+                           : (2 * p.n_chunks - 1 - rank) * p.sub_len + (local - p.sub_len);
+}
 
 // Wait that ignores the abort flag (used to drain in-flight copies/MMAs
 // after an abort), still bounded in time.
@@ -199,13 +217,15 @@ __device__ void fwd_mma(FwdSmem<D>& sm, uint32_t tmem, int nkv, volatile int* ab
   }
 }
 
-template <int D>
+template <int D, bool kStep>
 __device__ void fwd_softmax(FwdSmem<D>& sm, uint32_t tmem, int t, const FwdDev& p, const CUtensorMap* tm_o,
-                            int q0, int q_z, const int32_t* rg, int nr, volatile int* ab, int* err) {
+                            int q0, int q_z, int q_rank, int kv_rank, const int32_t* rg, int nr, volatile int* ab,
+                            int* err) {
   const int wq = (threadIdx.x >> 5) & 3;  // TMEM lane quadrant of this warp
   const int lane = threadIdx.x & 31;
   const int row = wq * 32 + lane;
-  const int qpos = q0 + 128 * t + row;
+  const int qpos = q0 + 128 * t + row;        // row of the slice
+  const int qseq = seq_pos<kStep>(p, q_rank, qpos);  // its sequence position (causal mask)
   const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
   const uint32_t t_s = tmem + 128 * t + lane_off;
   const uint32_t t_o = tmem + 256 + 128 * t + lane_off;
@@ -237,8 +257,9 @@ __device__ void fwd_softmax(FwdSmem<D>& sm, uint32_t tmem, int t, const FwdDev& 
         s[96 + i] = __uint_as_float(r3[i]);
       }
       const int kv0 = jt * 128;
-      if (kv0 + 128 > p.L || (p.causal && kv0 + 127 > qpos)) {
-        const int lim = min(p.L - 1, p.causal ? qpos : INT_MAX) - kv0;  // valid columns: i <= lim
+      const int kvseq = seq_pos<kStep>(p, kv_rank, kv0);  // tiles never straddle a sub-chunk
+      if (kv0 + 128 > p.L || (p.causal && kvseq + 127 > qseq)) {
+        const int lim = min(p.L - 1 - kv0, p.causal ? qseq - kvseq : INT_MAX);  // valid columns: i <= lim
 #pragma unroll
         for (int i = 0; i < 128; ++i)
           if (i > lim) s[i] = -INFINITY;
@@ -312,35 +333,55 @@ __device__ void fwd_softmax(FwdSmem<D>& sm, uint32_t tmem, int t, const FwdDev& 
   if (ok) {
     tc_fence_after();
     const float inv = l > 0.f ? 1.f / l : 0.f;
-    // Normalised O row -> bf16 -> the staging slot (see above), laid out as
-    // the 128-byte-swizzled boxes of the output tensor map.
-    auto emit = [&](int c0, const uint32_t (&r)[32]) {
+    if constexpr (kStep) {
+      // Ring step: the normalised partial O row in fp32, as 32-column boxes
+      // of 128-byte rows: boxes 0 .. d/64-1 in the dead Q_t buffer, the rest
+      // in the free key/value slot (Q_t was last read by S_t(last), which
+      // o_final covers).
+      const uint32_t qbase = smem_u32(sm.q[t]);
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const int ch = c0 * 4 + q4;
-        const float* f = reinterpret_cast<const float*>(r) + q4 * 8;
-        st_shared_v4(pbase + (ch >> 3) * 16384 + sw128_offset(row, ch & 7), pack_bf16(f[0] * inv, f[1] * inv),
-                     pack_bf16(f[2] * inv, f[3] * inv), pack_bf16(f[4] * inv, f[5] * inv),
-                     pack_bf16(f[6] * inv, f[7] * inv));
+      for (int c0 = 0; c0 < D / 32; ++c0) {
+        uint32_t r[32];
+        tmem_ld32(t_o + c0 * 32, r);
+        const uint32_t box = (c0 < D / 64 ? qbase + c0 * 16384 : pbase + (c0 - D / 64) * 16384);
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch)
+          st_shared_v4(box + sw128_offset(row, ch), __float_as_uint(__uint_as_float(r[4 * ch]) * inv),
+                       __float_as_uint(__uint_as_float(r[4 * ch + 1]) * inv),
+                       __float_as_uint(__uint_as_float(r[4 * ch + 2]) * inv),
+                       __float_as_uint(__uint_as_float(r[4 * ch + 3]) * inv));
       }
-    };
-    {
-      uint32_t r0[32], r1[32];
-      tmem_ld32_async(t_o, r0);
-      tmem_ld32_async(t_o + 32, r1);
-      tmem_wait_ld(r0);
-      reg_fence(r1);
-      emit(0, r0);
-      emit(1, r1);
-    }
-    if (D == 128) {
-      uint32_t r2[32], r3[32];
-      tmem_ld32_async(t_o + 64, r2);
-      tmem_ld32_async(t_o + 96, r3);
-      tmem_wait_ld(r2);
-      reg_fence(r3);
-      emit(2, r2);
-      emit(3, r3);
+    } else {
+      // Normalised O row -> bf16 -> the staging slot (see above), laid out as
+      // the 128-byte-swizzled boxes of the output tensor map.
+      auto emit = [&](int c0, const uint32_t (&r)[32]) {
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int ch = c0 * 4 + q4;
+          const float* f = reinterpret_cast<const float*>(r) + q4 * 8;
+          st_shared_v4(pbase + (ch >> 3) * 16384 + sw128_offset(row, ch & 7), pack_bf16(f[0] * inv, f[1] * inv),
+                       pack_bf16(f[2] * inv, f[3] * inv), pack_bf16(f[4] * inv, f[5] * inv),
+                       pack_bf16(f[6] * inv, f[7] * inv));
+        }
+      };
+      {
+        uint32_t r0[32], r1[32];
+        tmem_ld32_async(t_o, r0);
+        tmem_ld32_async(t_o + 32, r1);
+        tmem_wait_ld(r0);
+        reg_fence(r1);
+        emit(0, r0);
+        emit(1, r1);
+      }
+      if (D == 128) {
+        uint32_t r2[32], r3[32];
+        tmem_ld32_async(t_o + 64, r2);
+        tmem_ld32_async(t_o + 96, r3);
+        tmem_wait_ld(r2);
+        reg_fence(r3);
+        emit(2, r2);
+        emit(3, r3);
+      }
     }
     if (qpos < p.L) p.lse[static_cast<size_t>(q_z) * p.L + qpos] = (m + log2f(l)) * kLn2;
     fence_proxy_async_smem();
@@ -348,13 +389,20 @@ __device__ void fwd_softmax(FwdSmem<D>& sm, uint32_t tmem, int t, const FwdDev& 
   tc_fence_before();
   named_bar_sync(1 + t, 128);
   if (ok && row == 0 && q0 + 128 * t < p.L) {  // no store for a tile wholly past the end
-    for (int sub = 0; sub < FwdSmem<D>::kSub; ++sub) tma_store_3d(tm_o, pbase + sub * 16384, sub * 64, q0 + 128 * t, q_z);
+    if constexpr (kStep) {
+      for (int c0 = 0; c0 < D / 32; ++c0)
+        tma_store_3d(tm_o, c0 < D / 64 ? smem_u32(sm.q[t]) + c0 * 16384 : pbase + (c0 - D / 64) * 16384, 32 * c0,
+                     q0 + 128 * t, q_z);
+    } else {
+      for (int sub = 0; sub < FwdSmem<D>::kSub; ++sub)
+        tma_store_3d(tm_o, pbase + sub * 16384, sub * 64, q0 + 128 * t, q_z);
+    }
     bulk_commit_group();
     bulk_wait_group<0>();
   }
 }
 
-template <int D>
+template <int D, bool kStep>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     ring_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -368,13 +416,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   S& sm = *reinterpret_cast<S*>(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int BH = p.B * p.Hq;
-  const int u = p.order[blockIdx.x / BH];
+  const int item = p.order[blockIdx.x / BH];
   const int bh = blockIdx.x % BH;
   const int b = bh / p.Hq, h = bh % p.Hq;
-  const int kv_z = b * p.Hkv + h / (p.Hq / p.Hkv);
+  int u = item, q_rank = 0, kv_rank = 0;
+  int q_z = bh, kv_z = b * p.Hkv + h / (p.Hq / p.Hkv);
+  if constexpr (kStep) {
+    q_rank = p.rank_lo + item / p.step_nb;
+    u = item % p.step_nb;
+    kv_rank = ((q_rank - p.step) % p.n_chunks + p.n_chunks) % p.n_chunks;
+    q_z += q_rank * p.z_rank * BH;
+    kv_z += kv_rank * p.z_rank * (p.B * p.Hkv);
+  }
   const int q0 = u * 256;
-  const int32_t* rg = p.ranges + 2 * p.offsets[u];
-  const int nr = p.offsets[u + 1] - p.offsets[u];
+  const int32_t* rg = p.ranges + 2 * p.offsets[item];
+  const int nr = p.offsets[item + 1] - p.offsets[item];
+  int nkv = 0;
+  for (int ri = 0; ri < nr; ++ri) nkv += rg[2 * ri + 1] - rg[2 * ri];
   volatile int* ab = &sm.abort_flag;
 
   if (threadIdx.x == 0) {
@@ -405,15 +463,25 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
 
-  if (warp == 0) {
-    if (lane == 0) fwd_producer<D>(sm, &tm_q, &tm_k, &tm_v, q0, bh, kv_z, rg, nr, ab, p.err);
+  if (kStep && nkv == 0) {
+    // A ring-step block that sees none of the source's keys (causal): its
+    // partial result is the merge's neutral element, o = 0, lse = -inf.
+    if (warp >= 4) {
+      const int qpos = q0 + 128 * ((warp - 4) >> 2) + (threadIdx.x & 127);
+      if (qpos < p.L) {
+        float4* dst = reinterpret_cast<float4*>(p.o32 + (static_cast<size_t>(q_z) * p.L + qpos) * D);
+#pragma unroll 4
+        for (int x = 0; x < D / 4; ++x) dst[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+        p.lse[static_cast<size_t>(q_z) * p.L + qpos] = -INFINITY;
+      }
+    }
+  } else if (warp == 0) {
+    if (lane == 0) fwd_producer<D>(sm, &tm_q, &tm_k, &tm_v, q0, q_z, kv_z, rg, nr, ab, p.err);
   } else if (warp == 1) {
     // the whole warp runs the issue loop; one elected lane issues
-    int nkv = 0;
-    for (int ri = 0; ri < nr; ++ri) nkv += rg[2 * ri + 1] - rg[2 * ri];
     fwd_mma<D>(sm, tmem, nkv, ab, p.err);
   } else if (warp >= 4) {
-    fwd_softmax<D>(sm, tmem, (warp - 4) >> 2, p, &tm_o, q0, bh, rg, nr, ab, p.err);
+    fwd_softmax<D, kStep>(sm, tmem, (warp - 4) >> 2, p, &tm_o, q0, q_z, q_rank, kv_rank, rg, nr, ab, p.err);
   }
   tc_fence_before();
   __syncthreads();
@@ -456,16 +524,20 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
   p.scale_log2 = kLog2e / sqrtf(static_cast<float>(a.d));
   p.order = a.order; p.offsets = a.offsets; p.ranges = a.ranges;
   p.lse = a.lse; p.err = a.err;
+  p.step_nb = a.step_nb; p.step = a.step; p.rank_lo = a.rank_lo; p.n_chunks = a.n_chunks;
+  p.sub_len = a.sub_len; p.z_rank = a.z_rank; p.o32 = a.o32;
   const size_t smem = fwd_smem_bytes(a.d);
   const dim3 grid(static_cast<unsigned>(a.n_blocks) * a.B * a.Hq);
   cudaError_t e;
-  auto kernel = a.d == 128 ? ring_attn_fwd_kernel<128> : ring_attn_fwd_kernel<64>;
+  auto kernel = a.step_nb ? (a.d == 128 ? ring_attn_fwd_kernel<128, true> : ring_attn_fwd_kernel<64, true>)
+                          : (a.d == 128 ? ring_attn_fwd_kernel<128, false> : ring_attn_fwd_kernel<64, false>);
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  if (a.timer) a.timer->mark(0, false, stream);
+  const int kind = a.step_nb ? 4 : 0;  // profiling kinds of include/ring_attn.h: forward / ring step
+  if (a.timer) a.timer->mark(kind, false, stream);
   kernel<<<grid, kFwdThreads, smem, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, p);
   e = cudaGetLastError();
-  if (a.timer) a.timer->mark(0, true, stream);
+  if (a.timer) a.timer->mark(kind, true, stream);
   return e;
 }
 

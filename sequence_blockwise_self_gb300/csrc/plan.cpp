@@ -90,4 +90,33 @@ Plan build_bwd_plan(int L, int N, bool causal) {
   return p;
 }
 
+Plan build_step_plan(int L, int N, bool causal, int step, int rank_lo, int rank_hi) {
+  Plan p;
+  const int C = L / N;
+  const int nt = C / kTileRows;                       // tiles per chunk
+  const int nb = (C + kQBlockRows - 1) / kQBlockRows;  // 256-row blocks per chunk
+  p.n_blocks = (rank_hi - rank_lo) * nb;
+  p.offsets.push_back(0);
+  std::vector<int> tiles;
+  for (int r = rank_lo; r < rank_hi; ++r) {
+    const int src = ((r - step) % N + N) % N;
+    for (int u = 0; u < nb; ++u) {
+      tiles.clear();
+      int q_tiles = 0;
+      for (int qt = 2 * u; qt < 2 * u + 2 && qt < nt; ++qt) ++q_tiles;
+      for (int kt = 0; kt < nt; ++kt) {
+        bool seen = !causal;
+        for (int qt = 2 * u; qt < 2 * u + 2 && qt < nt && !seen; ++qt)
+          seen = chunk_pos(L, N, true, src, kt * kTileRows) <= chunk_pos(L, N, true, r, qt * kTileRows + kTileRows - 1);
+        if (seen) tiles.push_back(kt);
+      }
+      append_ranges(tiles, p.ranges);
+      p.offsets.push_back(static_cast<int32_t>(p.ranges.size() / 2));
+      p.work.push_back(static_cast<int64_t>(tiles.size()) * q_tiles);
+    }
+  }
+  finish(p);
+  return p;
+}
+
 }  // namespace ra

@@ -15,6 +15,12 @@
 #include <cstdint>
 #include <vector>
 
+#ifdef __CUDACC__
+#define RA_HOST_DEVICE __host__ __device__
+#else
+#define RA_HOST_DEVICE
+#endif
+
 namespace ra {
 
 constexpr int kTileRows = 128;      // rows per query / key-value tile
@@ -52,5 +58,32 @@ Plan build_fwd_plan(int L, int N, bool causal);
 // the order the block meets them going round the ring: its own rank first,
 // then ranks r + 1, r + 2, ... mod N.
 Plan build_bwd_plan(int L, int N, bool causal);
+
+// ----------------------------------------------------------- ring step mode
+// One ring step run explicitly, as each rank of a multi-GPU ring would: rank
+// r holds its chunk of C = L/N rows in chunk order (encoder: rows [rC,
+// (r+1)C); causal: sub-chunk r, then sub-chunk 2N-1-r, each L/(2N) rows),
+// and at step s the key/value chunk of rank (r - s) mod N.
+
+// Chunks must be whole 128-row tiles: C (encoder) or the sub-chunk length
+// (causal) a multiple of 128.
+inline bool step_chunking_ok(int L, int N, bool causal) {
+  if (!chunking_ok(L, N, causal)) return false;
+  return (causal ? L / (2 * N) : L / N) % kTileRows == 0;
+}
+
+// Sequence position of row `local` of rank `rank`'s chunk.
+RA_HOST_DEVICE inline int chunk_pos(int L, int N, bool causal, int rank, int local) {
+  if (!causal) return rank * (L / N) + local;
+  const int c = L / (2 * N);
+  return local < c ? rank * c + local : (2 * N - 1 - rank) * c + (local - c);
+}
+
+// Step s for ranks [rank_lo, rank_hi): item k is 256-row block k % nb of
+// rank rank_lo + k / nb's chunk (nb = ceil(C / 256)); it lists the tiles of
+// the source rank's key/value chunk (chunk-local indices, ascending) that
+// hold a key some query row of the block may see.  An item may list none
+// (a causal block entirely before the source's keys).
+Plan build_step_plan(int L, int N, bool causal, int step, int rank_lo, int rank_hi);
 
 }  // namespace ra

@@ -30,6 +30,8 @@ struct DevicePlan {
 };
 
 std::map<std::tuple<int, int, int, int, int>, DevicePlan> g_plans;  // (device, kind, L, N, causal)
+// ring step plans: (device, L, N, causal, step, first rank, end rank)
+std::map<std::tuple<int, int, int, int, int, int, int>, DevicePlan> g_step_plans;
 std::map<int, int*> g_status_ptr;                                   // device -> &g_device_status
 
 // Event pairs around launches while profiling is on.
@@ -99,15 +101,9 @@ int check_shape(int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal) 
 
 int current_device(int* dev) { return cudaGetDevice(dev) == cudaSuccess ? RING_ATTN_OK : RING_ATTN_ERR_CUDA; }
 
-// Device copy of a plan, built and uploaded on first use of a shape.
-int get_plan(int dev, int kind, int L, int N, int causal, DevicePlan* out) {
-  auto key = std::make_tuple(dev, kind, L, N, causal);
-  auto it = g_plans.find(key);
-  if (it != g_plans.end()) {
-    *out = it->second;
-    return RING_ATTN_OK;
-  }
-  Plan p = kind == 0 ? build_fwd_plan(L, N, causal != 0) : build_bwd_plan(L, N, causal != 0);
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int upload_plan(const Plan& p, DevicePlan* out) {
   std::vector<int32_t> flat;
   flat.insert(flat.end(), p.order.begin(), p.order.end());
   flat.insert(flat.end(), p.offsets.begin(), p.offsets.end());
@@ -119,6 +115,21 @@ int get_plan(int dev, int kind, int L, int N, int causal, DevicePlan* out) {
     cudaFree(dp.dev);
     return RING_ATTN_ERR_CUDA;
   }
+  *out = dp;
+  return RING_ATTN_OK;
+}
+
+// Device copy of a plan, built and uploaded on first use of a shape.
+int get_plan(int dev, int kind, int L, int N, int causal, DevicePlan* out) {
+  auto key = std::make_tuple(dev, kind, L, N, causal);
+  auto it = g_plans.find(key);
+  if (it != g_plans.end()) {
+    *out = it->second;
+    return RING_ATTN_OK;
+  }
+  DevicePlan dp;
+  int rc = upload_plan(kind == 0 ? build_fwd_plan(L, N, causal != 0) : build_bwd_plan(L, N, causal != 0), &dp);
+  if (rc != RING_ATTN_OK) return rc;
   g_plans[key] = dp;
   *out = dp;
   return RING_ATTN_OK;
@@ -137,7 +148,79 @@ int status_ptr(int dev, int** out) {
   return RING_ATTN_OK;
 }
 
-size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+int get_step_plan(int dev, int L, int N, int causal, int step, int rank_lo, int rank_hi, DevicePlan* out) {
+  auto key = std::make_tuple(dev, L, N, causal, step, rank_lo, rank_hi);
+  auto it = g_step_plans.find(key);
+  if (it != g_step_plans.end()) {
+    *out = it->second;
+    return RING_ATTN_OK;
+  }
+  DevicePlan dp;
+  int rc = upload_plan(build_step_plan(L, N, causal != 0, step, rank_lo, rank_hi), &dp);
+  if (rc != RING_ATTN_OK) return rc;
+  g_step_plans[key] = dp;
+  *out = dp;
+  return RING_ATTN_OK;
+}
+
+int check_ring_shape(int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal) {
+  int rc = check_shape(B, Hq, Hkv, L, d, n_chunks, causal);
+  if (rc != RING_ATTN_OK) return rc;
+  if (L > 0 && !step_chunking_ok(L, n_chunks, causal != 0)) return RING_ATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(n_chunks) * B * Hq >= 65536) return RING_ATTN_ERR_UNSUPPORTED;
+  return RING_ATTN_OK;
+}
+
+// Launch one ring step for ranks [rank_lo, rank_hi) on chunk buffers: with
+// z_rank = 1 the buffers hold every rank's chunk ([N][B][H][C][d]), with
+// z_rank = 0 only the chunks of the one rank and its source.
+int launch_step(int dev, const void* q, const void* k, const void* v, float* o_s, float* lse_s, int B, int Hq,
+                int Hkv, int L, int d, int N, int causal, int step, int rank_lo, int rank_hi, int z_rank,
+                cudaStream_t stream) {
+  const int C = L / N;
+  const int zq = (z_rank ? N : 1) * B * Hq, zkv = (z_rank ? N : 1) * B * Hkv;
+  FwdArgs a;
+  std::memset(&a, 0, sizeof a);
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (!make_map(&a.tm_q, q, bf, 2, d, C, zq, 64) || !make_map(&a.tm_k, k, bf, 2, d, C, zkv, 64) ||
+      !make_map(&a.tm_v, v, bf, 2, d, C, zkv, 64) ||
+      !make_map(&a.tm_o, o_s, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, C, zq, 32))
+    return RING_ATTN_ERR_CUDA;
+  DevicePlan plan;
+  int rc = get_step_plan(dev, L, N, causal, step, rank_lo, rank_hi, &plan);
+  if (rc != RING_ATTN_OK) return rc;
+  int* err;
+  if ((rc = status_ptr(dev, &err)) != RING_ATTN_OK) return rc;
+  a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.L = C; a.d = d; a.causal = causal != 0;
+  a.n_blocks = plan.n_blocks;
+  a.order = plan.order(); a.offsets = plan.offsets(); a.ranges = plan.ranges();
+  a.lse = lse_s; a.err = err; a.timer = active_timer();
+  a.step_nb = (C + kQBlockRows - 1) / kQBlockRows;
+  a.step = step; a.rank_lo = rank_lo; a.n_chunks = N;
+  a.sub_len = causal ? L / (2 * N) : 0;
+  a.z_rank = z_rank; a.o32 = o_s;
+  return launch_fwd(a, stream) == cudaSuccess ? RING_ATTN_OK : RING_ATTN_ERR_CUDA;
+}
+
+// Parts of the ring_attn_ring_fwd workspace (byte offsets, 256-aligned).
+struct RingWorkspace {
+  size_t qc = 0, kc = 0, vc = 0, oacc = 0, lacc = 0, os = 0, ls = 0, total = 0;
+};
+
+RingWorkspace ring_workspace(int B, int Hq, int Hkv, int L, int d) {
+  auto up = [](size_t x) { return round_up(x, 256); };
+  const size_t nq = static_cast<size_t>(B) * Hq * L, nkv = static_cast<size_t>(B) * Hkv * L;
+  RingWorkspace w;
+  w.kc = w.qc + up(nq * d * 2);
+  w.vc = w.kc + up(nkv * d * 2);
+  w.oacc = w.vc + up(nkv * d * 2);
+  w.lacc = w.oacc + up(nq * d * 4);
+  w.os = w.lacc + up(nq * 4);
+  w.ls = w.os + up(nq * d * 4);
+  w.total = w.ls + up(nq * 4);
+  return w;
+}
+
 
 int plan_query(int kind, int L, int n_chunks, int causal, int* n_blocks, int* n_ranges, int32_t* order,
                int32_t* offsets, int32_t* ranges) {
@@ -195,6 +278,20 @@ int ring_attn_fwd_plan(int L, int n_chunks, int causal, int* n_blocks, int* n_ra
 int ring_attn_bwd_plan(int L, int n_chunks, int causal, int* n_blocks, int* n_ranges, int32_t* block_order,
                        int32_t* range_offsets, int32_t* ranges) {
   return plan_query(1, L, n_chunks, causal, n_blocks, n_ranges, block_order, range_offsets, ranges);
+}
+
+int ring_attn_step_plan(int L, int n_chunks, int causal, int step, int rank, int* n_blocks, int* n_ranges,
+                        int32_t* block_order, int32_t* range_offsets, int32_t* ranges) {
+  if (L <= 0 || n_chunks <= 0 || !chunking_ok(L, n_chunks, causal != 0)) return RING_ATTN_ERR_SHAPE;
+  if (!step_chunking_ok(L, n_chunks, causal != 0)) return RING_ATTN_ERR_UNSUPPORTED;
+  if (step < 0 || step >= n_chunks || rank < 0 || rank >= n_chunks) return RING_ATTN_ERR_SHAPE;
+  Plan p = build_step_plan(L, n_chunks, causal != 0, step, rank, rank + 1);
+  if (n_blocks) *n_blocks = p.n_blocks;
+  if (n_ranges) *n_ranges = static_cast<int>(p.ranges.size() / 2);
+  if (block_order) std::memcpy(block_order, p.order.data(), p.order.size() * sizeof(int32_t));
+  if (range_offsets) std::memcpy(range_offsets, p.offsets.data(), p.offsets.size() * sizeof(int32_t));
+  if (ranges) std::memcpy(ranges, p.ranges.data(), p.ranges.size() * sizeof(int32_t));
+  return RING_ATTN_OK;
 }
 
 int ring_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int L,
@@ -328,6 +425,93 @@ int ring_attn_profile_read(double* ms, long long* launches) {
   return rc;
 }
 
+int ring_attn_fwd_step(const void* q_chunk, const void* k_chunk, const void* v_chunk, float* o_s, float* lse_s,
+                       int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal, int rank, int src,
+                       cudaStream_t stream) {
+  int rc = check_ring_shape(B, Hq, Hkv, L, d, n_chunks, causal);
+  if (rc != RING_ATTN_OK) return rc;
+  if (rank < 0 || rank >= n_chunks || src < 0 || src >= n_chunks) return RING_ATTN_ERR_SHAPE;
+  if (B == 0 || L == 0) return RING_ATTN_OK;
+  if (!q_chunk || !k_chunk || !v_chunk || !o_s || !lse_s) return RING_ATTN_ERR_NULL;
+  if (!aligned16(q_chunk) || !aligned16(k_chunk) || !aligned16(v_chunk) || !aligned16(o_s) || !aligned16(lse_s))
+    return RING_ATTN_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  int dev;
+  if ((rc = current_device(&dev)) != RING_ATTN_OK) return rc;
+  const int step = ((rank - src) % n_chunks + n_chunks) % n_chunks;
+  return launch_step(dev, q_chunk, k_chunk, v_chunk, o_s, lse_s, B, Hq, Hkv, L, d, n_chunks, causal, step, rank,
+                     rank + 1, 0, stream);
+}
+
+int ring_attn_merge(float* o, float* lse, const float* o_s, const float* lse_s, long long n_rows, int d,
+                    void* o_out, cudaStream_t stream) {
+  if (n_rows < 0) return RING_ATTN_ERR_SHAPE;
+  if (d != 64 && d != 128) return RING_ATTN_ERR_UNSUPPORTED;
+  if (n_rows == 0) return RING_ATTN_OK;
+  if (!o || !lse || !o_s || !lse_s) return RING_ATTN_ERR_NULL;
+  if (!aligned16(o) || !aligned16(o_s) || (o_out && !aligned16(o_out))) return RING_ATTN_ERR_UNSUPPORTED;
+  LaunchTimer* t = active_timer();
+  if (t) t->mark(RING_ATTN_KERNEL_RING_MERGE, false, stream);
+  const cudaError_t e = launch_ring_merge(o, lse, o_s, lse_s, o_out, n_rows, d, stream);
+  if (t) t->mark(RING_ATTN_KERNEL_RING_MERGE, true, stream);
+  return e == cudaSuccess ? RING_ATTN_OK : RING_ATTN_ERR_CUDA;
+}
+
+size_t ring_attn_ring_fwd_workspace_size(int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal) {
+  if (check_ring_shape(B, Hq, Hkv, L, d, n_chunks, causal) != RING_ATTN_OK) return 0;
+  return ring_workspace(B, Hq, Hkv, L, d).total;
+}
+
+int ring_attn_ring_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                       int L, int d, int n_chunks, int causal, void* workspace, size_t workspace_bytes,
+                       cudaStream_t stream) {
+  int rc = check_ring_shape(B, Hq, Hkv, L, d, n_chunks, causal);
+  if (rc != RING_ATTN_OK) return rc;
+  if (B == 0 || L == 0) return RING_ATTN_OK;
+  if (!q || !k || !v || !o || !lse) return RING_ATTN_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return RING_ATTN_ERR_UNSUPPORTED;
+  const RingWorkspace w = ring_workspace(B, Hq, Hkv, L, d);
+  if (!workspace || workspace_bytes < w.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return RING_ATTN_ERR_WORKSPACE;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  int dev;
+  if ((rc = current_device(&dev)) != RING_ATTN_OK) return rc;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* qc = ws + w.qc;
+  void* kc = ws + w.kc;
+  void* vc = ws + w.vc;
+  float* oacc = reinterpret_cast<float*>(ws + w.oacc);
+  float* lacc = reinterpret_cast<float*>(ws + w.lacc);
+  float* os = reinterpret_cast<float*>(ws + w.os);
+  float* ls = reinterpret_cast<float*>(ws + w.ls);
+  const int N = n_chunks;
+  LaunchTimer* t = active_timer();
+  if (t) t->mark(RING_ATTN_KERNEL_RING_IO, false, stream);
+  if (launch_ring_gather(q, qc, B * Hq, L, d, N, causal != 0, stream) != cudaSuccess ||
+      launch_ring_gather(k, kc, B * Hkv, L, d, N, causal != 0, stream) != cudaSuccess ||
+      launch_ring_gather(v, vc, B * Hkv, L, d, N, causal != 0, stream) != cudaSuccess)
+    return RING_ATTN_ERR_CUDA;
+  if (t) t->mark(RING_ATTN_KERNEL_RING_IO, true, stream);
+  const long long rows = static_cast<long long>(B) * Hq * L;
+  for (int s = 0; s < N; ++s) {
+    // step 0 (every rank's own chunk) starts the running result
+    if ((rc = launch_step(dev, qc, kc, vc, s == 0 ? oacc : os, s == 0 ? lacc : ls, B, Hq, Hkv, L, d, N, causal, s,
+                          0, N, 1, stream)) != RING_ATTN_OK)
+      return rc;
+    if (s > 0) {
+      if (t) t->mark(RING_ATTN_KERNEL_RING_MERGE, false, stream);
+      if (launch_ring_merge(oacc, lacc, os, ls, nullptr, rows, d, stream) != cudaSuccess) return RING_ATTN_ERR_CUDA;
+      if (t) t->mark(RING_ATTN_KERNEL_RING_MERGE, true, stream);
+    }
+  }
+  if (t) t->mark(RING_ATTN_KERNEL_RING_IO, false, stream);
+  if (launch_ring_scatter(oacc, lacc, o, lse, B * Hq, L, d, N, causal != 0, stream) != cudaSuccess)
+    return RING_ATTN_ERR_CUDA;
+  if (t) t->mark(RING_ATTN_KERNEL_RING_IO, true, stream);
+  return RING_ATTN_OK;
+}
+
 void ring_attn_release(void) {
   std::lock_guard<std::mutex> lock(g_mutex);
   int cur = 0;
@@ -336,8 +520,13 @@ void ring_attn_release(void) {
     cudaSetDevice(std::get<0>(kv.first));
     cudaFree(kv.second.dev);
   }
+  for (auto& kv : g_step_plans) {
+    cudaSetDevice(std::get<0>(kv.first));
+    cudaFree(kv.second.dev);
+  }
   cudaSetDevice(cur);
   g_plans.clear();
+  g_step_plans.clear();
 }
 
 }  // extern "C"

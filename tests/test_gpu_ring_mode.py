@@ -1,0 +1,142 @@
+"""Ring mode on the GPU, through the C ABI, against the fp64 oracle.
+
+One ring step (ring_attn_fwd_step) is compared with the oracle's ring_step
+for every (rank, source) pair of small rings; the merge kernel with the
+oracle's merge; the whole ring run step by step on one GPU
+(ring_attn_ring_fwd) with the oracle's plain forward and with the fused
+forward.  Tolerances as for the fused path (tolerance.py): o within 2e-2
+max-abs beyond bf16 output rounding and 2e-3 mean-abs, lse within 1e-3;
+the merge alone, fp32 in and out, within 1e-5.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sequence_blockwise_self_gb300 as ra
+from sequence_blockwise_self_gb300 import build as lib_build
+from sequence_blockwise_self_gb300 import inputs
+from tolerance import TOL_LSE, check_bf16, check_fp32
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    lib_build.build()
+    ra.load()
+
+
+def f64(t):
+    return t.detach().float().cpu().double().numpy()
+
+
+def assert_status_ok():
+    st, site = ra.device_status()
+    assert st == 0, f"device status {st} at site {site:#x}"
+
+
+def chunk_positions(L, N, causal, r):
+    return torch.tensor([p for p in range(L) if oracle.owner_rank(L, N, causal, p) == r], dtype=torch.long)
+
+
+# (B, Hq, Hkv, L, d, N, causal): chunks of whole 128-row tiles
+STEP_CASES = [
+    (1, 4, 2, 1024, 128, 4, True),    # sub-chunks of one tile: every block spans both
+    (2, 2, 1, 1024, 64, 4, False),
+    (1, 2, 2, 1536, 128, 3, True),    # sub-chunks of two tiles
+    (1, 2, 1, 768, 64, 3, False),
+    (1, 3, 1, 3072, 128, 4, True),    # sub-chunks of three tiles: a block straddles them
+]
+
+
+@pytest.mark.parametrize("case", STEP_CASES, ids=lambda c: "B{}Hq{}Hkv{}L{}d{}N{}{}".format(*c[:6], "c" if c[6] else "e"))
+def test_every_step_of_a_small_ring_matches_the_oracle(case):
+    B, Hq, Hkv, L, d, N, causal = case
+    q, k, v, _ = inputs.make_inputs(B, Hq, Hkv, L, d, seed=sum(case[:6]))
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    for r in range(N):
+        rows = chunk_positions(L, N, causal, r)
+        q_chunk = qd[:, :, rows.cuda()].contiguous()
+        for src in range(N):
+            srows = chunk_positions(L, N, causal, src)
+            k_chunk = kd[:, :, srows.cuda()].contiguous()
+            v_chunk = vd[:, :, srows.cuda()].contiguous()
+            o_s, lse_s = ra.ring_attn_fwd_step(q_chunk, k_chunk, v_chunk, N, causal, r, src)
+            torch.cuda.synchronize()
+            assert_status_ok()
+            o_ref, lse_ref = oracle.ring_step(q.double(), k.double(), v.double(), causal, N, r, src)
+            o_ref, lse_ref = o_ref[:, :, rows.numpy()], lse_ref[:, :, rows.numpy()]
+            got_o, got_l = f64(o_s), f64(lse_s)
+            empty = np.isneginf(lse_ref)
+            assert np.array_equal(np.isneginf(got_l), empty), f"rank {r} src {src}: rows with no visible key differ"
+            assert np.all(got_o[empty] == 0.0)
+            if (~empty).any():
+                check_bf16(f"o_s r{r} s{src}", got_o[~empty], o_ref[~empty])
+                check_fp32(f"lse_s r{r} s{src}", got_l[~empty], lse_ref[~empty], TOL_LSE)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_merge_matches_the_oracle(d):
+    rng = np.random.default_rng(d)
+    rows = 3000
+    o_a, o_b = rng.standard_normal((rows, d)), rng.standard_normal((rows, d))
+    l_a, l_b = rng.standard_normal(rows) * 4, rng.standard_normal(rows) * 4
+    l_a[::7] = -np.inf      # side a empty
+    l_b[::5] = -np.inf      # side b empty (both, every 35th row)
+    l_b[1::11] = l_a[1::11] + 60.0   # one side dominates
+    ta = torch.tensor(o_a, dtype=torch.float32)
+    tb = torch.tensor(o_b, dtype=torch.float32)
+    tla = torch.tensor(l_a, dtype=torch.float32)
+    tlb = torch.tensor(l_b, dtype=torch.float32)
+    o, lse = ta.cuda(), tla.cuda()
+    o_out = torch.empty((rows, d), dtype=torch.bfloat16, device="cuda")
+    ra.ring_attn_merge(o, lse, tb.cuda(), tlb.cuda(), o_out=o_out)
+    torch.cuda.synchronize()
+    want_o, want_l = oracle.merge(ta.double().numpy(), tla.double().numpy(), tb.double().numpy(),
+                                  tlb.double().numpy())
+    got_o, got_l = f64(o), f64(lse)
+    np.testing.assert_array_equal(np.isneginf(got_l), np.isneginf(want_l))
+    fin = np.isfinite(want_l)
+    assert np.abs(got_l[fin] - want_l[fin]).max() <= 1e-5
+    assert np.abs(got_o - want_o).max() <= 1e-5
+    assert torch.equal(o_out.cpu(), o.cpu().to(torch.bfloat16))
+
+
+# (B, Hq, Hkv, L, d, N, causal)
+RING_CASES = [
+    (1, 4, 2, 1024, 128, 4, True),
+    (2, 2, 1, 1024, 64, 4, False),
+    (1, 3, 1, 3072, 128, 4, True),
+    (1, 4, 4, 4096, 64, 8, False),
+    (1, 2, 2, 1024, 128, 1, True),   # one rank: a single step, nothing to merge
+]
+
+
+@pytest.mark.parametrize("case", RING_CASES, ids=lambda c: "B{}Hq{}Hkv{}L{}d{}N{}{}".format(*c[:6], "c" if c[6] else "e"))
+def test_whole_ring_on_one_gpu_matches_the_oracle_and_the_fused_kernel(case):
+    B, Hq, Hkv, L, d, N, causal = case
+    q, k, v, _ = inputs.make_inputs(B, Hq, Hkv, L, d, seed=7 + sum(case[:6]))
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o, lse = ra.ring_attn_ring_fwd(qd, kd, vd, N, causal)
+    o_f, lse_f = ra.ring_attn_fwd(qd, kd, vd, N, causal)
+    torch.cuda.synchronize()
+    assert_status_ok()
+    o_ref, lse_ref = oracle.fwd(q.double(), k.double(), v.double(), causal)
+    check_bf16("o (ring mode)", f64(o), o_ref)
+    check_fp32("lse (ring mode)", f64(lse), lse_ref, TOL_LSE)
+    check_bf16("o (ring mode vs fused)", f64(o), f64(o_f), ulps=2)
+    check_fp32("lse (ring mode vs fused)", f64(lse), f64(lse_f), TOL_LSE)
+
+
+def test_ring_mode_at_32k_on_sampled_rows():
+    w = inputs.WORKLOADS["gqa_32k"]
+    q, k, v, _ = inputs.workload_inputs(w)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o, lse = ra.ring_attn_ring_fwd(qd, kd, vd, w.n_chunks, w.causal)
+    torch.cuda.synchronize()
+    assert_status_ok()
+    rows = inputs.sample_rows(w.L, w.n_chunks, w.causal, 64, seed=5)
+    o_ref, lse_ref, _ = oracle.fwd_rows(q.double(), k.double(), v.double(), w.causal, rows)
+    check_bf16("o (ring mode, 32k)", f64(o[:, :, rows]), o_ref)
+    check_fp32("lse (ring mode, 32k)", f64(lse[:, :, rows]), lse_ref, TOL_LSE)

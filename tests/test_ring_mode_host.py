@@ -1,0 +1,117 @@
+"""Ring mode on the host (no GPU): the step planner and the argument checks
+of the ring-mode entry points of include/ring_attn.h."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle
+from sequence_blockwise_self_gb300 import build as lib_build
+from sequence_blockwise_self_gb300 import capi
+
+
+@pytest.fixture(scope="module")
+def lib():
+    lib_build.build()
+    return capi.load()
+
+
+def _chunk_positions(L, N, causal, r):
+    """Sequence positions of rank r's rows in chunk order (ascending: for the
+    fold that is sub-chunk r, then sub-chunk 2N-1-r)."""
+    return np.array([p for p in range(L) if oracle.owner_rank(L, N, causal, p) == r])
+
+
+CASES = [(1024, 4, True), (1024, 4, False), (2048, 4, True), (1536, 3, True), (3072, 8, False), (4096, 8, True)]
+
+
+@pytest.mark.parametrize("L,N,causal", CASES)
+def test_step_plan_lists_exactly_the_visible_tile_pairs(lib, L, N, causal):
+    C = L // N
+    nt = C // 128
+    for r in range(N):
+        qpos = _chunk_positions(L, N, causal, r)
+        for s in range(N):
+            src = (r - s) % N
+            kpos = _chunk_positions(L, N, causal, src)
+            plan = capi.step_plan(L, N, causal, s, r)
+            assert len(plan["visits"]) == (C + 255) // 256
+            assert sorted(plan["order"].tolist()) == list(range(len(plan["visits"])))
+            for u, visits in enumerate(plan["visits"]):
+                listed = [kt for b, e in visits for kt in range(b, e)]
+                assert listed == sorted(set(listed))
+                qts = [qt for qt in (2 * u, 2 * u + 1) if qt < nt]
+                want = set()
+                for qt in qts:
+                    qmax = qpos[qt * 128:(qt + 1) * 128].max()
+                    for kt in range(nt):
+                        if not causal or kpos[kt * 128:(kt + 1) * 128].min() <= qmax:
+                            want.add(kt)
+                assert set(listed) == want, (r, s, u)
+
+
+@pytest.mark.parametrize("N", [2, 4, 8])
+def test_fold_gives_every_causal_step_the_same_work(lib, N):
+    """Section 8.2 of the pages: with the fold every rank does the same work
+    at every step s > 0 (half of a chunk pair's tiles); step 0 is the
+    diagonal pair."""
+    L = 256 * N
+    nt = L // N // 128
+    works = {}
+    for s in range(N):
+        for r in range(N):
+            qpos = _chunk_positions(L, N, True, r)
+            kpos = _chunk_positions(L, N, True, (r - s) % N)
+            plan = capi.step_plan(L, N, True, s, r)
+            pairs = 0  # (query tile, listed key tile) pairs with a visible position pair
+            for u, visits in enumerate(plan["visits"]):
+                for qt in (2 * u, 2 * u + 1):
+                    if qt >= nt:
+                        continue
+                    qmax = qpos[qt * 128:(qt + 1) * 128].max()
+                    pairs += sum(1 for b, e in visits for kt in range(b, e)
+                                 if kpos[kt * 128:(kt + 1) * 128].min() <= qmax)
+            works[(s, r)] = pairs
+    for s in range(1, N):
+        assert len({works[(s, r)] for r in range(N)}) == 1
+
+
+I = ctypes.c_int
+NUL = ctypes.c_void_p(0)
+P256 = ctypes.c_void_p(256)
+
+
+def test_step_rejects_bad_arguments(lib):
+    def step(L=1024, N=4, causal=1, rank=0, src=0, d=64, ptr=P256):
+        return lib.ring_attn_fwd_step(ptr, ptr, ptr, ptr, ptr, 1, 2, 1, L, d, N, causal, rank, src, NUL)
+    assert step(rank=4) == capi.ERR_SHAPE
+    assert step(src=-1) == capi.ERR_SHAPE
+    assert step(L=1001) == capi.ERR_SHAPE                 # L % 2N
+    assert step(L=1000) == capi.ERR_UNSUPPORTED           # sub-chunks of 125 rows: not whole tiles
+    assert step(L=512, N=4) == capi.ERR_UNSUPPORTED       # sub-chunks of 64 rows
+    assert step(L=512, N=4, causal=0, ptr=NUL) == capi.ERR_NULL  # chunks of 128 rows: whole tiles
+    assert step(d=96) == capi.ERR_UNSUPPORTED
+    assert step(ptr=ctypes.c_void_p(8)) == capi.ERR_UNSUPPORTED
+    assert lib.ring_attn_fwd_step(NUL, NUL, NUL, NUL, NUL, 0, 2, 1, 1024, 64, 4, 1, 0, 0, NUL) == capi.OK
+
+
+def test_merge_rejects_bad_arguments(lib):
+    assert lib.ring_attn_merge(P256, P256, P256, P256, -1, 128, NUL, NUL) == capi.ERR_SHAPE
+    assert lib.ring_attn_merge(P256, P256, P256, P256, 10, 96, NUL, NUL) == capi.ERR_UNSUPPORTED
+    assert lib.ring_attn_merge(NUL, P256, P256, P256, 10, 128, NUL, NUL) == capi.ERR_NULL
+    assert lib.ring_attn_merge(P256, P256, P256, P256, 10, 128, ctypes.c_void_p(4), NUL) == capi.ERR_UNSUPPORTED
+    assert lib.ring_attn_merge(NUL, NUL, NUL, NUL, 0, 128, NUL, NUL) == capi.OK
+
+
+def test_ring_fwd_workspace_and_arguments(lib):
+    ws = lib.ring_attn_ring_fwd_workspace_size(1, 2, 1, 1024, 64, 4, 1)
+    # q, k, v in chunk order (bf16), running result and one partial (fp32 o + lse)
+    rows_q, rows_kv = 2 * 1024, 1024
+    assert ws == rows_q * 64 * 2 + 2 * rows_kv * 64 * 2 + 2 * (rows_q * 64 * 4 + rows_q * 4)
+    assert lib.ring_attn_ring_fwd_workspace_size(1, 2, 1, 512, 64, 4, 1) == 0  # not whole tiles
+    args = [P256] * 5
+    assert lib.ring_attn_ring_fwd(*args, 1, 2, 1, 1024, 64, 4, 1, NUL, ws, NUL) == capi.ERR_WORKSPACE
+    assert lib.ring_attn_ring_fwd(*args, 1, 2, 1, 1024, 64, 4, 1, P256, ws - 1, NUL) == capi.ERR_WORKSPACE
+    assert lib.ring_attn_ring_fwd(*args, 1, 2, 1, 1024, 64, 4, 1, ctypes.c_void_p(272), ws, NUL) == \
+        capi.ERR_WORKSPACE
+    assert lib.ring_attn_ring_fwd(*([NUL] * 5), 1, 2, 1, 1024, 64, 4, 1, P256, ws, NUL) == capi.ERR_NULL
