@@ -432,7 +432,50 @@ def run_ours(args, w):
         e2e.update(link)
         del dev_in, dev_out
 
-    # (4) CPU oracle baseline (rank 0, one GPU only)
+    # (4) ring mode: the same forward run step by step the way each rank of a
+    # multi-GPU ring runs it (every rank's step s in one launch, then the
+    # log-sum-exp merge), on this GPU; its merge kernel is HBM-bound
+    ring = None
+    if not args.no_ring_mode and w.L % (256 * w.n_chunks if w.causal else 128 * w.n_chunks) == 0:
+        o_r = torch.empty_like(qd)
+        lse_r = torch.empty_like(lse)
+        ws_r = torch.empty(ra.ring_fwd_workspace_size(w.B, w.Hq, w.Hkv, w.L, w.d, w.n_chunks, w.causal),
+                           dtype=torch.uint8, device=dev)
+        ring_fwd = lambda: ra.ring_attn_ring_fwd(qd, kd, vd, w.n_chunks, w.causal, o=o_r, lse=lse_r,  # noqa: E731
+                                                 workspace=ws_r, stream=stream)
+        ring_fwd()
+        torch.cuda.synchronize(dev)
+        r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        r0.record(stream)
+        for _ in range(args.steps):
+            ring_fwd()
+        r1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms_ring = r0.elapsed_time(r1) / args.steps
+        ra.profile_enable(True)
+        for _ in range(args.steps):
+            ring_fwd()
+        torch.cuda.synchronize(dev)
+        rp = ra.profile_read()
+        ra.profile_enable(False)
+        st, site = ra.device_status()
+        if st != 0:
+            raise RuntimeError(f"device status {st} at site {site:#x} in ring mode")
+        merge_ms, merge_n = rp["ring_merge"]
+        rows = w.B * w.Hq * w.L
+        merge_bytes = rows * (3 * w.d * 4 + 3 * 4)  # read o, o_s, lse, lse_s; write o, lse
+        merge_gbs = merge_bytes / (merge_ms / merge_n * 1e-3) / 1e9 if merge_n else None
+        ring = {
+            "fwd_ms": ms_ring, "fwd_tflops": F / (ms_ring * 1e-3) / 1e12,
+            "per_kernel_ms_per_fwd": {k: rp[k][0] / args.steps for k in ("ring_step", "ring_merge", "ring_io")},
+            "launches_per_fwd": {k: rp[k][1] // args.steps for k in ("ring_step", "ring_merge", "ring_io")},
+            "merge_roofline": {"bound": "hbm", "achieved": merge_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                               "frac": (merge_gbs / peaks["hbm_gbs"]) if merge_gbs else None,
+                               "bytes_per_launch": merge_bytes},
+        }
+        del o_r, lse_r, ws_r
+
+    # (5) CPU oracle baseline (rank 0, one GPU only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tf, det = oracle_sample(w, q, k, v, dO, seconds_target=15.0, seed=7)
@@ -458,6 +501,7 @@ def run_ours(args, w):
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
+            "ring_mode": ring,
             "gpu_launches": 4 * args.steps,
             "clocks": clocks,
         }
@@ -475,6 +519,7 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-ring-mode", action="store_true")
     args = ap.parse_args()
     from sequence_blockwise_self_gb300 import inputs
 

@@ -318,8 +318,8 @@ def profile_enable(on: bool = True):
 
 def profile_read():
     """{kernel: (summed ms, launches)} since the last read (waits for them)."""
-    ms = (ctypes.c_double * 4)()
-    n = (ctypes.c_longlong * 4)()
+    ms = (ctypes.c_double * len(KERNEL_NAMES))()   # RING_ATTN_N_KERNELS entries
+    n = (ctypes.c_longlong * len(KERNEL_NAMES))()
     rc = load().ring_attn_profile_read(ms, n)
     if rc != OK:
         raise RingAttnError(rc, "ring_attn_profile_read")

@@ -185,3 +185,14 @@ def test_folded_assignment_balances_tile_work_across_ranks(lib, L, N):
     for qt in range(L // 128):
         contiguous[qt * 128 // (L // N)] += qt + 1
     assert contiguous.max() > 1.5 * contiguous.mean()
+
+
+def test_profile_kinds_match_the_header(lib):
+    """The binding's kernel-kind list has RING_ATTN_N_KERNELS entries, and a
+    read with nothing recorded (no CUDA call) returns every kind at zero."""
+    text = open(os.path.join(ROOT, "include", "ring_attn.h")).read()
+    n = int(re.search(r"RING_ATTN_N_KERNELS\s*=\s*(\d+)", text).group(1))
+    assert len(capi.KERNEL_NAMES) == n
+    got = capi.profile_read()
+    assert list(got) == list(capi.KERNEL_NAMES)
+    assert all(v == (0.0, 0) for v in got.values())
