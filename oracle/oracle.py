@@ -53,11 +53,11 @@ def _bind(lib):
     lib.oracle_bwd.argtypes = [_dp, _dp, _dp, _dp, I, I, I, I, I, I, _dp, _dp, _dp, _dp, _dp, I]
     lib.oracle_bwd_rows.argtypes = [_dp, _dp, _dp, _dp, I, I, I, I, I, I, _ip, I, _ip, I,
                                     _dp, _dp, _dp, I]
-    lib.oracle_ring_fwd.argtypes = [_dp, _dp, _dp, I, I, I, I, I, I, I, _dp, _dp, I]
-    lib.oracle_ring_step.argtypes = [_dp, _dp, _dp, I, I, I, I, I, I, I, I, I, _dp, _dp, I]
+    lib.oracle_ring_fwd.argtypes = [_dp, _dp, _dp, I, I, I, I, I, I, I, I, _dp, _dp, I]
+    lib.oracle_ring_step.argtypes = [_dp, _dp, _dp, I, I, I, I, I, I, I, I, I, I, _dp, _dp, I]
     lib.oracle_merge.argtypes = [_dp, _dp, _dp, _dp, ctypes.c_long, I]
     lib.oracle_merge.restype = None
-    lib.oracle_owner_rank.argtypes = [I, I, I, I]
+    lib.oracle_owner_rank.argtypes = [I, I, I, I, I]
     for f in (lib.oracle_fwd, lib.oracle_fwd_rows, lib.oracle_bwd, lib.oracle_bwd_rows,
               lib.oracle_ring_fwd, lib.oracle_ring_step, lib.oracle_owner_rank):
         f.restype = ctypes.c_int
@@ -181,31 +181,31 @@ def bwd_rows(q, k, v, dO, causal: bool, q_rows, k_rows, threads: int = 0):
     return dq, dk, dv
 
 
-def ring_fwd(q, k, v, causal: bool, n_chunks: int, threads: int = 0):
+def ring_fwd(q, k, v, causal: bool, n_chunks: int, threads: int = 0, striped: bool = False):
     """Ring form: per ring step partial (o_s, lse_s) merged by log-sum-exp
     (SP series sections 2.3 and 6.2; causal ranks own folded sub-chunks,
-    section 8.2)."""
+    section 8.2, or, with striped, the positions r, r+N, r+2N, ...)."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, Hq, Hkv, L, d = _shape(q, k)
     o = np.zeros((B, Hq, L, d))
     lse = np.zeros((B, Hq, L))
     _check(_load().oracle_ring_fwd(_p(q), _p(k), _p(v), B, Hq, Hkv, L, d, int(causal), int(n_chunks),
-                                   _p(o), _p(lse), _threads(threads)))
+                                   int(bool(striped)), _p(o), _p(lse), _threads(threads)))
     return o, lse
 
 
-def ring_step(q, k, v, causal: bool, n_chunks: int, rank: int, src: int, threads: int = 0):
+def ring_step(q, k, v, causal: bool, n_chunks: int, rank: int, src: int, threads: int = 0, striped: bool = False):
     """One ring step in isolation (SP series sections 2.3 and 6.2): the
     partial result (o_s, lse_s) of rank `rank`'s query rows against the keys
     and values of rank `src`.  Returned in global row order, [B,Hq,L,d] and
     [B,Hq,L]; rows of other ranks are 0 and -inf, as are rows of `rank` that
-    see none of src's keys."""
+    see none of src's keys.  striped: rank r owns positions r, r+N, ..."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, Hq, Hkv, L, d = _shape(q, k)
     o = np.zeros((B, Hq, L, d))
     lse = np.full((B, Hq, L), -np.inf)
     _check(_load().oracle_ring_step(_p(q), _p(k), _p(v), B, Hq, Hkv, L, d, int(causal), int(n_chunks),
-                                    int(rank), int(src), _p(o), _p(lse), _threads(threads)))
+                                    int(rank), int(src), int(bool(striped)), _p(o), _p(lse), _threads(threads)))
     return o, lse
 
 
@@ -227,11 +227,11 @@ def merge(o_a, lse_a, o_b, lse_b):
 
 # ------------------------------------------------------------ chunk map (host)
 
-def owner_rank(L: int, n_chunks: int, causal: bool, p: int) -> int:
+def owner_rank(L: int, n_chunks: int, causal: bool, p: int, striped: bool = False) -> int:
     """Rank owning sequence position p: chunk p // (L/N) for the encoder;
     for causal the folded pair {r, 2N-1-r} of sub-chunks of length L/(2N)
-    (SP series section 8.2)."""
-    r = _load().oracle_owner_rank(int(L), int(n_chunks), int(causal), int(p))
+    (SP series section 8.2); p mod N when striped."""
+    r = _load().oracle_owner_rank(int(L), int(n_chunks), int(causal), int(bool(striped)), int(p))
     if r < 0:
         raise ValueError("bad chunk map arguments")
     return r

@@ -38,7 +38,10 @@
  *   the fold of the USP section 8.2).  At ring step s = 0..N-1 rank r holds
  *   the keys/values of rank (r - s) mod N, computes the partial result of
  *   that block (o_s, lse_s) and merges it into its running result with the
- *   log-sum-exp rule (the online-softmax correction of section 6.2):
+ *   log-sum-exp rule (the online-softmax correction of section 6.2).  With
+ *   the striped assignment (a causal schedule variant the pages compare
+ *   with the fold: rank r owns positions r, r+N, r+2N, ...), every rank's
+ *   chunk spreads over the whole sequence instead:
  *
  *     lse <- log(exp(lse) + exp(lse_s)),
  *     o   <- exp(lse_old - lse) * o + exp(lse_s - lse) * o_s.
@@ -121,6 +124,7 @@ struct task_s {
   double *o, *lse, *D, *dq, *dk, *dv;
   int n_chunks;
   int rank, src;      /* ring step mode: query rank and key/value source rank */
+  int striped;        /* ring forms: striped assignment instead of chunks/fold */
   const int *stat_lo; /* per (b,h): first query row whose stats exist (rows mode) */
 };
 
@@ -362,24 +366,33 @@ int oracle_bwd_rows(const double *q, const double *k, const double *v, const dou
 
 /* --------------------------------------------------------------- ring form */
 
-/* Rank that owns sequence position p. */
-static int owner_rank(int L, int N, int causal, int p) {
+/* Rank that owns sequence position p: contiguous chunks (encoder), the
+ * fold (causal), or stripes (p mod N) when `striped`. */
+static int owner_rank(int L, int N, int causal, int striped, int p) {
+  if (striped) return p % N;
   if (!causal) return p / (L / N);
   const int sub = p / (L / (2 * N));
   return sub < N ? sub : 2 * N - 1 - sub;
 }
 
+/* Chunk map valid for this length: L % N == 0 (encoder, striped) or
+ * L % 2N == 0 (fold). */
+static int bad_chunking(int L, int n_chunks, int causal, int striped) {
+  if (n_chunks <= 0) return 1;
+  return L % ((causal && !striped) ? 2 * n_chunks : n_chunks) != 0;
+}
+
 /* Partial attention of query row i against the keys of rank src that i may
  * see.  Returns 0 if there is none; otherwise writes (o_s, lse_s). */
 static int ring_block(const problem_t *P, int N, int b, int h, int i, int src, double *s, double *o_s,
-                      double *lse_s) {
+                      double *lse_s, int striped) {
   const int g = h / (P->Hq / P->Hkv);
   const double *qi = q_row(P, b, h, i);
   double m = -INFINITY;
   int cnt = 0;
   for (int j = 0; j < P->L; ++j) {
     s[j] = -INFINITY;
-    if (owner_rank(P->L, N, P->causal, j) != src) continue;
+    if (owner_rank(P->L, N, P->causal, striped, j) != src) continue;
     if (P->causal && j > i) continue;
     s[j] = P->scale * dot(qi, k_row(P, b, g, j), P->d);
     if (s[j] > m) m = s[j];
@@ -405,7 +418,7 @@ static void ring_item(task_t *t, long item, double *s) {
   const int i = (int)(item % P->L);
   const long bh = item / P->L;
   const int h = (int)(bh % P->Hq), b = (int)(bh / P->Hq);
-  const int r = owner_rank(P->L, N, P->causal, i);
+  const int r = owner_rank(P->L, N, P->causal, t->striped, i);
   double *o_s = s + P->L;
   double *o = t->o + ((size_t)bh * P->L + i) * P->d;
   double lse = -INFINITY;
@@ -413,7 +426,7 @@ static void ring_item(task_t *t, long item, double *s) {
   for (int step = 0; step < N; ++step) {
     const int src = ((r - step) % N + N) % N;
     double lse_s;
-    if (!ring_block(P, N, b, h, i, src, s, o_s, &lse_s)) continue;
+    if (!ring_block(P, N, b, h, i, src, s, o_s, &lse_s, t->striped)) continue;
     const double hi = lse > lse_s ? lse : lse_s;
     const double merged = hi + log(exp(lse - hi) + exp(lse_s - hi));
     const double a = exp(lse - merged), w = exp(lse_s - merged);
@@ -426,13 +439,12 @@ static void ring_item(task_t *t, long item, double *s) {
 /* Ring form of the forward with n_chunks ranks.  Requires L % n_chunks == 0
  * (encoder) or L % (2 n_chunks) == 0 (causal, folded sub-chunks). */
 int oracle_ring_fwd(const double *q, const double *k, const double *v, int B, int Hq, int Hkv, int L,
-                    int d, int causal, int n_chunks, double *o, double *lse, int n_threads) {
-  if (bad_shape(B, Hq, Hkv, L, d) || n_chunks <= 0) return -1;
-  if (L % (causal ? 2 * n_chunks : n_chunks) != 0) return -1;
+                    int d, int causal, int n_chunks, int striped, double *o, double *lse, int n_threads) {
+  if (bad_shape(B, Hq, Hkv, L, d) || bad_chunking(L, n_chunks, causal, striped)) return -1;
   problem_t P = make_problem(q, k, v, NULL, B, Hq, Hkv, L, d, causal);
   task_t t; memset(&t, 0, sizeof t);
   t.P = &P; t.n_items = (long)B * Hq * L; t.fn = ring_item; t.scratch_len = (size_t)L + d;
-  t.o = o; t.lse = lse; t.n_chunks = n_chunks;
+  t.o = o; t.lse = lse; t.n_chunks = n_chunks; t.striped = striped;
   return run_parallel(&t, n_threads);
 }
 
@@ -446,10 +458,10 @@ static void step_item(task_t *t, long item, double *s) {
   const int i = (int)(item % P->L);
   const long bh = item / P->L;
   const int h = (int)(bh % P->Hq), b = (int)(bh / P->Hq);
-  if (owner_rank(P->L, t->n_chunks, P->causal, i) != t->rank) return;
+  if (owner_rank(P->L, t->n_chunks, P->causal, t->striped, i) != t->rank) return;
   double *o_s = t->o + ((size_t)bh * P->L + i) * P->d;
   double lse_s;
-  if (!ring_block(P, t->n_chunks, b, h, i, t->src, s, o_s, &lse_s)) {
+  if (!ring_block(P, t->n_chunks, b, h, i, t->src, s, o_s, &lse_s, t->striped)) {
     for (int c = 0; c < P->d; ++c) o_s[c] = 0.0;
     lse_s = -INFINITY;
   }
@@ -457,14 +469,14 @@ static void step_item(task_t *t, long item, double *s) {
 }
 
 int oracle_ring_step(const double *q, const double *k, const double *v, int B, int Hq, int Hkv, int L, int d,
-                     int causal, int n_chunks, int rank, int src, double *o_s, double *lse_s, int n_threads) {
-  if (bad_shape(B, Hq, Hkv, L, d) || n_chunks <= 0) return -1;
-  if (L % (causal ? 2 * n_chunks : n_chunks) != 0) return -1;
+                     int causal, int n_chunks, int rank, int src, int striped, double *o_s, double *lse_s,
+                     int n_threads) {
+  if (bad_shape(B, Hq, Hkv, L, d) || bad_chunking(L, n_chunks, causal, striped)) return -1;
   if (rank < 0 || rank >= n_chunks || src < 0 || src >= n_chunks) return -1;
   problem_t P = make_problem(q, k, v, NULL, B, Hq, Hkv, L, d, causal);
   task_t t; memset(&t, 0, sizeof t);
   t.P = &P; t.n_items = (long)B * Hq * L; t.fn = step_item; t.scratch_len = (size_t)L;
-  t.o = o_s; t.lse = lse_s; t.n_chunks = n_chunks; t.rank = rank; t.src = src;
+  t.o = o_s; t.lse = lse_s; t.n_chunks = n_chunks; t.rank = rank; t.src = src; t.striped = striped;
   return run_parallel(&t, n_threads);
 }
 
@@ -493,8 +505,7 @@ void oracle_merge(double *o_a, double *lse_a, const double *o_b, const double *l
   }
 }
 
-int oracle_owner_rank(int L, int n_chunks, int causal, int p) {
-  if (n_chunks <= 0 || p < 0 || p >= L) return -1;
-  if (L % (causal ? 2 * n_chunks : n_chunks) != 0) return -1;
-  return owner_rank(L, n_chunks, causal, p);
+int oracle_owner_rank(int L, int n_chunks, int causal, int striped, int p) {
+  if (p < 0 || p >= L || bad_chunking(L, n_chunks, causal, striped)) return -1;
+  return owner_rank(L, n_chunks, causal, striped, p);
 }

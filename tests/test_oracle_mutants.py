@@ -33,8 +33,9 @@ MUTANTS = {
     "fold_wrong_pair": ("return sub < N ? sub : 2 * N - 1 - sub;", "return sub < N ? sub : sub - N;"),
     "merge_weights_swapped": ("for (int c = 0; c < d; ++c) oa[c] = wa * oa[c] + wb * ob[c];",
                               "for (int c = 0; c < d; ++c) oa[c] = wb * oa[c] + wa * ob[c];"),
-    "step_wrong_source": ("if (!ring_block(P, t->n_chunks, b, h, i, t->src, s, o_s, &lse_s)) {",
-                          "if (!ring_block(P, t->n_chunks, b, h, i, t->rank, s, o_s, &lse_s)) {"),
+    "step_wrong_source": ("if (!ring_block(P, t->n_chunks, b, h, i, t->src, s, o_s, &lse_s, t->striped)) {",
+                          "if (!ring_block(P, t->n_chunks, b, h, i, t->rank, s, o_s, &lse_s, t->striped)) {"),
+    "stripes_as_blocks": ("if (striped) return p % N;", "if (striped) return p / (L / N);"),
     "transposed_score": ("s[j] = P->scale * dot(qi, k_row(P, b, g, j), P->d);\n    if (s[j] > m) m = s[j];\n  }\n  double sum",
                          "s[j] = P->scale * dot(q_row(P, b, h, j), k_row(P, b, g, i), P->d);\n    if (s[j] > m) m = s[j];\n  }\n  double sum"),
 }
@@ -51,8 +52,10 @@ def _quick_pins():
         ("gqa", lambda: [pins.test_gqa_equals_repeated_mha(c) for c in (False, True)]),
         ("fold", lambda: [pins.test_fold_gives_every_rank_equal_causal_work(n) for n in (2, 4)]),
         ("hand", lambda: [pins.test_hand_worked_example(m) for m in ("enc", "cau")]),
-        ("steps", lambda: [steps.test_steps_merged_in_ring_order_equal_plain(48, 3, c) for c in (False, True)]),
+        ("steps", lambda: [steps.test_steps_merged_in_ring_order_equal_plain(48, 3, c, st)
+                           for c in (False, True) for st in (False, True)]),
         ("merge", steps.test_merge_weights_are_a_sigmoid_of_the_lse_gap),
+        ("stripes", lambda: steps.test_striped_step_with_zero_queries_closed_form(3)),
     ]
     failed = []
     for name, fn in checks:

@@ -24,23 +24,24 @@ def _problem(B, Hq, Hkv, L, d, seed):
     return q, k, v
 
 
-def _rows_of(L, N, causal, r):
-    return np.array([p for p in range(L) if oracle.owner_rank(L, N, causal, p) == r])
+def _rows_of(L, N, causal, r, striped=False):
+    return np.array([p for p in range(L) if oracle.owner_rank(L, N, causal, p, striped) == r])
 
 
+@pytest.mark.parametrize("striped", [False, True])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("L,N", [(48, 2), (48, 3), (64, 4)])
-def test_steps_merged_in_ring_order_equal_plain(L, N, causal):
-    if causal and L % (2 * N):
+def test_steps_merged_in_ring_order_equal_plain(L, N, causal, striped):
+    if causal and not striped and L % (2 * N):
         pytest.skip("fold needs L % 2N == 0")
     q, k, v = _problem(1, 4, 2, L, 8, seed=10 * L + N + causal)
     o_ref, lse_ref = oracle.fwd(q, k, v, causal)
     for r in range(N):
-        rows = _rows_of(L, N, causal, r)
+        rows = _rows_of(L, N, causal, r, striped)
         o = np.zeros((1, 4, L, 8))
         lse = np.full((1, 4, L), -np.inf)
         for src in oracle.ring_sources(r, N):
-            o_s, lse_s = oracle.ring_step(q, k, v, causal, N, r, src)
+            o_s, lse_s = oracle.ring_step(q, k, v, causal, N, r, src, striped=striped)
             o, lse = oracle.merge(o, lse, o_s, lse_s)
         np.testing.assert_allclose(o[:, :, rows], o_ref[:, :, rows], rtol=0, atol=1e-12)
         np.testing.assert_allclose(lse[:, :, rows], lse_ref[:, :, rows], rtol=0, atol=1e-12)
@@ -125,3 +126,42 @@ def test_merge_is_symmetric_and_order_free():
         acc2 = oracle.merge(*acc2, *p)
     np.testing.assert_allclose(acc[0], acc2[0], rtol=0, atol=1e-13)
     np.testing.assert_allclose(acc[1], acc2[1], rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("L", [36, 60])
+def test_striped_ring_form_invariant_in_chunk_count(L):
+    """Striped attention: rank r owns positions r, r+N, ...; the ring form
+    still equals the plain definition for every N dividing L."""
+    q, k, v = _problem(1, 2, 1, L, 8, seed=L)
+    o, lse = oracle.fwd(q, k, v, True)
+    for n in [n for n in range(1, L + 1) if L % n == 0]:
+        o_r, lse_r = oracle.ring_fwd(q, k, v, True, n, striped=True)
+        np.testing.assert_allclose(o_r, o, rtol=0, atol=1e-12, err_msg=f"N={n}")
+        np.testing.assert_allclose(lse_r, lse, rtol=0, atol=1e-12, err_msg=f"N={n}")
+
+
+@pytest.mark.parametrize("N", [2, 3, 5])
+def test_striped_step_with_zero_queries_closed_form(N):
+    """q = 0 makes every score 0: a step's partial result is the mean of the
+    visible v rows and lse_s = log(their count).  With stripes, row i of
+    rank r (position r + N i) sees keys src + N j for j <= i if src <= r,
+    j <= i - 1 if src > r: the same triangle at every step, one diagonal
+    apart."""
+    C = 7
+    L = N * C
+    rng = np.random.default_rng(N)
+    q = np.zeros((1, 1, L, 4))
+    k = rng.standard_normal((1, 1, L, 4))
+    v = rng.standard_normal((1, 1, L, 4))
+    for r in range(N):
+        for src in range(N):
+            o_s, lse_s = oracle.ring_step(q, k, v, True, N, r, src, striped=True)
+            for i in range(C):
+                count = i + 1 if src <= r else i
+                pos = r + N * i
+                if count == 0:
+                    assert lse_s[0, 0, pos] == -np.inf and np.all(o_s[0, 0, pos] == 0)
+                    continue
+                keys = [src + N * j for j in range(count)]
+                assert abs(lse_s[0, 0, pos] - math.log(count)) < 1e-13
+                np.testing.assert_allclose(o_s[0, 0, pos], v[0, 0, keys].mean(axis=0), rtol=0, atol=1e-13)
