@@ -436,44 +436,54 @@ def run_ours(args, w):
     # multi-GPU ring runs it (every rank's step s in one launch, then the
     # log-sum-exp merge), on this GPU; its merge kernel is HBM-bound
     ring = None
-    if not args.no_ring_mode and w.L % (256 * w.n_chunks if w.causal else 128 * w.n_chunks) == 0:
-        o_r = torch.empty_like(qd)
-        lse_r = torch.empty_like(lse)
-        ws_r = torch.empty(ra.ring_fwd_workspace_size(w.B, w.Hq, w.Hkv, w.L, w.d, w.n_chunks, w.causal),
-                           dtype=torch.uint8, device=dev)
-        ring_fwd = lambda: ra.ring_attn_ring_fwd(qd, kd, vd, w.n_chunks, w.causal, o=o_r, lse=lse_r,  # noqa: E731
-                                                 workspace=ws_r, stream=stream)
-        ring_fwd()
-        torch.cuda.synchronize(dev)
-        r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        r0.record(stream)
-        for _ in range(args.steps):
+    if not args.no_ring_mode:
+        def measure_ring(striped):
+            o_r = torch.empty_like(qd)
+            lse_r = torch.empty_like(lse)
+            ws_r = torch.empty(ra.ring_fwd_workspace_size(w.B, w.Hq, w.Hkv, w.L, w.d, w.n_chunks, w.causal, striped),
+                               dtype=torch.uint8, device=dev)
+
+            def ring_fwd():
+                ra.ring_attn_ring_fwd(qd, kd, vd, w.n_chunks, w.causal, o=o_r, lse=lse_r, workspace=ws_r,
+                                      stream=stream, striped=striped)
             ring_fwd()
-        r1.record(stream)
-        torch.cuda.synchronize(dev)
-        ms_ring = r0.elapsed_time(r1) / args.steps
-        ra.profile_enable(True)
-        for _ in range(args.steps):
-            ring_fwd()
-        torch.cuda.synchronize(dev)
-        rp = ra.profile_read()
-        ra.profile_enable(False)
-        st, site = ra.device_status()
-        if st != 0:
-            raise RuntimeError(f"device status {st} at site {site:#x} in ring mode")
-        merge_ms, merge_n = rp["ring_merge"]
-        rows = w.B * w.Hq * w.L
-        merge_bytes = rows * (3 * w.d * 4 + 3 * 4)  # read o, o_s, lse, lse_s; write o, lse
-        merge_gbs = merge_bytes / (merge_ms / merge_n * 1e-3) / 1e9 if merge_n else None
-        ring = {
-            "fwd_ms": ms_ring, "fwd_tflops": F / (ms_ring * 1e-3) / 1e12,
-            "per_kernel_ms_per_fwd": {k: rp[k][0] / args.steps for k in ("ring_step", "ring_merge", "ring_io")},
-            "launches_per_fwd": {k: rp[k][1] // args.steps for k in ("ring_step", "ring_merge", "ring_io")},
-            "merge_roofline": {"bound": "hbm", "achieved": merge_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                               "frac": (merge_gbs / peaks["hbm_gbs"]) if merge_gbs else None,
-                               "bytes_per_launch": merge_bytes},
-        }
-        del o_r, lse_r, ws_r
+            torch.cuda.synchronize(dev)
+            r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            r0.record(stream)
+            for _ in range(args.steps):
+                ring_fwd()
+            r1.record(stream)
+            torch.cuda.synchronize(dev)
+            ms_ring = r0.elapsed_time(r1) / args.steps
+            ra.profile_enable(True)
+            for _ in range(args.steps):
+                ring_fwd()
+            torch.cuda.synchronize(dev)
+            rp = ra.profile_read()
+            ra.profile_enable(False)
+            st, site = ra.device_status()
+            if st != 0:
+                raise RuntimeError(f"device status {st} at site {site:#x} in ring mode")
+            merge_ms, merge_n = rp["ring_merge"]
+            rows = w.B * w.Hq * w.L
+            merge_bytes = rows * (3 * w.d * 4 + 3 * 4)  # read o, o_s, lse, lse_s; write o, lse
+            merge_gbs = merge_bytes / (merge_ms / merge_n * 1e-3) / 1e9 if merge_n else None
+            return {
+                "fwd_ms": ms_ring, "fwd_tflops": F / (ms_ring * 1e-3) / 1e12,
+                "per_kernel_ms_per_fwd": {k: rp[k][0] / args.steps for k in ("ring_step", "ring_merge", "ring_io")},
+                "launches_per_fwd": {k: rp[k][1] // args.steps for k in ("ring_step", "ring_merge", "ring_io")},
+                "merge_roofline": {"bound": "hbm", "achieved": merge_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                   "frac": (merge_gbs / peaks["hbm_gbs"]) if merge_gbs else None,
+                                   "bytes_per_launch": merge_bytes},
+            }
+
+        C = w.L // w.n_chunks
+        ring = {}
+        if (w.L // (2 * w.n_chunks) if w.causal else C) % 128 == 0 and (not w.causal or w.L % (2 * w.n_chunks) == 0):
+            ring["fold" if w.causal else "chunks"] = measure_ring(False)
+        if w.causal and w.L % w.n_chunks == 0 and C % 128 == 0:
+            ring["striped"] = measure_ring(True)
+        ring = ring or None
 
     # (5) CPU oracle baseline (rank 0, one GPU only)
     cpu = None

@@ -115,9 +115,12 @@ int ring_attn_bwd_noalloc(const void* q, const void* k, const void* v, const voi
  * with the online-softmax correction).  Rank r holds chunk r of the
  * sequence, in chunk order: rows [rC, (r+1)C), C = L / n_chunks, when
  * causal == 0; sub-chunk r followed by sub-chunk 2N-1-r, each L/(2N) rows,
- * when causal != 0 (the fold that balances causal work, section 8.2).
- * Chunks must be whole 128-row tiles -- C (causal == 0) or L/(2N) (causal)
- * a multiple of 128 -- else RING_ATTN_ERR_UNSUPPORTED.  Pointers are device
+ * when causal != 0 (the fold that balances causal work, section 8.2); with
+ * striped != 0, the positions r, r+N, r+2N, ... (striped attention, the
+ * causal schedule variant the pages compare with the fold; it needs only
+ * L % N == 0).  Chunks must be whole 128-row tiles -- C (causal == 0 or
+ * striped) or L/(2N) (the fold) a multiple of 128 -- else
+ * RING_ATTN_ERR_UNSUPPORTED.  Pointers are device
  * pointers, 16-byte aligned and owned by the caller; calls are asynchronous
  * on `stream`; argument errors return before anything is launched.
  * ------------------------------------------------------------------- */
@@ -135,7 +138,7 @@ int ring_attn_bwd_noalloc(const void* q, const void* k, const void* v, const voi
  *                                           gets lse_s = -inf and o_s = 0
  */
 int ring_attn_fwd_step(const void* q_chunk, const void* k_chunk, const void* v_chunk, float* o_s, float* lse_s,
-                       int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal, int rank, int src,
+                       int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal, int striped, int rank, int src,
                        cudaStream_t stream);
 
 /*
@@ -149,7 +152,8 @@ int ring_attn_merge(float* o, float* lse, const float* o_s, const float* lse_s, 
                     void* o_out, cudaStream_t stream);
 
 /* Workspace bytes ring_attn_ring_fwd needs for this shape, or 0 if invalid. */
-size_t ring_attn_ring_fwd_workspace_size(int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal);
+size_t ring_attn_ring_fwd_workspace_size(int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal,
+                                         int striped);
 
 /*
  * The whole ring on one GPU, every rank of it, the ring-mode way: q, k, v
@@ -163,7 +167,7 @@ size_t ring_attn_ring_fwd_workspace_size(int B, int Hq, int Hkv, int L, int d, i
  * partial result.
  */
 int ring_attn_ring_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
-                       int L, int d, int n_chunks, int causal, void* workspace, size_t workspace_bytes,
+                       int L, int d, int n_chunks, int causal, int striped, void* workspace, size_t workspace_bytes,
                        cudaStream_t stream);
 
 /* Static description of a status code. */
@@ -251,8 +255,8 @@ int ring_attn_bwd_plan(int L, int n_chunks, int causal, int* n_blocks, int* n_ra
  * ring_attn_fwd_plan, with n_blocks = blocks of one chunk.  Chunks must be
  * whole 128-row tiles (see ring mode above).
  */
-int ring_attn_step_plan(int L, int n_chunks, int causal, int step, int rank, int* n_blocks, int* n_ranges,
-                        int32_t* block_order, int32_t* range_offsets, int32_t* ranges);
+int ring_attn_step_plan(int L, int n_chunks, int causal, int striped, int step, int rank, int* n_blocks,
+                        int* n_ranges, int32_t* block_order, int32_t* range_offsets, int32_t* ranges);
 
 #ifdef __cplusplus
 }

@@ -71,15 +71,15 @@ def load():
     for f in (lib.ring_attn_fwd_plan, lib.ring_attn_bwd_plan):
         f.argtypes = [I, I, I, IP, IP, I32P, I32P, I32P]
         f.restype = I
-    lib.ring_attn_step_plan.argtypes = [I, I, I, I, I, IP, IP, I32P, I32P, I32P]
+    lib.ring_attn_step_plan.argtypes = [I, I, I, I, I, I, IP, IP, I32P, I32P, I32P]
     lib.ring_attn_step_plan.restype = I
-    lib.ring_attn_fwd_step.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, P]
+    lib.ring_attn_fwd_step.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, P]
     lib.ring_attn_fwd_step.restype = I
     lib.ring_attn_merge.argtypes = [P, P, P, P, ctypes.c_longlong, I, P, P]
     lib.ring_attn_merge.restype = I
-    lib.ring_attn_ring_fwd_workspace_size.argtypes = [I, I, I, I, I, I, I]
+    lib.ring_attn_ring_fwd_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
     lib.ring_attn_ring_fwd_workspace_size.restype = S
-    lib.ring_attn_ring_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, P, S, P]
+    lib.ring_attn_ring_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, P, S, P]
     lib.ring_attn_ring_fwd.restype = I
     _lib = lib
     return lib
@@ -113,11 +113,12 @@ def _plan(fn, L, n_chunks, causal):
     return {"order": order, "offsets": offsets, "ranges": ranges, "visits": visits}
 
 
-def step_plan(L: int, n_chunks: int, causal: bool, step: int, rank: int):
+def step_plan(L: int, n_chunks: int, causal: bool, step: int, rank: int, striped: bool = False):
     """Ring mode: per 256-row block of rank's chunk, the source chunk's tile
     ranges it visits at this step (chunk-local indices)."""
     fn = load().ring_attn_step_plan
-    return _plan(lambda L_, N_, c_, *rest: fn(L_, N_, c_, int(step), int(rank), *rest), L, n_chunks, causal)
+    return _plan(lambda L_, N_, c_, *rest: fn(L_, N_, c_, int(bool(striped)), int(step), int(rank), *rest),
+                 L, n_chunks, causal)
 
 
 def fwd_plan(L: int, n_chunks: int, causal: bool):
@@ -179,7 +180,7 @@ def ring_attn_fwd(q, k, v, n_chunks: int, causal: bool, o=None, lse=None, stream
 # ------------------------------------------------------------------ ring mode
 
 def ring_attn_fwd_step(q_chunk, k_chunk, v_chunk, n_chunks: int, causal: bool, rank: int, src: int, o_s=None,
-                       lse_s=None, stream=None):
+                       lse_s=None, stream=None, striped: bool = False):
     """One ring step of rank `rank` against the key/value chunk of rank `src`
     (chunks in chunk order, see include/ring_attn.h); returns the fp32
     partial result (o_s [B,Hq,C,d], lse_s [B,Hq,C])."""
@@ -194,8 +195,8 @@ def ring_attn_fwd_step(q_chunk, k_chunk, v_chunk, n_chunks: int, causal: bool, r
     _check_tensor(o_s, "o_s", torch.float32, (B, Hq, C, d))
     _check_tensor(lse_s, "lse_s", torch.float32, (B, Hq, C))
     rc = load().ring_attn_fwd_step(_ptr(q_chunk), _ptr(k_chunk), _ptr(v_chunk), _ptr(o_s), _ptr(lse_s), B, Hq, Hkv,
-                                   C * int(n_chunks), d, int(n_chunks), int(bool(causal)), int(rank), int(src),
-                                   _stream(stream))
+                                   C * int(n_chunks), d, int(n_chunks), int(bool(causal)), int(bool(striped)),
+                                   int(rank), int(src), _stream(stream))
     if rc != OK:
         raise RingAttnError(rc, "ring_attn_fwd_step")
     return o_s, lse_s
@@ -219,11 +220,13 @@ def ring_attn_merge(o, lse, o_s, lse_s, o_out=None, stream=None):
     return o, lse
 
 
-def ring_fwd_workspace_size(B, Hq, Hkv, L, d, n_chunks, causal) -> int:
-    return int(load().ring_attn_ring_fwd_workspace_size(B, Hq, Hkv, L, d, int(n_chunks), int(bool(causal))))
+def ring_fwd_workspace_size(B, Hq, Hkv, L, d, n_chunks, causal, striped: bool = False) -> int:
+    return int(load().ring_attn_ring_fwd_workspace_size(B, Hq, Hkv, L, d, int(n_chunks), int(bool(causal)),
+                                                         int(bool(striped))))
 
 
-def ring_attn_ring_fwd(q, k, v, n_chunks: int, causal: bool, o=None, lse=None, workspace=None, stream=None):
+def ring_attn_ring_fwd(q, k, v, n_chunks: int, causal: bool, o=None, lse=None, workspace=None, stream=None,
+                       striped: bool = False):
     """The forward of ring_attn_fwd computed the ring-mode way (every rank's
     steps as separate launches, merged step by step); returns (o, lse)."""
     import torch
@@ -236,11 +239,11 @@ def ring_attn_ring_fwd(q, k, v, n_chunks: int, causal: bool, o=None, lse=None, w
     lse = torch.empty((B, Hq, L), dtype=torch.float32, device=q.device) if lse is None else lse
     _check_tensor(o, "o", torch.bfloat16, (B, Hq, L, d))
     _check_tensor(lse, "lse", torch.float32, (B, Hq, L))
-    ws_bytes = ring_fwd_workspace_size(B, Hq, Hkv, L, d, n_chunks, causal)
+    ws_bytes = ring_fwd_workspace_size(B, Hq, Hkv, L, d, n_chunks, causal, striped)
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
     rc = load().ring_attn_ring_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, L, d, int(n_chunks),
-                                   int(bool(causal)), _ptr(workspace),
+                                   int(bool(causal)), int(bool(striped)), _ptr(workspace),
                                    int(workspace.numel() * workspace.element_size()), _stream(stream))
     if rc != OK:
         raise RingAttnError(rc, "ring_attn_ring_fwd")

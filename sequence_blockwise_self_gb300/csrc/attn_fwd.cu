@@ -79,18 +79,28 @@ struct FwdDev {
   // src * z_rank * B*Hkv + (b, kv head): z_rank = 1 for chunk-major buffers
   // holding every rank, 0 for buffers holding one chunk.  The output is the
   // normalised partial result in fp32 (o32 / the fp32 output map).
-  int step_nb, step, rank_lo, n_chunks, sub_len, z_rank;
+  int step_nb, step, rank_lo, n_chunks, sub_len, z_rank, striped;
   float* o32;
 };
 
-// Sequence position of row `local` of rank `rank`'s chunk, as far as the
-// causal mask needs it (the fold: sub-chunks `rank` and 2N-1-rank of
-// sub_len rows); rows of the whole sequence are their own positions.
+// Keys of the causal mask: key column i of a tile is visible to a query
+// row iff kv_key(tile) + i <= q_key(row).  Rows of the whole sequence use
+// their positions.  In ring steps with the fold they are the rows' sequence
+// positions (sub-chunks `rank` and 2N-1-rank of sub_len rows; a tile never
+// straddles the two).  With stripes (rank r owns r, r+N, ...), position
+// src + N j <= r + N i  <=>  j <= i - (src > r), so the keys are the local
+// rows, the key tile's shifted by one when its rank is above the query's.
 template <bool kStep>
-__device__ __forceinline__ int seq_pos(const FwdDev& p, int rank, int local) {
-  if (!kStep || !p.causal) return local;
+__device__ __forceinline__ int q_key(const FwdDev& p, int rank, int local) {
+  if (!kStep || !p.causal || p.striped) return local;
   return local < p.sub_len ? rank * p.sub_len + local
                            : (2 * p.n_chunks - 1 - rank) * p.sub_len + (local - p.sub_len);
+}
+template <bool kStep>
+__device__ __forceinline__ int kv_key(const FwdDev& p, int kv_rank, int q_rank, int kv0) {
+  if (!kStep || !p.causal) return kv0;
+  if (p.striped) return kv0 + (kv_rank > q_rank ? 1 : 0);
+  return q_key<kStep>(p, kv_rank, kv0);
 }
 
 // Wait that ignores the abort flag (used to drain in-flight copies/MMAs
@@ -225,7 +235,7 @@ __device__ void fwd_softmax(FwdSmem<D>& sm, uint32_t tmem, int t, const FwdDev& 
   const int lane = threadIdx.x & 31;
   const int row = wq * 32 + lane;
   const int qpos = q0 + 128 * t + row;        // row of the slice
-  const int qseq = seq_pos<kStep>(p, q_rank, qpos);  // its sequence position (causal mask)
+  const int qseq = q_key<kStep>(p, q_rank, qpos);  // its key for the causal mask
   const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
   const uint32_t t_s = tmem + 128 * t + lane_off;
   const uint32_t t_o = tmem + 256 + 128 * t + lane_off;
@@ -257,7 +267,7 @@ __device__ void fwd_softmax(FwdSmem<D>& sm, uint32_t tmem, int t, const FwdDev& 
         s[96 + i] = __uint_as_float(r3[i]);
       }
       const int kv0 = jt * 128;
-      const int kvseq = seq_pos<kStep>(p, kv_rank, kv0);  // tiles never straddle a sub-chunk
+      const int kvseq = kv_key<kStep>(p, kv_rank, q_rank, kv0);
       if (kv0 + 128 > p.L || (p.causal && kvseq + 127 > qseq)) {
         const int lim = min(p.L - 1 - kv0, p.causal ? qseq - kvseq : INT_MAX);  // valid columns: i <= lim
 #pragma unroll
@@ -525,7 +535,7 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
   p.order = a.order; p.offsets = a.offsets; p.ranges = a.ranges;
   p.lse = a.lse; p.err = a.err;
   p.step_nb = a.step_nb; p.step = a.step; p.rank_lo = a.rank_lo; p.n_chunks = a.n_chunks;
-  p.sub_len = a.sub_len; p.z_rank = a.z_rank; p.o32 = a.o32;
+  p.sub_len = a.sub_len; p.z_rank = a.z_rank; p.striped = a.striped; p.o32 = a.o32;
   const size_t smem = fwd_smem_bytes(a.d);
   const dim3 grid(static_cast<unsigned>(a.n_blocks) * a.B * a.Hq);
   cudaError_t e;

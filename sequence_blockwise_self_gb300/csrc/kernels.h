@@ -42,7 +42,7 @@ struct FwdArgs {
   LaunchTimer* timer;       // nullptr unless profiling
   // ring step mode (step_nb > 0; L is then the chunk length, n_blocks the
   // number of items, tm_o an fp32 map with 32-column boxes, see attn_fwd.cu)
-  int step_nb = 0, step = 0, rank_lo = 0, n_chunks = 1, sub_len = 0, z_rank = 0;
+  int step_nb = 0, step = 0, rank_lo = 0, n_chunks = 1, sub_len = 0, z_rank = 0, striped = 0;
   float* o32 = nullptr;
 };
 
@@ -105,10 +105,10 @@ cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
 // [N][Z][C][d] (+ lse [N][Z][C]) back to sequence order as bf16 (+ lse).
 cudaError_t launch_ring_merge(float* o, float* lse, const float* o_s, const float* lse_s, void* o_out,
                               long long n_rows, int d, cudaStream_t stream);
-cudaError_t launch_ring_gather(const void* src, void* dst, int Z, int L, int d, int N, bool causal,
+cudaError_t launch_ring_gather(const void* src, void* dst, int Z, int L, int d, int N, bool causal, bool striped,
                                cudaStream_t stream);
 cudaError_t launch_ring_scatter(const float* acc, const float* lse_acc, void* o, float* lse, int Z, int L, int d,
-                                int N, bool causal, cudaStream_t stream);
+                                int N, bool causal, bool striped, cudaStream_t stream);
 
 // Dynamic shared memory each kernel needs (bytes), for the C ABI's checks.
 size_t fwd_smem_bytes(int d);

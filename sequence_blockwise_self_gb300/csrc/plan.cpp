@@ -90,7 +90,7 @@ Plan build_bwd_plan(int L, int N, bool causal) {
   return p;
 }
 
-Plan build_step_plan(int L, int N, bool causal, int step, int rank_lo, int rank_hi) {
+Plan build_step_plan(int L, int N, bool causal, bool striped, int step, int rank_lo, int rank_hi) {
   Plan p;
   const int C = L / N;
   const int nt = C / kTileRows;                       // tiles per chunk
@@ -107,7 +107,8 @@ Plan build_step_plan(int L, int N, bool causal, int step, int rank_lo, int rank_
       for (int kt = 0; kt < nt; ++kt) {
         bool seen = !causal;
         for (int qt = 2 * u; qt < 2 * u + 2 && qt < nt && !seen; ++qt)
-          seen = chunk_pos(L, N, true, src, kt * kTileRows) <= chunk_pos(L, N, true, r, qt * kTileRows + kTileRows - 1);
+          seen = chunk_pos(L, N, true, striped, src, kt * kTileRows) <=
+                 chunk_pos(L, N, true, striped, r, qt * kTileRows + kTileRows - 1);
         if (seen) tiles.push_back(kt);
       }
       append_ranges(tiles, p.ranges);

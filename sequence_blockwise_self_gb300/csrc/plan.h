@@ -62,18 +62,21 @@ Plan build_bwd_plan(int L, int N, bool causal);
 // ----------------------------------------------------------- ring step mode
 // One ring step run explicitly, as each rank of a multi-GPU ring would: rank
 // r holds its chunk of C = L/N rows in chunk order (encoder: rows [rC,
-// (r+1)C); causal: sub-chunk r, then sub-chunk 2N-1-r, each L/(2N) rows),
-// and at step s the key/value chunk of rank (r - s) mod N.
+// (r+1)C); causal: sub-chunk r, then sub-chunk 2N-1-r, each L/(2N) rows;
+// striped: positions r, r+N, r+2N, ...), and at step s the key/value chunk
+// of rank (r - s) mod N.
 
-// Chunks must be whole 128-row tiles: C (encoder) or the sub-chunk length
-// (causal) a multiple of 128.
-inline bool step_chunking_ok(int L, int N, bool causal) {
+// Chunks must be whole 128-row tiles: C (encoder, striped) or the
+// sub-chunk length (causal fold) a multiple of 128.
+inline bool step_chunking_ok(int L, int N, bool causal, bool striped) {
+  if (striped) return N >= 1 && L >= N && L % N == 0 && (L / N) % kTileRows == 0;
   if (!chunking_ok(L, N, causal)) return false;
   return (causal ? L / (2 * N) : L / N) % kTileRows == 0;
 }
 
 // Sequence position of row `local` of rank `rank`'s chunk.
-RA_HOST_DEVICE inline int chunk_pos(int L, int N, bool causal, int rank, int local) {
+RA_HOST_DEVICE inline int chunk_pos(int L, int N, bool causal, bool striped, int rank, int local) {
+  if (striped) return rank + N * local;
   if (!causal) return rank * (L / N) + local;
   const int c = L / (2 * N);
   return local < c ? rank * c + local : (2 * N - 1 - rank) * c + (local - c);
@@ -84,6 +87,6 @@ RA_HOST_DEVICE inline int chunk_pos(int L, int N, bool causal, int rank, int loc
 // the source rank's key/value chunk (chunk-local indices, ascending) that
 // hold a key some query row of the block may see.  An item may list none
 // (a causal block entirely before the source's keys).
-Plan build_step_plan(int L, int N, bool causal, int step, int rank_lo, int rank_hi);
+Plan build_step_plan(int L, int N, bool causal, bool striped, int step, int rank_lo, int rank_hi);
 
 }  // namespace ra

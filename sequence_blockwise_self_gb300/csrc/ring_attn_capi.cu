@@ -30,8 +30,8 @@ struct DevicePlan {
 };
 
 std::map<std::tuple<int, int, int, int, int>, DevicePlan> g_plans;  // (device, kind, L, N, causal)
-// ring step plans: (device, L, N, causal, step, first rank, end rank)
-std::map<std::tuple<int, int, int, int, int, int, int>, DevicePlan> g_step_plans;
+// ring step plans: (device, L, N, causal, striped, step, first rank, end rank)
+std::map<std::tuple<int, int, int, int, int, int, int, int>, DevicePlan> g_step_plans;
 std::map<int, int*> g_status_ptr;                                   // device -> &g_device_status
 
 // Event pairs around launches while profiling is on.
@@ -148,25 +148,27 @@ int status_ptr(int dev, int** out) {
   return RING_ATTN_OK;
 }
 
-int get_step_plan(int dev, int L, int N, int causal, int step, int rank_lo, int rank_hi, DevicePlan* out) {
-  auto key = std::make_tuple(dev, L, N, causal, step, rank_lo, rank_hi);
+int get_step_plan(int dev, int L, int N, int causal, int striped, int step, int rank_lo, int rank_hi,
+                  DevicePlan* out) {
+  auto key = std::make_tuple(dev, L, N, causal, striped, step, rank_lo, rank_hi);
   auto it = g_step_plans.find(key);
   if (it != g_step_plans.end()) {
     *out = it->second;
     return RING_ATTN_OK;
   }
   DevicePlan dp;
-  int rc = upload_plan(build_step_plan(L, N, causal != 0, step, rank_lo, rank_hi), &dp);
+  int rc = upload_plan(build_step_plan(L, N, causal != 0, striped != 0, step, rank_lo, rank_hi), &dp);
   if (rc != RING_ATTN_OK) return rc;
   g_step_plans[key] = dp;
   *out = dp;
   return RING_ATTN_OK;
 }
 
-int check_ring_shape(int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal) {
-  int rc = check_shape(B, Hq, Hkv, L, d, n_chunks, causal);
+int check_ring_shape(int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal, int striped) {
+  // stripes need only L % N == 0 (the fold L % 2N)
+  int rc = check_shape(B, Hq, Hkv, L, d, n_chunks, striped ? 0 : causal);
   if (rc != RING_ATTN_OK) return rc;
-  if (L > 0 && !step_chunking_ok(L, n_chunks, causal != 0)) return RING_ATTN_ERR_UNSUPPORTED;
+  if (L > 0 && !step_chunking_ok(L, n_chunks, causal != 0, striped != 0)) return RING_ATTN_ERR_UNSUPPORTED;
   if (static_cast<long long>(n_chunks) * B * Hq >= 65536) return RING_ATTN_ERR_UNSUPPORTED;
   return RING_ATTN_OK;
 }
@@ -175,7 +177,7 @@ int check_ring_shape(int B, int Hq, int Hkv, int L, int d, int n_chunks, int cau
 // z_rank = 1 the buffers hold every rank's chunk ([N][B][H][C][d]), with
 // z_rank = 0 only the chunks of the one rank and its source.
 int launch_step(int dev, const void* q, const void* k, const void* v, float* o_s, float* lse_s, int B, int Hq,
-                int Hkv, int L, int d, int N, int causal, int step, int rank_lo, int rank_hi, int z_rank,
+                int Hkv, int L, int d, int N, int causal, int striped, int step, int rank_lo, int rank_hi, int z_rank,
                 cudaStream_t stream) {
   const int C = L / N;
   const int zq = (z_rank ? N : 1) * B * Hq, zkv = (z_rank ? N : 1) * B * Hkv;
@@ -187,7 +189,7 @@ int launch_step(int dev, const void* q, const void* k, const void* v, float* o_s
       !make_map(&a.tm_o, o_s, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, C, zq, 32))
     return RING_ATTN_ERR_CUDA;
   DevicePlan plan;
-  int rc = get_step_plan(dev, L, N, causal, step, rank_lo, rank_hi, &plan);
+  int rc = get_step_plan(dev, L, N, causal, striped, step, rank_lo, rank_hi, &plan);
   if (rc != RING_ATTN_OK) return rc;
   int* err;
   if ((rc = status_ptr(dev, &err)) != RING_ATTN_OK) return rc;
@@ -197,8 +199,8 @@ int launch_step(int dev, const void* q, const void* k, const void* v, float* o_s
   a.lse = lse_s; a.err = err; a.timer = active_timer();
   a.step_nb = (C + kQBlockRows - 1) / kQBlockRows;
   a.step = step; a.rank_lo = rank_lo; a.n_chunks = N;
-  a.sub_len = causal ? L / (2 * N) : 0;
-  a.z_rank = z_rank; a.o32 = o_s;
+  a.sub_len = (causal && !striped) ? L / (2 * N) : 0;
+  a.z_rank = z_rank; a.striped = striped != 0; a.o32 = o_s;
   return launch_fwd(a, stream) == cudaSuccess ? RING_ATTN_OK : RING_ATTN_ERR_CUDA;
 }
 
@@ -280,12 +282,13 @@ int ring_attn_bwd_plan(int L, int n_chunks, int causal, int* n_blocks, int* n_ra
   return plan_query(1, L, n_chunks, causal, n_blocks, n_ranges, block_order, range_offsets, ranges);
 }
 
-int ring_attn_step_plan(int L, int n_chunks, int causal, int step, int rank, int* n_blocks, int* n_ranges,
-                        int32_t* block_order, int32_t* range_offsets, int32_t* ranges) {
-  if (L <= 0 || n_chunks <= 0 || !chunking_ok(L, n_chunks, causal != 0)) return RING_ATTN_ERR_SHAPE;
-  if (!step_chunking_ok(L, n_chunks, causal != 0)) return RING_ATTN_ERR_UNSUPPORTED;
+int ring_attn_step_plan(int L, int n_chunks, int causal, int striped, int step, int rank, int* n_blocks,
+                        int* n_ranges, int32_t* block_order, int32_t* range_offsets, int32_t* ranges) {
+  if (L <= 0 || n_chunks <= 0 || !chunking_ok(L, n_chunks, striped ? false : causal != 0))
+    return RING_ATTN_ERR_SHAPE;
+  if (!step_chunking_ok(L, n_chunks, causal != 0, striped != 0)) return RING_ATTN_ERR_UNSUPPORTED;
   if (step < 0 || step >= n_chunks || rank < 0 || rank >= n_chunks) return RING_ATTN_ERR_SHAPE;
-  Plan p = build_step_plan(L, n_chunks, causal != 0, step, rank, rank + 1);
+  Plan p = build_step_plan(L, n_chunks, causal != 0, striped != 0, step, rank, rank + 1);
   if (n_blocks) *n_blocks = p.n_blocks;
   if (n_ranges) *n_ranges = static_cast<int>(p.ranges.size() / 2);
   if (block_order) std::memcpy(block_order, p.order.data(), p.order.size() * sizeof(int32_t));
@@ -426,9 +429,9 @@ int ring_attn_profile_read(double* ms, long long* launches) {
 }
 
 int ring_attn_fwd_step(const void* q_chunk, const void* k_chunk, const void* v_chunk, float* o_s, float* lse_s,
-                       int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal, int rank, int src,
+                       int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal, int striped, int rank, int src,
                        cudaStream_t stream) {
-  int rc = check_ring_shape(B, Hq, Hkv, L, d, n_chunks, causal);
+  int rc = check_ring_shape(B, Hq, Hkv, L, d, n_chunks, causal, striped);
   if (rc != RING_ATTN_OK) return rc;
   if (rank < 0 || rank >= n_chunks || src < 0 || src >= n_chunks) return RING_ATTN_ERR_SHAPE;
   if (B == 0 || L == 0) return RING_ATTN_OK;
@@ -439,8 +442,8 @@ int ring_attn_fwd_step(const void* q_chunk, const void* k_chunk, const void* v_c
   int dev;
   if ((rc = current_device(&dev)) != RING_ATTN_OK) return rc;
   const int step = ((rank - src) % n_chunks + n_chunks) % n_chunks;
-  return launch_step(dev, q_chunk, k_chunk, v_chunk, o_s, lse_s, B, Hq, Hkv, L, d, n_chunks, causal, step, rank,
-                     rank + 1, 0, stream);
+  return launch_step(dev, q_chunk, k_chunk, v_chunk, o_s, lse_s, B, Hq, Hkv, L, d, n_chunks, causal, striped, step,
+                     rank, rank + 1, 0, stream);
 }
 
 int ring_attn_merge(float* o, float* lse, const float* o_s, const float* lse_s, long long n_rows, int d,
@@ -457,15 +460,16 @@ int ring_attn_merge(float* o, float* lse, const float* o_s, const float* lse_s, 
   return e == cudaSuccess ? RING_ATTN_OK : RING_ATTN_ERR_CUDA;
 }
 
-size_t ring_attn_ring_fwd_workspace_size(int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal) {
-  if (check_ring_shape(B, Hq, Hkv, L, d, n_chunks, causal) != RING_ATTN_OK) return 0;
+size_t ring_attn_ring_fwd_workspace_size(int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal,
+                                         int striped) {
+  if (check_ring_shape(B, Hq, Hkv, L, d, n_chunks, causal, striped) != RING_ATTN_OK) return 0;
   return ring_workspace(B, Hq, Hkv, L, d).total;
 }
 
 int ring_attn_ring_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
-                       int L, int d, int n_chunks, int causal, void* workspace, size_t workspace_bytes,
+                       int L, int d, int n_chunks, int causal, int striped, void* workspace, size_t workspace_bytes,
                        cudaStream_t stream) {
-  int rc = check_ring_shape(B, Hq, Hkv, L, d, n_chunks, causal);
+  int rc = check_ring_shape(B, Hq, Hkv, L, d, n_chunks, causal, striped);
   if (rc != RING_ATTN_OK) return rc;
   if (B == 0 || L == 0) return RING_ATTN_OK;
   if (!q || !k || !v || !o || !lse) return RING_ATTN_ERR_NULL;
@@ -488,16 +492,17 @@ int ring_attn_ring_fwd(const void* q, const void* k, const void* v, void* o, flo
   const int N = n_chunks;
   LaunchTimer* t = active_timer();
   if (t) t->mark(RING_ATTN_KERNEL_RING_IO, false, stream);
-  if (launch_ring_gather(q, qc, B * Hq, L, d, N, causal != 0, stream) != cudaSuccess ||
-      launch_ring_gather(k, kc, B * Hkv, L, d, N, causal != 0, stream) != cudaSuccess ||
-      launch_ring_gather(v, vc, B * Hkv, L, d, N, causal != 0, stream) != cudaSuccess)
+  const bool sc = causal != 0, st = striped != 0;
+  if (launch_ring_gather(q, qc, B * Hq, L, d, N, sc, st, stream) != cudaSuccess ||
+      launch_ring_gather(k, kc, B * Hkv, L, d, N, sc, st, stream) != cudaSuccess ||
+      launch_ring_gather(v, vc, B * Hkv, L, d, N, sc, st, stream) != cudaSuccess)
     return RING_ATTN_ERR_CUDA;
   if (t) t->mark(RING_ATTN_KERNEL_RING_IO, true, stream);
   const long long rows = static_cast<long long>(B) * Hq * L;
   for (int s = 0; s < N; ++s) {
     // step 0 (every rank's own chunk) starts the running result
-    if ((rc = launch_step(dev, qc, kc, vc, s == 0 ? oacc : os, s == 0 ? lacc : ls, B, Hq, Hkv, L, d, N, causal, s,
-                          0, N, 1, stream)) != RING_ATTN_OK)
+    if ((rc = launch_step(dev, qc, kc, vc, s == 0 ? oacc : os, s == 0 ? lacc : ls, B, Hq, Hkv, L, d, N, causal,
+                          striped, s, 0, N, 1, stream)) != RING_ATTN_OK)
       return rc;
     if (s > 0) {
       if (t) t->mark(RING_ATTN_KERNEL_RING_MERGE, false, stream);
@@ -506,7 +511,7 @@ int ring_attn_ring_fwd(const void* q, const void* k, const void* v, void* o, flo
     }
   }
   if (t) t->mark(RING_ATTN_KERNEL_RING_IO, false, stream);
-  if (launch_ring_scatter(oacc, lacc, o, lse, B * Hq, L, d, N, causal != 0, stream) != cudaSuccess)
+  if (launch_ring_scatter(oacc, lacc, o, lse, B * Hq, L, d, N, sc, st, stream) != cudaSuccess)
     return RING_ATTN_ERR_CUDA;
   if (t) t->mark(RING_ATTN_KERNEL_RING_IO, true, stream);
   return RING_ATTN_OK;

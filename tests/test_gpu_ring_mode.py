@@ -36,36 +36,45 @@ def assert_status_ok():
     assert st == 0, f"device status {st} at site {site:#x}"
 
 
-def chunk_positions(L, N, causal, r):
-    return torch.tensor([p for p in range(L) if oracle.owner_rank(L, N, causal, p) == r], dtype=torch.long)
+def chunk_positions(L, N, causal, r, striped=False):
+    return torch.tensor([p for p in range(L) if oracle.owner_rank(L, N, causal, p, striped) == r], dtype=torch.long)
 
 
-# (B, Hq, Hkv, L, d, N, causal): chunks of whole 128-row tiles
+def case_id(c):
+    return "B{}Hq{}Hkv{}L{}d{}N{}".format(*c[:6]) + ("c" if c[6] else "e") + ("s" if c[7] else "")
+
+
+# (B, Hq, Hkv, L, d, N, causal, striped): chunks of whole 128-row tiles
 STEP_CASES = [
-    (1, 4, 2, 1024, 128, 4, True),    # sub-chunks of one tile: every block spans both
-    (2, 2, 1, 1024, 64, 4, False),
-    (1, 2, 2, 1536, 128, 3, True),    # sub-chunks of two tiles
-    (1, 2, 1, 768, 64, 3, False),
-    (1, 3, 1, 3072, 128, 4, True),    # sub-chunks of three tiles: a block straddles them
+    (1, 4, 2, 1024, 128, 4, True, False),    # sub-chunks of one tile: every block spans both
+    (2, 2, 1, 1024, 64, 4, False, False),
+    (1, 2, 2, 1536, 128, 3, True, False),    # sub-chunks of two tiles
+    (1, 2, 1, 768, 64, 3, False, False),
+    (1, 3, 1, 3072, 128, 4, True, False),    # sub-chunks of three tiles: a block straddles them
+    (1, 4, 2, 1024, 128, 4, True, True),     # stripes: every step the same tile triangle
+    (1, 2, 1, 1536, 64, 3, True, True),
+    (1, 3, 1, 1280, 128, 5, True, True),     # L % 2N != 0: stripes only
+    (1, 2, 2, 1024, 64, 8, False, True),
 ]
 
 
-@pytest.mark.parametrize("case", STEP_CASES, ids=lambda c: "B{}Hq{}Hkv{}L{}d{}N{}{}".format(*c[:6], "c" if c[6] else "e"))
+@pytest.mark.parametrize("case", STEP_CASES, ids=case_id)
 def test_every_step_of_a_small_ring_matches_the_oracle(case):
-    B, Hq, Hkv, L, d, N, causal = case
+    B, Hq, Hkv, L, d, N, causal, striped = case
     q, k, v, _ = inputs.make_inputs(B, Hq, Hkv, L, d, seed=sum(case[:6]))
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
     for r in range(N):
-        rows = chunk_positions(L, N, causal, r)
+        rows = chunk_positions(L, N, causal, r, striped)
         q_chunk = qd[:, :, rows.cuda()].contiguous()
         for src in range(N):
-            srows = chunk_positions(L, N, causal, src)
+            srows = chunk_positions(L, N, causal, src, striped)
             k_chunk = kd[:, :, srows.cuda()].contiguous()
             v_chunk = vd[:, :, srows.cuda()].contiguous()
-            o_s, lse_s = ra.ring_attn_fwd_step(q_chunk, k_chunk, v_chunk, N, causal, r, src)
+            o_s, lse_s = ra.ring_attn_fwd_step(q_chunk, k_chunk, v_chunk, N, causal, r, src, striped=striped)
             torch.cuda.synchronize()
             assert_status_ok()
-            o_ref, lse_ref = oracle.ring_step(q.double(), k.double(), v.double(), causal, N, r, src)
+            o_ref, lse_ref = oracle.ring_step(q.double(), k.double(), v.double(), causal, N, r, src,
+                                              striped=striped)
             o_ref, lse_ref = o_ref[:, :, rows.numpy()], lse_ref[:, :, rows.numpy()]
             got_o, got_l = f64(o_s), f64(lse_s)
             empty = np.isneginf(lse_ref)
@@ -103,23 +112,25 @@ def test_merge_matches_the_oracle(d):
     assert torch.equal(o_out.cpu(), o.cpu().to(torch.bfloat16))
 
 
-# (B, Hq, Hkv, L, d, N, causal)
+# (B, Hq, Hkv, L, d, N, causal, striped)
 RING_CASES = [
-    (1, 4, 2, 1024, 128, 4, True),
-    (2, 2, 1, 1024, 64, 4, False),
-    (1, 3, 1, 3072, 128, 4, True),
-    (1, 4, 4, 4096, 64, 8, False),
-    (1, 2, 2, 1024, 128, 1, True),   # one rank: a single step, nothing to merge
+    (1, 4, 2, 1024, 128, 4, True, False),
+    (2, 2, 1, 1024, 64, 4, False, False),
+    (1, 3, 1, 3072, 128, 4, True, False),
+    (1, 4, 4, 4096, 64, 8, False, False),
+    (1, 2, 2, 1024, 128, 1, True, False),   # one rank: a single step, nothing to merge
+    (1, 4, 2, 1024, 128, 4, True, True),
+    (1, 2, 1, 1280, 128, 5, True, True),
 ]
 
 
-@pytest.mark.parametrize("case", RING_CASES, ids=lambda c: "B{}Hq{}Hkv{}L{}d{}N{}{}".format(*c[:6], "c" if c[6] else "e"))
+@pytest.mark.parametrize("case", RING_CASES, ids=case_id)
 def test_whole_ring_on_one_gpu_matches_the_oracle_and_the_fused_kernel(case):
-    B, Hq, Hkv, L, d, N, causal = case
+    B, Hq, Hkv, L, d, N, causal, striped = case
     q, k, v, _ = inputs.make_inputs(B, Hq, Hkv, L, d, seed=7 + sum(case[:6]))
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
-    o, lse = ra.ring_attn_ring_fwd(qd, kd, vd, N, causal)
-    o_f, lse_f = ra.ring_attn_fwd(qd, kd, vd, N, causal)
+    o, lse = ra.ring_attn_ring_fwd(qd, kd, vd, N, causal, striped=striped)
+    o_f, lse_f = ra.ring_attn_fwd(qd, kd, vd, N if not striped or L % (2 * N) == 0 else 1, causal)
     torch.cuda.synchronize()
     assert_status_ok()
     o_ref, lse_ref = oracle.fwd(q.double(), k.double(), v.double(), causal)
@@ -129,11 +140,12 @@ def test_whole_ring_on_one_gpu_matches_the_oracle_and_the_fused_kernel(case):
     check_fp32("lse (ring mode vs fused)", f64(lse), f64(lse_f), TOL_LSE)
 
 
-def test_ring_mode_at_32k_on_sampled_rows():
+@pytest.mark.parametrize("striped", [False, True])
+def test_ring_mode_at_32k_on_sampled_rows(striped):
     w = inputs.WORKLOADS["gqa_32k"]
     q, k, v, _ = inputs.workload_inputs(w)
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
-    o, lse = ra.ring_attn_ring_fwd(qd, kd, vd, w.n_chunks, w.causal)
+    o, lse = ra.ring_attn_ring_fwd(qd, kd, vd, w.n_chunks, w.causal, striped=striped)
     torch.cuda.synchronize()
     assert_status_ok()
     rows = inputs.sample_rows(w.L, w.n_chunks, w.causal, 64, seed=5)

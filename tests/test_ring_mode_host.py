@@ -16,25 +16,27 @@ def lib():
     return capi.load()
 
 
-def _chunk_positions(L, N, causal, r):
+def _chunk_positions(L, N, causal, r, striped=False):
     """Sequence positions of rank r's rows in chunk order (ascending: for the
-    fold that is sub-chunk r, then sub-chunk 2N-1-r)."""
-    return np.array([p for p in range(L) if oracle.owner_rank(L, N, causal, p) == r])
+    fold that is sub-chunk r, then sub-chunk 2N-1-r; r, r+N, ... striped)."""
+    return np.array([p for p in range(L) if oracle.owner_rank(L, N, causal, p, striped) == r])
 
 
-CASES = [(1024, 4, True), (1024, 4, False), (2048, 4, True), (1536, 3, True), (3072, 8, False), (4096, 8, True)]
+CASES = [(1024, 4, True, False), (1024, 4, False, False), (2048, 4, True, False), (1536, 3, True, False),
+         (3072, 8, False, False), (4096, 8, True, False), (1024, 4, True, True), (1536, 3, True, True),
+         (2048, 8, True, True), (1024, 8, False, True)]
 
 
-@pytest.mark.parametrize("L,N,causal", CASES)
-def test_step_plan_lists_exactly_the_visible_tile_pairs(lib, L, N, causal):
+@pytest.mark.parametrize("L,N,causal,striped", CASES)
+def test_step_plan_lists_exactly_the_visible_tile_pairs(lib, L, N, causal, striped):
     C = L // N
     nt = C // 128
     for r in range(N):
-        qpos = _chunk_positions(L, N, causal, r)
+        qpos = _chunk_positions(L, N, causal, r, striped)
         for s in range(N):
             src = (r - s) % N
-            kpos = _chunk_positions(L, N, causal, src)
-            plan = capi.step_plan(L, N, causal, s, r)
+            kpos = _chunk_positions(L, N, causal, src, striped)
+            plan = capi.step_plan(L, N, causal, s, r, striped)
             assert len(plan["visits"]) == (C + 255) // 256
             assert sorted(plan["order"].tolist()) == list(range(len(plan["visits"])))
             for u, visits in enumerate(plan["visits"]):
@@ -50,19 +52,20 @@ def test_step_plan_lists_exactly_the_visible_tile_pairs(lib, L, N, causal):
                 assert set(listed) == want, (r, s, u)
 
 
+@pytest.mark.parametrize("striped", [False, True])
 @pytest.mark.parametrize("N", [2, 4, 8])
-def test_fold_gives_every_causal_step_the_same_work(lib, N):
+def test_fold_and_stripes_give_every_causal_step_the_same_work(lib, N, striped):
     """Section 8.2 of the pages: with the fold every rank does the same work
     at every step s > 0 (half of a chunk pair's tiles); step 0 is the
-    diagonal pair."""
+    diagonal pair.  With stripes every step is the same tile triangle."""
     L = 256 * N
     nt = L // N // 128
     works = {}
     for s in range(N):
         for r in range(N):
-            qpos = _chunk_positions(L, N, True, r)
-            kpos = _chunk_positions(L, N, True, (r - s) % N)
-            plan = capi.step_plan(L, N, True, s, r)
+            qpos = _chunk_positions(L, N, True, r, striped)
+            kpos = _chunk_positions(L, N, True, (r - s) % N, striped)
+            plan = capi.step_plan(L, N, True, s, r, striped)
             pairs = 0  # (query tile, listed key tile) pairs with a visible position pair
             for u, visits in enumerate(plan["visits"]):
                 for qt in (2 * u, 2 * u + 1):
@@ -82,8 +85,8 @@ P256 = ctypes.c_void_p(256)
 
 
 def test_step_rejects_bad_arguments(lib):
-    def step(L=1024, N=4, causal=1, rank=0, src=0, d=64, ptr=P256):
-        return lib.ring_attn_fwd_step(ptr, ptr, ptr, ptr, ptr, 1, 2, 1, L, d, N, causal, rank, src, NUL)
+    def step(L=1024, N=4, causal=1, rank=0, src=0, d=64, ptr=P256, striped=0):
+        return lib.ring_attn_fwd_step(ptr, ptr, ptr, ptr, ptr, 1, 2, 1, L, d, N, causal, striped, rank, src, NUL)
     assert step(rank=4) == capi.ERR_SHAPE
     assert step(src=-1) == capi.ERR_SHAPE
     assert step(L=1001) == capi.ERR_SHAPE                 # L % 2N
@@ -92,7 +95,14 @@ def test_step_rejects_bad_arguments(lib):
     assert step(L=512, N=4, causal=0, ptr=NUL) == capi.ERR_NULL  # chunks of 128 rows: whole tiles
     assert step(d=96) == capi.ERR_UNSUPPORTED
     assert step(ptr=ctypes.c_void_p(8)) == capi.ERR_UNSUPPORTED
-    assert lib.ring_attn_fwd_step(NUL, NUL, NUL, NUL, NUL, 0, 2, 1, 1024, 64, 4, 1, 0, 0, NUL) == capi.OK
+    assert lib.ring_attn_fwd_step(NUL, NUL, NUL, NUL, NUL, 0, 2, 1, 1024, 64, 4, 1, 0, 0, 0, NUL) == capi.OK
+    # stripes need L % N only, and chunks of whole tiles
+    assert step(L=1536, N=4) == capi.ERR_UNSUPPORTED                     # fold: sub-chunks of 192 rows
+    assert step(L=1536, N=4, striped=1, ptr=NUL) == capi.ERR_NULL        # stripes: chunks of 384 rows
+    assert step(L=1280, N=5, striped=1, ptr=NUL) == capi.ERR_NULL        # L % 2N != 0 is fine for stripes
+    assert step(L=1000, N=4, striped=1) == capi.ERR_UNSUPPORTED          # chunks of 250 rows
+    assert step(L=1001, N=4, striped=1) == capi.ERR_SHAPE                # L % N
+
 
 
 def test_merge_rejects_bad_arguments(lib):
@@ -104,14 +114,15 @@ def test_merge_rejects_bad_arguments(lib):
 
 
 def test_ring_fwd_workspace_and_arguments(lib):
-    ws = lib.ring_attn_ring_fwd_workspace_size(1, 2, 1, 1024, 64, 4, 1)
+    ws = lib.ring_attn_ring_fwd_workspace_size(1, 2, 1, 1024, 64, 4, 1, 0)
     # q, k, v in chunk order (bf16), running result and one partial (fp32 o + lse)
     rows_q, rows_kv = 2 * 1024, 1024
     assert ws == rows_q * 64 * 2 + 2 * rows_kv * 64 * 2 + 2 * (rows_q * 64 * 4 + rows_q * 4)
-    assert lib.ring_attn_ring_fwd_workspace_size(1, 2, 1, 512, 64, 4, 1) == 0  # not whole tiles
+    assert lib.ring_attn_ring_fwd_workspace_size(1, 2, 1, 512, 64, 4, 1, 0) == 0  # not whole tiles
+    assert lib.ring_attn_ring_fwd_workspace_size(1, 2, 1, 512, 64, 4, 1, 1) == ws // 2  # stripes of 128 rows
     args = [P256] * 5
-    assert lib.ring_attn_ring_fwd(*args, 1, 2, 1, 1024, 64, 4, 1, NUL, ws, NUL) == capi.ERR_WORKSPACE
-    assert lib.ring_attn_ring_fwd(*args, 1, 2, 1, 1024, 64, 4, 1, P256, ws - 1, NUL) == capi.ERR_WORKSPACE
-    assert lib.ring_attn_ring_fwd(*args, 1, 2, 1, 1024, 64, 4, 1, ctypes.c_void_p(272), ws, NUL) == \
+    assert lib.ring_attn_ring_fwd(*args, 1, 2, 1, 1024, 64, 4, 1, 0, NUL, ws, NUL) == capi.ERR_WORKSPACE
+    assert lib.ring_attn_ring_fwd(*args, 1, 2, 1, 1024, 64, 4, 1, 0, P256, ws - 1, NUL) == capi.ERR_WORKSPACE
+    assert lib.ring_attn_ring_fwd(*args, 1, 2, 1, 1024, 64, 4, 1, 0, ctypes.c_void_p(272), ws, NUL) == \
         capi.ERR_WORKSPACE
-    assert lib.ring_attn_ring_fwd(*([NUL] * 5), 1, 2, 1, 1024, 64, 4, 1, P256, ws, NUL) == capi.ERR_NULL
+    assert lib.ring_attn_ring_fwd(*([NUL] * 5), 1, 2, 1, 1024, 64, 4, 1, 0, P256, ws, NUL) == capi.ERR_NULL
