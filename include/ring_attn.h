@@ -170,6 +170,35 @@ int ring_attn_ring_fwd(const void* q, const void* k, const void* v, void* o, flo
                        int L, int d, int n_chunks, int causal, int striped, void* workspace, size_t workspace_bytes,
                        cudaStream_t stream);
 
+/* ---------------------------------------------------------------------
+ * Ulysses sequence parallelism on one GPU ("Large-scale distributed AI
+ * model training series: sequence parallelism", section 5 DeepSpeed-
+ * Ulysses): the input is sharded along the sequence, rank r holding tokens
+ * [rC, (r+1)C) of every head (C = L / n_ranks); an all-to-all gives every
+ * rank all L tokens of H / n_ranks heads, attention runs on each head group
+ * independently, and an all-to-all brings the result back to the sequence
+ * shards.  Every tensor is passed as the n_ranks shards stacked, rank-major:
+ *   q, o, dO, dq  bf16 [n_ranks][B][Hq][C][d]     lse fp32 [n_ranks][B][Hq][C]
+ *   k, v, dk, dv  bf16 [n_ranks][B][Hkv][C][d]
+ * (rank r's shard is the r-th [B][H][C][d] block).  The head groups must
+ * split evenly: Hq, Hkv and L multiples of n_ranks, else
+ * RING_ATTN_ERR_SHAPE.  The attention itself is the fused kernel of
+ * ring_attn_fwd / ring_attn_bwd on the head shards (batch n_ranks * B),
+ * with the whole sequence in view, so the chunk schedule does not apply.
+ * `workspace`: caller-owned device memory, 256-byte aligned, of
+ * ring_attn_ulysses_workspace_size() bytes (enough for the backward; the
+ * forward uses its head-shard part only).
+ * ------------------------------------------------------------------- */
+size_t ring_attn_ulysses_workspace_size(int B, int Hq, int Hkv, int L, int d, int n_ranks, int causal);
+
+int ring_attn_ulysses_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                          int L, int d, int n_ranks, int causal, void* workspace, size_t workspace_bytes,
+                          cudaStream_t stream);
+
+int ring_attn_ulysses_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                          const void* dO, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int L, int d,
+                          int n_ranks, int causal, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* Static description of a status code. */
 const char* ring_attn_strerror(int status);
 
@@ -206,7 +235,8 @@ enum {
   RING_ATTN_KERNEL_RING_STEP = 4,  /* ring mode: one step of attention (every rank or one) */
   RING_ATTN_KERNEL_RING_MERGE = 5, /* ring mode: log-sum-exp merge */
   RING_ATTN_KERNEL_RING_IO = 6,    /* ring mode: gather into / scatter out of chunk order */
-  RING_ATTN_N_KERNELS = 7
+  RING_ATTN_KERNEL_ULYSSES_A2A = 7, /* Ulysses: all-to-all between sequence and head shards */
+  RING_ATTN_N_KERNELS = 8
 };
 int ring_attn_profile_enable(int on);
 int ring_attn_profile_read(double* ms, long long* launches);

@@ -81,6 +81,12 @@ def load():
     lib.ring_attn_ring_fwd_workspace_size.restype = S
     lib.ring_attn_ring_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, P, S, P]
     lib.ring_attn_ring_fwd.restype = I
+    lib.ring_attn_ulysses_workspace_size.argtypes = [I, I, I, I, I, I, I]
+    lib.ring_attn_ulysses_workspace_size.restype = S
+    lib.ring_attn_ulysses_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, P, S, P]
+    lib.ring_attn_ulysses_fwd.restype = I
+    lib.ring_attn_ulysses_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, S, P]
+    lib.ring_attn_ulysses_bwd.restype = I
     _lib = lib
     return lib
 
@@ -250,6 +256,64 @@ def ring_attn_ring_fwd(q, k, v, n_chunks: int, causal: bool, o=None, lse=None, w
     return o, lse
 
 
+# ------------------------------------------------------------------ Ulysses
+
+def ulysses_workspace_size(B, Hq, Hkv, L, d, n_ranks, causal) -> int:
+    return int(load().ring_attn_ulysses_workspace_size(B, Hq, Hkv, L, d, int(n_ranks), int(bool(causal))))
+
+
+def _ulysses_shapes(q, k):
+    N, B, Hq, C, d = q.shape
+    return N, B, Hq, k.shape[2], C * N, C, d
+
+
+def ring_attn_ulysses_fwd(q, k, v, causal: bool, o=None, lse=None, workspace=None, stream=None):
+    """Ulysses on one GPU: q [N,B,Hq,C,d], k, v [N,B,Hkv,C,d] (sequence
+    shards, rank-major) -> (o [N,B,Hq,C,d], lse [N,B,Hq,C])."""
+    import torch
+    N, B, Hq, Hkv, L, C, d = _ulysses_shapes(q, k)
+    _check_tensor(q, "q", torch.bfloat16, (N, B, Hq, C, d))
+    _check_tensor(k, "k", torch.bfloat16, (N, B, Hkv, C, d))
+    _check_tensor(v, "v", torch.bfloat16, (N, B, Hkv, C, d))
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((N, B, Hq, C), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check_tensor(o, "o", torch.bfloat16, (N, B, Hq, C, d))
+    _check_tensor(lse, "lse", torch.float32, (N, B, Hq, C))
+    if workspace is None:
+        workspace = torch.empty(max(ulysses_workspace_size(B, Hq, Hkv, L, d, N, causal), 1), dtype=torch.uint8,
+                                device=q.device)
+    rc = load().ring_attn_ulysses_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, L, d, N,
+                                      int(bool(causal)), _ptr(workspace),
+                                      int(workspace.numel() * workspace.element_size()), _stream(stream))
+    if rc != OK:
+        raise RingAttnError(rc, "ring_attn_ulysses_fwd")
+    return o, lse
+
+
+def ring_attn_ulysses_bwd(q, k, v, o, lse, dO, causal: bool, dq=None, dk=None, dv=None, workspace=None,
+                          stream=None):
+    """Gradients for Ulysses on one GPU, all tensors as sequence shards
+    (see ring_attn_ulysses_fwd); returns (dq, dk, dv)."""
+    import torch
+    N, B, Hq, Hkv, L, C, d = _ulysses_shapes(q, k)
+    for t, n, s in ((q, "q", (N, B, Hq, C, d)), (k, "k", (N, B, Hkv, C, d)), (v, "v", (N, B, Hkv, C, d)),
+                    (o, "o", (N, B, Hq, C, d)), (dO, "dO", (N, B, Hq, C, d))):
+        _check_tensor(t, n, torch.bfloat16, s)
+    _check_tensor(lse, "lse", torch.float32, (N, B, Hq, C))
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if workspace is None:
+        workspace = torch.empty(max(ulysses_workspace_size(B, Hq, Hkv, L, d, N, causal), 1), dtype=torch.uint8,
+                                device=q.device)
+    rc = load().ring_attn_ulysses_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk),
+                                      _ptr(dv), B, Hq, Hkv, L, d, N, int(bool(causal)), _ptr(workspace),
+                                      int(workspace.numel() * workspace.element_size()), _stream(stream))
+    if rc != OK:
+        raise RingAttnError(rc, "ring_attn_ulysses_bwd")
+    return dq, dk, dv
+
+
 def bwd_workspace_size(B, Hq, Hkv, L, d, n_chunks, causal) -> int:
     return int(load().ring_attn_bwd_workspace_size(B, Hq, Hkv, L, d, int(n_chunks), int(bool(causal))))
 
@@ -312,7 +376,7 @@ def device_status(stream=None):
     return rc, site.value
 
 
-KERNEL_NAMES = ("fwd", "bwd_pre", "bwd_main", "bwd_post", "ring_step", "ring_merge", "ring_io")
+KERNEL_NAMES = ("fwd", "bwd_pre", "bwd_main", "bwd_post", "ring_step", "ring_merge", "ring_io", "ulysses_a2a")
 
 
 def profile_enable(on: bool = True):

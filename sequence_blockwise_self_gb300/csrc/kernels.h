@@ -107,6 +107,11 @@ cudaError_t launch_ring_merge(float* o, float* lse, const float* o_s, const floa
                               long long n_rows, int d, cudaStream_t stream);
 cudaError_t launch_ring_gather(const void* src, void* dst, int Z, int L, int d, int N, bool causal, bool striped,
                                cudaStream_t stream);
+// Ulysses (ulysses.cu): the all-to-all between sequence shards
+// [N][B][H][L/N][row] and head shards [N][B][H/N][L][row] (to_heads) or
+// back; row_bytes a multiple of 16 (d values of bf16) or 4 (one fp32).
+cudaError_t launch_ulysses_a2a(const void* src, void* dst, int row_bytes, int B, int H, int N, int L, bool to_heads,
+                               cudaStream_t stream);
 cudaError_t launch_ring_scatter(const float* acc, const float* lse_acc, void* o, float* lse, int Z, int L, int d,
                                 int N, bool causal, bool striped, cudaStream_t stream);
 

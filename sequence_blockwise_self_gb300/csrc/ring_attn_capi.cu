@@ -236,6 +236,102 @@ int plan_query(int kind, int L, int n_chunks, int causal, int* n_blocks, int* n_
   return RING_ATTN_OK;
 }
 
+// The fused forward on checked arguments (caller holds g_mutex).
+int fwd_impl(int dev, const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int L,
+             int d, int n_chunks, int causal, cudaStream_t stream) {
+  FwdArgs a;
+  std::memset(&a, 0, sizeof a);
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (!make_map(&a.tm_q, q, bf, 2, d, L, B * Hq, 64) || !make_map(&a.tm_k, k, bf, 2, d, L, B * Hkv, 64) ||
+      !make_map(&a.tm_v, v, bf, 2, d, L, B * Hkv, 64) || !make_map(&a.tm_o, o, bf, 2, d, L, B * Hq, 64))
+    return RING_ATTN_ERR_CUDA;
+  DevicePlan plan;
+  int rc;
+  if ((rc = get_plan(dev, 0, L, n_chunks, causal != 0, &plan)) != RING_ATTN_OK) return rc;
+  int* err;
+  if ((rc = status_ptr(dev, &err)) != RING_ATTN_OK) return rc;
+  a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.L = L; a.d = d; a.causal = causal != 0;
+  a.n_blocks = plan.n_blocks;
+  a.order = plan.order(); a.offsets = plan.offsets(); a.ranges = plan.ranges();
+  a.lse = lse; a.err = err; a.timer = active_timer();
+  return launch_fwd(a, stream) == cudaSuccess ? RING_ATTN_OK : RING_ATTN_ERR_CUDA;
+}
+
+// The fused backward on checked arguments and a workspace of at least
+// bwd_workspace(...).total bytes (caller holds g_mutex).
+int bwd_impl(int dev, const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+             void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal,
+             void* workspace, cudaStream_t stream) {
+  const BwdWorkspace w = bwd_workspace(B, Hq, Hkv, L, d);
+  BwdArgs a;
+  std::memset(&a, 0, sizeof a);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const int Lpad = static_cast<int>(round_up(static_cast<size_t>(L), 128));
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (!make_map(&a.tm_q, q, bf, 2, d, L, B * Hq, 64) || !make_map(&a.tm_k, k, bf, 2, d, L, B * Hkv, 64) ||
+      !make_map(&a.tm_v, v, bf, 2, d, L, B * Hkv, 64) || !make_map(&a.tm_do, dO, bf, 2, d, L, B * Hq, 64))
+    return RING_ATTN_ERR_CUDA;
+  if (w.kv_accumulate &&
+      (!make_map(&a.tm_dkacc, ws + w.dk, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, Lpad, B * Hkv, 32, 32) ||
+       !make_map(&a.tm_dvacc, ws + w.dv, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, Lpad, B * Hkv, 32, 32)))
+    return RING_ATTN_ERR_CUDA;
+  DevicePlan plan;
+  int rc;
+  if ((rc = get_plan(dev, 1, L, n_chunks, causal != 0, &plan)) != RING_ATTN_OK) return rc;
+  int* err;
+  if ((rc = status_ptr(dev, &err)) != RING_ATTN_OK) return rc;
+  a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.L = L; a.Lpad = Lpad; a.d = d; a.causal = causal != 0;
+  a.n_blocks = plan.n_blocks;
+  a.order = plan.order(); a.offsets = plan.offsets(); a.ranges = plan.ranges();
+  a.o = o; a.dO = dO; a.lse = lse;
+  a.lse2 = reinterpret_cast<float*>(ws + w.lse2);
+  a.Dvec = reinterpret_cast<float*>(ws + w.dvec);
+  a.dq_acc = reinterpret_cast<float*>(ws + w.dq);
+  a.dk_acc = w.kv_accumulate ? reinterpret_cast<float*>(ws + w.dk) : nullptr;
+  a.dv_acc = w.kv_accumulate ? reinterpret_cast<float*>(ws + w.dv) : nullptr;
+  a.dq = dq; a.dk = dk; a.dv = dv; a.err = err; a.timer = active_timer();
+  return launch_bwd(a, stream) == cudaSuccess ? RING_ATTN_OK : RING_ATTN_ERR_CUDA;
+}
+
+// Ulysses: parts of the workspace (byte offsets, 256-aligned): head-shard
+// copies of q, k, v, o, lse (forward), then dO, dq, dk, dv and the fused
+// backward's own workspace for the head-shard problem (backward).
+struct UlyssesWorkspace {
+  size_t q = 0, k = 0, v = 0, o = 0, lse = 0, dO = 0, dq = 0, dk = 0, dv = 0, bwd = 0, fwd_total = 0, total = 0;
+};
+
+UlyssesWorkspace ulysses_workspace(int B, int Hq, int Hkv, int L, int d, int N) {
+  auto up = [](size_t x) { return round_up(x, 256); };
+  const size_t nq = static_cast<size_t>(B) * Hq * L * d * 2, nkv = static_cast<size_t>(B) * Hkv * L * d * 2;
+  UlyssesWorkspace w;
+  w.k = w.q + up(nq);
+  w.v = w.k + up(nkv);
+  w.o = w.v + up(nkv);
+  w.lse = w.o + up(nq);
+  w.fwd_total = w.lse + up(static_cast<size_t>(B) * Hq * L * 4);
+  w.dO = w.fwd_total;
+  w.dq = w.dO + up(nq);
+  w.dk = w.dq + up(nq);
+  w.dv = w.dk + up(nkv);
+  w.bwd = w.dv + up(nkv);
+  w.total = w.bwd + bwd_workspace(N * B, Hq / N, Hkv / N, L, d).total;
+  return w;
+}
+
+int check_ulysses(int B, int Hq, int Hkv, int L, int d, int N, int causal) {
+  if (N <= 0) return RING_ATTN_ERR_SHAPE;
+  int rc = check_shape(B, Hq, Hkv, L, d, 1, causal);
+  if (rc != RING_ATTN_OK) return rc;
+  // every rank takes H/N of the query heads and of the key/value heads
+  if (Hq % N || Hkv % N || L % N) return RING_ATTN_ERR_SHAPE;
+  return RING_ATTN_OK;
+}
+
+cudaError_t a2a(const void* src, void* dst, int row_bytes, int B, int H, int N, int L, bool to_heads,
+                cudaStream_t stream) {
+  return launch_ulysses_a2a(src, dst, row_bytes, B, H, N, L, to_heads, stream);
+}
+
 }  // namespace
 
 // Device status word of the current device, for the library's other entry
@@ -308,21 +404,7 @@ int ring_attn_fwd(const void* q, const void* k, const void* v, void* o, float* l
   std::lock_guard<std::mutex> lock(g_mutex);
   int dev;
   if ((rc = current_device(&dev)) != RING_ATTN_OK) return rc;
-  FwdArgs a;
-  std::memset(&a, 0, sizeof a);
-  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  if (!make_map(&a.tm_q, q, bf, 2, d, L, B * Hq, 64) || !make_map(&a.tm_k, k, bf, 2, d, L, B * Hkv, 64) ||
-      !make_map(&a.tm_v, v, bf, 2, d, L, B * Hkv, 64) || !make_map(&a.tm_o, o, bf, 2, d, L, B * Hq, 64))
-    return RING_ATTN_ERR_CUDA;
-  DevicePlan plan;
-  if ((rc = get_plan(dev, 0, L, n_chunks, causal != 0, &plan)) != RING_ATTN_OK) return rc;
-  int* err;
-  if ((rc = status_ptr(dev, &err)) != RING_ATTN_OK) return rc;
-  a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.L = L; a.d = d; a.causal = causal != 0;
-  a.n_blocks = plan.n_blocks;
-  a.order = plan.order(); a.offsets = plan.offsets(); a.ranges = plan.ranges();
-  a.lse = lse; a.err = err; a.timer = active_timer();
-  return launch_fwd(a, stream) == cudaSuccess ? RING_ATTN_OK : RING_ATTN_ERR_CUDA;
+  return fwd_impl(dev, q, k, v, o, lse, B, Hq, Hkv, L, d, n_chunks, causal, stream);
 }
 
 size_t ring_attn_bwd_workspace_size(int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal) {
@@ -346,33 +428,7 @@ int ring_attn_bwd(const void* q, const void* k, const void* v, const void* o, co
   std::lock_guard<std::mutex> lock(g_mutex);
   int dev;
   if ((rc = current_device(&dev)) != RING_ATTN_OK) return rc;
-  BwdArgs a;
-  std::memset(&a, 0, sizeof a);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  const int Lpad = static_cast<int>(round_up(static_cast<size_t>(L), 128));
-  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  if (!make_map(&a.tm_q, q, bf, 2, d, L, B * Hq, 64) || !make_map(&a.tm_k, k, bf, 2, d, L, B * Hkv, 64) ||
-      !make_map(&a.tm_v, v, bf, 2, d, L, B * Hkv, 64) || !make_map(&a.tm_do, dO, bf, 2, d, L, B * Hq, 64))
-    return RING_ATTN_ERR_CUDA;
-  if (w.kv_accumulate &&
-      (!make_map(&a.tm_dkacc, ws + w.dk, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, Lpad, B * Hkv, 32, 32) ||
-       !make_map(&a.tm_dvacc, ws + w.dv, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, Lpad, B * Hkv, 32, 32)))
-    return RING_ATTN_ERR_CUDA;
-  DevicePlan plan;
-  if ((rc = get_plan(dev, 1, L, n_chunks, causal != 0, &plan)) != RING_ATTN_OK) return rc;
-  int* err;
-  if ((rc = status_ptr(dev, &err)) != RING_ATTN_OK) return rc;
-  a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.L = L; a.Lpad = Lpad; a.d = d; a.causal = causal != 0;
-  a.n_blocks = plan.n_blocks;
-  a.order = plan.order(); a.offsets = plan.offsets(); a.ranges = plan.ranges();
-  a.o = o; a.dO = dO; a.lse = lse;
-  a.lse2 = reinterpret_cast<float*>(ws + w.lse2);
-  a.Dvec = reinterpret_cast<float*>(ws + w.dvec);
-  a.dq_acc = reinterpret_cast<float*>(ws + w.dq);
-  a.dk_acc = w.kv_accumulate ? reinterpret_cast<float*>(ws + w.dk) : nullptr;
-  a.dv_acc = w.kv_accumulate ? reinterpret_cast<float*>(ws + w.dv) : nullptr;
-  a.dq = dq; a.dk = dk; a.dv = dv; a.err = err; a.timer = active_timer();
-  return launch_bwd(a, stream) == cudaSuccess ? RING_ATTN_OK : RING_ATTN_ERR_CUDA;
+  return bwd_impl(dev, q, k, v, o, lse, dO, dq, dk, dv, B, Hq, Hkv, L, d, n_chunks, causal, workspace, stream);
 }
 
 int ring_attn_device_status(cudaStream_t stream, int* site) {
@@ -514,6 +570,88 @@ int ring_attn_ring_fwd(const void* q, const void* k, const void* v, void* o, flo
   if (launch_ring_scatter(oacc, lacc, o, lse, B * Hq, L, d, N, sc, st, stream) != cudaSuccess)
     return RING_ATTN_ERR_CUDA;
   if (t) t->mark(RING_ATTN_KERNEL_RING_IO, true, stream);
+  return RING_ATTN_OK;
+}
+
+size_t ring_attn_ulysses_workspace_size(int B, int Hq, int Hkv, int L, int d, int n_ranks, int causal) {
+  if (check_ulysses(B, Hq, Hkv, L, d, n_ranks, causal) != RING_ATTN_OK) return 0;
+  return ulysses_workspace(B, Hq, Hkv, L, d, n_ranks).total;
+}
+
+int ring_attn_ulysses_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                          int L, int d, int n_ranks, int causal, void* workspace, size_t workspace_bytes,
+                          cudaStream_t stream) {
+  int rc = check_ulysses(B, Hq, Hkv, L, d, n_ranks, causal);
+  if (rc != RING_ATTN_OK) return rc;
+  if (B == 0 || L == 0) return RING_ATTN_OK;
+  if (!q || !k || !v || !o || !lse) return RING_ATTN_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return RING_ATTN_ERR_UNSUPPORTED;
+  const UlyssesWorkspace w = ulysses_workspace(B, Hq, Hkv, L, d, n_ranks);
+  if (!workspace || workspace_bytes < w.fwd_total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return RING_ATTN_ERR_WORKSPACE;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  int dev;
+  if ((rc = current_device(&dev)) != RING_ATTN_OK) return rc;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const int N = n_ranks, row = d * 2;
+  LaunchTimer* t = active_timer();
+  if (t) t->mark(RING_ATTN_KERNEL_ULYSSES_A2A, false, stream);
+  if (a2a(q, ws + w.q, row, B, Hq, N, L, true, stream) != cudaSuccess ||
+      a2a(k, ws + w.k, row, B, Hkv, N, L, true, stream) != cudaSuccess ||
+      a2a(v, ws + w.v, row, B, Hkv, N, L, true, stream) != cudaSuccess)
+    return RING_ATTN_ERR_CUDA;
+  if (t) t->mark(RING_ATTN_KERNEL_ULYSSES_A2A, true, stream);
+  // every rank's head group over the whole sequence: one launch, batch N*B
+  if ((rc = fwd_impl(dev, ws + w.q, ws + w.k, ws + w.v, ws + w.o, reinterpret_cast<float*>(ws + w.lse), N * B,
+                     Hq / N, Hkv / N, L, d, 1, causal, stream)) != RING_ATTN_OK)
+    return rc;
+  if (t) t->mark(RING_ATTN_KERNEL_ULYSSES_A2A, false, stream);
+  if (a2a(ws + w.o, o, row, B, Hq, N, L, false, stream) != cudaSuccess ||
+      a2a(ws + w.lse, lse, 4, B, Hq, N, L, false, stream) != cudaSuccess)
+    return RING_ATTN_ERR_CUDA;
+  if (t) t->mark(RING_ATTN_KERNEL_ULYSSES_A2A, true, stream);
+  return RING_ATTN_OK;
+}
+
+int ring_attn_ulysses_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                          const void* dO, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int L, int d,
+                          int n_ranks, int causal, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  int rc = check_ulysses(B, Hq, Hkv, L, d, n_ranks, causal);
+  if (rc != RING_ATTN_OK) return rc;
+  if (B == 0 || L == 0) return RING_ATTN_OK;
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return RING_ATTN_ERR_NULL;
+  const void* ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return RING_ATTN_ERR_UNSUPPORTED;
+  const UlyssesWorkspace w = ulysses_workspace(B, Hq, Hkv, L, d, n_ranks);
+  if (!workspace || workspace_bytes < w.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return RING_ATTN_ERR_WORKSPACE;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  int dev;
+  if ((rc = current_device(&dev)) != RING_ATTN_OK) return rc;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const int N = n_ranks, row = d * 2;
+  LaunchTimer* t = active_timer();
+  if (t) t->mark(RING_ATTN_KERNEL_ULYSSES_A2A, false, stream);
+  if (a2a(q, ws + w.q, row, B, Hq, N, L, true, stream) != cudaSuccess ||
+      a2a(k, ws + w.k, row, B, Hkv, N, L, true, stream) != cudaSuccess ||
+      a2a(v, ws + w.v, row, B, Hkv, N, L, true, stream) != cudaSuccess ||
+      a2a(o, ws + w.o, row, B, Hq, N, L, true, stream) != cudaSuccess ||
+      a2a(lse, ws + w.lse, 4, B, Hq, N, L, true, stream) != cudaSuccess ||
+      a2a(dO, ws + w.dO, row, B, Hq, N, L, true, stream) != cudaSuccess)
+    return RING_ATTN_ERR_CUDA;
+  if (t) t->mark(RING_ATTN_KERNEL_ULYSSES_A2A, true, stream);
+  if ((rc = bwd_impl(dev, ws + w.q, ws + w.k, ws + w.v, ws + w.o, reinterpret_cast<const float*>(ws + w.lse),
+                     ws + w.dO, ws + w.dq, ws + w.dk, ws + w.dv, N * B, Hq / N, Hkv / N, L, d, 1, causal,
+                     ws + w.bwd, stream)) != RING_ATTN_OK)
+    return rc;
+  if (t) t->mark(RING_ATTN_KERNEL_ULYSSES_A2A, false, stream);
+  if (a2a(ws + w.dq, dq, row, B, Hq, N, L, false, stream) != cudaSuccess ||
+      a2a(ws + w.dk, dk, row, B, Hkv, N, L, false, stream) != cudaSuccess ||
+      a2a(ws + w.dv, dv, row, B, Hkv, N, L, false, stream) != cudaSuccess)
+    return RING_ATTN_ERR_CUDA;
+  if (t) t->mark(RING_ATTN_KERNEL_ULYSSES_A2A, true, stream);
   return RING_ATTN_OK;
 }
 

@@ -126,3 +126,18 @@ def test_ring_fwd_workspace_and_arguments(lib):
     assert lib.ring_attn_ring_fwd(*args, 1, 2, 1, 1024, 64, 4, 1, 0, ctypes.c_void_p(272), ws, NUL) == \
         capi.ERR_WORKSPACE
     assert lib.ring_attn_ring_fwd(*([NUL] * 5), 1, 2, 1, 1024, 64, 4, 1, 0, P256, ws, NUL) == capi.ERR_NULL
+
+
+def test_ulysses_rejects_bad_arguments(lib):
+    ws = lib.ring_attn_ulysses_workspace_size(1, 4, 2, 512, 64, 2, 1)
+    assert ws > 0
+    assert lib.ring_attn_ulysses_workspace_size(1, 6, 3, 512, 64, 4, 1) == 0   # heads do not split
+    assert lib.ring_attn_ulysses_workspace_size(1, 8, 2, 512, 64, 4, 1) == 0   # kv heads do not split
+    assert lib.ring_attn_ulysses_workspace_size(1, 4, 4, 510, 64, 4, 1) == 0   # tokens do not split
+    args = [P256] * 5
+    assert lib.ring_attn_ulysses_fwd(*args, 1, 4, 2, 512, 64, 0, 1, P256, ws, NUL) == capi.ERR_SHAPE
+    assert lib.ring_attn_ulysses_fwd(*([NUL] * 5), 1, 4, 2, 512, 64, 2, 1, P256, ws, NUL) == capi.ERR_NULL
+    assert lib.ring_attn_ulysses_fwd(*args, 1, 4, 2, 512, 64, 2, 1, NUL, ws, NUL) == capi.ERR_WORKSPACE
+    bargs = [P256] * 9
+    assert lib.ring_attn_ulysses_bwd(*bargs, 1, 4, 2, 512, 64, 2, 1, P256, ws - 1, NUL) == capi.ERR_WORKSPACE
+    assert lib.ring_attn_ulysses_bwd(*bargs, 1, 4, 2, 512, 96, 2, 1, P256, ws, NUL) == capi.ERR_UNSUPPORTED
