@@ -485,7 +485,58 @@ def run_ours(args, w):
             ring["striped"] = measure_ring(True)
         ring = ring or None
 
-    # (5) CPU oracle baseline (rank 0, one GPU only)
+    # (5) Ulysses on this GPU at the largest degree the heads allow (<= 8):
+    # sequence shards -> head shards -> fused attention -> back; the
+    # all-to-all kernels are HBM-bound
+    ulysses = None
+    deg = max([n for n in range(2, 9) if w.Hq % n == 0 and w.Hkv % n == 0 and w.L % n == 0] or [0])
+    if not args.no_ulysses and deg:
+        N = deg
+        shard = lambda x: x.reshape(*x.shape[:2], N, w.L // N, *x.shape[3:]).movedim(2, 0).contiguous()  # noqa: E731
+        qs, ks, vs, dOs = (shard(x) for x in (qd, kd, vd, dOd))
+        ws_u = torch.empty(ra.ulysses_workspace_size(w.B, w.Hq, w.Hkv, w.L, w.d, N, w.causal), dtype=torch.uint8,
+                           device=dev)
+        o_u, lse_u = torch.empty_like(qs), torch.empty((N, w.B, w.Hq, w.L // N), dtype=torch.float32, device=dev)
+        g_u = [torch.empty_like(qs), torch.empty_like(ks), torch.empty_like(vs)]
+
+        def u_step():
+            ra.ring_attn_ulysses_fwd(qs, ks, vs, w.causal, o=o_u, lse=lse_u, workspace=ws_u, stream=stream)
+            ra.ring_attn_ulysses_bwd(qs, ks, vs, o_u, lse_u, dOs, w.causal, dq=g_u[0], dk=g_u[1], dv=g_u[2],
+                                     workspace=ws_u, stream=stream)
+        u_step()
+        torch.cuda.synchronize(dev)
+        u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        u0.record(stream)
+        for _ in range(args.steps):
+            u_step()
+        u1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms_u = u0.elapsed_time(u1) / args.steps
+        ra.profile_enable(True)
+        for _ in range(args.steps):
+            u_step()
+        torch.cuda.synchronize(dev)
+        up = ra.profile_read()
+        ra.profile_enable(False)
+        st, site = ra.device_status()
+        if st != 0:
+            raise RuntimeError(f"device status {st} at site {site:#x} in Ulysses")
+        a2a_ms, a2a_n = up["ulysses_a2a"]
+        # bytes moved per step by the all-to-alls (each read once, written once):
+        # fwd q, k, v in, o, lse out; bwd q, k, v, o, lse, dO in, dq, dk, dv out
+        bq, bkv, bl = w.B * w.Hq * w.L * w.d * 2, w.B * w.Hkv * w.L * w.d * 2, w.B * w.Hq * w.L * 4
+        a2a_bytes = 2 * ((bq + 2 * bkv) + (bq + bl) + (2 * bq + 2 * bkv + bq + bl) + (bq + 2 * bkv))
+        a2a_gbs = a2a_bytes / (a2a_ms / args.steps * 1e-3) / 1e9 if a2a_n else None
+        ulysses = {
+            "degree": N, "step_ms": ms_u, "tflops": step_flops / (ms_u * 1e-3) / 1e12,
+            "per_kernel_ms_per_step": {k: up[k][0] / args.steps for k in ("fwd", "bwd_main", "ulysses_a2a")},
+            "a2a_roofline": {"bound": "hbm", "achieved": a2a_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                             "frac": (a2a_gbs / peaks["hbm_gbs"]) if a2a_gbs else None,
+                             "bytes_per_step": a2a_bytes},
+        }
+        del qs, ks, vs, dOs, ws_u, o_u, lse_u, g_u
+
+    # (6) CPU oracle baseline (rank 0, one GPU only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tf, det = oracle_sample(w, q, k, v, dO, seconds_target=15.0, seed=7)
@@ -512,6 +563,7 @@ def run_ours(args, w):
             "cpu_baseline": cpu,
             "e2e": e2e,
             "ring_mode": ring,
+            "ulysses": ulysses,
             "gpu_launches": 4 * args.steps,
             "clocks": clocks,
         }
@@ -530,6 +582,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-ring-mode", action="store_true")
+    ap.add_argument("--no-ulysses", action="store_true")
     args = ap.parse_args()
     from sequence_blockwise_self_gb300 import inputs
 
