@@ -199,6 +199,27 @@ int ring_attn_ulysses_bwd(const void* q, const void* k, const void* v, const voi
                           const void* dO, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int L, int d,
                           int n_ranks, int causal, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* Workspace bytes ring_attn_ring_bwd needs for this shape, or 0 if invalid. */
+size_t ring_attn_ring_bwd_workspace_size(int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal,
+                                         int striped);
+
+/*
+ * The backward of ring_attn_ring_fwd, the ring-mode way (the same results
+ * as ring_attn_bwd; o and lse from either forward): q, k, v, o, dO, lse are
+ * gathered into chunk order; the statistics of every rank's rows are formed
+ * once; at each step s = 0..n_chunks-1 one launch runs, for every rank r,
+ * the tiles of the key/value chunk it holds (rank (r - s) mod n_chunks)
+ * against its query chunk, adding into rank r's fp32 dQ accumulator and
+ * into the source chunk's fp32 dK, dV accumulators (the gradients that in a
+ * multi-GPU ring travel with K and V back to their owner); the gradients
+ * are scattered back to sequence order as bf16.  `workspace`: caller-owned
+ * device memory of ring_attn_ring_bwd_workspace_size() bytes, 256-byte
+ * aligned.
+ */
+int ring_attn_ring_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                       void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal,
+                       int striped, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* Static description of a status code. */
 const char* ring_attn_strerror(int status);
 

@@ -5,7 +5,8 @@ library's CUDA kernels):
     ring_attn_fwd(q, k, v, n_chunks, causal) -> (o, lse)
     ring_attn_bwd(q, k, v, o, lse, dO, n_chunks, causal) -> (dq, dk, dv)
 Ring mode (the ring run step by step, as each rank of a multi-GPU ring
-would): ring_attn_fwd_step, ring_attn_merge, ring_attn_ring_fwd.
+would): ring_attn_fwd_step, ring_attn_merge, ring_attn_ring_fwd,
+ring_attn_ring_bwd.
 Ulysses on one GPU (sequence shards -> head shards -> back):
 ring_attn_ulysses_fwd, ring_attn_ulysses_bwd.
 Host-only queries: owner_rank, fwd_plan, bwd_plan, step_plan.
@@ -30,6 +31,8 @@ from .capi import (  # noqa: F401
     ring_attn_merge,
     ring_attn_ring_fwd,
     ring_fwd_workspace_size,
+    ring_attn_ring_bwd,
+    ring_bwd_workspace_size,
     ring_attn_ulysses_bwd,
     ring_attn_ulysses_fwd,
     ulysses_workspace_size,

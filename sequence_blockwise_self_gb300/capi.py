@@ -81,6 +81,10 @@ def load():
     lib.ring_attn_ring_fwd_workspace_size.restype = S
     lib.ring_attn_ring_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, P, S, P]
     lib.ring_attn_ring_fwd.restype = I
+    lib.ring_attn_ring_bwd_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
+    lib.ring_attn_ring_bwd_workspace_size.restype = S
+    lib.ring_attn_ring_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, P, S, P]
+    lib.ring_attn_ring_bwd.restype = I
     lib.ring_attn_ulysses_workspace_size.argtypes = [I, I, I, I, I, I, I]
     lib.ring_attn_ulysses_workspace_size.restype = S
     lib.ring_attn_ulysses_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, P, S, P]
@@ -254,6 +258,37 @@ def ring_attn_ring_fwd(q, k, v, n_chunks: int, causal: bool, o=None, lse=None, w
     if rc != OK:
         raise RingAttnError(rc, "ring_attn_ring_fwd")
     return o, lse
+
+
+def ring_bwd_workspace_size(B, Hq, Hkv, L, d, n_chunks, causal, striped: bool = False) -> int:
+    return int(load().ring_attn_ring_bwd_workspace_size(B, Hq, Hkv, L, d, int(n_chunks), int(bool(causal)),
+                                                         int(bool(striped))))
+
+
+def ring_attn_ring_bwd(q, k, v, o, lse, dO, n_chunks: int, causal: bool, dq=None, dk=None, dv=None, workspace=None,
+                       stream=None, striped: bool = False):
+    """The backward computed the ring-mode way (every rank's steps as
+    separate launches); returns (dq, dk, dv)."""
+    import torch
+    B, Hq, L, d = q.shape
+    Hkv = k.shape[1]
+    for t, n, s in ((q, "q", (B, Hq, L, d)), (k, "k", (B, Hkv, L, d)), (v, "v", (B, Hkv, L, d)),
+                    (o, "o", (B, Hq, L, d)), (dO, "dO", (B, Hq, L, d))):
+        _check_tensor(t, n, torch.bfloat16, s)
+    _check_tensor(lse, "lse", torch.float32, (B, Hq, L))
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if workspace is None:
+        workspace = torch.empty(max(ring_bwd_workspace_size(B, Hq, Hkv, L, d, n_chunks, causal, striped), 1),
+                                dtype=torch.uint8, device=q.device)
+    rc = load().ring_attn_ring_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk),
+                                   _ptr(dv), B, Hq, Hkv, L, d, int(n_chunks), int(bool(causal)), int(bool(striped)),
+                                   _ptr(workspace), int(workspace.numel() * workspace.element_size()),
+                                   _stream(stream))
+    if rc != OK:
+        raise RingAttnError(rc, "ring_attn_ring_bwd")
+    return dq, dk, dv
 
 
 # ------------------------------------------------------------------ Ulysses

@@ -64,6 +64,7 @@
 #include <cfloat>
 
 #include "kernels.h"
+#include "plan.h"
 #include "sm103_ptx.cuh"
 
 namespace ra {
@@ -129,7 +130,28 @@ struct BwdDev {
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   int* err;
+  // Ring step mode (step_nt > 0): item k is key/value tile k % step_nt of
+  // the chunk rank r = k / step_nt holds at ring step `step` (rank (r - step)
+  // mod n_chunks), against rank r's query chunk; L = Lpad = the chunk
+  // length; slices: q, dO, statistics, dQ at r * B*Hq + (b, h), k, v, dK, dV
+  // at src * B*Hkv + (b, kv head); causal keys from the fold or stripes.
+  int step_nt, step, n_chunks, striped;
 };
+
+// Causal-mask keys of the backward (as in the forward's step mode): a key
+// row with key kk is visible to query column qq of a tile whose first row
+// has key q0k iff kk <= q0k + qq.
+template <bool kStep>
+__device__ __forceinline__ int bwd_q_key(const BwdDev& p, int rank, int local) {
+  if (!kStep || !p.causal || p.striped) return local;
+  return chunk_pos(p.L * p.n_chunks, p.n_chunks, true, false, rank, local);
+}
+template <bool kStep>
+__device__ __forceinline__ int bwd_kv_key(const BwdDev& p, int kv_rank, int q_rank, int local) {
+  if (!kStep || !p.causal) return local;
+  if (p.striped) return local + (kv_rank > q_rank ? 1 : 0);
+  return chunk_pos(p.L * p.n_chunks, p.n_chunks, true, false, kv_rank, local);
+}
 
 __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, int* err) {
   int local = 0;
@@ -299,14 +321,16 @@ __device__ void bwd_dq_reducer(BwdSmem<D>& sm, float* dq_acc, int Lpad, int q_z,
   bulk_wait_group<0>();
 }
 
-template <int D>
-__device__ void bwd_compute(BwdSmem<D>& sm, uint32_t tmem, const BwdDev& p, const CUtensorMap* tm_dkacc, const CUtensorMap* tm_dvacc, int kv_z, int q_z, int kv_tile,
+template <int D, bool kStep>
+__device__ void bwd_compute(BwdSmem<D>& sm, uint32_t tmem, const BwdDev& p, const CUtensorMap* tm_dkacc,
+                            const CUtensorMap* tm_dvacc, int kv_z, int q_z, int kv_tile, int q_rank, int kv_rank,
                             const int32_t* rg, int nr, volatile int* ab, int* err) {
   const int wg = ((threadIdx.x >> 5) - 4) >> 2;  // 0 or 1: which half of the query columns
   const int wq = (threadIdx.x >> 5) & 3;         // TMEM lane quadrant
   const int lane = threadIdx.x & 31;
   const int row = wq * 32 + lane;  // key row (S^T lane) and also dQ query row
-  const int kv_pos = kv_tile * 128 + row;
+  const int kv_pos = kv_tile * 128 + row;  // row of the key/value slice
+  const int kv_key = bwd_kv_key<kStep>(p, kv_rank, q_rank, kv_pos);
   const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
   const uint32_t t_s = tmem + 64 * wg + lane_off;          // this half's S^T columns
   const uint32_t t_dp = tmem + 128 + 64 * wg + lane_off;   // this half's dP^T columns
@@ -325,7 +349,7 @@ __device__ void bwd_compute(BwdSmem<D>& sm, uint32_t tmem, const BwdDev& p, cons
     const int q0 = qi.it * 128;
     // Probabilities are zero where the key is after the query (causal) or
     // past the end; padded query rows have -lse2 = -inf, hence P = 0.
-    const int first_valid_q = p.causal ? kv_pos - q0 : 0;  // local query index
+    const int first_valid_q = p.causal ? kv_key - bwd_q_key<kStep>(p, q_rank, q0) : 0;  // local query index
     const bool row_dead = kv_pos >= p.L;
     const bool need_mask = row_dead || first_valid_q > 64 * wg;
     const float* nlse2 = sm.lse2[slot];  // -lse * log2(e)
@@ -496,7 +520,7 @@ __device__ void bwd_compute(BwdSmem<D>& sm, uint32_t tmem, const BwdDev& p, cons
   }
 }
 
-template <int D>
+template <int D, bool kStep>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     ring_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -512,11 +536,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // items head-major: all key tiles of query head 0 (longest first), then head 1, ...
   const int qh = blockIdx.x / p.n_blocks;  // b * Hq + h
-  const int kv_tile = p.order[blockIdx.x % p.n_blocks];
+  const int item = p.order[blockIdx.x % p.n_blocks];
   const int b = qh / p.Hq, h = qh % p.Hq;
-  const int kv_z = b * p.Hkv + h / (p.Hq / p.Hkv);
-  const int32_t* rg = p.ranges + 2 * p.offsets[kv_tile];
-  const int nr = p.offsets[kv_tile + 1] - p.offsets[kv_tile];
+  int kv_tile = item, q_rank = 0, kv_rank = 0;
+  int q_z = qh, kv_z = b * p.Hkv + h / (p.Hq / p.Hkv);
+  if constexpr (kStep) {
+    q_rank = item / p.step_nt;
+    kv_tile = item % p.step_nt;
+    kv_rank = ((q_rank - p.step) % p.n_chunks + p.n_chunks) % p.n_chunks;
+    q_z += q_rank * p.B * p.Hq;
+    kv_z += kv_rank * p.B * p.Hkv;
+  }
+  const int32_t* rg = p.ranges + 2 * p.offsets[item];
+  const int nr = p.offsets[item + 1] - p.offsets[item];
+  if (kStep && nr == 0) return;  // a ring-step tile no query of the rank sees: nothing to add
   volatile int* ab = &sm.abort_flag;
 
   if (threadIdx.x == 0) {
@@ -556,18 +589,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   if (warp == 0) {
-    if (lane == 0) bwd_producer<D>(sm, &tm_q, &tm_k, &tm_v, &tm_do, p, kv_z, qh, kv_tile, rg, nr, ab, p.err);
+    if (lane == 0) bwd_producer<D>(sm, &tm_q, &tm_k, &tm_v, &tm_do, p, kv_z, q_z, kv_tile, rg, nr, ab, p.err);
   } else if (warp == 1) {
     // the whole warp runs the issue loop; one elected lane issues
     int nq = 0;
     for (int ri = 0; ri < nr; ++ri) nq += rg[2 * ri + 1] - rg[2 * ri];
     bwd_mma<D>(sm, tmem, static_cast<uint32_t>(nq), ab, p.err);
   } else if (warp == 3) {
-    if (lane == 0) bwd_dq_reducer<D>(sm, p.dq_acc, p.Lpad, qh, rg, nr, ab, p.err);
+    if (lane == 0) bwd_dq_reducer<D>(sm, p.dq_acc, p.Lpad, q_z, rg, nr, ab, p.err);
     __syncwarp();
     named_bar_sync(1, 288);
   } else if (warp >= 4) {
-    bwd_compute<D>(sm, tmem, p, &tm_dkacc, &tm_dvacc, kv_z, qh, kv_tile, rg, nr, ab, p.err);
+    bwd_compute<D, kStep>(sm, tmem, p, &tm_dkacc, &tm_dvacc, kv_z, q_z, kv_tile, q_rank, kv_rank, rg, nr, ab,
+                          p.err);
   }
   tc_fence_before();
   __syncthreads();
@@ -682,16 +716,25 @@ __global__ void __launch_bounds__(256) ring_attn_bwd_dq_post_kernel(const float*
 }
 
 template <int D>
-cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
-  const long long rows = static_cast<long long>(a.B) * a.Hq * a.Lpad;
+cudaError_t launch_bwd_pre_d(const BwdArgs& a, long long q_slices, long long kv_slices, cudaStream_t stream) {
+  const long long rows = q_slices * a.Lpad;
   const unsigned pre_blocks = static_cast<unsigned>((rows * 32 + 255) / 256);
   if (a.timer) a.timer->mark(1, false, stream);
   ring_attn_bwd_pre_kernel<D><<<pre_blocks, 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dO), a.lse, a.lse2, a.Dvec,
-      a.dq_acc, a.dk_acc, a.dv_acc, a.L, a.Lpad, rows, static_cast<long long>(a.B) * a.Hkv * a.Lpad);
+      a.dq_acc, a.dk_acc, a.dv_acc, a.L, a.Lpad, rows, kv_slices * a.Lpad);
   cudaError_t e = cudaGetLastError();
   if (a.timer) a.timer->mark(1, true, stream);
-  if (e != cudaSuccess) return e;
+  return e;
+}
+
+template <int D>
+cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
+  cudaError_t e;
+  if (!a.step_nt) {
+    e = launch_bwd_pre_d<D>(a, static_cast<long long>(a.B) * a.Hq, static_cast<long long>(a.B) * a.Hkv, stream);
+    if (e != cudaSuccess) return e;
+  }
 
   BwdDev p;
   p.B = a.B; p.Hq = a.Hq; p.Hkv = a.Hkv; p.L = a.L; p.Lpad = a.Lpad; p.causal = a.causal;
@@ -704,16 +747,18 @@ cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
   p.dk = static_cast<__nv_bfloat16*>(a.dk);
   p.dv = static_cast<__nv_bfloat16*>(a.dv);
   p.err = a.err;
+  p.step_nt = a.step_nt; p.step = a.step; p.n_chunks = a.n_chunks; p.striped = a.striped;
   const size_t smem = sizeof(BwdSmem<D>);
-  e = cudaFuncSetAttribute(ring_attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  auto kernel = a.step_nt ? ring_attn_bwd_kernel<D, true> : ring_attn_bwd_kernel<D, false>;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const dim3 grid(static_cast<unsigned>(a.n_blocks) * a.B * a.Hq);
-  if (a.timer) a.timer->mark(2, false, stream);
-  ring_attn_bwd_kernel<D><<<grid, kBwdThreads, smem, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dkacc,
-                                                               a.tm_dvacc, p);
+  const int kind = a.step_nt ? 4 : 2;  // profiling kinds of include/ring_attn.h: ring step / backward main
+  if (a.timer) a.timer->mark(kind, false, stream);
+  kernel<<<grid, kBwdThreads, smem, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dkacc, a.tm_dvacc, p);
   e = cudaGetLastError();
-  if (a.timer) a.timer->mark(2, true, stream);
-  if (e != cudaSuccess) return e;
+  if (a.timer) a.timer->mark(kind, true, stream);
+  if (e != cudaSuccess || a.step_nt) return e;  // ring steps: the driver converts the gradients
 
   const long long nq8 = static_cast<long long>(a.B) * a.Hq * a.Lpad * D / 8;
   if (a.timer) a.timer->mark(3, false, stream);
@@ -740,6 +785,11 @@ size_t bwd_smem_bytes(int d) {
 
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream) {
   return a.d == 128 ? launch_bwd_d<128>(a, stream) : launch_bwd_d<64>(a, stream);
+}
+
+cudaError_t launch_bwd_pre(const BwdArgs& a, long long q_slices, long long kv_slices, cudaStream_t stream) {
+  return a.d == 128 ? launch_bwd_pre_d<128>(a, q_slices, kv_slices, stream)
+                    : launch_bwd_pre_d<64>(a, q_slices, kv_slices, stream);
 }
 
 }  // namespace ra

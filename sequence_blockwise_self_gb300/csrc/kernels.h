@@ -93,11 +93,19 @@ struct BwdArgs {
   void* dv;                 // bf16 [B*Hkv*L*d]
   int* err;
   LaunchTimer* timer;       // nullptr unless profiling
+  // ring step mode (step_nt > 0: key/value tiles per chunk; n_blocks = n_chunks
+  // * step_nt items; L = Lpad = the chunk length; slices chunk-major, see
+  // attn_bwd.cu): only the main kernel runs, with dK/dV always reduced into
+  // the fp32 accumulators; the driver runs launch_bwd_pre and the conversions
+  int step_nt = 0, step = 0, n_chunks = 1, striped = 0;
 };
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_selftest_wait(int* err, unsigned long long timeout_ns, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
+// The backward's statistics pre-pass alone over q_slices (and kv_slices for
+// zeroing the dK/dV accumulators) slices of Lpad rows.
+cudaError_t launch_bwd_pre(const BwdArgs& a, long long q_slices, long long kv_slices, cudaStream_t stream);
 
 // Ring mode (ring_step.cu): the log-sum-exp merge of n_rows rows (in place
 // into o, lse; optional bf16 copy into o_out), and the gather of a [Z][L][d]
@@ -107,6 +115,15 @@ cudaError_t launch_ring_merge(float* o, float* lse, const float* o_s, const floa
                               long long n_rows, int d, cudaStream_t stream);
 cudaError_t launch_ring_gather(const void* src, void* dst, int Z, int L, int d, int N, bool causal, bool striped,
                                cudaStream_t stream);
+// Ring-mode backward (ring_step.cu): gather of one fp32 per row (lse) into
+// chunk order, and the scatter of an fp32 gradient accumulator in chunk
+// order (plain, or the tiled dQ layout) back to sequence order as
+// bf16(scale * acc).
+cudaError_t launch_ring_gather_rows(const float* src, float* dst, int Z, int L, int N, bool causal, bool striped,
+                                    cudaStream_t stream);
+cudaError_t launch_ring_scatter_grad(const float* acc, void* g, float scale, bool tiled, int Z, int L, int d, int N,
+                                     bool causal, bool striped, cudaStream_t stream);
+
 // Ulysses (ulysses.cu): the all-to-all between sequence shards
 // [N][B][H][L/N][row] and head shards [N][B][H/N][L][row] (to_heads) or
 // back; row_bytes a multiple of 16 (d values of bf16) or 4 (one fp32).

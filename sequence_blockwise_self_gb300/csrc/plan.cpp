@@ -120,4 +120,27 @@ Plan build_step_plan(int L, int N, bool causal, bool striped, int step, int rank
   return p;
 }
 
+Plan build_bwd_step_plan(int L, int N, bool causal, bool striped, int step) {
+  Plan p;
+  const int C = L / N;
+  const int nt = C / kTileRows;
+  p.n_blocks = N * nt;
+  p.offsets.push_back(0);
+  std::vector<int> tiles;
+  for (int r = 0; r < N; ++r) {
+    const int src = ((r - step) % N + N) % N;
+    for (int kt = 0; kt < nt; ++kt) {
+      tiles.clear();
+      const int kmin = chunk_pos(L, N, causal, striped, src, kt * kTileRows);
+      for (int qt = 0; qt < nt; ++qt)
+        if (!causal || kmin <= chunk_pos(L, N, causal, striped, r, qt * kTileRows + kTileRows - 1)) tiles.push_back(qt);
+      append_ranges(tiles, p.ranges);
+      p.offsets.push_back(static_cast<int32_t>(p.ranges.size() / 2));
+      p.work.push_back(static_cast<int64_t>(tiles.size()));
+    }
+  }
+  finish(p);
+  return p;
+}
+
 }  // namespace ra

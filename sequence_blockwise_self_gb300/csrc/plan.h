@@ -89,4 +89,10 @@ RA_HOST_DEVICE inline int chunk_pos(int L, int N, bool causal, bool striped, int
 // (a causal block entirely before the source's keys).
 Plan build_step_plan(int L, int N, bool causal, bool striped, int step, int rank_lo, int rank_hi);
 
+// Backward of step s for every rank: item k is tile k % nt (nt = C / 128) of
+// the key/value chunk rank r = k / nt holds at step s (its source); it lists
+// the tiles of rank r's query chunk (chunk-local, ascending) holding a query
+// that may see a key of that tile.  An item may list none.
+Plan build_bwd_step_plan(int L, int N, bool causal, bool striped, int step);
+
 }  // namespace ra

@@ -30,7 +30,8 @@ struct DevicePlan {
 };
 
 std::map<std::tuple<int, int, int, int, int>, DevicePlan> g_plans;  // (device, kind, L, N, causal)
-// ring step plans: (device, L, N, causal, striped, step, first rank, end rank)
+// ring step plans: (device, L, N, causal, striped, step, first rank, end rank;
+// end rank -1 = the backward plan of the step)
 std::map<std::tuple<int, int, int, int, int, int, int, int>, DevicePlan> g_step_plans;
 std::map<int, int*> g_status_ptr;                                   // device -> &g_device_status
 
@@ -157,7 +158,9 @@ int get_step_plan(int dev, int L, int N, int causal, int striped, int step, int 
     return RING_ATTN_OK;
   }
   DevicePlan dp;
-  int rc = upload_plan(build_step_plan(L, N, causal != 0, striped != 0, step, rank_lo, rank_hi), &dp);
+  int rc = upload_plan(rank_hi < 0 ? build_bwd_step_plan(L, N, causal != 0, striped != 0, step)
+                                   : build_step_plan(L, N, causal != 0, striped != 0, step, rank_lo, rank_hi),
+                       &dp);
   if (rc != RING_ATTN_OK) return rc;
   g_step_plans[key] = dp;
   *out = dp;
@@ -291,6 +294,31 @@ int bwd_impl(int dev, const void* q, const void* k, const void* v, const void* o
   a.dv_acc = w.kv_accumulate ? reinterpret_cast<float*>(ws + w.dv) : nullptr;
   a.dq = dq; a.dk = dk; a.dv = dv; a.err = err; a.timer = active_timer();
   return launch_bwd(a, stream) == cudaSuccess ? RING_ATTN_OK : RING_ATTN_ERR_CUDA;
+}
+
+// Ring-mode backward: parts of the workspace (byte offsets, 256-aligned):
+// q, k, v, o, dO and lse in chunk order, the statistics (-lse log2 e, -D),
+// and the fp32 gradient accumulators (dQ tiled as in the fused backward).
+struct RingBwdWorkspace {
+  size_t qc = 0, kc = 0, vc = 0, oc = 0, dOc = 0, lsec = 0, lse2 = 0, dvec = 0, dq = 0, dk = 0, dv = 0, total = 0;
+};
+
+RingBwdWorkspace ring_bwd_workspace(int B, int Hq, int Hkv, int L, int d) {
+  auto up = [](size_t x) { return round_up(x, 256); };
+  const size_t nq = static_cast<size_t>(B) * Hq * L, nkv = static_cast<size_t>(B) * Hkv * L;
+  RingBwdWorkspace w;
+  w.kc = w.qc + up(nq * d * 2);
+  w.vc = w.kc + up(nkv * d * 2);
+  w.oc = w.vc + up(nkv * d * 2);
+  w.dOc = w.oc + up(nq * d * 2);
+  w.lsec = w.dOc + up(nq * d * 2);
+  w.lse2 = w.lsec + up(nq * 4);
+  w.dvec = w.lse2 + up(nq * 4);
+  w.dq = w.dvec + up(nq * 4);
+  w.dk = w.dq + up(nq * d * 4);
+  w.dv = w.dk + up(nkv * d * 4);
+  w.total = w.dv + up(nkv * d * 4);
+  return w;
 }
 
 // Ulysses: parts of the workspace (byte offsets, 256-aligned): head-shard
@@ -568,6 +596,83 @@ int ring_attn_ring_fwd(const void* q, const void* k, const void* v, void* o, flo
   }
   if (t) t->mark(RING_ATTN_KERNEL_RING_IO, false, stream);
   if (launch_ring_scatter(oacc, lacc, o, lse, B * Hq, L, d, N, sc, st, stream) != cudaSuccess)
+    return RING_ATTN_ERR_CUDA;
+  if (t) t->mark(RING_ATTN_KERNEL_RING_IO, true, stream);
+  return RING_ATTN_OK;
+}
+
+size_t ring_attn_ring_bwd_workspace_size(int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal,
+                                         int striped) {
+  if (check_ring_shape(B, Hq, Hkv, L, d, n_chunks, causal, striped) != RING_ATTN_OK) return 0;
+  return ring_bwd_workspace(B, Hq, Hkv, L, d).total;
+}
+
+int ring_attn_ring_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                       void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal,
+                       int striped, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  int rc = check_ring_shape(B, Hq, Hkv, L, d, n_chunks, causal, striped);
+  if (rc != RING_ATTN_OK) return rc;
+  if (B == 0 || L == 0) return RING_ATTN_OK;
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return RING_ATTN_ERR_NULL;
+  const void* ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return RING_ATTN_ERR_UNSUPPORTED;
+  const RingBwdWorkspace w = ring_bwd_workspace(B, Hq, Hkv, L, d);
+  if (!workspace || workspace_bytes < w.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return RING_ATTN_ERR_WORKSPACE;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  int dev;
+  if ((rc = current_device(&dev)) != RING_ATTN_OK) return rc;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const int N = n_chunks, C = L / N;
+  const bool sc = causal != 0, st = striped != 0;
+  LaunchTimer* t = active_timer();
+  // every rank's rows in chunk order
+  if (t) t->mark(RING_ATTN_KERNEL_RING_IO, false, stream);
+  if (launch_ring_gather(q, ws + w.qc, B * Hq, L, d, N, sc, st, stream) != cudaSuccess ||
+      launch_ring_gather(k, ws + w.kc, B * Hkv, L, d, N, sc, st, stream) != cudaSuccess ||
+      launch_ring_gather(v, ws + w.vc, B * Hkv, L, d, N, sc, st, stream) != cudaSuccess ||
+      launch_ring_gather(o, ws + w.oc, B * Hq, L, d, N, sc, st, stream) != cudaSuccess ||
+      launch_ring_gather(dO, ws + w.dOc, B * Hq, L, d, N, sc, st, stream) != cudaSuccess ||
+      launch_ring_gather_rows(lse, reinterpret_cast<float*>(ws + w.lsec), B * Hq, L, N, sc, st, stream) !=
+          cudaSuccess)
+    return RING_ATTN_ERR_CUDA;
+  if (t) t->mark(RING_ATTN_KERNEL_RING_IO, true, stream);
+  BwdArgs a;
+  std::memset(&a, 0, sizeof a);
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const int zq = N * B * Hq, zkv = N * B * Hkv;
+  if (!make_map(&a.tm_q, ws + w.qc, bf, 2, d, C, zq, 64) || !make_map(&a.tm_k, ws + w.kc, bf, 2, d, C, zkv, 64) ||
+      !make_map(&a.tm_v, ws + w.vc, bf, 2, d, C, zkv, 64) || !make_map(&a.tm_do, ws + w.dOc, bf, 2, d, C, zq, 64) ||
+      !make_map(&a.tm_dkacc, ws + w.dk, f32, 4, d, C, zkv, 32, 32) ||
+      !make_map(&a.tm_dvacc, ws + w.dv, f32, 4, d, C, zkv, 32, 32))
+    return RING_ATTN_ERR_CUDA;
+  int* err;
+  if ((rc = status_ptr(dev, &err)) != RING_ATTN_OK) return rc;
+  a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.L = C; a.Lpad = C; a.d = d; a.causal = sc;
+  a.o = ws + w.oc; a.dO = ws + w.dOc; a.lse = reinterpret_cast<const float*>(ws + w.lsec);
+  a.lse2 = reinterpret_cast<float*>(ws + w.lse2);
+  a.Dvec = reinterpret_cast<float*>(ws + w.dvec);
+  a.dq_acc = reinterpret_cast<float*>(ws + w.dq);
+  a.dk_acc = reinterpret_cast<float*>(ws + w.dk);
+  a.dv_acc = reinterpret_cast<float*>(ws + w.dv);
+  a.err = err; a.timer = t;
+  // statistics of every rank's rows, accumulators zeroed
+  if (launch_bwd_pre(a, zq, zkv, stream) != cudaSuccess) return RING_ATTN_ERR_CUDA;
+  a.step_nt = C / kTileRows; a.n_chunks = N; a.striped = st;
+  for (int s = 0; s < N; ++s) {
+    DevicePlan plan;
+    if ((rc = get_step_plan(dev, L, N, causal, striped, s, 0, -1, &plan)) != RING_ATTN_OK) return rc;
+    a.n_blocks = plan.n_blocks;
+    a.order = plan.order(); a.offsets = plan.offsets(); a.ranges = plan.ranges();
+    a.step = s;
+    if (launch_bwd(a, stream) != cudaSuccess) return RING_ATTN_ERR_CUDA;
+  }
+  const float scale = 1.0f / sqrtf(static_cast<float>(d));
+  if (t) t->mark(RING_ATTN_KERNEL_RING_IO, false, stream);
+  if (launch_ring_scatter_grad(a.dq_acc, dq, scale, true, B * Hq, L, d, N, sc, st, stream) != cudaSuccess ||
+      launch_ring_scatter_grad(a.dk_acc, dk, scale, false, B * Hkv, L, d, N, sc, st, stream) != cudaSuccess ||
+      launch_ring_scatter_grad(a.dv_acc, dv, 1.f, false, B * Hkv, L, d, N, sc, st, stream) != cudaSuccess)
     return RING_ATTN_ERR_CUDA;
   if (t) t->mark(RING_ATTN_KERNEL_RING_IO, true, stream);
   return RING_ATTN_OK;

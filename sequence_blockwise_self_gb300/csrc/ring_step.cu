@@ -117,9 +117,84 @@ __global__ void __launch_bounds__(256) ring_scatter_kernel(const float* __restri
   if (c8 == 0) lse[out] = lse_acc[rowg];
 }
 
+// dst[r][z][i] = src[z][pos(r, i)] for one fp32 per row (lse).
+__global__ void __launch_bounds__(256) ring_gather_rows_kernel(const float* __restrict__ src, float* __restrict__ dst,
+                                                               int Z, int L, int N, int causal, int striped,
+                                                               long long n_rows) {
+  const long long rowg = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (rowg >= n_rows) return;
+  const int C = L / N;
+  const int i = static_cast<int>(rowg % C);
+  const long long rz = rowg / C;
+  const int z = static_cast<int>(rz % Z);
+  const int r = static_cast<int>(rz / Z);
+  dst[rowg] = src[static_cast<size_t>(z) * L + chunk_pos(L, N, causal != 0, striped != 0, r, i)];
+}
+
+// Gradient back to sequence order: g[z][pos(r, i)][:] = bf16(scale * acc)
+// for the fp32 accumulator in chunk order, either plain ([r][z][i][d]) or in
+// the backward kernel's tiled dQ layout (per 128-row tile, [d/4][128][4]).
+template <int D, bool kTiled>
+__global__ void __launch_bounds__(256) ring_scatter_grad_kernel(const float* __restrict__ acc,
+                                                                __nv_bfloat16* __restrict__ g, float scale, int Z,
+                                                                int L, int N, int causal, int striped,
+                                                                long long n_vec) {
+  const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= n_vec) return;
+  constexpr int kVec = D / 8;
+  const int c8 = static_cast<int>(t % kVec);
+  const long long rowg = t / kVec;
+  const int C = L / N;
+  const int i = static_cast<int>(rowg % C);
+  const long long rz = rowg / C;
+  const int z = static_cast<int>(rz % Z);
+  const int r = static_cast<int>(rz / Z);
+  float4 a, b;
+  if (kTiled) {  // slice rz of C rows, tile i / 128, column quads 2 c8 and 2 c8 + 1
+    const float* base = acc + static_cast<size_t>(rz) * C * D + static_cast<size_t>(i >> 7) * 128 * D +
+                        (i & 127) * 4;
+    a = *reinterpret_cast<const float4*>(base + (2 * c8) * 512);
+    b = *reinterpret_cast<const float4*>(base + (2 * c8 + 1) * 512);
+  } else {
+    const float4* s = reinterpret_cast<const float4*>(acc + rowg * D) + 2 * c8;
+    a = s[0];
+    b = s[1];
+  }
+  const size_t out = static_cast<size_t>(z) * L + chunk_pos(L, N, causal != 0, striped != 0, r, i);
+  reinterpret_cast<uint4*>(g + out * D)[c8] =
+      make_uint4(pack_bf16(a.x * scale, a.y * scale), pack_bf16(a.z * scale, a.w * scale),
+                 pack_bf16(b.x * scale, b.y * scale), pack_bf16(b.z * scale, b.w * scale));
+}
+
 unsigned blocks_for(long long n) { return static_cast<unsigned>((n + 255) / 256); }
 
 }  // namespace
+
+cudaError_t launch_ring_gather_rows(const float* src, float* dst, int Z, int L, int N, bool causal, bool striped,
+                                    cudaStream_t stream) {
+  const long long n = static_cast<long long>(Z) * L;
+  ring_gather_rows_kernel<<<blocks_for(n), 256, 0, stream>>>(src, dst, Z, L, N, causal, striped, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ring_scatter_grad(const float* acc, void* g, float scale, bool tiled, int Z, int L, int d, int N,
+                                     bool causal, bool striped, cudaStream_t stream) {
+  const long long n = static_cast<long long>(Z) * L * (d / 8);
+  auto* out = static_cast<__nv_bfloat16*>(g);
+  const unsigned nb = blocks_for(n);
+  if (d == 128) {
+    if (tiled)
+      ring_scatter_grad_kernel<128, true><<<nb, 256, 0, stream>>>(acc, out, scale, Z, L, N, causal, striped, n);
+    else
+      ring_scatter_grad_kernel<128, false><<<nb, 256, 0, stream>>>(acc, out, scale, Z, L, N, causal, striped, n);
+  } else {
+    if (tiled)
+      ring_scatter_grad_kernel<64, true><<<nb, 256, 0, stream>>>(acc, out, scale, Z, L, N, causal, striped, n);
+    else
+      ring_scatter_grad_kernel<64, false><<<nb, 256, 0, stream>>>(acc, out, scale, Z, L, N, causal, striped, n);
+  }
+  return cudaGetLastError();
+}
 
 cudaError_t launch_ring_merge(float* o, float* lse, const float* o_s, const float* lse_s, void* o_out,
                               long long n_rows, int d, cudaStream_t stream) {

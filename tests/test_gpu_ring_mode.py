@@ -152,3 +152,32 @@ def test_ring_mode_at_32k_on_sampled_rows(striped):
     o_ref, lse_ref, _ = oracle.fwd_rows(q.double(), k.double(), v.double(), w.causal, rows)
     check_bf16("o (ring mode, 32k)", f64(o[:, :, rows]), o_ref)
     check_fp32("lse (ring mode, 32k)", f64(lse[:, :, rows]), lse_ref, TOL_LSE)
+
+
+@pytest.mark.parametrize("case", RING_CASES, ids=case_id)
+def test_ring_backward_matches_the_oracle_and_the_fused_kernel(case):
+    B, Hq, Hkv, L, d, N, causal, striped = case
+    q, k, v, dO = inputs.make_inputs(B, Hq, Hkv, L, d, seed=13 + sum(case[:6]))
+    qd, kd, vd, dOd = q.cuda(), k.cuda(), v.cuda(), dO.cuda()
+    o, lse = ra.ring_attn_fwd(qd, kd, vd, 1, causal)
+    dq, dk, dv = ra.ring_attn_ring_bwd(qd, kd, vd, o, lse, dOd, N, causal, striped=striped)
+    dq_f, dk_f, dv_f = ra.ring_attn_bwd(qd, kd, vd, o, lse, dOd, 1, causal)
+    torch.cuda.synchronize()
+    assert_status_ok()
+    dq_ref, dk_ref, dv_ref, _, _ = oracle.bwd(q.double(), k.double(), v.double(), dO.double(), causal)
+    for name, got, want, fused in (("dq", dq, dq_ref, dq_f), ("dk", dk, dk_ref, dk_f), ("dv", dv, dv_ref, dv_f)):
+        check_bf16(f"{name} (ring mode)", f64(got), want)
+        check_bf16(f"{name} (ring mode vs fused)", f64(got), f64(fused), ulps=2)
+
+
+@pytest.mark.parametrize("striped", [False, True])
+def test_ring_backward_at_32k_matches_the_fused_kernel(striped):
+    w = inputs.WORKLOADS["gqa_32k"]
+    q, k, v, dO = (x.cuda() for x in inputs.workload_inputs(w))
+    o, lse = ra.ring_attn_fwd(q, k, v, w.n_chunks, w.causal)
+    got = ra.ring_attn_ring_bwd(q, k, v, o, lse, dO, w.n_chunks, w.causal, striped=striped)
+    want = ra.ring_attn_bwd(q, k, v, o, lse, dO, w.n_chunks, w.causal)
+    torch.cuda.synchronize()
+    assert_status_ok()
+    for name, g, f in zip(("dq", "dk", "dv"), got, want):
+        check_bf16(f"{name} (ring mode vs fused, 32k)", f64(g), f64(f), ulps=2)

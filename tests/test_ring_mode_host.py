@@ -141,3 +141,15 @@ def test_ulysses_rejects_bad_arguments(lib):
     bargs = [P256] * 9
     assert lib.ring_attn_ulysses_bwd(*bargs, 1, 4, 2, 512, 64, 2, 1, P256, ws - 1, NUL) == capi.ERR_WORKSPACE
     assert lib.ring_attn_ulysses_bwd(*bargs, 1, 4, 2, 512, 96, 2, 1, P256, ws, NUL) == capi.ERR_UNSUPPORTED
+
+
+def test_ring_bwd_workspace_and_arguments(lib):
+    ws = lib.ring_attn_ring_bwd_workspace_size(1, 2, 1, 1024, 64, 4, 1, 0)
+    rows_q, rows_kv = 2 * 1024, 1024
+    # q, o, dO, k, v in chunk order (bf16); lse, -lse log2 e, -D; fp32 dq, dk, dv accumulators
+    assert ws == 3 * rows_q * 64 * 2 + 2 * rows_kv * 64 * 2 + 3 * rows_q * 4 + rows_q * 64 * 4 + 2 * rows_kv * 64 * 4
+    assert lib.ring_attn_ring_bwd_workspace_size(1, 2, 1, 512, 64, 4, 1, 0) == 0  # not whole tiles
+    args = [P256] * 9
+    assert lib.ring_attn_ring_bwd(*args, 1, 2, 1, 1024, 64, 4, 1, 0, NUL, ws, NUL) == capi.ERR_WORKSPACE
+    assert lib.ring_attn_ring_bwd(*args, 1, 2, 1, 1024, 64, 4, 1, 0, P256, ws - 1, NUL) == capi.ERR_WORKSPACE
+    assert lib.ring_attn_ring_bwd(*([NUL] * 9), 1, 2, 1, 1024, 64, 4, 1, 0, P256, ws, NUL) == capi.ERR_NULL
