@@ -446,7 +446,15 @@ def run_ours(args, w):
             def ring_fwd():
                 ra.ring_attn_ring_fwd(qd, kd, vd, w.n_chunks, w.causal, o=o_r, lse=lse_r, workspace=ws_r,
                                       stream=stream, striped=striped)
+            ws_b = torch.empty(ra.ring_bwd_workspace_size(w.B, w.Hq, w.Hkv, w.L, w.d, w.n_chunks, w.causal, striped),
+                               dtype=torch.uint8, device=dev)
+            g_r = [torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)]
+
+            def ring_bwd():
+                ra.ring_attn_ring_bwd(qd, kd, vd, o_r, lse_r, dOd, w.n_chunks, w.causal, dq=g_r[0], dk=g_r[1],
+                                      dv=g_r[2], workspace=ws_b, stream=stream, striped=striped)
             ring_fwd()
+            ring_bwd()
             torch.cuda.synchronize(dev)
             r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             r0.record(stream)
@@ -455,6 +463,13 @@ def run_ours(args, w):
             r1.record(stream)
             torch.cuda.synchronize(dev)
             ms_ring = r0.elapsed_time(r1) / args.steps
+            b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            b0.record(stream)
+            for _ in range(args.steps):
+                ring_bwd()
+            b1.record(stream)
+            torch.cuda.synchronize(dev)
+            ms_ring_bwd = b0.elapsed_time(b1) / args.steps
             ra.profile_enable(True)
             for _ in range(args.steps):
                 ring_fwd()
@@ -468,8 +483,11 @@ def run_ours(args, w):
             rows = w.B * w.Hq * w.L
             merge_bytes = rows * (3 * w.d * 4 + 3 * 4)  # read o, o_s, lse, lse_s; write o, lse
             merge_gbs = merge_bytes / (merge_ms / merge_n * 1e-3) / 1e9 if merge_n else None
+            del ws_b, g_r
             return {
                 "fwd_ms": ms_ring, "fwd_tflops": F / (ms_ring * 1e-3) / 1e12,
+                "bwd_ms": ms_ring_bwd, "bwd_tflops": 2.5 * F / (ms_ring_bwd * 1e-3) / 1e12,
+                "fwd_bwd_tflops": step_flops / ((ms_ring + ms_ring_bwd) * 1e-3) / 1e12,
                 "per_kernel_ms_per_fwd": {k: rp[k][0] / args.steps for k in ("ring_step", "ring_merge", "ring_io")},
                 "launches_per_fwd": {k: rp[k][1] // args.steps for k in ("ring_step", "ring_merge", "ring_io")},
                 "merge_roofline": {"bound": "hbm", "achieved": merge_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
