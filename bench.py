@@ -155,6 +155,31 @@ def _gpu_id(torch, dev):
         return vis.split(",")[dev] if vis else str(dev)
 
 
+def _cpulist(text: str):
+    """Parse a Linux cpu list ("0-3,8,10-11")."""
+    cpus = set()
+    for part in text.strip().split(","):
+        if "-" in part:
+            a, b = part.split("-")
+            cpus.update(range(int(a), int(b) + 1))
+        elif part:
+            cpus.add(int(part))
+    return cpus
+
+
+def gpu_local_cpus(gpu_id: str):
+    """CPUs local to the GPU (its NUMA node), from sysfs, or None."""
+    try:
+        bus = subprocess.check_output(["nvidia-smi", "-i", gpu_id, "--query-gpu=pci.bus_id", "--format=csv,noheader"],
+                                      text=True, timeout=30).strip()
+        dom, rest = bus.split(":", 1)
+        with open(f"/sys/bus/pci/devices/{dom[-4:].lower()}:{rest.lower()}/local_cpulist") as f:
+            cpus = _cpulist(f.read()) & os.sched_getaffinity(0)
+        return cpus or None
+    except Exception:
+        return None
+
+
 # ----------------------------------------------------------- multi-rank
 
 def max_over_ranks(x: float, world: int, device=None) -> float:
@@ -270,7 +295,14 @@ def run_ours(args, w):
         if world > 1:
             dist.barrier()
 
-    # inputs: seeded on the CPU (rank-dependent seed), pinned for the e2e leg
+    # inputs: seeded on the CPU (rank-dependent seed), pinned for the e2e leg.
+    # The process runs on the GPU's local CPUs while it pins and copies, so
+    # that the pinned pages sit on the GPU's NUMA node (restored before the
+    # CPU baseline).
+    all_cpus = os.sched_getaffinity(0)
+    local_cpus = gpu_local_cpus(_gpu_id(torch, local)) if not args.no_e2e else None
+    if local_cpus and local_cpus != all_cpus:
+        os.sched_setaffinity(0, local_cpus)
     q, k, v, dO = inputs.workload_inputs(w, seed=inputs.WORKLOAD_SEEDS[w.name] + 1000 * rank)
     host_in = [t.pin_memory() for t in (q, k, v, dO)]
     qd, kd, vd, dOd = (t.to(dev) for t in host_in)
@@ -430,6 +462,8 @@ def run_ours(args, w):
             c1.synchronize()
             link[name] = src.numel() * src.element_size() / (c0.elapsed_time(c1) * 1e6)
         e2e.update(link)
+        e2e["host_cpus"] = (f"{len(local_cpus)} CPUs local to the GPU" if local_cpus and local_cpus != all_cpus
+                            else "all CPUs of the process")
         del dev_in, dev_out
 
     # (4) ring mode: the same forward run step by step the way each rank of a
@@ -553,6 +587,9 @@ def run_ours(args, w):
                              "bytes_per_step": a2a_bytes},
         }
         del qs, ks, vs, dOs, ws_u, o_u, lse_u, g_u
+
+    if os.sched_getaffinity(0) != all_cpus:
+        os.sched_setaffinity(0, all_cpus)
 
     # (6) CPU oracle baseline (rank 0, one GPU only)
     cpu = None

@@ -54,3 +54,10 @@ def test_reference_arm_does_nothing_off_rank_zero(monkeypatch, capsys):
 
     bench.run_reference(argparse.Namespace(gpus=2, steps=1, warmup=0), inputs.WORKLOADS["tiny"])
     assert capsys.readouterr().out == ""
+
+
+def test_cpulist_parsing():
+    import bench
+    assert bench._cpulist("0-3,8,10-11\n") == {0, 1, 2, 3, 8, 10, 11}
+    assert bench._cpulist("5") == {5}
+    assert bench._cpulist("") == set()
