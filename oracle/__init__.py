@@ -14,6 +14,7 @@ from .oracle import (  # noqa: F401
     ring_fwd,
     ring_step,
     merge,
+    ffn,
     owner_rank,
     ring_sources,
     visible_pairs,

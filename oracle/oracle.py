@@ -58,6 +58,8 @@ def _bind(lib):
     lib.oracle_merge.argtypes = [_dp, _dp, _dp, _dp, ctypes.c_long, I]
     lib.oracle_merge.restype = None
     lib.oracle_owner_rank.argtypes = [I, I, I, I, I]
+    lib.oracle_ffn.argtypes = [_dp, _dp, _dp, _dp, _dp, ctypes.c_long, I, I, _dp, I]
+    lib.oracle_ffn.restype = ctypes.c_int
     for f in (lib.oracle_fwd, lib.oracle_fwd_rows, lib.oracle_bwd, lib.oracle_bwd_rows,
               lib.oracle_ring_fwd, lib.oracle_ring_step, lib.oracle_owner_rank):
         f.restype = ctypes.c_int
@@ -223,6 +225,21 @@ def merge(o_a, lse_a, o_b, lse_b):
         raise ValueError("merge: shape mismatch")
     _load().oracle_merge(_p(o), _p(lse), _p(ob), _p(lb), int(lse.size), int(d))
     return o, lse
+
+
+def ffn(x, w1, b1, w2, b2, threads: int = 0):
+    """The BPT feed-forward block with its residual (SP series section 4.2,
+    two linear layers with a 4x up-projection, section 8):
+    y = x + gelu(x W1 + b1) W2 + b2 with the exact GELU x Phi(x); x [M, D],
+    W1 [D, F], W2 [F, D].  Rows are independent (blockwise order is moot)."""
+    x, w1, b1, w2, b2 = (_f64(a) for a in (x, w1, b1, w2, b2))
+    M, D = x.shape
+    F = w1.shape[1]
+    if w1.shape != (D, F) or w2.shape != (F, D) or b1.shape != (F,) or b2.shape != (D,):
+        raise ValueError("ffn: shape mismatch")
+    y = np.zeros((M, D))
+    _check(_load().oracle_ffn(_p(x), _p(w1), _p(b1), _p(w2), _p(b2), M, D, F, _p(y), _threads(threads)))
+    return y
 
 
 # ------------------------------------------------------------ chunk map (host)

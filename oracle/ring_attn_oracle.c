@@ -505,6 +505,64 @@ void oracle_merge(double *o_a, double *lse_a, const double *o_b, const double *l
   }
 }
 
+/* ------------------------------------------------------ blockwise FFN */
+
+/* GELU in its exact form, x * Phi(x) with the standard normal CDF Phi. */
+static double gelu(double x) { return 0.5 * x * (1.0 + erf(x / sqrt(2.0))); }
+
+/* The feed-forward block the BPT section of the pages fuses after attention
+ * for each query block ("Large-scale distributed AI model training series:
+ * sequence parallelism", section 4.2: for the current query block, attention,
+ * then the FFN and the residual connection), with the two linear layers and
+ * the 4x up-projection of the GPT-style FFN the pages assume (section 8):
+ *   y_m = x_m + W2^T gelu(W1^T x_m + b1) + b2
+ * for rows m of x [M][D]; W1 [D][F], W2 [F][D], b1 [F], b2 [D].  Rows are
+ * independent, so the blockwise order changes nothing: plain row loop. */
+typedef struct { const double *x, *w1, *b1, *w2, *b2; double *y; int D, F; } ffn_t;
+
+static void ffn_row(const ffn_t *f, long m, double *h) {
+  const double *x = f->x + (size_t)m * f->D;
+  for (int j = 0; j < f->F; ++j) {
+    double a = f->b1[j];
+    for (int k = 0; k < f->D; ++k) a += x[k] * f->w1[(size_t)k * f->F + j];
+    h[j] = gelu(a);
+  }
+  double *y = f->y + (size_t)m * f->D;
+  for (int c = 0; c < f->D; ++c) {
+    double a = f->b2[c];
+    for (int j = 0; j < f->F; ++j) a += h[j] * f->w2[(size_t)j * f->D + c];
+    y[c] = x[c] + a;
+  }
+}
+
+typedef struct { const ffn_t *f; long n, next; } ffn_task_t;
+
+static void *ffn_worker(void *arg) {
+  ffn_task_t *t = (ffn_task_t *)arg;
+  double *h = (double *)malloc(sizeof(double) * (size_t)t->f->F);
+  for (;;) {
+    long m = __atomic_fetch_add(&t->next, 1, __ATOMIC_RELAXED);
+    if (m >= t->n) break;
+    ffn_row(t->f, m, h);
+  }
+  free(h);
+  return NULL;
+}
+
+int oracle_ffn(const double *x, const double *w1, const double *b1, const double *w2, const double *b2, long M,
+               int D, int F, double *y, int n_threads) {
+  if (M < 0 || D <= 0 || F <= 0) return -1;
+  ffn_t f = {x, w1, b1, w2, b2, y, D, F};
+  ffn_task_t t = {&f, M, 0};
+  if (n_threads <= 0) n_threads = (int)sysconf(_SC_NPROCESSORS_ONLN);
+  if (n_threads < 1) n_threads = 1;
+  if (n_threads > 256) n_threads = 256;
+  pthread_t th[256];
+  for (int i = 0; i < n_threads; ++i) pthread_create(&th[i], NULL, ffn_worker, &t);
+  for (int i = 0; i < n_threads; ++i) pthread_join(th[i], NULL);
+  return n_threads;
+}
+
 int oracle_owner_rank(int L, int n_chunks, int causal, int striped, int p) {
   if (p < 0 || p >= L || bad_chunking(L, n_chunks, causal, striped)) return -1;
   return owner_rank(L, n_chunks, causal, striped, p);

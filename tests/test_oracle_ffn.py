@@ -1,0 +1,69 @@
+"""Pins of the oracle's blockwise-FFN routine (CPU).
+
+The BPT section of the pages ("Large-scale distributed AI model training
+series: sequence parallelism", section 4.2) runs, for each query block,
+attention and then the FFN with its residual connection; the FFN is the
+GPT-style two linear layers with a 4x up-projection (section 8).  The oracle
+computes y = x + gelu(x W1 + b1) W2 + b2 with the exact GELU.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+
+def _weights(D, F, seed):
+    rng = np.random.default_rng(seed)
+    w1 = rng.standard_normal((D, F)) / math.sqrt(D)
+    w2 = rng.standard_normal((F, D)) / math.sqrt(F)
+    return w1, rng.standard_normal(F) * 0.1, w2, rng.standard_normal(D) * 0.1
+
+
+@pytest.mark.parametrize("M,D,F", [(7, 16, 64), (33, 24, 96)])
+def test_ffn_matches_torch(M, D, F):
+    """Library special case: torch in fp64 (erf GELU, matmul)."""
+    rng = np.random.default_rng(M)
+    x = rng.standard_normal((M, D))
+    w1, b1, w2, b2 = _weights(D, F, M + 1)
+    got = oracle.ffn(x, w1, b1, w2, b2)
+    tx = torch.tensor(x)
+    h = torch.nn.functional.gelu(tx @ torch.tensor(w1) + torch.tensor(b1), approximate="none")
+    want = (tx + h @ torch.tensor(w2) + torch.tensor(b2)).numpy()
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-12)
+
+
+def test_gelu_odd_part_closed_form():
+    """gelu(a) - gelu(-a) = a exactly (a Phi(a) + a Phi(-a) = a): with hidden
+    units a and -a weighted +1 and -1 the block adds its pre-activation."""
+    rng = np.random.default_rng(3)
+    M, D = 9, 5
+    x = rng.standard_normal((M, D)) * 3
+    u = rng.standard_normal(D)
+    w1 = np.stack([u, -u], axis=1)          # [D, 2]: a = x.u, then -a
+    b1 = np.zeros(2)
+    w2 = np.zeros((2, D))
+    w2[0, :] = 1.0
+    w2[1, :] = -1.0
+    b2 = rng.standard_normal(D)
+    y = oracle.ffn(x, w1, b1, w2, b2)
+    want = x + (x @ u)[:, None] + b2
+    np.testing.assert_allclose(y, want, rtol=0, atol=1e-12)
+
+
+def test_zero_second_layer_leaves_the_residual():
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((6, 8))
+    w1, b1, _, b2 = _weights(8, 32, 5)
+    y = oracle.ffn(x, w1, b1, np.zeros((32, 8)), b2)
+    np.testing.assert_array_equal(y, x + b2)
+
+
+def test_gelu_values():
+    """A single hidden unit exposes gelu: gelu(0) = 0, gelu(x) -> x for large
+    x, -> 0 for very negative x; gelu(1) = Phi(1) = 0.841344746..."""
+    for a, want in ((0.0, 0.0), (1.0, 0.8413447460685429), (12.0, 12.0), (-12.0, 0.0)):
+        y = oracle.ffn(np.array([[a]]), np.array([[1.0]]), np.zeros(1), np.array([[1.0]]), np.zeros(1))
+        assert abs(y[0, 0] - (a + want)) < 1e-13

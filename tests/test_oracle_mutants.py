@@ -15,6 +15,7 @@ from oracle import oracle as _oracle_mod
 
 import test_oracle_pins as pins
 import test_oracle_ring_step as steps
+import test_oracle_ffn as ffn_pins
 
 SRC = os.path.join(os.path.dirname(pins.__file__), "..", "oracle", "ring_attn_oracle.c")
 
@@ -36,6 +37,8 @@ MUTANTS = {
     "step_wrong_source": ("if (!ring_block(P, t->n_chunks, b, h, i, t->src, s, o_s, &lse_s, t->striped)) {",
                           "if (!ring_block(P, t->n_chunks, b, h, i, t->rank, s, o_s, &lse_s, t->striped)) {"),
     "stripes_as_blocks": ("if (striped) return p % N;", "if (striped) return p / (L / N);"),
+    "ffn_residual_dropped": ("    y[c] = x[c] + a;", "    y[c] = a;"),
+    "ffn_gelu_wrong_scale": ("return 0.5 * x * (1.0 + erf(x / sqrt(2.0)));", "return 0.5 * x * (1.0 + erf(x / 2.0));"),
     "transposed_score": ("s[j] = P->scale * dot(qi, k_row(P, b, g, j), P->d);\n    if (s[j] > m) m = s[j];\n  }\n  double sum",
                          "s[j] = P->scale * dot(q_row(P, b, h, j), k_row(P, b, g, i), P->d);\n    if (s[j] > m) m = s[j];\n  }\n  double sum"),
 }
@@ -56,6 +59,7 @@ def _quick_pins():
                            for c in (False, True) for st in (False, True)]),
         ("merge", steps.test_merge_weights_are_a_sigmoid_of_the_lse_gap),
         ("stripes", lambda: steps.test_striped_step_with_zero_queries_closed_form(3)),
+        ("ffn", lambda: [ffn_pins.test_ffn_matches_torch(7, 16, 64), ffn_pins.test_gelu_values()]),
     ]
     failed = []
     for name, fn in checks:
