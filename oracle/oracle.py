@@ -58,7 +58,7 @@ def _bind(lib):
     lib.oracle_merge.argtypes = [_dp, _dp, _dp, _dp, ctypes.c_long, I]
     lib.oracle_merge.restype = None
     lib.oracle_owner_rank.argtypes = [I, I, I, I, I]
-    lib.oracle_ffn.argtypes = [_dp, _dp, _dp, _dp, _dp, ctypes.c_long, I, I, _dp, I]
+    lib.oracle_ffn.argtypes = [_dp, _dp, _dp, _dp, _dp, ctypes.c_long, I, I, _dp, _dp, I]
     lib.oracle_ffn.restype = ctypes.c_int
     for f in (lib.oracle_fwd, lib.oracle_fwd_rows, lib.oracle_bwd, lib.oracle_bwd_rows,
               lib.oracle_ring_fwd, lib.oracle_ring_step, lib.oracle_owner_rank):
@@ -227,19 +227,33 @@ def merge(o_a, lse_a, o_b, lse_b):
     return o, lse
 
 
-def ffn(x, w1, b1, w2, b2, threads: int = 0):
+def ffn(x, w1, b1, w2, b2, threads: int = 0, rows=None, hidden: bool = False):
     """The BPT feed-forward block with its residual (SP series section 4.2,
     two linear layers with a 4x up-projection, section 8):
     y = x + gelu(x W1 + b1) W2 + b2 with the exact GELU x Phi(x); x [M, D],
-    W1 [D, F], W2 [F, D].  Rows are independent (blockwise order is moot)."""
+    W1 [D, F], W2 [F, D].  Rows are independent (blockwise order is moot).
+    rows: optional row indices; then only those rows are computed and the
+    result is y[rows] ([len(rows), D]).  hidden=True also returns the
+    hidden activation gelu(x W1 + b1) of the same rows."""
     x, w1, b1, w2, b2 = (_f64(a) for a in (x, w1, b1, w2, b2))
     M, D = x.shape
     F = w1.shape[1]
     if w1.shape != (D, F) or w2.shape != (F, D) or b1.shape != (F,) or b2.shape != (D,):
         raise ValueError("ffn: shape mismatch")
-    y = np.zeros((M, D))
-    _check(_load().oracle_ffn(_p(x), _p(w1), _p(b1), _p(w2), _p(b2), M, D, F, _p(y), _threads(threads)))
-    return y
+    if rows is None:
+        y = np.zeros((M, D))
+        h = np.zeros((M, F)) if hidden else None
+        _check(_load().oracle_ffn(_p(x), _p(w1), _p(b1), _p(w2), _p(b2), M, D, F, _p(y),
+                                  _p(h) if hidden else None, _threads(threads)))
+        return (y, h) if hidden else y
+    idx = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1))
+    xs = np.ascontiguousarray(x[idx])
+    n = idx.size
+    y = np.zeros((n, D))
+    h = np.zeros((n, F)) if hidden else None
+    _check(_load().oracle_ffn(_p(xs), _p(w1), _p(b1), _p(w2), _p(b2), n, D, F, _p(y),
+                              _p(h) if hidden else None, _threads(threads)))
+    return (y, h) if hidden else y
 
 
 # ------------------------------------------------------------ chunk map (host)

@@ -518,41 +518,49 @@ static double gelu(double x) { return 0.5 * x * (1.0 + erf(x / sqrt(2.0))); }
  *   y_m = x_m + W2^T gelu(W1^T x_m + b1) + b2
  * for rows m of x [M][D]; W1 [D][F], W2 [F][D], b1 [F], b2 [D].  Rows are
  * independent, so the blockwise order changes nothing: plain row loop. */
-typedef struct { const double *x, *w1, *b1, *w2, *b2; double *y; int D, F; } ffn_t;
+typedef struct { const double *x, *w1, *b1, *w2, *b2; double *y, *h_out; int D, F; } ffn_t;
 
-static void ffn_row(const ffn_t *f, long m, double *h) {
+/* One row.  Each sum runs in ascending order of its index (k for the first
+ * layer, j for the second) starting from the bias; the loops walk the
+ * weights row by row so that they stream through memory. */
+static void ffn_row(const ffn_t *f, long m, double *h, double *acc) {
   const double *x = f->x + (size_t)m * f->D;
+  for (int j = 0; j < f->F; ++j) h[j] = f->b1[j];
+  for (int k = 0; k < f->D; ++k) {
+    const double *w = f->w1 + (size_t)k * f->F;
+    for (int j = 0; j < f->F; ++j) h[j] += x[k] * w[j];
+  }
+  for (int j = 0; j < f->F; ++j) h[j] = gelu(h[j]);
+  if (f->h_out) memcpy(f->h_out + (size_t)m * f->F, h, sizeof(double) * (size_t)f->F);
+  for (int c = 0; c < f->D; ++c) acc[c] = f->b2[c];
   for (int j = 0; j < f->F; ++j) {
-    double a = f->b1[j];
-    for (int k = 0; k < f->D; ++k) a += x[k] * f->w1[(size_t)k * f->F + j];
-    h[j] = gelu(a);
+    const double *w = f->w2 + (size_t)j * f->D;
+    for (int c = 0; c < f->D; ++c) acc[c] += h[j] * w[c];
   }
   double *y = f->y + (size_t)m * f->D;
-  for (int c = 0; c < f->D; ++c) {
-    double a = f->b2[c];
-    for (int j = 0; j < f->F; ++j) a += h[j] * f->w2[(size_t)j * f->D + c];
-    y[c] = x[c] + a;
-  }
+  for (int c = 0; c < f->D; ++c) y[c] = x[c] + acc[c];
 }
 
 typedef struct { const ffn_t *f; long n, next; } ffn_task_t;
 
 static void *ffn_worker(void *arg) {
   ffn_task_t *t = (ffn_task_t *)arg;
-  double *h = (double *)malloc(sizeof(double) * (size_t)t->f->F);
+  double *h = (double *)malloc(sizeof(double) * ((size_t)t->f->F + (size_t)t->f->D));
   for (;;) {
-    long m = __atomic_fetch_add(&t->next, 1, __ATOMIC_RELAXED);
-    if (m >= t->n) break;
-    ffn_row(t->f, m, h);
+    long i = __atomic_fetch_add(&t->next, 1, __ATOMIC_RELAXED);
+    if (i >= t->n) break;
+    ffn_row(t->f, i, h, h + t->f->F);
   }
   free(h);
   return NULL;
 }
 
+/* y [M][D] and, if h_out is not NULL, the hidden activation
+ * gelu(W1^T x_m + b1) of every row into h_out [M][F]. */
 int oracle_ffn(const double *x, const double *w1, const double *b1, const double *w2, const double *b2, long M,
-               int D, int F, double *y, int n_threads) {
+               int D, int F, double *y, double *h_out, int n_threads) {
   if (M < 0 || D <= 0 || F <= 0) return -1;
-  ffn_t f = {x, w1, b1, w2, b2, y, D, F};
+  ffn_t f = {x, w1, b1, w2, b2, y, h_out, D, F};
   ffn_task_t t = {&f, M, 0};
   if (n_threads <= 0) n_threads = (int)sysconf(_SC_NPROCESSORS_ONLN);
   if (n_threads < 1) n_threads = 1;

@@ -67,3 +67,20 @@ def test_gelu_values():
     for a, want in ((0.0, 0.0), (1.0, 0.8413447460685429), (12.0, 12.0), (-12.0, 0.0)):
         y = oracle.ffn(np.array([[a]]), np.array([[1.0]]), np.zeros(1), np.array([[1.0]]), np.zeros(1))
         assert abs(y[0, 0] - (a + want)) < 1e-13
+
+
+def test_hidden_activation_and_row_subsets():
+    """The hidden output is gelu(x W1 + b1) (torch fp64, erf GELU) and
+    feeds y; a row subset gives exactly those rows of the full result."""
+    rng = np.random.default_rng(6)
+    M, D, F = 11, 12, 40
+    x = rng.standard_normal((M, D))
+    w1, b1, w2, b2 = _weights(D, F, 7)
+    y, h = oracle.ffn(x, w1, b1, w2, b2, hidden=True)
+    th = torch.nn.functional.gelu(torch.tensor(x) @ torch.tensor(w1) + torch.tensor(b1), approximate="none")
+    np.testing.assert_allclose(h, th.numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(y, x + h @ w2 + b2, rtol=0, atol=1e-12)
+    rows = [10, 0, 4, 4]
+    ys, hs = oracle.ffn(x, w1, b1, w2, b2, rows=rows, hidden=True)
+    np.testing.assert_array_equal(ys, y[rows])
+    np.testing.assert_array_equal(hs, h[rows])

@@ -37,7 +37,7 @@ MUTANTS = {
     "step_wrong_source": ("if (!ring_block(P, t->n_chunks, b, h, i, t->src, s, o_s, &lse_s, t->striped)) {",
                           "if (!ring_block(P, t->n_chunks, b, h, i, t->rank, s, o_s, &lse_s, t->striped)) {"),
     "stripes_as_blocks": ("if (striped) return p % N;", "if (striped) return p / (L / N);"),
-    "ffn_residual_dropped": ("    y[c] = x[c] + a;", "    y[c] = a;"),
+    "ffn_residual_dropped": ("y[c] = x[c] + acc[c];", "y[c] = acc[c];"),
     "ffn_gelu_wrong_scale": ("return 0.5 * x * (1.0 + erf(x / sqrt(2.0)));", "return 0.5 * x * (1.0 + erf(x / 2.0));"),
     "transposed_score": ("s[j] = P->scale * dot(qi, k_row(P, b, g, j), P->d);\n    if (s[j] > m) m = s[j];\n  }\n  double sum",
                          "s[j] = P->scale * dot(q_row(P, b, h, j), k_row(P, b, g, i), P->d);\n    if (s[j] > m) m = s[j];\n  }\n  double sum"),
