@@ -16,6 +16,10 @@ step's q, k, v, dO are copied in and its o, lse, dq, dk, dv copied out,
 on a second stream that overlaps those copies with the neighbouring steps'
 compute, as a training loop would.
 
+The line also carries the ring mode (step kernels + merge), Ulysses (the
+all-to-alls around the fused kernels) and the BPT feed-forward block after
+attention (128k rows, D = 3584, F = 4 D), each timed on its own.
+
 With N > 1 (torchrun) every rank runs an independent replica of the step
 (the ring is emulated on one GPU; nothing is exchanged), and `value` is the
 sum of all ranks' FLOPs over the slowest rank's time.
@@ -588,6 +592,59 @@ def run_ours(args, w):
         }
         del qs, ks, vs, dOs, ws_u, o_u, lse_u, g_u
 
+    # (5b) the BPT feed-forward block after attention: the 128k tokens of
+    # hidden size Hq * d through the two-layer FFN in blocks of 8192 rows
+    # (two tensor-core GEMM launches per block)
+    ffn = None
+    if not args.no_ffn:
+        fw = inputs.FFN_WORKLOADS["ffn_gqa_128k"]
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(11 + rank)
+        xf = torch.randn((fw.M, fw.D), generator=gen, device=dev).to(torch.bfloat16)
+        w1f = (torch.randn((fw.F, fw.D), generator=gen, device=dev) / fw.D ** 0.5).to(torch.bfloat16)
+        w2f = (torch.randn((fw.D, fw.F), generator=gen, device=dev) / fw.F ** 0.5).to(torch.bfloat16)
+        b1f = torch.randn((fw.F,), generator=gen, device=dev) * 0.1
+        b2f = torch.randn((fw.D,), generator=gen, device=dev) * 0.1
+        yf = torch.empty_like(xf)
+        wsf = torch.empty(ra.ffn_workspace_size(fw.D, fw.F, fw.block_rows), dtype=torch.uint8, device=dev)
+
+        def f_step():
+            ra.ring_attn_ffn_fwd(xf, w1f, b1f, w2f, b2f, block_rows=fw.block_rows, y=yf, workspace=wsf,
+                                 stream=stream)
+        for _ in range(3):
+            f_step()
+        torch.cuda.synchronize(dev)
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(args.steps):
+            f_step()
+        f1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms_f = f0.elapsed_time(f1) / args.steps
+        ra.profile_enable(True)
+        for _ in range(args.steps):
+            f_step()
+        torch.cuda.synchronize(dev)
+        fp = ra.profile_read()
+        ra.profile_enable(False)
+        st, site = ra.device_status()
+        if st != 0:
+            raise RuntimeError(f"device status {st} at site {site:#x} in the FFN")
+        tf_f = fw.flops() / (ms_f * 1e-3) / 1e12
+        gemm_ms, gemm_n = fp["ffn_gemm"]
+        tf_gemm = fw.flops() * args.steps / (gemm_ms * 1e-3) / 1e12 if gemm_n else None
+        ffn = {
+            "workload": f"{fw.name}: M={fw.M} rows, D={fw.D}, F={fw.F} (4 D), blocks of {fw.block_rows} rows, "
+                        "y = x + gelu(x W1 + b1) W2 + b2",
+            "ms": ms_f, "tflops": tf_f,
+            "gemm_launches_per_step": gemm_n // args.steps,
+            "roofline": {"bound": "tensor", "achieved": tf_gemm, "peak": peaks["burst"], "unit": "TFLOP/s",
+                         "frac": tf_gemm / peaks["burst"] if tf_gemm else None,
+                         "frac_of_sustained": tf_gemm / peaks["sustained"] if tf_gemm else None,
+                         "flops_per_step": fw.flops()},
+        }
+        del xf, w1f, w2f, b1f, b2f, yf, wsf
+
     if os.sched_getaffinity(0) != all_cpus:
         os.sched_setaffinity(0, all_cpus)
 
@@ -619,6 +676,7 @@ def run_ours(args, w):
             "e2e": e2e,
             "ring_mode": ring,
             "ulysses": ulysses,
+            "ffn": ffn,
             "gpu_launches": 4 * args.steps,
             "clocks": clocks,
         }
@@ -638,6 +696,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-ring-mode", action="store_true")
     ap.add_argument("--no-ulysses", action="store_true")
+    ap.add_argument("--no-ffn", action="store_true")
     args = ap.parse_args()
     from sequence_blockwise_self_gb300 import inputs
 

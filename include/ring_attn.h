@@ -242,6 +242,41 @@ int ring_attn_device_status(cudaStream_t stream, int* site);
 int ring_attn_selftest_bounded_wait(unsigned timeout_us, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------
+ * Blockwise feed-forward (web page "Large-scale distributed AI model
+ * training series: sequence parallelism", section 4.2 Blockwise Parallel
+ * Transformer: after a query block's attention, the FFN and the residual
+ * connection are computed for that block; section 8: the FFN is two linear
+ * layers around an up-projection to F = 4 D in the GPT-style model).  For
+ * every row x_m of x (a token's hidden state):
+ *   y_m = x_m + W2 gelu(W1 x_m + b1) + b2,   gelu(t) = t Phi(t) (exact erf)
+ * The rows are processed in blocks of block_rows rows; only one block's
+ * hidden activation (block_rows x F) exists at a time, in the workspace.
+ *   x, y : bf16 [M][D]     (y may be x: the update is then in place)
+ *   w1   : bf16 [F][D]     (W1, output-major: row f holds the weights of
+ *                           hidden unit f, the layout of a linear layer's
+ *                           weight [out_features][in_features])
+ *   b1   : fp32 [F]
+ *   w2   : bf16 [D][F]     (W2, output-major)
+ *   b2   : fp32 [D]
+ * Products accumulate in fp32; the hidden activation is rounded to bf16
+ * before the second layer (it is the second GEMM's operand).
+ * Supported: D % 256 == 0 and F % 256 == 0 (both >= 256), block_rows a
+ * positive multiple of 128, any M >= 0 (M == 0 is a no-op); every pointer
+ * 16-byte aligned (RING_ATTN_ERR_UNSUPPORTED otherwise), below 2^31 rows.
+ * ------------------------------------------------------------------- */
+
+/* Bytes of workspace ring_attn_ffn_fwd needs (the bf16 hidden block), or 0
+ * for an unsupported shape. */
+size_t ring_attn_ffn_workspace_size(int D, int F, int block_rows);
+
+/* Forward of the blockwise FFN: two persistent tensor-core GEMM launches per
+ * row block (first layer with bias + GELU, second with bias + residual).
+ * workspace: device, 256-byte aligned, >= ring_attn_ffn_workspace_size(). */
+int ring_attn_ffn_fwd(const void* x, const void* w1, const float* b1, const void* w2, const float* b2, void* y,
+                      long long M, int D, int F, int block_rows, void* workspace, size_t workspace_bytes,
+                      cudaStream_t stream);
+
+/* ---------------------------------------------------------------------
  * Per-kernel timing, for measurement.  While enabled, every kernel launch
  * of the library is bracketed by two CUDA events recorded on the launch
  * stream.  ring_attn_profile_read() waits for those events and returns,
@@ -257,7 +292,8 @@ enum {
   RING_ATTN_KERNEL_RING_MERGE = 5, /* ring mode: log-sum-exp merge */
   RING_ATTN_KERNEL_RING_IO = 6,    /* ring mode: gather into / scatter out of chunk order */
   RING_ATTN_KERNEL_ULYSSES_A2A = 7, /* Ulysses: all-to-all between sequence and head shards */
-  RING_ATTN_N_KERNELS = 8
+  RING_ATTN_KERNEL_FFN_GEMM = 8,    /* blockwise feed-forward: one of its two GEMMs */
+  RING_ATTN_N_KERNELS = 9
 };
 int ring_attn_profile_enable(int on);
 int ring_attn_profile_read(double* ms, long long* launches);

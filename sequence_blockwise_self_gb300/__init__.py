@@ -9,6 +9,7 @@ would): ring_attn_fwd_step, ring_attn_merge, ring_attn_ring_fwd,
 ring_attn_ring_bwd.
 Ulysses on one GPU (sequence shards -> head shards -> back):
 ring_attn_ulysses_fwd, ring_attn_ulysses_bwd.
+Blockwise feed-forward (BPT): ring_attn_ffn_fwd.
 Host-only queries: owner_rank, fwd_plan, bwd_plan, step_plan.
 """
 from .capi import (  # noqa: F401
@@ -27,6 +28,8 @@ from .capi import (  # noqa: F401
     ring_attn_bwd,
     ring_attn_bwd_noalloc,
     ring_attn_fwd,
+    ring_attn_ffn_fwd,
+    ffn_workspace_size,
     ring_attn_fwd_step,
     ring_attn_merge,
     ring_attn_ring_fwd,

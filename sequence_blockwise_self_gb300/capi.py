@@ -91,6 +91,10 @@ def load():
     lib.ring_attn_ulysses_fwd.restype = I
     lib.ring_attn_ulysses_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, S, P]
     lib.ring_attn_ulysses_bwd.restype = I
+    lib.ring_attn_ffn_workspace_size.argtypes = [I, I, I]
+    lib.ring_attn_ffn_workspace_size.restype = S
+    lib.ring_attn_ffn_fwd.argtypes = [P, P, P, P, P, P, ctypes.c_longlong, I, I, I, P, S, P]
+    lib.ring_attn_ffn_fwd.restype = I
     _lib = lib
     return lib
 
@@ -349,6 +353,37 @@ def ring_attn_ulysses_bwd(q, k, v, o, lse, dO, causal: bool, dq=None, dk=None, d
     return dq, dk, dv
 
 
+def ffn_workspace_size(D: int, F: int, block_rows: int) -> int:
+    return int(load().ring_attn_ffn_workspace_size(int(D), int(F), int(block_rows)))
+
+
+def ring_attn_ffn_fwd(x, w1, b1, w2, b2, block_rows: int = 8192, y=None, workspace=None, stream=None):
+    """Blockwise feed-forward: y = x + gelu(x W1^T + b1) W2^T + b2 row by row,
+    block_rows rows at a time.  x [M, D] bf16; w1 [F, D], w2 [D, F] bf16
+    (output-major, as a linear layer's weight); b1 [F], b2 [D] fp32.  y may
+    be x (in place)."""
+    import torch
+    if x.dim() != 2 or w1.dim() != 2:
+        raise ValueError("x must be [M, D] and w1 [F, D]")
+    M, D = x.shape
+    F = w1.shape[0]
+    _check_tensor(x, "x", torch.bfloat16, (M, D))
+    _check_tensor(w1, "w1", torch.bfloat16, (F, D))
+    _check_tensor(w2, "w2", torch.bfloat16, (D, F))
+    _check_tensor(b1, "b1", torch.float32, (F,))
+    _check_tensor(b2, "b2", torch.float32, (D,))
+    y = torch.empty_like(x) if y is None else y
+    _check_tensor(y, "y", torch.bfloat16, (M, D))
+    if workspace is None:
+        workspace = torch.empty(max(ffn_workspace_size(D, F, block_rows), 1), dtype=torch.uint8, device=x.device)
+    rc = load().ring_attn_ffn_fwd(_ptr(x), _ptr(w1), _ptr(b1), _ptr(w2), _ptr(b2), _ptr(y), M, D, F,
+                                  int(block_rows), _ptr(workspace),
+                                  int(workspace.numel() * workspace.element_size()), _stream(stream))
+    if rc != OK:
+        raise RingAttnError(rc, "ring_attn_ffn_fwd")
+    return y
+
+
 def bwd_workspace_size(B, Hq, Hkv, L, d, n_chunks, causal) -> int:
     return int(load().ring_attn_bwd_workspace_size(B, Hq, Hkv, L, d, int(n_chunks), int(bool(causal))))
 
@@ -411,7 +446,8 @@ def device_status(stream=None):
     return rc, site.value
 
 
-KERNEL_NAMES = ("fwd", "bwd_pre", "bwd_main", "bwd_post", "ring_step", "ring_merge", "ring_io", "ulysses_a2a")
+KERNEL_NAMES = ("fwd", "bwd_pre", "bwd_main", "bwd_post", "ring_step", "ring_merge", "ring_io", "ulysses_a2a",
+                "ffn_gemm")
 
 
 def profile_enable(on: bool = True):

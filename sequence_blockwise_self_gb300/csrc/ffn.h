@@ -1,0 +1,40 @@
+// ffn.h -- launch interface of the blockwise feed-forward GEMM (ffn.cu).
+#pragma once
+#include "kernels.h"
+
+namespace ra {
+
+// Device-side error sites of the feed-forward GEMM.
+enum FfnErrSite : int {
+  kSiteGemmProducer = 0x401,
+  kSiteGemmMma = 0x402,
+  kSiteGemmEpilogue = 0x404,
+  kSiteGemmDrain = 0x405,
+  kSiteGemmMisaligned = 0x4FF,
+};
+
+// Profiling kind of the feed-forward GEMM (matches the C ABI's list).
+constexpr int kProfFfnGemm = 8;
+
+// C = epilogue(A B^T) with A [rows][K] and B [N][K] bf16, K-major, through
+// 128B-swizzled tensor maps (A and C boxes 64 x 128, B boxes 64 x 256); C
+// bf16 [c_rows][N].
+//   kind 0: C = gelu(acc + bias)         kind 1: C = acc + bias + resid
+// M rows of C starting at c_row0 are produced from M rows of A starting at
+// a_row0; N % 256 == 0, K % 64 == 0; rows past c_rows are neither read
+// (resid) nor written (the store clips them).
+struct FfnGemmArgs {
+  CUtensorMap tm_a, tm_b, tm_c;
+  int M = 0, N = 0, K = 0, a_row0 = 0, c_row0 = 0, c_rows = 0, kind = 0;
+  int group_rows = 8;  // tile order: row tiles per group (row tiles fastest inside a group)
+  const float* bias = nullptr;
+  const void* resid = nullptr;
+  int* err = nullptr;
+  int n_sms = 0;
+  LaunchTimer* timer = nullptr;
+};
+
+cudaError_t launch_ffn_gemm(const FfnGemmArgs& a, cudaStream_t stream);
+size_t ffn_gemm_smem_bytes();
+
+}  // namespace ra

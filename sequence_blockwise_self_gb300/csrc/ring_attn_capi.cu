@@ -2,6 +2,7 @@
 // checks, tensor-map encoding, cached launch plans and kernel launches.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstring>
 #include <map>
 #include <memory>
@@ -9,6 +10,7 @@
 #include <tuple>
 
 #include "../../include/ring_attn.h"
+#include "ffn.h"
 #include "kernels.h"
 #include "plan.h"
 
@@ -164,6 +166,14 @@ int get_step_plan(int dev, int L, int N, int causal, int striped, int step, int 
   if (rc != RING_ATTN_OK) return rc;
   g_step_plans[key] = dp;
   *out = dp;
+  return RING_ATTN_OK;
+}
+
+int ffn_shape(int D, int F, int block_rows) {
+  if (D <= 0 || F <= 0 || block_rows <= 0) return RING_ATTN_ERR_SHAPE;
+  if (D % 256 || F % 256 || block_rows % 128) return RING_ATTN_ERR_UNSUPPORTED;
+  if (D > (1 << 20) || F > (1 << 20)) return RING_ATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(block_rows) * F >= (1ll << 40)) return RING_ATTN_ERR_UNSUPPORTED;
   return RING_ATTN_OK;
 }
 
@@ -757,6 +767,67 @@ int ring_attn_ulysses_bwd(const void* q, const void* k, const void* v, const voi
       a2a(ws + w.dv, dv, row, B, Hkv, N, L, false, stream) != cudaSuccess)
     return RING_ATTN_ERR_CUDA;
   if (t) t->mark(RING_ATTN_KERNEL_ULYSSES_A2A, true, stream);
+  return RING_ATTN_OK;
+}
+
+size_t ring_attn_ffn_workspace_size(int D, int F, int block_rows) {
+  if (ffn_shape(D, F, block_rows) != RING_ATTN_OK) return 0;
+  return round_up(static_cast<size_t>(block_rows) * F * 2, 256);
+}
+
+int ring_attn_ffn_fwd(const void* x, const void* w1, const float* b1, const void* w2, const float* b2, void* y,
+                      long long M, int D, int F, int block_rows, void* workspace, size_t workspace_bytes,
+                      cudaStream_t stream) {
+  int rc = ffn_shape(D, F, block_rows);
+  if (rc != RING_ATTN_OK) return rc;
+  if (M < 0) return RING_ATTN_ERR_SHAPE;
+  if (M >= (1ll << 31)) return RING_ATTN_ERR_UNSUPPORTED;
+  if (M == 0) return RING_ATTN_OK;
+  if (!x || !w1 || !b1 || !w2 || !b2 || !y) return RING_ATTN_ERR_NULL;
+  const void* ptrs[] = {x, w1, b1, w2, b2, y};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return RING_ATTN_ERR_UNSUPPORTED;
+  const size_t need = ring_attn_ffn_workspace_size(D, F, block_rows);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return RING_ATTN_ERR_WORKSPACE;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  int dev;
+  if ((rc = current_device(&dev)) != RING_ATTN_OK) return rc;
+  int n_sms = 0, optin = 0;
+  if (cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+    return RING_ATTN_ERR_CUDA;
+  if (ffn_gemm_smem_bytes() > static_cast<size_t>(optin)) return RING_ATTN_ERR_UNSUPPORTED;
+  int* err;
+  if ((rc = status_ptr(dev, &err)) != RING_ATTN_OK) return rc;
+  const int rows = static_cast<int>(M);
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  // first layer: A = x [M][D], B = W1 [F][D], C = h [block_rows][F]
+  // second layer: A = h, B = W2 [D][F], C = y [M][D], residual x
+  FfnGemmArgs g1, g2;
+  if (!make_map(&g1.tm_a, x, bf, 2, D, rows, 1, 64) || !make_map(&g1.tm_b, w1, bf, 2, D, F, 1, 64, 256) ||
+      !make_map(&g1.tm_c, workspace, bf, 2, F, block_rows, 1, 64) ||
+      !make_map(&g2.tm_a, workspace, bf, 2, F, block_rows, 1, 64) ||
+      !make_map(&g2.tm_b, w2, bf, 2, F, D, 1, 64, 256) || !make_map(&g2.tm_c, y, bf, 2, D, rows, 1, 64))
+    return RING_ATTN_ERR_CUDA;
+  g1.N = F; g1.K = D; g1.c_rows = block_rows; g1.kind = 0; g1.bias = b1;
+  g2.N = D; g2.K = F; g2.c_rows = rows; g2.kind = 1; g2.bias = b2; g2.resid = x;
+  for (FfnGemmArgs* g : {&g1, &g2}) {
+    g->err = err;
+    g->n_sms = n_sms;
+    g->timer = active_timer();
+    // tile order: groups of row tiles whose rows of A take about 16 MiB, so
+    // that a group's A stays in L2 while its column tiles go by
+    const long long a_tile_bytes = 128ll * g->K * 2;
+    g->group_rows = static_cast<int>(std::max(1ll, (1ll << 24) / a_tile_bytes));
+  }
+  for (int r0 = 0; r0 < rows; r0 += block_rows) {
+    const int rb = rows - r0 < block_rows ? rows - r0 : block_rows;
+    g1.M = rb; g1.a_row0 = r0; g1.c_row0 = 0;
+    g2.M = rb; g2.a_row0 = 0; g2.c_row0 = r0;
+    if (launch_ffn_gemm(g1, stream) != cudaSuccess || launch_ffn_gemm(g2, stream) != cudaSuccess)
+      return RING_ATTN_ERR_CUDA;
+  }
   return RING_ATTN_OK;
 }
 

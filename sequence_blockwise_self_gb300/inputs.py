@@ -96,3 +96,62 @@ def tail_rows(L: int, n: int):
     queries i >= j, so the fp64 statistics needed for its gradient stay cheap."""
     n = min(n, L)
     return np.arange(L - n, L, dtype=np.int32)
+
+
+# ---------------------------------------------------------------- blockwise FFN
+
+@dataclass(frozen=True)
+class FfnWorkload:
+    """The feed-forward block after attention: M token rows of hidden size D,
+    hidden layer F = 4 D, processed block_rows rows at a time."""
+    name: str
+    M: int
+    D: int
+    F: int
+    block_rows: int
+
+    def flops(self) -> float:
+        """Two GEMMs of 2 M D F each (bias, GELU and residual not counted)."""
+        return 4.0 * self.M * self.D * self.F
+
+
+# Hidden size 3584 = 28 heads x 128 (the GQA attention above), F = 4 D; the
+# 128k-token sequence in blocks of 8192 rows.
+FFN_WORKLOADS = {
+    "ffn_small": FfnWorkload("ffn_small", 1000, 512, 2048, 384),
+    "ffn_gqa_128k": FfnWorkload("ffn_gqa_128k", 131072, 3584, 14336, 8192),
+}
+FFN_SEEDS = {"ffn_small": 20, "ffn_gqa_128k": 21}
+
+
+def make_ffn_inputs(M, D, F, seed):
+    """Return CPU tensors (x, w1, b1, w2, b2): x [M, D] ~ N(0, 1), w1 [F, D] ~
+    N(0, 1/D), w2 [D, F] ~ N(0, 1/F) (weights output-major, as a linear
+    layer stores them), all rounded to bf16; biases b1 [F], b2 [D] ~
+    N(0, 0.01) in fp32.  Drawn as float32 from a CPU torch.Generator seeded
+    with `seed`, in the order x, w1, b1, w2, b2."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    x = torch.randn((M, D), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    w1 = (torch.randn((F, D), generator=g, dtype=torch.float32) / D ** 0.5).to(torch.bfloat16)
+    b1 = torch.randn((F,), generator=g, dtype=torch.float32) * 0.1
+    w2 = (torch.randn((D, F), generator=g, dtype=torch.float32) / F ** 0.5).to(torch.bfloat16)
+    b2 = torch.randn((D,), generator=g, dtype=torch.float32) * 0.1
+    return x, w1, b1, w2, b2
+
+
+def ffn_sample_rows(M: int, block_rows: int, n: int, seed: int):
+    """Sorted sample of distinct rows: the first and last row of every block
+    and of every 128-row tile edge next to a block edge, then uniform draws
+    from numpy's default_rng(seed + 2000) up to n rows."""
+    rows = {0, M - 1}
+    for b in range(0, M, block_rows):
+        for r in (b, b + 127, b + 128, min(M, b + block_rows) - 1):
+            if 0 <= r < M:
+                rows.add(r)
+    rows = set(sorted(rows)[:n]) if len(rows) > n else rows
+    if len(rows) < n:
+        rng = np.random.default_rng(seed + 2000)
+        rest = np.setdiff1d(np.arange(M), np.array(sorted(rows)))
+        rows |= set(int(r) for r in rng.choice(rest, size=min(n - len(rows), rest.size), replace=False))
+    return np.array(sorted(rows), dtype=np.int64)

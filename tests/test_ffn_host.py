@@ -1,0 +1,53 @@
+"""The blockwise feed-forward entry points of include/ring_attn.h on the
+host (no GPU): workspace size and the argument checks that return before
+anything is launched."""
+import ctypes
+
+import pytest
+
+from sequence_blockwise_self_gb300 import build as lib_build
+from sequence_blockwise_self_gb300 import capi
+
+P256 = ctypes.c_void_p(256)   # an aligned, never dereferenced address
+P8 = ctypes.c_void_p(264)     # 8-byte but not 16-byte aligned
+NUL = ctypes.c_void_p(0)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    lib_build.build()
+    return capi.load()
+
+
+def test_workspace_is_one_hidden_block(lib):
+    # the BPT saving: one block of the hidden activation, bf16
+    assert lib.ring_attn_ffn_workspace_size(3584, 14336, 8192) == 8192 * 14336 * 2
+    assert lib.ring_attn_ffn_workspace_size(256, 768, 128) == 128 * 768 * 2
+
+
+@pytest.mark.parametrize("D,F,R", [(256, 1000, 128), (300, 1024, 128), (256, 1024, 100), (0, 1024, 128),
+                                   (256, 1024, 0), (256, -256, 128)])
+def test_unsupported_shapes_have_no_workspace(lib, D, F, R):
+    assert lib.ring_attn_ffn_workspace_size(D, F, R) == 0
+
+
+def test_argument_errors(lib):
+    ws = lib.ring_attn_ffn_workspace_size(256, 1024, 256)
+    ptrs = [P256] * 6
+    f = lib.ring_attn_ffn_fwd
+    assert f(*ptrs, -1, 256, 1024, 256, P256, ws, NUL) == capi.ERR_SHAPE
+    assert f(*ptrs, 1 << 31, 256, 1024, 256, P256, ws, NUL) == capi.ERR_UNSUPPORTED
+    assert f(*ptrs, 1000, 200, 1024, 256, P256, ws, NUL) == capi.ERR_UNSUPPORTED
+    assert f(*ptrs, 1000, 256, 1024, 0, P256, ws, NUL) == capi.ERR_SHAPE
+    assert f(*([NUL] * 6), 1000, 256, 1024, 256, P256, ws, NUL) == capi.ERR_NULL
+    for i in range(6):
+        args = list(ptrs)
+        args[i] = P8
+        assert f(*args, 1000, 256, 1024, 256, P256, ws, NUL) == capi.ERR_UNSUPPORTED
+    assert f(*ptrs, 1000, 256, 1024, 256, NUL, ws, NUL) == capi.ERR_WORKSPACE
+    assert f(*ptrs, 1000, 256, 1024, 256, P256, ws - 1, NUL) == capi.ERR_WORKSPACE
+    assert f(*ptrs, 1000, 256, 1024, 256, ctypes.c_void_p(256 + 16), ws, NUL) == capi.ERR_WORKSPACE
+
+
+def test_empty_input_is_a_no_op(lib):
+    assert lib.ring_attn_ffn_fwd(*([NUL] * 6), 0, 256, 1024, 256, NUL, 0, NUL) == capi.OK

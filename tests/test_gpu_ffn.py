@@ -1,0 +1,128 @@
+"""Blockwise feed-forward (BPT) on the GB300 through the C ABI, against the
+fp64 oracle.
+
+The GPU computes y = x + gelu(x W1^T + b1) W2^T + b2 with bf16 operands, fp32
+accumulation and the hidden activation rounded to bf16 between the layers
+(it is the second GEMM's operand); the oracle computes the same block in
+fp64 from the same bf16 values.  Tolerance, per element of y, from that
+arithmetic:
+  * output rounding: half a bf16 ulp of y (at most 2^-8 |y|);
+  * the hidden rounding carried through W2: each h_f moves by at most half
+    a bf16 ulp (2^-8 |h_f|), roughly uniformly, so the error of y_d has
+    standard deviation at most 2^-8 / sqrt(3) * sqrt(sum_f (h_f W2_fd)^2);
+    six of those are allowed;
+  * fp32 accumulation and erff: 1e-4 absolute (several orders below the
+    terms above at these sizes).
+On top, the errors must be typical, not bunched near their bounds: the
+mean-abs error stays within a quarter of the mean bound (a faithful
+computation lands near one sixth of it: one standard deviation plus a
+quarter ulp of output rounding on average).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sequence_blockwise_self_gb300 as ra
+from sequence_blockwise_self_gb300 import build as lib_build
+from sequence_blockwise_self_gb300 import inputs
+from tolerance import bf16_half_ulp
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    lib_build.build()
+    ra.load()
+
+
+def f64(t):
+    return t.detach().float().cpu().double().numpy()
+
+
+def reference(x, w1, b1, w2, b2, rows=None):
+    """Oracle y (and the bound on |y_gpu - y|) for the given rows of x."""
+    W1, W2 = f64(w1).T.copy(), f64(w2).T.copy()   # oracle layout: W1 [D][F], W2 [F][D]
+    xs = f64(x if rows is None else x[torch.as_tensor(rows)])
+    y, h = oracle.ffn(xs, W1, f64(b1), W2, f64(b2), hidden=True)
+    sigma = 2.0 ** -8 / math.sqrt(3.0) * np.sqrt((h * h) @ (W2 * W2))
+    return y, bf16_half_ulp(y) + 6.0 * sigma + 1e-4
+
+
+def check(got, want, bound):
+    got = np.asarray(got, dtype=np.float64)
+    assert np.all(np.isfinite(got))
+    err = np.abs(got - want)
+    worst = np.unravel_index(np.argmax(err - bound), err.shape)
+    assert np.all(err <= bound), (f"error {err[worst]:.3e} above its bound {bound[worst]:.3e} at {worst}; "
+                                  f"max-abs {err.max():.3e}")
+    assert err.mean() <= 0.25 * bound.mean(), f"mean-abs {err.mean():.3e}, mean bound {bound.mean():.3e}"
+
+
+# (M, D, F, block_rows): ragged row counts, several blocks, several column
+# tiles of both GEMMs, block_rows larger than M
+CASES = [
+    (128, 256, 1024, 128),
+    (300, 256, 1024, 128),
+    (1000, 512, 2048, 384),
+    (77, 768, 512, 256),
+    (640, 256, 2816, 640),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "M{}D{}F{}R{}".format(*c))
+def test_ffn_matches_the_oracle(case):
+    M, D, F, R = case
+    x, w1, b1, w2, b2 = inputs.make_ffn_inputs(M, D, F, seed=40 + M + D)
+    y = ra.ring_attn_ffn_fwd(*(t.cuda() for t in (x, w1, b1, w2, b2)), block_rows=R)
+    torch.cuda.synchronize()
+    assert ra.device_status()[0] == 0
+    want, bound = reference(x, w1, b1, w2, b2)
+    check(f64(y), want, bound)
+
+
+def test_ffn_block_size_does_not_change_the_result():
+    """Rows are independent and each output tile sums K in the same order
+    whatever the block, so every block size gives the same bits."""
+    M, D, F = 1000, 512, 1536
+    dev = [t.cuda() for t in inputs.make_ffn_inputs(M, D, F, seed=7)]
+    ys = [ra.ring_attn_ffn_fwd(*dev, block_rows=R) for R in (128, 256, 384, 1024, 4096)]
+    for y in ys[1:]:
+        assert torch.equal(y, ys[0])
+
+
+def test_ffn_in_place():
+    M, D, F = 700, 256, 1024
+    x, w1, b1, w2, b2 = inputs.make_ffn_inputs(M, D, F, seed=8)
+    dev = [t.cuda() for t in (x, w1, b1, w2, b2)]
+    y = ra.ring_attn_ffn_fwd(*dev, block_rows=256)
+    xin = dev[0].clone()
+    out = ra.ring_attn_ffn_fwd(xin, *dev[1:], block_rows=256, y=xin)
+    assert out.data_ptr() == xin.data_ptr()
+    assert torch.equal(xin, y)
+
+
+def test_ffn_zero_second_layer_is_residual_plus_bias():
+    """W2 = 0: y = bf16(x + b2) exactly (one rounding of an exact sum)."""
+    M, D, F = 260, 256, 512
+    x, w1, b1, w2, b2 = inputs.make_ffn_inputs(M, D, F, seed=9)
+    y = ra.ring_attn_ffn_fwd(x.cuda(), w1.cuda(), b1.cuda(), torch.zeros_like(w2).cuda(), b2.cuda(), block_rows=128)
+    want = (x.double() + b2.double()).float().to(torch.bfloat16)
+    assert torch.equal(y.cpu(), want)
+
+
+def test_ffn_full_size_sampled_rows():
+    """The benchmark's workload (M = 131072 rows, D = 3584, F = 14336, blocks
+    of 8192 rows) in the launch configuration the benchmark times; rows at
+    block and tile edges plus random rows against the oracle."""
+    w = inputs.FFN_WORKLOADS["ffn_gqa_128k"]
+    x, w1, b1, w2, b2 = inputs.make_ffn_inputs(w.M, w.D, w.F, inputs.FFN_SEEDS[w.name])
+    y = ra.ring_attn_ffn_fwd(*(t.cuda() for t in (x, w1, b1, w2, b2)), block_rows=w.block_rows)
+    torch.cuda.synchronize()
+    assert ra.device_status()[0] == 0
+    rows = inputs.ffn_sample_rows(w.M, w.block_rows, 96, seed=1)
+    want, bound = reference(x, w1, b1, w2, b2, rows=rows)
+    check(f64(y[torch.as_tensor(rows).cuda()]), want, bound)
