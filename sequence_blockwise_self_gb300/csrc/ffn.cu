@@ -11,19 +11,26 @@
 // saving), in a caller-provided buffer reused block after block.
 //
 // Both layers are one persistent GEMM kernel C = A B^T with A [M][K] and
-// B [N][K] bf16 (K-major: the weights are passed transposed), fp32
+// B [N][K] bf16 (K-major: the weights are passed output-major), fp32
 // accumulation in tensor memory and a fused epilogue:
 //   kind 0:  C = bf16(gelu(acc + bias[n]))
 //   kind 1:  C = bf16(acc + bias[n] + resid[m][n])
-// Tiles of 128 x 256 (one tcgen05.mma 128x256x16 per 16 of K, 128 cycles),
-// K in stages of 64 through a 4-slot TMA ring.  Warp roles (256 threads):
-//   warp 0      TMA producer (A and B tiles)
-//   warp 1      tcgen05 issuer (converged warp, one elected lane)
-//   warp 2      tensor-memory allocator
+// It runs on CTA pairs (clusters of two CTAs on the two SMs of a TPC,
+// tcgen05 cta_group::2): 256 x 256 output tiles, each CTA staging its 128
+// rows of A and 128 of the 256 rows of B^T per 64-deep K stage, the even
+// CTA issuing the 256x256x16 products.  Per SM a stage then moves 32 KB
+// through shared memory for 128x256x64 of product; a single CTA computing
+// 128 x 256 would move 48 KB, and the TMA writes plus tensor-core reads of
+// that traffic are what bounds a single-CTA tile below the tensor peak.
+// Warp roles (256 threads per CTA):
+//   warp 0      TMA producer (A and B halves), both CTAs
+//   warp 1      tcgen05 issuer (converged warp, one elected lane), even CTA
+//   warp 2      tensor-memory allocator (collective over the pair)
 //   warps 4-7   epilogue: thread = output row (TMEM lane), 256 columns
 // Two accumulators of 256 columns alternate between tiles, so the epilogue
 // of one tile overlaps the products of the next.  Every wait is bounded (the
-// attention kernels' scheme: abort flag, status word, drain).
+// attention kernels' scheme: abort flag, status word, drain); both CTAs of
+// a pair always meet at the cluster barriers around the work.
 #include <cmath>
 
 #include "ffn.h"
@@ -34,27 +41,13 @@ namespace ra {
 namespace {
 
 constexpr int kGemmThreads = 256;
-constexpr int kBM = 128, kBN = 256, kBK = 64, kStages = 4;
-constexpr int kATile = kBM * kBK * 2;  // 16 KB
-constexpr int kBTile = kBN * kBK * 2;  // 32 KB
-
-struct GemmSmem {
-  alignas(1024) uint8_t a[kStages][kATile];
-  alignas(1024) uint8_t b[kStages][kBTile];
-  alignas(1024) uint8_t c[2][kBM * 64 * 2];  // output staging: two boxes of 128 rows x 64 columns
-  alignas(8) uint64_t full[kStages];
-  alignas(8) uint64_t empty[kStages];
-  alignas(8) uint64_t acc_full[2];
-  alignas(8) uint64_t acc_empty[2];
-  alignas(8) uint64_t drain;
-  uint32_t tmem_base;
-  int abort_flag;
-};
+constexpr int kBM = 128, kBN = 256, kBK = 64;  // rows per CTA, columns per tile, K per stage
 
 struct GemmDev {
   int M, N, K;          // M rows in this launch (ragged tail allowed), N % 256 == 0, K % 64 == 0
   int a_row0, c_row0;   // first row of this launch in the A and C tensor maps
   int c_rows;           // rows of the C tensor (the residual's rows; rows past it are not read)
+  int c_end;            // rows [c_row0, c_end) of C belong to this launch: no other row is read or written
   int kind;             // 0: gelu(acc + bias), 1: acc + bias + resid
   int group_rows;       // tile order, see tile_coords
   const float* bias;    // [N]
@@ -65,11 +58,11 @@ struct GemmDev {
 // Tile order: groups of G row tiles, row tiles fastest inside a group, so
 // that the CTAs resident together share operand tiles in L2 and a group's
 // rows of A stay there while its columns go by.
-__device__ __forceinline__ void tile_coords(int tile, int n_m, int n_n, int G, int& m0, int& n0) {
+__device__ __forceinline__ void tile_coords(int tile, int n_m, int n_n, int G, int tile_m, int& m0, int& n0) {
   const int per_group = G * n_n;
   const int g = tile / per_group, w = tile % per_group;
   const int rows = min(G, n_m - g * G);
-  m0 = (g * G + w % rows) * kBM;
+  m0 = (g * G + w % rows) * tile_m;
   n0 = (w / rows) * kBN;
 }
 
@@ -93,30 +86,229 @@ __device__ __forceinline__ void gemm_drain_wait(uint32_t bar, uint32_t parity, i
 
 __device__ __forceinline__ float gelu(float x) { return 0.5f * x * (1.f + erff(x * 0.70710678118654752f)); }
 
-__global__ void __launch_bounds__(kGemmThreads, 1)
-    ffn_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                    const __grid_constant__ CUtensorMap tm_c, const GemmDev p) {
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  if (smem_u32(smem_raw) & 1023u) {
-    if (threadIdx.x == 0) atomicCAS(p.err, 0, kSiteGemmMisaligned);
-    return;
+// The epilogue of one output tile for the 128 rows this CTA holds (thread =
+// row = tensor-memory lane): accumulator columns [t_acc, t_acc + 256) ->
+// + bias, then GELU (kind 0) or + residual (kind 1) -> bf16 into two
+// 64-column staging boxes in turn -> TMA stores of 128 x 64.  c_row0 is the
+// C row of lane 0; boxes_in_use says whether stores of an earlier tile may
+// still be reading the boxes.  release() runs once every accumulator column
+// has been read.  Called by the 128 epilogue threads (named barrier 1).
+template <class Release>
+__device__ __forceinline__ void epilogue_tile(const GemmDev& p, const CUtensorMap* tm_c, uint32_t box0, uint32_t box1,
+                                              uint32_t t_acc, int row, int c_row0, int n0, bool boxes_in_use,
+                                              Release release) {
+  const int c_row = c_row0 + row;  // this thread's output row
+  const bool has_res = p.kind == 1 && c_row < p.c_end;
+  // a box starts on a 128-row boundary of the launch, whose rows end on one
+  // or at the end of C: it lies inside the launch's rows, or all past them
+  const bool store = c_row0 < p.c_end;
+  const __nv_bfloat16* res_row = has_res ? p.resid + static_cast<size_t>(c_row) * p.N + n0 : nullptr;
+  for (int qtr = 0; qtr < 4; ++qtr) {
+    const uint32_t box = (qtr & 1) ? box1 : box0;
+    if (boxes_in_use || qtr >= 2) {  // the store that used this box two quarters ago has read it
+      if (threadIdx.x == 128) bulk_wait_group_read<1>();
+      named_bar_sync(1, 128);
+    }
+#pragma unroll
+    for (int h32 = 0; h32 < 2; ++h32) {
+      uint32_t r[32];
+      const int col0 = qtr * 64 + h32 * 32;  // within the tile
+      tmem_ld32(t_acc + col0, r);
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) + __ldg(p.bias + n0 + col0 + i);
+      if (p.kind == 0) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = gelu(v[i]);
+      } else if (has_res) {
+#pragma unroll
+        for (int c8 = 0; c8 < 4; ++c8) {
+          const uint4 rv = *reinterpret_cast<const uint4*>(res_row + col0 + 8 * c8);
+          const __nv_bfloat162* r2 = reinterpret_cast<const __nv_bfloat162*>(&rv);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 f = __bfloat1622float2(r2[j]);
+            v[8 * c8 + 2 * j] += f.x;
+            v[8 * c8 + 2 * j + 1] += f.y;
+          }
+        }
+      }
+#pragma unroll
+      for (int c8 = 0; c8 < 4; ++c8)
+        st_shared_v4(box + sw128_offset(row, h32 * 4 + c8), pack_bf16(v[8 * c8], v[8 * c8 + 1]),
+                     pack_bf16(v[8 * c8 + 2], v[8 * c8 + 3]), pack_bf16(v[8 * c8 + 4], v[8 * c8 + 5]),
+                     pack_bf16(v[8 * c8 + 6], v[8 * c8 + 7]));
+    }
+    if (qtr == 3) release();  // every column of this accumulator has been read
+    fence_proxy_async_smem();
+    named_bar_sync(1, 128);
+    if (threadIdx.x == 128 && store) {
+      tma_store_3d(tm_c, box, n0 + qtr * 64, c_row0, 0);
+      bulk_commit_group();
+    }
   }
-  GemmSmem& sm = *reinterpret_cast<GemmSmem*>(smem_raw);
+}
+
+// ------------------------------------------------ CTA pairs (cta_group::2)
+// A cluster of two CTAs on the two SMs of a TPC computes one 256-row tile:
+// each CTA stages its own 128 rows of A and half of the tile's columns of
+// B, the even CTA issues tcgen05.mma.cta_group::2 (M = 256), and each CTA's
+// tensor memory receives its 128 rows of the product.
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of both CTAs arrives, then waits for all of them.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// shared::cluster address of the variable at shared::cta address `addr` in
+// the CTA of cluster rank `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait (as mbar_wait) with cluster-scope acquire, for phases that
+// arrivals from the peer CTA complete.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err,
+                                                  int site) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+        *abort_flag = 1;
+        if (err) atomicCAS(err, 0, site);
+        return false;
+      }
+    }
+  }
+}
+
+// Tiled 3-D TMA load into this CTA's shared memory whose completion is
+// signalled on an mbarrier of either CTA of the pair (cluster address).
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster, int x,
+                                                 int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar_cluster)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_pair_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive once on the mbarrier at shared offset `bar` in every CTA of
+// `cta_mask` when the pair MMAs issued so far have completed.
+__device__ __forceinline__ void umma_commit_pair_mc_warp(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}" ::
+          "r"(bar), "h"(cta_mask)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+constexpr int kPairStages = 6;
+constexpr int kPairBRows = kBN / 2;               // rows of B^T each CTA stages
+constexpr int kPairATile = kBM * kBK * 2;         // 16 KB
+constexpr int kPairBTile = kPairBRows * kBK * 2;  // 16 KB
+
+struct PairSmem {
+  alignas(1024) uint8_t a[kPairStages][kPairATile];
+  alignas(1024) uint8_t b[kPairStages][kPairBTile];
+  alignas(1024) uint8_t c[2][kBM * 64 * 2];
+  alignas(8) uint64_t full[kPairStages];   // even CTA: both CTAs' operand bytes of a stage
+  alignas(8) uint64_t empty[kPairStages];  // each CTA: its stage may be refilled
+  alignas(8) uint64_t acc_full[2];         // each CTA: accumulator ready
+  alignas(8) uint64_t acc_empty[2];        // even CTA: both CTAs' epilogues have read the accumulator
+  alignas(8) uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// The same GEMM on CTA pairs: 256 x 256 output tiles, one per cluster of
+// two CTAs at a time (persistent over tiles), K in stages of 64 through a
+// 6-slot ring in each CTA.  Per stage each CTA loads its 128 rows of A and
+// its 128 rows of B^T (16 KB each); both loads complete on the even CTA's
+// `full` barrier, which expects the 64 KB of the pair.  The even CTA's MMA
+// warp issues the four 256x256x16 products of a stage and commits to the
+// `empty` barriers of both CTAs (multicast); after a tile it commits to
+// both `acc_full` barriers.  Each CTA's epilogue reads its own 128 rows and
+// signals the even CTA's `acc_empty` (one arrival per warp, 8 in all).
+// Per SM a stage moves 32 KB through shared memory for 128x256x64 of
+// product, against 48 KB for the single-CTA 128x256 tile.
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
+    ffn_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                         const __grid_constant__ CUtensorMap tm_c, const GemmDev p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // the same for both CTAs (same kernel, same layout): skipping the work
+  // keeps the collective steps (allocation, cluster barriers) on both sides
+  const bool misaligned = (smem_u32(smem_raw) & 1023u) != 0;
+  PairSmem& sm = *reinterpret_cast<PairSmem*>(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_m = (p.M + kBM - 1) / kBM, n_n = p.N / kBN, n_tiles = n_m * n_n, n_k = p.K / kBK;
-  // this CTA's tiles: blockIdx.x, blockIdx.x + gridDim.x, ...
-  const int my_tiles = blockIdx.x < n_tiles ? (n_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs
+  const uint32_t leader = rank & ~1u;
+  const int pair = static_cast<int>(blockIdx.x >> 1), n_pairs = static_cast<int>(gridDim.x >> 1);
+  const int tile_m = 2 * kBM;
+  const int n_m = (p.M + tile_m - 1) / tile_m, n_n = p.N / kBN, n_tiles = n_m * n_n, n_k = p.K / kBK;
+  const int my_tiles = misaligned ? 0 : (pair < n_tiles ? (n_tiles - 1 - pair) / n_pairs + 1 : 0);
   volatile int* ab = &sm.abort_flag;
 
   if (threadIdx.x == 0) {
+    if (misaligned) atomicCAS(p.err, 0, kSiteGemmMisaligned);
     sm.abort_flag = 0;
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kPairStages; ++s) {
       mbar_init(smem_u32(&sm.full[s]), 1);
       mbar_init(smem_u32(&sm.empty[s]), 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&sm.acc_full[a]), 1);
-      mbar_init(smem_u32(&sm.acc_empty[a]), 128);
+      mbar_init(smem_u32(&sm.acc_empty[a]), 8);
     }
     mbar_init(smem_u32(&sm.drain), 1);
     fence_mbar_init();
@@ -124,12 +316,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tma_prefetch_desc(&tm_b);
     tma_prefetch_desc(&tm_c);
   }
-  if (warp == 2) {
-    tmem_alloc(smem_u32(&sm.tmem_base), 512);
-    tmem_relinquish();
+  if (warp == 2) {  // one warp in each CTA of the pair, collectively
+    tmem_alloc_pair(smem_u32(&sm.tmem_base), 512);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();  // barriers initialised and tensor memory allocated on both sides
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   const uint32_t total_uses = static_cast<uint32_t>(my_tiles) * n_k;
@@ -138,151 +330,134 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (lane == 0) {
       bool ok = true;
       uint32_t n = 0;
+      const uint32_t full0 = mapa_shared(smem_u32(&sm.full[0]), leader);
       for (int t = 0; t < my_tiles && ok; ++t) {
         int m0, n0;
-        tile_coords(blockIdx.x + t * gridDim.x, n_m, n_n, p.group_rows, m0, n0);
+        tile_coords(pair + t * n_pairs, n_m, n_n, p.group_rows, tile_m, m0, n0);
         for (int ks = 0; ks < n_k && ok; ++ks, ++n) {
-          const uint32_t s = n % kStages, use = n / kStages;
-          if (use > 0) ok = mbar_wait(smem_u32(&sm.empty[s]), (use - 1) & 1, ab, p.err, kSiteGemmProducer);
+          const uint32_t s = n % kPairStages, use = n / kPairStages;
+          if (use > 0)
+            ok = mbar_wait_cluster(smem_u32(&sm.empty[s]), (use - 1) & 1, ab, p.err, kSiteGemmProducer);
           if (!ok) break;
-          const uint32_t fb = smem_u32(&sm.full[s]);
-          mbar_arrive_expect_tx(fb, kATile + kBTile);
-          tma_load_3d(smem_u32(sm.a[s]), &tm_a, fb, ks * kBK, p.a_row0 + m0, 0);
-          tma_load_3d(smem_u32(sm.b[s]), &tm_b, fb, ks * kBK, n0, 0);
+          if (rank == leader) mbar_arrive_expect_tx(smem_u32(&sm.full[s]), 2 * (kPairATile + kPairBTile));
+          const uint32_t fb = full0 + 8u * s;
+          tma_load_3d_pair(smem_u32(sm.a[s]), &tm_a, fb, ks * kBK, p.a_row0 + m0 + kBM * static_cast<int>(rank - leader),
+                           0);
+          tma_load_3d_pair(smem_u32(sm.b[s]), &tm_b, fb, ks * kBK, n0 + kPairBRows * static_cast<int>(rank - leader),
+                           0);
         }
       }
-      if (!ok) {  // let the copies in flight land before the CTA exits
-        for (uint32_t i = 0; i < kStages && i < n; ++i) {
-          const uint32_t last = i + kStages * ((n - 1 - i) / kStages);
-          gemm_drain_wait(smem_u32(&sm.full[i]), (last / kStages) & 1, p.err);
+      if (!ok && rank == leader) {  // let the copies in flight land before the pair exits
+        for (uint32_t i = 0; i < kPairStages && i < n; ++i) {
+          const uint32_t last = i + kPairStages * ((n - 1 - i) / kPairStages);
+          gemm_drain_wait(smem_u32(&sm.full[i]), (last / kPairStages) & 1, p.err);
         }
       }
     }
   } else if (warp == 1) {
-    constexpr uint32_t kId = idesc_bf16(kBM, kBN, false, false);
-    bool ok = true;
-    uint32_t n = 0;
-    for (int t = 0; t < my_tiles && ok; ++t) {
-      const uint32_t acc = t & 1;
-      if (t >= 2)
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.acc_empty[acc]), ((t >> 1) - 1) & 1, ab, p.err,
-                                               kSiteGemmMma));
-      if (!ok) break;
-      tc_fence_after();
-      for (int ks = 0; ks < n_k && ok; ++ks, ++n) {
-        const uint32_t s = n % kStages;
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.full[s]), (n / kStages) & 1, ab, p.err, kSiteGemmMma));
+    if (rank == leader) {
+      constexpr uint32_t kId = idesc_bf16(2 * kBM, kBN, false, false);
+      const uint16_t both = static_cast<uint16_t>(3u << leader);
+      bool ok = true;
+      uint32_t n = 0;
+      for (int t = 0; t < my_tiles && ok; ++t) {
+        const uint32_t acc = t & 1;
+        if (t >= 2)
+          ok = __all_sync(0xffffffffu, mbar_wait_cluster(smem_u32(&sm.acc_empty[acc]), ((t >> 1) - 1) & 1, ab,
+                                                         p.err, kSiteGemmMma));
         if (!ok) break;
         tc_fence_after();
-        const uint32_t aa = smem_u32(sm.a[s]), ba = smem_u32(sm.b[s]);
+        for (int ks = 0; ks < n_k && ok; ++ks, ++n) {
+          const uint32_t s = n % kPairStages;
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait_cluster(smem_u32(&sm.full[s]), (n / kPairStages) & 1, ab, p.err, kSiteGemmMma));
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t aa = smem_u32(sm.a[s]), ba = smem_u32(sm.b[s]);
 #pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk)
-          umma_ss_warp(tmem + acc * kBN, sdesc_sw128(aa + kk * 32, 16, 1024), sdesc_sw128(ba + kk * 32, 16, 1024), kId,
-                       (ks > 0 || kk > 0) ? 1u : 0u);
-        // the slot goes back to the producer once these products have read
-        // it, if the producer will refill it
-        if (n + kStages < total_uses) umma_commit_warp(smem_u32(&sm.empty[s]));
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            umma_pair_warp(tmem + acc * kBN, sdesc_sw128(aa + kk * 32, 16, 1024), sdesc_sw128(ba + kk * 32, 16, 1024),
+                           kId, (ks > 0 || kk > 0) ? 1u : 0u);
+          if (n + kPairStages < total_uses) umma_commit_pair_mc_warp(smem_u32(&sm.empty[s]), both);
+        }
+        if (ok) umma_commit_pair_mc_warp(smem_u32(&sm.acc_full[acc]), both);
       }
-      if (ok) umma_commit_warp(smem_u32(&sm.acc_full[acc]));
-    }
-    if (!ok) {
-      umma_commit_warp(smem_u32(&sm.drain));
-      gemm_drain_wait(smem_u32(&sm.drain), 0, p.err);
+      if (!ok) {
+        umma_commit_pair_mc_warp(smem_u32(&sm.drain), static_cast<uint16_t>(1u << leader));
+        gemm_drain_wait(smem_u32(&sm.drain), 0, p.err);
+      }
     }
   } else if (warp >= 4) {
-    const int wq = warp & 3;
-    const int row = wq * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const int row = (warp & 3) * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t acc_empty0 = mapa_shared(smem_u32(&sm.acc_empty[0]), leader);
     bool ok = true;
     for (int t = 0; t < my_tiles && ok; ++t) {
       int m0, n0;
-      tile_coords(blockIdx.x + t * gridDim.x, n_m, n_n, p.group_rows, m0, n0);
+      tile_coords(pair + t * n_pairs, n_m, n_n, p.group_rows, tile_m, m0, n0);
       const uint32_t acc = t & 1;
-      // one decision for the four warps: they meet at named barriers below
-      ok = named_bar_and(1, 128, mbar_wait(smem_u32(&sm.acc_full[acc]), (t >> 1) & 1, ab, p.err, kSiteGemmEpilogue));
+      ok = named_bar_and(1, 128, mbar_wait_cluster(smem_u32(&sm.acc_full[acc]), (t >> 1) & 1, ab, p.err,
+                                                   kSiteGemmEpilogue));
       if (!ok) break;
       tc_fence_after();
-      const uint32_t t_acc = tmem + acc * kBN + lane_off;
-      const int c_row = p.c_row0 + m0 + row;  // this thread's output row
-      const bool has_res = p.kind == 1 && c_row < p.c_rows;
-      const __nv_bfloat16* res_row = has_res ? p.resid + static_cast<size_t>(c_row) * p.N + n0 : nullptr;
-      // four quarters of 64 columns, two staging boxes in turn
-      for (int qtr = 0; qtr < 4; ++qtr) {
-        const uint32_t box = smem_u32(sm.c[qtr & 1]);
-        if (t > 0 || qtr >= 2) {  // the store that used this box two quarters ago has read it
-          if (threadIdx.x == 128) bulk_wait_group_read<1>();
-          named_bar_sync(1, 128);
-        }
-#pragma unroll
-        for (int h32 = 0; h32 < 2; ++h32) {
-          uint32_t r[32];
-          const int col0 = qtr * 64 + h32 * 32;  // within the tile
-          tmem_ld32(t_acc + col0, r);
-          float v[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) + __ldg(p.bias + n0 + col0 + i);
-          if (p.kind == 0) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = gelu(v[i]);
-          } else if (has_res) {
-#pragma unroll
-            for (int c8 = 0; c8 < 4; ++c8) {
-              const uint4 rv = *reinterpret_cast<const uint4*>(res_row + col0 + 8 * c8);
-              const __nv_bfloat162* r2 = reinterpret_cast<const __nv_bfloat162*>(&rv);
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const float2 f = __bfloat1622float2(r2[j]);
-                v[8 * c8 + 2 * j] += f.x;
-                v[8 * c8 + 2 * j + 1] += f.y;
-              }
-            }
-          }
-#pragma unroll
-          for (int c8 = 0; c8 < 4; ++c8)
-            st_shared_v4(box + sw128_offset(row, h32 * 4 + c8), pack_bf16(v[8 * c8], v[8 * c8 + 1]),
-                         pack_bf16(v[8 * c8 + 2], v[8 * c8 + 3]), pack_bf16(v[8 * c8 + 4], v[8 * c8 + 5]),
-                         pack_bf16(v[8 * c8 + 6], v[8 * c8 + 7]));
-        }
-        if (qtr == 3) {  // every column of this accumulator has been read
-          tc_fence_before();
-          mbar_arrive(smem_u32(&sm.acc_empty[acc]));
-        }
-        fence_proxy_async_smem();
-        named_bar_sync(1, 128);
-        if (threadIdx.x == 128) {
-          tma_store_3d(&tm_c, box, n0 + qtr * 64, p.c_row0 + m0, 0);
-          bulk_commit_group();
-        }
-      }
+      epilogue_tile(p, &tm_c, smem_u32(sm.c[0]), smem_u32(sm.c[1]), tmem + acc * kBN + lane_off, row,
+                    p.c_row0 + m0 + kBM * static_cast<int>(rank - leader), n0, t > 0, [&] {
+                      tc_fence_before();
+                      __syncwarp();
+                      if (lane == 0) mbar_arrive_cluster(acc_empty0 + 8u * acc);
+                    });
     }
     if (threadIdx.x == 128) bulk_wait_group<0>();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();  // no more products, arrivals or reads of the peer's memory
   tc_fence_after();
-  if (warp == 2) tmem_dealloc(tmem, 512);
+  if (warp == 2) tmem_dealloc_pair(tmem, 512);
 }
 
 }  // namespace
 
-size_t ffn_gemm_smem_bytes() { return sizeof(GemmSmem); }
+size_t ffn_gemm_smem_bytes() { return sizeof(PairSmem); }
+
+int ffn_pair_max_clusters() {
+  const size_t smem = sizeof(PairSmem);
+  if (cudaFuncSetAttribute(ffn_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = 2;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, ffn_gemm_pair_kernel, &cfg) != cudaSuccess) return 0;
+  return n;
+}
 
 cudaError_t launch_ffn_gemm(const FfnGemmArgs& a, cudaStream_t stream) {
   GemmDev p;
   p.M = a.M; p.N = a.N; p.K = a.K;
   p.a_row0 = a.a_row0; p.c_row0 = a.c_row0; p.c_rows = a.c_rows;
+  p.c_end = a.c_row0 + a.M < a.c_rows ? a.c_row0 + a.M : a.c_rows;
   p.kind = a.kind; p.bias = a.bias;
   p.group_rows = a.group_rows > 0 ? a.group_rows : 1;
   p.resid = static_cast<const __nv_bfloat16*>(a.resid);
   p.err = a.err;
-  const int n_sms = a.n_sms;
-  const int n_tiles = ((a.M + kBM - 1) / kBM) * (a.N / kBN);
-  const int grid = n_tiles < n_sms ? n_tiles : n_sms;
-  const size_t smem = sizeof(GemmSmem);
-  cudaError_t e = cudaFuncSetAttribute(ffn_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (a.pair_clusters <= 0) return cudaErrorInvalidConfiguration;
+  const int n_tiles = ((a.M + 2 * kBM - 1) / (2 * kBM)) * (a.N / kBN);
+  const int clusters = n_tiles < a.pair_clusters ? n_tiles : a.pair_clusters;
+  const size_t smem = sizeof(PairSmem);
+  const cudaError_t e =
+      cudaFuncSetAttribute(ffn_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   if (a.timer) a.timer->mark(kProfFfnGemm, false, stream);
-  ffn_gemm_kernel<<<grid, kGemmThreads, smem, stream>>>(a.tm_a, a.tm_b, a.tm_c, p);
+  ffn_gemm_pair_kernel<<<2 * clusters, kGemmThreads, smem, stream>>>(a.tm_a, a.tm_b, a.tm_c, p);
   if (a.timer) a.timer->mark(kProfFfnGemm, true, stream);
   return cudaGetLastError();
 }

@@ -17,12 +17,13 @@ enum FfnErrSite : int {
 constexpr int kProfFfnGemm = 8;
 
 // C = epilogue(A B^T) with A [rows][K] and B [N][K] bf16, K-major, through
-// 128B-swizzled tensor maps (A and C boxes 64 x 128, B boxes 64 x 256); C
-// bf16 [c_rows][N].
+// 128B-swizzled tensor maps (boxes of 64 x 128 for A, B and C), on CTA
+// pairs; C bf16 [c_rows][N].
 //   kind 0: C = gelu(acc + bias)         kind 1: C = acc + bias + resid
 // M rows of C starting at c_row0 are produced from M rows of A starting at
-// a_row0; N % 256 == 0, K % 64 == 0; rows past c_rows are neither read
-// (resid) nor written (the store clips them).
+// a_row0; N % 256 == 0, K % 64 == 0; M is a multiple of 128 unless the rows
+// end at c_rows.  Only rows [c_row0, min(c_row0 + M, c_rows)) of C and of
+// the residual are touched.
 struct FfnGemmArgs {
   CUtensorMap tm_a, tm_b, tm_c;
   int M = 0, N = 0, K = 0, a_row0 = 0, c_row0 = 0, c_rows = 0, kind = 0;
@@ -31,10 +32,14 @@ struct FfnGemmArgs {
   const void* resid = nullptr;
   int* err = nullptr;
   int n_sms = 0;
+  int pair_clusters = 0;  // clusters of two CTAs resident at once (ffn_pair_max_clusters())
   LaunchTimer* timer = nullptr;
 };
 
 cudaError_t launch_ffn_gemm(const FfnGemmArgs& a, cudaStream_t stream);
 size_t ffn_gemm_smem_bytes();
+// Clusters of two CTAs of the pair kernel that fit on the device at once (0
+// if none or the query fails).
+int ffn_pair_max_clusters();
 
 }  // namespace ra

@@ -35,6 +35,7 @@ std::map<std::tuple<int, int, int, int, int>, DevicePlan> g_plans;  // (device, 
 // ring step plans: (device, L, N, causal, striped, step, first rank, end rank;
 // end rank -1 = the backward plan of the step)
 std::map<std::tuple<int, int, int, int, int, int, int, int>, DevicePlan> g_step_plans;
+std::map<int, int> g_ffn_pair_clusters;                          // device -> clusters of 2 (0: none)
 std::map<int, int*> g_status_ptr;                                   // device -> &g_device_status
 
 // Event pairs around launches while profiling is on.
@@ -801,24 +802,31 @@ int ring_attn_ffn_fwd(const void* x, const void* w1, const float* b1, const void
   int* err;
   if ((rc = status_ptr(dev, &err)) != RING_ATTN_OK) return rc;
   const int rows = static_cast<int>(M);
+  // the GEMM runs on CTA pairs: clusters of two that fit at once
+  auto it = g_ffn_pair_clusters.find(dev);
+  if (it == g_ffn_pair_clusters.end()) it = g_ffn_pair_clusters.emplace(dev, ffn_pair_max_clusters()).first;
+  const int pair_clusters = it->second;
+  if (pair_clusters <= 0) return RING_ATTN_ERR_UNSUPPORTED;
+  const int tile_m = 256, b_box = 128;
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   // first layer: A = x [M][D], B = W1 [F][D], C = h [block_rows][F]
   // second layer: A = h, B = W2 [D][F], C = y [M][D], residual x
   FfnGemmArgs g1, g2;
-  if (!make_map(&g1.tm_a, x, bf, 2, D, rows, 1, 64) || !make_map(&g1.tm_b, w1, bf, 2, D, F, 1, 64, 256) ||
+  if (!make_map(&g1.tm_a, x, bf, 2, D, rows, 1, 64) || !make_map(&g1.tm_b, w1, bf, 2, D, F, 1, 64, b_box) ||
       !make_map(&g1.tm_c, workspace, bf, 2, F, block_rows, 1, 64) ||
       !make_map(&g2.tm_a, workspace, bf, 2, F, block_rows, 1, 64) ||
-      !make_map(&g2.tm_b, w2, bf, 2, F, D, 1, 64, 256) || !make_map(&g2.tm_c, y, bf, 2, D, rows, 1, 64))
+      !make_map(&g2.tm_b, w2, bf, 2, F, D, 1, 64, b_box) || !make_map(&g2.tm_c, y, bf, 2, D, rows, 1, 64))
     return RING_ATTN_ERR_CUDA;
   g1.N = F; g1.K = D; g1.c_rows = block_rows; g1.kind = 0; g1.bias = b1;
   g2.N = D; g2.K = F; g2.c_rows = rows; g2.kind = 1; g2.bias = b2; g2.resid = x;
   for (FfnGemmArgs* g : {&g1, &g2}) {
     g->err = err;
     g->n_sms = n_sms;
+    g->pair_clusters = pair_clusters;
     g->timer = active_timer();
     // tile order: groups of row tiles whose rows of A take about 16 MiB, so
     // that a group's A stays in L2 while its column tiles go by
-    const long long a_tile_bytes = 128ll * g->K * 2;
+    const long long a_tile_bytes = static_cast<long long>(tile_m) * g->K * 2;
     g->group_rows = static_cast<int>(std::max(1ll, (1ll << 24) / a_tile_bytes));
   }
   for (int r0 = 0; r0 < rows; r0 += block_rows) {

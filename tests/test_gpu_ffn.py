@@ -94,13 +94,17 @@ def test_ffn_block_size_does_not_change_the_result():
         assert torch.equal(y, ys[0])
 
 
-def test_ffn_in_place():
+@pytest.mark.parametrize("R", [128, 256, 384])
+def test_ffn_in_place(R):
+    """y = x: a block's output rows replace its input rows only after the
+    block has read them, and no launch touches rows of another block (with
+    256-row tile pairs, blocks of 128 or 384 rows end inside a tile)."""
     M, D, F = 700, 256, 1024
     x, w1, b1, w2, b2 = inputs.make_ffn_inputs(M, D, F, seed=8)
     dev = [t.cuda() for t in (x, w1, b1, w2, b2)]
-    y = ra.ring_attn_ffn_fwd(*dev, block_rows=256)
+    y = ra.ring_attn_ffn_fwd(*dev, block_rows=R)
     xin = dev[0].clone()
-    out = ra.ring_attn_ffn_fwd(xin, *dev[1:], block_rows=256, y=xin)
+    out = ra.ring_attn_ffn_fwd(xin, *dev[1:], block_rows=R, y=xin)
     assert out.data_ptr() == xin.data_ptr()
     assert torch.equal(xin, y)
 
