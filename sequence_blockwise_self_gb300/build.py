@@ -17,7 +17,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libring_attn.so")
 SOURCES = ["ring_attn_capi.cu", "attn_fwd.cu", "attn_bwd.cu", "plan.cpp", "ring_attn_noalloc.cu", "ring_step.cu",
            "ulysses.cu", "ffn.cu"]
-HEADERS = ["kernels.h", "plan.h", "sm103_ptx.cuh", "ffn.h"]
+HEADERS = ["kernels.h", "plan.h", "sm103_ptx.cuh", "sm103_pair.cuh", "ffn.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
