@@ -643,6 +643,39 @@ def run_ours(args, w):
                          "frac_of_sustained": tf_gemm / peaks["sustained"] if tf_gemm else None,
                          "flops_per_step": fw.flops()},
         }
+        # the blockwise transformer forward on this workload: per 8192-row
+        # query block, the block's attention (token-major output) and then
+        # the FFN with its residual on those rows (hidden size Hq * d)
+        if w.B * w.L == fw.M and w.Hq * w.d == fw.D:
+            a_tok = torch.empty((w.B, w.L, fw.D), dtype=torch.bfloat16, device=dev)
+            lse_b = torch.empty((w.B, w.Hq, w.L), dtype=torch.float32, device=dev)
+            y_b = torch.empty_like(a_tok)
+            ws_b = torch.empty(ra.bpt_workspace_size(w.Hq, w.d, fw.F, fw.block_rows), dtype=torch.uint8,
+                               device=dev)
+
+            def b_step():
+                ra.ring_attn_bpt_fwd(qd, kd, vd, w1f, b1f, w2f, b2f, w.n_chunks, w.causal,
+                                     block_rows=fw.block_rows, a_tok=a_tok, lse=lse_b, y=y_b, workspace=ws_b,
+                                     stream=stream)
+            b_step()
+            torch.cuda.synchronize(dev)
+            f0.record(stream)
+            for _ in range(args.steps):
+                b_step()
+            f1.record(stream)
+            torch.cuda.synchronize(dev)
+            ms_b = f0.elapsed_time(f1) / args.steps
+            st, site = ra.device_status()
+            if st != 0:
+                raise RuntimeError(f"device status {st} at site {site:#x} in the BPT forward")
+            fl_b = w.fwd_flops() + fw.flops()
+            ffn["bpt_forward"] = {
+                "what": "per query block of 8192 rows: attention (all heads, ring order), then the FFN and "
+                        "residual on its token rows",
+                "ms": ms_b, "tflops": fl_b / (ms_b * 1e-3) / 1e12, "flops_per_step": fl_b,
+                "launches_per_step": 3 * (w.L // fw.block_rows),
+            }
+            del a_tok, lse_b, y_b, ws_b
         del xf, w1f, w2f, b1f, b2f, yf, wsf
 
     if os.sched_getaffinity(0) != all_cpus:

@@ -277,6 +277,37 @@ int ring_attn_ffn_fwd(const void* x, const void* w1, const float* b1, const void
                       cudaStream_t stream);
 
 /* ---------------------------------------------------------------------
+ * Blockwise transformer forward (BPT; same page, section 4.2: the outer
+ * loop runs over query blocks, and for each block the attention over every
+ * key/value block, with the online-softmax correction, is followed by the
+ * feed-forward network and the residual connection of that block).  For
+ * each block of block_rows query rows, in order:
+ *   a = attention of those rows (all batches and heads; the ring order and
+ *       chunk map of ring_attn_fwd), written token-major
+ *   y = a + W2 gelu(W1 a + b1) + b2 on the block's token rows, a row being
+ *       the Hq * d outputs of one token (hidden size D = Hq * d)
+ * so only one block's FFN hidden activation exists at a time.
+ *   q, k, v  : as ring_attn_fwd
+ *   a_tok, y : bf16 [B][L][Hq * d] (token-major; a_tok keeps the attention
+ *              output, the FFN's residual input)
+ *   lse      : fp32 [B][Hq][L], as ring_attn_fwd
+ *   w1 [F][D], b1 [F], w2 [D][F], b2 [D]: as ring_attn_ffn_fwd
+ * Supported: ring_attn_fwd's domain, Hq * d % 256 == 0, F % 256 == 0,
+ * block_rows a positive multiple of 256, B * L below 2^31.
+ * ------------------------------------------------------------------- */
+
+/* Bytes of workspace ring_attn_bpt_fwd needs (one block's bf16 hidden
+ * activation), or 0 for an unsupported shape. */
+size_t ring_attn_bpt_workspace_size(int Hq, int d, int F, int block_rows);
+
+/* Per row block: one launch of the fused attention forward (that block's
+ * work items), then the two GEMM launches of the FFN per batch. */
+int ring_attn_bpt_fwd(const void* q, const void* k, const void* v, void* a_tok, float* lse, const void* w1,
+                      const float* b1, const void* w2, const float* b2, void* y, int B, int Hq, int Hkv, int L, int d,
+                      int n_chunks, int causal, int F, int block_rows, void* workspace, size_t workspace_bytes,
+                      cudaStream_t stream);
+
+/* ---------------------------------------------------------------------
  * Per-kernel timing, for measurement.  While enabled, every kernel launch
  * of the library is bracketed by two CUDA events recorded on the launch
  * stream.  ring_attn_profile_read() waits for those events and returns,

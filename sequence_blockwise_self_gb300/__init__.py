@@ -9,7 +9,8 @@ would): ring_attn_fwd_step, ring_attn_merge, ring_attn_ring_fwd,
 ring_attn_ring_bwd.
 Ulysses on one GPU (sequence shards -> head shards -> back):
 ring_attn_ulysses_fwd, ring_attn_ulysses_bwd.
-Blockwise feed-forward (BPT): ring_attn_ffn_fwd.
+Blockwise feed-forward (BPT): ring_attn_ffn_fwd; the blockwise transformer
+forward (attention, then FFN, per query block): ring_attn_bpt_fwd.
 Host-only queries: owner_rank, fwd_plan, bwd_plan, step_plan.
 """
 from .capi import (  # noqa: F401
@@ -30,6 +31,8 @@ from .capi import (  # noqa: F401
     ring_attn_fwd,
     ring_attn_ffn_fwd,
     ffn_workspace_size,
+    ring_attn_bpt_fwd,
+    bpt_workspace_size,
     ring_attn_fwd_step,
     ring_attn_merge,
     ring_attn_ring_fwd,

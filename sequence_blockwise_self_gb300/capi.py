@@ -95,6 +95,10 @@ def load():
     lib.ring_attn_ffn_workspace_size.restype = S
     lib.ring_attn_ffn_fwd.argtypes = [P, P, P, P, P, P, ctypes.c_longlong, I, I, I, P, S, P]
     lib.ring_attn_ffn_fwd.restype = I
+    lib.ring_attn_bpt_workspace_size.argtypes = [I, I, I, I]
+    lib.ring_attn_bpt_workspace_size.restype = S
+    lib.ring_attn_bpt_fwd.argtypes = [P] * 10 + [I] * 9 + [P, S, P]
+    lib.ring_attn_bpt_fwd.restype = I
     _lib = lib
     return lib
 
@@ -382,6 +386,46 @@ def ring_attn_ffn_fwd(x, w1, b1, w2, b2, block_rows: int = 8192, y=None, workspa
     if rc != OK:
         raise RingAttnError(rc, "ring_attn_ffn_fwd")
     return y
+
+
+def bpt_workspace_size(Hq: int, d: int, F: int, block_rows: int) -> int:
+    return int(load().ring_attn_bpt_workspace_size(int(Hq), int(d), int(F), int(block_rows)))
+
+
+def ring_attn_bpt_fwd(q, k, v, w1, b1, w2, b2, n_chunks: int, causal: bool, block_rows: int = 8192, a_tok=None,
+                      lse=None, y=None, workspace=None, stream=None):
+    """Blockwise transformer forward: per block of query rows, the block's
+    attention (written token-major, a_tok [B, L, Hq*d]) and then
+    y = a_tok + gelu(a_tok W1^T + b1) W2^T + b2 on its rows.  q [B,Hq,L,d],
+    k, v [B,Hkv,L,d] bf16; w1 [F, Hq*d], w2 [Hq*d, F] bf16; b1, b2 fp32.
+    Returns (a_tok, lse, y)."""
+    import torch
+    B, Hq, L, d = q.shape
+    Hkv = k.shape[1]
+    D, F = Hq * d, w1.shape[0]
+    _check_tensor(q, "q", torch.bfloat16, (B, Hq, L, d))
+    _check_tensor(k, "k", torch.bfloat16, (B, Hkv, L, d))
+    _check_tensor(v, "v", torch.bfloat16, (B, Hkv, L, d))
+    _check_tensor(w1, "w1", torch.bfloat16, (F, D))
+    _check_tensor(w2, "w2", torch.bfloat16, (D, F))
+    _check_tensor(b1, "b1", torch.float32, (F,))
+    _check_tensor(b2, "b2", torch.float32, (D,))
+    a_tok = torch.empty((B, L, D), dtype=torch.bfloat16, device=q.device) if a_tok is None else a_tok
+    lse = torch.empty((B, Hq, L), dtype=torch.float32, device=q.device) if lse is None else lse
+    y = torch.empty((B, L, D), dtype=torch.bfloat16, device=q.device) if y is None else y
+    _check_tensor(a_tok, "a_tok", torch.bfloat16, (B, L, D))
+    _check_tensor(lse, "lse", torch.float32, (B, Hq, L))
+    _check_tensor(y, "y", torch.bfloat16, (B, L, D))
+    if workspace is None:
+        workspace = torch.empty(max(bpt_workspace_size(Hq, d, F, block_rows), 1), dtype=torch.uint8,
+                                device=q.device)
+    rc = load().ring_attn_bpt_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(a_tok), _ptr(lse), _ptr(w1), _ptr(b1), _ptr(w2),
+                                  _ptr(b2), _ptr(y), B, Hq, Hkv, L, d, int(n_chunks), int(bool(causal)), F,
+                                  int(block_rows), _ptr(workspace), int(workspace.numel() * workspace.element_size()),
+                                  _stream(stream))
+    if rc != OK:
+        raise RingAttnError(rc, "ring_attn_bpt_fwd")
+    return a_tok, lse, y
 
 
 def bwd_workspace_size(B, Hq, Hkv, L, d, n_chunks, causal) -> int:

@@ -81,6 +81,9 @@ struct FwdDev {
   // normalised partial result in fp32 (o32 / the fp32 output map).
   int step_nb, step, rank_lo, n_chunks, sub_len, z_rank, striped;
   float* o32;
+  // o token-major, [B][L][Hq][d] (tm_o is then 4-D: d, Hq, L, B), for the
+  // blockwise transformer whose feed-forward takes token rows of Hq * d
+  int o_tok;
 };
 
 // Keys of the causal mask: key column i of a tile is visible to a query
@@ -101,6 +104,15 @@ __device__ __forceinline__ int kv_key(const FwdDev& p, int kv_rank, int q_rank, 
   if (!kStep || !p.causal) return kv0;
   if (p.striped) return kv0 + (kv_rank > q_rank ? 1 : 0);
   return q_key<kStep>(p, kv_rank, kv0);
+}
+
+// 4-D tiled TMA store (the token-major output map).
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, uint32_t src, int x, int y, int z, int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
 }
 
 // Wait that ignores the abort flag (used to drain in-flight copies/MMAs
@@ -404,8 +416,12 @@ __device__ void fwd_softmax(FwdSmem<D>& sm, uint32_t tmem, int t, const FwdDev& 
         tma_store_3d(tm_o, c0 < D / 64 ? smem_u32(sm.q[t]) + c0 * 16384 : pbase + (c0 - D / 64) * 16384, 32 * c0,
                      q0 + 128 * t, q_z);
     } else {
-      for (int sub = 0; sub < FwdSmem<D>::kSub; ++sub)
-        tma_store_3d(tm_o, pbase + sub * 16384, sub * 64, q0 + 128 * t, q_z);
+      for (int sub = 0; sub < FwdSmem<D>::kSub; ++sub) {
+        if (p.o_tok)  // box (64 columns, 1 head, 128 rows, 1 batch): clipped at this batch's L
+          tma_store_4d(tm_o, pbase + sub * 16384, sub * 64, q_z % p.Hq, q0 + 128 * t, q_z / p.Hq);
+        else
+          tma_store_3d(tm_o, pbase + sub * 16384, sub * 64, q0 + 128 * t, q_z);
+      }
     }
     bulk_commit_group();
     bulk_wait_group<0>();
@@ -536,6 +552,7 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
   p.lse = a.lse; p.err = a.err;
   p.step_nb = a.step_nb; p.step = a.step; p.rank_lo = a.rank_lo; p.n_chunks = a.n_chunks;
   p.sub_len = a.sub_len; p.z_rank = a.z_rank; p.striped = a.striped; p.o32 = a.o32;
+  p.o_tok = a.o_token_major;
   const size_t smem = fwd_smem_bytes(a.d);
   const dim3 grid(static_cast<unsigned>(a.n_blocks) * a.B * a.Hq);
   cudaError_t e;

@@ -5,6 +5,7 @@
 #include <algorithm>
 #include <cstring>
 #include <map>
+#include <numeric>
 #include <memory>
 #include <mutex>
 #include <tuple>
@@ -35,7 +36,9 @@ std::map<std::tuple<int, int, int, int, int>, DevicePlan> g_plans;  // (device, 
 // ring step plans: (device, L, N, causal, striped, step, first rank, end rank;
 // end rank -1 = the backward plan of the step)
 std::map<std::tuple<int, int, int, int, int, int, int, int>, DevicePlan> g_step_plans;
-std::map<int, int> g_ffn_pair_clusters;                          // device -> clusters of 2 (0: none)
+std::map<int, int> g_ffn_pair_clusters;
+// forward work items grouped by row block: (device, L, N, causal, block rows)
+std::map<std::tuple<int, int, int, int, int>, int32_t*> g_block_orders;                          // device -> clusters of 2 (0: none)
 std::map<int, int*> g_status_ptr;                                   // device -> &g_device_status
 
 // Event pairs around launches while profiling is on.
@@ -176,6 +179,108 @@ int ffn_shape(int D, int F, int block_rows) {
   if (D > (1 << 20) || F > (1 << 20)) return RING_ATTN_ERR_UNSUPPORTED;
   if (static_cast<long long>(block_rows) * F >= (1ll << 40)) return RING_ATTN_ERR_UNSUPPORTED;
   return RING_ATTN_OK;
+}
+
+// The blockwise FFN's two GEMM launches over a [rows][D] input, prepared
+// once per call (tensor maps, tile order, CTA-pair clusters); ffn_rows then
+// runs the block of rb <= block_rows rows starting at row r0, with its
+// hidden activation in the workspace (caller holds g_mutex).
+struct FfnLaunch {
+  FfnGemmArgs g1, g2;
+};
+
+int ffn_prepare(int dev, const void* x, const void* w1, const float* b1, const void* w2, const float* b2, void* y,
+                int rows, int D, int F, int block_rows, void* workspace, FfnLaunch* out) {
+  int n_sms = 0, optin = 0;
+  if (cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+    return RING_ATTN_ERR_CUDA;
+  if (ffn_gemm_smem_bytes() > static_cast<size_t>(optin)) return RING_ATTN_ERR_UNSUPPORTED;
+  int* err;
+  int rc;
+  if ((rc = status_ptr(dev, &err)) != RING_ATTN_OK) return rc;
+  // the GEMM runs on CTA pairs: clusters of two that fit at once
+  auto it = g_ffn_pair_clusters.find(dev);
+  if (it == g_ffn_pair_clusters.end()) it = g_ffn_pair_clusters.emplace(dev, ffn_pair_max_clusters()).first;
+  const int pair_clusters = it->second;
+  if (pair_clusters <= 0) return RING_ATTN_ERR_UNSUPPORTED;
+  const int tile_m = 256, b_box = 128;
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  // first layer: A = x [rows][D], B = W1 [F][D], C = h [block_rows][F]
+  // second layer: A = h, B = W2 [D][F], C = y [rows][D], residual x
+  FfnGemmArgs& g1 = out->g1;
+  FfnGemmArgs& g2 = out->g2;
+  if (!make_map(&g1.tm_a, x, bf, 2, D, rows, 1, 64) || !make_map(&g1.tm_b, w1, bf, 2, D, F, 1, 64, b_box) ||
+      !make_map(&g1.tm_c, workspace, bf, 2, F, block_rows, 1, 64) ||
+      !make_map(&g2.tm_a, workspace, bf, 2, F, block_rows, 1, 64) ||
+      !make_map(&g2.tm_b, w2, bf, 2, F, D, 1, 64, b_box) || !make_map(&g2.tm_c, y, bf, 2, D, rows, 1, 64))
+    return RING_ATTN_ERR_CUDA;
+  g1.N = F; g1.K = D; g1.c_rows = block_rows; g1.kind = 0; g1.bias = b1;
+  g2.N = D; g2.K = F; g2.c_rows = rows; g2.kind = 1; g2.bias = b2; g2.resid = x;
+  for (FfnGemmArgs* g : {&g1, &g2}) {
+    g->err = err;
+    g->n_sms = n_sms;
+    g->pair_clusters = pair_clusters;
+    g->timer = active_timer();
+    // tile order: groups of row tiles whose rows of A take about 16 MiB, so
+    // that a group's A stays in L2 while its column tiles go by
+    const long long a_tile_bytes = static_cast<long long>(tile_m) * g->K * 2;
+    g->group_rows = static_cast<int>(std::max(1ll, (1ll << 24) / a_tile_bytes));
+  }
+  return RING_ATTN_OK;
+}
+
+int ffn_rows(FfnLaunch& f, int r0, int rb, cudaStream_t stream) {
+  f.g1.M = rb; f.g1.a_row0 = r0; f.g1.c_row0 = 0;
+  f.g2.M = rb; f.g2.a_row0 = 0; f.g2.c_row0 = r0;
+  if (launch_ffn_gemm(f.g1, stream) != cudaSuccess || launch_ffn_gemm(f.g2, stream) != cudaSuccess)
+    return RING_ATTN_ERR_CUDA;
+  return RING_ATTN_OK;
+}
+
+// Forward work items (256-row query blocks) grouped by row blocks of R rows
+// (R % 256 == 0): the items of row block k, longest first, at [k R/256,
+// min((k+1) R/256, n_items)) of a device array.
+int get_block_orders(int dev, int L, int N, int causal, int R, int32_t** out) {
+  auto key = std::make_tuple(dev, L, N, causal, R);
+  auto it = g_block_orders.find(key);
+  if (it != g_block_orders.end()) {
+    *out = it->second;
+    return RING_ATTN_OK;
+  }
+  const Plan p = build_fwd_plan(L, N, causal != 0);
+  const int per = R / kQBlockRows;
+  std::vector<int32_t> v(p.n_blocks);
+  for (int u0 = 0; u0 < p.n_blocks; u0 += per) {
+    const int u1 = std::min(u0 + per, p.n_blocks);
+    std::iota(v.begin() + u0, v.begin() + u1, u0);
+    std::stable_sort(v.begin() + u0, v.begin() + u1, [&](int a, int b) { return p.work[a] > p.work[b]; });
+  }
+  int32_t* d = nullptr;
+  if (cudaMalloc(&d, v.size() * sizeof(int32_t)) != cudaSuccess) return RING_ATTN_ERR_CUDA;
+  if (cudaMemcpy(d, v.data(), v.size() * sizeof(int32_t), cudaMemcpyHostToDevice) != cudaSuccess) {
+    cudaFree(d);
+    return RING_ATTN_ERR_CUDA;
+  }
+  g_block_orders[key] = d;
+  *out = d;
+  return RING_ATTN_OK;
+}
+
+// 4-D map over a token-major [B][L][H][d] bf16 tensor, box (64, 1, 128, 1),
+// 128-byte swizzle: the smem image of a box is that of the 3-D maps' boxes.
+bool make_map_tok(CUtensorMap* m, const void* base, int d, int H, int L, int B) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(L),
+                        static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(d) * H * 2,
+                           static_cast<cuuint64_t>(d) * H * L * 2};
+  cuuint32_t box[4] = {64u, 1u, 128u, 1u};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 int check_ring_shape(int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal, int striped) {
@@ -794,47 +899,78 @@ int ring_attn_ffn_fwd(const void* x, const void* w1, const float* b1, const void
   std::lock_guard<std::mutex> lock(g_mutex);
   int dev;
   if ((rc = current_device(&dev)) != RING_ATTN_OK) return rc;
-  int n_sms = 0, optin = 0;
-  if (cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+  FfnLaunch f;
+  if ((rc = ffn_prepare(dev, x, w1, b1, w2, b2, y, static_cast<int>(M), D, F, block_rows, workspace, &f)) !=
+      RING_ATTN_OK)
+    return rc;
+  for (int r0 = 0; r0 < static_cast<int>(M); r0 += block_rows)
+    if ((rc = ffn_rows(f, r0, std::min(block_rows, static_cast<int>(M) - r0), stream)) != RING_ATTN_OK) return rc;
+  return RING_ATTN_OK;
+}
+
+size_t ring_attn_bpt_workspace_size(int Hq, int d, int F, int block_rows) {
+  if (Hq <= 0 || block_rows <= 0 || block_rows % kQBlockRows) return 0;
+  return ring_attn_ffn_workspace_size(Hq * d, F, block_rows);
+}
+
+int ring_attn_bpt_fwd(const void* q, const void* k, const void* v, void* a_tok, float* lse, const void* w1,
+                      const float* b1, const void* w2, const float* b2, void* y, int B, int Hq, int Hkv, int L, int d,
+                      int n_chunks, int causal, int F, int block_rows, void* workspace, size_t workspace_bytes,
+                      cudaStream_t stream) {
+  int rc = check_shape(B, Hq, Hkv, L, d, n_chunks, causal);
+  if (rc != RING_ATTN_OK) return rc;
+  if (block_rows <= 0) return RING_ATTN_ERR_SHAPE;
+  if (block_rows % kQBlockRows) return RING_ATTN_ERR_UNSUPPORTED;
+  const int D = Hq * d;
+  if ((rc = ffn_shape(D, F, block_rows)) != RING_ATTN_OK) return rc;
+  if (static_cast<long long>(B) * L >= (1ll << 31)) return RING_ATTN_ERR_UNSUPPORTED;
+  if (B == 0 || L == 0) return RING_ATTN_OK;
+  if (!q || !k || !v || !a_tok || !lse || !w1 || !b1 || !w2 || !b2 || !y) return RING_ATTN_ERR_NULL;
+  const void* ptrs[] = {q, k, v, a_tok, lse, w1, b1, w2, b2, y};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return RING_ATTN_ERR_UNSUPPORTED;
+  const size_t need = ring_attn_bpt_workspace_size(Hq, d, F, block_rows);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return RING_ATTN_ERR_WORKSPACE;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  int dev;
+  if ((rc = current_device(&dev)) != RING_ATTN_OK) return rc;
+  // attention: the fused forward, one launch per row block, output token-major
+  FwdArgs a;
+  std::memset(&a, 0, sizeof a);
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (!make_map(&a.tm_q, q, bf, 2, d, L, B * Hq, 64) || !make_map(&a.tm_k, k, bf, 2, d, L, B * Hkv, 64) ||
+      !make_map(&a.tm_v, v, bf, 2, d, L, B * Hkv, 64) || !make_map_tok(&a.tm_o, a_tok, d, Hq, L, B))
     return RING_ATTN_ERR_CUDA;
-  if (ffn_gemm_smem_bytes() > static_cast<size_t>(optin)) return RING_ATTN_ERR_UNSUPPORTED;
+  DevicePlan plan;
+  if ((rc = get_plan(dev, 0, L, n_chunks, causal != 0, &plan)) != RING_ATTN_OK) return rc;
+  int32_t* orders;
+  if ((rc = get_block_orders(dev, L, n_chunks, causal, block_rows, &orders)) != RING_ATTN_OK) return rc;
   int* err;
   if ((rc = status_ptr(dev, &err)) != RING_ATTN_OK) return rc;
-  const int rows = static_cast<int>(M);
-  // the GEMM runs on CTA pairs: clusters of two that fit at once
-  auto it = g_ffn_pair_clusters.find(dev);
-  if (it == g_ffn_pair_clusters.end()) it = g_ffn_pair_clusters.emplace(dev, ffn_pair_max_clusters()).first;
-  const int pair_clusters = it->second;
-  if (pair_clusters <= 0) return RING_ATTN_ERR_UNSUPPORTED;
-  const int tile_m = 256, b_box = 128;
-  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  // first layer: A = x [M][D], B = W1 [F][D], C = h [block_rows][F]
-  // second layer: A = h, B = W2 [D][F], C = y [M][D], residual x
-  FfnGemmArgs g1, g2;
-  if (!make_map(&g1.tm_a, x, bf, 2, D, rows, 1, 64) || !make_map(&g1.tm_b, w1, bf, 2, D, F, 1, 64, b_box) ||
-      !make_map(&g1.tm_c, workspace, bf, 2, F, block_rows, 1, 64) ||
-      !make_map(&g2.tm_a, workspace, bf, 2, F, block_rows, 1, 64) ||
-      !make_map(&g2.tm_b, w2, bf, 2, F, D, 1, 64, b_box) || !make_map(&g2.tm_c, y, bf, 2, D, rows, 1, 64))
-    return RING_ATTN_ERR_CUDA;
-  g1.N = F; g1.K = D; g1.c_rows = block_rows; g1.kind = 0; g1.bias = b1;
-  g2.N = D; g2.K = F; g2.c_rows = rows; g2.kind = 1; g2.bias = b2; g2.resid = x;
-  for (FfnGemmArgs* g : {&g1, &g2}) {
-    g->err = err;
-    g->n_sms = n_sms;
-    g->pair_clusters = pair_clusters;
-    g->timer = active_timer();
-    // tile order: groups of row tiles whose rows of A take about 16 MiB, so
-    // that a group's A stays in L2 while its column tiles go by
-    const long long a_tile_bytes = static_cast<long long>(tile_m) * g->K * 2;
-    g->group_rows = static_cast<int>(std::max(1ll, (1ll << 24) / a_tile_bytes));
-  }
-  for (int r0 = 0; r0 < rows; r0 += block_rows) {
-    const int rb = rows - r0 < block_rows ? rows - r0 : block_rows;
-    g1.M = rb; g1.a_row0 = r0; g1.c_row0 = 0;
-    g2.M = rb; g2.a_row0 = 0; g2.c_row0 = r0;
-    if (launch_ffn_gemm(g1, stream) != cudaSuccess || launch_ffn_gemm(g2, stream) != cudaSuccess)
-      return RING_ATTN_ERR_CUDA;
+  a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.L = L; a.d = d; a.causal = causal != 0;
+  a.offsets = plan.offsets(); a.ranges = plan.ranges();
+  a.lse = lse; a.err = err; a.timer = active_timer();
+  a.o_token_major = 1;
+  // feed-forward on the token rows [L][Hq d] of each batch's attention
+  // output; one set of tensor maps per batch, so that the stores of a block
+  // that ends inside a 128-row box are clipped at that batch's last row
+  std::vector<FfnLaunch> f(B);
+  const size_t batch_bytes = static_cast<size_t>(L) * D * 2;
+  for (int b = 0; b < B; ++b)
+    if ((rc = ffn_prepare(dev, static_cast<const uint8_t*>(a_tok) + b * batch_bytes, w1, b1, w2, b2,
+                          static_cast<uint8_t*>(y) + b * batch_bytes, L, D, F, block_rows, workspace, &f[b])) !=
+        RING_ATTN_OK)
+      return rc;
+  const int per = block_rows / kQBlockRows;
+  for (int r0 = 0; r0 < L; r0 += block_rows) {
+    const int u0 = r0 / kQBlockRows;
+    a.order = orders + u0;
+    a.n_blocks = std::min(per, plan.n_blocks - u0);
+    if (launch_fwd(a, stream) != cudaSuccess) return RING_ATTN_ERR_CUDA;
+    const int rb = std::min(block_rows, L - r0);
+    for (int b = 0; b < B; ++b)
+      if ((rc = ffn_rows(f[b], r0, rb, stream)) != RING_ATTN_OK) return rc;
   }
   return RING_ATTN_OK;
 }
@@ -851,9 +987,14 @@ void ring_attn_release(void) {
     cudaSetDevice(std::get<0>(kv.first));
     cudaFree(kv.second.dev);
   }
+  for (auto& kv : g_block_orders) {
+    cudaSetDevice(std::get<0>(kv.first));
+    cudaFree(kv.second);
+  }
   cudaSetDevice(cur);
   g_plans.clear();
   g_step_plans.clear();
+  g_block_orders.clear();
 }
 
 }  // extern "C"

@@ -51,3 +51,23 @@ def test_argument_errors(lib):
 
 def test_empty_input_is_a_no_op(lib):
     assert lib.ring_attn_ffn_fwd(*([NUL] * 6), 0, 256, 1024, 256, NUL, 0, NUL) == capi.OK
+
+
+def test_bpt_workspace_and_argument_errors(lib):
+    assert lib.ring_attn_bpt_workspace_size(28, 128, 14336, 8192) == 8192 * 14336 * 2
+    assert lib.ring_attn_bpt_workspace_size(28, 128, 14336, 128) == 0   # not whole 256-row work items
+    f = lib.ring_attn_bpt_fwd
+    ws = lib.ring_attn_bpt_workspace_size(2, 128, 1024, 256)
+    ptrs = [P256] * 10
+    # (B, Hq, Hkv, L, d, N, causal, F, block_rows)
+    assert f(*ptrs, 1, 2, 1, 1024, 128, 4, 1, 1024, 128, P256, ws, NUL) == capi.ERR_UNSUPPORTED
+    assert f(*ptrs, 1, 2, 1, 1024, 128, 4, 1, 1024, 0, P256, ws, NUL) == capi.ERR_SHAPE
+    assert f(*ptrs, 1, 3, 1, 1024, 128, 4, 1, 1024, 256, P256, ws, NUL) == capi.ERR_UNSUPPORTED  # D = 384
+    assert f(*ptrs, 1, 2, 1, 1024, 128, 4, 1, 1000, 256, P256, ws, NUL) == capi.ERR_UNSUPPORTED  # F % 256
+    assert f(*ptrs, 1, 2, 1, 1004, 128, 4, 1, 1024, 256, P256, ws, NUL) == capi.ERR_SHAPE  # causal L % 2N
+    assert f(*([NUL] * 10), 1, 2, 1, 1024, 128, 4, 1, 1024, 256, P256, ws, NUL) == capi.ERR_NULL
+    assert f(*ptrs, 1, 2, 1, 1024, 128, 4, 1, 1024, 256, P256, ws - 1, NUL) == capi.ERR_WORKSPACE
+    args = list(ptrs)
+    args[3] = P8
+    assert f(*args, 1, 2, 1, 1024, 128, 4, 1, 1024, 256, P256, ws, NUL) == capi.ERR_UNSUPPORTED
+    assert f(*([NUL] * 10), 0, 2, 1, 1024, 128, 4, 1, 1024, 256, NUL, 0, NUL) == capi.OK   # B == 0

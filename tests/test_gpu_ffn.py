@@ -1,34 +1,17 @@
 """Blockwise feed-forward (BPT) on the GB300 through the C ABI, against the
-fp64 oracle.
-
-The GPU computes y = x + gelu(x W1^T + b1) W2^T + b2 with bf16 operands, fp32
-accumulation and the hidden activation rounded to bf16 between the layers
-(it is the second GEMM's operand); the oracle computes the same block in
-fp64 from the same bf16 values.  Tolerance, per element of y, from that
-arithmetic:
-  * output rounding: half a bf16 ulp of y (at most 2^-8 |y|);
-  * the hidden rounding carried through W2: each h_f moves by at most half
-    a bf16 ulp (2^-8 |h_f|), roughly uniformly, so the error of y_d has
-    standard deviation at most 2^-8 / sqrt(3) * sqrt(sum_f (h_f W2_fd)^2);
-    six of those are allowed;
-  * fp32 accumulation and erff: 1e-4 absolute (several orders below the
-    terms above at these sizes).
-On top, the errors must be typical, not bunched near their bounds: the
-mean-abs error stays within a quarter of the mean bound (a faithful
-computation lands near one sixth of it: one standard deviation plus a
-quarter ulp of output rounding on average).
+fp64 oracle, within the per-element bound of ffn_tolerance.py (output
+rounding plus the bf16 rounding of the hidden activation carried through
+the second layer).
 """
-import math
-
-import numpy as np
 import pytest
 import torch
 
-import oracle
 import sequence_blockwise_self_gb300 as ra
+from ffn_tolerance import check_ffn as check
+from ffn_tolerance import f64
+from ffn_tolerance import ffn_reference
 from sequence_blockwise_self_gb300 import build as lib_build
 from sequence_blockwise_self_gb300 import inputs
-from tolerance import bf16_half_ulp
 
 pytestmark = pytest.mark.gpu
 
@@ -39,27 +22,8 @@ def _built():
     ra.load()
 
 
-def f64(t):
-    return t.detach().float().cpu().double().numpy()
-
-
 def reference(x, w1, b1, w2, b2, rows=None):
-    """Oracle y (and the bound on |y_gpu - y|) for the given rows of x."""
-    W1, W2 = f64(w1).T.copy(), f64(w2).T.copy()   # oracle layout: W1 [D][F], W2 [F][D]
-    xs = f64(x if rows is None else x[torch.as_tensor(rows)])
-    y, h = oracle.ffn(xs, W1, f64(b1), W2, f64(b2), hidden=True)
-    sigma = 2.0 ** -8 / math.sqrt(3.0) * np.sqrt((h * h) @ (W2 * W2))
-    return y, bf16_half_ulp(y) + 6.0 * sigma + 1e-4
-
-
-def check(got, want, bound):
-    got = np.asarray(got, dtype=np.float64)
-    assert np.all(np.isfinite(got))
-    err = np.abs(got - want)
-    worst = np.unravel_index(np.argmax(err - bound), err.shape)
-    assert np.all(err <= bound), (f"error {err[worst]:.3e} above its bound {bound[worst]:.3e} at {worst}; "
-                                  f"max-abs {err.max():.3e}")
-    assert err.mean() <= 0.25 * bound.mean(), f"mean-abs {err.mean():.3e}, mean bound {bound.mean():.3e}"
+    return ffn_reference(x if rows is None else x[torch.as_tensor(rows)], w1, b1, w2, b2)
 
 
 # (M, D, F, block_rows): ragged row counts, several blocks, several column
