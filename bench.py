@@ -583,8 +583,41 @@ def run_ours(args, w):
         bq, bkv, bl = w.B * w.Hq * w.L * w.d * 2, w.B * w.Hkv * w.L * w.d * 2, w.B * w.Hq * w.L * 4
         a2a_bytes = 2 * ((bq + 2 * bkv) + (bq + bl) + (2 * bq + 2 * bkv + bq + bl) + (bq + 2 * bkv))
         a2a_gbs = a2a_bytes / (a2a_ms / args.steps * 1e-3) / 1e9 if a2a_n else None
+        # USP: Ulysses groups of this degree and a ring across N_chunks / N
+        # of them (the fused kernel's fold over the ring groups); the shard
+        # order does not change the work, so the shards are plain slices
+        usp = None
+        R = w.n_chunks // N
+        if R > 1 and ra.usp_workspace_size(w.B, w.Hq, w.Hkv, w.L, w.d, N, R, w.causal) > 0:
+            NR = N * R
+            shard_r = lambda x: x.reshape(*x.shape[:2], NR, w.L // NR, *x.shape[3:]).movedim(2, 0).contiguous()  # noqa: E731
+            qr, kr, vr, dOr = (shard_r(x) for x in (qd, kd, vd, dOd))
+            ws_r = torch.empty(ra.usp_workspace_size(w.B, w.Hq, w.Hkv, w.L, w.d, N, R, w.causal),
+                               dtype=torch.uint8, device=dev)
+            o_r = torch.empty_like(qr)
+            lse_r = torch.empty((NR, w.B, w.Hq, w.L // NR), dtype=torch.float32, device=dev)
+            g_r = [torch.empty_like(qr), torch.empty_like(kr), torch.empty_like(vr)]
+
+            def r_step():
+                ra.ring_attn_usp_fwd(qr, kr, vr, N, w.causal, o=o_r, lse=lse_r, workspace=ws_r, stream=stream)
+                ra.ring_attn_usp_bwd(qr, kr, vr, o_r, lse_r, dOr, N, w.causal, dq=g_r[0], dk=g_r[1], dv=g_r[2],
+                                     workspace=ws_r, stream=stream)
+            r_step()
+            torch.cuda.synchronize(dev)
+            u0.record(stream)
+            for _ in range(args.steps):
+                r_step()
+            u1.record(stream)
+            torch.cuda.synchronize(dev)
+            ms_r = u0.elapsed_time(u1) / args.steps
+            st, site = ra.device_status()
+            if st != 0:
+                raise RuntimeError(f"device status {st} at site {site:#x} in USP")
+            usp = {"ulysses_degree": N, "ring_degree": R, "step_ms": ms_r,
+                   "tflops": step_flops / (ms_r * 1e-3) / 1e12}
+            del qr, kr, vr, dOr, ws_r, o_r, lse_r, g_r
         ulysses = {
-            "degree": N, "step_ms": ms_u, "tflops": step_flops / (ms_u * 1e-3) / 1e12,
+            "degree": N, "step_ms": ms_u, "tflops": step_flops / (ms_u * 1e-3) / 1e12, "usp": usp,
             "per_kernel_ms_per_step": {k: up[k][0] / args.steps for k in ("fwd", "bwd_main", "ulysses_a2a")},
             "a2a_roofline": {"bound": "hbm", "achieved": a2a_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                              "frac": (a2a_gbs / peaks["hbm_gbs"]) if a2a_gbs else None,

@@ -199,6 +199,34 @@ int ring_attn_ulysses_bwd(const void* q, const void* k, const void* v, const voi
                           const void* dO, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int L, int d,
                           int n_ranks, int causal, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * USP (same page, section 8.2): Ulysses within groups of U ranks and a ring
+ * across R groups, over N = U * R sequence shards; rank n = r * U + u (ring
+ * group r, Ulysses rank u) holds L / N tokens of every head, tensors
+ * stacked rank-major as for Ulysses ([N][B][H][L/N][d], lse [N][B][Hq][L/N]).
+ * The all-to-all within a group gives each rank H/U heads of its group's
+ * tokens; attention per head group is a ring over the R groups.  Token i of
+ * rank (r, u): encoder, or R == 1, sequence position n L/N + i; causal with
+ * R > 1, the ring's fold: group r owns sub-chunks r and 2R-1-r of
+ * c = L/(2R) tokens, each split into U pieces of c/U, rank u taking piece u
+ * of both (i < c/U: r c + u c/U + i; else (2R-1-r) c + u c/U + i - c/U).
+ * Requires Hq % U == 0, Hkv % U == 0, L % N == 0 (causal, R > 1: L % 2N ==
+ * 0) and the fused kernels' domain for the head groups.  On one GPU both
+ * all-to-alls are permutations (HBM copies) around one launch of the fused
+ * kernels with batch U * B, H/U heads and the ring over R chunks.
+ * ring_attn_ulysses_* are the case R == 1.
+ */
+size_t ring_attn_usp_workspace_size(int B, int Hq, int Hkv, int L, int d, int ulysses_degree, int ring_degree,
+                                    int causal);
+
+int ring_attn_usp_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int L,
+                      int d, int ulysses_degree, int ring_degree, int causal, void* workspace, size_t workspace_bytes,
+                      cudaStream_t stream);
+
+int ring_attn_usp_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                      void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int L, int d, int ulysses_degree,
+                      int ring_degree, int causal, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* Workspace bytes ring_attn_ring_bwd needs for this shape, or 0 if invalid. */
 size_t ring_attn_ring_bwd_workspace_size(int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal,
                                          int striped);

@@ -8,7 +8,8 @@ Ring mode (the ring run step by step, as each rank of a multi-GPU ring
 would): ring_attn_fwd_step, ring_attn_merge, ring_attn_ring_fwd,
 ring_attn_ring_bwd.
 Ulysses on one GPU (sequence shards -> head shards -> back):
-ring_attn_ulysses_fwd, ring_attn_ulysses_bwd.
+ring_attn_ulysses_fwd, ring_attn_ulysses_bwd; USP (Ulysses groups and a ring
+across them): ring_attn_usp_fwd, ring_attn_usp_bwd.
 Blockwise feed-forward (BPT): ring_attn_ffn_fwd; the blockwise transformer
 forward (attention, then FFN, per query block): ring_attn_bpt_fwd.
 Host-only queries: owner_rank, fwd_plan, bwd_plan, step_plan.
@@ -41,6 +42,9 @@ from .capi import (  # noqa: F401
     ring_bwd_workspace_size,
     ring_attn_ulysses_bwd,
     ring_attn_ulysses_fwd,
+    ring_attn_usp_bwd,
+    ring_attn_usp_fwd,
     ulysses_workspace_size,
+    usp_workspace_size,
     strerror,
 )

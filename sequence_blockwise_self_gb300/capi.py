@@ -91,6 +91,12 @@ def load():
     lib.ring_attn_ulysses_fwd.restype = I
     lib.ring_attn_ulysses_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, S, P]
     lib.ring_attn_ulysses_bwd.restype = I
+    lib.ring_attn_usp_workspace_size.argtypes = [I] * 8
+    lib.ring_attn_usp_workspace_size.restype = S
+    lib.ring_attn_usp_fwd.argtypes = [P, P, P, P, P] + [I] * 8 + [P, S, P]
+    lib.ring_attn_usp_fwd.restype = I
+    lib.ring_attn_usp_bwd.argtypes = [P] * 9 + [I] * 8 + [P, S, P]
+    lib.ring_attn_usp_bwd.restype = I
     lib.ring_attn_ffn_workspace_size.argtypes = [I, I, I]
     lib.ring_attn_ffn_workspace_size.restype = S
     lib.ring_attn_ffn_fwd.argtypes = [P, P, P, P, P, P, ctypes.c_longlong, I, I, I, P, S, P]
@@ -354,6 +360,65 @@ def ring_attn_ulysses_bwd(q, k, v, o, lse, dO, causal: bool, dq=None, dk=None, d
                                       int(workspace.numel() * workspace.element_size()), _stream(stream))
     if rc != OK:
         raise RingAttnError(rc, "ring_attn_ulysses_bwd")
+    return dq, dk, dv
+
+
+def usp_workspace_size(B, Hq, Hkv, L, d, ulysses_degree, ring_degree, causal) -> int:
+    return int(load().ring_attn_usp_workspace_size(int(B), int(Hq), int(Hkv), int(L), int(d), int(ulysses_degree),
+                                                    int(ring_degree), int(bool(causal))))
+
+
+def ring_attn_usp_fwd(q, k, v, ulysses_degree: int, causal: bool, o=None, lse=None, workspace=None, stream=None):
+    """USP on one GPU: q [N,B,Hq,C,d], k, v [N,B,Hkv,C,d] as the N = U*R
+    sequence shards stacked rank-major (rank r*U + u), U = ulysses_degree,
+    R = N / U; returns (o [N,B,Hq,C,d], lse [N,B,Hq,C])."""
+    import torch
+    N, B, Hq, Hkv, L, C, d = _ulysses_shapes(q, k)
+    U = int(ulysses_degree)
+    if U <= 0 or N % U:
+        raise ValueError("the shard count must be a multiple of the Ulysses degree")
+    _check_tensor(q, "q", torch.bfloat16, (N, B, Hq, C, d))
+    _check_tensor(k, "k", torch.bfloat16, (N, B, Hkv, C, d))
+    _check_tensor(v, "v", torch.bfloat16, (N, B, Hkv, C, d))
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((N, B, Hq, C), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check_tensor(o, "o", torch.bfloat16, (N, B, Hq, C, d))
+    _check_tensor(lse, "lse", torch.float32, (N, B, Hq, C))
+    if workspace is None:
+        workspace = torch.empty(max(usp_workspace_size(B, Hq, Hkv, L, d, U, N // U, causal), 1), dtype=torch.uint8,
+                                device=q.device)
+    rc = load().ring_attn_usp_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, L, d, U, N // U,
+                                  int(bool(causal)), _ptr(workspace), int(workspace.numel() * workspace.element_size()),
+                                  _stream(stream))
+    if rc != OK:
+        raise RingAttnError(rc, "ring_attn_usp_fwd")
+    return o, lse
+
+
+def ring_attn_usp_bwd(q, k, v, o, lse, dO, ulysses_degree: int, causal: bool, dq=None, dk=None, dv=None,
+                      workspace=None, stream=None):
+    """Gradients for USP on one GPU, all tensors as sequence shards (see
+    ring_attn_usp_fwd); returns (dq, dk, dv)."""
+    import torch
+    N, B, Hq, Hkv, L, C, d = _ulysses_shapes(q, k)
+    U = int(ulysses_degree)
+    if U <= 0 or N % U:
+        raise ValueError("the shard count must be a multiple of the Ulysses degree")
+    for t, n, sh in ((q, "q", (N, B, Hq, C, d)), (k, "k", (N, B, Hkv, C, d)), (v, "v", (N, B, Hkv, C, d)),
+                     (o, "o", (N, B, Hq, C, d)), (dO, "dO", (N, B, Hq, C, d))):
+        _check_tensor(t, n, torch.bfloat16, sh)
+    _check_tensor(lse, "lse", torch.float32, (N, B, Hq, C))
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if workspace is None:
+        workspace = torch.empty(max(usp_workspace_size(B, Hq, Hkv, L, d, U, N // U, causal), 1), dtype=torch.uint8,
+                                device=q.device)
+    rc = load().ring_attn_usp_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk),
+                                  _ptr(dv), B, Hq, Hkv, L, d, U, N // U, int(bool(causal)), _ptr(workspace),
+                                  int(workspace.numel() * workspace.element_size()), _stream(stream))
+    if rc != OK:
+        raise RingAttnError(rc, "ring_attn_usp_bwd")
     return dq, dk, dv
 
 

@@ -127,11 +127,12 @@ cudaError_t launch_ring_gather_rows(const float* src, float* dst, int Z, int L, 
 cudaError_t launch_ring_scatter_grad(const float* acc, void* g, float scale, bool tiled, int Z, int L, int d, int N,
                                      bool causal, bool striped, cudaStream_t stream);
 
-// Ulysses (ulysses.cu): the all-to-all between sequence shards
-// [N][B][H][L/N][row] and head shards [N][B][H/N][L][row] (to_heads) or
-// back; row_bytes a multiple of 16 (d values of bf16) or 4 (one fp32).
-cudaError_t launch_ulysses_a2a(const void* src, void* dst, int row_bytes, int B, int H, int N, int L, bool to_heads,
-                               cudaStream_t stream);
+// Ulysses / USP (ulysses.cu): the all-to-all between the N = U R sequence
+// shards [N][B][H][L/N][row] and the U head groups [U][B][H/U][L][row]
+// (to_heads) or back; row_bytes a multiple of 16 (d values of bf16) or 4
+// (one fp32).  causal with R > 1: the shards follow the ring's fold.
+cudaError_t launch_ulysses_a2a(const void* src, void* dst, int row_bytes, int B, int H, int U, int R, int L,
+                               bool causal, bool to_heads, cudaStream_t stream);
 cudaError_t launch_ring_scatter(const float* acc, const float* lse_acc, void* o, float* lse, int Z, int L, int d,
                                 int N, bool causal, bool striped, cudaStream_t stream);
 

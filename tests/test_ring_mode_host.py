@@ -153,3 +153,21 @@ def test_ring_bwd_workspace_and_arguments(lib):
     assert lib.ring_attn_ring_bwd(*args, 1, 2, 1, 1024, 64, 4, 1, 0, NUL, ws, NUL) == capi.ERR_WORKSPACE
     assert lib.ring_attn_ring_bwd(*args, 1, 2, 1, 1024, 64, 4, 1, 0, P256, ws - 1, NUL) == capi.ERR_WORKSPACE
     assert lib.ring_attn_ring_bwd(*([NUL] * 9), 1, 2, 1, 1024, 64, 4, 1, 0, P256, ws, NUL) == capi.ERR_NULL
+
+
+def test_usp_workspace_and_arguments(lib):
+    # (B, Hq, Hkv, L, d, U, R, causal)
+    assert lib.ring_attn_usp_workspace_size(1, 4, 2, 512, 64, 2, 1, 1) == lib.ring_attn_ulysses_workspace_size(
+        1, 4, 2, 512, 64, 2, 1)
+    assert lib.ring_attn_usp_workspace_size(1, 4, 2, 1024, 64, 2, 2, 1) > 0
+    assert lib.ring_attn_usp_workspace_size(1, 4, 2, 1028, 64, 2, 2, 1) == 0   # causal ring: L % 2UR
+    assert lib.ring_attn_usp_workspace_size(1, 6, 3, 1024, 64, 4, 2, 1) == 0   # heads do not split by U
+    assert lib.ring_attn_usp_workspace_size(1, 4, 2, 1024, 64, 2, 0, 1) == 0   # no ring groups
+    ws = lib.ring_attn_usp_workspace_size(1, 4, 2, 1024, 64, 2, 2, 1)
+    args = [P256] * 5
+    assert lib.ring_attn_usp_fwd(*args, 1, 4, 2, 1024, 64, 0, 2, 1, P256, ws, NUL) == capi.ERR_SHAPE
+    assert lib.ring_attn_usp_fwd(*([NUL] * 5), 1, 4, 2, 1024, 64, 2, 2, 1, P256, ws, NUL) == capi.ERR_NULL
+    assert lib.ring_attn_usp_fwd(*args, 1, 4, 2, 1024, 64, 2, 2, 1, NUL, ws, NUL) == capi.ERR_WORKSPACE
+    bargs = [P256] * 9
+    assert lib.ring_attn_usp_bwd(*bargs, 1, 4, 2, 1024, 64, 2, 2, 1, P256, ws - 1, NUL) == capi.ERR_WORKSPACE
+    assert lib.ring_attn_usp_bwd(*bargs, 1, 4, 2, 1024, 96, 2, 2, 1, P256, ws, NUL) == capi.ERR_UNSUPPORTED
