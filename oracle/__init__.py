@@ -15,6 +15,7 @@ from .oracle import (  # noqa: F401
     ring_step,
     merge,
     ffn,
+    ffn_bwd,
     owner_rank,
     ring_sources,
     visible_pairs,

@@ -571,6 +571,119 @@ int oracle_ffn(const double *x, const double *w1, const double *b1, const double
   return n_threads;
 }
 
+/* ------------------------------------------------ blockwise FFN backward */
+
+/* Derivative of the exact GELU: d/dx [x Phi(x)] = Phi(x) + x phi(x). */
+static double gelu_grad(double x) {
+  const double Phi = 0.5 * (1.0 + erf(x / sqrt(2.0)));
+  const double phi = exp(-0.5 * x * x) / sqrt(2.0 * acos(-1.0));  /* standard normal density */
+  return Phi + x * phi;
+}
+
+/* Gradients of the loss sum(dy * y) for the FFN block above, by the chain
+ * rule, with a and h recomputed from x (the BPT section's recomputation of
+ * the block's activations in the backward pass):
+ *   dh_f  = sum_d dy_d W2[f][d]
+ *   da_f  = dh_f gelu'(a_f)
+ *   dx_d  = dy_d + sum_f da_f W1[d][f]
+ *   dW2[f][d] = sum_m h_mf dy_md     db2_d = sum_m dy_md
+ *   dW1[d][f] = sum_m x_md da_mf     db1_f = sum_m da_mf
+ * Sums over rows run in ascending row order. */
+typedef struct {
+  const double *x, *w1, *b1, *w2, *dy;
+  double *dx, *h, *da, *dw1, *db1, *dw2, *db2;
+  long M;
+  int D, F;
+} ffn_bwd_t;
+
+typedef struct { const ffn_bwd_t *f; int phase; long n, next; } ffn_bwd_task_t;
+
+static void ffn_bwd_row(const ffn_bwd_t *f, long m) {
+  const double *x = f->x + (size_t)m * f->D, *dy = f->dy + (size_t)m * f->D;
+  double *h = f->h + (size_t)m * f->F, *da = f->da + (size_t)m * f->F;
+  /* a (kept in da until it is replaced), then h */
+  for (int j = 0; j < f->F; ++j) da[j] = f->b1[j];
+  for (int k = 0; k < f->D; ++k) {
+    const double *w = f->w1 + (size_t)k * f->F;
+    for (int j = 0; j < f->F; ++j) da[j] += x[k] * w[j];
+  }
+  for (int j = 0; j < f->F; ++j) {
+    const double a = da[j];
+    h[j] = gelu(a);
+    double dh = 0.0;
+    const double *w = f->w2 + (size_t)j * f->D;
+    for (int c = 0; c < f->D; ++c) dh += dy[c] * w[c];
+    da[j] = dh * gelu_grad(a);
+  }
+  double *dx = f->dx + (size_t)m * f->D;
+  for (int c = 0; c < f->D; ++c) dx[c] = dy[c];
+  for (int j = 0; j < f->F; ++j) {
+    const double *w = f->w1;
+    for (int c = 0; c < f->D; ++c) dx[c] += da[j] * w[(size_t)c * f->F + j];
+  }
+}
+
+/* weight and bias gradients of hidden unit j (row j of dW2, column j of dW1) */
+static void ffn_bwd_unit(const ffn_bwd_t *f, long j) {
+  double *dw2 = f->dw2 + (size_t)j * f->D;
+  for (int c = 0; c < f->D; ++c) dw2[c] = 0.0;
+  double db1 = 0.0;
+  for (int c = 0; c < f->D; ++c) f->dw1[(size_t)c * f->F + j] = 0.0;
+  for (long m = 0; m < f->M; ++m) {
+    const double hm = f->h[(size_t)m * f->F + j], dam = f->da[(size_t)m * f->F + j];
+    const double *dy = f->dy + (size_t)m * f->D, *x = f->x + (size_t)m * f->D;
+    for (int c = 0; c < f->D; ++c) dw2[c] += hm * dy[c];
+    for (int c = 0; c < f->D; ++c) f->dw1[(size_t)c * f->F + j] += x[c] * dam;
+    db1 += dam;
+  }
+  f->db1[j] = db1;
+}
+
+static void *ffn_bwd_worker(void *arg) {
+  ffn_bwd_task_t *t = (ffn_bwd_task_t *)arg;
+  for (;;) {
+    long i = __atomic_fetch_add(&t->next, 1, __ATOMIC_RELAXED);
+    if (i >= t->n) break;
+    if (t->phase == 0)
+      ffn_bwd_row(t->f, i);
+    else
+      ffn_bwd_unit(t->f, i);
+  }
+  return NULL;
+}
+
+/* x [M][D], W1 [D][F], b1 [F], W2 [F][D], dy [M][D] -> dx [M][D],
+ * dW1 [D][F], db1 [F], dW2 [F][D], db2 [D].  (b2 does not enter.) */
+int oracle_ffn_bwd(const double *x, const double *w1, const double *b1, const double *w2, const double *dy, long M,
+                   int D, int F, double *dx, double *dw1, double *db1, double *dw2, double *db2, int n_threads) {
+  if (M < 0 || D <= 0 || F <= 0) return -1;
+  double *h = (double *)malloc(sizeof(double) * (size_t)(M > 0 ? M : 1) * F);
+  double *da = (double *)malloc(sizeof(double) * (size_t)(M > 0 ? M : 1) * F);
+  if (!h || !da) {
+    free(h);
+    free(da);
+    return -2;
+  }
+  ffn_bwd_t f = {x, w1, b1, w2, dy, dx, h, da, dw1, db1, dw2, db2, M, D, F};
+  if (n_threads <= 0) n_threads = (int)sysconf(_SC_NPROCESSORS_ONLN);
+  if (n_threads < 1) n_threads = 1;
+  if (n_threads > 256) n_threads = 256;
+  pthread_t th[256];
+  for (int phase = 0; phase < 2; ++phase) {
+    ffn_bwd_task_t t = {&f, phase, phase == 0 ? M : (long)F, 0};
+    for (int i = 0; i < n_threads; ++i) pthread_create(&th[i], NULL, ffn_bwd_worker, &t);
+    for (int i = 0; i < n_threads; ++i) pthread_join(th[i], NULL);
+  }
+  for (int c = 0; c < D; ++c) {
+    double s = 0.0;
+    for (long m = 0; m < M; ++m) s += dy[(size_t)m * D + c];
+    db2[c] = s;
+  }
+  free(h);
+  free(da);
+  return n_threads;
+}
+
 int oracle_owner_rank(int L, int n_chunks, int causal, int striped, int p) {
   if (p < 0 || p >= L || bad_chunking(L, n_chunks, causal, striped)) return -1;
   return owner_rank(L, n_chunks, causal, striped, p);

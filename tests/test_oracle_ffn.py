@@ -84,3 +84,56 @@ def test_hidden_activation_and_row_subsets():
     ys, hs = oracle.ffn(x, w1, b1, w2, b2, rows=rows, hidden=True)
     np.testing.assert_array_equal(ys, y[rows])
     np.testing.assert_array_equal(hs, h[rows])
+
+
+def _problem(M, D, F, seed):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((M, D))
+    w1, b1, w2, b2 = _weights(D, F, seed + 1)
+    dy = rng.standard_normal((M, D))
+    return x, w1, b1, w2, b2, dy
+
+
+@pytest.mark.parametrize("M,D,F", [(5, 8, 24), (13, 12, 40)])
+def test_ffn_backward_matches_torch_autograd(M, D, F):
+    """Library special case: torch autograd in fp64 through the exact GELU."""
+    x, w1, b1, w2, b2, dy = _problem(M, D, F, M)
+    got = oracle.ffn_bwd(x, w1, b1, w2, dy)
+    tx, tw1, tb1, tw2, tb2 = (torch.tensor(a, requires_grad=True) for a in (x, w1, b1, w2, b2))
+    y = tx + torch.nn.functional.gelu(tx @ tw1 + tb1, approximate="none") @ tw2 + tb2
+    (y * torch.tensor(dy)).sum().backward()
+    for name, g, t in zip(("dx", "dW1", "db1", "dW2", "db2"), got, (tx, tw1, tb1, tw2, tb2)):
+        np.testing.assert_allclose(g, t.grad.numpy(), rtol=0, atol=1e-11, err_msg=name)
+
+
+def test_ffn_backward_finite_differences():
+    """Central differences of the oracle's own forward (loss sum(dy * y)) on a
+    few entries of every argument."""
+    M, D, F = 4, 6, 16
+    x, w1, b1, w2, b2, dy = _problem(M, D, F, 9)
+    grads = dict(zip(("x", "w1", "b1", "w2", "b2"), oracle.ffn_bwd(x, w1, b1, w2, dy)))
+    args = {"x": x, "w1": w1, "b1": b1, "w2": w2, "b2": b2}
+    loss = lambda a: float((oracle.ffn(a["x"], a["w1"], a["b1"], a["w2"], a["b2"]) * dy).sum())  # noqa: E731
+    rng = np.random.default_rng(10)
+    step = 1e-6
+    for name, arr in args.items():
+        for _ in range(4):
+            idx = tuple(int(rng.integers(n)) for n in arr.shape)
+            plus = {k: v.copy() for k, v in args.items()}
+            minus = {k: v.copy() for k, v in args.items()}
+            plus[name][idx] += step
+            minus[name][idx] -= step
+            fd = (loss(plus) - loss(minus)) / (2 * step)
+            assert abs(fd - grads[name][idx]) <= 1e-6 * max(1.0, abs(fd)), (name, idx, fd, grads[name][idx])
+
+
+def test_ffn_backward_with_zero_second_layer():
+    """W2 = 0: no gradient reaches the first layer; dx = dy, dW2 = h^T dy with
+    h = gelu(x W1 + b1), db2 = the column sums of dy."""
+    M, D, F = 7, 5, 12
+    x, w1, b1, _, _, dy = _problem(M, D, F, 11)
+    dx, dw1, db1, dw2, db2 = oracle.ffn_bwd(x, w1, b1, np.zeros((F, D)), dy)
+    assert np.array_equal(dx, dy) and not dw1.any() and not db1.any()
+    h = torch.nn.functional.gelu(torch.tensor(x @ w1 + b1), approximate="none").numpy()
+    np.testing.assert_allclose(dw2, h.T @ dy, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(db2, dy.sum(axis=0), rtol=0, atol=1e-12)

@@ -39,6 +39,8 @@ MUTANTS = {
     "stripes_as_blocks": ("if (striped) return p % N;", "if (striped) return p / (L / N);"),
     "ffn_residual_dropped": ("y[c] = x[c] + acc[c];", "y[c] = acc[c];"),
     "ffn_gelu_wrong_scale": ("return 0.5 * x * (1.0 + erf(x / sqrt(2.0)));", "return 0.5 * x * (1.0 + erf(x / 2.0));"),
+    "ffn_gelu_grad_missing_term": ("return Phi + x * phi;", "return Phi;"),
+    "ffn_dx_residual_dropped": ("for (int c = 0; c < f->D; ++c) dx[c] = dy[c];", "for (int c = 0; c < f->D; ++c) dx[c] = 0.0;"),
     "transposed_score": ("s[j] = P->scale * dot(qi, k_row(P, b, g, j), P->d);\n    if (s[j] > m) m = s[j];\n  }\n  double sum",
                          "s[j] = P->scale * dot(q_row(P, b, h, j), k_row(P, b, g, i), P->d);\n    if (s[j] > m) m = s[j];\n  }\n  double sum"),
 }
@@ -60,6 +62,7 @@ def _quick_pins():
         ("merge", steps.test_merge_weights_are_a_sigmoid_of_the_lse_gap),
         ("stripes", lambda: steps.test_striped_step_with_zero_queries_closed_form(3)),
         ("ffn", lambda: [ffn_pins.test_ffn_matches_torch(7, 16, 64), ffn_pins.test_gelu_values()]),
+        ("ffn_bwd", lambda: ffn_pins.test_ffn_backward_matches_torch_autograd(5, 8, 24)),
     ]
     failed = []
     for name, fn in checks:
