@@ -676,6 +676,25 @@ def run_ours(args, w):
                          "frac_of_sustained": tf_gemm / peaks["sustained"] if tf_gemm else None,
                          "flops_per_step": fw.flops()},
         }
+        # its backward (recomputing each block's hidden activation): five
+        # GEMMs per block, 2.5 x the forward's FLOPs
+        dyf = torch.randn((fw.M, fw.D), generator=gen, device=dev).to(torch.bfloat16)
+        ws_fb = torch.empty(ra.ffn_bwd_workspace_size(fw.D, fw.F, fw.block_rows), dtype=torch.uint8, device=dev)
+        ra.ring_attn_ffn_bwd(xf, w1f, b1f, w2f, dyf, block_rows=fw.block_rows, workspace=ws_fb, stream=stream)
+        torch.cuda.synchronize(dev)
+        f0.record(stream)
+        for _ in range(args.steps):
+            ra.ring_attn_ffn_bwd(xf, w1f, b1f, w2f, dyf, block_rows=fw.block_rows, workspace=ws_fb, stream=stream)
+        f1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms_fb = f0.elapsed_time(f1) / args.steps
+        st, site = ra.device_status()
+        if st != 0:
+            raise RuntimeError(f"device status {st} at site {site:#x} in the FFN backward")
+        ffn["bwd"] = {"ms": ms_fb, "tflops": 2.5 * fw.flops() / (ms_fb * 1e-3) / 1e12,
+                      "flops_per_step": 2.5 * fw.flops(),
+                      "what": "dx, dW1, db1, dW2, db2 of sum(dy * y), hidden activation recomputed per block"}
+        del dyf, ws_fb
         # the blockwise transformer forward on this workload: per 8192-row
         # query block, the block's attention (token-major output) and then
         # the FFN with its residual on those rows (hidden size Hq * d)

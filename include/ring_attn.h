@@ -304,6 +304,27 @@ int ring_attn_ffn_fwd(const void* x, const void* w1, const float* b1, const void
                       long long M, int D, int F, int block_rows, void* workspace, size_t workspace_bytes,
                       cudaStream_t stream);
 
+/* Backward of the blockwise FFN: gradients of sum(dy * y) for y as in
+ * ring_attn_ffn_fwd (b2 does not enter), block by block with the block's
+ * hidden activation recomputed (the BPT section's recomputation):
+ *   dx  = dy + (dy W2 * gelu'(a)) W1          bf16 [M][D]
+ *   dw1 = sum over rows of da^T x             fp32 [F][D]  (W1's layout)
+ *   db1 = sum over rows of da                 fp32 [F]
+ *   dw2 = sum over rows of dy^T h             fp32 [D][F]  (W2's layout)
+ *   db2 = sum over rows of dy                 fp32 [D]
+ * with a = x W1^T + b1, h = gelu(a), da = (dy W2) * gelu'(a).  The four
+ * gradient sums are overwritten (started from zero), accumulated in fp32
+ * over the blocks.  Per block: five tensor-core GEMM launches (the first
+ * layer again with GELU and its derivative, dh * gelu', dx, dw2, dw1), the
+ * weight gradients' operands transposed by a copy kernel.  Same domain and
+ * errors as ring_attn_ffn_fwd; workspace >= ring_attn_ffn_bwd_workspace_size.
+ */
+size_t ring_attn_ffn_bwd_workspace_size(int D, int F, int block_rows);
+
+int ring_attn_ffn_bwd(const void* x, const void* w1, const float* b1, const void* w2, const void* dy, void* dx,
+                      float* dw1, float* db1, float* dw2, float* db2, long long M, int D, int F, int block_rows,
+                      void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* ---------------------------------------------------------------------
  * Blockwise transformer forward (BPT; same page, section 4.2: the outer
  * loop runs over query blocks, and for each block the attention over every

@@ -60,7 +60,7 @@ def _bind(lib):
     lib.oracle_owner_rank.argtypes = [I, I, I, I, I]
     lib.oracle_ffn.argtypes = [_dp, _dp, _dp, _dp, _dp, ctypes.c_long, I, I, _dp, _dp, I]
     lib.oracle_ffn.restype = ctypes.c_int
-    lib.oracle_ffn_bwd.argtypes = [_dp, _dp, _dp, _dp, _dp, ctypes.c_long, I, I, _dp, _dp, _dp, _dp, _dp, I]
+    lib.oracle_ffn_bwd.argtypes = [_dp, _dp, _dp, _dp, _dp, ctypes.c_long, I, I, _dp, _dp, _dp, _dp, _dp, _dp, _dp, I]
     lib.oracle_ffn_bwd.restype = ctypes.c_int
     for f in (lib.oracle_fwd, lib.oracle_fwd_rows, lib.oracle_bwd, lib.oracle_bwd_rows,
               lib.oracle_ring_fwd, lib.oracle_ring_step, lib.oracle_owner_rank):
@@ -258,20 +258,23 @@ def ffn(x, w1, b1, w2, b2, threads: int = 0, rows=None, hidden: bool = False):
     return (y, h) if hidden else y
 
 
-def ffn_bwd(x, w1, b1, w2, dy, threads: int = 0):
+def ffn_bwd(x, w1, b1, w2, dy, threads: int = 0, hidden: bool = False):
     """Gradients of sum(dy * y) for the FFN block of ffn() (the BPT section's
     backward, recomputing the block's hidden activation): returns dx [M, D],
     dW1 [D, F], db1 [F], dW2 [F, D], db2 [D] (oracle layout, W1 [D, F], W2
-    [F, D]), by the chain rule with gelu'(a) = Phi(a) + a phi(a)."""
+    [F, D]), by the chain rule with gelu'(a) = Phi(a) + a phi(a).
+    hidden=True also returns h and da [M, F]."""
     x, w1, b1, w2, dy = (_f64(a) for a in (x, w1, b1, w2, dy))
     M, D = x.shape
     F = w1.shape[1]
     if w1.shape != (D, F) or w2.shape != (F, D) or b1.shape != (F,) or dy.shape != (M, D):
         raise ValueError("ffn_bwd: shape mismatch")
     dx, dw1, db1, dw2, db2 = np.zeros((M, D)), np.zeros((D, F)), np.zeros(F), np.zeros((F, D)), np.zeros(D)
+    h = np.zeros((M, F)) if hidden else None
+    da = np.zeros((M, F)) if hidden else None
     _check(_load().oracle_ffn_bwd(_p(x), _p(w1), _p(b1), _p(w2), _p(dy), M, D, F, _p(dx), _p(dw1), _p(db1), _p(dw2),
-                                  _p(db2), _threads(threads)))
-    return dx, dw1, db1, dw2, db2
+                                  _p(db2), _p(h) if hidden else None, _p(da) if hidden else None, _threads(threads)))
+    return (dx, dw1, db1, dw2, db2, h, da) if hidden else (dx, dw1, db1, dw2, db2)
 
 
 # ------------------------------------------------------------ chunk map (host)

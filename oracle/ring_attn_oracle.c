@@ -653,15 +653,17 @@ static void *ffn_bwd_worker(void *arg) {
 }
 
 /* x [M][D], W1 [D][F], b1 [F], W2 [F][D], dy [M][D] -> dx [M][D],
- * dW1 [D][F], db1 [F], dW2 [F][D], db2 [D].  (b2 does not enter.) */
+ * dW1 [D][F], db1 [F], dW2 [F][D], db2 [D] (b2 does not enter); h_out and
+ * da_out [M][F], if not NULL, receive h and da. */
 int oracle_ffn_bwd(const double *x, const double *w1, const double *b1, const double *w2, const double *dy, long M,
-                   int D, int F, double *dx, double *dw1, double *db1, double *dw2, double *db2, int n_threads) {
+                   int D, int F, double *dx, double *dw1, double *db1, double *dw2, double *db2, double *h_out,
+                   double *da_out, int n_threads) {
   if (M < 0 || D <= 0 || F <= 0) return -1;
-  double *h = (double *)malloc(sizeof(double) * (size_t)(M > 0 ? M : 1) * F);
-  double *da = (double *)malloc(sizeof(double) * (size_t)(M > 0 ? M : 1) * F);
+  double *h = h_out ? h_out : (double *)malloc(sizeof(double) * (size_t)(M > 0 ? M : 1) * F);
+  double *da = da_out ? da_out : (double *)malloc(sizeof(double) * (size_t)(M > 0 ? M : 1) * F);
   if (!h || !da) {
-    free(h);
-    free(da);
+    if (!h_out) free(h);
+    if (!da_out) free(da);
     return -2;
   }
   ffn_bwd_t f = {x, w1, b1, w2, dy, dx, h, da, dw1, db1, dw2, db2, M, D, F};
@@ -679,8 +681,8 @@ int oracle_ffn_bwd(const double *x, const double *w1, const double *b1, const do
     for (long m = 0; m < M; ++m) s += dy[(size_t)m * D + c];
     db2[c] = s;
   }
-  free(h);
-  free(da);
+  if (!h_out) free(h);
+  if (!da_out) free(da);
   return n_threads;
 }
 

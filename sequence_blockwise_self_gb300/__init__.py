@@ -10,7 +10,7 @@ ring_attn_ring_bwd.
 Ulysses on one GPU (sequence shards -> head shards -> back):
 ring_attn_ulysses_fwd, ring_attn_ulysses_bwd; USP (Ulysses groups and a ring
 across them): ring_attn_usp_fwd, ring_attn_usp_bwd.
-Blockwise feed-forward (BPT): ring_attn_ffn_fwd; the blockwise transformer
+Blockwise feed-forward (BPT): ring_attn_ffn_fwd, ring_attn_ffn_bwd; the blockwise transformer
 forward (attention, then FFN, per query block): ring_attn_bpt_fwd.
 Host-only queries: owner_rank, fwd_plan, bwd_plan, step_plan.
 """
@@ -31,7 +31,9 @@ from .capi import (  # noqa: F401
     ring_attn_bwd_noalloc,
     ring_attn_fwd,
     ring_attn_ffn_fwd,
+    ring_attn_ffn_bwd,
     ffn_workspace_size,
+    ffn_bwd_workspace_size,
     ring_attn_bpt_fwd,
     bpt_workspace_size,
     ring_attn_fwd_step,

@@ -101,6 +101,10 @@ def load():
     lib.ring_attn_ffn_workspace_size.restype = S
     lib.ring_attn_ffn_fwd.argtypes = [P, P, P, P, P, P, ctypes.c_longlong, I, I, I, P, S, P]
     lib.ring_attn_ffn_fwd.restype = I
+    lib.ring_attn_ffn_bwd_workspace_size.argtypes = [I, I, I]
+    lib.ring_attn_ffn_bwd_workspace_size.restype = S
+    lib.ring_attn_ffn_bwd.argtypes = [P] * 10 + [ctypes.c_longlong, I, I, I, P, S, P]
+    lib.ring_attn_ffn_bwd.restype = I
     lib.ring_attn_bpt_workspace_size.argtypes = [I, I, I, I]
     lib.ring_attn_bpt_workspace_size.restype = S
     lib.ring_attn_bpt_fwd.argtypes = [P] * 10 + [I] * 9 + [P, S, P]
@@ -451,6 +455,37 @@ def ring_attn_ffn_fwd(x, w1, b1, w2, b2, block_rows: int = 8192, y=None, workspa
     if rc != OK:
         raise RingAttnError(rc, "ring_attn_ffn_fwd")
     return y
+
+
+def ffn_bwd_workspace_size(D: int, F: int, block_rows: int) -> int:
+    return int(load().ring_attn_ffn_bwd_workspace_size(int(D), int(F), int(block_rows)))
+
+
+def ring_attn_ffn_bwd(x, w1, b1, w2, dy, block_rows: int = 8192, workspace=None, stream=None):
+    """Backward of ring_attn_ffn_fwd for the loss sum(dy * y): returns
+    (dx [M, D] bf16, dw1 [F, D], db1 [F], dw2 [D, F], db2 [D] fp32)."""
+    import torch
+    M, D = x.shape
+    F = w1.shape[0]
+    _check_tensor(x, "x", torch.bfloat16, (M, D))
+    _check_tensor(w1, "w1", torch.bfloat16, (F, D))
+    _check_tensor(w2, "w2", torch.bfloat16, (D, F))
+    _check_tensor(b1, "b1", torch.float32, (F,))
+    _check_tensor(dy, "dy", torch.bfloat16, (M, D))
+    dev = x.device
+    dx = torch.empty_like(x)
+    dw1 = torch.empty((F, D), dtype=torch.float32, device=dev)
+    db1 = torch.empty((F,), dtype=torch.float32, device=dev)
+    dw2 = torch.empty((D, F), dtype=torch.float32, device=dev)
+    db2 = torch.empty((D,), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(max(ffn_bwd_workspace_size(D, F, block_rows), 1), dtype=torch.uint8, device=dev)
+    rc = load().ring_attn_ffn_bwd(_ptr(x), _ptr(w1), _ptr(b1), _ptr(w2), _ptr(dy), _ptr(dx), _ptr(dw1), _ptr(db1),
+                                  _ptr(dw2), _ptr(db2), M, D, F, int(block_rows), _ptr(workspace),
+                                  int(workspace.numel() * workspace.element_size()), _stream(stream))
+    if rc != OK:
+        raise RingAttnError(rc, "ring_attn_ffn_bwd")
+    return dx, dw1, db1, dw2, db2
 
 
 def bpt_workspace_size(Hq: int, d: int, F: int, block_rows: int) -> int:

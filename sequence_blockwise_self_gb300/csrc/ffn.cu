@@ -49,10 +49,11 @@ struct GemmDev {
   int a_row0, c_row0;   // first row of this launch in the A and C tensor maps
   int c_rows;           // rows of the C tensor (the residual's rows; rows past it are not read)
   int c_end;            // rows [c_row0, c_end) of C belong to this launch: no other row is read or written
-  int kind;             // 0: gelu(acc + bias), 1: acc + bias + resid
+  int kind;             // see FfnGemmArgs::kind
   int group_rows;       // tile order, see tile_coords
-  const float* bias;    // [N]
-  const __nv_bfloat16* resid;  // [c_rows][N] (kind 1)
+  const float* bias;    // [N] (kinds 0, 1, 2)
+  const __nv_bfloat16* resid;  // [c_rows][N]: the residual (kind 1), gelu'(a) (kind 3)
+  __nv_bfloat16* aux;          // [c_rows][N]: gelu'(acc + bias) out (kind 2)
   int* err;
 };
 
@@ -87,6 +88,11 @@ __device__ __forceinline__ void gemm_drain_wait(uint32_t bar, uint32_t parity, i
 
 __device__ __forceinline__ float gelu(float x) { return 0.5f * x * (1.f + erff(x * 0.70710678118654752f)); }
 
+// d/dx gelu(x) = Phi(x) + x phi(x), phi the standard normal density.
+__device__ __forceinline__ float gelu_grad(float x) {
+  return 0.5f * (1.f + erff(x * 0.70710678118654752f)) + x * 0.3989422804014327f * __expf(-0.5f * x * x);
+}
+
 // The epilogue of one output tile for the 128 rows this CTA holds (thread =
 // row = tensor-memory lane): accumulator columns [t_acc, t_acc + 256) ->
 // + bias, then GELU (kind 0) or + residual (kind 1) -> bf16 into two
@@ -99,7 +105,9 @@ __device__ __forceinline__ void epilogue_tile(const GemmDev& p, const CUtensorMa
                                               uint32_t t_acc, int row, int c_row0, int n0, bool boxes_in_use,
                                               Release release) {
   const int c_row = c_row0 + row;  // this thread's output row
-  const bool has_res = p.kind == 1 && c_row < p.c_end;
+  const bool has_res = (p.kind == 1 || p.kind == 3) && c_row < p.c_end;
+  const bool has_aux = p.kind == 2 && c_row < p.c_end;
+  __nv_bfloat16* aux_row = has_aux ? p.aux + static_cast<size_t>(c_row) * p.N + n0 : nullptr;
   // a box starts on a 128-row boundary of the launch, whose rows end on one
   // or at the end of C: it lies inside the launch's rows, or all past them
   const bool store = c_row0 < p.c_end;
@@ -116,12 +124,32 @@ __device__ __forceinline__ void epilogue_tile(const GemmDev& p, const CUtensorMa
       const int col0 = qtr * 64 + h32 * 32;  // within the tile
       tmem_ld32(t_acc + col0, r);
       float v[32];
+      if (p.kind == 3) {  // no bias: the product is scaled elementwise below
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) + __ldg(p.bias + n0 + col0 + i);
+        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) + __ldg(p.bias + n0 + col0 + i);
+      }
       if (p.kind == 0) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = gelu(v[i]);
-      } else if (has_res) {
+      } else if (p.kind == 2) {
+        // h = gelu(a) to C, gelu'(a) to aux (the backward's recomputation)
+        if (has_aux) {
+#pragma unroll
+          for (int c8 = 0; c8 < 4; ++c8) {
+            uint4 g;
+            g.x = pack_bf16(gelu_grad(v[8 * c8]), gelu_grad(v[8 * c8 + 1]));
+            g.y = pack_bf16(gelu_grad(v[8 * c8 + 2]), gelu_grad(v[8 * c8 + 3]));
+            g.z = pack_bf16(gelu_grad(v[8 * c8 + 4]), gelu_grad(v[8 * c8 + 5]));
+            g.w = pack_bf16(gelu_grad(v[8 * c8 + 6]), gelu_grad(v[8 * c8 + 7]));
+            *reinterpret_cast<uint4*>(aux_row + col0 + 8 * c8) = g;
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = gelu(v[i]);
+      } else if (has_res) {  // kind 1: + residual; kind 3: times gelu'(a)
 #pragma unroll
         for (int c8 = 0; c8 < 4; ++c8) {
           const uint4 rv = *reinterpret_cast<const uint4*>(res_row + col0 + 8 * c8);
@@ -129,8 +157,13 @@ __device__ __forceinline__ void epilogue_tile(const GemmDev& p, const CUtensorMa
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const float2 f = __bfloat1622float2(r2[j]);
-            v[8 * c8 + 2 * j] += f.x;
-            v[8 * c8 + 2 * j + 1] += f.y;
+            if (p.kind == 1) {
+              v[8 * c8 + 2 * j] += f.x;
+              v[8 * c8 + 2 * j + 1] += f.y;
+            } else {
+              v[8 * c8 + 2 * j] *= f.x;
+              v[8 * c8 + 2 * j + 1] *= f.y;
+            }
           }
         }
       }
@@ -145,6 +178,35 @@ __device__ __forceinline__ void epilogue_tile(const GemmDev& p, const CUtensorMa
     named_bar_sync(1, 128);
     if (threadIdx.x == 128 && store) {
       tma_store_3d(tm_c, box, n0 + qtr * 64, c_row0, 0);
+      bulk_commit_group();
+    }
+  }
+}
+
+// Kind 4: C (fp32) += acc, by TMA reduce-add of eight 32-column boxes of
+// 128 rows (128-byte rows), the two staging buffers in turn; otherwise as
+// epilogue_tile.
+template <class Release>
+__device__ __forceinline__ void epilogue_tile_add(const GemmDev& p, const CUtensorMap* tm_c, uint32_t box0,
+                                                  uint32_t box1, uint32_t t_acc, int row, int c_row0, int n0,
+                                                  bool boxes_in_use, Release release) {
+  const bool store = c_row0 < p.c_end;
+  for (int e = 0; e < kBN / 32; ++e) {
+    const uint32_t box = (e & 1) ? box1 : box0;
+    if (boxes_in_use || e >= 2) {  // the reduction that used this box two steps ago has read it
+      if (threadIdx.x == 128) bulk_wait_group_read<1>();
+      named_bar_sync(1, 128);
+    }
+    uint32_t r[32];
+    tmem_ld32(t_acc + 32 * e, r);
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch)
+      st_shared_v4(box + sw128_offset(row, ch), r[4 * ch], r[4 * ch + 1], r[4 * ch + 2], r[4 * ch + 3]);
+    if (e == kBN / 32 - 1) release();  // every column of this accumulator has been read
+    fence_proxy_async_smem();
+    named_bar_sync(1, 128);
+    if (threadIdx.x == 128 && store) {
+      tma_reduce_add_3d(tm_c, box, n0 + 32 * e, c_row0, 0);
       bulk_commit_group();
     }
   }
@@ -297,12 +359,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                                                    kSiteGemmEpilogue));
       if (!ok) break;
       tc_fence_after();
-      epilogue_tile(p, &tm_c, smem_u32(sm.c[0]), smem_u32(sm.c[1]), tmem + acc * kBN + lane_off, row,
-                    p.c_row0 + m0 + kBM * static_cast<int>(rank - leader), n0, t > 0, [&] {
-                      tc_fence_before();
-                      __syncwarp();
-                      if (lane == 0) mbar_arrive_cluster(acc_empty0 + 8u * acc);
-                    });
+      auto release = [&] {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(acc_empty0 + 8u * acc);
+      };
+      const int c_row0 = p.c_row0 + m0 + kBM * static_cast<int>(rank - leader);
+      if (p.kind == 4)
+        epilogue_tile_add(p, &tm_c, smem_u32(sm.c[0]), smem_u32(sm.c[1]), tmem + acc * kBN + lane_off, row, c_row0,
+                          n0, t > 0, release);
+      else
+        epilogue_tile(p, &tm_c, smem_u32(sm.c[0]), smem_u32(sm.c[1]), tmem + acc * kBN + lane_off, row, c_row0, n0,
+                      t > 0, release);
     }
     if (threadIdx.x == 128) bulk_wait_group<0>();
   }
@@ -310,6 +378,53 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   cluster_sync_all();  // no more products, arrivals or reads of the peer's memory
   tc_fence_after();
   if (warp == 2) tmem_dealloc_pair(tmem, 512);
+}
+
+// out[c][r] = in[r][c] for bf16 in [rows][cols] (row stride cols) and out
+// [cols][ld_out]; columns r in [rows, rows_pad) of out are zero (the K
+// padding of the weight-gradient GEMMs).  64 x 64 tiles through shared
+// memory, two bf16 per 32-bit access on both sides.  HBM-bound.
+__global__ void __launch_bounds__(256) transpose_bf16_kernel(const __nv_bfloat16* __restrict__ in,
+                                                            __nv_bfloat16* __restrict__ out, int rows, int cols,
+                                                            int rows_pad, int ld_out) {
+  __shared__ __nv_bfloat16 tile[64][66];
+  const int c0 = blockIdx.x * 64, r0 = blockIdx.y * 64;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+  for (int i = ty; i < 64; i += 8) {
+    const int r = r0 + i, c = c0 + 2 * tx;
+    __nv_bfloat162 v = __floats2bfloat162_rn(0.f, 0.f);
+    if (r < rows && c < cols) v = *reinterpret_cast<const __nv_bfloat162*>(in + static_cast<size_t>(r) * cols + c);
+    tile[i][2 * tx] = v.x;
+    tile[i][2 * tx + 1] = v.y;
+  }
+  __syncthreads();
+  for (int i = ty; i < 64; i += 8) {
+    const int c = c0 + i, r = r0 + 2 * tx;
+    if (c < cols && r < rows_pad) {
+      __nv_bfloat162 v;
+      v.x = tile[2 * tx][i];
+      v.y = tile[2 * tx + 1][i];
+      *reinterpret_cast<__nv_bfloat162*>(out + static_cast<size_t>(c) * ld_out + r) = v;
+    }
+  }
+}
+
+// out[c] += sum over rows r < rows of x[r][c] (bf16 x, row stride ld, cols
+// even): one thread per two columns and a slice of rows per block row,
+// partial sums added with fp32 atomics.
+__global__ void __launch_bounds__(256) colsum_add_kernel(const __nv_bfloat16* __restrict__ x, int rows, int cols, int ld,
+                                                        int rows_per_block, float* __restrict__ out) {
+  const int c = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
+  if (c >= cols) return;
+  const int r0 = blockIdx.y * rows_per_block, r1 = min(rows, r0 + rows_per_block);
+  float s0 = 0.f, s1 = 0.f;
+  for (int r = r0; r < r1; ++r) {
+    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(x + static_cast<size_t>(r) * ld + c));
+    s0 += f.x;
+    s1 += f.y;
+  }
+  atomicAdd(out + c, s0);
+  atomicAdd(out + c + 1, s1);
 }
 
 }  // namespace
@@ -345,6 +460,7 @@ cudaError_t launch_ffn_gemm(const FfnGemmArgs& a, cudaStream_t stream) {
   p.kind = a.kind; p.bias = a.bias;
   p.group_rows = a.group_rows > 0 ? a.group_rows : 1;
   p.resid = static_cast<const __nv_bfloat16*>(a.resid);
+  p.aux = static_cast<__nv_bfloat16*>(a.aux);
   p.err = a.err;
   if (a.pair_clusters <= 0) return cudaErrorInvalidConfiguration;
   const int n_tiles = ((a.M + 2 * kBM - 1) / (2 * kBM)) * (a.N / kBN);
@@ -356,6 +472,23 @@ cudaError_t launch_ffn_gemm(const FfnGemmArgs& a, cudaStream_t stream) {
   if (a.timer) a.timer->mark(kProfFfnGemm, false, stream);
   ffn_gemm_pair_kernel<<<2 * clusters, kGemmThreads, smem, stream>>>(a.tm_a, a.tm_b, a.tm_c, p);
   if (a.timer) a.timer->mark(kProfFfnGemm, true, stream);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_bf16(const void* in, void* out, int rows, int cols, int rows_pad, int ld_out,
+                                  cudaStream_t stream) {
+  const dim3 grid(static_cast<unsigned>((cols + 63) / 64), static_cast<unsigned>((rows_pad + 63) / 64));
+  transpose_bf16_kernel<<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(in),
+                                                  static_cast<__nv_bfloat16*>(out), rows, cols, rows_pad, ld_out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_colsum_add(const void* x, int rows, int cols, int ld, float* out, cudaStream_t stream) {
+  const int rows_per_block = 256;
+  const dim3 grid(static_cast<unsigned>((cols / 2 + 255) / 256), static_cast<unsigned>((rows + rows_per_block - 1) /
+                                                                                          rows_per_block));
+  colsum_add_kernel<<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(x), rows, cols, ld, rows_per_block,
+                                              out);
   return cudaGetLastError();
 }
 

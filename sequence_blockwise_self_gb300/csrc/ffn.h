@@ -17,9 +17,13 @@ enum FfnErrSite : int {
 constexpr int kProfFfnGemm = 8;
 
 // C = epilogue(A B^T) with A [rows][K] and B [N][K] bf16, K-major, through
-// 128B-swizzled tensor maps (boxes of 64 x 128 for A, B and C), on CTA
-// pairs; C bf16 [c_rows][N].
-//   kind 0: C = gelu(acc + bias)         kind 1: C = acc + bias + resid
+// 128B-swizzled tensor maps (boxes of 64 x 128 for A, B and a bf16 C; 32 x
+// 128 for an fp32 C), on CTA pairs.
+//   kind 0: C = gelu(acc + bias)                      (bf16)
+//   kind 1: C = acc + bias + resid                    (bf16)
+//   kind 2: C = gelu(acc + bias), aux = gelu'(acc + bias)   (bf16, bf16)
+//   kind 3: C = acc * resid   (resid: gelu'(a))       (bf16)
+//   kind 4: C += acc                                  (fp32, TMA reduce-add)
 // M rows of C starting at c_row0 are produced from M rows of A starting at
 // a_row0; N % 256 == 0, K % 64 == 0; M is a multiple of 128 unless the rows
 // end at c_rows.  Only rows [c_row0, min(c_row0 + M, c_rows)) of C and of
@@ -29,7 +33,8 @@ struct FfnGemmArgs {
   int M = 0, N = 0, K = 0, a_row0 = 0, c_row0 = 0, c_rows = 0, kind = 0;
   int group_rows = 8;  // tile order: row tiles per group (row tiles fastest inside a group)
   const float* bias = nullptr;
-  const void* resid = nullptr;
+  const void* resid = nullptr;  // [c_rows][N] bf16 (kinds 1, 3)
+  void* aux = nullptr;          // [c_rows][N] bf16 (kind 2)
   int* err = nullptr;
   int n_sms = 0;
   int pair_clusters = 0;  // clusters of two CTAs resident at once (ffn_pair_max_clusters())
@@ -41,5 +46,12 @@ size_t ffn_gemm_smem_bytes();
 // Clusters of two CTAs of the pair kernel that fit on the device at once (0
 // if none or the query fails).
 int ffn_pair_max_clusters();
+
+// out [cols][ld_out] = transpose of in [rows][cols] (bf16), columns
+// [rows, rows_pad) of out zeroed; rows_pad <= ld_out.
+cudaError_t launch_transpose_bf16(const void* in, void* out, int rows, int cols, int rows_pad, int ld_out,
+                                  cudaStream_t stream);
+// out[c] += sum_{r < rows} x[r][c]: x bf16 [rows][ld], cols even; fp32 out.
+cudaError_t launch_colsum_add(const void* x, int rows, int cols, int ld, float* out, cudaStream_t stream);
 
 }  // namespace ra

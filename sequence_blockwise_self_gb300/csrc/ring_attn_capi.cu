@@ -238,6 +238,29 @@ int ffn_rows(FfnLaunch& f, int r0, int rb, cudaStream_t stream) {
   return RING_ATTN_OK;
 }
 
+// Parts of the FFN backward workspace (byte offsets, 256-aligned): W1^T
+// [D][F] and W2^T [F][D] (bf16), one block's h [R][F] and gelu'(a) / da
+// [R][F] (bf16), the transposed operands of the weight gradients [F][R]
+// and [D][R] (bf16), and a zero bias [D] (fp32).
+struct FfnBwdWorkspace {
+  size_t w1t = 0, w2t = 0, h = 0, g = 0, tbig = 0, tsmall = 0, zero = 0, total = 0;
+};
+
+FfnBwdWorkspace ffn_bwd_workspace(int D, int F, int R) {
+  auto up = [](size_t x) { return round_up(x, 256); };
+  const size_t df = static_cast<size_t>(D) * F * 2, rf = static_cast<size_t>(R) * F * 2,
+               rd = static_cast<size_t>(R) * D * 2;
+  FfnBwdWorkspace w;
+  w.w2t = w.w1t + up(df);
+  w.h = w.w2t + up(df);
+  w.g = w.h + up(rf);
+  w.tbig = w.g + up(rf);
+  w.tsmall = w.tbig + up(rf);
+  w.zero = w.tsmall + up(rd);
+  w.total = w.zero + up(static_cast<size_t>(D) * 4);
+  return w;
+}
+
 // Forward work items (256-row query blocks) grouped by row blocks of R rows
 // (R % 256 == 0): the items of row block k, longest first, at [k R/256,
 // min((k+1) R/256, n_items)) of a device array.
@@ -932,6 +955,106 @@ int ring_attn_ffn_fwd(const void* x, const void* w1, const float* b1, const void
     return rc;
   for (int r0 = 0; r0 < static_cast<int>(M); r0 += block_rows)
     if ((rc = ffn_rows(f, r0, std::min(block_rows, static_cast<int>(M) - r0), stream)) != RING_ATTN_OK) return rc;
+  return RING_ATTN_OK;
+}
+
+size_t ring_attn_ffn_bwd_workspace_size(int D, int F, int block_rows) {
+  if (ffn_shape(D, F, block_rows) != RING_ATTN_OK) return 0;
+  return ffn_bwd_workspace(D, F, block_rows).total;
+}
+
+int ring_attn_ffn_bwd(const void* x, const void* w1, const float* b1, const void* w2, const void* dy, void* dx,
+                      float* dw1, float* db1, float* dw2, float* db2, long long M, int D, int F, int block_rows,
+                      void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  int rc = ffn_shape(D, F, block_rows);
+  if (rc != RING_ATTN_OK) return rc;
+  if (M < 0) return RING_ATTN_ERR_SHAPE;
+  if (M >= (1ll << 31)) return RING_ATTN_ERR_UNSUPPORTED;
+  if (!x || !w1 || !b1 || !w2 || !dy || !dx || !dw1 || !db1 || !dw2 || !db2) return RING_ATTN_ERR_NULL;
+  const void* ptrs[] = {x, w1, b1, w2, dy, dx, dw1, db1, dw2, db2};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return RING_ATTN_ERR_UNSUPPORTED;
+  const FfnBwdWorkspace w = ffn_bwd_workspace(D, F, block_rows);
+  if (!workspace || workspace_bytes < w.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return RING_ATTN_ERR_WORKSPACE;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  int dev;
+  if ((rc = current_device(&dev)) != RING_ATTN_OK) return rc;
+  // the gradients are sums over the rows: start from zero
+  if (cudaMemsetAsync(dw1, 0, static_cast<size_t>(F) * D * 4, stream) != cudaSuccess ||
+      cudaMemsetAsync(dw2, 0, static_cast<size_t>(D) * F * 4, stream) != cudaSuccess ||
+      cudaMemsetAsync(db1, 0, static_cast<size_t>(F) * 4, stream) != cudaSuccess ||
+      cudaMemsetAsync(db2, 0, static_cast<size_t>(D) * 4, stream) != cudaSuccess)
+    return RING_ATTN_ERR_CUDA;
+  if (M == 0) return RING_ATTN_OK;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void *w1t = ws + w.w1t, *w2t = ws + w.w2t, *h = ws + w.h, *g = ws + w.g, *tbig = ws + w.tbig,
+       *tsmall = ws + w.tsmall;
+  float* zero = reinterpret_cast<float*>(ws + w.zero);
+  const int rows = static_cast<int>(M), R = block_rows;
+  int n_sms = 0, optin = 0;
+  if (cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+    return RING_ATTN_ERR_CUDA;
+  if (ffn_gemm_smem_bytes() > static_cast<size_t>(optin)) return RING_ATTN_ERR_UNSUPPORTED;
+  int* err;
+  if ((rc = status_ptr(dev, &err)) != RING_ATTN_OK) return rc;
+  auto it = g_ffn_pair_clusters.find(dev);
+  if (it == g_ffn_pair_clusters.end()) it = g_ffn_pair_clusters.emplace(dev, ffn_pair_max_clusters()).first;
+  if (it->second <= 0) return RING_ATTN_ERR_UNSUPPORTED;
+  LaunchTimer* tmr = active_timer();
+  if (cudaMemsetAsync(zero, 0, static_cast<size_t>(D) * 4, stream) != cudaSuccess ||
+      launch_transpose_bf16(w1, w1t, F, D, F, F, stream) != cudaSuccess ||   // W1 [F][D] -> W1^T [D][F]
+      launch_transpose_bf16(w2, w2t, D, F, D, D, stream) != cudaSuccess)     // W2 [D][F] -> W2^T [F][D]
+    return RING_ATTN_ERR_CUDA;
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  // G1: h = gelu(x W1^T + b1), g = gelu'(.)   G2: da = (dy W2) * g (in g's place)
+  // G3: dx = da W1 + dy                      G4: dW2 += dy^T h   G5: dW1 += da^T x
+  FfnGemmArgs g1, g2, g3, g4, g5;
+  if (!make_map(&g1.tm_a, x, bf, 2, D, rows, 1, 64) || !make_map(&g1.tm_b, w1, bf, 2, D, F, 1, 64) ||
+      !make_map(&g1.tm_c, h, bf, 2, F, R, 1, 64) ||
+      !make_map(&g2.tm_a, dy, bf, 2, D, rows, 1, 64) || !make_map(&g2.tm_b, w2t, bf, 2, D, F, 1, 64) ||
+      !make_map(&g2.tm_c, g, bf, 2, F, R, 1, 64) ||
+      !make_map(&g3.tm_a, g, bf, 2, F, R, 1, 64) || !make_map(&g3.tm_b, w1t, bf, 2, F, D, 1, 64) ||
+      !make_map(&g3.tm_c, dx, bf, 2, D, rows, 1, 64) ||
+      !make_map(&g4.tm_a, tsmall, bf, 2, R, D, 1, 64) || !make_map(&g4.tm_b, tbig, bf, 2, R, F, 1, 64) ||
+      !make_map(&g4.tm_c, dw2, f32, 4, F, D, 1, 32) ||
+      !make_map(&g5.tm_a, tbig, bf, 2, R, F, 1, 64) || !make_map(&g5.tm_b, tsmall, bf, 2, R, D, 1, 64) ||
+      !make_map(&g5.tm_c, dw1, f32, 4, D, F, 1, 32))
+    return RING_ATTN_ERR_CUDA;
+  g1.N = F; g1.K = D; g1.c_rows = R; g1.kind = 2; g1.bias = b1; g1.aux = g;
+  g2.N = F; g2.K = D; g2.c_rows = R; g2.kind = 3; g2.resid = g;
+  g3.N = D; g3.K = F; g3.c_rows = rows; g3.kind = 1; g3.bias = zero; g3.resid = dy;
+  g4.M = D; g4.N = F; g4.c_rows = D; g4.kind = 4;
+  g5.M = F; g5.N = D; g5.c_rows = F; g5.kind = 4;
+  for (FfnGemmArgs* a : {&g1, &g2, &g3, &g4, &g5}) {
+    a->err = err;
+    a->n_sms = n_sms;
+    a->pair_clusters = it->second;
+    a->timer = tmr;
+  }
+  auto group_rows = [](int K) { return static_cast<int>(std::max(1ll, (1ll << 24) / (256ll * K * 2))); };
+  g1.group_rows = group_rows(D); g2.group_rows = group_rows(D); g3.group_rows = group_rows(F);
+  for (int r0 = 0; r0 < rows; r0 += R) {
+    const int rb = std::min(R, rows - r0), kp = (rb + 63) / 64 * 64;
+    const uint8_t* dy_blk = static_cast<const uint8_t*>(dy) + static_cast<size_t>(r0) * D * 2;
+    const uint8_t* x_blk = static_cast<const uint8_t*>(x) + static_cast<size_t>(r0) * D * 2;
+    g1.M = rb; g1.a_row0 = r0; g1.c_row0 = 0;
+    g2.M = rb; g2.a_row0 = r0; g2.c_row0 = 0;
+    g3.M = rb; g3.a_row0 = 0; g3.c_row0 = r0;
+    g4.K = kp; g5.K = kp;
+    g4.group_rows = group_rows(kp); g5.group_rows = group_rows(kp);
+    if (launch_ffn_gemm(g1, stream) != cudaSuccess || launch_ffn_gemm(g2, stream) != cudaSuccess ||
+        launch_ffn_gemm(g3, stream) != cudaSuccess ||
+        launch_transpose_bf16(h, tbig, rb, F, kp, R, stream) != cudaSuccess ||
+        launch_transpose_bf16(dy_blk, tsmall, rb, D, kp, R, stream) != cudaSuccess ||
+        launch_ffn_gemm(g4, stream) != cudaSuccess ||
+        launch_transpose_bf16(g, tbig, rb, F, kp, R, stream) != cudaSuccess ||
+        launch_transpose_bf16(x_blk, tsmall, rb, D, kp, R, stream) != cudaSuccess ||
+        launch_ffn_gemm(g5, stream) != cudaSuccess || launch_colsum_add(g, rb, F, F, db1, stream) != cudaSuccess ||
+        launch_colsum_add(dy_blk, rb, D, D, db2, stream) != cudaSuccess)
+      return RING_ATTN_ERR_CUDA;
+  }
   return RING_ATTN_OK;
 }
 

@@ -137,3 +137,13 @@ def test_ffn_backward_with_zero_second_layer():
     h = torch.nn.functional.gelu(torch.tensor(x @ w1 + b1), approximate="none").numpy()
     np.testing.assert_allclose(dw2, h.T @ dy, rtol=0, atol=1e-12)
     np.testing.assert_allclose(db2, dy.sum(axis=0), rtol=0, atol=1e-12)
+
+
+def test_ffn_backward_hidden_outputs():
+    """The returned h is the forward's hidden activation and sum_m da is db1."""
+    x, w1, b1, w2, b2, dy = _problem(6, 8, 20, 12)
+    dx, dw1, db1, dw2, db2, h, da = oracle.ffn_bwd(x, w1, b1, w2, dy, hidden=True)
+    _, h_fwd = oracle.ffn(x, w1, b1, w2, b2, hidden=True)
+    np.testing.assert_array_equal(h, h_fwd)
+    np.testing.assert_allclose(da.sum(axis=0), db1, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(x.T @ da, dw1, rtol=0, atol=1e-12)
