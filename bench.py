@@ -727,7 +727,35 @@ def run_ours(args, w):
                 "ms": ms_b, "tflops": fl_b / (ms_b * 1e-3) / 1e12, "flops_per_step": fl_b,
                 "launches_per_step": 3 * (w.L // fw.block_rows),
             }
-            del a_tok, lse_b, y_b, ws_b
+            del y_b, ws_b
+            # and its backward: the FFN backward (hidden activation recomputed
+            # per block), then the fused attention backward
+            dy_b = torch.randn((w.B, w.L, fw.D), generator=gen, device=dev).to(torch.bfloat16)
+            ws_bb = torch.empty(ra.bpt_bwd_workspace_size(w.B, w.Hq, w.Hkv, w.L, w.d, w.n_chunks, w.causal, fw.F,
+                                                          fw.block_rows), dtype=torch.uint8, device=dev)
+
+            def bb_step():
+                return ra.ring_attn_bpt_bwd(qd, kd, vd, a_tok, lse_b, w1f, b1f, w2f, dy_b, w.n_chunks, w.causal,
+                                            block_rows=fw.block_rows, workspace=ws_bb, stream=stream)
+            grads = bb_step()
+            torch.cuda.synchronize(dev)
+            del grads
+            f0.record(stream)
+            for _ in range(args.steps):
+                grads = bb_step()
+            f1.record(stream)
+            torch.cuda.synchronize(dev)
+            del grads
+            ms_bb = f0.elapsed_time(f1) / args.steps
+            st, site = ra.device_status()
+            if st != 0:
+                raise RuntimeError(f"device status {st} at site {site:#x} in the BPT backward")
+            fl_bb = 2.5 * fl_b
+            ffn["bpt_backward"] = {
+                "what": "FFN backward (hidden activation recomputed per block), then the fused attention backward",
+                "ms": ms_bb, "tflops": fl_bb / (ms_bb * 1e-3) / 1e12, "flops_per_step": fl_bb,
+            }
+            del a_tok, lse_b, dy_b, ws_bb
         del xf, w1f, w2f, b1f, b2f, yf, wsf
 
     if os.sched_getaffinity(0) != all_cpus:

@@ -356,6 +356,25 @@ int ring_attn_bpt_fwd(const void* q, const void* k, const void* v, void* a_tok, 
                       int n_chunks, int causal, int F, int block_rows, void* workspace, size_t workspace_bytes,
                       cudaStream_t stream);
 
+/* Backward of the blockwise transformer forward for the loss sum(dy * y):
+ * the FFN backward over the token rows, block by block with each block's
+ * hidden activation recomputed (ring_attn_ffn_bwd: fp32 dw1 [F][D], db1
+ * [F], dw2 [D][F], db2 [D], overwritten), which gives the gradient at the
+ * attention output, dy plus the FFN's input gradient; then the fused
+ * attention backward (ring_attn_bwd) on the attention output and that
+ * gradient, permuted to head-major: dq, dk, dv bf16 as ring_attn_bwd.
+ * a_tok and lse are ring_attn_bpt_fwd's outputs; dy bf16 [B][L][Hq * d].
+ * Same domain as ring_attn_bpt_fwd; workspace >=
+ * ring_attn_bpt_bwd_workspace_size(), 256-byte aligned. */
+size_t ring_attn_bpt_bwd_workspace_size(int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal, int F,
+                                        int block_rows);
+
+int ring_attn_bpt_bwd(const void* q, const void* k, const void* v, const void* a_tok, const float* lse, const void* w1,
+                      const float* b1, const void* w2, const void* dy, void* dq, void* dk, void* dv, float* dw1,
+                      float* db1, float* dw2, float* db2, int B, int Hq, int Hkv, int L, int d, int n_chunks,
+                      int causal, int F, int block_rows, void* workspace, size_t workspace_bytes,
+                      cudaStream_t stream);
+
 /* ---------------------------------------------------------------------
  * Per-kernel timing, for measurement.  While enabled, every kernel launch
  * of the library is bracketed by two CUDA events recorded on the launch

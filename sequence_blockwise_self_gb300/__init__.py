@@ -11,7 +11,8 @@ Ulysses on one GPU (sequence shards -> head shards -> back):
 ring_attn_ulysses_fwd, ring_attn_ulysses_bwd; USP (Ulysses groups and a ring
 across them): ring_attn_usp_fwd, ring_attn_usp_bwd.
 Blockwise feed-forward (BPT): ring_attn_ffn_fwd, ring_attn_ffn_bwd; the blockwise transformer
-forward (attention, then FFN, per query block): ring_attn_bpt_fwd.
+forward (attention, then FFN, per query block) and its backward:
+ring_attn_bpt_fwd, ring_attn_bpt_bwd.
 Host-only queries: owner_rank, fwd_plan, bwd_plan, step_plan.
 """
 from .capi import (  # noqa: F401
@@ -35,7 +36,9 @@ from .capi import (  # noqa: F401
     ffn_workspace_size,
     ffn_bwd_workspace_size,
     ring_attn_bpt_fwd,
+    ring_attn_bpt_bwd,
     bpt_workspace_size,
+    bpt_bwd_workspace_size,
     ring_attn_fwd_step,
     ring_attn_merge,
     ring_attn_ring_fwd,

@@ -105,6 +105,10 @@ def load():
     lib.ring_attn_ffn_bwd_workspace_size.restype = S
     lib.ring_attn_ffn_bwd.argtypes = [P] * 10 + [ctypes.c_longlong, I, I, I, P, S, P]
     lib.ring_attn_ffn_bwd.restype = I
+    lib.ring_attn_bpt_bwd_workspace_size.argtypes = [I] * 9
+    lib.ring_attn_bpt_bwd_workspace_size.restype = S
+    lib.ring_attn_bpt_bwd.argtypes = [P] * 16 + [I] * 9 + [P, S, P]
+    lib.ring_attn_bpt_bwd.restype = I
     lib.ring_attn_bpt_workspace_size.argtypes = [I, I, I, I]
     lib.ring_attn_bpt_workspace_size.restype = S
     lib.ring_attn_bpt_fwd.argtypes = [P] * 10 + [I] * 9 + [P, S, P]
@@ -526,6 +530,46 @@ def ring_attn_bpt_fwd(q, k, v, w1, b1, w2, b2, n_chunks: int, causal: bool, bloc
     if rc != OK:
         raise RingAttnError(rc, "ring_attn_bpt_fwd")
     return a_tok, lse, y
+
+
+def bpt_bwd_workspace_size(B, Hq, Hkv, L, d, n_chunks, causal, F, block_rows) -> int:
+    return int(load().ring_attn_bpt_bwd_workspace_size(int(B), int(Hq), int(Hkv), int(L), int(d), int(n_chunks),
+                                                        int(bool(causal)), int(F), int(block_rows)))
+
+
+def ring_attn_bpt_bwd(q, k, v, a_tok, lse, w1, b1, w2, dy, n_chunks: int, causal: bool, block_rows: int = 8192,
+                      workspace=None, stream=None):
+    """Backward of ring_attn_bpt_fwd for the loss sum(dy * y), dy [B, L, Hq*d]
+    bf16: returns (dq, dk, dv, dw1, db1, dw2, db2)."""
+    import torch
+    B, Hq, L, d = q.shape
+    Hkv = k.shape[1]
+    D, F = Hq * d, w1.shape[0]
+    _check_tensor(q, "q", torch.bfloat16, (B, Hq, L, d))
+    _check_tensor(k, "k", torch.bfloat16, (B, Hkv, L, d))
+    _check_tensor(v, "v", torch.bfloat16, (B, Hkv, L, d))
+    _check_tensor(a_tok, "a_tok", torch.bfloat16, (B, L, D))
+    _check_tensor(lse, "lse", torch.float32, (B, Hq, L))
+    _check_tensor(w1, "w1", torch.bfloat16, (F, D))
+    _check_tensor(w2, "w2", torch.bfloat16, (D, F))
+    _check_tensor(b1, "b1", torch.float32, (F,))
+    _check_tensor(dy, "dy", torch.bfloat16, (B, L, D))
+    dev = q.device
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dw1 = torch.empty((F, D), dtype=torch.float32, device=dev)
+    db1 = torch.empty((F,), dtype=torch.float32, device=dev)
+    dw2 = torch.empty((D, F), dtype=torch.float32, device=dev)
+    db2 = torch.empty((D,), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(max(bpt_bwd_workspace_size(B, Hq, Hkv, L, d, n_chunks, causal, F, block_rows), 1),
+                                dtype=torch.uint8, device=dev)
+    rc = load().ring_attn_bpt_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(a_tok), _ptr(lse), _ptr(w1), _ptr(b1), _ptr(w2),
+                                  _ptr(dy), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dw1), _ptr(db1), _ptr(dw2), _ptr(db2),
+                                  B, Hq, Hkv, L, d, int(n_chunks), int(bool(causal)), F, int(block_rows),
+                                  _ptr(workspace), int(workspace.numel() * workspace.element_size()), _stream(stream))
+    if rc != OK:
+        raise RingAttnError(rc, "ring_attn_bpt_bwd")
+    return dq, dk, dv, dw1, db1, dw2, db2
 
 
 def bwd_workspace_size(B, Hq, Hkv, L, d, n_chunks, causal) -> int:

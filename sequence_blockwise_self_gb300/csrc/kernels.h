@@ -133,6 +133,10 @@ cudaError_t launch_ring_scatter_grad(const float* acc, void* g, float scale, boo
 // (one fp32).  causal with R > 1: the shards follow the ring's fold.
 cudaError_t launch_ulysses_a2a(const void* src, void* dst, int row_bytes, int B, int H, int U, int R, int L,
                                bool causal, bool to_heads, cudaStream_t stream);
+// Token-major [B][L][H][row] <-> head-major [B][H][L][row]; row_bytes a
+// multiple of 16 (ulysses.cu).
+cudaError_t launch_tokens_heads(const void* src, void* dst, int row_bytes, int B, int H, int L, bool to_heads,
+                                cudaStream_t stream);
 cudaError_t launch_ring_scatter(const float* acc, const float* lse_acc, void* o, float* lse, int Z, int L, int d,
                                 int N, bool causal, bool striped, cudaStream_t stream);
 

@@ -963,23 +963,12 @@ size_t ring_attn_ffn_bwd_workspace_size(int D, int F, int block_rows) {
   return ffn_bwd_workspace(D, F, block_rows).total;
 }
 
-int ring_attn_ffn_bwd(const void* x, const void* w1, const float* b1, const void* w2, const void* dy, void* dx,
-                      float* dw1, float* db1, float* dw2, float* db2, long long M, int D, int F, int block_rows,
-                      void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-  int rc = ffn_shape(D, F, block_rows);
-  if (rc != RING_ATTN_OK) return rc;
-  if (M < 0) return RING_ATTN_ERR_SHAPE;
-  if (M >= (1ll << 31)) return RING_ATTN_ERR_UNSUPPORTED;
-  if (!x || !w1 || !b1 || !w2 || !dy || !dx || !dw1 || !db1 || !dw2 || !db2) return RING_ATTN_ERR_NULL;
-  const void* ptrs[] = {x, w1, b1, w2, dy, dx, dw1, db1, dw2, db2};
-  for (const void* p : ptrs)
-    if (!aligned16(p)) return RING_ATTN_ERR_UNSUPPORTED;
+// The FFN backward on checked arguments (caller holds g_mutex).
+static int ffn_bwd_impl(int dev, const void* x, const void* w1, const float* b1, const void* w2, const void* dy,
+                        void* dx, float* dw1, float* db1, float* dw2, float* db2, long long M, int D, int F,
+                        int block_rows, void* workspace, cudaStream_t stream) {
+  int rc;
   const FfnBwdWorkspace w = ffn_bwd_workspace(D, F, block_rows);
-  if (!workspace || workspace_bytes < w.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
-    return RING_ATTN_ERR_WORKSPACE;
-  std::lock_guard<std::mutex> lock(g_mutex);
-  int dev;
-  if ((rc = current_device(&dev)) != RING_ATTN_OK) return rc;
   // the gradients are sums over the rows: start from zero
   if (cudaMemsetAsync(dw1, 0, static_cast<size_t>(F) * D * 4, stream) != cudaSuccess ||
       cudaMemsetAsync(dw2, 0, static_cast<size_t>(D) * F * 4, stream) != cudaSuccess ||
@@ -1056,6 +1045,96 @@ int ring_attn_ffn_bwd(const void* x, const void* w1, const float* b1, const void
       return RING_ATTN_ERR_CUDA;
   }
   return RING_ATTN_OK;
+}
+
+int ring_attn_ffn_bwd(const void* x, const void* w1, const float* b1, const void* w2, const void* dy, void* dx,
+                      float* dw1, float* db1, float* dw2, float* db2, long long M, int D, int F, int block_rows,
+                      void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  int rc = ffn_shape(D, F, block_rows);
+  if (rc != RING_ATTN_OK) return rc;
+  if (M < 0) return RING_ATTN_ERR_SHAPE;
+  if (M >= (1ll << 31)) return RING_ATTN_ERR_UNSUPPORTED;
+  if (!x || !w1 || !b1 || !w2 || !dy || !dx || !dw1 || !db1 || !dw2 || !db2) return RING_ATTN_ERR_NULL;
+  const void* ptrs[] = {x, w1, b1, w2, dy, dx, dw1, db1, dw2, db2};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return RING_ATTN_ERR_UNSUPPORTED;
+  const FfnBwdWorkspace w = ffn_bwd_workspace(D, F, block_rows);
+  if (!workspace || workspace_bytes < w.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return RING_ATTN_ERR_WORKSPACE;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  int dev;
+  if ((rc = current_device(&dev)) != RING_ATTN_OK) return rc;
+  return ffn_bwd_impl(dev, x, w1, b1, w2, dy, dx, dw1, db1, dw2, db2, M, D, F, block_rows, workspace, stream);
+}
+
+// Parts of the blockwise transformer's backward workspace (byte offsets,
+// 256-aligned): the FFN backward's, the gradient at the attention output
+// (token-major), the attention output and that gradient head-major, and the
+// fused attention backward's.
+struct BptBwdWorkspace {
+  size_t ffn = 0, da = 0, o = 0, dO = 0, attn = 0, total = 0;
+};
+
+BptBwdWorkspace bpt_bwd_workspace(int B, int Hq, int Hkv, int L, int d, int F, int block_rows) {
+  auto up = [](size_t x) { return round_up(x, 256); };
+  const size_t act = static_cast<size_t>(B) * L * Hq * d * 2;
+  BptBwdWorkspace w;
+  w.da = w.ffn + up(ffn_bwd_workspace(Hq * d, F, block_rows).total);
+  w.o = w.da + up(act);
+  w.dO = w.o + up(act);
+  w.attn = w.dO + up(act);
+  w.total = w.attn + bwd_workspace(B, Hq, Hkv, L, d).total;
+  return w;
+}
+
+size_t ring_attn_bpt_bwd_workspace_size(int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal, int F,
+                                        int block_rows) {
+  if (check_shape(B, Hq, Hkv, L, d, n_chunks, causal) != RING_ATTN_OK || block_rows <= 0 ||
+      block_rows % kQBlockRows || ffn_shape(Hq * d, F, block_rows) != RING_ATTN_OK)
+    return 0;
+  return bpt_bwd_workspace(B, Hq, Hkv, L, d, F, block_rows).total;
+}
+
+int ring_attn_bpt_bwd(const void* q, const void* k, const void* v, const void* a_tok, const float* lse, const void* w1,
+                      const float* b1, const void* w2, const void* dy, void* dq, void* dk, void* dv, float* dw1,
+                      float* db1, float* dw2, float* db2, int B, int Hq, int Hkv, int L, int d, int n_chunks,
+                      int causal, int F, int block_rows, void* workspace, size_t workspace_bytes,
+                      cudaStream_t stream) {
+  int rc = check_shape(B, Hq, Hkv, L, d, n_chunks, causal);
+  if (rc != RING_ATTN_OK) return rc;
+  if (block_rows <= 0) return RING_ATTN_ERR_SHAPE;
+  if (block_rows % kQBlockRows) return RING_ATTN_ERR_UNSUPPORTED;
+  const int D = Hq * d;
+  if ((rc = ffn_shape(D, F, block_rows)) != RING_ATTN_OK) return rc;
+  if (static_cast<long long>(B) * L >= (1ll << 31)) return RING_ATTN_ERR_UNSUPPORTED;
+  if (!q || !k || !v || !a_tok || !lse || !w1 || !b1 || !w2 || !dy || !dq || !dk || !dv || !dw1 || !db1 || !dw2 ||
+      !db2)
+    return RING_ATTN_ERR_NULL;
+  const void* ptrs[] = {q, k, v, a_tok, lse, w1, b1, w2, dy, dq, dk, dv, dw1, db1, dw2, db2};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return RING_ATTN_ERR_UNSUPPORTED;
+  const BptBwdWorkspace w = bpt_bwd_workspace(B, Hq, Hkv, L, d, F, block_rows);
+  if (!workspace || workspace_bytes < w.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return RING_ATTN_ERR_WORKSPACE;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  int dev;
+  if ((rc = current_device(&dev)) != RING_ATTN_OK) return rc;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  // FFN: recompute each block's hidden activation; the gradient at the
+  // attention output is dy + the FFN's input gradient (its residual path)
+  if ((rc = ffn_bwd_impl(dev, a_tok, w1, b1, w2, dy, ws + w.da, dw1, db1, dw2, db2, static_cast<long long>(B) * L,
+                         D, F, block_rows, ws + w.ffn, stream)) != RING_ATTN_OK)
+    return rc;
+  if (B == 0 || L == 0) return RING_ATTN_OK;
+  // attention: the fused backward on head-major o and dO
+  LaunchTimer* t = active_timer();
+  if (t) t->mark(RING_ATTN_KERNEL_RING_IO, false, stream);
+  if (launch_tokens_heads(a_tok, ws + w.o, d * 2, B, Hq, L, true, stream) != cudaSuccess ||
+      launch_tokens_heads(ws + w.da, ws + w.dO, d * 2, B, Hq, L, true, stream) != cudaSuccess)
+    return RING_ATTN_ERR_CUDA;
+  if (t) t->mark(RING_ATTN_KERNEL_RING_IO, true, stream);
+  return bwd_impl(dev, q, k, v, ws + w.o, lse, ws + w.dO, dq, dk, dv, B, Hq, Hkv, L, d, n_chunks, causal,
+                  ws + w.attn, stream);
 }
 
 size_t ring_attn_bpt_workspace_size(int Hq, int d, int F, int block_rows) {

@@ -101,4 +101,33 @@ cudaError_t launch_ulysses_a2a(const void* src, void* dst, int row_bytes, int B,
   return cudaGetLastError();
 }
 
+// Token-major [B][L][H][row] <-> head-major [B][H][L][row] (the
+// blockwise transformer's FFN rows against the attention kernels' layout),
+// 16 bytes per thread, walking the head-major side.
+__global__ void __launch_bounds__(256) tokens_heads_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                                           int vec16, int H, int L, int to_heads, long long n_vec) {
+  const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= n_vec) return;
+  const int c = static_cast<int>(t % vec16);
+  const long long hm = t / vec16;  // head-major row ((b H + h) L + l)
+  const int l = static_cast<int>(hm % L);
+  const long long bh = hm / L;
+  const int h = static_cast<int>(bh % H);
+  const long long b = bh / H;
+  const long long tm = (b * L + l) * H + h;  // token-major row
+  if (to_heads)
+    dst[hm * vec16 + c] = src[tm * vec16 + c];
+  else
+    dst[tm * vec16 + c] = src[hm * vec16 + c];
+}
+
+cudaError_t launch_tokens_heads(const void* src, void* dst, int row_bytes, int B, int H, int L, bool to_heads,
+                                cudaStream_t stream) {
+  const int vec16 = row_bytes / 16;
+  const long long n = static_cast<long long>(B) * H * L * vec16;
+  tokens_heads_kernel<<<blocks_for(n), 256, 0, stream>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst),
+                                                         vec16, H, L, to_heads ? 1 : 0, n);
+  return cudaGetLastError();
+}
+
 }  // namespace ra

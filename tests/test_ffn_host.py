@@ -71,3 +71,23 @@ def test_bpt_workspace_and_argument_errors(lib):
     args[3] = P8
     assert f(*args, 1, 2, 1, 1024, 128, 4, 1, 1024, 256, P256, ws, NUL) == capi.ERR_UNSUPPORTED
     assert f(*([NUL] * 10), 0, 2, 1, 1024, 128, 4, 1, 1024, 256, NUL, 0, NUL) == capi.OK   # B == 0
+
+
+def test_ffn_bwd_and_bpt_bwd_arguments(lib):
+    assert lib.ring_attn_ffn_bwd_workspace_size(256, 512, 128) > 0
+    assert lib.ring_attn_ffn_bwd_workspace_size(200, 512, 128) == 0
+    ws = lib.ring_attn_ffn_bwd_workspace_size(256, 512, 128)
+    f = lib.ring_attn_ffn_bwd
+    ptrs = [P256] * 10
+    assert f(*ptrs, -1, 256, 512, 128, P256, ws, NUL) == capi.ERR_SHAPE
+    assert f(*([NUL] * 10), 100, 256, 512, 128, P256, ws, NUL) == capi.ERR_NULL
+    assert f(*ptrs, 100, 256, 512, 128, P256, ws - 1, NUL) == capi.ERR_WORKSPACE
+    assert f(*ptrs, 100, 256, 512, 100, P256, ws, NUL) == capi.ERR_UNSUPPORTED
+    g = lib.ring_attn_bpt_bwd
+    wsb = lib.ring_attn_bpt_bwd_workspace_size(1, 2, 1, 1024, 128, 4, 1, 1024, 256)
+    assert wsb > ws
+    assert lib.ring_attn_bpt_bwd_workspace_size(1, 2, 1, 1024, 128, 4, 1, 1024, 128) == 0
+    bptrs = [P256] * 16
+    assert g(*bptrs, 1, 2, 1, 1024, 128, 4, 1, 1024, 128, P256, wsb, NUL) == capi.ERR_UNSUPPORTED
+    assert g(*([NUL] * 16), 1, 2, 1, 1024, 128, 4, 1, 1024, 256, P256, wsb, NUL) == capi.ERR_NULL
+    assert g(*bptrs, 1, 2, 1, 1024, 128, 4, 1, 1024, 256, P256, wsb - 1, NUL) == capi.ERR_WORKSPACE

@@ -70,3 +70,46 @@ def test_bpt_forward(case):
             torch.as_tensor(inputs.ffn_sample_rows(B * L, R, n_rows, seed=2)))
     want, bound = ffn_reference(x[rows.cuda()], *dev[3:])
     check_ffn(f64(y.reshape(B * L, D)[rows.cuda()]), want, bound)
+
+
+# (B, Hq, Hkv, L, d, N, causal, F, block_rows)
+BWD_CASES = [
+    (1, 2, 1, 1024, 128, 4, True, 1024, 256),
+    (2, 4, 2, 1000, 64, 4, True, 512, 512),
+]
+
+
+@pytest.mark.parametrize("case", BWD_CASES, ids=lambda c: "B{}Hq{}Hkv{}L{}d{}N{}{}F{}R{}".format(
+    *c[:6], "c" if c[6] else "e", c[7], c[8]))
+def test_bpt_backward(case):
+    """The chain rule through y = a + FFN(a), a = attention(q, k, v): the
+    attention gradients against the oracle's attention backward driven by
+    the oracle's gradient at a (dy plus the FFN's input gradient, on the
+    GPU's a); the FFN's weight gradients equal ring_attn_ffn_bwd on a."""
+    B, Hq, Hkv, L, d, N, causal, F, R = case
+    D = Hq * d
+    q, k, v, _ = inputs.make_inputs(B, Hq, Hkv, L, d, seed=65 + L + Hq, with_grad=False)
+    _, w1, b1, w2, b2 = inputs.make_ffn_inputs(1, D, F, seed=66 + F)
+    dy = torch.randn((B, L, D), generator=torch.Generator().manual_seed(67)).to(torch.bfloat16)
+    dev = [t.cuda() for t in (q, k, v, w1, b1, w2, b2)]
+    a_tok, lse, _ = ra.ring_attn_bpt_fwd(*dev[:3], *dev[3:], N, causal, block_rows=R)
+    dq, dk, dv, dw1, db1, dw2, db2 = ra.ring_attn_bpt_bwd(*dev[:3], a_tok, lse, dev[3], dev[4], dev[5],
+                                                          dy.cuda(), N, causal, block_rows=R)
+    torch.cuda.synchronize()
+    assert ra.device_status()[0] == 0
+
+    # gradient at the attention output, by the oracle, from the GPU's a
+    x = f64(a_tok).reshape(B * L, D)
+    da = oracle.ffn_bwd(x, f64(w1).T.copy(), f64(b1), f64(w2).T.copy(), f64(dy).reshape(B * L, D))[0]
+    dO = da.reshape(B, L, Hq, d).transpose(0, 2, 1, 3)
+    dq_ref, dk_ref, dv_ref, _, _ = oracle.bwd(f64(q), f64(k), f64(v), dO, causal)
+    check_bf16("dq", f64(dq), dq_ref)
+    check_bf16("dk", f64(dk), dk_ref)
+    check_bf16("dv", f64(dv), dv_ref)
+
+    # the FFN part is the blockwise FFN backward on the token rows
+    fdx, fdw1, fdb1, fdw2, fdb2 = ra.ring_attn_ffn_bwd(a_tok.reshape(B * L, D), dev[3], dev[4], dev[5],
+                                                       dy.cuda().reshape(B * L, D), block_rows=R)
+    assert torch.equal(dw1, fdw1) and torch.equal(dw2, fdw2)
+    torch.testing.assert_close(db1, fdb1, rtol=1e-5, atol=1e-4)   # column sums by fp32 atomics
+    torch.testing.assert_close(db2, fdb2, rtol=1e-5, atol=1e-4)
