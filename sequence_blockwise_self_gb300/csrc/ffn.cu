@@ -53,7 +53,6 @@ struct GemmDev {
   int group_rows;       // tile order, see tile_coords
   const float* bias;    // [N] (kinds 0, 1, 2)
   const __nv_bfloat16* resid;  // [c_rows][N]: the residual (kind 1), gelu'(a) (kind 3)
-  __nv_bfloat16* aux;          // [c_rows][N]: gelu'(acc + bias) out (kind 2)
   int* err;
 };
 
@@ -88,11 +87,6 @@ __device__ __forceinline__ void gemm_drain_wait(uint32_t bar, uint32_t parity, i
 
 __device__ __forceinline__ float gelu(float x) { return 0.5f * x * (1.f + erff(x * 0.70710678118654752f)); }
 
-// d/dx gelu(x) = Phi(x) + x phi(x), phi the standard normal density.
-__device__ __forceinline__ float gelu_grad(float x) {
-  return 0.5f * (1.f + erff(x * 0.70710678118654752f)) + x * 0.3989422804014327f * __expf(-0.5f * x * x);
-}
-
 // The epilogue of one output tile for the 128 rows this CTA holds (thread =
 // row = tensor-memory lane): accumulator columns [t_acc, t_acc + 256) ->
 // + bias, then GELU (kind 0) or + residual (kind 1) -> bf16 into two
@@ -106,8 +100,6 @@ __device__ __forceinline__ void epilogue_tile(const GemmDev& p, const CUtensorMa
                                               Release release) {
   const int c_row = c_row0 + row;  // this thread's output row
   const bool has_res = (p.kind == 1 || p.kind == 3) && c_row < p.c_end;
-  const bool has_aux = p.kind == 2 && c_row < p.c_end;
-  __nv_bfloat16* aux_row = has_aux ? p.aux + static_cast<size_t>(c_row) * p.N + n0 : nullptr;
   // a box starts on a 128-row boundary of the launch, whose rows end on one
   // or at the end of C: it lies inside the launch's rows, or all past them
   const bool store = c_row0 < p.c_end;
@@ -132,21 +124,6 @@ __device__ __forceinline__ void epilogue_tile(const GemmDev& p, const CUtensorMa
         for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) + __ldg(p.bias + n0 + col0 + i);
       }
       if (p.kind == 0) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = gelu(v[i]);
-      } else if (p.kind == 2) {
-        // h = gelu(a) to C, gelu'(a) to aux (the backward's recomputation)
-        if (has_aux) {
-#pragma unroll
-          for (int c8 = 0; c8 < 4; ++c8) {
-            uint4 g;
-            g.x = pack_bf16(gelu_grad(v[8 * c8]), gelu_grad(v[8 * c8 + 1]));
-            g.y = pack_bf16(gelu_grad(v[8 * c8 + 2]), gelu_grad(v[8 * c8 + 3]));
-            g.z = pack_bf16(gelu_grad(v[8 * c8 + 4]), gelu_grad(v[8 * c8 + 5]));
-            g.w = pack_bf16(gelu_grad(v[8 * c8 + 6]), gelu_grad(v[8 * c8 + 7]));
-            *reinterpret_cast<uint4*>(aux_row + col0 + 8 * c8) = g;
-          }
-        }
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = gelu(v[i]);
       } else if (has_res) {  // kind 1: + residual; kind 3: times gelu'(a)
@@ -178,6 +155,54 @@ __device__ __forceinline__ void epilogue_tile(const GemmDev& p, const CUtensorMa
     named_bar_sync(1, 128);
     if (threadIdx.x == 128 && store) {
       tma_store_3d(tm_c, box, n0 + qtr * 64, c_row0, 0);
+      bulk_commit_group();
+    }
+  }
+}
+
+// Kind 2 (the backward's recomputation of the first layer): from
+// a = acc + bias, h = gelu(a) = a Phi(a) to C and gelu'(a) = Phi(a) +
+// a phi(a) to the aux map (one erf and one exp per element), each quarter
+// of 64 columns staged in its own buffer (h in box0, gelu' in box1) and
+// stored by TMA; otherwise as epilogue_tile.
+template <class Release>
+__device__ __forceinline__ void epilogue_tile_dual(const GemmDev& p, const CUtensorMap* tm_c, const CUtensorMap* tm_aux,
+                                                   uint32_t box0, uint32_t box1, uint32_t t_acc, int row, int c_row0,
+                                                   int n0, bool boxes_in_use, Release release) {
+  const bool store = c_row0 < p.c_end;
+  for (int qtr = 0; qtr < 4; ++qtr) {
+    if (boxes_in_use || qtr > 0) {  // the stores of the previous quarter have read both buffers
+      if (threadIdx.x == 128) bulk_wait_group_read<0>();
+      named_bar_sync(1, 128);
+    }
+#pragma unroll
+    for (int h32 = 0; h32 < 2; ++h32) {
+      uint32_t r[32];
+      const int col0 = qtr * 64 + h32 * 32;
+      tmem_ld32(t_acc + col0, r);
+#pragma unroll
+      for (int c8 = 0; c8 < 4; ++c8) {
+        float hv[8], gv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float a = __uint_as_float(r[8 * c8 + i]) + __ldg(p.bias + n0 + col0 + 8 * c8 + i);
+          const float Phi = 0.5f * (1.f + erff(a * 0.70710678118654752f));
+          const float phi = 0.3989422804014327f * __expf(-0.5f * a * a);
+          hv[i] = a * Phi;
+          gv[i] = fmaf(a, phi, Phi);
+        }
+        st_shared_v4(box0 + sw128_offset(row, h32 * 4 + c8), pack_bf16(hv[0], hv[1]), pack_bf16(hv[2], hv[3]),
+                     pack_bf16(hv[4], hv[5]), pack_bf16(hv[6], hv[7]));
+        st_shared_v4(box1 + sw128_offset(row, h32 * 4 + c8), pack_bf16(gv[0], gv[1]), pack_bf16(gv[2], gv[3]),
+                     pack_bf16(gv[4], gv[5]), pack_bf16(gv[6], gv[7]));
+      }
+    }
+    if (qtr == 3) release();
+    fence_proxy_async_smem();
+    named_bar_sync(1, 128);
+    if (threadIdx.x == 128 && store) {
+      tma_store_3d(tm_c, box0, n0 + qtr * 64, c_row0, 0);
+      tma_store_3d(tm_aux, box1, n0 + qtr * 64, c_row0, 0);
       bulk_commit_group();
     }
   }
@@ -243,7 +268,8 @@ struct PairSmem {
 // product, against 48 KB for the single-CTA 128x256 tile.
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     ffn_gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                         const __grid_constant__ CUtensorMap tm_c, const GemmDev p) {
+                         const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_aux,
+                         const GemmDev p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // the same for both CTAs (same kernel, same layout): skipping the work
   // keeps the collective steps (allocation, cluster barriers) on both sides
@@ -274,6 +300,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     tma_prefetch_desc(&tm_a);
     tma_prefetch_desc(&tm_b);
     tma_prefetch_desc(&tm_c);
+    if (p.kind == 2) tma_prefetch_desc(&tm_aux);
   }
   if (warp == 2) {  // one warp in each CTA of the pair, collectively
     tmem_alloc_pair(smem_u32(&sm.tmem_base), 512);
@@ -368,6 +395,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       if (p.kind == 4)
         epilogue_tile_add(p, &tm_c, smem_u32(sm.c[0]), smem_u32(sm.c[1]), tmem + acc * kBN + lane_off, row, c_row0,
                           n0, t > 0, release);
+      else if (p.kind == 2)
+        epilogue_tile_dual(p, &tm_c, &tm_aux, smem_u32(sm.c[0]), smem_u32(sm.c[1]), tmem + acc * kBN + lane_off, row,
+                           c_row0, n0, t > 0, release);
       else
         epilogue_tile(p, &tm_c, smem_u32(sm.c[0]), smem_u32(sm.c[1]), tmem + acc * kBN + lane_off, row, c_row0, n0,
                       t > 0, release);
@@ -460,7 +490,6 @@ cudaError_t launch_ffn_gemm(const FfnGemmArgs& a, cudaStream_t stream) {
   p.kind = a.kind; p.bias = a.bias;
   p.group_rows = a.group_rows > 0 ? a.group_rows : 1;
   p.resid = static_cast<const __nv_bfloat16*>(a.resid);
-  p.aux = static_cast<__nv_bfloat16*>(a.aux);
   p.err = a.err;
   if (a.pair_clusters <= 0) return cudaErrorInvalidConfiguration;
   const int n_tiles = ((a.M + 2 * kBM - 1) / (2 * kBM)) * (a.N / kBN);
@@ -470,7 +499,8 @@ cudaError_t launch_ffn_gemm(const FfnGemmArgs& a, cudaStream_t stream) {
       cudaFuncSetAttribute(ffn_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   if (a.timer) a.timer->mark(kProfFfnGemm, false, stream);
-  ffn_gemm_pair_kernel<<<2 * clusters, kGemmThreads, smem, stream>>>(a.tm_a, a.tm_b, a.tm_c, p);
+  ffn_gemm_pair_kernel<<<2 * clusters, kGemmThreads, smem, stream>>>(a.tm_a, a.tm_b, a.tm_c,
+                                                                      a.kind == 2 ? a.tm_aux : a.tm_c, p);
   if (a.timer) a.timer->mark(kProfFfnGemm, true, stream);
   return cudaGetLastError();
 }

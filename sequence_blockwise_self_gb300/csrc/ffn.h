@@ -21,7 +21,8 @@ constexpr int kProfFfnGemm = 8;
 // 128 for an fp32 C), on CTA pairs.
 //   kind 0: C = gelu(acc + bias)                      (bf16)
 //   kind 1: C = acc + bias + resid                    (bf16)
-//   kind 2: C = gelu(acc + bias), aux = gelu'(acc + bias)   (bf16, bf16)
+//   kind 2: C = gelu(acc + bias), aux = gelu'(acc + bias)   (bf16, bf16;
+//           aux through tm_aux)
 //   kind 3: C = acc * resid   (resid: gelu'(a))       (bf16)
 //   kind 4: C += acc                                  (fp32, TMA reduce-add)
 // M rows of C starting at c_row0 are produced from M rows of A starting at
@@ -30,11 +31,11 @@ constexpr int kProfFfnGemm = 8;
 // the residual are touched.
 struct FfnGemmArgs {
   CUtensorMap tm_a, tm_b, tm_c;
+  CUtensorMap tm_aux;  // kind 2: the gelu'(a) output, laid out as tm_c
   int M = 0, N = 0, K = 0, a_row0 = 0, c_row0 = 0, c_rows = 0, kind = 0;
   int group_rows = 8;  // tile order: row tiles per group (row tiles fastest inside a group)
   const float* bias = nullptr;
   const void* resid = nullptr;  // [c_rows][N] bf16 (kinds 1, 3)
-  void* aux = nullptr;          // [c_rows][N] bf16 (kind 2)
   int* err = nullptr;
   int n_sms = 0;
   int pair_clusters = 0;  // clusters of two CTAs resident at once (ffn_pair_max_clusters())

@@ -1001,7 +1001,7 @@ static int ffn_bwd_impl(int dev, const void* x, const void* w1, const float* b1,
   // G3: dx = da W1 + dy                      G4: dW2 += dy^T h   G5: dW1 += da^T x
   FfnGemmArgs g1, g2, g3, g4, g5;
   if (!make_map(&g1.tm_a, x, bf, 2, D, rows, 1, 64) || !make_map(&g1.tm_b, w1, bf, 2, D, F, 1, 64) ||
-      !make_map(&g1.tm_c, h, bf, 2, F, R, 1, 64) ||
+      !make_map(&g1.tm_c, h, bf, 2, F, R, 1, 64) || !make_map(&g1.tm_aux, g, bf, 2, F, R, 1, 64) ||
       !make_map(&g2.tm_a, dy, bf, 2, D, rows, 1, 64) || !make_map(&g2.tm_b, w2t, bf, 2, D, F, 1, 64) ||
       !make_map(&g2.tm_c, g, bf, 2, F, R, 1, 64) ||
       !make_map(&g3.tm_a, g, bf, 2, F, R, 1, 64) || !make_map(&g3.tm_b, w1t, bf, 2, F, D, 1, 64) ||
@@ -1011,7 +1011,7 @@ static int ffn_bwd_impl(int dev, const void* x, const void* w1, const float* b1,
       !make_map(&g5.tm_a, tbig, bf, 2, R, F, 1, 64) || !make_map(&g5.tm_b, tsmall, bf, 2, R, D, 1, 64) ||
       !make_map(&g5.tm_c, dw1, f32, 4, D, F, 1, 32))
     return RING_ATTN_ERR_CUDA;
-  g1.N = F; g1.K = D; g1.c_rows = R; g1.kind = 2; g1.bias = b1; g1.aux = g;
+  g1.N = F; g1.K = D; g1.c_rows = R; g1.kind = 2; g1.bias = b1;
   g2.N = F; g2.K = D; g2.c_rows = R; g2.kind = 3; g2.resid = g;
   g3.N = D; g3.K = F; g3.c_rows = rows; g3.kind = 1; g3.bias = zero; g3.resid = dy;
   g4.M = D; g4.N = F; g4.c_rows = D; g4.kind = 4;
