@@ -15,9 +15,9 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libring_attn.so")
-SOURCES = ["ring_attn_capi.cu", "attn_fwd.cu", "attn_bwd.cu", "plan.cpp", "ring_attn_noalloc.cu", "ring_step.cu",
-           "ulysses.cu", "ffn.cu"]
-HEADERS = ["kernels.h", "plan.h", "sm103_ptx.cuh", "sm103_pair.cuh", "ffn.h"]
+SOURCES = ["ring_attn_capi.cu", "capi_parallel.cu", "capi_ffn.cu", "attn_fwd.cu", "attn_bwd.cu", "plan.cpp",
+           "ring_attn_noalloc.cu", "ring_step.cu", "ulysses.cu", "ffn.cu"]
+HEADERS = ["kernels.h", "plan.h", "sm103_ptx.cuh", "sm103_pair.cuh", "ffn.h", "capi_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
