@@ -87,11 +87,11 @@ int ffn_rows(FfnLaunch& f, int r0, int rb, cudaStream_t stream) {
 }
 
 // Parts of the FFN backward workspace (byte offsets, 256-aligned): W1^T
-// [D][F] and W2^T [F][D] (bf16), one block's h [R][F] and gelu'(a) / da
-// [R][F] (bf16), the transposed operands of the weight gradients [F][R]
-// and [D][R] (bf16), and a zero bias [D] (fp32).
+// [D][F] and W2^T [F][D] (bf16), one block's gelu'(a) / da [R][F] (bf16),
+// the transposed operands of the weight gradients, h^T / da^T [F][R] and
+// dy^T / x^T [D][R] (bf16), and a zero bias [D] (fp32).
 struct FfnBwdWorkspace {
-  size_t w1t = 0, w2t = 0, h = 0, g = 0, tbig = 0, tsmall = 0, zero = 0, total = 0;
+  size_t w1t = 0, w2t = 0, g = 0, tbig = 0, tsmall = 0, zero = 0, total = 0;
 };
 
 FfnBwdWorkspace ffn_bwd_workspace(int D, int F, int R) {
@@ -100,13 +100,26 @@ FfnBwdWorkspace ffn_bwd_workspace(int D, int F, int R) {
                rd = static_cast<size_t>(R) * D * 2;
   FfnBwdWorkspace w;
   w.w2t = w.w1t + up(df);
-  w.h = w.w2t + up(df);
-  w.g = w.h + up(rf);
+  w.g = w.w2t + up(df);
   w.tbig = w.g + up(rf);
   w.tsmall = w.tbig + up(rf);
   w.zero = w.tsmall + up(rd);
   w.total = w.zero + up(static_cast<size_t>(D) * 4);
   return w;
+}
+
+// 2-D (as 3-D) map over a bf16 [rows][cols] tensor with 64 x 64 boxes and no
+// swizzle: the transposed outputs of the FFN backward's epilogues.
+bool make_map_t(CUtensorMap* m, const void* base, int cols, int rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows), 1};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2, static_cast<cuuint64_t>(cols) * rows * 2};
+  cuuint32_t box[3] = {64u, 64u, 1u};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // 4-D map over a token-major [B][L][H][d] bf16 tensor, box (64, 1, 128, 1),
@@ -139,8 +152,7 @@ int ffn_bwd_impl(int dev, const void* x, const void* w1, const float* b1, const 
     return RING_ATTN_ERR_CUDA;
   if (M == 0) return RING_ATTN_OK;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  void *w1t = ws + w.w1t, *w2t = ws + w.w2t, *h = ws + w.h, *g = ws + w.g, *tbig = ws + w.tbig,
-       *tsmall = ws + w.tsmall;
+  void *w1t = ws + w.w1t, *w2t = ws + w.w2t, *g = ws + w.g, *tbig = ws + w.tbig, *tsmall = ws + w.tsmall;
   float* zero = reinterpret_cast<float*>(ws + w.zero);
   const int rows = static_cast<int>(M), R = block_rows;
   int n_sms = 0, optin = 0;
@@ -159,13 +171,16 @@ int ffn_bwd_impl(int dev, const void* x, const void* w1, const float* b1, const 
       launch_transpose_bf16(w2, w2t, D, F, D, D, stream) != cudaSuccess)     // W2 [D][F] -> W2^T [F][D]
     return RING_ATTN_ERR_CUDA;
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
-  // G1: h = gelu(x W1^T + b1), g = gelu'(.)   G2: da = (dy W2) * g (in g's place)
-  // G3: dx = da W1 + dy                      G4: dW2 += dy^T h   G5: dW1 += da^T x
+  // per block, in this order:
+  //   G1: g = gelu'(x W1^T + b1), h^T = gelu(.)^T     G4: dW2 += dy^T h
+  //   G2: da = (dy W2) * g in g's place, and da^T     G3: dx = da W1 + dy
+  //   G5: dW1 += da^T x
+  // h^T and da^T share one buffer (G4 has read h^T before G2 writes da^T)
   FfnGemmArgs g1, g2, g3, g4, g5;
   if (!make_map(&g1.tm_a, x, bf, 2, D, rows, 1, 64) || !make_map(&g1.tm_b, w1, bf, 2, D, F, 1, 64) ||
-      !make_map(&g1.tm_c, h, bf, 2, F, R, 1, 64) || !make_map(&g1.tm_aux, g, bf, 2, F, R, 1, 64) ||
+      !make_map(&g1.tm_c, g, bf, 2, F, R, 1, 64) || !make_map_t(&g1.tm_aux, tbig, R, F) ||
       !make_map(&g2.tm_a, dy, bf, 2, D, rows, 1, 64) || !make_map(&g2.tm_b, w2t, bf, 2, D, F, 1, 64) ||
-      !make_map(&g2.tm_c, g, bf, 2, F, R, 1, 64) ||
+      !make_map(&g2.tm_c, g, bf, 2, F, R, 1, 64) || !make_map_t(&g2.tm_aux, tbig, R, F) ||
       !make_map(&g3.tm_a, g, bf, 2, F, R, 1, 64) || !make_map(&g3.tm_b, w1t, bf, 2, F, D, 1, 64) ||
       !make_map(&g3.tm_c, dx, bf, 2, D, rows, 1, 64) ||
       !make_map(&g4.tm_a, tsmall, bf, 2, R, D, 1, 64) || !make_map(&g4.tm_b, tbig, bf, 2, R, F, 1, 64) ||
@@ -174,7 +189,7 @@ int ffn_bwd_impl(int dev, const void* x, const void* w1, const float* b1, const 
       !make_map(&g5.tm_c, dw1, f32, 4, D, F, 1, 32))
     return RING_ATTN_ERR_CUDA;
   g1.N = F; g1.K = D; g1.c_rows = R; g1.kind = 2; g1.bias = b1;
-  g2.N = F; g2.K = D; g2.c_rows = R; g2.kind = 3; g2.resid = g;
+  g2.N = F; g2.K = D; g2.c_rows = R; g2.kind = 3; g2.resid = g; g2.trans = 1;
   g3.N = D; g3.K = F; g3.c_rows = rows; g3.kind = 1; g3.bias = zero; g3.resid = dy;
   g4.M = D; g4.N = F; g4.c_rows = D; g4.kind = 4;
   g5.M = F; g5.N = D; g5.c_rows = F; g5.kind = 4;
@@ -195,12 +210,10 @@ int ffn_bwd_impl(int dev, const void* x, const void* w1, const float* b1, const 
     g3.M = rb; g3.a_row0 = 0; g3.c_row0 = r0;
     g4.K = kp; g5.K = kp;
     g4.group_rows = group_rows(kp); g5.group_rows = group_rows(kp);
-    if (launch_ffn_gemm(g1, stream) != cudaSuccess || launch_ffn_gemm(g2, stream) != cudaSuccess ||
-        launch_ffn_gemm(g3, stream) != cudaSuccess ||
-        launch_transpose_bf16(h, tbig, rb, F, kp, R, stream) != cudaSuccess ||
+    if (launch_ffn_gemm(g1, stream) != cudaSuccess ||
         launch_transpose_bf16(dy_blk, tsmall, rb, D, kp, R, stream) != cudaSuccess ||
-        launch_ffn_gemm(g4, stream) != cudaSuccess ||
-        launch_transpose_bf16(g, tbig, rb, F, kp, R, stream) != cudaSuccess ||
+        launch_ffn_gemm(g4, stream) != cudaSuccess || launch_ffn_gemm(g2, stream) != cudaSuccess ||
+        launch_ffn_gemm(g3, stream) != cudaSuccess ||
         launch_transpose_bf16(x_blk, tsmall, rb, D, kp, R, stream) != cudaSuccess ||
         launch_ffn_gemm(g5, stream) != cudaSuccess || launch_colsum_add(g, rb, F, F, db1, stream) != cudaSuccess ||
         launch_colsum_add(dy_blk, rb, D, D, db2, stream) != cudaSuccess)

@@ -50,6 +50,7 @@ struct GemmDev {
   int c_rows;           // rows of the C tensor (the residual's rows; rows past it are not read)
   int c_end;            // rows [c_row0, c_end) of C belong to this launch: no other row is read or written
   int kind;             // see FfnGemmArgs::kind
+  int trans;            // kind 3: also store the transposed output through tm_aux
   int group_rows;       // tile order, see tile_coords
   const float* bias;    // [N] (kinds 0, 1, 2)
   const __nv_bfloat16* resid;  // [c_rows][N]: the residual (kind 1), gelu'(a) (kind 3)
@@ -160,16 +161,28 @@ __device__ __forceinline__ void epilogue_tile(const GemmDev& p, const CUtensorMa
   }
 }
 
-// Kind 2 (the backward's recomputation of the first layer): from
-// a = acc + bias, h = gelu(a) = a Phi(a) to C and gelu'(a) = Phi(a) +
-// a phi(a) to the aux map (one erf and one exp per element), each quarter
-// of 64 columns staged in its own buffer (h in box0, gelu' in box1) and
-// stored by TMA; otherwise as epilogue_tile.
+// Epilogues with a second, transposed output (the backward's recomputation
+// of the first layer, kind 2, and da, kind 3 with tm_aux): per quarter of 64
+// columns the normal output is staged in box0 (128-byte swizzle, stored by
+// TMA through tm_c) and the transposed output in box1 as two 64 x 64 tiles
+// [column][row] without swizzle, stored through tm_aux (a map over the
+// transposed tensor [N][rows], box 64 x 64).  Rows at or past c_end go to
+// the transposed output as zeros: they pad the weight-gradient GEMMs' K.
+//   kind 2: a = acc + bias; normal gelu'(a) = Phi(a) + a phi(a), transposed
+//           h = gelu(a) = a Phi(a) (one erf and one exp per element)
+//   kind 3: normal and transposed da = acc * gelu'(a) (gelu'(a) from resid)
 template <class Release>
-__device__ __forceinline__ void epilogue_tile_dual(const GemmDev& p, const CUtensorMap* tm_c, const CUtensorMap* tm_aux,
-                                                   uint32_t box0, uint32_t box1, uint32_t t_acc, int row, int c_row0,
-                                                   int n0, bool boxes_in_use, Release release) {
+__device__ __forceinline__ void epilogue_tile_trans(const GemmDev& p, const CUtensorMap* tm_c,
+                                                    const CUtensorMap* tm_aux, uint32_t box0, uint32_t box1,
+                                                    uint32_t t_acc, int row, int c_row0, int n0, bool boxes_in_use,
+                                                    Release release) {
+  const int c_row = c_row0 + row;
+  const bool live = c_row < p.c_end;
   const bool store = c_row0 < p.c_end;
+  const __nv_bfloat16* res_row = (p.kind == 3 && live) ? p.resid + static_cast<size_t>(c_row) * p.N + n0 : nullptr;
+  // this thread's element (column c) of the transposed tile: row c of the
+  // 64 x 64 tile row / 64, position row % 64
+  const uint32_t tbase = box1 + static_cast<uint32_t>(row >> 6) * 8192u + static_cast<uint32_t>(row & 63) * 2u;
   for (int qtr = 0; qtr < 4; ++qtr) {
     if (boxes_in_use || qtr > 0) {  // the stores of the previous quarter have read both buffers
       if (threadIdx.x == 128) bulk_wait_group_read<0>();
@@ -182,19 +195,40 @@ __device__ __forceinline__ void epilogue_tile_dual(const GemmDev& p, const CUten
       tmem_ld32(t_acc + col0, r);
 #pragma unroll
       for (int c8 = 0; c8 < 4; ++c8) {
-        float hv[8], gv[8];
+        float nv[8], tv[8];
+        if (p.kind == 2) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float a = __uint_as_float(r[8 * c8 + i]) + __ldg(p.bias + n0 + col0 + 8 * c8 + i);
+            const float Phi = 0.5f * (1.f + erff(a * 0.70710678118654752f));
+            const float phi = 0.3989422804014327f * __expf(-0.5f * a * a);
+            nv[i] = fmaf(a, phi, Phi);
+            tv[i] = a * Phi;
+          }
+        } else {
+          float gr[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          if (live) {
+            const uint4 rv = *reinterpret_cast<const uint4*>(res_row + col0 + 8 * c8);
+            const __nv_bfloat162* r2 = reinterpret_cast<const __nv_bfloat162*>(&rv);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float2 f = __bfloat1622float2(r2[j]);
+              gr[2 * j] = f.x;
+              gr[2 * j + 1] = f.y;
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) nv[i] = tv[i] = __uint_as_float(r[8 * c8 + i]) * gr[i];
+        }
+        st_shared_v4(box0 + sw128_offset(row, h32 * 4 + c8), pack_bf16(nv[0], nv[1]), pack_bf16(nv[2], nv[3]),
+                     pack_bf16(nv[4], nv[5]), pack_bf16(nv[6], nv[7]));
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float a = __uint_as_float(r[8 * c8 + i]) + __ldg(p.bias + n0 + col0 + 8 * c8 + i);
-          const float Phi = 0.5f * (1.f + erff(a * 0.70710678118654752f));
-          const float phi = 0.3989422804014327f * __expf(-0.5f * a * a);
-          hv[i] = a * Phi;
-          gv[i] = fmaf(a, phi, Phi);
+          const __nv_bfloat16 t = __float2bfloat16_rn(live ? tv[i] : 0.f);
+          const uint32_t addr = tbase + static_cast<uint32_t>(h32 * 32 + 8 * c8 + i) * 128u;
+          asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(*reinterpret_cast<const uint16_t*>(&t))
+                       : "memory");
         }
-        st_shared_v4(box0 + sw128_offset(row, h32 * 4 + c8), pack_bf16(hv[0], hv[1]), pack_bf16(hv[2], hv[3]),
-                     pack_bf16(hv[4], hv[5]), pack_bf16(hv[6], hv[7]));
-        st_shared_v4(box1 + sw128_offset(row, h32 * 4 + c8), pack_bf16(gv[0], gv[1]), pack_bf16(gv[2], gv[3]),
-                     pack_bf16(gv[4], gv[5]), pack_bf16(gv[6], gv[7]));
       }
     }
     if (qtr == 3) release();
@@ -202,7 +236,8 @@ __device__ __forceinline__ void epilogue_tile_dual(const GemmDev& p, const CUten
     named_bar_sync(1, 128);
     if (threadIdx.x == 128 && store) {
       tma_store_3d(tm_c, box0, n0 + qtr * 64, c_row0, 0);
-      tma_store_3d(tm_aux, box1, n0 + qtr * 64, c_row0, 0);
+      tma_store_3d(tm_aux, box1, c_row0, n0 + qtr * 64, 0);
+      tma_store_3d(tm_aux, box1 + 8192u, c_row0 + 64, n0 + qtr * 64, 0);
       bulk_commit_group();
     }
   }
@@ -300,7 +335,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     tma_prefetch_desc(&tm_a);
     tma_prefetch_desc(&tm_b);
     tma_prefetch_desc(&tm_c);
-    if (p.kind == 2) tma_prefetch_desc(&tm_aux);
+    if (p.kind == 2 || p.trans) tma_prefetch_desc(&tm_aux);
   }
   if (warp == 2) {  // one warp in each CTA of the pair, collectively
     tmem_alloc_pair(smem_u32(&sm.tmem_base), 512);
@@ -395,9 +430,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       if (p.kind == 4)
         epilogue_tile_add(p, &tm_c, smem_u32(sm.c[0]), smem_u32(sm.c[1]), tmem + acc * kBN + lane_off, row, c_row0,
                           n0, t > 0, release);
-      else if (p.kind == 2)
-        epilogue_tile_dual(p, &tm_c, &tm_aux, smem_u32(sm.c[0]), smem_u32(sm.c[1]), tmem + acc * kBN + lane_off, row,
-                           c_row0, n0, t > 0, release);
+      else if (p.kind == 2 || (p.kind == 3 && p.trans))
+        epilogue_tile_trans(p, &tm_c, &tm_aux, smem_u32(sm.c[0]), smem_u32(sm.c[1]), tmem + acc * kBN + lane_off, row,
+                            c_row0, n0, t > 0, release);
       else
         epilogue_tile(p, &tm_c, smem_u32(sm.c[0]), smem_u32(sm.c[1]), tmem + acc * kBN + lane_off, row, c_row0, n0,
                       t > 0, release);
@@ -488,6 +523,7 @@ cudaError_t launch_ffn_gemm(const FfnGemmArgs& a, cudaStream_t stream) {
   p.a_row0 = a.a_row0; p.c_row0 = a.c_row0; p.c_rows = a.c_rows;
   p.c_end = a.c_row0 + a.M < a.c_rows ? a.c_row0 + a.M : a.c_rows;
   p.kind = a.kind; p.bias = a.bias;
+  p.trans = a.kind == 3 && a.trans ? 1 : 0;
   p.group_rows = a.group_rows > 0 ? a.group_rows : 1;
   p.resid = static_cast<const __nv_bfloat16*>(a.resid);
   p.err = a.err;
@@ -499,8 +535,9 @@ cudaError_t launch_ffn_gemm(const FfnGemmArgs& a, cudaStream_t stream) {
       cudaFuncSetAttribute(ffn_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   if (a.timer) a.timer->mark(kProfFfnGemm, false, stream);
-  ffn_gemm_pair_kernel<<<2 * clusters, kGemmThreads, smem, stream>>>(a.tm_a, a.tm_b, a.tm_c,
-                                                                      a.kind == 2 ? a.tm_aux : a.tm_c, p);
+  const bool aux = a.kind == 2 || (a.kind == 3 && a.trans);
+  ffn_gemm_pair_kernel<<<2 * clusters, kGemmThreads, smem, stream>>>(a.tm_a, a.tm_b, a.tm_c, aux ? a.tm_aux : a.tm_c,
+                                                                      p);
   if (a.timer) a.timer->mark(kProfFfnGemm, true, stream);
   return cudaGetLastError();
 }

@@ -21,9 +21,12 @@ constexpr int kProfFfnGemm = 8;
 // 128 for an fp32 C), on CTA pairs.
 //   kind 0: C = gelu(acc + bias)                      (bf16)
 //   kind 1: C = acc + bias + resid                    (bf16)
-//   kind 2: C = gelu(acc + bias), aux = gelu'(acc + bias)   (bf16, bf16;
-//           aux through tm_aux)
-//   kind 3: C = acc * resid   (resid: gelu'(a))       (bf16)
+//   kind 2: C = gelu'(acc + bias), and gelu(acc + bias) transposed through
+//           tm_aux                                    (bf16, bf16)
+//   kind 3: C = acc * resid   (resid: gelu'(a))       (bf16; with trans, also
+//           transposed through tm_aux)
+// The transposed outputs go to a [N][rows] tensor through tm_aux (64 x 64
+// boxes, no swizzle), rows at or past the launch's end as zeros.
 //   kind 4: C += acc                                  (fp32, TMA reduce-add)
 // M rows of C starting at c_row0 are produced from M rows of A starting at
 // a_row0; N % 256 == 0, K % 64 == 0; M is a multiple of 128 unless the rows
@@ -31,11 +34,12 @@ constexpr int kProfFfnGemm = 8;
 // the residual are touched.
 struct FfnGemmArgs {
   CUtensorMap tm_a, tm_b, tm_c;
-  CUtensorMap tm_aux;  // kind 2: the gelu'(a) output, laid out as tm_c
+  CUtensorMap tm_aux;  // kinds 2, 3 with trans: the transposed output
   int M = 0, N = 0, K = 0, a_row0 = 0, c_row0 = 0, c_rows = 0, kind = 0;
   int group_rows = 8;  // tile order: row tiles per group (row tiles fastest inside a group)
   const float* bias = nullptr;
   const void* resid = nullptr;  // [c_rows][N] bf16 (kinds 1, 3)
+  int trans = 0;                // kind 3: also write the transposed output
   int* err = nullptr;
   int n_sms = 0;
   int pair_clusters = 0;  // clusters of two CTAs resident at once (ffn_pair_max_clusters())
