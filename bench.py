@@ -790,7 +790,10 @@ def run_ours(args, w):
             "ring_mode": ring,
             "ulysses": ulysses,
             "ffn": ffn,
-            "gpu_launches": 4 * args.steps,
+            # per step: forward, backward pre-pass, fused backward, dq conversion,
+            # and with grouped queries the dk and dv conversions (the launch
+            # list in profiles/launch_list_gqa_128k_step.md shows the same)
+            "gpu_launches": (4 + (2 if w.Hq > w.Hkv else 0)) * args.steps,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
