@@ -10,11 +10,19 @@
 // Only one block's hidden activation h exists at a time (the BPT memory
 // saving), in a caller-provided buffer reused block after block.
 //
-// Both layers are one persistent GEMM kernel C = A B^T with A [M][K] and
+// The backward (same section: the block's activations are recomputed, not
+// kept) differentiates the loss sum(dy * y) block by block:
+//   a = x W1 + b1, g = gelu'(a), h = gelu(a)     (recomputed)
+//   dW2 += h^T dy    da = (dy W2^T) * g    dx = dy + da W1^T    dW1 += x^T da
+//
+// Every product is one persistent GEMM kernel C = A B^T with A [M][K] and
 // B [N][K] bf16 (K-major: the weights are passed output-major), fp32
 // accumulation in tensor memory and a fused epilogue:
-//   kind 0:  C = bf16(gelu(acc + bias[n]))
-//   kind 1:  C = bf16(acc + bias[n] + resid[m][n])
+//   kind 0:  C = bf16(gelu(acc + bias[n]))                 forward layer 1
+//   kind 1:  C = bf16(acc + bias[n] + resid[m][n])         forward layer 2, dx
+//   kind 2:  C = bf16(gelu'(a)), h^T = bf16(gelu(a))^T     recompute (a = acc + bias)
+//   kind 3:  C = bf16(acc * g[m][n]) (and C^T)             da
+//   kind 4:  C (fp32) += acc, TMA reduce-add               dW1, dW2
 // It runs on CTA pairs (clusters of two CTAs on the two SMs of a TPC,
 // tcgen05 cta_group::2): 256 x 256 output tiles, each CTA staging its 128
 // rows of A and 128 of the 256 rows of B^T per 64-deep K stage, the even
