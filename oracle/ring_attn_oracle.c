@@ -507,8 +507,13 @@ void oracle_merge(double *o_a, double *lse_a, const double *o_b, const double *l
 
 /* ------------------------------------------------------ blockwise FFN */
 
+/* The standard normal CDF, Phi(x) = (1 + erf(x / sqrt 2)) / 2, written with
+ * erfc so that the tail x << 0 keeps its relative accuracy (1 + erf cancels
+ * to exactly 0 below x = -8.3 in double precision). */
+static double normal_cdf(double x) { return 0.5 * erfc(-x / sqrt(2.0)); }
+
 /* GELU in its exact form, x * Phi(x) with the standard normal CDF Phi. */
-static double gelu(double x) { return 0.5 * x * (1.0 + erf(x / sqrt(2.0))); }
+static double gelu(double x) { return x * normal_cdf(x); }
 
 /* The feed-forward block the BPT section of the pages fuses after attention
  * for each query block ("Large-scale distributed AI model training series:
@@ -575,7 +580,7 @@ int oracle_ffn(const double *x, const double *w1, const double *b1, const double
 
 /* Derivative of the exact GELU: d/dx [x Phi(x)] = Phi(x) + x phi(x). */
 static double gelu_grad(double x) {
-  const double Phi = 0.5 * (1.0 + erf(x / sqrt(2.0)));
+  const double Phi = normal_cdf(x);
   const double phi = exp(-0.5 * x * x) / sqrt(2.0 * acos(-1.0));  /* standard normal density */
   return Phi + x * phi;
 }

@@ -69,6 +69,19 @@ def test_gelu_values():
         assert abs(y[0, 0] - (a + want)) < 1e-13
 
 
+def test_gelu_tail_keeps_relative_accuracy():
+    """Far below zero gelu(a) = a Phi(a) is tiny but not zero: the hidden
+    output matches a 40-digit evaluation of a erfc(-a / sqrt 2) / 2 to 1e-12
+    relative down to a = -30 (where Phi is 5e-198)."""
+    mpmath = pytest.importorskip("mpmath")
+    mpmath.mp.dps = 40
+    for a in (-3.0, -8.0, -8.5, -10.0, -20.0, -30.0):
+        _, h = oracle.ffn(np.array([[a]]), np.array([[1.0]]), np.zeros(1), np.array([[1.0]]), np.zeros(1),
+                          hidden=True)
+        want = float(mpmath.mpf(a) * mpmath.erfc(-mpmath.mpf(a) / mpmath.sqrt(2)) / 2)
+        assert want < 0 and abs(h[0, 0] / want - 1) < 1e-12, (a, h[0, 0], want)
+
+
 def test_hidden_activation_and_row_subsets():
     """The hidden output is gelu(x W1 + b1) (torch fp64, erf GELU) and
     feeds y; a row subset gives exactly those rows of the full result."""

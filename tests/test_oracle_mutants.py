@@ -38,7 +38,8 @@ MUTANTS = {
                           "if (!ring_block(P, t->n_chunks, b, h, i, t->rank, s, o_s, &lse_s, t->striped)) {"),
     "stripes_as_blocks": ("if (striped) return p % N;", "if (striped) return p / (L / N);"),
     "ffn_residual_dropped": ("y[c] = x[c] + acc[c];", "y[c] = acc[c];"),
-    "ffn_gelu_wrong_scale": ("return 0.5 * x * (1.0 + erf(x / sqrt(2.0)));", "return 0.5 * x * (1.0 + erf(x / 2.0));"),
+    "ffn_gelu_wrong_scale": ("return 0.5 * erfc(-x / sqrt(2.0));", "return 0.5 * erfc(-x / 2.0);"),
+    "ffn_cdf_wrong_sign": ("return 0.5 * erfc(-x / sqrt(2.0));", "return 0.5 * erfc(x / sqrt(2.0));"),
     "ffn_gelu_grad_missing_term": ("return Phi + x * phi;", "return Phi;"),
     "ffn_dx_residual_dropped": ("for (int c = 0; c < f->D; ++c) dx[c] = dy[c];", "for (int c = 0; c < f->D; ++c) dx[c] = 0.0;"),
     "transposed_score": ("s[j] = P->scale * dot(qi, k_row(P, b, g, j), P->d);\n    if (s[j] > m) m = s[j];\n  }\n  double sum",
