@@ -108,8 +108,8 @@ FfnBwdWorkspace ffn_bwd_workspace(int D, int F, int R) {
   return w;
 }
 
-// 2-D (as 3-D) map over a bf16 [rows][cols] tensor with 64 x 64 boxes and no
-// swizzle: the transposed outputs of the FFN backward's epilogues.
+// 2-D (as 3-D) map over a bf16 [rows][cols] tensor with 64 x 64 boxes and a
+// 128-byte swizzle: the transposed outputs of the FFN backward's epilogues.
 bool make_map_t(CUtensorMap* m, const void* base, int cols, int rows) {
   auto fn = encode_fn();
   if (!fn) return false;
@@ -118,7 +118,7 @@ bool make_map_t(CUtensorMap* m, const void* base, int cols, int rows) {
   cuuint32_t box[3] = {64u, 64u, 1u};
   cuuint32_t es[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

@@ -5,7 +5,7 @@
 // block, attention, then the FFN and the residual connection; the FFN is
 // the GPT-style pair of linear layers with a 4x up-projection, section 8.)
 // For a block of rows x [R][D]:
-//   h = gelu(x W1 + b1)      [R][F]   (exact GELU, x Phi(x))
+//   h = gelu(x W1 + b1)      [R][F]   (exact GELU, x Phi(x), Phi the normal CDF)
 //   y = x + h W2 + b2        [R][D]
 // Only one block's hidden activation h exists at a time (the BPT memory
 // saving), in a caller-provided buffer reused block after block.
@@ -94,7 +94,41 @@ __device__ __forceinline__ void gemm_drain_wait(uint32_t bar, uint32_t parity, i
   mbar_wait(bar, parity, &local, err, kSiteGemmDrain);
 }
 
-__device__ __forceinline__ float gelu(float x) { return 0.5f * x * (1.f + erff(x * 0.70710678118654752f)); }
+// 16-byte copy global -> shared that bypasses L1 (cp.async, one group per
+// commit); the issuing thread waits for its groups with cp_async_wait_all.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// Phi(a), the standard normal distribution function, for the exact GELU
+// a Phi(a) and its derivative Phi(a) + a phi(a).  From the complementary
+// error function, z = |a| / sqrt 2: Phi(a) = erfc(z) / 2 for a < 0 and
+// 1 - erfc(z) / 2 otherwise, with erfc(z) = t exp(-z^2 + c(t)),
+// t = 1 / (1 + z / 2), c the degree-9 Chebyshev-fitted polynomial of
+// Numerical Recipes in C (2nd ed., section 6.2, erfcc), whose fractional
+// error is below 1.2e-7 for every z >= 0.  Unlike 1 + erf(-z), which cancels
+// in fp32 (to exactly 0 below a = -5.4), the tail a << 0 keeps its
+// relative accuracy.  z2 = a^2 / 2.
+__device__ __forceinline__ float normal_cdf(float a, float z2) {
+  const float z = fabsf(a) * 0.70710678118654752f;
+  const float t = __fdividef(1.f, fmaf(0.5f, z, 1.f));
+  float c = 0.17087277f;
+  c = fmaf(c, t, -0.82215223f);
+  c = fmaf(c, t, 1.48851587f);
+  c = fmaf(c, t, -1.13520398f);
+  c = fmaf(c, t, 0.27886807f);
+  c = fmaf(c, t, -0.18628806f);
+  c = fmaf(c, t, 0.09678418f);
+  c = fmaf(c, t, 0.37409196f);
+  c = fmaf(c, t, 1.00002368f);
+  c = fmaf(c, t, -1.26551223f);
+  const float half_erfc = 0.5f * t * __expf(c - z2);
+  return a < 0.f ? half_erfc : 1.f - half_erfc;
+}
+
+__device__ __forceinline__ float gelu(float x) { return x * normal_cdf(x, 0.5f * x * x); }
 
 // The epilogue of one output tile for the 128 rows this CTA holds (thread =
 // row = tensor-memory lane): accumulator columns [t_acc, t_acc + 256) ->
@@ -105,8 +139,8 @@ __device__ __forceinline__ float gelu(float x) { return 0.5f * x * (1.f + erff(x
 // has been read.  Called by the 128 epilogue threads (named barrier 1).
 template <class Release>
 __device__ __forceinline__ void epilogue_tile(const GemmDev& p, const CUtensorMap* tm_c, uint32_t box0, uint32_t box1,
-                                              uint32_t t_acc, int row, int c_row0, int n0, bool boxes_in_use,
-                                              Release release) {
+                                              uint32_t t_acc, const float* bias_s, int row, int c_row0, int n0,
+                                              bool boxes_in_use, Release release) {
   const int c_row = c_row0 + row;  // this thread's output row
   const bool has_res = (p.kind == 1 || p.kind == 3) && c_row < p.c_end;
   // a box starts on a 128-row boundary of the launch, whose rows end on one
@@ -130,7 +164,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmDev& p, const CUtensorMa
         for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
       } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) + __ldg(p.bias + n0 + col0 + i);
+        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) + bias_s[col0 + i];
       }
       if (p.kind == 0) {
 #pragma unroll
@@ -173,43 +207,47 @@ __device__ __forceinline__ void epilogue_tile(const GemmDev& p, const CUtensorMa
 // of the first layer, kind 2, and da, kind 3 with tm_aux): per quarter of 64
 // columns the normal output is staged in box0 (128-byte swizzle, stored by
 // TMA through tm_c) and the transposed output in box1 as two 64 x 64 tiles
-// [column][row] without swizzle, stored through tm_aux (a map over the
-// transposed tensor [N][rows], box 64 x 64).  Rows at or past c_end go to
-// the transposed output as zeros: they pad the weight-gradient GEMMs' K.
+// [column][row], 128-byte swizzled, stored through tm_aux (a map over the
+// transposed tensor [N][rows], box 64 x 64).  Two neighbouring rows (lanes
+// 2j, 2j+1) swap one value so that each writes one 32-bit pair: the even
+// lane the pair of column c, the odd lane that of column c+1.  Rows at or
+// past c_end go to the transposed output as zeros: they pad the
+// weight-gradient GEMMs' K.
 //   kind 2: a = acc + bias; normal gelu'(a) = Phi(a) + a phi(a), transposed
-//           h = gelu(a) = a Phi(a) (one erf and one exp per element)
+//           h = gelu(a) = a Phi(a) (two exponentials per element)
 //   kind 3: normal and transposed da = acc * gelu'(a) (gelu'(a) from resid)
 template <class Release>
 __device__ __forceinline__ void epilogue_tile_trans(const GemmDev& p, const CUtensorMap* tm_c,
                                                     const CUtensorMap* tm_aux, uint32_t box0, uint32_t box1,
-                                                    uint32_t t_acc, int row, int c_row0, int n0, bool boxes_in_use,
-                                                    Release release) {
+                                                    uint32_t t_acc, const float* bias_s, int row, int c_row0, int n0,
+                                                    bool boxes_in_use, Release release) {
   const int c_row = c_row0 + row;
   const bool live = c_row < p.c_end;
   const bool store = c_row0 < p.c_end;
   const __nv_bfloat16* res_row = (p.kind == 3 && live) ? p.resid + static_cast<size_t>(c_row) * p.N + n0 : nullptr;
-  // this thread's element (column c) of the transposed tile: row c of the
-  // 64 x 64 tile row / 64, position row % 64
-  const uint32_t tbase = box1 + static_cast<uint32_t>(row >> 6) * 8192u + static_cast<uint32_t>(row & 63) * 2u;
+  // this thread's pair of rows in the transposed tile: tile row / 64, byte
+  // offset 2 (row % 64) rounded down to the pair, in 16-byte chunk
+  // (row % 64) / 8 of the tile's 128-byte rows (swizzled by the tile row)
+  const uint32_t tbox = box1 + static_cast<uint32_t>(row >> 6) * 8192u;
+  const uint32_t tchunk = static_cast<uint32_t>(row & 63) >> 3, tin = (static_cast<uint32_t>(row & 7) & ~1u) * 2u;
+  const bool odd = row & 1;
   for (int qtr = 0; qtr < 4; ++qtr) {
-    if (boxes_in_use || qtr > 0) {  // the stores of the previous quarter have read both buffers
-      if (threadIdx.x == 128) bulk_wait_group_read<0>();
-      named_bar_sync(1, 128);
-    }
 #pragma unroll
     for (int h32 = 0; h32 < 2; ++h32) {
       uint32_t r[32];
       const int col0 = qtr * 64 + h32 * 32;
       tmem_ld32(t_acc + col0, r);
+      uint32_t nw[16], tw[16];  // packed bf16 pairs: normal (4 per c8), transposed (4 per c8)
 #pragma unroll
       for (int c8 = 0; c8 < 4; ++c8) {
         float nv[8], tv[8];
         if (p.kind == 2) {
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            const float a = __uint_as_float(r[8 * c8 + i]) + __ldg(p.bias + n0 + col0 + 8 * c8 + i);
-            const float Phi = 0.5f * (1.f + erff(a * 0.70710678118654752f));
-            const float phi = 0.3989422804014327f * __expf(-0.5f * a * a);
+            const float a = __uint_as_float(r[8 * c8 + i]) + bias_s[col0 + 8 * c8 + i];
+            const float z2 = 0.5f * a * a;
+            const float Phi = normal_cdf(a, z2);
+            const float phi = 0.3989422804014327f * __expf(-z2);  // exp(-a^2 / 2) / sqrt(2 pi)
             nv[i] = fmaf(a, phi, Phi);
             tv[i] = a * Phi;
           }
@@ -228,14 +266,30 @@ __device__ __forceinline__ void epilogue_tile_trans(const GemmDev& p, const CUte
 #pragma unroll
           for (int i = 0; i < 8; ++i) nv[i] = tv[i] = __uint_as_float(r[8 * c8 + i]) * gr[i];
         }
-        st_shared_v4(box0 + sw128_offset(row, h32 * 4 + c8), pack_bf16(nv[0], nv[1]), pack_bf16(nv[2], nv[3]),
-                     pack_bf16(nv[4], nv[5]), pack_bf16(nv[6], nv[7]));
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const __nv_bfloat16 t = __float2bfloat16_rn(live ? tv[i] : 0.f);
-          const uint32_t addr = tbase + static_cast<uint32_t>(h32 * 32 + 8 * c8 + i) * 128u;
-          asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(*reinterpret_cast<const uint16_t*>(&t))
-                       : "memory");
+        for (int j = 0; j < 4; ++j) nw[4 * c8 + j] = pack_bf16(nv[2 * j], nv[2 * j + 1]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float a0 = live ? tv[2 * j] : 0.f, a1 = live ? tv[2 * j + 1] : 0.f;
+          // even lane keeps column c and sends c+1, odd lane the reverse
+          const float other = __shfl_xor_sync(0xffffffffu, odd ? a0 : a1, 1);
+          tw[4 * c8 + j] = odd ? pack_bf16(other, a1) : pack_bf16(a0, other);
+        }
+      }
+      // the stores of the previous quarter have read both buffers: waited for
+      // after the first half's arithmetic, which overlaps them
+      if (h32 == 0 && (boxes_in_use || qtr > 0)) {
+        if (threadIdx.x == 128) bulk_wait_group_read<0>();
+        named_bar_sync(1, 128);
+      }
+#pragma unroll
+      for (int c8 = 0; c8 < 4; ++c8) {
+        st_shared_v4(box0 + sw128_offset(row, h32 * 4 + c8), nw[4 * c8], nw[4 * c8 + 1], nw[4 * c8 + 2], nw[4 * c8 + 3]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t c = static_cast<uint32_t>(h32 * 32 + 8 * c8 + 2 * j) + (odd ? 1u : 0u);  // tile row
+          const uint32_t addr = tbox + c * 128u + (((tchunk ^ (c & 7u)) << 4) | tin);
+          asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(tw[4 * c8 + j]) : "memory");
         }
       }
     }
@@ -289,6 +343,7 @@ struct PairSmem {
   alignas(1024) uint8_t a[kPairStages][kPairATile];
   alignas(1024) uint8_t b[kPairStages][kPairBTile];
   alignas(1024) uint8_t c[2][kBM * 64 * 2];
+  alignas(16) float bias[2][kBN];          // kinds 0-2: a tile's bias columns, staged one tile ahead
   alignas(8) uint64_t full[kPairStages];   // even CTA: both CTAs' operand bytes of a stage
   alignas(8) uint64_t empty[kPairStages];  // each CTA: its stage may be refilled
   alignas(8) uint64_t acc_full[2];         // each CTA: accumulator ready
@@ -420,15 +475,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     const int row = (warp & 3) * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t acc_empty0 = mapa_shared(smem_u32(&sm.acc_empty[0]), leader);
+    // kinds 0-2: a tile's 256 bias columns are copied into sm.bias[t & 1] by
+    // the first 64 epilogue threads a whole tile ahead, so that the epilogue
+    // reads them from shared memory instead of waiting on L2 for each group
+    // of columns (the bias pointer is 16-byte aligned, N % 256 == 0)
+    const bool stage_bias = p.kind <= 2;
+    auto fetch_bias = [&](int tt) {
+      if (!stage_bias || tt >= my_tiles || row >= kBN / 4) return;
+      int bm0, bn0;
+      tile_coords(pair + tt * n_pairs, n_m, n_n, p.group_rows, tile_m, bm0, bn0);
+      cp_async_16(smem_u32(&sm.bias[tt & 1][4 * row]), p.bias + bn0 + 4 * row);
+      cp_async_commit();
+    };
     bool ok = true;
+    fetch_bias(0);
     for (int t = 0; t < my_tiles && ok; ++t) {
       int m0, n0;
       tile_coords(pair + t * n_pairs, n_m, n_n, p.group_rows, tile_m, m0, n0);
       const uint32_t acc = t & 1;
+      cp_async_wait_all();  // this thread's copies of tile t's columns; the barrier publishes them
       ok = named_bar_and(1, 128, mbar_wait_cluster(smem_u32(&sm.acc_full[acc]), (t >> 1) & 1, ab, p.err,
                                                    kSiteGemmEpilogue));
       if (!ok) break;
       tc_fence_after();
+      fetch_bias(t + 1);  // every epilogue thread has finished tile t - 1, the last reader of that buffer
+      const float* bias_s = sm.bias[acc];
       auto release = [&] {
         tc_fence_before();
         __syncwarp();
@@ -439,12 +510,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         epilogue_tile_add(p, &tm_c, smem_u32(sm.c[0]), smem_u32(sm.c[1]), tmem + acc * kBN + lane_off, row, c_row0,
                           n0, t > 0, release);
       else if (p.kind == 2 || (p.kind == 3 && p.trans))
-        epilogue_tile_trans(p, &tm_c, &tm_aux, smem_u32(sm.c[0]), smem_u32(sm.c[1]), tmem + acc * kBN + lane_off, row,
-                            c_row0, n0, t > 0, release);
+        epilogue_tile_trans(p, &tm_c, &tm_aux, smem_u32(sm.c[0]), smem_u32(sm.c[1]), tmem + acc * kBN + lane_off,
+                            bias_s, row, c_row0, n0, t > 0, release);
       else
-        epilogue_tile(p, &tm_c, smem_u32(sm.c[0]), smem_u32(sm.c[1]), tmem + acc * kBN + lane_off, row, c_row0, n0,
-                      t > 0, release);
+        epilogue_tile(p, &tm_c, smem_u32(sm.c[0]), smem_u32(sm.c[1]), tmem + acc * kBN + lane_off, bias_s, row,
+                      c_row0, n0, t > 0, release);
     }
+    cp_async_wait_all();  // no copy into this CTA's memory outlives it (a tile ahead, after an abort)
     if (threadIdx.x == 128) bulk_wait_group<0>();
   }
   tc_fence_before();
@@ -536,6 +608,8 @@ cudaError_t launch_ffn_gemm(const FfnGemmArgs& a, cudaStream_t stream) {
   p.resid = static_cast<const __nv_bfloat16*>(a.resid);
   p.err = a.err;
   if (a.pair_clusters <= 0) return cudaErrorInvalidConfiguration;
+  // kinds 0-2 stage the bias by 16-byte copies
+  if (a.kind <= 2 && (!a.bias || (reinterpret_cast<uintptr_t>(a.bias) & 15u))) return cudaErrorInvalidValue;
   const int n_tiles = ((a.M + 2 * kBM - 1) / (2 * kBM)) * (a.N / kBN);
   const int clusters = n_tiles < a.pair_clusters ? n_tiles : a.pair_clusters;
   const size_t smem = sizeof(PairSmem);

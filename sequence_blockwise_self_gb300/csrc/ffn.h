@@ -26,7 +26,7 @@ constexpr int kProfFfnGemm = 8;
 //   kind 3: C = acc * resid   (resid: gelu'(a))       (bf16; with trans, also
 //           transposed through tm_aux)
 // The transposed outputs go to a [N][rows] tensor through tm_aux (64 x 64
-// boxes, no swizzle), rows at or past the launch's end as zeros.
+// boxes, 128-byte swizzle), rows at or past the launch's end as zeros.
 //   kind 4: C += acc                                  (fp32, TMA reduce-add)
 // M rows of C starting at c_row0 are produced from M rows of A starting at
 // a_row0; N % 256 == 0, K % 64 == 0; M is a multiple of 128 unless the rows

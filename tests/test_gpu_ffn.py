@@ -3,15 +3,18 @@ fp64 oracle, within the per-element bound of ffn_tolerance.py (output
 rounding plus the bf16 rounding of the hidden activation carried through
 the second layer).
 """
+import numpy as np
 import pytest
 import torch
 
+import oracle
 import sequence_blockwise_self_gb300 as ra
 from ffn_tolerance import check_ffn as check
 from ffn_tolerance import f64
 from ffn_tolerance import ffn_reference
 from sequence_blockwise_self_gb300 import build as lib_build
 from sequence_blockwise_self_gb300 import inputs
+from tolerance import bf16_half_ulp
 
 pytestmark = pytest.mark.gpu
 
@@ -94,3 +97,33 @@ def test_ffn_full_size_sampled_rows():
     rows = inputs.ffn_sample_rows(w.M, w.block_rows, 96, seed=1)
     want, bound = reference(x, w1, b1, w2, b2, rows=rows)
     check(f64(y[torch.as_tensor(rows).cuda()]), want, bound)
+
+
+def test_ffn_hidden_activation_keeps_relative_accuracy_in_the_gelu_tail():
+    """gelu(a) = a Phi(a) per element, over a in [-9.5, 9.5], against the
+    fp64 oracle within half a bf16 ulp plus 3e-5 relative (the fp32 rounding
+    of a and of the exponentials): the tail a << 0, where Phi(a) falls to
+    1e-19, must keep its relative accuracy (1 + erf(a / sqrt 2) cancels to 0
+    in fp32 below a = -5.4).  Each row of x has one nonzero entry, so every
+    first-layer sum is one exact bf16 product and a = fp32(product + b1);
+    b1 sweeps the range.  On return the workspace holds the last block's h."""
+    M, D, F = 256, 256, 1024
+    g = torch.Generator().manual_seed(11)
+    x = torch.zeros((M, D))
+    x[torch.arange(M), torch.arange(M) % D] = (torch.rand(M, generator=g) - 0.5).to(torch.bfloat16).float()
+    x = x.to(torch.bfloat16)
+    w1 = (torch.rand((F, D), generator=g) - 0.5).to(torch.bfloat16)
+    b1 = torch.linspace(-9.0, 9.0, F, dtype=torch.float32)
+    w2 = torch.zeros((D, F), dtype=torch.bfloat16)
+    b2 = torch.zeros(D, dtype=torch.float32)
+    ws = torch.zeros(ra.ffn_workspace_size(D, F, M), dtype=torch.uint8, device="cuda")
+    ra.ring_attn_ffn_fwd(*(t.cuda() for t in (x, w1, b1, w2, b2)), block_rows=M, workspace=ws)
+    torch.cuda.synchronize()
+    assert ra.device_status()[0] == 0
+    h = f64(ws[:M * F * 2].view(torch.bfloat16).view(M, F))
+    _, want = oracle.ffn(f64(x), f64(w1).T.copy(), f64(b1), f64(w2).T.copy(), f64(b2), hidden=True)
+    assert np.any((want < 0) & (want > -1e-17)) and want.max() > 9.0   # the range is covered, tail included
+    bound = bf16_half_ulp(np.maximum(np.abs(want), np.abs(h))) + 3e-5 * np.abs(want)
+    err = np.abs(h - want)
+    worst = np.unravel_index(np.argmax(err / np.maximum(bound, 1e-300)), err.shape)
+    assert np.all(err <= bound), f"h at {worst}: {h[worst]:.6e} against {want[worst]:.6e}"
