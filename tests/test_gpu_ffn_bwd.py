@@ -92,3 +92,31 @@ def test_ffn_backward_zero_second_layer():
                                                   dy.cuda(), block_rows=128)
     assert torch.equal(dx.cpu(), dy)
     assert not dw1.any() and not db1.any()
+
+
+def test_ffn_backward_at_the_benchmark_width_sampled_rows():
+    """The benchmark's FFN width (D = 3584, F = 14336, blocks of 8192 rows)
+    over two blocks: dx on sampled rows (block and tile edges included)
+    against the oracle, which a row's dx depends on alone, with the bound of
+    the small cases; db2 against the fp64 column sums of dy over every row;
+    the weight gradients finite."""
+    wl = inputs.FFN_WORKLOADS["ffn_gqa_128k"]
+    R, D, F = wl.block_rows, wl.D, wl.F
+    M = 2 * R
+    x, w1, b1, w2, _ = inputs.make_ffn_inputs(M, D, F, seed=95)
+    dy = torch.randn((M, D), generator=torch.Generator().manual_seed(96)).to(torch.bfloat16)
+    dx, dw1, db1, dw2, db2 = ra.ring_attn_ffn_bwd(*(t.cuda() for t in (x, w1, b1, w2, dy)), block_rows=R)
+    torch.cuda.synchronize()
+    assert ra.device_status()[0] == 0
+    for name, t in (("dw1", dw1), ("db1", db1), ("dw2", dw2)):
+        assert torch.isfinite(t).all(), name
+
+    rows = np.asarray(inputs.ffn_sample_rows(M, R, 40, seed=95))
+    idx = torch.as_tensor(rows)
+    W1, W2 = f64(w1).T.copy(), f64(w2).T.copy()
+    rdx, _, _, _, _, _, da = oracle.ffn_bwd(f64(x[idx]), W1, f64(b1), W2, f64(dy[idx]), hidden=True)
+    w1o = f64(w1)
+    check("dx", f64(dx.cpu()[idx]), rdx,
+          bf16_half_ulp(rdx) + 6 * U * math.sqrt(2) * np.sqrt((da * da) @ (w1o * w1o)) + 1e-4)
+    rdb2 = f64(dy).sum(axis=0)
+    check("db2", f64(db2), rdb2, 1e-4 * max(1.0, np.abs(rdb2).max()) + np.zeros_like(rdb2))
