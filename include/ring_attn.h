@@ -276,9 +276,12 @@ int ring_attn_selftest_bounded_wait(unsigned timeout_us, cudaStream_t stream);
  * connection are computed for that block; section 8: the FFN is two linear
  * layers around an up-projection to F = 4 D in the GPT-style model).  For
  * every row x_m of x (a token's hidden state):
- *   y_m = x_m + W2 gelu(W1 x_m + b1) + b2,   gelu(t) = t Phi(t) (exact erf)
+ *   y_m = x_m + W2 gelu(W1 x_m + b1) + b2,   gelu(t) = t Phi(t)
+ * (the exact GELU, Phi the standard normal CDF, evaluated with relative
+ * accuracy in the tail t << 0).
  * The rows are processed in blocks of block_rows rows; only one block's
- * hidden activation (block_rows x F) exists at a time, in the workspace.
+ * hidden activation (block_rows x F) exists at a time, in the workspace:
+ * on return it holds the last block's, bf16 [rows of that block][F].
  *   x, y : bf16 [M][D]     (y may be x: the update is then in place)
  *   w1   : bf16 [F][D]     (W1, output-major: row f holds the weights of
  *                           hidden unit f, the layout of a linear layer's

@@ -108,9 +108,9 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 // 1 - erfc(z) / 2 otherwise, with erfc(z) = t exp(-z^2 + c(t)),
 // t = 1 / (1 + z / 2), c the degree-9 Chebyshev-fitted polynomial of
 // Numerical Recipes in C (2nd ed., section 6.2, erfcc), whose fractional
-// error is below 1.2e-7 for every z >= 0.  Unlike 1 + erf(-z), which cancels
-// in fp32 (to exactly 0 below a = -5.4), the tail a << 0 keeps its
-// relative accuracy.  z2 = a^2 / 2.
+// error is below 1.2e-7 for every z >= 0.  Unlike (1 + erf(a / sqrt 2)) / 2,
+// which cancels in fp32 (to exactly 0 below a = -5.4), the tail a << 0
+// keeps its relative accuracy.  z2 = a^2 / 2.
 __device__ __forceinline__ float normal_cdf(float a, float z2) {
   const float z = fabsf(a) * 0.70710678118654752f;
   const float t = __fdividef(1.f, fmaf(0.5f, z, 1.f));

@@ -10,8 +10,8 @@ block in fp64 from the same bf16 values.  Per element of y:
     a bf16 ulp (2^-8 |h_f|), roughly uniformly, so the error of y_d has
     standard deviation at most 2^-8 / sqrt(3) * sqrt(sum_f (h_f W2_fd)^2);
     six of those are allowed;
-  * fp32 accumulation and erff: 1e-4 absolute (several orders below the
-    terms above at these sizes).
+  * fp32 accumulation and the GELU evaluation (Phi to 1.2e-7 relative):
+    1e-4 absolute (several orders below the terms above at these sizes).
 On top, the errors must be typical, not bunched near their bounds: the
 mean-abs error stays within a quarter of the mean bound (a faithful
 computation lands near one sixth of it: one standard deviation plus a
