@@ -91,3 +91,27 @@ def test_ffn_bwd_and_bpt_bwd_arguments(lib):
     assert g(*bptrs, 1, 2, 1, 1024, 128, 4, 1, 1024, 128, P256, wsb, NUL) == capi.ERR_UNSUPPORTED
     assert g(*([NUL] * 16), 1, 2, 1, 1024, 128, 4, 1, 1024, 256, P256, wsb, NUL) == capi.ERR_NULL
     assert g(*bptrs, 1, 2, 1, 1024, 128, 4, 1, 1024, 256, P256, wsb - 1, NUL) == capi.ERR_WORKSPACE
+
+
+def test_every_pointer_must_be_16_byte_aligned(lib):
+    """The kernels read every operand with 16-byte accesses (TMA boxes, and
+    the biases by 16-byte copies into shared memory), so each pointer of the
+    FFN and BPT entries that is not 16-byte aligned is refused before any
+    device work."""
+    ws = lib.ring_attn_ffn_bwd_workspace_size(256, 512, 128)
+    for i in range(10):
+        args = [P256] * 10
+        args[i] = P8
+        assert lib.ring_attn_ffn_bwd(*args, 100, 256, 512, 128, P256, ws, NUL) == capi.ERR_UNSUPPORTED, i
+    ws = lib.ring_attn_bpt_workspace_size(2, 128, 1024, 256)
+    for i in range(10):
+        args = [P256] * 10
+        args[i] = P8
+        assert lib.ring_attn_bpt_fwd(*args, 1, 2, 1, 1024, 128, 4, 1, 1024, 256, P256, ws, NUL) == \
+            capi.ERR_UNSUPPORTED, i
+    wsb = lib.ring_attn_bpt_bwd_workspace_size(1, 2, 1, 1024, 128, 4, 1, 1024, 256)
+    for i in range(16):
+        args = [P256] * 16
+        args[i] = P8
+        assert lib.ring_attn_bpt_bwd(*args, 1, 2, 1, 1024, 128, 4, 1, 1024, 256, P256, wsb, NUL) == \
+            capi.ERR_UNSUPPORTED, i
