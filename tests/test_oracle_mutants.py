@@ -42,6 +42,12 @@ MUTANTS = {
     "ffn_cdf_wrong_sign": ("return 0.5 * erfc(-x / sqrt(2.0));", "return 0.5 * erfc(x / sqrt(2.0));"),
     "ffn_gelu_grad_missing_term": ("return Phi + x * phi;", "return Phi;"),
     "ffn_dx_residual_dropped": ("for (int c = 0; c < f->D; ++c) dx[c] = dy[c];", "for (int c = 0; c < f->D; ++c) dx[c] = 0.0;"),
+    "ffn_dw2_wrong_operand": ("for (int c = 0; c < f->D; ++c) dw2[c] += hm * dy[c];",
+                              "for (int c = 0; c < f->D; ++c) dw2[c] += hm * x[c];"),
+    "ffn_dw1_uses_h": ("f->dw1[(size_t)c * f->F + j] += x[c] * dam;", "f->dw1[(size_t)c * f->F + j] += x[c] * hm;"),
+    "ffn_db1_sums_h": ("db1 += dam;", "db1 += hm;"),
+    "ffn_da_uses_gelu": ("da[j] = dh * gelu_grad(a);", "da[j] = dh * gelu(a);"),
+    "ffn_dx_transposed_w1": ("dx[c] += da[j] * w[(size_t)c * f->F + j];", "dx[c] += da[j] * w[(size_t)j * f->D + c];"),
     "transposed_score": ("s[j] = P->scale * dot(qi, k_row(P, b, g, j), P->d);\n    if (s[j] > m) m = s[j];\n  }\n  double sum",
                          "s[j] = P->scale * dot(q_row(P, b, h, j), k_row(P, b, g, i), P->d);\n    if (s[j] > m) m = s[j];\n  }\n  double sum"),
 }
