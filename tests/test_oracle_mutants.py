@@ -48,6 +48,9 @@ MUTANTS = {
     "ffn_db1_sums_h": ("db1 += dam;", "db1 += hm;"),
     "ffn_da_uses_gelu": ("da[j] = dh * gelu_grad(a);", "da[j] = dh * gelu(a);"),
     "ffn_dx_transposed_w1": ("dx[c] += da[j] * w[(size_t)c * f->F + j];", "dx[c] += da[j] * w[(size_t)j * f->D + c];"),
+    "rows_stats_start_late": ("lo[bh] = causal ? kmin : 0;", "lo[bh] = causal ? kmin + 1 : 0;"),
+    "rows_dq_wrong_row": ("dq_row(P, b, h, t->rows[ri], lse, D, t->dq + ((size_t)bh * t->n_rows + ri) * P->d);",
+                          "dq_row(P, b, h, t->rows[ri], lse, D, t->dq + ((size_t)bh * t->n_rows + (t->n_rows - 1 - ri)) * P->d);"),
     "transposed_score": ("s[j] = P->scale * dot(qi, k_row(P, b, g, j), P->d);\n    if (s[j] > m) m = s[j];\n  }\n  double sum",
                          "s[j] = P->scale * dot(q_row(P, b, h, j), k_row(P, b, g, i), P->d);\n    if (s[j] > m) m = s[j];\n  }\n  double sum"),
 }
@@ -70,6 +73,7 @@ def _quick_pins():
         ("stripes", lambda: steps.test_striped_step_with_zero_queries_closed_form(3)),
         ("ffn", lambda: [ffn_pins.test_ffn_matches_torch(7, 16, 64), ffn_pins.test_gelu_values()]),
         ("ffn_bwd", lambda: ffn_pins.test_ffn_backward_matches_torch_autograd(5, 8, 24)),
+        ("rows", lambda: [pins.test_row_sampled_routines_agree_with_full(c) for c in (False, True)]),
     ]
     failed = []
     for name, fn in checks:
