@@ -61,3 +61,26 @@ def test_cpulist_parsing():
     assert bench._cpulist("0-3,8,10-11\n") == {0, 1, 2, 3, 8, 10, 11}
     assert bench._cpulist("5") == {5}
     assert bench._cpulist("") == set()
+
+
+def test_reference_arm_prints_one_contract_line(monkeypatch, capsys):
+    """Rank 0 of the reference arm times the oracle and prints one JSON line
+    with the keys the benchmark contract names (and no device traffic)."""
+    import argparse
+    import json
+
+    from sequence_blockwise_self_gb300 import inputs
+
+    monkeypatch.delenv("RANK", raising=False)
+    bench.run_reference(argparse.Namespace(gpus=1, steps=1, warmup=0), inputs.WORKLOADS["tiny"])
+    lines = [ln for ln in capsys.readouterr().out.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["value"] > 0 and d["higher_is_better"] is True
+    assert d["config"]["workload"].startswith("tiny")
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
