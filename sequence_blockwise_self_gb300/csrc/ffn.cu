@@ -132,8 +132,10 @@ __device__ __forceinline__ float gelu(float x) { return x * normal_cdf(x, 0.5f *
 
 // The epilogue of one output tile for the 128 rows this CTA holds (thread =
 // row = tensor-memory lane): accumulator columns [t_acc, t_acc + 256) ->
-// + bias, then GELU (kind 0) or + residual (kind 1) -> bf16 into two
-// 64-column staging boxes in turn -> TMA stores of 128 x 64.  c_row0 is the
+// + bias (bias_s: the tile's 256 columns, staged in shared memory), then
+// GELU (kind 0) or + residual (kind 1); or, kind 3 without the transposed
+// output, times gelu'(a) -> bf16 into two 64-column staging boxes in turn
+// -> TMA stores of 128 x 64.  c_row0 is the
 // C row of lane 0; boxes_in_use says whether stores of an earlier tile may
 // still be reading the boxes.  release() runs once every accumulator column
 // has been read.  Called by the 128 epilogue threads (named barrier 1).
