@@ -46,8 +46,22 @@
  *     lse <- log(exp(lse) + exp(lse_s)),
  *     o   <- exp(lse_old - lse) * o + exp(lse_s - lse) * o_s.
  *
+ *   Blockwise feed-forward of the BPT layer (section 4.2: per query block,
+ *   attention, then the FFN and the residual; section 8: two linear layers
+ *   around a 4x up-projection).  Per row x_m (rows are independent, so the
+ *   blockwise order does not change the result):
+ *
+ *     y_m = x_m + W2^T gelu(W1^T x_m + b1) + b2,  gelu(t) = t Phi(t),
+ *     Phi(t) = erfc(-t / sqrt 2) / 2  (the standard normal CDF)
+ *
+ *   and its backward for the loss sum(dy * y) by the chain rule, with the
+ *   hidden activation recomputed (oracle_ffn_bwd).  Pinned by torch's fp64
+ *   autograd, central differences, closed forms (W2 = 0) and a 40-digit
+ *   evaluation of the GELU tail.
+ *
  * Layout: q, o, dO, dq are [B][Hq][L][d]; k, v, dk, dv are [B][Hkv][L][d];
- * lse and D are [B][Hq][L]; all contiguous, row-major.
+ * lse and D are [B][Hq][L]; all contiguous, row-major.  FFN: x, y, dy, dx
+ * [M][D], W1 [D][F], W2 [F][D].
  *
  * Parallelism: plain pthreads over independent rows; no blocking, fusion
  * or reordering of the arithmetic of one row.
