@@ -66,36 +66,31 @@ def workload_inputs(w: Workload, seed=None, with_grad=True):
     return make_inputs(w.B, w.Hq, w.Hkv, w.L, w.d, s, with_grad)
 
 
-def boundary_rows(L: int, n_chunks: int, causal: bool):
+def boundary_rows(L: int, n_chunks: int, causal: bool, lo: int = 0):
     """First and last row of every chunk (encoder) or sub-chunk (causal, 2N
-    sub-chunks of length L/(2N)), plus rows 0 and L-1."""
+    sub-chunks of length L/(2N)), plus rows lo and L-1; only rows >= lo."""
     parts = 2 * n_chunks if causal else n_chunks
     c = L // parts
-    rows = {0, L - 1}
+    rows = {lo, L - 1}
     for i in range(parts):
         rows.add(i * c)
         rows.add(min(L - 1, (i + 1) * c - 1))
-    return rows
+    return {r for r in rows if r >= lo}
 
 
-def sample_rows(L: int, n_chunks: int, causal: bool, n: int, seed: int):
-    """Sorted sample of n distinct query rows: all chunk boundary rows, then
-    uniform draws without replacement from numpy's default_rng(seed + 1000)."""
-    rows = boundary_rows(L, n_chunks, causal)
-    if len(rows) >= n or n >= L:
-        base = sorted(rows) if n < L else list(range(L))
-        return np.array(base[:max(n, len(rows))] if n < L else base, dtype=np.int32)
+def sample_rows(L: int, n_chunks: int, causal: bool, n: int, seed: int, lo: int = 0):
+    """Sorted sample of n distinct rows of [lo, L): all chunk boundary rows
+    in that range, then uniform draws without replacement from numpy's
+    default_rng(seed + 1000)."""
+    rows = boundary_rows(L, n_chunks, causal, lo)
+    span = L - lo
+    if len(rows) >= n or n >= span:
+        base = sorted(rows) if n < span else list(range(lo, L))
+        return np.array(base[:max(n, len(rows))] if n < span else base, dtype=np.int32)
     rng = np.random.default_rng(seed + 1000)
-    rest = np.setdiff1d(np.arange(L), np.array(sorted(rows)))
+    rest = np.setdiff1d(np.arange(lo, L), np.array(sorted(rows)))
     extra = rng.choice(rest, size=n - len(rows), replace=False)
     return np.array(sorted(rows | set(int(x) for x in extra)), dtype=np.int32)
-
-
-def tail_rows(L: int, n: int):
-    """The last n rows: for a causal model a key row j is seen only by
-    queries i >= j, so the fp64 statistics needed for its gradient stay cheap."""
-    n = min(n, L)
-    return np.arange(L - n, L, dtype=np.int32)
 
 
 # ---------------------------------------------------------------- blockwise FFN

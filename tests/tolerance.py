@@ -8,10 +8,31 @@ a unit in the last place, 2^(e-8): 0.0156 for values in [4, 8) and more than
 excess of that unavoidable output rounding (of the reference value, or of the
 larger of two compared bf16 results); the mean-abs bound is applied to the raw
 error.
+
+Every check records its raw max-abs error beside the error beyond output
+rounding (RESULTS); the test session prints them as a summary.
 """
+import os
+
 import numpy as np
 
 TOL_MAX, TOL_MEAN, TOL_LSE = 2e-2, 2e-3, 1e-3
+
+# (name, raw max-abs, max-abs beyond output rounding, mean-abs, tol_max, tol_mean)
+RESULTS = []
+
+
+NOTES = []
+
+
+def note(msg):
+    """A line for the session summary (e.g. how long the fp64 oracle took)."""
+    NOTES.append(msg)
+
+
+def _record(name, raw, excess, mean, tol_max, tol_mean):
+    test = os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0]
+    RESULTS.append((f"{test}::{name}" if test else name, raw, excess, mean, tol_max, tol_mean))
 
 
 def bf16_half_ulp(x):
@@ -29,6 +50,8 @@ def check_bf16(name, got, want, tol_max=TOL_MAX, tol_mean=TOL_MEAN, ulps=1):
     assert np.all(np.isfinite(got)), f"{name}: non-finite values"
     err = np.abs(got - want)
     excess = np.maximum(err - ulps * bf16_half_ulp(np.maximum(np.abs(want), np.abs(got))), 0.0)
+    if err.size:
+        _record(name, float(err.max()), float(excess.max()), float(err.mean()), tol_max, tol_mean)
     assert excess.max() <= tol_max and err.mean() <= tol_mean, (
         f"{name}: max-abs {err.max():.3e}, beyond bf16 output rounding {excess.max():.3e} (tol {tol_max}), "
         f"mean-abs {err.mean():.3e} (tol {tol_mean})")
@@ -39,4 +62,6 @@ def check_fp32(name, got, want, tol=TOL_LSE):
     want = np.asarray(want, dtype=np.float64)
     assert np.all(np.isfinite(got)), f"{name}: non-finite values"
     err = np.abs(got - want)
+    if err.size:
+        _record(name, float(err.max()), float(err.max()), float(err.mean()), tol, tol)
     assert err.max() <= tol, f"{name}: max-abs {err.max():.3e} (tol {tol})"
