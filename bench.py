@@ -475,22 +475,22 @@ def run_ours(args, w):
     # log-sum-exp merge), on this GPU; its merge kernel is HBM-bound
     ring = None
     if not args.no_ring_mode:
-        def measure_ring(striped):
+        def measure_ring(schedule):
             o_r = torch.empty_like(qd)
             lse_r = torch.empty_like(lse)
-            ws_r = torch.empty(ra.ring_fwd_workspace_size(w.B, w.Hq, w.Hkv, w.L, w.d, w.n_chunks, w.causal, striped),
-                               dtype=torch.uint8, device=dev)
+            ws_r = torch.empty(ra.ring_fwd_workspace_size(w.B, w.Hq, w.Hkv, w.L, w.d, w.n_chunks, w.causal,
+                                                          schedule=schedule), dtype=torch.uint8, device=dev)
 
             def ring_fwd():
                 ra.ring_attn_ring_fwd(qd, kd, vd, w.n_chunks, w.causal, o=o_r, lse=lse_r, workspace=ws_r,
-                                      stream=stream, striped=striped)
-            ws_b = torch.empty(ra.ring_bwd_workspace_size(w.B, w.Hq, w.Hkv, w.L, w.d, w.n_chunks, w.causal, striped),
-                               dtype=torch.uint8, device=dev)
+                                      stream=stream, schedule=schedule)
+            ws_b = torch.empty(ra.ring_bwd_workspace_size(w.B, w.Hq, w.Hkv, w.L, w.d, w.n_chunks, w.causal,
+                                                          schedule=schedule), dtype=torch.uint8, device=dev)
             g_r = [torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)]
 
             def ring_bwd():
                 ra.ring_attn_ring_bwd(qd, kd, vd, o_r, lse_r, dOd, w.n_chunks, w.causal, dq=g_r[0], dk=g_r[1],
-                                      dv=g_r[2], workspace=ws_b, stream=stream, striped=striped)
+                                      dv=g_r[2], workspace=ws_b, stream=stream, schedule=schedule)
             ring_fwd()
             ring_bwd()
             torch.cuda.synchronize(dev)
@@ -518,9 +518,17 @@ def run_ours(args, w):
             if st != 0:
                 raise RuntimeError(f"device status {st} at site {site:#x} in ring mode")
             merge_ms, merge_n = rp["ring_merge"]
-            rows = w.B * w.Hq * w.L
-            merge_bytes = rows * (3 * w.d * 4 + 3 * 4)  # read o, o_s, lse, lse_s; write o, lse
-            merge_gbs = merge_bytes / (merge_ms / merge_n * 1e-3) / 1e9 if merge_n else None
+            # rows merged per forward: every row at each launch after the first
+            # (ring steps); DistFlashAttention: chunks t..N-1 and, unless t is
+            # the middle launch, the t chunks the idle workers helped
+            N = w.n_chunks
+            chunk_rows = w.B * w.Hq * (w.L // N)
+            if schedule == "dfa":
+                merged_rows = sum((N - t) + (t if t < N - t else 0) for t in range(1, N // 2 + 1)) * chunk_rows
+            else:
+                merged_rows = (N - 1) * N * chunk_rows
+            merge_bytes = merged_rows * (3 * w.d * 4 + 3 * 4)  # read o, o_s, lse, lse_s; write o, lse
+            merge_gbs = merge_bytes / (merge_ms / args.steps * 1e-3) / 1e9 if merge_n else None
             del ws_b, g_r
             return {
                 "fwd_ms": ms_ring, "fwd_tflops": F / (ms_ring * 1e-3) / 1e12,
@@ -530,15 +538,18 @@ def run_ours(args, w):
                 "launches_per_fwd": {k: rp[k][1] // args.steps for k in ("ring_step", "ring_merge", "ring_io")},
                 "merge_roofline": {"bound": "hbm", "achieved": merge_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                    "frac": (merge_gbs / peaks["hbm_gbs"]) if merge_gbs else None,
-                                   "bytes_per_launch": merge_bytes},
+                                   "bytes_per_fwd": merge_bytes},
             }
 
         C = w.L // w.n_chunks
         ring = {}
         if (w.L // (2 * w.n_chunks) if w.causal else C) % 128 == 0 and (not w.causal or w.L % (2 * w.n_chunks) == 0):
-            ring["fold" if w.causal else "chunks"] = measure_ring(False)
+            ring["fold" if w.causal else "chunks"] = measure_ring("fold")
         if w.causal and w.L % w.n_chunks == 0 and C % 128 == 0:
-            ring["striped"] = measure_ring(True)
+            # the other causal schedules: stripes, the plain contiguous ring and
+            # DistFlashAttention's balanced one (N/2 + 1 launches)
+            for sched in ("striped", "contiguous", "dfa"):
+                ring[sched] = measure_ring(sched)
         ring = ring or None
 
     # (5) Ulysses on this GPU at the largest degree the heads allow (<= 8):

@@ -113,22 +113,53 @@ int ring_attn_bwd_noalloc(const void* q, const void* k, const void* v, const voi
  * query chunk while the key/value blocks travel round the ring; section 6.2
  * Ring Attention: each step's partial result is merged into the running one
  * with the online-softmax correction).  Rank r holds chunk r of the
- * sequence, in chunk order: rows [rC, (r+1)C), C = L / n_chunks, when
- * causal == 0; sub-chunk r followed by sub-chunk 2N-1-r, each L/(2N) rows,
- * when causal != 0 (the fold that balances causal work, section 8.2); with
- * striped != 0, the positions r, r+N, r+2N, ... (striped attention, the
- * causal schedule variant the pages compare with the fold; it needs only
- * L % N == 0).  Chunks must be whole 128-row tiles -- C (causal == 0 or
- * striped) or L/(2N) (the fold) a multiple of 128 -- else
- * RING_ATTN_ERR_UNSUPPORTED.  Pointers are device
+ * sequence, in chunk order, C = L / n_chunks rows; `schedule` picks the
+ * chunk map and the order of the blocks:
+ *   RING_ATTN_SCHEDULE_FOLD (0): rows [rC, (r+1)C) when causal == 0;
+ *     sub-chunk r followed by sub-chunk 2N-1-r, each L/(2N) rows, when
+ *     causal != 0 (the fold that balances causal work, section 8.2).
+ *     N ring steps: at step s rank r holds the keys of rank (r - s) mod N.
+ *   RING_ATTN_SCHEDULE_STRIPED (1): positions r, r+N, r+2N, ... (striped
+ *     attention, the causal schedule variant the pages compare with the
+ *     fold; L % N == 0 suffices); N ring steps.
+ *   RING_ATTN_SCHEDULE_CONTIGUOUS (2): causal only, rows [rC, (r+1)C); N
+ *     ring steps -- the unbalanced ring (rank r has work only at steps
+ *     s <= r) of section 7.2.
+ *   RING_ATTN_SCHEDULE_DISTFLASH (3): causal only, rows [rC, (r+1)C);
+ *     DistFlashAttention's balanced schedule (section 7.2: a worker that
+ *     would wait takes over a later worker's block), N/2 + 1 launches:
+ *     at launch t worker w >= t runs block (query chunk w, keys of chunk
+ *     w - t) and worker w < t block (N - t + w, w), the block of ring step
+ *     N - t, unless t == N - t (then it is idle); see
+ *     ring_attn_schedule_pair.
+ * Chunks must be whole 128-row tiles -- C, or L/(2N) for the causal fold,
+ * a multiple of 128 -- else RING_ATTN_ERR_UNSUPPORTED.  Pointers are device
  * pointers, 16-byte aligned and owned by the caller; calls are asynchronous
  * on `stream`; argument errors return before anything is launched.
  * ------------------------------------------------------------------- */
+enum {
+  RING_ATTN_SCHEDULE_FOLD = 0,
+  RING_ATTN_SCHEDULE_STRIPED = 1,
+  RING_ATTN_SCHEDULE_CONTIGUOUS = 2,
+  RING_ATTN_SCHEDULE_DISTFLASH = 3
+};
+
+/* Host-only: launches of one pass of the schedule (N, or N/2 + 1 for
+ * RING_ATTN_SCHEDULE_DISTFLASH), or a negative code. */
+int ring_attn_schedule_launches(int n_chunks, int schedule);
+
+/* Host-only: the block worker `worker` runs at launch `launch` of the
+ * schedule: *q_chunk (whose queries) and *kv_chunk (whose keys/values).
+ * Returns 1 if the worker has a block, 0 if it is idle at that launch, or a
+ * negative code. */
+int ring_attn_schedule_pair(int n_chunks, int schedule, int launch, int worker, int* q_chunk, int* kv_chunk);
 
 /*
- * One ring step of rank `rank`: the attention of its query chunk against the
- * key/value chunk of rank `src` (the block it holds at step (rank - src) mod
- * n_chunks), with the causal mask taken on the rows' sequence positions.
+ * One block: the attention of rank `rank`'s query chunk against the
+ * key/value chunk of rank `src` (the block rank holds at ring step
+ * (rank - src) mod n_chunks), with the causal mask taken on the rows'
+ * sequence positions under the schedule's chunk map (the two contiguous
+ * schedules share one).
  *   q_chunk           bf16 [B][Hq][C][d]    rank's query rows, chunk order
  *   k_chunk, v_chunk  bf16 [B][Hkv][C][d]   src's key/value rows, chunk order
  *   o_s               fp32 [B][Hq][C][d]    out: the partial result, normalised
@@ -138,7 +169,7 @@ int ring_attn_bwd_noalloc(const void* q, const void* k, const void* v, const voi
  *                                           gets lse_s = -inf and o_s = 0
  */
 int ring_attn_fwd_step(const void* q_chunk, const void* k_chunk, const void* v_chunk, float* o_s, float* lse_s,
-                       int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal, int striped, int rank, int src,
+                       int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal, int schedule, int rank, int src,
                        cudaStream_t stream);
 
 /*
@@ -153,21 +184,23 @@ int ring_attn_merge(float* o, float* lse, const float* o_s, const float* lse_s, 
 
 /* Workspace bytes ring_attn_ring_fwd needs for this shape, or 0 if invalid. */
 size_t ring_attn_ring_fwd_workspace_size(int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal,
-                                         int striped);
+                                         int schedule);
 
 /*
- * The whole ring on one GPU, every rank of it, the ring-mode way: q, k, v
+ * The whole ring on one GPU, every worker of it, the ring-mode way: q, k, v
  * (sequence order, as for ring_attn_fwd) are gathered into chunk order; at
- * each step s = 0..n_chunks-1 one launch runs every rank's step (rank r
- * against rank (r - s) mod n_chunks) and the merge folds it into the running
- * fp32 result; the result is scattered back to sequence order into o (bf16)
- * and lse (fp32), as ring_attn_fwd writes them.  `workspace` (caller-owned
- * device memory of ring_attn_ring_fwd_workspace_size() bytes, 256-byte
- * aligned) holds the gathered chunks, the running result and one step's
- * partial result.
+ * each launch of the schedule one kernel launch runs every worker's block
+ * (ring steps: worker r against chunk (r - s) mod n_chunks) and merges fold
+ * each worker's partial result into the running fp32 result of the block's
+ * query chunk (DistFlashAttention: two merges per launch, the workers' own
+ * chunks and the chunks they helped); the result is scattered back to
+ * sequence order into o (bf16) and lse (fp32), as ring_attn_fwd writes
+ * them.  `workspace` (caller-owned device memory of
+ * ring_attn_ring_fwd_workspace_size() bytes, 256-byte aligned) holds the
+ * gathered chunks, the running result and one launch's partial results.
  */
 int ring_attn_ring_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
-                       int L, int d, int n_chunks, int causal, int striped, void* workspace, size_t workspace_bytes,
+                       int L, int d, int n_chunks, int causal, int schedule, void* workspace, size_t workspace_bytes,
                        cudaStream_t stream);
 
 /* ---------------------------------------------------------------------
@@ -229,16 +262,16 @@ int ring_attn_usp_bwd(const void* q, const void* k, const void* v, const void* o
 
 /* Workspace bytes ring_attn_ring_bwd needs for this shape, or 0 if invalid. */
 size_t ring_attn_ring_bwd_workspace_size(int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal,
-                                         int striped);
+                                         int schedule);
 
 /*
  * The backward of ring_attn_ring_fwd, the ring-mode way (the same results
  * as ring_attn_bwd; o and lse from either forward): q, k, v, o, dO, lse are
  * gathered into chunk order; the statistics of every rank's rows are formed
- * once; at each step s = 0..n_chunks-1 one launch runs, for every rank r,
- * the tiles of the key/value chunk it holds (rank (r - s) mod n_chunks)
- * against its query chunk, adding into rank r's fp32 dQ accumulator and
- * into the source chunk's fp32 dK, dV accumulators (the gradients that in a
+ * once; at each launch of the schedule one kernel launch runs, for every
+ * worker, the tiles of its block's key/value chunk against the block's
+ * query chunk, adding into that query chunk's fp32 dQ accumulator and
+ * into the key/value chunk's fp32 dK, dV accumulators (the gradients that in a
  * multi-GPU ring travel with K and V back to their owner); the gradients
  * are scattered back to sequence order as bf16.  `workspace`: caller-owned
  * device memory of ring_attn_ring_bwd_workspace_size() bytes, 256-byte
@@ -246,7 +279,7 @@ size_t ring_attn_ring_bwd_workspace_size(int B, int Hq, int Hkv, int L, int d, i
  */
 int ring_attn_ring_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
                        void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal,
-                       int striped, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+                       int schedule, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* Static description of a status code. */
 const char* ring_attn_strerror(int status);
@@ -436,15 +469,15 @@ int ring_attn_bwd_plan(int L, int n_chunks, int causal, int* n_blocks, int* n_ra
                        int32_t* range_offsets, int32_t* ranges);
 
 /*
- * Ring-mode step plan of rank `rank` at ring step `step` (it then holds the
- * key/value chunk of rank (rank - step) mod n_chunks): for each 256-row
- * block of the rank's chunk (chunk-order rows), the 128-row tiles of the
- * source chunk (chunk-order indices, ascending) holding a key some row of
- * the block may see; a block may list none.  Same array conventions as
- * ring_attn_fwd_plan, with n_blocks = blocks of one chunk.  Chunks must be
- * whole 128-row tiles (see ring mode above).
+ * Ring-mode plan of worker `rank` at launch `step` of the schedule (its
+ * block: ring_attn_schedule_pair): for each 256-row block of the block's
+ * query chunk (chunk-order rows), the 128-row tiles of its key/value chunk
+ * (chunk-order indices, ascending) holding a key some row of the block may
+ * see; a block may list none (and an idle worker lists none).  Same array
+ * conventions as ring_attn_fwd_plan, with n_blocks = blocks of one chunk.
+ * Chunks must be whole 128-row tiles (see ring mode above).
  */
-int ring_attn_step_plan(int L, int n_chunks, int causal, int striped, int step, int rank, int* n_blocks,
+int ring_attn_step_plan(int L, int n_chunks, int causal, int schedule, int step, int rank, int* n_blocks,
                         int* n_ranges, int32_t* block_order, int32_t* range_offsets, int32_t* ranges);
 
 #ifdef __cplusplus

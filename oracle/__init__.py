@@ -18,5 +18,7 @@ from .oracle import (  # noqa: F401
     ffn_bwd,
     owner_rank,
     ring_sources,
+    dfa_schedule,
+    SCHEDULES,
     visible_pairs,
 )

@@ -10,6 +10,9 @@ series: sequence parallelism" (the "SP series") and its sections:
     ring, N-1 transfers and N block computations per device;
   * section 6.2 (Ring Attention): one ring carries K and V together and the
     per-step partial results are merged with the online-softmax correction;
+  * section 7.2 (DistFlashAttention): with contiguous causal chunks the
+    ring is unbalanced; a worker that would wait takes over blocks of a
+    later worker (8 steps become 5 in the pages' example);
   * section 8.2 (USP): for a causal model the sequence is split by folding
     it, so that every device gets the same amount of work.
 
@@ -185,31 +188,54 @@ def bwd_rows(q, k, v, dO, causal: bool, q_rows, k_rows, threads: int = 0):
     return dq, dk, dv
 
 
-def ring_fwd(q, k, v, causal: bool, n_chunks: int, threads: int = 0, striped: bool = False):
+# Ring schedules (the oracle's SCHED_* codes): the chunk map and the order
+# of the blocks.  "fold": contiguous chunks (encoder) or the folded
+# sub-chunks {r, 2N-1-r} (causal, SP series section 8.2), N ring steps;
+# "striped": rank r owns positions r, r+N, ...; "contiguous": causal with
+# contiguous chunks, the plain (unbalanced) ring; "dfa": causal with
+# contiguous chunks in DistFlashAttention's balanced schedule (section 7.2,
+# see dfa_schedule).
+SCHEDULES = {"fold": 0, "striped": 1, "contiguous": 2, "dfa": 3}
+
+
+def _schedule(striped, schedule):
+    if schedule is None:
+        return SCHEDULES["striped" if striped else "fold"]
+    if striped and schedule != "striped":
+        raise ValueError("striped contradicts the schedule")
+    return SCHEDULES[schedule]
+
+
+def ring_fwd(q, k, v, causal: bool, n_chunks: int, threads: int = 0, striped: bool = False, schedule=None):
     """Ring form: per ring step partial (o_s, lse_s) merged by log-sum-exp
     (SP series sections 2.3 and 6.2; causal ranks own folded sub-chunks,
-    section 8.2, or, with striped, the positions r, r+N, r+2N, ...)."""
+    section 8.2, or, with striped, the positions r, r+N, r+2N, ...; or
+    contiguous chunks in ring order or DistFlashAttention's order, section
+    7.2, with schedule="contiguous" / "dfa")."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, Hq, Hkv, L, d = _shape(q, k)
     o = np.zeros((B, Hq, L, d))
     lse = np.zeros((B, Hq, L))
     _check(_load().oracle_ring_fwd(_p(q), _p(k), _p(v), B, Hq, Hkv, L, d, int(causal), int(n_chunks),
-                                   int(bool(striped)), _p(o), _p(lse), _threads(threads)))
+                                   _schedule(striped, schedule), _p(o), _p(lse), _threads(threads)))
     return o, lse
 
 
-def ring_step(q, k, v, causal: bool, n_chunks: int, rank: int, src: int, threads: int = 0, striped: bool = False):
+def ring_step(q, k, v, causal: bool, n_chunks: int, rank: int, src: int, threads: int = 0, striped: bool = False,
+              schedule=None):
     """One ring step in isolation (SP series sections 2.3 and 6.2): the
     partial result (o_s, lse_s) of rank `rank`'s query rows against the keys
     and values of rank `src`.  Returned in global row order, [B,Hq,L,d] and
     [B,Hq,L]; rows of other ranks are 0 and -inf, as are rows of `rank` that
-    see none of src's keys.  striped: rank r owns positions r, r+N, ..."""
+    see none of src's keys.  striped: rank r owns positions r, r+N, ...;
+    schedule "contiguous" or "dfa": contiguous causal chunks."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, Hq, Hkv, L, d = _shape(q, k)
     o = np.zeros((B, Hq, L, d))
     lse = np.full((B, Hq, L), -np.inf)
     _check(_load().oracle_ring_step(_p(q), _p(k), _p(v), B, Hq, Hkv, L, d, int(causal), int(n_chunks),
-                                    int(rank), int(src), int(bool(striped)), _p(o), _p(lse), _threads(threads)))
+                                    int(rank), int(src), _schedule(striped, schedule), _p(o), _p(lse),
+                                    _threads(threads)))
     return o, lse
 
 
@@ -279,14 +305,35 @@ def ffn_bwd(x, w1, b1, w2, dy, threads: int = 0, hidden: bool = False):
 
 # ------------------------------------------------------------ chunk map (host)
 
-def owner_rank(L: int, n_chunks: int, causal: bool, p: int, striped: bool = False) -> int:
-    """Rank owning sequence position p: chunk p // (L/N) for the encoder;
-    for causal the folded pair {r, 2N-1-r} of sub-chunks of length L/(2N)
-    (SP series section 8.2); p mod N when striped."""
-    r = _load().oracle_owner_rank(int(L), int(n_chunks), int(causal), int(bool(striped)), int(p))
+def owner_rank(L: int, n_chunks: int, causal: bool, p: int, striped: bool = False, schedule=None) -> int:
+    """Rank owning sequence position p: chunk p // (L/N) for the encoder
+    and the contiguous causal schedules; for the causal fold the pair
+    {r, 2N-1-r} of sub-chunks of length L/(2N) (SP series section 8.2);
+    p mod N when striped."""
+    r = _load().oracle_owner_rank(int(L), int(n_chunks), int(causal), _schedule(striped, schedule), int(p))
     if r < 0:
         raise ValueError("bad chunk map arguments")
     return r
+
+
+def dfa_schedule(n_chunks: int):
+    """DistFlashAttention's balanced causal schedule (SP series section 7.2:
+    a worker that would wait in the plain ring takes over a later worker's
+    block).  Returns one list per launch t = 0..N//2 of (worker, query
+    chunk, key/value chunk): worker w >= t does its own block (w, w - t);
+    worker w < t the block (N - t + w, w) of ring step N - t, unless that
+    step is this launch (N even, t = N/2), when it stays idle."""
+    N = int(n_chunks)
+    out = []
+    for t in range(N // 2 + 1):
+        launch = []
+        for w in range(N):
+            if w >= t:
+                launch.append((w, w, w - t))
+            elif t < N - t:
+                launch.append((w, N - t + w, w))
+        out.append(launch)
+    return out
 
 
 def ring_sources(r: int, n_chunks: int):

@@ -41,7 +41,10 @@
  *   log-sum-exp rule (the online-softmax correction of section 6.2).  With
  *   the striped assignment (a causal schedule variant the pages compare
  *   with the fold: rank r owns positions r, r+N, r+2N, ...), every rank's
- *   chunk spreads over the whole sequence instead:
+ *   chunk spreads over the whole sequence instead; with contiguous causal
+ *   chunks, either the plain ring or DistFlashAttention's balanced schedule
+ *   (section 7.2: a worker that would wait takes over a later worker's
+ *   block; see dfa_pair) orders the blocks.  The merge:
  *
  *     lse <- log(exp(lse) + exp(lse_s)),
  *     o   <- exp(lse_old - lse) * o + exp(lse_s - lse) * o_s.
@@ -138,7 +141,7 @@ struct task_s {
   double *o, *lse, *D, *dq, *dk, *dv;
   int n_chunks;
   int rank, src;      /* ring step mode: query rank and key/value source rank */
-  int striped;        /* ring forms: striped assignment instead of chunks/fold */
+  int schedule;       /* ring forms: chunk map and step order (SCHED_*) */
   const int *stat_lo; /* per (b,h): first query row whose stats exist (rows mode) */
 };
 
@@ -380,33 +383,71 @@ int oracle_bwd_rows(const double *q, const double *k, const double *v, const dou
 
 /* --------------------------------------------------------------- ring form */
 
-/* Rank that owns sequence position p: contiguous chunks (encoder), the
- * fold (causal), or stripes (p mod N) when `striped`. */
-static int owner_rank(int L, int N, int causal, int striped, int p) {
-  if (striped) return p % N;
-  if (!causal) return p / (L / N);
+/* Ring schedules: which rows each rank owns, and which key/value chunk it
+ * works on at each step.
+ *   SCHED_FOLD     contiguous chunks (encoder) or, causal, the fold of the
+ *                  USP section 8.2; N ring steps, step s pairs rank r with
+ *                  the keys of rank (r - s) mod N.
+ *   SCHED_STRIPED  rank r owns positions r, r+N, r+2N, ...; ring steps.
+ *   SCHED_CONTIG   causal, contiguous chunks, ring steps: the unbalanced
+ *                  ring of the DistFlashAttention section 7.2 (rank r has
+ *                  work only at steps s <= r).
+ *   SCHED_DFA      causal, contiguous chunks, DistFlashAttention's balanced
+ *                  schedule (section 7.2: a worker that would wait takes
+ *                  over work of a later worker): see dfa_pair. */
+enum { SCHED_FOLD = 0, SCHED_STRIPED = 1, SCHED_CONTIG = 2, SCHED_DFA = 3 };
+
+/* Rank that owns sequence position p under the schedule's chunk map. */
+static int owner_rank(int L, int N, int causal, int schedule, int p) {
+  if (schedule == SCHED_STRIPED) return p % N;
+  if (!causal || schedule != SCHED_FOLD) return p / (L / N);
   const int sub = p / (L / (2 * N));
   return sub < N ? sub : 2 * N - 1 - sub;
 }
 
-/* Chunk map valid for this length: L % N == 0 (encoder, striped) or
- * L % 2N == 0 (fold). */
-static int bad_chunking(int L, int n_chunks, int causal, int striped) {
-  if (n_chunks <= 0) return 1;
-  return L % ((causal && !striped) ? 2 * n_chunks : n_chunks) != 0;
+/* Chunk map valid for this length: L % 2N == 0 for the fold, L % N == 0
+ * otherwise; the contiguous causal schedules need causal. */
+static int bad_chunking(int L, int n_chunks, int causal, int schedule) {
+  if (n_chunks <= 0 || schedule < SCHED_FOLD || schedule > SCHED_DFA) return 1;
+  if (schedule >= SCHED_CONTIG && !causal) return 1;
+  return L % ((causal && schedule == SCHED_FOLD) ? 2 * n_chunks : n_chunks) != 0;
+}
+
+/* DistFlashAttention's balanced schedule for N workers (section 7.2).  In
+ * the plain causal ring, worker w (query chunk w) has work at step s only if
+ * s <= w (keys of chunk w - s); the others wait.  Here, at launch t = 0, 1,
+ * ..., N/2 (rounded down), worker w >= t computes its own block (query chunk
+ * w, keys of chunk w - t), and a worker w < t, which would wait, computes a
+ * block of the step N - t instead: query chunk N - t + w against its own
+ * keys, chunk w (the block worker N - t + w would meet at step N - t).  The
+ * step N - t is then never run on its own.  When N is even the middle launch
+ * t = N/2 has no such block (step N - t is that launch itself), and its
+ * workers w < N/2 stay idle.  Returns 0 for an idle worker. */
+static int dfa_pair(int N, int t, int w, int *q_chunk, int *kv_chunk) {
+  if (w >= t) {
+    *q_chunk = w;
+    *kv_chunk = w - t;
+    return 1;
+  }
+  if (t < N - t) {
+    *q_chunk = N - t + w;
+    *kv_chunk = w;
+    return 1;
+  }
+  return 0;
 }
 
 /* Partial attention of query row i against the keys of rank src that i may
  * see.  Returns 0 if there is none; otherwise writes (o_s, lse_s). */
 static int ring_block(const problem_t *P, int N, int b, int h, int i, int src, double *s, double *o_s,
-                      double *lse_s, int striped) {
+                      double *lse_s, int schedule) {
   const int g = h / (P->Hq / P->Hkv);
   const double *qi = q_row(P, b, h, i);
   double m = -INFINITY;
   int cnt = 0;
   for (int j = 0; j < P->L; ++j) {
     s[j] = -INFINITY;
-    if (owner_rank(P->L, N, P->causal, striped, j) != src) continue;
+    if (owner_rank(P->L, N, P->causal, schedule, j) != src) continue;
     if (P->causal && j > i) continue;
     s[j] = P->scale * dot(qi, k_row(P, b, g, j), P->d);
     if (s[j] > m) m = s[j];
@@ -426,26 +467,41 @@ static int ring_block(const problem_t *P, int N, int b, int h, int i, int src, d
   return 1;
 }
 
+/* Merge the partial result of row i against the keys of rank src into the
+ * running (o, lse) by the log-sum-exp rule; nothing if i sees none of them. */
+static void ring_merge_block(const problem_t *P, int N, int b, int h, int i, int src, double *s, double *o_s,
+                             int schedule, double *o, double *lse) {
+  double lse_s;
+  if (!ring_block(P, N, b, h, i, src, s, o_s, &lse_s, schedule)) return;
+  const double hi = *lse > lse_s ? *lse : lse_s;
+  const double merged = hi + log(exp(*lse - hi) + exp(lse_s - hi));
+  const double a = exp(*lse - merged), w = exp(lse_s - merged);
+  for (int c = 0; c < P->d; ++c) o[c] = a * o[c] + w * o_s[c];
+  *lse = merged;
+}
+
 static void ring_item(task_t *t, long item, double *s) {
   const problem_t *P = t->P;
   const int N = t->n_chunks;
   const int i = (int)(item % P->L);
   const long bh = item / P->L;
   const int h = (int)(bh % P->Hq), b = (int)(bh / P->Hq);
-  const int r = owner_rank(P->L, N, P->causal, t->striped, i);
+  const int r = owner_rank(P->L, N, P->causal, t->schedule, i);
   double *o_s = s + P->L;
   double *o = t->o + ((size_t)bh * P->L + i) * P->d;
   double lse = -INFINITY;
   for (int c = 0; c < P->d; ++c) o[c] = 0.0;
-  for (int step = 0; step < N; ++step) {
-    const int src = ((r - step) % N + N) % N;
-    double lse_s;
-    if (!ring_block(P, N, b, h, i, src, s, o_s, &lse_s, t->striped)) continue;
-    const double hi = lse > lse_s ? lse : lse_s;
-    const double merged = hi + log(exp(lse - hi) + exp(lse_s - hi));
-    const double a = exp(lse - merged), w = exp(lse_s - merged);
-    for (int c = 0; c < P->d; ++c) o[c] = a * o[c] + w * o_s[c];
-    lse = merged;
+  if (t->schedule == SCHED_DFA) {
+    /* every block of each launch whose query chunk is r, in worker order */
+    for (int launch = 0; launch <= N / 2; ++launch)
+      for (int w = 0; w < N; ++w) {
+        int qc, kc;
+        if (dfa_pair(N, launch, w, &qc, &kc) && qc == r) ring_merge_block(P, N, b, h, i, kc, s, o_s, t->schedule, o, &lse);
+      }
+  } else {
+    /* ring step s brings the keys of rank (r - s) mod N */
+    for (int step = 0; step < N; ++step)
+      ring_merge_block(P, N, b, h, i, ((r - step) % N + N) % N, s, o_s, t->schedule, o, &lse);
   }
   t->lse[(size_t)bh * P->L + i] = lse;
 }
@@ -453,12 +509,12 @@ static void ring_item(task_t *t, long item, double *s) {
 /* Ring form of the forward with n_chunks ranks.  Requires L % n_chunks == 0
  * (encoder) or L % (2 n_chunks) == 0 (causal, folded sub-chunks). */
 int oracle_ring_fwd(const double *q, const double *k, const double *v, int B, int Hq, int Hkv, int L,
-                    int d, int causal, int n_chunks, int striped, double *o, double *lse, int n_threads) {
-  if (bad_shape(B, Hq, Hkv, L, d) || bad_chunking(L, n_chunks, causal, striped)) return -1;
+                    int d, int causal, int n_chunks, int schedule, double *o, double *lse, int n_threads) {
+  if (bad_shape(B, Hq, Hkv, L, d) || bad_chunking(L, n_chunks, causal, schedule)) return -1;
   problem_t P = make_problem(q, k, v, NULL, B, Hq, Hkv, L, d, causal);
   task_t t; memset(&t, 0, sizeof t);
   t.P = &P; t.n_items = (long)B * Hq * L; t.fn = ring_item; t.scratch_len = (size_t)L + d;
-  t.o = o; t.lse = lse; t.n_chunks = n_chunks; t.striped = striped;
+  t.o = o; t.lse = lse; t.n_chunks = n_chunks; t.schedule = schedule;
   return run_parallel(&t, n_threads);
 }
 
@@ -472,10 +528,10 @@ static void step_item(task_t *t, long item, double *s) {
   const int i = (int)(item % P->L);
   const long bh = item / P->L;
   const int h = (int)(bh % P->Hq), b = (int)(bh / P->Hq);
-  if (owner_rank(P->L, t->n_chunks, P->causal, t->striped, i) != t->rank) return;
+  if (owner_rank(P->L, t->n_chunks, P->causal, t->schedule, i) != t->rank) return;
   double *o_s = t->o + ((size_t)bh * P->L + i) * P->d;
   double lse_s;
-  if (!ring_block(P, t->n_chunks, b, h, i, t->src, s, o_s, &lse_s, t->striped)) {
+  if (!ring_block(P, t->n_chunks, b, h, i, t->src, s, o_s, &lse_s, t->schedule)) {
     for (int c = 0; c < P->d; ++c) o_s[c] = 0.0;
     lse_s = -INFINITY;
   }
@@ -483,14 +539,14 @@ static void step_item(task_t *t, long item, double *s) {
 }
 
 int oracle_ring_step(const double *q, const double *k, const double *v, int B, int Hq, int Hkv, int L, int d,
-                     int causal, int n_chunks, int rank, int src, int striped, double *o_s, double *lse_s,
+                     int causal, int n_chunks, int rank, int src, int schedule, double *o_s, double *lse_s,
                      int n_threads) {
-  if (bad_shape(B, Hq, Hkv, L, d) || bad_chunking(L, n_chunks, causal, striped)) return -1;
+  if (bad_shape(B, Hq, Hkv, L, d) || bad_chunking(L, n_chunks, causal, schedule)) return -1;
   if (rank < 0 || rank >= n_chunks || src < 0 || src >= n_chunks) return -1;
   problem_t P = make_problem(q, k, v, NULL, B, Hq, Hkv, L, d, causal);
   task_t t; memset(&t, 0, sizeof t);
   t.P = &P; t.n_items = (long)B * Hq * L; t.fn = step_item; t.scratch_len = (size_t)L;
-  t.o = o_s; t.lse = lse_s; t.n_chunks = n_chunks; t.rank = rank; t.src = src; t.striped = striped;
+  t.o = o_s; t.lse = lse_s; t.n_chunks = n_chunks; t.rank = rank; t.src = src; t.schedule = schedule;
   return run_parallel(&t, n_threads);
 }
 
@@ -705,7 +761,7 @@ int oracle_ffn_bwd(const double *x, const double *w1, const double *b1, const do
   return n_threads;
 }
 
-int oracle_owner_rank(int L, int n_chunks, int causal, int striped, int p) {
-  if (p < 0 || p >= L || bad_chunking(L, n_chunks, causal, striped)) return -1;
-  return owner_rank(L, n_chunks, causal, striped, p);
+int oracle_owner_rank(int L, int n_chunks, int causal, int schedule, int p) {
+  if (p < 0 || p >= L || bad_chunking(L, n_chunks, causal, schedule)) return -1;
+  return owner_rank(L, n_chunks, causal, schedule, p);
 }

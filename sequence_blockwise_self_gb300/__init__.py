@@ -28,6 +28,9 @@ from .capi import (  # noqa: F401
     release,
     selftest_bounded_wait,
     step_plan,
+    schedule_launches,
+    schedule_pairs,
+    SCHEDULES,
     ring_attn_bwd,
     ring_attn_bwd_noalloc,
     ring_attn_fwd,

@@ -73,6 +73,10 @@ def load():
         f.restype = I
     lib.ring_attn_step_plan.argtypes = [I, I, I, I, I, I, IP, IP, I32P, I32P, I32P]
     lib.ring_attn_step_plan.restype = I
+    lib.ring_attn_schedule_launches.argtypes = [I, I]
+    lib.ring_attn_schedule_launches.restype = I
+    lib.ring_attn_schedule_pair.argtypes = [I, I, I, I, IP, IP]
+    lib.ring_attn_schedule_pair.restype = I
     lib.ring_attn_fwd_step.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, P]
     lib.ring_attn_fwd_step.restype = I
     lib.ring_attn_merge.argtypes = [P, P, P, P, ctypes.c_longlong, I, P, P]
@@ -145,11 +149,53 @@ def _plan(fn, L, n_chunks, causal):
     return {"order": order, "offsets": offsets, "ranges": ranges, "visits": visits}
 
 
-def step_plan(L: int, n_chunks: int, causal: bool, step: int, rank: int, striped: bool = False):
-    """Ring mode: per 256-row block of rank's chunk, the source chunk's tile
-    ranges it visits at this step (chunk-local indices)."""
+# Ring-mode schedules (RING_ATTN_SCHEDULE_* of include/ring_attn.h): the
+# chunk map and the order of the blocks.
+SCHEDULES = {"fold": 0, "striped": 1, "contiguous": 2, "dfa": 3}
+
+
+def schedule_code(striped: bool = False, schedule=None) -> int:
+    """The C ABI's schedule code: `schedule` by name, else fold or striped."""
+    if schedule is None:
+        return SCHEDULES["striped" if striped else "fold"]
+    if striped and schedule != "striped":
+        raise ValueError("striped contradicts the schedule")
+    return SCHEDULES[schedule]
+
+
+def schedule_launches(n_chunks: int, schedule="fold") -> int:
+    rc = load().ring_attn_schedule_launches(int(n_chunks), schedule_code(schedule=schedule))
+    if rc < 0:
+        raise RingAttnError(rc, "ring_attn_schedule_launches")
+    return rc
+
+
+def schedule_pairs(n_chunks: int, schedule="fold"):
+    """Per launch, the (worker, query chunk, key/value chunk) blocks of the
+    schedule (idle workers left out)."""
+    lib = load()
+    code = schedule_code(schedule=schedule)
+    out = []
+    for t in range(schedule_launches(n_chunks, schedule)):
+        launch = []
+        for w in range(int(n_chunks)):
+            a, b = ctypes.c_int(0), ctypes.c_int(0)
+            rc = lib.ring_attn_schedule_pair(int(n_chunks), code, t, w, ctypes.byref(a), ctypes.byref(b))
+            if rc < 0:
+                raise RingAttnError(rc, "ring_attn_schedule_pair")
+            if rc == 1:
+                launch.append((w, a.value, b.value))
+        out.append(launch)
+    return out
+
+
+def step_plan(L: int, n_chunks: int, causal: bool, step: int, rank: int, striped: bool = False, schedule=None):
+    """Ring mode: per 256-row block of the query chunk of worker `rank`'s
+    block at launch `step`, the key/value chunk's tile ranges it visits
+    (chunk-local indices)."""
     fn = load().ring_attn_step_plan
-    return _plan(lambda L_, N_, c_, *rest: fn(L_, N_, c_, int(bool(striped)), int(step), int(rank), *rest),
+    code = schedule_code(striped, schedule)
+    return _plan(lambda L_, N_, c_, *rest: fn(L_, N_, c_, code, int(step), int(rank), *rest),
                  L, n_chunks, causal)
 
 
@@ -212,7 +258,7 @@ def ring_attn_fwd(q, k, v, n_chunks: int, causal: bool, o=None, lse=None, stream
 # ------------------------------------------------------------------ ring mode
 
 def ring_attn_fwd_step(q_chunk, k_chunk, v_chunk, n_chunks: int, causal: bool, rank: int, src: int, o_s=None,
-                       lse_s=None, stream=None, striped: bool = False):
+                       lse_s=None, stream=None, striped: bool = False, schedule=None):
     """One ring step of rank `rank` against the key/value chunk of rank `src`
     (chunks in chunk order, see include/ring_attn.h); returns the fp32
     partial result (o_s [B,Hq,C,d], lse_s [B,Hq,C])."""
@@ -227,8 +273,8 @@ def ring_attn_fwd_step(q_chunk, k_chunk, v_chunk, n_chunks: int, causal: bool, r
     _check_tensor(o_s, "o_s", torch.float32, (B, Hq, C, d))
     _check_tensor(lse_s, "lse_s", torch.float32, (B, Hq, C))
     rc = load().ring_attn_fwd_step(_ptr(q_chunk), _ptr(k_chunk), _ptr(v_chunk), _ptr(o_s), _ptr(lse_s), B, Hq, Hkv,
-                                   C * int(n_chunks), d, int(n_chunks), int(bool(causal)), int(bool(striped)),
-                                   int(rank), int(src), _stream(stream))
+                                   C * int(n_chunks), d, int(n_chunks), int(bool(causal)),
+                                   schedule_code(striped, schedule), int(rank), int(src), _stream(stream))
     if rc != OK:
         raise RingAttnError(rc, "ring_attn_fwd_step")
     return o_s, lse_s
@@ -252,13 +298,13 @@ def ring_attn_merge(o, lse, o_s, lse_s, o_out=None, stream=None):
     return o, lse
 
 
-def ring_fwd_workspace_size(B, Hq, Hkv, L, d, n_chunks, causal, striped: bool = False) -> int:
+def ring_fwd_workspace_size(B, Hq, Hkv, L, d, n_chunks, causal, striped: bool = False, schedule=None) -> int:
     return int(load().ring_attn_ring_fwd_workspace_size(B, Hq, Hkv, L, d, int(n_chunks), int(bool(causal)),
-                                                         int(bool(striped))))
+                                                         schedule_code(striped, schedule)))
 
 
 def ring_attn_ring_fwd(q, k, v, n_chunks: int, causal: bool, o=None, lse=None, workspace=None, stream=None,
-                       striped: bool = False):
+                       striped: bool = False, schedule=None):
     """The forward of ring_attn_fwd computed the ring-mode way (every rank's
     steps as separate launches, merged step by step); returns (o, lse)."""
     import torch
@@ -271,24 +317,24 @@ def ring_attn_ring_fwd(q, k, v, n_chunks: int, causal: bool, o=None, lse=None, w
     lse = torch.empty((B, Hq, L), dtype=torch.float32, device=q.device) if lse is None else lse
     _check_tensor(o, "o", torch.bfloat16, (B, Hq, L, d))
     _check_tensor(lse, "lse", torch.float32, (B, Hq, L))
-    ws_bytes = ring_fwd_workspace_size(B, Hq, Hkv, L, d, n_chunks, causal, striped)
+    ws_bytes = ring_fwd_workspace_size(B, Hq, Hkv, L, d, n_chunks, causal, striped, schedule)
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
     rc = load().ring_attn_ring_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, L, d, int(n_chunks),
-                                   int(bool(causal)), int(bool(striped)), _ptr(workspace),
+                                   int(bool(causal)), schedule_code(striped, schedule), _ptr(workspace),
                                    int(workspace.numel() * workspace.element_size()), _stream(stream))
     if rc != OK:
         raise RingAttnError(rc, "ring_attn_ring_fwd")
     return o, lse
 
 
-def ring_bwd_workspace_size(B, Hq, Hkv, L, d, n_chunks, causal, striped: bool = False) -> int:
+def ring_bwd_workspace_size(B, Hq, Hkv, L, d, n_chunks, causal, striped: bool = False, schedule=None) -> int:
     return int(load().ring_attn_ring_bwd_workspace_size(B, Hq, Hkv, L, d, int(n_chunks), int(bool(causal)),
-                                                         int(bool(striped))))
+                                                         schedule_code(striped, schedule)))
 
 
 def ring_attn_ring_bwd(q, k, v, o, lse, dO, n_chunks: int, causal: bool, dq=None, dk=None, dv=None, workspace=None,
-                       stream=None, striped: bool = False):
+                       stream=None, striped: bool = False, schedule=None):
     """The backward computed the ring-mode way (every rank's steps as
     separate launches); returns (dq, dk, dv)."""
     import torch
@@ -302,10 +348,11 @@ def ring_attn_ring_bwd(q, k, v, o, lse, dO, n_chunks: int, causal: bool, dq=None
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     if workspace is None:
-        workspace = torch.empty(max(ring_bwd_workspace_size(B, Hq, Hkv, L, d, n_chunks, causal, striped), 1),
+        workspace = torch.empty(max(ring_bwd_workspace_size(B, Hq, Hkv, L, d, n_chunks, causal, striped, schedule), 1),
                                 dtype=torch.uint8, device=q.device)
     rc = load().ring_attn_ring_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk),
-                                   _ptr(dv), B, Hq, Hkv, L, d, int(n_chunks), int(bool(causal)), int(bool(striped)),
+                                   _ptr(dv), B, Hq, Hkv, L, d, int(n_chunks), int(bool(causal)),
+                                   schedule_code(striped, schedule),
                                    _ptr(workspace), int(workspace.numel() * workspace.element_size()),
                                    _stream(stream))
     if rc != OK:
@@ -465,9 +512,11 @@ def ffn_bwd_workspace_size(D: int, F: int, block_rows: int) -> int:
     return int(load().ring_attn_ffn_bwd_workspace_size(int(D), int(F), int(block_rows)))
 
 
-def ring_attn_ffn_bwd(x, w1, b1, w2, dy, block_rows: int = 8192, workspace=None, stream=None):
+def ring_attn_ffn_bwd(x, w1, b1, w2, dy, block_rows: int = 8192, workspace=None, stream=None, dx=None, dw1=None,
+                      db1=None, dw2=None, db2=None):
     """Backward of ring_attn_ffn_fwd for the loss sum(dy * y): returns
-    (dx [M, D] bf16, dw1 [F, D], db1 [F], dw2 [D, F], db2 [D] fp32)."""
+    (dx [M, D] bf16, dw1 [F, D], db1 [F], dw2 [D, F], db2 [D] fp32); the
+    outputs are allocated unless passed in."""
     import torch
     M, D = x.shape
     F = w1.shape[0]
@@ -477,11 +526,14 @@ def ring_attn_ffn_bwd(x, w1, b1, w2, dy, block_rows: int = 8192, workspace=None,
     _check_tensor(b1, "b1", torch.float32, (F,))
     _check_tensor(dy, "dy", torch.bfloat16, (M, D))
     dev = x.device
-    dx = torch.empty_like(x)
-    dw1 = torch.empty((F, D), dtype=torch.float32, device=dev)
-    db1 = torch.empty((F,), dtype=torch.float32, device=dev)
-    dw2 = torch.empty((D, F), dtype=torch.float32, device=dev)
-    db2 = torch.empty((D,), dtype=torch.float32, device=dev)
+    dx = torch.empty_like(x) if dx is None else dx
+    dw1 = torch.empty((F, D), dtype=torch.float32, device=dev) if dw1 is None else dw1
+    db1 = torch.empty((F,), dtype=torch.float32, device=dev) if db1 is None else db1
+    dw2 = torch.empty((D, F), dtype=torch.float32, device=dev) if dw2 is None else dw2
+    db2 = torch.empty((D,), dtype=torch.float32, device=dev) if db2 is None else db2
+    _check_tensor(dx, "dx", torch.bfloat16, (M, D))
+    for t, n, sh in ((dw1, "dw1", (F, D)), (db1, "db1", (F,)), (dw2, "dw2", (D, F)), (db2, "db2", (D,))):
+        _check_tensor(t, n, torch.float32, sh)
     if workspace is None:
         workspace = torch.empty(max(ffn_bwd_workspace_size(D, F, block_rows), 1), dtype=torch.uint8, device=dev)
     rc = load().ring_attn_ffn_bwd(_ptr(x), _ptr(w1), _ptr(b1), _ptr(w2), _ptr(dy), _ptr(dx), _ptr(dw1), _ptr(db1),
@@ -538,9 +590,10 @@ def bpt_bwd_workspace_size(B, Hq, Hkv, L, d, n_chunks, causal, F, block_rows) ->
 
 
 def ring_attn_bpt_bwd(q, k, v, a_tok, lse, w1, b1, w2, dy, n_chunks: int, causal: bool, block_rows: int = 8192,
-                      workspace=None, stream=None):
+                      workspace=None, stream=None, outs=None):
     """Backward of ring_attn_bpt_fwd for the loss sum(dy * y), dy [B, L, Hq*d]
-    bf16: returns (dq, dk, dv, dw1, db1, dw2, db2)."""
+    bf16: returns (dq, dk, dv, dw1, db1, dw2, db2), allocated unless `outs`
+    passes all seven."""
     import torch
     B, Hq, L, d = q.shape
     Hkv = k.shape[1]
@@ -555,11 +608,18 @@ def ring_attn_bpt_bwd(q, k, v, a_tok, lse, w1, b1, w2, dy, n_chunks: int, causal
     _check_tensor(b1, "b1", torch.float32, (F,))
     _check_tensor(dy, "dy", torch.bfloat16, (B, L, D))
     dev = q.device
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    dw1 = torch.empty((F, D), dtype=torch.float32, device=dev)
-    db1 = torch.empty((F,), dtype=torch.float32, device=dev)
-    dw2 = torch.empty((D, F), dtype=torch.float32, device=dev)
-    db2 = torch.empty((D,), dtype=torch.float32, device=dev)
+    if outs is None:
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        dw1 = torch.empty((F, D), dtype=torch.float32, device=dev)
+        db1 = torch.empty((F,), dtype=torch.float32, device=dev)
+        dw2 = torch.empty((D, F), dtype=torch.float32, device=dev)
+        db2 = torch.empty((D,), dtype=torch.float32, device=dev)
+    else:
+        dq, dk, dv, dw1, db1, dw2, db2 = outs
+    for t, n, sh in ((dq, "dq", (B, Hq, L, d)), (dk, "dk", (B, Hkv, L, d)), (dv, "dv", (B, Hkv, L, d))):
+        _check_tensor(t, n, torch.bfloat16, sh)
+    for t, n, sh in ((dw1, "dw1", (F, D)), (db1, "db1", (F,)), (dw2, "dw2", (D, F)), (db2, "db2", (D,))):
+        _check_tensor(t, n, torch.float32, sh)
     if workspace is None:
         workspace = torch.empty(max(bpt_bwd_workspace_size(B, Hq, Hkv, L, d, n_chunks, causal, F, block_rows), 1),
                                 dtype=torch.uint8, device=dev)

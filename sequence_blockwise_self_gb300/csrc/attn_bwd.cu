@@ -131,11 +131,12 @@ struct BwdDev {
   __nv_bfloat16* dv;
   int* err;
   // Ring step mode (step_nt > 0): item k is key/value tile k % step_nt of
-  // the chunk rank r = k / step_nt holds at ring step `step` (rank (r - step)
-  // mod n_chunks), against rank r's query chunk; L = Lpad = the chunk
-  // length; slices: q, dO, statistics, dQ at r * B*Hq + (b, h), k, v, dK, dV
-  // at src * B*Hkv + (b, kv head); causal keys from the fold or stripes.
-  int step_nt, step, n_chunks, striped;
+  // the block of worker w = k / step_nt at launch `step` of schedule `sched`
+  // (schedule_pair: query chunk a, key/value chunk b), against a's query
+  // chunk; L = Lpad = the chunk length; slices: q, dO, statistics, dQ at
+  // a * B*Hq + (b, h), k, v, dK, dV at b * B*Hkv + (b, kv head); causal keys
+  // from the schedule's chunk map.
+  int step_nt, step, n_chunks, sched;
 };
 
 // Causal-mask keys of the backward (as in the forward's step mode): a key
@@ -143,14 +144,14 @@ struct BwdDev {
 // has key q0k iff kk <= q0k + qq.
 template <bool kStep>
 __device__ __forceinline__ int bwd_q_key(const BwdDev& p, int rank, int local) {
-  if (!kStep || !p.causal || p.striped) return local;
-  return chunk_pos(p.L * p.n_chunks, p.n_chunks, true, false, rank, local);
+  if (!kStep || !p.causal || p.sched == kSchedStriped) return local;
+  return chunk_pos(p.L * p.n_chunks, p.n_chunks, true, p.sched, rank, local);
 }
 template <bool kStep>
 __device__ __forceinline__ int bwd_kv_key(const BwdDev& p, int kv_rank, int q_rank, int local) {
   if (!kStep || !p.causal) return local;
-  if (p.striped) return local + (kv_rank > q_rank ? 1 : 0);
-  return chunk_pos(p.L * p.n_chunks, p.n_chunks, true, false, kv_rank, local);
+  if (p.sched == kSchedStriped) return local + (kv_rank > q_rank ? 1 : 0);
+  return chunk_pos(p.L * p.n_chunks, p.n_chunks, true, p.sched, kv_rank, local);
 }
 
 __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, int* err) {
@@ -541,9 +542,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   int kv_tile = item, q_rank = 0, kv_rank = 0;
   int q_z = qh, kv_z = b * p.Hkv + h / (p.Hq / p.Hkv);
   if constexpr (kStep) {
-    q_rank = item / p.step_nt;
     kv_tile = item % p.step_nt;
-    kv_rank = ((q_rank - p.step) % p.n_chunks + p.n_chunks) % p.n_chunks;
+    schedule_pair(p.n_chunks, p.sched, p.step, item / p.step_nt, &q_rank, &kv_rank);
     q_z += q_rank * p.B * p.Hq;
     kv_z += kv_rank * p.B * p.Hkv;
   }
@@ -747,7 +747,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
   p.dk = static_cast<__nv_bfloat16*>(a.dk);
   p.dv = static_cast<__nv_bfloat16*>(a.dv);
   p.err = a.err;
-  p.step_nt = a.step_nt; p.step = a.step; p.n_chunks = a.n_chunks; p.striped = a.striped;
+  p.step_nt = a.step_nt; p.step = a.step; p.n_chunks = a.n_chunks; p.sched = a.sched;
   const size_t smem = sizeof(BwdSmem<D>);
   auto kernel = a.step_nt ? ring_attn_bwd_kernel<D, true> : ring_attn_bwd_kernel<D, false>;
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -36,6 +36,7 @@
 #include <climits>
 
 #include "kernels.h"
+#include "plan.h"
 #include "sm103_ptx.cuh"
 
 namespace ra {
@@ -73,13 +74,14 @@ struct FwdDev {
   const int32_t* ranges;
   float* lse;
   int* err;
-  // Ring step mode (step_nb > 0): item k = 256-row block k % step_nb of rank
-  // rank_lo + k / step_nb's chunk, against the chunk of rank (r - step) mod
-  // n_chunks.  Slice z of q, o, lse is r * z_rank * B*Hq + (b, h), of k, v
-  // src * z_rank * B*Hkv + (b, kv head): z_rank = 1 for chunk-major buffers
-  // holding every rank, 0 for buffers holding one chunk.  The output is the
-  // normalised partial result in fp32 (o32 / the fp32 output map).
-  int step_nb, step, rank_lo, n_chunks, sub_len, z_rank, striped;
+  // Ring step mode (step_nb > 0): item k = 256-row block k % step_nb of the
+  // block of worker w = rank_lo + k / step_nb at launch `step` of schedule
+  // `sched` (schedule_pair: query chunk a, key/value chunk b).  Slice z of
+  // q is a * z_rank * B*Hq + (b, h), of the output o, lse w * z_rank * B*Hq
+  // + (b, h), of k, v b * z_rank * B*Hkv + (b, kv head): z_rank = 1 for
+  // chunk-major buffers holding every chunk, 0 for buffers holding one.  The
+  // output is the normalised partial result in fp32 (o32 / the fp32 map).
+  int step_nb, step, rank_lo, n_chunks, sub_len, z_rank, sched;
   float* o32;
   // o token-major, [B][L][Hq][d] (tm_o is then 4-D: d, Hq, L, B), for the
   // blockwise transformer whose feed-forward takes token rows of Hq * d
@@ -88,21 +90,23 @@ struct FwdDev {
 
 // Keys of the causal mask: key column i of a tile is visible to a query
 // row iff kv_key(tile) + i <= q_key(row).  Rows of the whole sequence use
-// their positions.  In ring steps with the fold they are the rows' sequence
-// positions (sub-chunks `rank` and 2N-1-rank of sub_len rows; a tile never
-// straddles the two).  With stripes (rank r owns r, r+N, ...), position
-// src + N j <= r + N i  <=>  j <= i - (src > r), so the keys are the local
-// rows, the key tile's shifted by one when its rank is above the query's.
+// their positions.  In ring steps they are the rows' sequence positions:
+// with the fold, sub-chunks `rank` and 2N-1-rank of sub_len rows (a tile
+// never straddles the two); with contiguous chunks, rank * C + local.  With
+// stripes (rank r owns r, r+N, ...), position src + N j <= r + N i  <=>
+// j <= i - (src > r), so the keys are the local rows, the key tile's
+// shifted by one when its rank is above the query's.
 template <bool kStep>
 __device__ __forceinline__ int q_key(const FwdDev& p, int rank, int local) {
-  if (!kStep || !p.causal || p.striped) return local;
+  if (!kStep || !p.causal || p.sched == kSchedStriped) return local;
+  if (p.sched != kSchedFold) return rank * p.L + local;
   return local < p.sub_len ? rank * p.sub_len + local
                            : (2 * p.n_chunks - 1 - rank) * p.sub_len + (local - p.sub_len);
 }
 template <bool kStep>
 __device__ __forceinline__ int kv_key(const FwdDev& p, int kv_rank, int q_rank, int kv0) {
   if (!kStep || !p.causal) return kv0;
-  if (p.striped) return kv0 + (kv_rank > q_rank ? 1 : 0);
+  if (p.sched == kSchedStriped) return kv0 + (kv_rank > q_rank ? 1 : 0);
   return q_key<kStep>(p, kv_rank, kv0);
 }
 
@@ -241,8 +245,8 @@ __device__ void fwd_mma(FwdSmem<D>& sm, uint32_t tmem, int nkv, volatile int* ab
 
 template <int D, bool kStep>
 __device__ void fwd_softmax(FwdSmem<D>& sm, uint32_t tmem, int t, const FwdDev& p, const CUtensorMap* tm_o,
-                            int q0, int q_z, int q_rank, int kv_rank, const int32_t* rg, int nr, volatile int* ab,
-                            int* err) {
+                            int q0, int out_z, int q_rank, int kv_rank, const int32_t* rg, int nr,
+                            volatile int* ab, int* err) {
   const int wq = (threadIdx.x >> 5) & 3;  // TMEM lane quadrant of this warp
   const int lane = threadIdx.x & 31;
   const int row = wq * 32 + lane;
@@ -405,7 +409,7 @@ __device__ void fwd_softmax(FwdSmem<D>& sm, uint32_t tmem, int t, const FwdDev& 
         emit(3, r3);
       }
     }
-    if (qpos < p.L) p.lse[static_cast<size_t>(q_z) * p.L + qpos] = (m + log2f(l)) * kLn2;
+    if (qpos < p.L) p.lse[static_cast<size_t>(out_z) * p.L + qpos] = (m + log2f(l)) * kLn2;
     fence_proxy_async_smem();
   }
   tc_fence_before();
@@ -414,13 +418,13 @@ __device__ void fwd_softmax(FwdSmem<D>& sm, uint32_t tmem, int t, const FwdDev& 
     if constexpr (kStep) {
       for (int c0 = 0; c0 < D / 32; ++c0)
         tma_store_3d(tm_o, c0 < D / 64 ? smem_u32(sm.q[t]) + c0 * 16384 : pbase + (c0 - D / 64) * 16384, 32 * c0,
-                     q0 + 128 * t, q_z);
+                     q0 + 128 * t, out_z);
     } else {
       for (int sub = 0; sub < FwdSmem<D>::kSub; ++sub) {
         if (p.o_tok)  // box (64 columns, 1 head, 128 rows, 1 batch): clipped at this batch's L
-          tma_store_4d(tm_o, pbase + sub * 16384, sub * 64, q_z % p.Hq, q0 + 128 * t, q_z / p.Hq);
+          tma_store_4d(tm_o, pbase + sub * 16384, sub * 64, out_z % p.Hq, q0 + 128 * t, out_z / p.Hq);
         else
-          tma_store_3d(tm_o, pbase + sub * 16384, sub * 64, q0 + 128 * t, q_z);
+          tma_store_3d(tm_o, pbase + sub * 16384, sub * 64, q0 + 128 * t, out_z);
       }
     }
     bulk_commit_group();
@@ -446,12 +450,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int bh = blockIdx.x % BH;
   const int b = bh / p.Hq, h = bh % p.Hq;
   int u = item, q_rank = 0, kv_rank = 0;
-  int q_z = bh, kv_z = b * p.Hkv + h / (p.Hq / p.Hkv);
+  int q_z = bh, out_z = bh, kv_z = b * p.Hkv + h / (p.Hq / p.Hkv);
   if constexpr (kStep) {
-    q_rank = p.rank_lo + item / p.step_nb;
+    const int worker = p.rank_lo + item / p.step_nb;
     u = item % p.step_nb;
-    kv_rank = ((q_rank - p.step) % p.n_chunks + p.n_chunks) % p.n_chunks;
+    schedule_pair(p.n_chunks, p.sched, p.step, worker, &q_rank, &kv_rank);
     q_z += q_rank * p.z_rank * BH;
+    out_z += worker * p.z_rank * BH;
     kv_z += kv_rank * p.z_rank * (p.B * p.Hkv);
   }
   const int q0 = u * 256;
@@ -495,10 +500,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     if (warp >= 4) {
       const int qpos = q0 + 128 * ((warp - 4) >> 2) + (threadIdx.x & 127);
       if (qpos < p.L) {
-        float4* dst = reinterpret_cast<float4*>(p.o32 + (static_cast<size_t>(q_z) * p.L + qpos) * D);
+        float4* dst = reinterpret_cast<float4*>(p.o32 + (static_cast<size_t>(out_z) * p.L + qpos) * D);
 #pragma unroll 4
         for (int x = 0; x < D / 4; ++x) dst[x] = make_float4(0.f, 0.f, 0.f, 0.f);
-        p.lse[static_cast<size_t>(q_z) * p.L + qpos] = -INFINITY;
+        p.lse[static_cast<size_t>(out_z) * p.L + qpos] = -INFINITY;
       }
     }
   } else if (warp == 0) {
@@ -507,7 +512,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     // the whole warp runs the issue loop; one elected lane issues
     fwd_mma<D>(sm, tmem, nkv, ab, p.err);
   } else if (warp >= 4) {
-    fwd_softmax<D, kStep>(sm, tmem, (warp - 4) >> 2, p, &tm_o, q0, q_z, q_rank, kv_rank, rg, nr, ab, p.err);
+    fwd_softmax<D, kStep>(sm, tmem, (warp - 4) >> 2, p, &tm_o, q0, out_z, q_rank, kv_rank, rg, nr, ab, p.err);
   }
   tc_fence_before();
   __syncthreads();
@@ -551,7 +556,7 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
   p.order = a.order; p.offsets = a.offsets; p.ranges = a.ranges;
   p.lse = a.lse; p.err = a.err;
   p.step_nb = a.step_nb; p.step = a.step; p.rank_lo = a.rank_lo; p.n_chunks = a.n_chunks;
-  p.sub_len = a.sub_len; p.z_rank = a.z_rank; p.striped = a.striped; p.o32 = a.o32;
+  p.sub_len = a.sub_len; p.z_rank = a.z_rank; p.sched = a.sched; p.o32 = a.o32;
   p.o_tok = a.o_token_major;
   const size_t smem = fwd_smem_bytes(a.d);
   const dim3 grid(static_cast<unsigned>(a.n_blocks) * a.B * a.Hq);

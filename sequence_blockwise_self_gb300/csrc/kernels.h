@@ -42,7 +42,7 @@ struct FwdArgs {
   LaunchTimer* timer;       // nullptr unless profiling
   // ring step mode (step_nb > 0; L is then the chunk length, n_blocks the
   // number of items, tm_o an fp32 map with 32-column boxes, see attn_fwd.cu)
-  int step_nb = 0, step = 0, rank_lo = 0, n_chunks = 1, sub_len = 0, z_rank = 0, striped = 0;
+  int step_nb = 0, step = 0, rank_lo = 0, n_chunks = 1, sub_len = 0, z_rank = 0, sched = 0;
   float* o32 = nullptr;
   // not a ring step: o token-major [B][L][Hq][d] through a 4-D tm_o
   // (d, Hq, L, B; box 64 x 1 x 128 x 1)
@@ -100,7 +100,7 @@ struct BwdArgs {
   // * step_nt items; L = Lpad = the chunk length; slices chunk-major, see
   // attn_bwd.cu): only the main kernel runs, with dK/dV always reduced into
   // the fp32 accumulators; the driver runs launch_bwd_pre and the conversions
-  int step_nt = 0, step = 0, n_chunks = 1, striped = 0;
+  int step_nt = 0, step = 0, n_chunks = 1, sched = 0;
 };
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
@@ -116,16 +116,16 @@ cudaError_t launch_bwd_pre(const BwdArgs& a, long long q_slices, long long kv_sl
 // [N][Z][C][d] (+ lse [N][Z][C]) back to sequence order as bf16 (+ lse).
 cudaError_t launch_ring_merge(float* o, float* lse, const float* o_s, const float* lse_s, void* o_out,
                               long long n_rows, int d, cudaStream_t stream);
-cudaError_t launch_ring_gather(const void* src, void* dst, int Z, int L, int d, int N, bool causal, bool striped,
+cudaError_t launch_ring_gather(const void* src, void* dst, int Z, int L, int d, int N, bool causal, int sched,
                                cudaStream_t stream);
 // Ring-mode backward (ring_step.cu): gather of one fp32 per row (lse) into
 // chunk order, and the scatter of an fp32 gradient accumulator in chunk
 // order (plain, or the tiled dQ layout) back to sequence order as
 // bf16(scale * acc).
-cudaError_t launch_ring_gather_rows(const float* src, float* dst, int Z, int L, int N, bool causal, bool striped,
+cudaError_t launch_ring_gather_rows(const float* src, float* dst, int Z, int L, int N, bool causal, int sched,
                                     cudaStream_t stream);
 cudaError_t launch_ring_scatter_grad(const float* acc, void* g, float scale, bool tiled, int Z, int L, int d, int N,
-                                     bool causal, bool striped, cudaStream_t stream);
+                                     bool causal, int sched, cudaStream_t stream);
 
 // Ulysses / USP (ulysses.cu): the all-to-all between the N = U R sequence
 // shards [N][B][H][L/N][row] and the U head groups [U][B][H/U][L][row]
@@ -138,7 +138,7 @@ cudaError_t launch_ulysses_a2a(const void* src, void* dst, int row_bytes, int B,
 cudaError_t launch_tokens_heads(const void* src, void* dst, int row_bytes, int B, int H, int L, bool to_heads,
                                 cudaStream_t stream);
 cudaError_t launch_ring_scatter(const float* acc, const float* lse_acc, void* o, float* lse, int Z, int L, int d,
-                                int N, bool causal, bool striped, cudaStream_t stream);
+                                int N, bool causal, int sched, cudaStream_t stream);
 
 // Dynamic shared memory each kernel needs (bytes), for the C ABI's checks.
 size_t fwd_smem_bytes(int d);

@@ -90,7 +90,7 @@ Plan build_bwd_plan(int L, int N, bool causal) {
   return p;
 }
 
-Plan build_step_plan(int L, int N, bool causal, bool striped, int step, int rank_lo, int rank_hi) {
+Plan build_step_plan(int L, int N, bool causal, int sched, int step, int rank_lo, int rank_hi) {
   Plan p;
   const int C = L / N;
   const int nt = C / kTileRows;                       // tiles per chunk
@@ -98,17 +98,18 @@ Plan build_step_plan(int L, int N, bool causal, bool striped, int step, int rank
   p.n_blocks = (rank_hi - rank_lo) * nb;
   p.offsets.push_back(0);
   std::vector<int> tiles;
-  for (int r = rank_lo; r < rank_hi; ++r) {
-    const int src = ((r - step) % N + N) % N;
+  for (int w = rank_lo; w < rank_hi; ++w) {
+    int r, src;
+    const bool busy = schedule_pair(N, sched, step, w, &r, &src);
     for (int u = 0; u < nb; ++u) {
       tiles.clear();
       int q_tiles = 0;
       for (int qt = 2 * u; qt < 2 * u + 2 && qt < nt; ++qt) ++q_tiles;
-      for (int kt = 0; kt < nt; ++kt) {
+      for (int kt = 0; kt < nt && busy; ++kt) {
         bool seen = !causal;
         for (int qt = 2 * u; qt < 2 * u + 2 && qt < nt && !seen; ++qt)
-          seen = chunk_pos(L, N, true, striped, src, kt * kTileRows) <=
-                 chunk_pos(L, N, true, striped, r, qt * kTileRows + kTileRows - 1);
+          seen = chunk_pos(L, N, true, sched, src, kt * kTileRows) <=
+                 chunk_pos(L, N, true, sched, r, qt * kTileRows + kTileRows - 1);
         if (seen) tiles.push_back(kt);
       }
       append_ranges(tiles, p.ranges);
@@ -120,20 +121,21 @@ Plan build_step_plan(int L, int N, bool causal, bool striped, int step, int rank
   return p;
 }
 
-Plan build_bwd_step_plan(int L, int N, bool causal, bool striped, int step) {
+Plan build_bwd_step_plan(int L, int N, bool causal, int sched, int step) {
   Plan p;
   const int C = L / N;
   const int nt = C / kTileRows;
   p.n_blocks = N * nt;
   p.offsets.push_back(0);
   std::vector<int> tiles;
-  for (int r = 0; r < N; ++r) {
-    const int src = ((r - step) % N + N) % N;
+  for (int w = 0; w < N; ++w) {
+    int r, src;
+    const bool busy = schedule_pair(N, sched, step, w, &r, &src);
     for (int kt = 0; kt < nt; ++kt) {
       tiles.clear();
-      const int kmin = chunk_pos(L, N, causal, striped, src, kt * kTileRows);
-      for (int qt = 0; qt < nt; ++qt)
-        if (!causal || kmin <= chunk_pos(L, N, causal, striped, r, qt * kTileRows + kTileRows - 1)) tiles.push_back(qt);
+      const int kmin = chunk_pos(L, N, causal, sched, src, kt * kTileRows);
+      for (int qt = 0; qt < nt && busy; ++qt)
+        if (!causal || kmin <= chunk_pos(L, N, causal, sched, r, qt * kTileRows + kTileRows - 1)) tiles.push_back(qt);
       append_ranges(tiles, p.ranges);
       p.offsets.push_back(static_cast<int32_t>(p.ranges.size() / 2));
       p.work.push_back(static_cast<int64_t>(tiles.size()));

@@ -29,7 +29,7 @@ namespace {
 __device__ int g_device_status;
 
 std::map<std::tuple<int, int, int, int, int>, DevicePlan> g_plans;  // (device, kind, L, N, causal)
-// ring step plans: (device, L, N, causal, striped, step, first rank, end rank;
+// ring step plans: (device, L, N, causal, schedule, launch, first worker, end worker;
 // end rank -1 = the backward plan of the step)
 std::map<std::tuple<int, int, int, int, int, int, int, int>, DevicePlan> g_step_plans;
 // forward work items grouped by row block: (device, L, N, causal, block rows)
@@ -153,17 +153,17 @@ int status_ptr(int dev, int** out) {
   return RING_ATTN_OK;
 }
 
-int get_step_plan(int dev, int L, int N, int causal, int striped, int step, int rank_lo, int rank_hi,
+int get_step_plan(int dev, int L, int N, int causal, int schedule, int step, int rank_lo, int rank_hi,
                   DevicePlan* out) {
-  auto key = std::make_tuple(dev, L, N, causal, striped, step, rank_lo, rank_hi);
+  auto key = std::make_tuple(dev, L, N, causal, schedule, step, rank_lo, rank_hi);
   auto it = g_step_plans.find(key);
   if (it != g_step_plans.end()) {
     *out = it->second;
     return RING_ATTN_OK;
   }
   DevicePlan dp;
-  int rc = upload_plan(rank_hi < 0 ? build_bwd_step_plan(L, N, causal != 0, striped != 0, step)
-                                   : build_step_plan(L, N, causal != 0, striped != 0, step, rank_lo, rank_hi),
+  int rc = upload_plan(rank_hi < 0 ? build_bwd_step_plan(L, N, causal != 0, schedule, step)
+                                   : build_step_plan(L, N, causal != 0, schedule, step, rank_lo, rank_hi),
                        &dp);
   if (rc != RING_ATTN_OK) return rc;
   g_step_plans[key] = dp;
@@ -200,11 +200,13 @@ int get_block_orders(int dev, int L, int N, int causal, int R, int32_t** out) {
   return RING_ATTN_OK;
 }
 
-int check_ring_shape(int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal, int striped) {
-  // stripes need only L % N == 0 (the fold L % 2N)
-  int rc = check_shape(B, Hq, Hkv, L, d, n_chunks, striped ? 0 : causal);
+int check_ring_shape(int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal, int schedule) {
+  // the contiguous schedules are defined for causal attention only
+  if (!schedule_ok(schedule, causal != 0)) return RING_ATTN_ERR_UNSUPPORTED;
+  // only the fold needs L % 2N == 0; the other chunk maps L % N == 0
+  int rc = check_shape(B, Hq, Hkv, L, d, n_chunks, schedule == kSchedFold ? causal : 0);
   if (rc != RING_ATTN_OK) return rc;
-  if (L > 0 && !step_chunking_ok(L, n_chunks, causal != 0, striped != 0)) return RING_ATTN_ERR_UNSUPPORTED;
+  if (L > 0 && !step_chunking_ok(L, n_chunks, causal != 0, schedule)) return RING_ATTN_ERR_UNSUPPORTED;
   if (static_cast<long long>(n_chunks) * B * Hq >= 65536) return RING_ATTN_ERR_UNSUPPORTED;
   return RING_ATTN_OK;
 }
@@ -213,7 +215,7 @@ int check_ring_shape(int B, int Hq, int Hkv, int L, int d, int n_chunks, int cau
 // z_rank = 1 the buffers hold every rank's chunk ([N][B][H][C][d]), with
 // z_rank = 0 only the chunks of the one rank and its source.
 int launch_step(int dev, const void* q, const void* k, const void* v, float* o_s, float* lse_s, int B, int Hq,
-                int Hkv, int L, int d, int N, int causal, int striped, int step, int rank_lo, int rank_hi, int z_rank,
+                int Hkv, int L, int d, int N, int causal, int schedule, int step, int rank_lo, int rank_hi, int z_rank,
                 cudaStream_t stream) {
   const int C = L / N;
   const int zq = (z_rank ? N : 1) * B * Hq, zkv = (z_rank ? N : 1) * B * Hkv;
@@ -225,7 +227,7 @@ int launch_step(int dev, const void* q, const void* k, const void* v, float* o_s
       !make_map(&a.tm_o, o_s, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, C, zq, 32))
     return RING_ATTN_ERR_CUDA;
   DevicePlan plan;
-  int rc = get_step_plan(dev, L, N, causal, striped, step, rank_lo, rank_hi, &plan);
+  int rc = get_step_plan(dev, L, N, causal, schedule, step, rank_lo, rank_hi, &plan);
   if (rc != RING_ATTN_OK) return rc;
   int* err;
   if ((rc = status_ptr(dev, &err)) != RING_ATTN_OK) return rc;
@@ -235,8 +237,8 @@ int launch_step(int dev, const void* q, const void* k, const void* v, float* o_s
   a.lse = lse_s; a.err = err; a.timer = active_timer();
   a.step_nb = (C + kQBlockRows - 1) / kQBlockRows;
   a.step = step; a.rank_lo = rank_lo; a.n_chunks = N;
-  a.sub_len = (causal && !striped) ? L / (2 * N) : 0;
-  a.z_rank = z_rank; a.striped = striped != 0; a.o32 = o_s;
+  a.sub_len = (causal && schedule == kSchedFold) ? L / (2 * N) : 0;
+  a.z_rank = z_rank; a.sched = schedule; a.o32 = o_s;
   return launch_fwd(a, stream) == cudaSuccess ? RING_ATTN_OK : RING_ATTN_ERR_CUDA;
 }
 
@@ -401,13 +403,27 @@ int ring_attn_bwd_plan(int L, int n_chunks, int causal, int* n_blocks, int* n_ra
   return plan_query(1, L, n_chunks, causal, n_blocks, n_ranges, block_order, range_offsets, ranges);
 }
 
-int ring_attn_step_plan(int L, int n_chunks, int causal, int striped, int step, int rank, int* n_blocks,
-                        int* n_ranges, int32_t* block_order, int32_t* range_offsets, int32_t* ranges) {
-  if (L <= 0 || n_chunks <= 0 || !chunking_ok(L, n_chunks, striped ? false : causal != 0))
+int ring_attn_schedule_launches(int n_chunks, int schedule) {
+  if (n_chunks <= 0 || !schedule_ok(schedule, true)) return RING_ATTN_ERR_SHAPE;
+  return schedule_launches(n_chunks, schedule);
+}
+
+int ring_attn_schedule_pair(int n_chunks, int schedule, int launch, int worker, int* q_chunk, int* kv_chunk) {
+  if (n_chunks <= 0 || !schedule_ok(schedule, true)) return RING_ATTN_ERR_SHAPE;
+  if (launch < 0 || launch >= schedule_launches(n_chunks, schedule) || worker < 0 || worker >= n_chunks)
     return RING_ATTN_ERR_SHAPE;
-  if (!step_chunking_ok(L, n_chunks, causal != 0, striped != 0)) return RING_ATTN_ERR_UNSUPPORTED;
-  if (step < 0 || step >= n_chunks || rank < 0 || rank >= n_chunks) return RING_ATTN_ERR_SHAPE;
-  Plan p = build_step_plan(L, n_chunks, causal != 0, striped != 0, step, rank, rank + 1);
+  if (!q_chunk || !kv_chunk) return RING_ATTN_ERR_NULL;
+  return schedule_pair(n_chunks, schedule, launch, worker, q_chunk, kv_chunk) ? 1 : 0;
+}
+
+int ring_attn_step_plan(int L, int n_chunks, int causal, int schedule, int step, int rank, int* n_blocks,
+                        int* n_ranges, int32_t* block_order, int32_t* range_offsets, int32_t* ranges) {
+  if (L <= 0 || n_chunks <= 0 || !chunking_ok(L, n_chunks, schedule == kSchedFold && causal != 0))
+    return RING_ATTN_ERR_SHAPE;
+  if (!step_chunking_ok(L, n_chunks, causal != 0, schedule)) return RING_ATTN_ERR_UNSUPPORTED;
+  if (step < 0 || step >= schedule_launches(n_chunks, schedule) || rank < 0 || rank >= n_chunks)
+    return RING_ATTN_ERR_SHAPE;
+  Plan p = build_step_plan(L, n_chunks, causal != 0, schedule, step, rank, rank + 1);
   if (n_blocks) *n_blocks = p.n_blocks;
   if (n_ranges) *n_ranges = static_cast<int>(p.ranges.size() / 2);
   if (block_order) std::memcpy(block_order, p.order.data(), p.order.size() * sizeof(int32_t));
@@ -508,11 +524,15 @@ int ring_attn_profile_read(double* ms, long long* launches) {
 }
 
 int ring_attn_fwd_step(const void* q_chunk, const void* k_chunk, const void* v_chunk, float* o_s, float* lse_s,
-                       int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal, int striped, int rank, int src,
+                       int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal, int schedule, int rank, int src,
                        cudaStream_t stream) {
-  int rc = check_ring_shape(B, Hq, Hkv, L, d, n_chunks, causal, striped);
+  int rc = check_ring_shape(B, Hq, Hkv, L, d, n_chunks, causal, schedule);
   if (rc != RING_ATTN_OK) return rc;
   if (rank < 0 || rank >= n_chunks || src < 0 || src >= n_chunks) return RING_ATTN_ERR_SHAPE;
+  // one block (rank's queries, src's keys): for the contiguous chunk map the
+  // schedule only decides who runs it when, so DistFlashAttention's blocks
+  // are the plain ring's
+  if (schedule == kSchedDfa) schedule = kSchedContig;
   if (B == 0 || L == 0) return RING_ATTN_OK;
   if (!q_chunk || !k_chunk || !v_chunk || !o_s || !lse_s) return RING_ATTN_ERR_NULL;
   if (!aligned16(q_chunk) || !aligned16(k_chunk) || !aligned16(v_chunk) || !aligned16(o_s) || !aligned16(lse_s))
@@ -521,7 +541,7 @@ int ring_attn_fwd_step(const void* q_chunk, const void* k_chunk, const void* v_c
   int dev;
   if ((rc = current_device(&dev)) != RING_ATTN_OK) return rc;
   const int step = ((rank - src) % n_chunks + n_chunks) % n_chunks;
-  return launch_step(dev, q_chunk, k_chunk, v_chunk, o_s, lse_s, B, Hq, Hkv, L, d, n_chunks, causal, striped, step,
+  return launch_step(dev, q_chunk, k_chunk, v_chunk, o_s, lse_s, B, Hq, Hkv, L, d, n_chunks, causal, schedule, step,
                      rank, rank + 1, 0, stream);
 }
 
@@ -540,15 +560,15 @@ int ring_attn_merge(float* o, float* lse, const float* o_s, const float* lse_s, 
 }
 
 size_t ring_attn_ring_fwd_workspace_size(int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal,
-                                         int striped) {
-  if (check_ring_shape(B, Hq, Hkv, L, d, n_chunks, causal, striped) != RING_ATTN_OK) return 0;
+                                         int schedule) {
+  if (check_ring_shape(B, Hq, Hkv, L, d, n_chunks, causal, schedule) != RING_ATTN_OK) return 0;
   return ring_workspace(B, Hq, Hkv, L, d).total;
 }
 
 int ring_attn_ring_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
-                       int L, int d, int n_chunks, int causal, int striped, void* workspace, size_t workspace_bytes,
+                       int L, int d, int n_chunks, int causal, int schedule, void* workspace, size_t workspace_bytes,
                        cudaStream_t stream) {
-  int rc = check_ring_shape(B, Hq, Hkv, L, d, n_chunks, causal, striped);
+  int rc = check_ring_shape(B, Hq, Hkv, L, d, n_chunks, causal, schedule);
   if (rc != RING_ATTN_OK) return rc;
   if (B == 0 || L == 0) return RING_ATTN_OK;
   if (!q || !k || !v || !o || !lse) return RING_ATTN_ERR_NULL;
@@ -571,23 +591,37 @@ int ring_attn_ring_fwd(const void* q, const void* k, const void* v, void* o, flo
   const int N = n_chunks;
   LaunchTimer* t = active_timer();
   if (t) t->mark(RING_ATTN_KERNEL_RING_IO, false, stream);
-  const bool sc = causal != 0, st = striped != 0;
+  const bool sc = causal != 0;
+  const int st = schedule;
   if (launch_ring_gather(q, qc, B * Hq, L, d, N, sc, st, stream) != cudaSuccess ||
       launch_ring_gather(k, kc, B * Hkv, L, d, N, sc, st, stream) != cudaSuccess ||
       launch_ring_gather(v, vc, B * Hkv, L, d, N, sc, st, stream) != cudaSuccess)
     return RING_ATTN_ERR_CUDA;
   if (t) t->mark(RING_ATTN_KERNEL_RING_IO, true, stream);
   const long long rows = static_cast<long long>(B) * Hq * L;
-  for (int s = 0; s < N; ++s) {
-    // step 0 (every rank's own chunk) starts the running result
+  const long long chunk_rows = rows / N;  // rows of one chunk, chunk-major
+  auto merge = [&](long long first_acc, long long first_part, long long n) {
+    if (t) t->mark(RING_ATTN_KERNEL_RING_MERGE, false, stream);
+    const cudaError_t e = launch_ring_merge(oacc + first_acc * d, lacc + first_acc, os + first_part * d,
+                                            ls + first_part, nullptr, n, d, stream);
+    if (t) t->mark(RING_ATTN_KERNEL_RING_MERGE, true, stream);
+    return e;
+  };
+  for (int s = 0; s < schedule_launches(N, schedule); ++s) {
+    // launch 0 (every worker's own chunk against itself) starts the running
+    // result; each later launch leaves worker w's partial in slot w
     if ((rc = launch_step(dev, qc, kc, vc, s == 0 ? oacc : os, s == 0 ? lacc : ls, B, Hq, Hkv, L, d, N, causal,
-                          striped, s, 0, N, 1, stream)) != RING_ATTN_OK)
+                          schedule, s, 0, N, 1, stream)) != RING_ATTN_OK)
       return rc;
-    if (s > 0) {
-      if (t) t->mark(RING_ATTN_KERNEL_RING_MERGE, false, stream);
-      if (launch_ring_merge(oacc, lacc, os, ls, nullptr, rows, d, stream) != cudaSuccess) return RING_ATTN_ERR_CUDA;
-      if (t) t->mark(RING_ATTN_KERNEL_RING_MERGE, true, stream);
+    if (s == 0) continue;
+    if (schedule != kSchedDfa) {  // ring step: worker w's partial belongs to chunk w
+      if (merge(0, 0, rows) != cudaSuccess) return RING_ATTN_ERR_CUDA;
+      continue;
     }
+    // DistFlashAttention: workers s..N-1 ran blocks of their own chunks;
+    // workers 0..s-1 (busy unless s = N - s) those of chunks N-s..N-1
+    if (merge(s * chunk_rows, s * chunk_rows, (N - s) * chunk_rows) != cudaSuccess) return RING_ATTN_ERR_CUDA;
+    if (s < N - s && merge((N - s) * chunk_rows, 0, s * chunk_rows) != cudaSuccess) return RING_ATTN_ERR_CUDA;
   }
   if (t) t->mark(RING_ATTN_KERNEL_RING_IO, false, stream);
   if (launch_ring_scatter(oacc, lacc, o, lse, B * Hq, L, d, N, sc, st, stream) != cudaSuccess)
@@ -597,15 +631,15 @@ int ring_attn_ring_fwd(const void* q, const void* k, const void* v, void* o, flo
 }
 
 size_t ring_attn_ring_bwd_workspace_size(int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal,
-                                         int striped) {
-  if (check_ring_shape(B, Hq, Hkv, L, d, n_chunks, causal, striped) != RING_ATTN_OK) return 0;
+                                         int schedule) {
+  if (check_ring_shape(B, Hq, Hkv, L, d, n_chunks, causal, schedule) != RING_ATTN_OK) return 0;
   return ring_bwd_workspace(B, Hq, Hkv, L, d).total;
 }
 
 int ring_attn_ring_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
                        void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal,
-                       int striped, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-  int rc = check_ring_shape(B, Hq, Hkv, L, d, n_chunks, causal, striped);
+                       int schedule, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  int rc = check_ring_shape(B, Hq, Hkv, L, d, n_chunks, causal, schedule);
   if (rc != RING_ATTN_OK) return rc;
   if (B == 0 || L == 0) return RING_ATTN_OK;
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return RING_ATTN_ERR_NULL;
@@ -620,7 +654,8 @@ int ring_attn_ring_bwd(const void* q, const void* k, const void* v, const void* 
   if ((rc = current_device(&dev)) != RING_ATTN_OK) return rc;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const int N = n_chunks, C = L / N;
-  const bool sc = causal != 0, st = striped != 0;
+  const bool sc = causal != 0;
+  const int st = schedule;
   LaunchTimer* t = active_timer();
   // every rank's rows in chunk order
   if (t) t->mark(RING_ATTN_KERNEL_RING_IO, false, stream);
@@ -654,10 +689,10 @@ int ring_attn_ring_bwd(const void* q, const void* k, const void* v, const void* 
   a.err = err; a.timer = t;
   // statistics of every rank's rows, accumulators zeroed
   if (launch_bwd_pre(a, zq, zkv, stream) != cudaSuccess) return RING_ATTN_ERR_CUDA;
-  a.step_nt = C / kTileRows; a.n_chunks = N; a.striped = st;
-  for (int s = 0; s < N; ++s) {
+  a.step_nt = C / kTileRows; a.n_chunks = N; a.sched = schedule;
+  for (int s = 0; s < schedule_launches(N, schedule); ++s) {
     DevicePlan plan;
-    if ((rc = get_step_plan(dev, L, N, causal, striped, s, 0, -1, &plan)) != RING_ATTN_OK) return rc;
+    if ((rc = get_step_plan(dev, L, N, causal, schedule, s, 0, -1, &plan)) != RING_ATTN_OK) return rc;
     a.n_blocks = plan.n_blocks;
     a.order = plan.order(); a.offsets = plan.offsets(); a.ranges = plan.ranges();
     a.step = s;

@@ -74,7 +74,7 @@ __global__ void __launch_bounds__(256) ring_merge_kernel(float* __restrict__ o, 
 template <int D>
 __global__ void __launch_bounds__(256) ring_gather_kernel(const __nv_bfloat16* __restrict__ src,
                                                           __nv_bfloat16* __restrict__ dst, int Z, int L, int N,
-                                                          int causal, int striped, long long n_vec) {
+                                                          int causal, int sched, long long n_vec) {
   const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (t >= n_vec) return;
   constexpr int kVec = D / 8;
@@ -85,7 +85,7 @@ __global__ void __launch_bounds__(256) ring_gather_kernel(const __nv_bfloat16* _
   const long long rz = rowg / C;
   const int z = static_cast<int>(rz % Z);
   const int r = static_cast<int>(rz / Z);
-  const int pos = chunk_pos(L, N, causal != 0, striped != 0, r, i);
+  const int pos = chunk_pos(L, N, causal != 0, sched, r, i);
   const uint4 v = reinterpret_cast<const uint4*>(src + (static_cast<size_t>(z) * L + pos) * D)[c8];
   reinterpret_cast<uint4*>(dst + rowg * D)[c8] = v;
 }
@@ -96,7 +96,7 @@ template <int D>
 __global__ void __launch_bounds__(256) ring_scatter_kernel(const float* __restrict__ acc,
                                                            const float* __restrict__ lse_acc,
                                                            __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
-                                                           int Z, int L, int N, int causal, int striped,
+                                                           int Z, int L, int N, int causal, int sched,
                                                            long long n_vec) {
   const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (t >= n_vec) return;
@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(256) ring_scatter_kernel(const float* __restri
   const long long rz = rowg / C;
   const int z = static_cast<int>(rz % Z);
   const int r = static_cast<int>(rz / Z);
-  const int pos = chunk_pos(L, N, causal != 0, striped != 0, r, i);
+  const int pos = chunk_pos(L, N, causal != 0, sched, r, i);
   const float4* s = reinterpret_cast<const float4*>(acc + rowg * D) + 2 * c8;
   const float4 a = s[0], b = s[1];
   const size_t out = static_cast<size_t>(z) * L + pos;
@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(256) ring_scatter_kernel(const float* __restri
 
 // dst[r][z][i] = src[z][pos(r, i)] for one fp32 per row (lse).
 __global__ void __launch_bounds__(256) ring_gather_rows_kernel(const float* __restrict__ src, float* __restrict__ dst,
-                                                               int Z, int L, int N, int causal, int striped,
+                                                               int Z, int L, int N, int causal, int sched,
                                                                long long n_rows) {
   const long long rowg = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (rowg >= n_rows) return;
@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(256) ring_gather_rows_kernel(const float* __re
   const long long rz = rowg / C;
   const int z = static_cast<int>(rz % Z);
   const int r = static_cast<int>(rz / Z);
-  dst[rowg] = src[static_cast<size_t>(z) * L + chunk_pos(L, N, causal != 0, striped != 0, r, i)];
+  dst[rowg] = src[static_cast<size_t>(z) * L + chunk_pos(L, N, causal != 0, sched, r, i)];
 }
 
 // Gradient back to sequence order: g[z][pos(r, i)][:] = bf16(scale * acc)
@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(256) ring_gather_rows_kernel(const float* __re
 template <int D, bool kTiled>
 __global__ void __launch_bounds__(256) ring_scatter_grad_kernel(const float* __restrict__ acc,
                                                                 __nv_bfloat16* __restrict__ g, float scale, int Z,
-                                                                int L, int N, int causal, int striped,
+                                                                int L, int N, int causal, int sched,
                                                                 long long n_vec) {
   const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (t >= n_vec) return;
@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(256) ring_scatter_grad_kernel(const float* __r
     a = s[0];
     b = s[1];
   }
-  const size_t out = static_cast<size_t>(z) * L + chunk_pos(L, N, causal != 0, striped != 0, r, i);
+  const size_t out = static_cast<size_t>(z) * L + chunk_pos(L, N, causal != 0, sched, r, i);
   reinterpret_cast<uint4*>(g + out * D)[c8] =
       make_uint4(pack_bf16(a.x * scale, a.y * scale), pack_bf16(a.z * scale, a.w * scale),
                  pack_bf16(b.x * scale, b.y * scale), pack_bf16(b.z * scale, b.w * scale));
@@ -170,28 +170,28 @@ unsigned blocks_for(long long n) { return static_cast<unsigned>((n + 255) / 256)
 
 }  // namespace
 
-cudaError_t launch_ring_gather_rows(const float* src, float* dst, int Z, int L, int N, bool causal, bool striped,
+cudaError_t launch_ring_gather_rows(const float* src, float* dst, int Z, int L, int N, bool causal, int sched,
                                     cudaStream_t stream) {
   const long long n = static_cast<long long>(Z) * L;
-  ring_gather_rows_kernel<<<blocks_for(n), 256, 0, stream>>>(src, dst, Z, L, N, causal, striped, n);
+  ring_gather_rows_kernel<<<blocks_for(n), 256, 0, stream>>>(src, dst, Z, L, N, causal, sched, n);
   return cudaGetLastError();
 }
 
 cudaError_t launch_ring_scatter_grad(const float* acc, void* g, float scale, bool tiled, int Z, int L, int d, int N,
-                                     bool causal, bool striped, cudaStream_t stream) {
+                                     bool causal, int sched, cudaStream_t stream) {
   const long long n = static_cast<long long>(Z) * L * (d / 8);
   auto* out = static_cast<__nv_bfloat16*>(g);
   const unsigned nb = blocks_for(n);
   if (d == 128) {
     if (tiled)
-      ring_scatter_grad_kernel<128, true><<<nb, 256, 0, stream>>>(acc, out, scale, Z, L, N, causal, striped, n);
+      ring_scatter_grad_kernel<128, true><<<nb, 256, 0, stream>>>(acc, out, scale, Z, L, N, causal, sched, n);
     else
-      ring_scatter_grad_kernel<128, false><<<nb, 256, 0, stream>>>(acc, out, scale, Z, L, N, causal, striped, n);
+      ring_scatter_grad_kernel<128, false><<<nb, 256, 0, stream>>>(acc, out, scale, Z, L, N, causal, sched, n);
   } else {
     if (tiled)
-      ring_scatter_grad_kernel<64, true><<<nb, 256, 0, stream>>>(acc, out, scale, Z, L, N, causal, striped, n);
+      ring_scatter_grad_kernel<64, true><<<nb, 256, 0, stream>>>(acc, out, scale, Z, L, N, causal, sched, n);
     else
-      ring_scatter_grad_kernel<64, false><<<nb, 256, 0, stream>>>(acc, out, scale, Z, L, N, causal, striped, n);
+      ring_scatter_grad_kernel<64, false><<<nb, 256, 0, stream>>>(acc, out, scale, Z, L, N, causal, sched, n);
   }
   return cudaGetLastError();
 }
@@ -207,27 +207,27 @@ cudaError_t launch_ring_merge(float* o, float* lse, const float* o_s, const floa
   return cudaGetLastError();
 }
 
-cudaError_t launch_ring_gather(const void* src, void* dst, int Z, int L, int d, int N, bool causal, bool striped,
+cudaError_t launch_ring_gather(const void* src, void* dst, int Z, int L, int d, int N, bool causal, int sched,
                                cudaStream_t stream) {
   const long long n = static_cast<long long>(Z) * L * (d / 8);
   auto* s = static_cast<const __nv_bfloat16*>(src);
   auto* t = static_cast<__nv_bfloat16*>(dst);
   if (d == 128)
-    ring_gather_kernel<128><<<blocks_for(n), 256, 0, stream>>>(s, t, Z, L, N, causal, striped, n);
+    ring_gather_kernel<128><<<blocks_for(n), 256, 0, stream>>>(s, t, Z, L, N, causal, sched, n);
   else
-    ring_gather_kernel<64><<<blocks_for(n), 256, 0, stream>>>(s, t, Z, L, N, causal, striped, n);
+    ring_gather_kernel<64><<<blocks_for(n), 256, 0, stream>>>(s, t, Z, L, N, causal, sched, n);
   return cudaGetLastError();
 }
 
 cudaError_t launch_ring_scatter(const float* acc, const float* lse_acc, void* o, float* lse, int Z, int L, int d,
-                                int N, bool causal, bool striped, cudaStream_t stream) {
+                                int N, bool causal, int sched, cudaStream_t stream) {
   const long long n = static_cast<long long>(Z) * L * (d / 8);
   auto* out = static_cast<__nv_bfloat16*>(o);
   if (d == 128)
-    ring_scatter_kernel<128><<<blocks_for(n), 256, 0, stream>>>(acc, lse_acc, out, lse, Z, L, N, causal, striped,
+    ring_scatter_kernel<128><<<blocks_for(n), 256, 0, stream>>>(acc, lse_acc, out, lse, Z, L, N, causal, sched,
                                                                n);
   else
-    ring_scatter_kernel<64><<<blocks_for(n), 256, 0, stream>>>(acc, lse_acc, out, lse, Z, L, N, causal, striped,
+    ring_scatter_kernel<64><<<blocks_for(n), 256, 0, stream>>>(acc, lse_acc, out, lse, Z, L, N, causal, sched,
                                                               n);
   return cudaGetLastError();
 }

@@ -1,7 +1,9 @@
 """Ring mode on the GPU, through the C ABI, against the fp64 oracle.
 
 One ring step (ring_attn_fwd_step) is compared with the oracle's ring_step
-for every (rank, source) pair of small rings; the merge kernel with the
+for every (rank, source) pair of small rings, for each chunk map (the fold,
+stripes, contiguous causal chunks); the whole ring in each schedule,
+including DistFlashAttention's balanced one; the merge kernel with the
 oracle's merge; the whole ring run step by step on one GPU
 (ring_attn_ring_fwd) with the oracle's plain forward and with the fused
 forward.  Tolerances as for the fused path (tolerance.py): o within 2e-2
@@ -36,45 +38,48 @@ def assert_status_ok():
     assert st == 0, f"device status {st} at site {site:#x}"
 
 
-def chunk_positions(L, N, causal, r, striped=False):
-    return torch.tensor([p for p in range(L) if oracle.owner_rank(L, N, causal, p, striped) == r], dtype=torch.long)
+def chunk_positions(L, N, causal, r, schedule="fold"):
+    return torch.tensor([p for p in range(L) if oracle.owner_rank(L, N, causal, p, schedule=schedule) == r],
+                        dtype=torch.long)
 
 
 def case_id(c):
-    return "B{}Hq{}Hkv{}L{}d{}N{}".format(*c[:6]) + ("c" if c[6] else "e") + ("s" if c[7] else "")
+    return "B{}Hq{}Hkv{}L{}d{}N{}".format(*c[:6]) + ("c" if c[6] else "e") + "-" + c[7]
 
 
-# (B, Hq, Hkv, L, d, N, causal, striped): chunks of whole 128-row tiles
+# (B, Hq, Hkv, L, d, N, causal, schedule): chunks of whole 128-row tiles
 STEP_CASES = [
-    (1, 4, 2, 1024, 128, 4, True, False),    # sub-chunks of one tile: every block spans both
-    (2, 2, 1, 1024, 64, 4, False, False),
-    (1, 2, 2, 1536, 128, 3, True, False),    # sub-chunks of two tiles
-    (1, 2, 1, 768, 64, 3, False, False),
-    (1, 3, 1, 3072, 128, 4, True, False),    # sub-chunks of three tiles: a block straddles them
-    (1, 4, 2, 1024, 128, 4, True, True),     # stripes: every step the same tile triangle
-    (1, 2, 1, 1536, 64, 3, True, True),
-    (1, 3, 1, 1280, 128, 5, True, True),     # L % 2N != 0: stripes only
-    (1, 2, 2, 1024, 64, 8, False, True),
+    (1, 4, 2, 1024, 128, 4, True, "fold"),    # sub-chunks of one tile: every block spans both
+    (2, 2, 1, 1024, 64, 4, False, "fold"),
+    (1, 2, 2, 1536, 128, 3, True, "fold"),    # sub-chunks of two tiles
+    (1, 2, 1, 768, 64, 3, False, "fold"),
+    (1, 3, 1, 3072, 128, 4, True, "fold"),    # sub-chunks of three tiles: a block straddles them
+    (1, 4, 2, 1024, 128, 4, True, "striped"),  # stripes: every step the same tile triangle
+    (1, 2, 1, 1536, 64, 3, True, "striped"),
+    (1, 3, 1, 1280, 128, 5, True, "striped"),  # L % 2N != 0: stripes only
+    (1, 2, 2, 1024, 64, 8, False, "striped"),
+    (1, 4, 2, 1024, 128, 4, True, "contiguous"),  # contiguous causal chunks: blocks below, on, above the diagonal
+    (1, 2, 1, 1280, 64, 5, True, "dfa"),          # the same blocks, DistFlashAttention's chunk map
 ]
 
 
 @pytest.mark.parametrize("case", STEP_CASES, ids=case_id)
 def test_every_step_of_a_small_ring_matches_the_oracle(case):
-    B, Hq, Hkv, L, d, N, causal, striped = case
+    B, Hq, Hkv, L, d, N, causal, schedule = case
     q, k, v, _ = inputs.make_inputs(B, Hq, Hkv, L, d, seed=sum(case[:6]))
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
     for r in range(N):
-        rows = chunk_positions(L, N, causal, r, striped)
+        rows = chunk_positions(L, N, causal, r, schedule)
         q_chunk = qd[:, :, rows.cuda()].contiguous()
         for src in range(N):
-            srows = chunk_positions(L, N, causal, src, striped)
+            srows = chunk_positions(L, N, causal, src, schedule)
             k_chunk = kd[:, :, srows.cuda()].contiguous()
             v_chunk = vd[:, :, srows.cuda()].contiguous()
-            o_s, lse_s = ra.ring_attn_fwd_step(q_chunk, k_chunk, v_chunk, N, causal, r, src, striped=striped)
+            o_s, lse_s = ra.ring_attn_fwd_step(q_chunk, k_chunk, v_chunk, N, causal, r, src, schedule=schedule)
             torch.cuda.synchronize()
             assert_status_ok()
             o_ref, lse_ref = oracle.ring_step(q.double(), k.double(), v.double(), causal, N, r, src,
-                                              striped=striped)
+                                              schedule=schedule)
             o_ref, lse_ref = o_ref[:, :, rows.numpy()], lse_ref[:, :, rows.numpy()]
             got_o, got_l = f64(o_s), f64(lse_s)
             empty = np.isneginf(lse_ref)
@@ -112,25 +117,35 @@ def test_merge_matches_the_oracle(d):
     assert torch.equal(o_out.cpu(), o.cpu().to(torch.bfloat16))
 
 
-# (B, Hq, Hkv, L, d, N, causal, striped)
+# (B, Hq, Hkv, L, d, N, causal, schedule)
 RING_CASES = [
-    (1, 4, 2, 1024, 128, 4, True, False),
-    (2, 2, 1, 1024, 64, 4, False, False),
-    (1, 3, 1, 3072, 128, 4, True, False),
-    (1, 4, 4, 4096, 64, 8, False, False),
-    (1, 2, 2, 1024, 128, 1, True, False),   # one rank: a single step, nothing to merge
-    (1, 4, 2, 1024, 128, 4, True, True),
-    (1, 2, 1, 1280, 128, 5, True, True),
+    (1, 4, 2, 1024, 128, 4, True, "fold"),
+    (2, 2, 1, 1024, 64, 4, False, "fold"),
+    (1, 3, 1, 3072, 128, 4, True, "fold"),
+    (1, 4, 4, 4096, 64, 8, False, "fold"),
+    (1, 2, 2, 1024, 128, 1, True, "fold"),   # one rank: a single step, nothing to merge
+    (1, 4, 2, 1024, 128, 4, True, "striped"),
+    (1, 2, 1, 1280, 128, 5, True, "striped"),
+    (1, 4, 2, 1024, 128, 4, True, "contiguous"),  # the unbalanced ring
+    (1, 4, 2, 1024, 128, 4, True, "dfa"),   # 3 launches, the last with workers 0, 1 idle
+    (1, 3, 1, 1280, 128, 5, True, "dfa"),   # odd N: 3 launches, all workers busy
+    (2, 2, 2, 2048, 64, 8, True, "dfa"),    # the pages' example: 8 workers, 5 launches
+    (1, 2, 1, 256, 128, 2, True, "dfa"),    # 2 launches, the second half idle
+    (1, 2, 2, 1024, 64, 1, True, "dfa"),    # one worker
 ]
+
+
+def _fused_chunks(L, N):
+    return N if L % (2 * N) == 0 else 1  # the fused kernels' fold needs L % 2N
 
 
 @pytest.mark.parametrize("case", RING_CASES, ids=case_id)
 def test_whole_ring_on_one_gpu_matches_the_oracle_and_the_fused_kernel(case):
-    B, Hq, Hkv, L, d, N, causal, striped = case
+    B, Hq, Hkv, L, d, N, causal, schedule = case
     q, k, v, _ = inputs.make_inputs(B, Hq, Hkv, L, d, seed=7 + sum(case[:6]))
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
-    o, lse = ra.ring_attn_ring_fwd(qd, kd, vd, N, causal, striped=striped)
-    o_f, lse_f = ra.ring_attn_fwd(qd, kd, vd, N if not striped or L % (2 * N) == 0 else 1, causal)
+    o, lse = ra.ring_attn_ring_fwd(qd, kd, vd, N, causal, schedule=schedule)
+    o_f, lse_f = ra.ring_attn_fwd(qd, kd, vd, _fused_chunks(L, N), causal)
     torch.cuda.synchronize()
     assert_status_ok()
     o_ref, lse_ref = oracle.fwd(q.double(), k.double(), v.double(), causal)
@@ -140,12 +155,12 @@ def test_whole_ring_on_one_gpu_matches_the_oracle_and_the_fused_kernel(case):
     check_fp32("lse (ring mode vs fused)", f64(lse), f64(lse_f), TOL_LSE)
 
 
-@pytest.mark.parametrize("striped", [False, True])
-def test_ring_mode_at_32k_on_sampled_rows(striped):
+@pytest.mark.parametrize("schedule", ["fold", "striped", "dfa"])
+def test_ring_mode_at_32k_on_sampled_rows(schedule):
     w = inputs.WORKLOADS["gqa_32k"]
     q, k, v, _ = inputs.workload_inputs(w)
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
-    o, lse = ra.ring_attn_ring_fwd(qd, kd, vd, w.n_chunks, w.causal, striped=striped)
+    o, lse = ra.ring_attn_ring_fwd(qd, kd, vd, w.n_chunks, w.causal, schedule=schedule)
     torch.cuda.synchronize()
     assert_status_ok()
     rows = inputs.sample_rows(w.L, w.n_chunks, w.causal, 64, seed=5)
@@ -156,11 +171,11 @@ def test_ring_mode_at_32k_on_sampled_rows(striped):
 
 @pytest.mark.parametrize("case", RING_CASES, ids=case_id)
 def test_ring_backward_matches_the_oracle_and_the_fused_kernel(case):
-    B, Hq, Hkv, L, d, N, causal, striped = case
+    B, Hq, Hkv, L, d, N, causal, schedule = case
     q, k, v, dO = inputs.make_inputs(B, Hq, Hkv, L, d, seed=13 + sum(case[:6]))
     qd, kd, vd, dOd = q.cuda(), k.cuda(), v.cuda(), dO.cuda()
     o, lse = ra.ring_attn_fwd(qd, kd, vd, 1, causal)
-    dq, dk, dv = ra.ring_attn_ring_bwd(qd, kd, vd, o, lse, dOd, N, causal, striped=striped)
+    dq, dk, dv = ra.ring_attn_ring_bwd(qd, kd, vd, o, lse, dOd, N, causal, schedule=schedule)
     dq_f, dk_f, dv_f = ra.ring_attn_bwd(qd, kd, vd, o, lse, dOd, 1, causal)
     torch.cuda.synchronize()
     assert_status_ok()
@@ -170,12 +185,12 @@ def test_ring_backward_matches_the_oracle_and_the_fused_kernel(case):
         check_bf16(f"{name} (ring mode vs fused)", f64(got), f64(fused), ulps=2)
 
 
-@pytest.mark.parametrize("striped", [False, True])
-def test_ring_backward_at_32k_matches_the_fused_kernel(striped):
+@pytest.mark.parametrize("schedule", ["fold", "striped", "dfa"])
+def test_ring_backward_at_32k_matches_the_fused_kernel(schedule):
     w = inputs.WORKLOADS["gqa_32k"]
     q, k, v, dO = (x.cuda() for x in inputs.workload_inputs(w))
     o, lse = ra.ring_attn_fwd(q, k, v, w.n_chunks, w.causal)
-    got = ra.ring_attn_ring_bwd(q, k, v, o, lse, dO, w.n_chunks, w.causal, striped=striped)
+    got = ra.ring_attn_ring_bwd(q, k, v, o, lse, dO, w.n_chunks, w.causal, schedule=schedule)
     want = ra.ring_attn_bwd(q, k, v, o, lse, dO, w.n_chunks, w.causal)
     torch.cuda.synchronize()
     assert_status_ok()

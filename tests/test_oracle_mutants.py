@@ -29,14 +29,22 @@ MUTANTS = {
     "ds_missing_D": ("const double dsij = pij * (dpij - D);", "const double dsij = pij * dpij;"),
     "dk_wrong_operand": ("dk[c] += P->scale * dsij * qi[c];", "dk[c] += P->scale * dsij * doi[c];"),
     "dv_uses_ds": ("dv[c] += pij * doi[c];", "dv[c] += dsij * doi[c];"),
-    "merge_wrong_sign": ("const double a = exp(lse - merged), w = exp(lse_s - merged);",
-                         "const double a = exp(lse - merged), w = exp(merged - lse_s);"),
+    "merge_wrong_sign": ("const double a = exp(*lse - merged), w = exp(lse_s - merged);",
+                         "const double a = exp(*lse - merged), w = exp(merged - lse_s);"),
     "fold_wrong_pair": ("return sub < N ? sub : 2 * N - 1 - sub;", "return sub < N ? sub : sub - N;"),
     "merge_weights_swapped": ("for (int c = 0; c < d; ++c) oa[c] = wa * oa[c] + wb * ob[c];",
                               "for (int c = 0; c < d; ++c) oa[c] = wb * oa[c] + wa * ob[c];"),
-    "step_wrong_source": ("if (!ring_block(P, t->n_chunks, b, h, i, t->src, s, o_s, &lse_s, t->striped)) {",
-                          "if (!ring_block(P, t->n_chunks, b, h, i, t->rank, s, o_s, &lse_s, t->striped)) {"),
-    "stripes_as_blocks": ("if (striped) return p % N;", "if (striped) return p / (L / N);"),
+    "step_wrong_source": ("if (!ring_block(P, t->n_chunks, b, h, i, t->src, s, o_s, &lse_s, t->schedule)) {",
+                          "if (!ring_block(P, t->n_chunks, b, h, i, t->rank, s, o_s, &lse_s, t->schedule)) {"),
+    "stripes_as_blocks": ("if (schedule == SCHED_STRIPED) return p % N;",
+                          "if (schedule == SCHED_STRIPED) return p / (L / N);"),
+    "dfa_helper_wrong_keys": ("    *q_chunk = N - t + w;\n    *kv_chunk = w;",
+                              "    *q_chunk = N - t + w;\n    *kv_chunk = (w - t + N) % N;"),
+    "dfa_middle_launch_doubled": ("  if (t < N - t) {", "  if (t <= N - t) {"),
+    "dfa_last_launch_dropped": ("for (int launch = 0; launch <= N / 2; ++launch)",
+                                "for (int launch = 0; launch < N / 2; ++launch)"),
+    "contiguous_as_fold": ("if (!causal || schedule != SCHED_FOLD) return p / (L / N);",
+                           "if (!causal) return p / (L / N);"),
     "ffn_residual_dropped": ("y[c] = x[c] + acc[c];", "y[c] = acc[c];"),
     "ffn_gelu_wrong_scale": ("return 0.5 * erfc(-x / sqrt(2.0));", "return 0.5 * erfc(-x / 2.0);"),
     "ffn_cdf_wrong_sign": ("return 0.5 * erfc(-x / sqrt(2.0));", "return 0.5 * erfc(x / sqrt(2.0));"),
@@ -71,6 +79,9 @@ def _quick_pins():
                            for c in (False, True) for st in (False, True)]),
         ("merge", steps.test_merge_weights_are_a_sigmoid_of_the_lse_gap),
         ("stripes", lambda: steps.test_striped_step_with_zero_queries_closed_form(3)),
+        ("dfa", lambda: [steps.test_contiguous_causal_ring_forms_equal_plain(L, N, sc)
+                         for L, N in ((48, 3), (64, 4), (60, 5)) for sc in ("contiguous", "dfa")]),
+        ("contiguous", lambda: steps.test_contiguous_step_with_zero_queries_closed_form(3)),
         ("ffn", lambda: [ffn_pins.test_ffn_matches_torch(7, 16, 64), ffn_pins.test_gelu_values()]),
         ("ffn_bwd", lambda: ffn_pins.test_ffn_backward_matches_torch_autograd(5, 8, 24)),
         ("rows", lambda: [pins.test_row_sampled_routines_agree_with_full(c) for c in (False, True)]),

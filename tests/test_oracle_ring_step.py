@@ -165,3 +165,96 @@ def test_striped_step_with_zero_queries_closed_form(N):
                 keys = [src + N * j for j in range(count)]
                 assert abs(lse_s[0, 0, pos] - math.log(count)) < 1e-13
                 np.testing.assert_allclose(o_s[0, 0, pos], v[0, 0, keys].mean(axis=0), rtol=0, atol=1e-13)
+
+
+# ------------------------------------------ contiguous causal chunks, DistFlashAttention
+
+@pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 8, 9])
+def test_dfa_schedule_runs_every_causal_block_once(N):
+    """DistFlashAttention's balanced schedule (section 7.2): over its launches
+    every block (query chunk a, key chunk b <= a) is computed exactly once,
+    no worker holds two blocks in one launch, the keys a helper uses are its
+    own chunk, and the launch count is N//2 + 1 -- every launch but an even
+    N's middle one keeps all N workers busy (the pages' example: N = 8, 8
+    ring steps become 5)."""
+    sched = oracle.dfa_schedule(N)
+    assert len(sched) == N // 2 + 1
+    seen = []
+    for t, launch in enumerate(sched):
+        workers = [w for w, _, _ in launch]
+        assert len(set(workers)) == len(workers)
+        busy = len(launch)
+        assert busy == (N // 2 if (N % 2 == 0 and t == N // 2 and N > 1) else N)
+        for w, a, b in launch:
+            assert b <= a
+            if w != a:  # a helper: a later worker's block, on the helper's own keys
+                assert b == w and a > w
+            seen.append((a, b))
+    want = sorted((a, b) for a in range(N) for b in range(a + 1))
+    assert sorted(seen) == want
+    if N == 8:
+        assert len(sched) == 5
+
+
+@pytest.mark.parametrize("schedule", ["contiguous", "dfa"])
+@pytest.mark.parametrize("L,N", [(48, 2), (48, 3), (64, 4), (60, 5), (64, 8)])
+def test_contiguous_causal_ring_forms_equal_plain(L, N, schedule):
+    """Contiguous causal chunks, merged in plain ring order or in
+    DistFlashAttention's launch order: the plain definition to 1e-12."""
+    q, k, v = _problem(1, 4, 2, L, 8, seed=7 * L + N)
+    o_ref, lse_ref = oracle.fwd(q, k, v, True)
+    o, lse = oracle.ring_fwd(q, k, v, True, N, schedule=schedule)
+    np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_ref, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("N", [2, 4, 5])
+def test_dfa_blocks_merged_in_launch_order_equal_plain(N):
+    """The launches run block by block: every block of the schedule as a ring
+    step of the oracle (query chunk a against key chunk b), merged into its
+    query chunk in launch order, gives the plain definition."""
+    C = 6
+    L = N * C
+    q, k, v = _problem(1, 2, 1, L, 8, seed=N)
+    o_ref, lse_ref = oracle.fwd(q, k, v, True)
+    o = np.zeros((1, 2, L, 8))
+    lse = np.full((1, 2, L), -np.inf)
+    for launch in oracle.dfa_schedule(N):
+        for _, a, b in launch:
+            o_s, lse_s = oracle.ring_step(q, k, v, True, N, a, b, schedule="dfa")
+            o, lse = oracle.merge(o, lse, o_s, lse_s)
+    np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_ref, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("N", [2, 3, 4])
+def test_contiguous_step_with_zero_queries_closed_form(N):
+    """q = 0: chunk a against key chunk b < a sees all C keys of b (mean of
+    them, lse = log C); against itself a prefix (row i of the chunk sees i+1
+    keys); against b > a nothing (lse = -inf)."""
+    C = 5
+    L = N * C
+    rng = np.random.default_rng(10 + N)
+    q = np.zeros((1, 1, L, 4))
+    k = rng.standard_normal((1, 1, L, 4))
+    v = rng.standard_normal((1, 1, L, 4))
+    for a in range(N):
+        assert [oracle.owner_rank(L, N, True, p, schedule="dfa") for p in range(a * C, a * C + C)] == [a] * C
+        for b in range(N):
+            o_s, lse_s = oracle.ring_step(q, k, v, True, N, a, b, schedule="contiguous")
+            for i in range(C):
+                pos = a * C + i
+                count = C if b < a else (i + 1 if b == a else 0)
+                if count == 0:
+                    assert lse_s[0, 0, pos] == -np.inf and np.all(o_s[0, 0, pos] == 0)
+                    continue
+                keys = list(range(b * C, b * C + count))
+                assert abs(lse_s[0, 0, pos] - math.log(count)) < 1e-13
+                np.testing.assert_allclose(o_s[0, 0, pos], v[0, 0, keys].mean(axis=0), rtol=0, atol=1e-13)
+
+
+def test_contiguous_schedules_need_causal():
+    q, k, v = _problem(1, 1, 1, 16, 4, seed=0)
+    for schedule in ("contiguous", "dfa"):
+        with pytest.raises(ValueError):
+            oracle.ring_fwd(q, k, v, False, 2, schedule=schedule)

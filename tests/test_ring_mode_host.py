@@ -16,10 +16,11 @@ def lib():
     return capi.load()
 
 
-def _chunk_positions(L, N, causal, r, striped=False):
+def _chunk_positions(L, N, causal, r, striped=False, schedule=None):
     """Sequence positions of rank r's rows in chunk order (ascending: for the
-    fold that is sub-chunk r, then sub-chunk 2N-1-r; r, r+N, ... striped)."""
-    return np.array([p for p in range(L) if oracle.owner_rank(L, N, causal, p, striped) == r])
+    fold that is sub-chunk r, then sub-chunk 2N-1-r; r, r+N, ... striped;
+    rows [rC, (r+1)C) for the contiguous schedules)."""
+    return np.array([p for p in range(L) if oracle.owner_rank(L, N, causal, p, striped, schedule) == r])
 
 
 CASES = [(1024, 4, True, False), (1024, 4, False, False), (2048, 4, True, False), (1536, 3, True, False),
@@ -171,3 +172,87 @@ def test_usp_workspace_and_arguments(lib):
     bargs = [P256] * 9
     assert lib.ring_attn_usp_bwd(*bargs, 1, 4, 2, 1024, 64, 2, 2, 1, P256, ws - 1, NUL) == capi.ERR_WORKSPACE
     assert lib.ring_attn_usp_bwd(*bargs, 1, 4, 2, 1024, 96, 2, 2, 1, P256, ws, NUL) == capi.ERR_UNSUPPORTED
+
+
+# ------------------------------------------------ schedules (DistFlashAttention)
+
+@pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 8, 16, 32])
+def test_schedule_pairs_match_the_oracle(lib, N):
+    """The library's schedule (include/ring_attn.h) against the oracle's
+    reading of the pages: DistFlashAttention's launches (section 7.2), and
+    ring steps (w, (w - s) mod N) for the ring schedules."""
+    assert capi.schedule_pairs(N, "dfa") == oracle.dfa_schedule(N)
+    assert capi.schedule_launches(N, "dfa") == N // 2 + 1
+    for sched in ("fold", "striped", "contiguous"):
+        assert capi.schedule_launches(N, sched) == N
+        assert capi.schedule_pairs(N, sched) == [[(w, w, (w - s) % N) for w in range(N)] for s in range(N)]
+
+
+DFA_CASES = [(1024, 4), (1280, 5), (2048, 8), (768, 3), (256, 2)]
+
+
+@pytest.mark.parametrize("schedule", ["contiguous", "dfa"])
+@pytest.mark.parametrize("L,N", DFA_CASES)
+def test_contiguous_step_plans_list_exactly_the_visible_tile_pairs(lib, L, N, schedule):
+    C = L // N
+    nt = C // 128
+    pairs = {(t, w): (a, b) for t, launch in enumerate(capi.schedule_pairs(N, schedule)) for w, a, b in launch}
+    for t in range(capi.schedule_launches(N, schedule)):
+        for w in range(N):
+            plan = capi.step_plan(L, N, True, t, w, schedule=schedule)
+            assert len(plan["visits"]) == (C + 255) // 256
+            if (t, w) not in pairs:  # idle worker: nothing listed
+                assert all(not v for v in plan["visits"])
+                continue
+            a, b = pairs[(t, w)]
+            qpos = _chunk_positions(L, N, True, a, schedule=schedule)
+            kpos = _chunk_positions(L, N, True, b, schedule=schedule)
+            assert np.array_equal(qpos, np.arange(a * C, (a + 1) * C))
+            for u, visits in enumerate(plan["visits"]):
+                listed = [kt for lo, hi in visits for kt in range(lo, hi)]
+                want = set()
+                for qt in (2 * u, 2 * u + 1):
+                    if qt >= nt:
+                        continue
+                    qmax = qpos[qt * 128:(qt + 1) * 128].max()
+                    want |= {kt for kt in range(nt) if kpos[kt * 128:(kt + 1) * 128].min() <= qmax}
+                assert listed == sorted(want), (t, w, u)
+
+
+@pytest.mark.parametrize("N", [2, 3, 4, 8])
+def test_dfa_launches_after_the_first_give_every_busy_worker_a_whole_block(lib, N):
+    """After the diagonal launch every busy worker runs one whole C x C block
+    (its key chunk lies before its query chunk), so the launches are
+    balanced; the plain contiguous ring leaves worker w idle from step w + 1
+    on (the waiting the pages' figure shows)."""
+    L = 256 * N
+    nt = L // N // 128
+    for t in range(1, N // 2 + 1):
+        for w in range(N):
+            plan = capi.step_plan(L, N, True, t, w, schedule="dfa")
+            listed = sum(hi - lo for v in plan["visits"] for lo, hi in v)
+            busy = w >= t or t < N - t
+            assert listed == (nt if busy else 0)  # the block's one 256-row item visits every key tile
+    for s in range(N):
+        for w in range(N):
+            plan = capi.step_plan(L, N, True, s, w, schedule="contiguous")
+            listed = sum(hi - lo for v in plan["visits"] for lo, hi in v)
+            assert (listed > 0) == (s <= w)
+
+
+def test_contiguous_schedules_reject_bad_arguments(lib):
+    def step(L=1024, N=4, causal=1, sched=3, ptr=P256):
+        return lib.ring_attn_fwd_step(ptr, ptr, ptr, ptr, ptr, 1, 2, 1, L, 64, N, causal, sched, 0, 0, NUL)
+    assert step(causal=0) == capi.ERR_UNSUPPORTED           # defined for causal attention only
+    assert step(causal=0, sched=2) == capi.ERR_UNSUPPORTED
+    assert step(sched=4) == capi.ERR_UNSUPPORTED
+    assert step(L=1280, N=5, ptr=NUL) == capi.ERR_NULL      # L % N suffices (chunks of 256 rows)
+    assert step(L=600, N=5) == capi.ERR_UNSUPPORTED          # chunks of 120 rows: not whole tiles
+    assert lib.ring_attn_schedule_launches(0, 3) == capi.ERR_SHAPE
+    a, b = ctypes.c_int(), ctypes.c_int()
+    assert lib.ring_attn_schedule_pair(4, 3, 3, 0, ctypes.byref(a), ctypes.byref(b)) == capi.ERR_SHAPE
+    assert lib.ring_attn_schedule_pair(4, 3, 2, 0, ctypes.byref(a), ctypes.byref(b)) == 0   # middle launch: idle
+    assert lib.ring_attn_schedule_pair(4, 3, 1, 0, ctypes.byref(a), ctypes.byref(b)) == 1
+    assert (a.value, b.value) == (3, 0)
+    assert lib.ring_attn_ring_fwd_workspace_size(1, 2, 1, 1280, 64, 5, 1, 3) > 0
+    assert lib.ring_attn_ring_fwd_workspace_size(1, 2, 1, 1280, 64, 5, 0, 3) == 0
