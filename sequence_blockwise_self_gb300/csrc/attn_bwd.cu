@@ -45,10 +45,12 @@
 // (S^T has been read by then; the next S^T waits for the dQ drain).  Packed
 // P^T of warpgroup h occupies [128+64h, 128+64h+32).
 //
-// Product order per query tile i: S^T(i), dP^T(i) | dQ(i), dV(i), dK(i).
-// dQ(i) is signalled on its own, so its drain from tensor memory overlaps
-// dV(i) and dK(i), and S^T(i+1) (over the drained dQ columns) follows dK(i)
-// on the tensor core without a gap.
+// Product order per query tile i: dP^T(i), S^T(i) | dV(i), dK(i) one
+// 16-query k-step at a time, each as soon as the compute warps have finished
+// that chunk of P^T / dS^T (chunk_ready), so the tensor core runs them
+// during the softmax-gradient phase | dQ(i).  dP^T(i+1) then overlaps the
+// drain of dQ(i) from tensor memory, and S^T(i+1) (over the drained dQ
+// columns) follows it.
 //
 // Buffers: K, V stationary; Q (with its rows' lse and D) and dO double
 // buffered; dS^T single.  The dQ drain of tile i stages fp32 in the Q and
@@ -56,8 +58,8 @@
 // warpgroup 0's half tile in Q, warpgroup 1's in dO, each in the
 // accumulator's own layout.  Warp 3 adds each half into the accumulator
 // with one 1-D bulk reduce-add, waits until it has read shared memory and
-// then hands the buffer back to the producer (Q first: S^T(i+2) needs only
-// Q), so no compute warp ever waits on a bulk copy.  (Vector atomics from
+// then hands the buffer back to the producer (dO first: dP^T(i+2) is the
+// first product of tile i+2), so no compute warp ever waits on a bulk copy.  (Vector atomics from
 // registers instead of bulk reduce-adds ran slower, with either row layout
 // of the accumulator; both paths reduce at the same per-SM rate, ~21 B/clk
 // with every SM busy.)
@@ -91,7 +93,9 @@ struct BwdSmem {
   alignas(8) uint64_t do_full[2];
   alignas(8) uint64_t do_empty[2];
   alignas(8) uint64_t s_full;
-  alignas(8) uint64_t ds_full;
+  // P^T and dS^T of query columns [16c, 16c+16) of both halves are in
+  // place (one arrival per compute warp)
+  alignas(8) uint64_t chunk_ready[4];
   alignas(8) uint64_t dq_full;
   alignas(8) uint64_t dq_free;
   alignas(8) uint64_t qdo_read;    // dV(i), dK(i) done: Q(i), dO(i) free for staging
@@ -185,9 +189,18 @@ __device__ void bwd_producer(BwdSmem<D>& sm, const CUtensorMap* tm_q, const CUte
   }
   bool ok = true;
   uint32_t nq = 0, ndo = 0;  // Q and dO fills issued
+  // dO(i) first: dP^T(i) is the tile's first product, and the dQ reducer
+  // hands the dO buffer back first
   for (QIter qi(rg, nr); qi.valid() && ok; qi.next()) {
-    const uint32_t i = nq;
+    const uint32_t i = ndo;
     const uint32_t slot = i & 1;
+    if (i >= 2) ok = mbar_wait(smem_u32(&sm.do_empty[slot]), ((i >> 1) - 1) & 1, ab, err, kSiteBwdProducer);
+    if (!ok) break;
+    const uint32_t db = smem_u32(&sm.do_full[slot]);
+    mbar_arrive_expect_tx(db, S::kTile);
+    for (int sub = 0; sub < S::kSub; ++sub)
+      tma_load_3d(smem_u32(sm.dO[slot]) + sub * 16384, tm_do, db, sub * 64, qi.it * 128, q_z);
+    ++ndo;
     if (i >= 2) ok = mbar_wait(smem_u32(&sm.q_empty[slot]), ((i >> 1) - 1) & 1, ab, err, kSiteBwdProducer);
     if (!ok) break;
     const uint32_t qb = smem_u32(&sm.q_full[slot]);
@@ -198,13 +211,6 @@ __device__ void bwd_producer(BwdSmem<D>& sm, const CUtensorMap* tm_q, const CUte
     bulk_load_1d(smem_u32(sm.lse2[slot]), p.lse2 + roff, 512, qb);
     bulk_load_1d(smem_u32(sm.dvec[slot]), p.dvec + roff, 512, qb);
     ++nq;
-    if (i >= 2) ok = mbar_wait(smem_u32(&sm.do_empty[slot]), ((i >> 1) - 1) & 1, ab, err, kSiteBwdProducer);
-    if (!ok) break;
-    const uint32_t db = smem_u32(&sm.do_full[slot]);
-    mbar_arrive_expect_tx(db, S::kTile);
-    for (int sub = 0; sub < S::kSub; ++sub)
-      tma_load_3d(smem_u32(sm.dO[slot]) + sub * 16384, tm_do, db, sub * 64, qi.it * 128, q_z);
-    ++ndo;
   }
   if (!ok) {
     // Let every copy this thread issued land before the CTA exits.
@@ -233,22 +239,9 @@ __device__ void bwd_mma(BwdSmem<D>& sm, uint32_t tmem, uint32_t n_total, volatil
   for (uint32_t i = 0; i < n_total && ok; ++i) {
     const uint32_t slot = i & 1;
     const uint32_t qa = smem_u32(sm.q[slot]), da = smem_u32(sm.dO[slot]);
-    // Q(i) is refilled before dO(i) (the reduce warp returns the Q buffer
-    // first), so S^T(i) goes as soon as Q(i) and the dQ(i-1) columns are
-    // there, and dP^T(i) waits for dO(i) on its own.
-    ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.q_full[slot]), (i >> 1) & 1, ab, err, kSiteBwdMma));
-    if (ok && i > 0) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.dq_free), (i - 1) & 1, ab, err, kSiteBwdMma));
-    if (!ok) break;
-    tc_fence_after();
-    // S^T = K Q^T and dP^T = V dO^T (both operands K-major).  S^T overwrites
-    // dQ(i-1), whose drain released dq_free; dP^T overwrites the packed P^T
-    // of the previous tile, read by dV(i-1), which the tensor core ran
-    // before these.
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-      umma_ss_warp(t_s, sdesc_sw128(ka + off, 16, 1024), sdesc_sw128(qa + off, 16, 1024), kIdS, kk > 0);
-    }
+    // dP^T = V dO^T first: it overwrites the packed P^T of the previous
+    // tile, which dV(i-1) read earlier in this thread's issue order, so it
+    // waits only for dO(i) and runs while the compute warps drain dQ(i-1).
     ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.do_full[slot]), (i >> 1) & 1, ab, err, kSiteBwdMma));
     if (!ok) break;
     tc_fence_after();
@@ -257,30 +250,48 @@ __device__ void bwd_mma(BwdSmem<D>& sm, uint32_t tmem, uint32_t n_total, volatil
       const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
       umma_ss_warp(t_dp, sdesc_sw128(va + off, 16, 1024), sdesc_sw128(da + off, 16, 1024), kIdS, kk > 0);
     }
-    umma_commit_warp(smem_u32(&sm.s_full));
-    ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.ds_full), i & 1, ab, err, kSiteBwdMma));
+    // S^T = K Q^T (both operands K-major) overwrites dQ(i-1): it waits for
+    // Q(i) and for the drain of dQ(i-1) (dq_free).
+    ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.q_full[slot]), (i >> 1) & 1, ab, err, kSiteBwdMma));
+    if (ok && i > 0) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.dq_free), (i - 1) & 1, ab, err, kSiteBwdMma));
     if (!ok) break;
     tc_fence_after();
-    // dQ = dS K : A = dS (MN-major view of dS^T), B = K (MN-major)
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+      umma_ss_warp(t_s, sdesc_sw128(ka + off, 16, 1024), sdesc_sw128(qa + off, 16, 1024), kIdS, kk > 0);
+    }
+    umma_commit_warp(smem_u32(&sm.s_full));
+    // dV += P^T dO and dK += dS^T Q one query k-step (16 queries) at a
+    // time, as the compute warps finish each 16-column chunk c of both
+    // halves: k-steps c (warpgroup 0's half) and 4 + c (warpgroup 1's), so
+    // the tensor core works while the softmax-gradient phase runs.
+    //   dV: A = packed P^T in tensor memory (k-step kk at column
+    //       128 + 64 (kk/4) + 8 (kk%4)), B = dO (MN-major)
+    //   dK: A = dS^T (K-major), B = Q (MN-major)
+    for (int c = 0; c < 4 && ok; ++c) {
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.chunk_ready[c]), i & 1, ab, err, kSiteBwdMma));
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int kk = 4 * h + c;
+        umma_ts_warp(t_dv, tmem + 128 + 64 * h + 8 * c, sdesc_sw128(da + kk * 2048, 16384, 1024), kIdKV,
+                     (i > 0 || kk > 0) ? 1u : 0u);
+        umma_ss_warp(t_dk, sdesc_sw128(sa + h * 16384 + c * 32, 16, 1024), sdesc_sw128(qa + kk * 2048, 16384, 1024),
+                     kIdKV, (i > 0 || kk > 0) ? 1u : 0u);
+      }
+    }
+    if (!ok) break;
+    umma_commit_warp(smem_u32(&sm.qdo_read));  // Q(i), dO(i) no longer read: free for the dQ staging
+    // dQ = dS K : A = dS (MN-major view of dS^T), B = K (MN-major); the
+    // last chunk_ready covers every chunk of dS^T.  Over the S^T columns
+    // for d = 128 (read by then).
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
       umma_ss_warp(t_dq, sdesc_sw128(sa + kk * 2048, 16384, 1024), sdesc_sw128(ka + kk * 2048, 16384, 1024), kIdQ,
                    kk > 0);
     umma_commit_warp(smem_u32(&sm.dq_full));
-    // dV += P^T dO : A = packed P^T in tensor memory (query k-step kk lives
-    // in warpgroup kk/4's columns), B = dO (MN-major)
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk)
-      umma_ts_warp(t_dv, tmem + 128 + 64 * (kk >> 2) + 8 * (kk & 3), sdesc_sw128(da + kk * 2048, 16384, 1024), kIdKV,
-                   (i > 0 || kk > 0) ? 1u : 0u);
-    // dK += dS^T Q : A = dS^T (K-major), B = Q (MN-major)
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-      umma_ss_warp(t_dk, sdesc_sw128(sa + off, 16, 1024), sdesc_sw128(qa + kk * 2048, 16384, 1024), kIdKV,
-                   (i > 0 || kk > 0) ? 1u : 0u);
-    }
-    umma_commit_warp(smem_u32(&sm.qdo_read));
   }
   if (ok) {
     umma_commit_warp(smem_u32(&sm.kv_final));
@@ -305,19 +316,20 @@ __device__ void bwd_dq_reducer(BwdSmem<D>& sm, float* dq_acc, int Lpad, int q_z,
     ok = mbar_wait(smem_u32(&sm.stage_full[slot]), (i >> 1) & 1, ab, err, kSiteBwdReducer);
     if (!ok) break;
     const int q0 = qi.it * 128;
-    // warpgroup 0's half tile (staged in the Q buffer), then warpgroup 1's
-    // (in the dO buffer), as two groups: Q goes back to the producer (which
-    // refills it first) as soon as its half has been read
+    // warpgroup 1's half tile (staged in the dO buffer), then warpgroup 0's
+    // (in the Q buffer), as two groups: dO goes back to the producer (which
+    // refills it first, for the tile's first product) as soon as its half
+    // has been read
     float* const dst = dq_acc + dq_acc_offset<D>(q_z, Lpad, q0, 0);
     constexpr uint32_t kHalf = 128 * (D / 2) * 4;
-    bulk_reduce_add_f32(dst, smem_u32(sm.q[slot]), kHalf);
-    bulk_commit_group();
     bulk_reduce_add_f32(dst + kHalf / 4, smem_u32(sm.dO[slot]), kHalf);
     bulk_commit_group();
+    bulk_reduce_add_f32(dst, smem_u32(sm.q[slot]), kHalf);
+    bulk_commit_group();
     bulk_wait_group_read<1>();
-    mbar_arrive(smem_u32(&sm.q_empty[slot]));
-    bulk_wait_group_read<0>();
     mbar_arrive(smem_u32(&sm.do_empty[slot]));
+    bulk_wait_group_read<0>();
+    mbar_arrive(smem_u32(&sm.q_empty[slot]));
   }
   bulk_wait_group<0>();
 }
@@ -394,6 +406,16 @@ __device__ void bwd_compute(BwdSmem<D>& sm, uint32_t tmem, const BwdDev& p, cons
       st_shared_v4(sa + wg * 16384 + sw128_offset(row, ch), dk8[0], dk8[1], dk8[2], dk8[3]);
       st_shared_v4(sa + wg * 16384 + sw128_offset(row, ch + 1), dk8[4], dk8[5], dk8[6], dk8[7]);
     };
+    // chunk c of this warp's rows is in place -- P^T in tensor memory, dS^T
+    // in shared memory, made visible to the tensor core's async proxy -- so
+    // the MMA warp may run the chunk's dV and dK k-steps
+    auto signal = [&](int c) {
+      tmem_wait_st();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm.chunk_ready[c]));
+    };
     {
       uint32_t sA[16], pA[16], sB[16], pB[16];
       tmem_ld16_async(t_s, sA);
@@ -403,24 +425,24 @@ __device__ void bwd_compute(BwdSmem<D>& sm, uint32_t tmem, const BwdDev& p, cons
       tmem_ld16_async(t_s + 16, sB);
       tmem_ld16_async(t_dp + 16, pB);
       process(0, sA, pA);
+      signal(0);
       tmem_wait_ld(sB);
       reg_fence(pB);
       tmem_ld16_async(t_s + 32, sA);
       tmem_ld16_async(t_dp + 32, pA);
       process(1, sB, pB);
+      signal(1);
       tmem_wait_ld(sA);
       reg_fence(pA);
       tmem_ld16_async(t_s + 48, sB);
       tmem_ld16_async(t_dp + 48, pB);
       process(2, sA, pA);
+      signal(2);
       tmem_wait_ld(sB);
       reg_fence(pB);
       process(3, sB, pB);
+      signal(3);
     }
-    tmem_wait_st();
-    fence_proxy_async_smem();
-    tc_fence_before();
-    mbar_arrive(smem_u32(&sm.ds_full));
     // dQ drain: this thread's dQ row (a query row), this half's columns,
     // leaves tensor memory in one batched load; the columns are released at
     // once, then the row is staged as fp32 in the tile's Q and dO buffers
@@ -562,7 +584,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(smem_u32(&sm.do_empty[s]), 1);
     }
     mbar_init(smem_u32(&sm.s_full), 1);
-    mbar_init(smem_u32(&sm.ds_full), 256);
+    for (int c = 0; c < 4; ++c) mbar_init(smem_u32(&sm.chunk_ready[c]), 8);
     mbar_init(smem_u32(&sm.dq_full), 1);
     mbar_init(smem_u32(&sm.dq_free), 256);
     mbar_init(smem_u32(&sm.qdo_read), 1);
