@@ -471,8 +471,9 @@ def run_ours(args, w):
         del dev_in, dev_out
 
     # (4) ring mode: the same forward run step by step the way each rank of a
-    # multi-GPU ring runs it (every rank's step s in one launch, then the
-    # log-sum-exp merge), on this GPU; its merge kernel is HBM-bound
+    # multi-GPU ring runs it (every rank's block of a schedule launch in one
+    # kernel launch, accumulated into the running result), on this GPU, for
+    # each causal schedule; and the standalone merge kernel (HBM-bound)
     ring = None
     if not args.no_ring_mode:
         def measure_ring(schedule):
@@ -517,18 +518,6 @@ def run_ours(args, w):
             st, site = ra.device_status()
             if st != 0:
                 raise RuntimeError(f"device status {st} at site {site:#x} in ring mode")
-            merge_ms, merge_n = rp["ring_merge"]
-            # rows merged per forward: every row at each launch after the first
-            # (ring steps); DistFlashAttention: chunks t..N-1 and, unless t is
-            # the middle launch, the t chunks the idle workers helped
-            N = w.n_chunks
-            chunk_rows = w.B * w.Hq * (w.L // N)
-            if schedule == "dfa":
-                merged_rows = sum((N - t) + (t if t < N - t else 0) for t in range(1, N // 2 + 1)) * chunk_rows
-            else:
-                merged_rows = (N - 1) * N * chunk_rows
-            merge_bytes = merged_rows * (3 * w.d * 4 + 3 * 4)  # read o, o_s, lse, lse_s; write o, lse
-            merge_gbs = merge_bytes / (merge_ms / args.steps * 1e-3) / 1e9 if merge_n else None
             del ws_b, g_r
             return {
                 "fwd_ms": ms_ring, "fwd_tflops": F / (ms_ring * 1e-3) / 1e12,
@@ -536,10 +525,33 @@ def run_ours(args, w):
                 "fwd_bwd_tflops": step_flops / ((ms_ring + ms_ring_bwd) * 1e-3) / 1e12,
                 "per_kernel_ms_per_fwd": {k: rp[k][0] / args.steps for k in ("ring_step", "ring_merge", "ring_io")},
                 "launches_per_fwd": {k: rp[k][1] // args.steps for k in ("ring_step", "ring_merge", "ring_io")},
-                "merge_roofline": {"bound": "hbm", "achieved": merge_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                                   "frac": (merge_gbs / peaks["hbm_gbs"]) if merge_gbs else None,
-                                   "bytes_per_fwd": merge_bytes},
             }
+
+        def measure_merge():
+            # the standalone log-sum-exp merge (the building block a multi-GPU
+            # ring uses between receiving a partial result and the next step):
+            # one merge over every row of the workload, HBM-bound
+            rows = w.B * w.Hq * w.L
+            o_a = torch.zeros((rows, w.d), dtype=torch.float32, device=dev)
+            o_b = torch.zeros_like(o_a)
+            l_a = torch.zeros((rows,), dtype=torch.float32, device=dev)
+            l_b = torch.zeros_like(l_a)
+            for _ in range(3):
+                ra.ring_attn_merge(o_a, l_a, o_b, l_b, stream=stream)
+            torch.cuda.synchronize(dev)
+            m0, m1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            m0.record(stream)
+            for _ in range(args.steps):
+                ra.ring_attn_merge(o_a, l_a, o_b, l_b, stream=stream)
+            m1.record(stream)
+            torch.cuda.synchronize(dev)
+            ms = m0.elapsed_time(m1) / args.steps
+            nbytes = rows * (3 * w.d * 4 + 3 * 4)  # read o, o_s, lse, lse_s; write o, lse
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            del o_a, o_b, l_a, l_b
+            return {"ms": ms, "bytes_per_launch": nbytes,
+                    "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                 "frac": gbs / peaks["hbm_gbs"]}}
 
         C = w.L // w.n_chunks
         ring = {}
@@ -550,6 +562,8 @@ def run_ours(args, w):
             # DistFlashAttention's balanced one (N/2 + 1 launches)
             for sched in ("striped", "contiguous", "dfa"):
                 ring[sched] = measure_ring(sched)
+        if ring:
+            ring["merge"] = measure_merge()
         ring = ring or None
 
     # (5) Ulysses on this GPU at the largest degree the heads allow (<= 8):

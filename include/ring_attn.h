@@ -173,6 +173,21 @@ int ring_attn_fwd_step(const void* q_chunk, const void* k_chunk, const void* v_c
                        cudaStream_t stream);
 
 /*
+ * The same block, accumulated into a running result instead of returned as
+ * a partial one: (o_run, lse_run) -- fp32 [B][Hq][C][d] and [B][Hq][C],
+ * rank's rows in chunk order -- hold the result of the blocks merged so far
+ * and are overwritten with that result merged with this block's (what
+ * ring_attn_fwd_step followed by ring_attn_merge gives, without writing the
+ * partial result or reading it back).  The kernel continues its online
+ * softmax from the running state.  lse_run = -inf (and o_run = 0) is the
+ * empty result; rows that see none of src's keys keep theirs.  The order in
+ * which a rank's blocks are accumulated changes only the rounding.
+ */
+int ring_attn_fwd_step_accumulate(const void* q_chunk, const void* k_chunk, const void* v_chunk, float* o_run,
+                                  float* lse_run, int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal,
+                                  int schedule, int rank, int src, cudaStream_t stream);
+
+/*
  * Merge of two partial results of the same n_rows rows of width d (64 or
  * 128), in place: lse <- log(e^lse + e^lse_s), o <- e^(lse_old - lse) o +
  * e^(lse_s - lse) o_s; a side with lse = -inf contributes nothing.  o, o_s
@@ -190,14 +205,14 @@ size_t ring_attn_ring_fwd_workspace_size(int B, int Hq, int Hkv, int L, int d, i
  * The whole ring on one GPU, every worker of it, the ring-mode way: q, k, v
  * (sequence order, as for ring_attn_fwd) are gathered into chunk order; at
  * each launch of the schedule one kernel launch runs every worker's block
- * (ring steps: worker r against chunk (r - s) mod n_chunks) and merges fold
- * each worker's partial result into the running fp32 result of the block's
- * query chunk (DistFlashAttention: two merges per launch, the workers' own
- * chunks and the chunks they helped); the result is scattered back to
- * sequence order into o (bf16) and lse (fp32), as ring_attn_fwd writes
- * them.  `workspace` (caller-owned device memory of
- * ring_attn_ring_fwd_workspace_size() bytes, 256-byte aligned) holds the
- * gathered chunks, the running result and one launch's partial results.
+ * (ring steps: worker r against chunk (r - s) mod n_chunks), each
+ * accumulated into the running fp32 result of its query chunk as
+ * ring_attn_fwd_step_accumulate does (DistFlashAttention: two kernel
+ * launches per schedule launch, the workers' own chunks, then the chunks the
+ * idle workers took over); the result is scattered back to sequence order
+ * into o (bf16) and lse (fp32), as ring_attn_fwd writes them.  `workspace`
+ * (caller-owned device memory of ring_attn_ring_fwd_workspace_size() bytes,
+ * 256-byte aligned) holds the gathered chunks and the running result.
  */
 int ring_attn_ring_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                        int L, int d, int n_chunks, int causal, int schedule, void* workspace, size_t workspace_bytes,

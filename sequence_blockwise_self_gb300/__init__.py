@@ -43,6 +43,7 @@ from .capi import (  # noqa: F401
     bpt_workspace_size,
     bpt_bwd_workspace_size,
     ring_attn_fwd_step,
+    ring_attn_fwd_step_accumulate,
     ring_attn_merge,
     ring_attn_ring_fwd,
     ring_fwd_workspace_size,

@@ -79,6 +79,8 @@ def load():
     lib.ring_attn_schedule_pair.restype = I
     lib.ring_attn_fwd_step.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, P]
     lib.ring_attn_fwd_step.restype = I
+    lib.ring_attn_fwd_step_accumulate.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, P]
+    lib.ring_attn_fwd_step_accumulate.restype = I
     lib.ring_attn_merge.argtypes = [P, P, P, P, ctypes.c_longlong, I, P, P]
     lib.ring_attn_merge.restype = I
     lib.ring_attn_ring_fwd_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
@@ -278,6 +280,27 @@ def ring_attn_fwd_step(q_chunk, k_chunk, v_chunk, n_chunks: int, causal: bool, r
     if rc != OK:
         raise RingAttnError(rc, "ring_attn_fwd_step")
     return o_s, lse_s
+
+
+def ring_attn_fwd_step_accumulate(q_chunk, k_chunk, v_chunk, o_run, lse_run, n_chunks: int, causal: bool, rank: int,
+                                  src: int, stream=None, striped: bool = False, schedule=None):
+    """The block of ring_attn_fwd_step (rank's queries, src's keys) merged
+    in place into the running fp32 result (o_run [B,Hq,C,d], lse_run
+    [B,Hq,C]; lse_run = -inf is the empty result).  Returns (o_run, lse_run)."""
+    import torch
+    B, Hq, C, d = q_chunk.shape
+    Hkv = k_chunk.shape[1]
+    _check_tensor(q_chunk, "q_chunk", torch.bfloat16, (B, Hq, C, d))
+    _check_tensor(k_chunk, "k_chunk", torch.bfloat16, (B, Hkv, C, d))
+    _check_tensor(v_chunk, "v_chunk", torch.bfloat16, (B, Hkv, C, d))
+    _check_tensor(o_run, "o_run", torch.float32, (B, Hq, C, d))
+    _check_tensor(lse_run, "lse_run", torch.float32, (B, Hq, C))
+    rc = load().ring_attn_fwd_step_accumulate(_ptr(q_chunk), _ptr(k_chunk), _ptr(v_chunk), _ptr(o_run), _ptr(lse_run),
+                                              B, Hq, Hkv, C * int(n_chunks), d, int(n_chunks), int(bool(causal)),
+                                              schedule_code(striped, schedule), int(rank), int(src), _stream(stream))
+    if rc != OK:
+        raise RingAttnError(rc, "ring_attn_fwd_step_accumulate")
+    return o_run, lse_run
 
 
 def ring_attn_merge(o, lse, o_s, lse_s, o_out=None, stream=None):

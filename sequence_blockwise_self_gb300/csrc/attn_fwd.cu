@@ -83,6 +83,11 @@ struct FwdDev {
   // output is the normalised partial result in fp32 (o32 / the fp32 map).
   int step_nb, step, rank_lo, n_chunks, sub_len, z_rank, sched;
   float* o32;
+  // Ring step accumulating into the running result (acc_state != 0): o32
+  // and lse hold the running fp32 (o, lse) of the block's query chunk (slice
+  // q_z), read before the first key tile and overwritten with the merged
+  // result; the online softmax simply continues from that state.
+  int acc_state;
   // o token-major, [B][L][Hq][d] (tm_o is then 4-D: d, Hq, L, B), for the
   // blockwise transformer whose feed-forward takes token rows of Hq * d
   int o_tok;
@@ -164,7 +169,7 @@ __device__ void fwd_producer(FwdSmem<D>& sm, const CUtensorMap* tm_q, const CUte
 }
 
 template <int D>
-__device__ void fwd_mma(FwdSmem<D>& sm, uint32_t tmem, int nkv, volatile int* ab, int* err) {
+__device__ void fwd_mma(FwdSmem<D>& sm, uint32_t tmem, int nkv, bool o_preloaded, volatile int* ab, int* err) {
   using S = FwdSmem<D>;
   constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
   constexpr uint32_t kIdO = idesc_bf16(128, D, false, true);
@@ -220,7 +225,7 @@ __device__ void fwd_mma(FwdSmem<D>& sm, uint32_t tmem, int nkv, volatile int* ab
       ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.p_full[t]), j & 1, ab, err, kSiteFwdMma));
       if (!ok) break;
       tc_fence_after();
-      issue_pv(t, vs, j > 0);
+      issue_pv(t, vs, j > 0 || o_preloaded);
       if (has_next) {
         if (t == 0) {
           ok = wait_full(ks, ku);
@@ -257,6 +262,35 @@ __device__ void fwd_softmax(FwdSmem<D>& sm, uint32_t tmem, int t, const FwdDev& 
   const uint32_t t_o = tmem + 256 + 128 * t + lane_off;
   const float c = p.scale_log2;
   float m = -INFINITY, l = 0.f;
+  if (kStep && p.acc_state) {
+    // Continue from the running result (o_run, lse_run) of this row: the
+    // state m = lse_run log2(e), l = 1, O = o_run has exactly that
+    // normalised output and log-sum-exp; an empty row (lse_run = -inf)
+    // starts from m = -inf, l = 0, O = 0.  O goes to tensor memory before
+    // this thread's first p_full arrival, which orders it before PV_t(0).
+    const size_t rrow = static_cast<size_t>(out_z) * p.L + qpos;
+    const float lrun = qpos < p.L ? p.lse[rrow] : -INFINITY;
+    const bool live = lrun != -INFINITY;
+    if (live) {
+      m = lrun * kLog2e;
+      l = 1.f;
+    }
+    const float4* src = reinterpret_cast<const float4*>(p.o32 + rrow * D);
+#pragma unroll
+    for (int c0 = 0; c0 < D / 32; ++c0) {
+      uint32_t r[32];
+#pragma unroll
+      for (int x = 0; x < 8; ++x) {
+        const float4 v = live ? src[c0 * 8 + x] : make_float4(0.f, 0.f, 0.f, 0.f);
+        r[4 * x] = __float_as_uint(v.x);
+        r[4 * x + 1] = __float_as_uint(v.y);
+        r[4 * x + 2] = __float_as_uint(v.z);
+        r[4 * x + 3] = __float_as_uint(v.w);
+      }
+      tmem_st32_async(t_o + c0 * 32, r);
+    }
+    tmem_wait_st();
+  }
   bool ok = true;
   int j = 0;
   for (int ri = 0; ri < nr && ok; ++ri) {
@@ -334,7 +368,7 @@ __device__ void fwd_softmax(FwdSmem<D>& sm, uint32_t tmem, int t, const FwdDev& 
       // accumulated so far is rescaled to the new reference.  O_t is
       // quiescent here (the commit that signalled S_t(j) covers PV_t(j-1)),
       // and PV_t(j) is only issued after this thread arrives on p_full.
-      if (j > 0 && __any_sync(0xffffffffu, resc)) {
+      if ((j > 0 || (kStep && p.acc_state)) && __any_sync(0xffffffffu, resc)) {
         const float f = resc ? ex2(m_old - m) : 1.f;
 #pragma unroll
         for (int c0 = 0; c0 < D / 32; ++c0) {
@@ -456,7 +490,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     u = item % p.step_nb;
     schedule_pair(p.n_chunks, p.sched, p.step, worker, &q_rank, &kv_rank);
     q_z += q_rank * p.z_rank * BH;
-    out_z += worker * p.z_rank * BH;
+    // a partial result goes to the worker's slot; the running result is the
+    // query chunk's own
+    out_z += (p.acc_state ? q_rank : worker) * p.z_rank * BH;
     kv_z += kv_rank * p.z_rank * (p.B * p.Hkv);
   }
   const int q0 = u * 256;
@@ -496,8 +532,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
   if (kStep && nkv == 0) {
     // A ring-step block that sees none of the source's keys (causal): its
-    // partial result is the merge's neutral element, o = 0, lse = -inf.
-    if (warp >= 4) {
+    // partial result is the merge's neutral element, o = 0, lse = -inf (a
+    // running result stays as it is).
+    if (warp >= 4 && !p.acc_state) {
       const int qpos = q0 + 128 * ((warp - 4) >> 2) + (threadIdx.x & 127);
       if (qpos < p.L) {
         float4* dst = reinterpret_cast<float4*>(p.o32 + (static_cast<size_t>(out_z) * p.L + qpos) * D);
@@ -510,7 +547,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     if (lane == 0) fwd_producer<D>(sm, &tm_q, &tm_k, &tm_v, q0, q_z, kv_z, rg, nr, ab, p.err);
   } else if (warp == 1) {
     // the whole warp runs the issue loop; one elected lane issues
-    fwd_mma<D>(sm, tmem, nkv, ab, p.err);
+    fwd_mma<D>(sm, tmem, nkv, kStep && p.acc_state, ab, p.err);
   } else if (warp >= 4) {
     fwd_softmax<D, kStep>(sm, tmem, (warp - 4) >> 2, p, &tm_o, q0, out_z, q_rank, kv_rank, rg, nr, ab, p.err);
   }
@@ -556,7 +593,7 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
   p.order = a.order; p.offsets = a.offsets; p.ranges = a.ranges;
   p.lse = a.lse; p.err = a.err;
   p.step_nb = a.step_nb; p.step = a.step; p.rank_lo = a.rank_lo; p.n_chunks = a.n_chunks;
-  p.sub_len = a.sub_len; p.z_rank = a.z_rank; p.sched = a.sched; p.o32 = a.o32;
+  p.sub_len = a.sub_len; p.z_rank = a.z_rank; p.sched = a.sched; p.o32 = a.o32; p.acc_state = a.acc_state;
   p.o_tok = a.o_token_major;
   const size_t smem = fwd_smem_bytes(a.d);
   const dim3 grid(static_cast<unsigned>(a.n_blocks) * a.B * a.Hq);

@@ -44,6 +44,9 @@ struct FwdArgs {
   // number of items, tm_o an fp32 map with 32-column boxes, see attn_fwd.cu)
   int step_nb = 0, step = 0, rank_lo = 0, n_chunks = 1, sub_len = 0, z_rank = 0, sched = 0;
   float* o32 = nullptr;
+  // ring step that continues from and overwrites the running result in o32
+  // and lse (the query chunk's slices) instead of writing a partial result
+  int acc_state = 0;
   // not a ring step: o token-major [B][L][Hq][d] through a 4-D tm_o
   // (d, Hq, L, B; box 64 x 1 x 128 x 1)
   int o_token_major = 0;

@@ -216,7 +216,7 @@ int check_ring_shape(int B, int Hq, int Hkv, int L, int d, int n_chunks, int cau
 // z_rank = 0 only the chunks of the one rank and its source.
 int launch_step(int dev, const void* q, const void* k, const void* v, float* o_s, float* lse_s, int B, int Hq,
                 int Hkv, int L, int d, int N, int causal, int schedule, int step, int rank_lo, int rank_hi, int z_rank,
-                cudaStream_t stream) {
+                cudaStream_t stream, int acc_state = 0) {
   const int C = L / N;
   const int zq = (z_rank ? N : 1) * B * Hq, zkv = (z_rank ? N : 1) * B * Hkv;
   FwdArgs a;
@@ -238,13 +238,14 @@ int launch_step(int dev, const void* q, const void* k, const void* v, float* o_s
   a.step_nb = (C + kQBlockRows - 1) / kQBlockRows;
   a.step = step; a.rank_lo = rank_lo; a.n_chunks = N;
   a.sub_len = (causal && schedule == kSchedFold) ? L / (2 * N) : 0;
-  a.z_rank = z_rank; a.sched = schedule; a.o32 = o_s;
+  a.z_rank = z_rank; a.sched = schedule; a.o32 = o_s; a.acc_state = acc_state;
   return launch_fwd(a, stream) == cudaSuccess ? RING_ATTN_OK : RING_ATTN_ERR_CUDA;
 }
 
-// Parts of the ring_attn_ring_fwd workspace (byte offsets, 256-aligned).
+// Parts of the ring_attn_ring_fwd workspace (byte offsets, 256-aligned):
+// q, k, v in chunk order and the running fp32 result.
 struct RingWorkspace {
-  size_t qc = 0, kc = 0, vc = 0, oacc = 0, lacc = 0, os = 0, ls = 0, total = 0;
+  size_t qc = 0, kc = 0, vc = 0, oacc = 0, lacc = 0, total = 0;
 };
 
 RingWorkspace ring_workspace(int B, int Hq, int Hkv, int L, int d) {
@@ -255,9 +256,7 @@ RingWorkspace ring_workspace(int B, int Hq, int Hkv, int L, int d) {
   w.vc = w.kc + up(nkv * d * 2);
   w.oacc = w.vc + up(nkv * d * 2);
   w.lacc = w.oacc + up(nq * d * 4);
-  w.os = w.lacc + up(nq * 4);
-  w.ls = w.os + up(nq * d * 4);
-  w.total = w.ls + up(nq * 4);
+  w.total = w.lacc + up(nq * 4);
   return w;
 }
 
@@ -545,6 +544,25 @@ int ring_attn_fwd_step(const void* q_chunk, const void* k_chunk, const void* v_c
                      rank, rank + 1, 0, stream);
 }
 
+int ring_attn_fwd_step_accumulate(const void* q_chunk, const void* k_chunk, const void* v_chunk, float* o_run,
+                                  float* lse_run, int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal,
+                                  int schedule, int rank, int src, cudaStream_t stream) {
+  int rc = check_ring_shape(B, Hq, Hkv, L, d, n_chunks, causal, schedule);
+  if (rc != RING_ATTN_OK) return rc;
+  if (rank < 0 || rank >= n_chunks || src < 0 || src >= n_chunks) return RING_ATTN_ERR_SHAPE;
+  if (schedule == kSchedDfa) schedule = kSchedContig;  // the same block
+  if (B == 0 || L == 0) return RING_ATTN_OK;
+  if (!q_chunk || !k_chunk || !v_chunk || !o_run || !lse_run) return RING_ATTN_ERR_NULL;
+  if (!aligned16(q_chunk) || !aligned16(k_chunk) || !aligned16(v_chunk) || !aligned16(o_run) || !aligned16(lse_run))
+    return RING_ATTN_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  int dev;
+  if ((rc = current_device(&dev)) != RING_ATTN_OK) return rc;
+  const int step = ((rank - src) % n_chunks + n_chunks) % n_chunks;
+  return launch_step(dev, q_chunk, k_chunk, v_chunk, o_run, lse_run, B, Hq, Hkv, L, d, n_chunks, causal, schedule,
+                     step, rank, rank + 1, 0, stream, 1);
+}
+
 int ring_attn_merge(float* o, float* lse, const float* o_s, const float* lse_s, long long n_rows, int d,
                     void* o_out, cudaStream_t stream) {
   if (n_rows < 0) return RING_ATTN_ERR_SHAPE;
@@ -586,8 +604,6 @@ int ring_attn_ring_fwd(const void* q, const void* k, const void* v, void* o, flo
   void* vc = ws + w.vc;
   float* oacc = reinterpret_cast<float*>(ws + w.oacc);
   float* lacc = reinterpret_cast<float*>(ws + w.lacc);
-  float* os = reinterpret_cast<float*>(ws + w.os);
-  float* ls = reinterpret_cast<float*>(ws + w.ls);
   const int N = n_chunks;
   LaunchTimer* t = active_timer();
   if (t) t->mark(RING_ATTN_KERNEL_RING_IO, false, stream);
@@ -598,30 +614,22 @@ int ring_attn_ring_fwd(const void* q, const void* k, const void* v, void* o, flo
       launch_ring_gather(v, vc, B * Hkv, L, d, N, sc, st, stream) != cudaSuccess)
     return RING_ATTN_ERR_CUDA;
   if (t) t->mark(RING_ATTN_KERNEL_RING_IO, true, stream);
-  const long long rows = static_cast<long long>(B) * Hq * L;
-  const long long chunk_rows = rows / N;  // rows of one chunk, chunk-major
-  auto merge = [&](long long first_acc, long long first_part, long long n) {
-    if (t) t->mark(RING_ATTN_KERNEL_RING_MERGE, false, stream);
-    const cudaError_t e = launch_ring_merge(oacc + first_acc * d, lacc + first_acc, os + first_part * d,
-                                            ls + first_part, nullptr, n, d, stream);
-    if (t) t->mark(RING_ATTN_KERNEL_RING_MERGE, true, stream);
-    return e;
-  };
+  // Launch 0 (every worker's own chunk against itself) writes the running
+  // result; every later launch continues each block's query chunk from it
+  // and overwrites it with the merged result (the step kernel's accumulate
+  // mode), so no partial result or separate merge is needed.  A query chunk
+  // must appear once per launch: DistFlashAttention's launches run as two,
+  // the workers' own chunks (workers t..N-1), then the chunks the idle
+  // workers 0..t-1 take over (chunks N-t..N-1, unless t = N - t).
   for (int s = 0; s < schedule_launches(N, schedule); ++s) {
-    // launch 0 (every worker's own chunk against itself) starts the running
-    // result; each later launch leaves worker w's partial in slot w
-    if ((rc = launch_step(dev, qc, kc, vc, s == 0 ? oacc : os, s == 0 ? lacc : ls, B, Hq, Hkv, L, d, N, causal,
-                          schedule, s, 0, N, 1, stream)) != RING_ATTN_OK)
+    const int lo = (schedule == kSchedDfa) ? s : 0;
+    if ((rc = launch_step(dev, qc, kc, vc, oacc, lacc, B, Hq, Hkv, L, d, N, causal, schedule, s, lo, N, 1, stream,
+                          s > 0 ? 1 : 0)) != RING_ATTN_OK)
       return rc;
-    if (s == 0) continue;
-    if (schedule != kSchedDfa) {  // ring step: worker w's partial belongs to chunk w
-      if (merge(0, 0, rows) != cudaSuccess) return RING_ATTN_ERR_CUDA;
-      continue;
-    }
-    // DistFlashAttention: workers s..N-1 ran blocks of their own chunks;
-    // workers 0..s-1 (busy unless s = N - s) those of chunks N-s..N-1
-    if (merge(s * chunk_rows, s * chunk_rows, (N - s) * chunk_rows) != cudaSuccess) return RING_ATTN_ERR_CUDA;
-    if (s < N - s && merge((N - s) * chunk_rows, 0, s * chunk_rows) != cudaSuccess) return RING_ATTN_ERR_CUDA;
+    if (schedule == kSchedDfa && s > 0 && s < N - s &&
+        (rc = launch_step(dev, qc, kc, vc, oacc, lacc, B, Hq, Hkv, L, d, N, causal, schedule, s, 0, s, 1, stream, 1)) !=
+            RING_ATTN_OK)
+      return rc;
   }
   if (t) t->mark(RING_ATTN_KERNEL_RING_IO, false, stream);
   if (launch_ring_scatter(oacc, lacc, o, lse, B * Hq, L, d, N, sc, st, stream) != cudaSuccess)

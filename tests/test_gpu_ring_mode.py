@@ -8,7 +8,9 @@ oracle's merge; the whole ring run step by step on one GPU
 (ring_attn_ring_fwd) with the oracle's plain forward and with the fused
 forward.  Tolerances as for the fused path (tolerance.py): o within 2e-2
 max-abs beyond bf16 output rounding and 2e-3 mean-abs, lse within 1e-3;
-the merge alone, fp32 in and out, within 1e-5.
+the merge alone, fp32 in and out, within 1e-5.  The accumulating step
+(ring_attn_fwd_step_accumulate) against the oracle and against a step
+followed by a merge.
 """
 import numpy as np
 import pytest
@@ -88,6 +90,66 @@ def test_every_step_of_a_small_ring_matches_the_oracle(case):
             if (~empty).any():
                 check_bf16(f"o_s r{r} s{src}", got_o[~empty], o_ref[~empty])
                 check_fp32(f"lse_s r{r} s{src}", got_l[~empty], lse_ref[~empty], TOL_LSE)
+
+
+@pytest.mark.parametrize("case", STEP_CASES, ids=case_id)
+def test_step_accumulate_matches_the_oracle_and_step_then_merge(case):
+    """Every rank runs its blocks in ring order accumulating into a running
+    result that starts empty (lse = -inf); the result equals the plain
+    definition on the rank's rows, and the partial-result path (step, then
+    merge).  The two GPU paths round P to bf16 relative to different maxima
+    (the running one, the block's own), so they agree within the parity
+    bound, not to fp32 rounding."""
+    B, Hq, Hkv, L, d, N, causal, schedule = case
+    q, k, v, _ = inputs.make_inputs(B, Hq, Hkv, L, d, seed=3 + sum(case[:6]))
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o_ref, lse_ref = oracle.fwd(q.double(), k.double(), v.double(), causal)
+    C = L // N
+    for r in range(N):
+        rows = chunk_positions(L, N, causal, r, schedule)
+        q_chunk = qd[:, :, rows.cuda()].contiguous()
+        o_run = torch.zeros((B, Hq, C, d), dtype=torch.float32, device="cuda")
+        lse_run = torch.full((B, Hq, C), float("-inf"), dtype=torch.float32, device="cuda")
+        o_m, lse_m = o_run.clone(), lse_run.clone()
+        for src in oracle.ring_sources(r, N):
+            srows = chunk_positions(L, N, causal, src, schedule).cuda()
+            k_chunk, v_chunk = kd[:, :, srows].contiguous(), vd[:, :, srows].contiguous()
+            ra.ring_attn_fwd_step_accumulate(q_chunk, k_chunk, v_chunk, o_run, lse_run, N, causal, r, src,
+                                             schedule=schedule)
+            o_s, lse_s = ra.ring_attn_fwd_step(q_chunk, k_chunk, v_chunk, N, causal, r, src, schedule=schedule)
+            ra.ring_attn_merge(o_m, lse_m, o_s, lse_s)
+        torch.cuda.synchronize()
+        assert_status_ok()
+        idx = rows.numpy()
+        check_bf16(f"o_run r{r}", f64(o_run), o_ref[:, :, idx])
+        check_fp32(f"lse_run r{r}", f64(lse_run), lse_ref[:, :, idx], TOL_LSE)
+        check_bf16(f"o_run vs step+merge r{r}", f64(o_run), f64(o_m), ulps=0)
+        check_fp32(f"lse_run vs step+merge r{r}", f64(lse_run), f64(lse_m), 1e-4)
+
+
+def test_step_accumulate_keeps_rows_that_see_nothing():
+    """Causal, the fold: rank 0's first sub-chunk sees none of rank 1's keys,
+    so accumulating that block leaves those rows' running result as it was
+    (o bit for bit; lse up to the rounding of its trip through log2 units),
+    while the second sub-chunk's rows change."""
+    B, Hq, Hkv, L, d, N = 1, 2, 1, 1024, 128, 4
+    q, k, v, _ = inputs.make_inputs(B, Hq, Hkv, L, d, seed=71)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    rows0 = chunk_positions(L, N, True, 0).cuda()
+    rows1 = chunk_positions(L, N, True, 1).cuda()
+    q_chunk = qd[:, :, rows0].contiguous()
+    C, c = L // N, L // (2 * N)
+    gen = torch.Generator(device="cpu").manual_seed(5)
+    o_run = torch.randn((B, Hq, C, d), generator=gen).cuda()
+    lse_run = torch.randn((B, Hq, C), generator=gen).cuda()
+    o0, l0 = o_run.clone(), lse_run.clone()
+    ra.ring_attn_fwd_step_accumulate(q_chunk, kd[:, :, rows1].contiguous(), vd[:, :, rows1].contiguous(), o_run,
+                                     lse_run, N, True, 0, 1)
+    torch.cuda.synchronize()
+    assert_status_ok()
+    assert torch.equal(o_run[:, :, :c], o0[:, :, :c])
+    assert (lse_run[:, :, :c] - l0[:, :, :c]).abs().max().item() <= 2e-6 * max(1.0, l0.abs().max().item())
+    assert not torch.equal(lse_run[:, :, c:], l0[:, :, c:])
 
 
 @pytest.mark.parametrize("d", [64, 128])
