@@ -296,6 +296,48 @@ int ring_attn_ring_bwd(const void* q, const void* k, const void* v, const void* 
                        void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal,
                        int schedule, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* ---------------------------------------------------------------------
+ * One rank's share of the ring-mode backward, for a ring whose ranks run
+ * on different GPUs ("Large-scale distributed AI model training series:
+ * sequence parallelism", section 6.2 Ring Attention: the blocks are
+ * recomputed in the backward pass; the key/value gradients travel round the
+ * ring with their key/value block and end at its owner).  Tensors are the
+ * rank's chunks in chunk order, as for ring_attn_fwd_step; C = L/n_chunks.
+ *   begin  the rank's statistics from its forward outputs (o_chunk, lse_chunk)
+ *          and dO_chunk; zeroes its fp32 dQ accumulator (both in `workspace`,
+ *          ring_attn_bwd_rank_workspace_size() bytes, 256-byte aligned)
+ *   step   the block (rank's queries, src's keys): adds its dQ contribution
+ *          to the workspace's accumulator and its dK, dV contributions to
+ *          dk_acc, dv_acc -- fp32 [B][Hkv][C][d], plain row-major, the
+ *          accumulators travelling with src's key/value chunk (zeroed by
+ *          src before the ring starts; src's own block is the first step)
+ *   end    dq_chunk = bf16(dQ / sqrt(d)) [B][Hq][C][d]
+ * Once dk_acc, dv_acc are back at their owner, ring_attn_grad_to_bf16 gives
+ * dk = bf16(dk_acc / sqrt(d)) and dv = bf16(dv_acc).  The schedule's chunk
+ * map decides the causal mask (RING_ATTN_SCHEDULE_DISTFLASH blocks are the
+ * contiguous ring's).  Steps of one rank must not overlap on the GPU with
+ * each other (they add into the same dQ accumulator) unless ordered by the
+ * caller; the workspace must not be shared between ranks.
+ * ------------------------------------------------------------------- */
+size_t ring_attn_bwd_rank_workspace_size(int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal,
+                                         int schedule);
+
+int ring_attn_bwd_rank_begin(const void* o_chunk, const void* dO_chunk, const float* lse_chunk, int B, int Hq,
+                             int Hkv, int L, int d, int n_chunks, int causal, int schedule, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream);
+
+int ring_attn_bwd_rank_step(const void* q_chunk, const void* k_chunk, const void* v_chunk, const void* dO_chunk,
+                            float* dk_acc, float* dv_acc, int B, int Hq, int Hkv, int L, int d, int n_chunks,
+                            int causal, int schedule, int rank, int src, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream);
+
+int ring_attn_bwd_rank_end(void* dq_chunk, int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal,
+                           int schedule, const void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* out = bf16(scale * acc) elementwise for n_elems fp32 values (a multiple
+ * of 128); out [n_elems] bf16. */
+int ring_attn_grad_to_bf16(const float* acc, void* out, long long n_elems, float scale, cudaStream_t stream);
+
 /* Static description of a status code. */
 const char* ring_attn_strerror(int status);
 

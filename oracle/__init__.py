@@ -13,6 +13,7 @@ from .oracle import (  # noqa: F401
     bwd_rows,
     ring_fwd,
     ring_step,
+    ring_step_bwd,
     merge,
     ffn,
     ffn_bwd,

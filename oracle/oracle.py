@@ -58,6 +58,8 @@ def _bind(lib):
                                     _dp, _dp, _dp, I]
     lib.oracle_ring_fwd.argtypes = [_dp, _dp, _dp, I, I, I, I, I, I, I, I, _dp, _dp, I]
     lib.oracle_ring_step.argtypes = [_dp, _dp, _dp, I, I, I, I, I, I, I, I, I, I, _dp, _dp, I]
+    lib.oracle_ring_step_bwd.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp] + [I] * 10 + [_dp, _dp, _dp, I]
+    lib.oracle_ring_step_bwd.restype = ctypes.c_int
     lib.oracle_merge.argtypes = [_dp, _dp, _dp, _dp, ctypes.c_long, I]
     lib.oracle_merge.restype = None
     lib.oracle_owner_rank.argtypes = [I, I, I, I, I]
@@ -237,6 +239,24 @@ def ring_step(q, k, v, causal: bool, n_chunks: int, rank: int, src: int, threads
                                     int(rank), int(src), _schedule(striped, schedule), _p(o), _p(lse),
                                     _threads(threads)))
     return o, lse
+
+
+def ring_step_bwd(q, k, v, dO, lse, D, causal: bool, n_chunks: int, rank: int, src: int, threads: int = 0,
+                  striped: bool = False, schedule=None):
+    """One ring block of the backward (SP series section 6.2): the
+    contribution of rank's query rows against src's keys, with the full
+    statistics lse, D [B,Hq,L] of the plain definition (oracle.bwd returns
+    them): dq on rank's rows, dk and dv on src's rows (global row order,
+    zero elsewhere).  Summed over every block: the plain backward."""
+    q, k, v, dO, lse, D = (_f64(a) for a in (q, k, v, dO, lse, D))
+    B, Hq, Hkv, L, d = _shape(q, k)
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    _check(_load().oracle_ring_step_bwd(_p(q), _p(k), _p(v), _p(dO), _p(lse), _p(D), B, Hq, Hkv, L, d, int(causal),
+                                        int(n_chunks), int(rank), int(src), _schedule(striped, schedule), _p(dq),
+                                        _p(dk), _p(dv), _threads(threads)))
+    return dq, dk, dv
 
 
 def merge(o_a, lse_a, o_b, lse_b):

@@ -550,6 +550,82 @@ int oracle_ring_step(const double *q, const double *k, const double *v, int B, i
   return run_parallel(&t, n_threads);
 }
 
+/* One ring block of the backward (Ring Attention, section 6.2: each block
+ * is recomputed in the backward pass; the key/value gradients travel with
+ * their block).  For the rows i of rank `rank` and the keys j of rank `src`
+ * that i may see, with the full statistics lse_i and D_i of the plain
+ * definition:
+ *   P_ij = exp(s_ij - lse_i),  dS_ij = P_ij (dO_i . v_j - D_i)
+ *   dq_i += scale sum_j dS_ij k_j                (rows of rank)
+ *   dk_j += scale sum_{h in group} sum_i dS_ij q_i,
+ *   dv_j +=       sum_{h in group} sum_i P_ij dO_i  (rows of src)
+ * Outputs are in global row order (full [B][H][L][d] arrays), zero outside
+ * those rows.  Summed over every (rank, src) block they give the plain
+ * backward. */
+static int block_visible(const problem_t *P, const task_t *t, int i, int j) {
+  return owner_rank(P->L, t->n_chunks, P->causal, t->schedule, i) == t->rank &&
+         owner_rank(P->L, t->n_chunks, P->causal, t->schedule, j) == t->src && (!P->causal || j <= i);
+}
+static void block_dq_item(task_t *t, long item, double *s) {
+  (void)s;
+  const problem_t *P = t->P;
+  const int i = (int)(item % P->L);
+  const long bh = item / P->L;
+  const int h = (int)(bh % P->Hq), b = (int)(bh / P->Hq);
+  const int g = h / (P->Hq / P->Hkv);
+  double *dq = t->dq + ((size_t)bh * P->L + i) * P->d;
+  for (int c = 0; c < P->d; ++c) dq[c] = 0.0;
+  if (owner_rank(P->L, t->n_chunks, P->causal, t->schedule, i) != t->rank) return;
+  const double *qi = q_row(P, b, h, i), *doi = do_row(P, b, h, i);
+  const double lse = t->lse[(size_t)bh * P->L + i], D = t->D[(size_t)bh * P->L + i];
+  for (int j = 0; j < P->L; ++j) {
+    if (!block_visible(P, t, i, j)) continue;
+    const double pij = exp(P->scale * dot(qi, k_row(P, b, g, j), P->d) - lse);
+    const double dsij = pij * (dot(doi, v_row(P, b, g, j), P->d) - D);
+    const double *kj = k_row(P, b, g, j);
+    for (int c = 0; c < P->d; ++c) dq[c] += P->scale * dsij * kj[c];
+  }
+}
+static void block_dkdv_item(task_t *t, long item, double *s) {
+  (void)s;
+  const problem_t *P = t->P;
+  const int j = (int)(item % P->L);
+  const long bg = item / P->L;
+  const int g = (int)(bg % P->Hkv), b = (int)(bg / P->Hkv);
+  const int G = P->Hq / P->Hkv;
+  double *dk = t->dk + ((size_t)bg * P->L + j) * P->d, *dv = t->dv + ((size_t)bg * P->L + j) * P->d;
+  for (int c = 0; c < P->d; ++c) { dk[c] = 0.0; dv[c] = 0.0; }
+  if (owner_rank(P->L, t->n_chunks, P->causal, t->schedule, j) != t->src) return;
+  const double *kj = k_row(P, b, g, j), *vj = v_row(P, b, g, j);
+  for (int h = g * G; h < (g + 1) * G; ++h) {
+    const size_t base = ((size_t)b * P->Hq + h) * P->L;
+    for (int i = 0; i < P->L; ++i) {
+      if (!block_visible(P, t, i, j)) continue;
+      const double *qi = q_row(P, b, h, i), *doi = do_row(P, b, h, i);
+      const double pij = exp(P->scale * dot(qi, kj, P->d) - t->lse[base + i]);
+      const double dsij = pij * (dot(doi, vj, P->d) - t->D[base + i]);
+      for (int c = 0; c < P->d; ++c) {
+        dv[c] += pij * doi[c];
+        dk[c] += P->scale * dsij * qi[c];
+      }
+    }
+  }
+}
+
+int oracle_ring_step_bwd(const double *q, const double *k, const double *v, const double *dO, const double *lse,
+                         const double *D, int B, int Hq, int Hkv, int L, int d, int causal, int n_chunks, int rank,
+                         int src, int schedule, double *dq, double *dk, double *dv, int n_threads) {
+  if (bad_shape(B, Hq, Hkv, L, d) || bad_chunking(L, n_chunks, causal, schedule)) return -1;
+  if (rank < 0 || rank >= n_chunks || src < 0 || src >= n_chunks) return -1;
+  problem_t P = make_problem(q, k, v, dO, B, Hq, Hkv, L, d, causal);
+  task_t t; memset(&t, 0, sizeof t);
+  t.P = &P; t.n_chunks = n_chunks; t.rank = rank; t.src = src; t.schedule = schedule;
+  t.lse = (double *)lse; t.D = (double *)D; t.dq = dq; t.dk = dk; t.dv = dv;
+  t.n_items = (long)B * Hq * L; t.fn = block_dq_item; run_parallel(&t, n_threads);
+  t.n_items = (long)B * Hkv * L; t.fn = block_dkdv_item;
+  return run_parallel(&t, n_threads);
+}
+
 /* The merge of two partial results of the same query rows (the log-sum-exp
  * rule above), written out on its own: for each of n_rows rows of width d,
  *   lse = log(exp(lse_a) + exp(lse_b)),

@@ -44,6 +44,8 @@ from .capi import (  # noqa: F401
     bpt_bwd_workspace_size,
     ring_attn_fwd_step,
     ring_attn_fwd_step_accumulate,
+    RankBackward,
+    grad_to_bf16,
     ring_attn_merge,
     ring_attn_ring_fwd,
     ring_fwd_workspace_size,

@@ -81,6 +81,16 @@ def load():
     lib.ring_attn_fwd_step.restype = I
     lib.ring_attn_fwd_step_accumulate.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, P]
     lib.ring_attn_fwd_step_accumulate.restype = I
+    lib.ring_attn_bwd_rank_workspace_size.argtypes = [I] * 8
+    lib.ring_attn_bwd_rank_workspace_size.restype = S
+    lib.ring_attn_bwd_rank_begin.argtypes = [P, P, P] + [I] * 8 + [P, S, P]
+    lib.ring_attn_bwd_rank_begin.restype = I
+    lib.ring_attn_bwd_rank_step.argtypes = [P] * 6 + [I] * 10 + [P, S, P]
+    lib.ring_attn_bwd_rank_step.restype = I
+    lib.ring_attn_bwd_rank_end.argtypes = [P] + [I] * 8 + [P, S, P]
+    lib.ring_attn_bwd_rank_end.restype = I
+    lib.ring_attn_grad_to_bf16.argtypes = [P, P, ctypes.c_longlong, ctypes.c_float, P]
+    lib.ring_attn_grad_to_bf16.restype = I
     lib.ring_attn_merge.argtypes = [P, P, P, P, ctypes.c_longlong, I, P, P]
     lib.ring_attn_merge.restype = I
     lib.ring_attn_ring_fwd_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
@@ -301,6 +311,71 @@ def ring_attn_fwd_step_accumulate(q_chunk, k_chunk, v_chunk, o_run, lse_run, n_c
     if rc != OK:
         raise RingAttnError(rc, "ring_attn_fwd_step_accumulate")
     return o_run, lse_run
+
+
+class RankBackward:
+    """One rank's share of the ring-mode backward (ring_attn_bwd_rank_* of
+    include/ring_attn.h) on its chunks [B, H, C, d] in chunk order: begin()
+    forms the statistics, step() adds one block (the rank's queries against
+    src's keys) into the rank's dQ and into the travelling fp32 dK/dV of
+    src's chunk, end() returns dq."""
+
+    def __init__(self, o_chunk, dO_chunk, lse_chunk, Hkv: int, n_chunks: int, causal: bool, striped: bool = False,
+                 schedule=None, stream=None):
+        import torch
+        B, Hq, C, d = o_chunk.shape
+        _check_tensor(o_chunk, "o_chunk", torch.bfloat16, (B, Hq, C, d))
+        _check_tensor(dO_chunk, "dO_chunk", torch.bfloat16, (B, Hq, C, d))
+        _check_tensor(lse_chunk, "lse_chunk", torch.float32, (B, Hq, C))
+        self.shape = (B, Hq, int(Hkv), C * int(n_chunks), d, int(n_chunks), int(bool(causal)),
+                      schedule_code(striped, schedule))
+        nbytes = int(load().ring_attn_bwd_rank_workspace_size(*self.shape))
+        if nbytes == 0:
+            raise RingAttnError(ERR_SHAPE, "ring_attn_bwd_rank_workspace_size")
+        self.ws = torch.empty(nbytes, dtype=torch.uint8, device=o_chunk.device)
+        self.dO = dO_chunk
+        self.stream = stream
+        rc = load().ring_attn_bwd_rank_begin(_ptr(o_chunk), _ptr(dO_chunk), _ptr(lse_chunk), *self.shape,
+                                             _ptr(self.ws), nbytes, _stream(stream))
+        if rc != OK:
+            raise RingAttnError(rc, "ring_attn_bwd_rank_begin")
+
+    def step(self, q_chunk, k_chunk, v_chunk, dk_acc, dv_acc, rank: int, src: int):
+        import torch
+        B, Hq, Hkv, L, d = self.shape[:5]
+        C = L // self.shape[5]
+        _check_tensor(q_chunk, "q_chunk", torch.bfloat16, (B, Hq, C, d))
+        for t, n in ((k_chunk, "k_chunk"), (v_chunk, "v_chunk")):
+            _check_tensor(t, n, torch.bfloat16, (B, Hkv, C, d))
+        for t, n in ((dk_acc, "dk_acc"), (dv_acc, "dv_acc")):
+            _check_tensor(t, n, torch.float32, (B, Hkv, C, d))
+        rc = load().ring_attn_bwd_rank_step(_ptr(q_chunk), _ptr(k_chunk), _ptr(v_chunk), _ptr(self.dO), _ptr(dk_acc),
+                                            _ptr(dv_acc), *self.shape, int(rank), int(src), _ptr(self.ws),
+                                            self.ws.numel(), _stream(self.stream))
+        if rc != OK:
+            raise RingAttnError(rc, "ring_attn_bwd_rank_step")
+
+    def end(self, dq_chunk=None):
+        import torch
+        if dq_chunk is None:
+            dq_chunk = torch.empty_like(self.dO)
+        rc = load().ring_attn_bwd_rank_end(_ptr(dq_chunk), *self.shape, _ptr(self.ws), self.ws.numel(),
+                                           _stream(self.stream))
+        if rc != OK:
+            raise RingAttnError(rc, "ring_attn_bwd_rank_end")
+        return dq_chunk
+
+
+def grad_to_bf16(acc, scale: float, out=None, stream=None):
+    """bf16(scale * acc) for an fp32 accumulator (e.g. a travelling dK, dV)."""
+    import torch
+    if not isinstance(acc, torch.Tensor) or acc.dtype != torch.float32 or not acc.is_cuda or not acc.is_contiguous():
+        raise TypeError("acc must be a contiguous fp32 CUDA tensor")
+    out = torch.empty(acc.shape, dtype=torch.bfloat16, device=acc.device) if out is None else out
+    rc = load().ring_attn_grad_to_bf16(_ptr(acc), _ptr(out), acc.numel(), float(scale), _stream(stream))
+    if rc != OK:
+        raise RingAttnError(rc, "ring_attn_grad_to_bf16")
+    return out
 
 
 def ring_attn_merge(o, lse, o_s, lse_s, o_out=None, stream=None):

@@ -141,6 +141,10 @@ struct BwdDev {
   // a * B*Hq + (b, h), k, v, dK, dV at b * B*Hkv + (b, kv head); causal keys
   // from the schedule's chunk map.
   int step_nt, step, n_chunks, sched;
+  // step mode: the first worker of the launch (item k's worker is rank_lo +
+  // k / step_nt), and whether the buffers hold every chunk (z_rank = 1,
+  // chunk-major) or only the block's own query and key/value chunks (0)
+  int rank_lo, z_rank;
 };
 
 // Causal-mask keys of the backward (as in the forward's step mode): a key
@@ -565,9 +569,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   int q_z = qh, kv_z = b * p.Hkv + h / (p.Hq / p.Hkv);
   if constexpr (kStep) {
     kv_tile = item % p.step_nt;
-    schedule_pair(p.n_chunks, p.sched, p.step, item / p.step_nt, &q_rank, &kv_rank);
-    q_z += q_rank * p.B * p.Hq;
-    kv_z += kv_rank * p.B * p.Hkv;
+    schedule_pair(p.n_chunks, p.sched, p.step, p.rank_lo + item / p.step_nt, &q_rank, &kv_rank);
+    q_z += q_rank * p.z_rank * p.B * p.Hq;
+    kv_z += kv_rank * p.z_rank * p.B * p.Hkv;
   }
   const int32_t* rg = p.ranges + 2 * p.offsets[item];
   const int nr = p.offsets[item + 1] - p.offsets[item];
@@ -770,6 +774,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
   p.dv = static_cast<__nv_bfloat16*>(a.dv);
   p.err = a.err;
   p.step_nt = a.step_nt; p.step = a.step; p.n_chunks = a.n_chunks; p.sched = a.sched;
+  p.rank_lo = a.rank_lo; p.z_rank = a.z_rank;
   const size_t smem = sizeof(BwdSmem<D>);
   auto kernel = a.step_nt ? ring_attn_bwd_kernel<D, true> : ring_attn_bwd_kernel<D, false>;
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -807,6 +812,30 @@ size_t bwd_smem_bytes(int d) {
 
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream) {
   return a.d == 128 ? launch_bwd_d<128>(a, stream) : launch_bwd_d<64>(a, stream);
+}
+
+cudaError_t launch_bwd_dq_post(const BwdArgs& a, long long q_slices, cudaStream_t stream) {
+  const float scale = 1.0f / sqrtf(static_cast<float>(a.d));
+  const long long n8 = q_slices * a.Lpad * a.d / 8;
+  const unsigned blocks = static_cast<unsigned>((n8 + 255) / 256);
+  if (a.d == 128)
+    ring_attn_bwd_dq_post_kernel<128><<<blocks, 256, 0, stream>>>(a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), scale,
+                                                                   a.L, a.Lpad, n8);
+  else
+    ring_attn_bwd_dq_post_kernel<64><<<blocks, 256, 0, stream>>>(a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), scale,
+                                                                  a.L, a.Lpad, n8);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_grad_to_bf16(const float* acc, void* out, float scale, long long n_elems, cudaStream_t stream) {
+  // [n_elems / 128][128] rows of a plain fp32 accumulator (d = 128 columns a
+  // row is only a view: the conversion is elementwise, 8 per thread)
+  const long long n8 = n_elems / 8;
+  const unsigned blocks = static_cast<unsigned>((n8 + 255) / 256);
+  const int rows = static_cast<int>(n_elems / 128);
+  ring_attn_bwd_post_kernel<128><<<blocks, 256, 0, stream>>>(acc, static_cast<__nv_bfloat16*>(out), scale, rows, rows,
+                                                             n8);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_pre(const BwdArgs& a, long long q_slices, long long kv_slices, cudaStream_t stream) {

@@ -104,6 +104,9 @@ struct BwdArgs {
   // attn_bwd.cu): only the main kernel runs, with dK/dV always reduced into
   // the fp32 accumulators; the driver runs launch_bwd_pre and the conversions
   int step_nt = 0, step = 0, n_chunks = 1, sched = 0;
+  // step mode: first worker of the launch, and 1 for chunk-major buffers of
+  // every chunk or 0 for buffers holding only the block's two chunks
+  int rank_lo = 0, z_rank = 1;
 };
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
@@ -112,6 +115,11 @@ cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
 // The backward's statistics pre-pass alone over q_slices (and kv_slices for
 // zeroing the dK/dV accumulators) slices of Lpad rows.
 cudaError_t launch_bwd_pre(const BwdArgs& a, long long q_slices, long long kv_slices, cudaStream_t stream);
+// dq = bf16(scale * dQ_acc) for q_slices slices of a.L rows (a.Lpad rows
+// in the tiled accumulator), scale = 1/sqrt(d).
+cudaError_t launch_bwd_dq_post(const BwdArgs& a, long long q_slices, cudaStream_t stream);
+// out = bf16(scale * acc) for n_elems fp32 values (a multiple of 128).
+cudaError_t launch_grad_to_bf16(const float* acc, void* out, float scale, long long n_elems, cudaStream_t stream);
 
 // Ring mode (ring_step.cu): the log-sum-exp merge of n_rows rows (in place
 // into o, lse; optional bf16 copy into o_out), and the gather of a [Z][L][d]

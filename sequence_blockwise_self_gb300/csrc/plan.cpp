@@ -121,14 +121,14 @@ Plan build_step_plan(int L, int N, bool causal, int sched, int step, int rank_lo
   return p;
 }
 
-Plan build_bwd_step_plan(int L, int N, bool causal, int sched, int step) {
+Plan build_bwd_step_plan(int L, int N, bool causal, int sched, int step, int rank_lo, int rank_hi) {
   Plan p;
   const int C = L / N;
   const int nt = C / kTileRows;
-  p.n_blocks = N * nt;
+  p.n_blocks = (rank_hi - rank_lo) * nt;
   p.offsets.push_back(0);
   std::vector<int> tiles;
-  for (int w = 0; w < N; ++w) {
+  for (int w = rank_lo; w < rank_hi; ++w) {
     int r, src;
     const bool busy = schedule_pair(N, sched, step, w, &r, &src);
     for (int kt = 0; kt < nt; ++kt) {

@@ -133,10 +133,11 @@ RA_HOST_DEVICE inline int chunk_pos(int L, int N, bool causal, int sched, int ra
 // keys, or an idle worker).
 Plan build_step_plan(int L, int N, bool causal, int sched, int step, int rank_lo, int rank_hi);
 
-// Backward of launch t for every worker: item k is tile k % nt (nt = C /
-// 128) of worker w = k / nt's key/value chunk (schedule_pair); it lists the
-// tiles of w's query chunk (chunk-local, ascending) holding a query that may
-// see a key of that tile.  An item may list none.
-Plan build_bwd_step_plan(int L, int N, bool causal, int sched, int step);
+// Backward of launch t for workers [rank_lo, rank_hi): item k is tile k %
+// nt (nt = C / 128) of worker w = rank_lo + k / nt's key/value chunk
+// (schedule_pair); it lists the tiles of w's query chunk (chunk-local,
+// ascending) holding a query that may see a key of that tile.  An item may
+// list none.
+Plan build_bwd_step_plan(int L, int N, bool causal, int sched, int step, int rank_lo, int rank_hi);
 
 }  // namespace ra

@@ -29,8 +29,8 @@ namespace {
 __device__ int g_device_status;
 
 std::map<std::tuple<int, int, int, int, int>, DevicePlan> g_plans;  // (device, kind, L, N, causal)
-// ring step plans: (device, L, N, causal, schedule, launch, first worker, end worker;
-// end rank -1 = the backward plan of the step)
+// ring step plans: (device, L, N, causal, schedule, launch, first worker, end
+// worker; a negative end e: the backward plan of workers [first, -e - 1))
 std::map<std::tuple<int, int, int, int, int, int, int, int>, DevicePlan> g_step_plans;
 // forward work items grouped by row block: (device, L, N, causal, block rows)
 std::map<std::tuple<int, int, int, int, int>, int32_t*> g_block_orders;
@@ -162,7 +162,8 @@ int get_step_plan(int dev, int L, int N, int causal, int schedule, int step, int
     return RING_ATTN_OK;
   }
   DevicePlan dp;
-  int rc = upload_plan(rank_hi < 0 ? build_bwd_step_plan(L, N, causal != 0, schedule, step)
+  // rank_hi < 0: the backward plan of workers [rank_lo, -rank_hi - 1)
+  int rc = upload_plan(rank_hi < 0 ? build_bwd_step_plan(L, N, causal != 0, schedule, step, rank_lo, -rank_hi - 1)
                                    : build_step_plan(L, N, causal != 0, schedule, step, rank_lo, rank_hi),
                        &dp);
   if (rc != RING_ATTN_OK) return rc;
@@ -698,9 +699,10 @@ int ring_attn_ring_bwd(const void* q, const void* k, const void* v, const void* 
   // statistics of every rank's rows, accumulators zeroed
   if (launch_bwd_pre(a, zq, zkv, stream) != cudaSuccess) return RING_ATTN_ERR_CUDA;
   a.step_nt = C / kTileRows; a.n_chunks = N; a.sched = schedule;
+  a.rank_lo = 0; a.z_rank = 1;  // every worker's chunk, chunk-major
   for (int s = 0; s < schedule_launches(N, schedule); ++s) {
     DevicePlan plan;
-    if ((rc = get_step_plan(dev, L, N, causal, schedule, s, 0, -1, &plan)) != RING_ATTN_OK) return rc;
+    if ((rc = get_step_plan(dev, L, N, causal, schedule, s, 0, -N - 1, &plan)) != RING_ATTN_OK) return rc;
     a.n_blocks = plan.n_blocks;
     a.order = plan.order(); a.offsets = plan.offsets(); a.ranges = plan.ranges();
     a.step = s;
@@ -714,6 +716,132 @@ int ring_attn_ring_bwd(const void* q, const void* k, const void* v, const void* 
     return RING_ATTN_ERR_CUDA;
   if (t) t->mark(RING_ATTN_KERNEL_RING_IO, true, stream);
   return RING_ATTN_OK;
+}
+
+// ----------------------------------------------------- one rank's backward
+// Workspace of ring_attn_bwd_rank_*: the rank's statistics (-lse log2 e and
+// -D, [B*Hq][C] each) and its fp32 dQ accumulator (tiled as in the fused
+// backward), 256-byte aligned parts.
+struct RankBwdWorkspace {
+  size_t lse2 = 0, dvec = 0, dq = 0, total = 0;
+};
+
+RankBwdWorkspace rank_bwd_workspace(int B, int Hq, int C, int d) {
+  auto up = [](size_t x) { return round_up(x, 256); };
+  const size_t rows = static_cast<size_t>(B) * Hq * C;
+  RankBwdWorkspace w;
+  w.dvec = up(rows * 4);
+  w.dq = w.dvec + up(rows * 4);
+  w.total = w.dq + up(rows * d * 4);
+  return w;
+}
+
+size_t ring_attn_bwd_rank_workspace_size(int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal,
+                                         int schedule) {
+  if (check_ring_shape(B, Hq, Hkv, L, d, n_chunks, causal, schedule) != RING_ATTN_OK) return 0;
+  return rank_bwd_workspace(B, Hq, L / n_chunks, d).total;
+}
+
+namespace {
+// Common checks of the ring_attn_bwd_rank_* calls; fills the workspace parts.
+int rank_bwd_args(BwdArgs* a, int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal, int schedule,
+                  const void* ws, size_t ws_bytes) {
+  int rc = check_ring_shape(B, Hq, Hkv, L, d, n_chunks, causal, schedule);
+  if (rc != RING_ATTN_OK) return rc;
+  const int C = L / n_chunks;
+  const RankBwdWorkspace w = rank_bwd_workspace(B, Hq, C, d);
+  if (!ws || ws_bytes < w.total || (reinterpret_cast<uintptr_t>(ws) & 255u)) return RING_ATTN_ERR_WORKSPACE;
+  std::memset(a, 0, sizeof *a);
+  uint8_t* p = static_cast<uint8_t*>(const_cast<void*>(ws));
+  a->B = B; a->Hq = Hq; a->Hkv = Hkv; a->L = C; a->Lpad = C; a->d = d; a->causal = causal != 0;
+  a->lse2 = reinterpret_cast<float*>(p + w.lse2);
+  a->Dvec = reinterpret_cast<float*>(p + w.dvec);
+  a->dq_acc = reinterpret_cast<float*>(p + w.dq);
+  return RING_ATTN_OK;
+}
+}  // namespace
+
+int ring_attn_bwd_rank_begin(const void* o_chunk, const void* dO_chunk, const float* lse_chunk, int B, int Hq,
+                             int Hkv, int L, int d, int n_chunks, int causal, int schedule, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream) {
+  BwdArgs a;
+  int rc = rank_bwd_args(&a, B, Hq, Hkv, L, d, n_chunks, causal, schedule, workspace, workspace_bytes);
+  if (rc != RING_ATTN_OK) return rc;
+  if (B == 0 || L == 0) return RING_ATTN_OK;
+  if (!o_chunk || !dO_chunk || !lse_chunk) return RING_ATTN_ERR_NULL;
+  if (!aligned16(o_chunk) || !aligned16(dO_chunk) || !aligned16(lse_chunk)) return RING_ATTN_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  a.o = o_chunk; a.dO = dO_chunk; a.lse = lse_chunk; a.timer = active_timer();
+  return launch_bwd_pre(a, static_cast<long long>(B) * Hq, 0, stream) == cudaSuccess ? RING_ATTN_OK
+                                                                                       : RING_ATTN_ERR_CUDA;
+}
+
+int ring_attn_bwd_rank_step(const void* q_chunk, const void* k_chunk, const void* v_chunk, const void* dO_chunk,
+                            float* dk_acc, float* dv_acc, int B, int Hq, int Hkv, int L, int d, int n_chunks,
+                            int causal, int schedule, int rank, int src, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream) {
+  BwdArgs a;
+  int rc = rank_bwd_args(&a, B, Hq, Hkv, L, d, n_chunks, causal, schedule, workspace, workspace_bytes);
+  if (rc != RING_ATTN_OK) return rc;
+  if (rank < 0 || rank >= n_chunks || src < 0 || src >= n_chunks) return RING_ATTN_ERR_SHAPE;
+  if (B == 0 || L == 0) return RING_ATTN_OK;
+  if (!q_chunk || !k_chunk || !v_chunk || !dO_chunk || !dk_acc || !dv_acc) return RING_ATTN_ERR_NULL;
+  const void* ptrs[] = {q_chunk, k_chunk, v_chunk, dO_chunk, dk_acc, dv_acc};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return RING_ATTN_ERR_UNSUPPORTED;
+  if (schedule == kSchedDfa) schedule = kSchedContig;  // one block: DistFlashAttention's is the ring's
+  const int N = n_chunks, C = L / N;
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  if (!make_map(&a.tm_q, q_chunk, bf, 2, d, C, B * Hq, 64) || !make_map(&a.tm_k, k_chunk, bf, 2, d, C, B * Hkv, 64) ||
+      !make_map(&a.tm_v, v_chunk, bf, 2, d, C, B * Hkv, 64) ||
+      !make_map(&a.tm_do, dO_chunk, bf, 2, d, C, B * Hq, 64) ||
+      !make_map(&a.tm_dkacc, dk_acc, f32, 4, d, C, B * Hkv, 32, 32) ||
+      !make_map(&a.tm_dvacc, dv_acc, f32, 4, d, C, B * Hkv, 32, 32))
+    return RING_ATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  int dev;
+  if ((rc = current_device(&dev)) != RING_ATTN_OK) return rc;
+  const int step = ((rank - src) % N + N) % N;
+  DevicePlan plan;
+  if ((rc = get_step_plan(dev, L, N, causal, schedule, step, rank, -(rank + 1) - 1, &plan)) != RING_ATTN_OK) return rc;
+  int* err;
+  if ((rc = status_ptr(dev, &err)) != RING_ATTN_OK) return rc;
+  a.dk_acc = dk_acc; a.dv_acc = dv_acc;
+  a.n_blocks = plan.n_blocks;
+  a.order = plan.order(); a.offsets = plan.offsets(); a.ranges = plan.ranges();
+  a.err = err; a.timer = active_timer();
+  a.step_nt = C / kTileRows; a.n_chunks = N; a.sched = schedule; a.step = step;
+  a.rank_lo = rank; a.z_rank = 0;  // buffers hold the block's two chunks only
+  return launch_bwd(a, stream) == cudaSuccess ? RING_ATTN_OK : RING_ATTN_ERR_CUDA;
+}
+
+int ring_attn_bwd_rank_end(void* dq_chunk, int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal,
+                           int schedule, const void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  BwdArgs a;
+  int rc = rank_bwd_args(&a, B, Hq, Hkv, L, d, n_chunks, causal, schedule, workspace, workspace_bytes);
+  if (rc != RING_ATTN_OK) return rc;
+  if (B == 0 || L == 0) return RING_ATTN_OK;
+  if (!dq_chunk) return RING_ATTN_ERR_NULL;
+  if (!aligned16(dq_chunk)) return RING_ATTN_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  a.dq = dq_chunk;
+  LaunchTimer* t = active_timer();
+  if (t) t->mark(RING_ATTN_KERNEL_BWD_POST, false, stream);
+  const cudaError_t e = launch_bwd_dq_post(a, static_cast<long long>(B) * Hq, stream);
+  if (t) t->mark(RING_ATTN_KERNEL_BWD_POST, true, stream);
+  return e == cudaSuccess ? RING_ATTN_OK : RING_ATTN_ERR_CUDA;
+}
+
+int ring_attn_grad_to_bf16(const float* acc, void* out, long long n_elems, float scale, cudaStream_t stream) {
+  if (n_elems < 0 || n_elems % 128 != 0) return RING_ATTN_ERR_SHAPE;
+  if (n_elems == 0) return RING_ATTN_OK;
+  if (!acc || !out) return RING_ATTN_ERR_NULL;
+  if (!aligned16(acc) || !aligned16(out)) return RING_ATTN_ERR_UNSUPPORTED;
+  LaunchTimer* t = active_timer();
+  if (t) t->mark(RING_ATTN_KERNEL_BWD_POST, false, stream);
+  const cudaError_t e = launch_grad_to_bf16(acc, out, scale, n_elems, stream);
+  if (t) t->mark(RING_ATTN_KERNEL_BWD_POST, true, stream);
+  return e == cudaSuccess ? RING_ATTN_OK : RING_ATTN_ERR_CUDA;
 }
 
 void ring_attn_release(void) {

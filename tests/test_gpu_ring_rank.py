@@ -1,0 +1,94 @@
+"""The per-rank calls of a multi-GPU ring on the GPU, through the C ABI:
+ring_attn_fwd_step_accumulate for the forward and ring_attn_bwd_rank_*
+(with ring_attn_grad_to_bf16) for the backward.  One process plays every
+rank of the ring in the order ring_dist runs them -- at step s rank r
+holds the key/value chunk of rank (r - s) mod N and, in the backward, that
+chunk's travelling fp32 dK/dV accumulators -- with no communication (this
+pool gives one GPU per run; the exchange itself is tested over gloo ranks
+on the CPU).  Every rank's o, lse, dq, dk, dv against the fp64 oracle on its
+rows, with the parity bounds of tolerance.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sequence_blockwise_self_gb300 as ra
+from sequence_blockwise_self_gb300 import build as lib_build
+from sequence_blockwise_self_gb300 import inputs
+from tolerance import TOL_LSE, check_bf16, check_fp32
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    lib_build.build()
+    ra.load()
+
+
+def f64(t):
+    return t.detach().float().cpu().double().numpy()
+
+
+def positions(L, N, causal, r, schedule):
+    return torch.tensor([p for p in range(L) if oracle.owner_rank(L, N, causal, p, schedule=schedule) == r],
+                        dtype=torch.long)
+
+
+# (B, Hq, Hkv, L, d, N, causal, schedule): chunks of whole 128-row tiles
+CASES = [
+    (1, 4, 2, 1024, 128, 4, True, "fold"),
+    (2, 2, 2, 768, 64, 3, False, "fold"),
+    (1, 3, 1, 1536, 128, 3, True, "striped"),
+    (1, 2, 1, 1024, 64, 4, True, "contiguous"),
+    (1, 2, 2, 512, 128, 1, True, "fold"),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "B{}Hq{}Hkv{}L{}d{}N{}".format(*c[:6]) +
+                         ("c" if c[6] else "e") + "-" + c[7])
+def test_every_rank_of_an_emulated_ring(case):
+    B, Hq, Hkv, L, d, N, causal, schedule = case
+    q, k, v, dO = inputs.make_inputs(B, Hq, Hkv, L, d, seed=90 + sum(case[:6]))
+    qd, kd, vd, dOd = q.cuda(), k.cuda(), v.cuda(), dO.cuda()
+    C = L // N
+    pos = [positions(L, N, causal, r, schedule).cuda() for r in range(N)]
+    ch = lambda x, r: x[:, :, pos[r]].contiguous()  # noqa: E731
+
+    # forward: each rank accumulates its blocks in ring order
+    o_run = [torch.zeros((B, Hq, C, d), dtype=torch.float32, device="cuda") for _ in range(N)]
+    lse_run = [torch.full((B, Hq, C), float("-inf"), dtype=torch.float32, device="cuda") for _ in range(N)]
+    for s in range(N):
+        for r in range(N):
+            src = (r - s) % N
+            ra.ring_attn_fwd_step_accumulate(ch(qd, r), ch(kd, src), ch(vd, src), o_run[r], lse_run[r], N, causal, r,
+                                             src, schedule=schedule)
+    torch.cuda.synchronize()
+    assert ra.device_status()[0] == 0
+    o_ref, lse_ref = oracle.fwd(q.double(), k.double(), v.double(), causal)
+    dq_ref, dk_ref, dv_ref, _, _ = oracle.bwd(q.double(), k.double(), v.double(), dO.double(), causal)
+    for r in range(N):
+        idx = pos[r].cpu().numpy()
+        check_bf16(f"o rank {r}", f64(o_run[r]), o_ref[:, :, idx])
+        check_fp32(f"lse rank {r}", f64(lse_run[r]), lse_ref[:, :, idx], TOL_LSE)
+
+    # backward: dQ local; dK/dV accumulators travel with their chunk
+    o = [x.to(torch.bfloat16) for x in o_run]
+    ranks = [ra.RankBackward(o[r], ch(dOd, r), lse_run[r], Hkv, N, causal, schedule=schedule) for r in range(N)]
+    dk_acc = [torch.zeros((B, Hkv, C, d), dtype=torch.float32, device="cuda") for _ in range(N)]
+    dv_acc = [torch.zeros_like(a) for a in dk_acc]
+    for s in range(N):
+        for r in range(N):
+            src = (r - s) % N
+            ranks[r].step(ch(qd, r), ch(kd, src), ch(vd, src), dk_acc[src], dv_acc[src], r, src)
+    dq = [ranks[r].end() for r in range(N)]
+    dk = [ra.grad_to_bf16(dk_acc[r], 1.0 / d ** 0.5) for r in range(N)]
+    dv = [ra.grad_to_bf16(dv_acc[r], 1.0) for r in range(N)]
+    torch.cuda.synchronize()
+    assert ra.device_status()[0] == 0
+    for r in range(N):
+        idx = pos[r].cpu().numpy()
+        check_bf16(f"dq rank {r}", f64(dq[r]), dq_ref[:, :, idx])
+        check_bf16(f"dk rank {r}", f64(dk[r]), dk_ref[:, :, idx])
+        check_bf16(f"dv rank {r}", f64(dv[r]), dv_ref[:, :, idx])

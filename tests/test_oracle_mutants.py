@@ -25,10 +25,13 @@ MUTANTS = {
     "gqa_head_map": ("const int g = h / (P->Hq / P->Hkv);\n  const double *qi = q_row(P, b, h, i);\n  const int n",
                      "const int g = h % P->Hkv;\n  const double *qi = q_row(P, b, h, i);\n  const int n"),
     "lse_drops_max": ("const double lse = m + log(sum);", "const double lse = log(sum) + (m > 0 ? 0 : m);"),
-    "dq_missing_scale": ("dq[c] += P->scale * dsij * kj[c];", "dq[c] += dsij * kj[c];"),
+    "dq_missing_scale": ("(dpij - D);\n    const double *kj = k_row(P, b, g, j);\n    for (int c = 0; c < P->d; ++c) dq[c] += P->scale * dsij * kj[c];",
+                         "(dpij - D);\n    const double *kj = k_row(P, b, g, j);\n    for (int c = 0; c < P->d; ++c) dq[c] += dsij * kj[c];"),
     "ds_missing_D": ("const double dsij = pij * (dpij - D);", "const double dsij = pij * dpij;"),
-    "dk_wrong_operand": ("dk[c] += P->scale * dsij * qi[c];", "dk[c] += P->scale * dsij * doi[c];"),
-    "dv_uses_ds": ("dv[c] += pij * doi[c];", "dv[c] += dsij * doi[c];"),
+    "dk_wrong_operand": ("(dpij - D[base + i]);\n      for (int c = 0; c < P->d; ++c) {\n        dv[c] += pij * doi[c];\n        dk[c] += P->scale * dsij * qi[c];",
+                         "(dpij - D[base + i]);\n      for (int c = 0; c < P->d; ++c) {\n        dv[c] += pij * doi[c];\n        dk[c] += P->scale * dsij * doi[c];"),
+    "dv_uses_ds": ("(dpij - D[base + i]);\n      for (int c = 0; c < P->d; ++c) {\n        dv[c] += pij * doi[c];\n        dk[c] += P->scale * dsij * qi[c];",
+                   "(dpij - D[base + i]);\n      for (int c = 0; c < P->d; ++c) {\n        dv[c] += dsij * doi[c];\n        dk[c] += P->scale * dsij * qi[c];"),
     "merge_wrong_sign": ("const double a = exp(*lse - merged), w = exp(lse_s - merged);",
                          "const double a = exp(*lse - merged), w = exp(merged - lse_s);"),
     "fold_wrong_pair": ("return sub < N ? sub : 2 * N - 1 - sub;", "return sub < N ? sub : sub - N;"),
@@ -43,6 +46,10 @@ MUTANTS = {
     "dfa_middle_launch_doubled": ("  if (t < N - t) {", "  if (t <= N - t) {"),
     "dfa_last_launch_dropped": ("for (int launch = 0; launch <= N / 2; ++launch)",
                                 "for (int launch = 0; launch < N / 2; ++launch)"),
+    "block_bwd_mask_dropped": ("owner_rank(P->L, t->n_chunks, P->causal, t->schedule, j) == t->src && (!P->causal || j <= i);",
+                               "owner_rank(P->L, t->n_chunks, P->causal, t->schedule, j) == t->src;"),
+    "block_bwd_dv_uses_ds": ("t->D[base + i]);\n      for (int c = 0; c < P->d; ++c) {\n        dv[c] += pij * doi[c];",
+                             "t->D[base + i]);\n      for (int c = 0; c < P->d; ++c) {\n        dv[c] += dsij * doi[c];"),
     "contiguous_as_fold": ("if (!causal || schedule != SCHED_FOLD) return p / (L / N);",
                            "if (!causal) return p / (L / N);"),
     "ffn_residual_dropped": ("y[c] = x[c] + acc[c];", "y[c] = acc[c];"),
@@ -82,6 +89,8 @@ def _quick_pins():
         ("dfa", lambda: [steps.test_contiguous_causal_ring_forms_equal_plain(L, N, sc)
                          for L, N in ((48, 3), (64, 4), (60, 5)) for sc in ("contiguous", "dfa")]),
         ("contiguous", lambda: steps.test_contiguous_step_with_zero_queries_closed_form(3)),
+        ("block_bwd", lambda: [steps.test_backward_blocks_sum_to_the_plain_backward(sc, True)
+                               for sc in ("fold", "contiguous")]),
         ("ffn", lambda: [ffn_pins.test_ffn_matches_torch(7, 16, 64), ffn_pins.test_gelu_values()]),
         ("ffn_bwd", lambda: ffn_pins.test_ffn_backward_matches_torch_autograd(5, 8, 24)),
         ("rows", lambda: [pins.test_row_sampled_routines_agree_with_full(c) for c in (False, True)]),

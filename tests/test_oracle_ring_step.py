@@ -258,3 +258,49 @@ def test_contiguous_schedules_need_causal():
     for schedule in ("contiguous", "dfa"):
         with pytest.raises(ValueError):
             oracle.ring_fwd(q, k, v, False, 2, schedule=schedule)
+
+
+# ------------------------------------------------------------- backward blocks
+
+@pytest.mark.parametrize("schedule", ["fold", "striped", "contiguous"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_blocks_sum_to_the_plain_backward(schedule, causal):
+    """Section 6.2's backward block by block: every (rank, src) block's dq
+    (rank's rows) and dk, dv (src's rows), summed, equal the plain backward
+    (itself pinned to torch's autograd)."""
+    if schedule == "contiguous" and not causal:
+        pytest.skip("the contiguous causal schedule needs causal attention")
+    L, N = 48, 3
+    q, k, v = _problem(1, 4, 2, L, 8, seed=41 + causal)
+    dO = np.random.default_rng(42).standard_normal(q.shape)
+    dq_ref, dk_ref, dv_ref, lse, D = oracle.bwd(q, k, v, dO, causal)
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for r in range(N):
+        rows = _rows_of_sched(L, N, causal, r, schedule)
+        for src in range(N):
+            a, b, c = oracle.ring_step_bwd(q, k, v, dO, lse, D, causal, N, r, src, schedule=schedule)
+            others = np.setdiff1d(np.arange(L), rows)
+            assert np.all(a[:, :, others] == 0)
+            dq += a
+            dk += b
+            dv += c
+    np.testing.assert_allclose(dq, dq_ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dk, dk_ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dv, dv_ref, rtol=0, atol=1e-12)
+
+
+def _rows_of_sched(L, N, causal, r, schedule):
+    return np.array([p for p in range(L) if oracle.owner_rank(L, N, causal, p, schedule=schedule) == r])
+
+
+def test_backward_block_a_key_chunk_after_the_queries_gives_nothing():
+    """Causal, contiguous chunks: rank 0's queries see none of rank 1's keys,
+    so that block contributes exactly zero to every gradient."""
+    L, N = 32, 2
+    q, k, v = _problem(1, 2, 1, L, 4, seed=7)
+    dO = np.random.default_rng(8).standard_normal(q.shape)
+    _, _, _, lse, D = oracle.bwd(q, k, v, dO, True)
+    a, b, c = oracle.ring_step_bwd(q, k, v, dO, lse, D, True, N, 0, 1, schedule="contiguous")
+    assert not a.any() and not b.any() and not c.any()

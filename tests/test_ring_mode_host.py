@@ -256,3 +256,26 @@ def test_contiguous_schedules_reject_bad_arguments(lib):
     assert (a.value, b.value) == (3, 0)
     assert lib.ring_attn_ring_fwd_workspace_size(1, 2, 1, 1280, 64, 5, 1, 3) > 0
     assert lib.ring_attn_ring_fwd_workspace_size(1, 2, 1, 1280, 64, 5, 0, 3) == 0
+
+
+def test_rank_backward_workspace_and_arguments(lib):
+    # statistics (2 floats a row) and the fp32 dQ accumulator of the rank's rows
+    ws = lib.ring_attn_bwd_rank_workspace_size(1, 2, 1, 1024, 64, 4, 1, 0)
+    rows = 2 * 256
+    assert ws == rows * 4 * 2 + rows * 64 * 4
+    assert lib.ring_attn_bwd_rank_workspace_size(1, 2, 1, 512, 64, 4, 1, 0) == 0    # sub-chunks of 64 rows
+    assert lib.ring_attn_bwd_rank_workspace_size(1, 2, 1, 1024, 64, 4, 0, 3) == 0   # DistFlashAttention needs causal
+    I, P = ctypes.c_int, ctypes.c_void_p
+    args = (1, 2, 1, 1024, 64, 4, 1, 0)
+    assert lib.ring_attn_bwd_rank_begin(P256, P256, P256, *args, NUL, ws, NUL) == capi.ERR_WORKSPACE
+    assert lib.ring_attn_bwd_rank_begin(P256, P256, P256, *args, P256, ws - 1, NUL) == capi.ERR_WORKSPACE
+    assert lib.ring_attn_bwd_rank_begin(NUL, P256, P256, *args, P256, ws, NUL) == capi.ERR_NULL
+    six = [P256] * 6
+    assert lib.ring_attn_bwd_rank_step(*six, *args, 4, 0, P256, ws, NUL) == capi.ERR_SHAPE   # rank out of range
+    assert lib.ring_attn_bwd_rank_step(*([NUL] * 6), *args, 0, 0, P256, ws, NUL) == capi.ERR_NULL
+    assert lib.ring_attn_bwd_rank_step(*six[:5], ctypes.c_void_p(8), *args, 0, 0, P256, ws, NUL) == \
+        capi.ERR_UNSUPPORTED
+    assert lib.ring_attn_bwd_rank_end(NUL, *args, P256, ws, NUL) == capi.ERR_NULL
+    assert lib.ring_attn_grad_to_bf16(P256, P256, 100, ctypes.c_float(1.0), NUL) == capi.ERR_SHAPE
+    assert lib.ring_attn_grad_to_bf16(NUL, P256, 128, ctypes.c_float(1.0), NUL) == capi.ERR_NULL
+    assert lib.ring_attn_grad_to_bf16(NUL, NUL, 0, ctypes.c_float(1.0), NUL) == capi.OK
