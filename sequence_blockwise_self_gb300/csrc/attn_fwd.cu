@@ -68,6 +68,7 @@ struct FwdSmem {
 
 struct FwdDev {
   int B, Hq, Hkv, L, causal;  // L: rows of one (batch, head) slice (step mode: the chunk length C)
+  int n_blocks;               // work items per (batch, head) in this launch
   float scale_log2;
   const int32_t* order;
   const int32_t* offsets;
@@ -479,9 +480,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
   S& sm = *reinterpret_cast<S*>(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // CTAs kv group by kv group: within the group of (batch, kv head), the
+  // plan's items in its order (longest first), each for the group's G query
+  // heads side by side -- the CTAs running together read the keys and values
+  // of one kv head (which stay in L2), each tile by G CTAs at about the same
+  // time
   const int BH = p.B * p.Hq;
-  const int item = p.order[blockIdx.x / BH];
-  const int bh = blockIdx.x % BH;
+  const int G = p.Hq / p.Hkv;
+  const int per_group = p.n_blocks * G;
+  const int gz = blockIdx.x / per_group;  // b * Hkv + kv head
+  const int rem = blockIdx.x % per_group;
+  const int item = p.order[rem / G];
+  const int bh = (gz / p.Hkv) * p.Hq + (gz % p.Hkv) * G + rem % G;
   const int b = bh / p.Hq, h = bh % p.Hq;
   int u = item, q_rank = 0, kv_rank = 0;
   int q_z = bh, out_z = bh, kv_z = b * p.Hkv + h / (p.Hq / p.Hkv);
@@ -589,6 +599,7 @@ size_t fwd_smem_bytes(int d) {
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
   FwdDev p;
   p.B = a.B; p.Hq = a.Hq; p.Hkv = a.Hkv; p.L = a.L; p.causal = a.causal;
+  p.n_blocks = a.n_blocks;
   p.scale_log2 = kLog2e / sqrtf(static_cast<float>(a.d));
   p.order = a.order; p.offsets = a.offsets; p.ranges = a.ranges;
   p.lse = a.lse; p.err = a.err;
