@@ -96,11 +96,17 @@ int ring_attn_bwd(const void* q, const void* k, const void* v, const void* o, co
  * RING_ATTN_NOALLOC_SCRATCH_BYTES.  A problem whose workspace
  * (ring_attn_bwd_workspace_size) plus plan does not fit is rejected with
  * RING_ATTN_ERR_WORKSPACE before anything is launched.  The first call on
- * each device looks up the array's device address (cudaGetSymbolAddress);
- * make that first call before any stream capture.  All calls share the one
- * array and it keeps the last call's contents (each call rewrites what it
- * needs): calls whose work may overlap on the GPU race and must be ordered
- * by the caller, e.g. by issuing them on one stream.
+ * each device looks up the array's device address (cudaGetSymbolAddress),
+ * and the first call for each (L, n_chunks, causal) builds its launch plan
+ * in page-locked host memory (cudaMallocHost, held until the process
+ * exits): make those first calls outside stream capture.  Later calls may
+ * be captured into a CUDA graph and replayed; each call (and each replay)
+ * copies the plan in and runs the pre-pass, main and conversion kernels on
+ * `stream`.  Its launches are counted by ring_attn_profile_read like those
+ * of ring_attn_bwd.  All calls share the one array and it keeps the last
+ * call's contents (each call rewrites what it needs): calls whose work may
+ * overlap on the GPU race and must be ordered by the caller, e.g. by
+ * issuing them on one stream.
  */
 int ring_attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
                           const void* dO, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int L, int d,

@@ -64,3 +64,36 @@ def test_noalloc_backward_matches_workspace_backward_on_two_calls_in_a_row():
 
 def capi_limit():
     return 64 * 1024 * 1024
+
+
+def test_noalloc_backward_captured_in_a_cuda_graph_and_replayed():
+    """A call captured into a CUDA graph (after one plain call of the same
+    shape) replays the whole backward: its gradients equal ring_attn_bwd's,
+    and after the inputs change in place a second replay follows them."""
+    lib_build.build()
+    ra.load()
+    B, Hq, Hkv, L, d, N, causal = 1, 4, 2, 1024, 128, 4, True
+    q, k, v, dO = (t.cuda() for t in inputs.make_inputs(B, Hq, Hkv, L, d, seed=520))
+    o, lse = ra.ring_attn_fwd(q, k, v, N, causal)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ra.ring_attn_bwd_noalloc(q, k, v, o, lse, dO, N, causal, dq, dk, dv)  # first call of this shape: not captured
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        ra.ring_attn_bwd_noalloc(q, k, v, o, lse, dO, N, causal, dq, dk, dv)
+    for seed in (521, 522):
+        q2, k2, v2, dO2 = (t.cuda() for t in inputs.make_inputs(B, Hq, Hkv, L, d, seed=seed))
+        for dst, src in ((q, q2), (k, k2), (v, v2), (dO, dO2)):
+            dst.copy_(src)
+        o2, lse2 = ra.ring_attn_fwd(q, k, v, N, causal)
+        o.copy_(o2)
+        lse.copy_(lse2)
+        for t in (dq, dk, dv):
+            t.fill_(float("nan"))
+        graph.replay()
+        ref = ra.ring_attn_bwd(q, k, v, o, lse, dO, N, causal)
+        torch.cuda.synchronize()
+        st, site = ra.device_status()
+        assert st == 0, f"device status {st} at {site:#x}"
+        for name, got, want in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+            _close(f"{name} replay seed {seed}", got, want)
