@@ -783,10 +783,59 @@ def run_ours(args, w):
             del a_tok, lse_b, dy_b, ws_bb
         del xf, w1f, w2f, b1f, b2f, yf, wsf
 
+    # (6) the other workloads of the parity suite (smaller), fused forward and
+    # backward each timed per launch by events on the launching stream, with
+    # the L2 flushed (a 256 MB write) before every step: their inputs fit in L2
+    others = None
+    if not args.no_workloads:
+        others = {}
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        for name, wo in inputs.WORKLOADS.items():
+            if name in (w.name, "tiny"):  # tiny: a parity case of 256 rows, nothing to time
+                continue
+            qo, ko, vo, dOo = (t.to(dev) for t in inputs.workload_inputs(wo, seed=inputs.WORKLOAD_SEEDS[name]))
+            oo, lseo = torch.empty_like(qo), torch.empty((wo.B, wo.Hq, wo.L), dtype=torch.float32, device=dev)
+            dqo, dko, dvo = torch.empty_like(qo), torch.empty_like(ko), torch.empty_like(vo)
+            wso = torch.empty(ra.bwd_workspace_size(wo.B, wo.Hq, wo.Hkv, wo.L, wo.d, wo.n_chunks, wo.causal),
+                              dtype=torch.uint8, device=dev)
+
+            def o_step():
+                flush.zero_()
+                ra.ring_attn_fwd(qo, ko, vo, wo.n_chunks, wo.causal, o=oo, lse=lseo, stream=stream)
+                ra.ring_attn_bwd(qo, ko, vo, oo, lseo, dOo, wo.n_chunks, wo.causal, dq=dqo, dk=dko, dv=dvo,
+                                 workspace=wso, stream=stream)
+            for _ in range(max(args.warmup, 3)):
+                o_step()
+            torch.cuda.synchronize(dev)
+            reps = max(args.steps, 10)
+            ra.profile_enable(True)
+            for _ in range(reps):
+                o_step()
+            torch.cuda.synchronize(dev)
+            pr = ra.profile_read()
+            ra.profile_enable(False)
+            st, site = ra.device_status()
+            if st != 0:
+                raise RuntimeError(f"device status {st} at site {site:#x} on workload {name}")
+            avg = {kk: (ms / n if n else 0.0) for kk, (ms, n) in pr.items()}
+            Fo = wo.fwd_flops()
+            tf_f = Fo / (avg["fwd"] * 1e-3) / 1e12
+            t_b = avg["bwd_pre"] + avg["bwd_main"] + avg["bwd_post"]
+            tf_b = 2.5 * Fo / (t_b * 1e-3) / 1e12
+            tf_bm = 2.5 * Fo / (avg["bwd_main"] * 1e-3) / 1e12
+            others[name] = {
+                "config": _describe(wo), "steps": reps, "l2": "flushed (256 MB write) before every step",
+                "fwd": {"ms": avg["fwd"], "tflops": tf_f, "frac_of_burst_peak": tf_f / peaks["burst"]},
+                "bwd": {"ms": t_b, "tflops": tf_b, "frac_of_burst_peak": tf_b / peaks["burst"],
+                        "main_kernel_ms": avg["bwd_main"], "main_kernel_tflops": tf_bm},
+            }
+            del qo, ko, vo, dOo, oo, lseo, dqo, dko, dvo, wso
+        del flush
+
     if os.sched_getaffinity(0) != all_cpus:
         os.sched_setaffinity(0, all_cpus)
 
-    # (6) CPU oracle baseline (rank 0, one GPU only)
+    # (7) CPU oracle baseline (rank 0, one GPU only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tf, det = oracle_sample(w, q, k, v, dO, seconds_target=15.0, seed=7)
@@ -815,6 +864,7 @@ def run_ours(args, w):
             "ring_mode": ring,
             "ulysses": ulysses,
             "ffn": ffn,
+            "workloads": others,
             # per step: forward, backward pre-pass, fused backward, dq conversion,
             # and with grouped queries the dk and dv conversions (the launch
             # list in profiles/launch_list_gqa_128k_step.md shows the same)
@@ -838,6 +888,7 @@ def main():
     ap.add_argument("--no-ring-mode", action="store_true")
     ap.add_argument("--no-ulysses", action="store_true")
     ap.add_argument("--no-ffn", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true", help="skip the smaller workloads' fwd/bwd timings")
     args = ap.parse_args()
     from sequence_blockwise_self_gb300 import inputs
 
