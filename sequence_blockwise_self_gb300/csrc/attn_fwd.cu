@@ -16,22 +16,32 @@
 //   warp 2      tensor-memory allocator
 //   warps 4-7   softmax of query tile 0 (one thread per row = TMEM lane)
 //   warps 8-11  softmax of query tile 1
-// Tensor memory (512 columns, fp32): S_0 [0,128) S_1 [128,256)
-// O_0 [256,256+d) O_1 [384,384+d).  P_t (bf16, two per 32-bit column) is
+// Tensor memory (512 columns, fp32), d = 128: S_0 [0,128) S_1 [128,256)
+// O_0 [256,384) O_1 [384,512).  P_t (bf16, two per 32-bit column) is
 // written over the first 64 columns of S_t once the softmax has the scores
 // in registers, and feeds O_t += P_t V as the tensor-memory A operand, so P
 // never touches shared memory (whose bandwidth the two SS products nearly
 // fill).  The next S_t is issued behind PV_t by the same thread; tcgen05
 // MMAs from one thread execute in issue order, so it cannot overwrite P_t
-// before PV_t has read it.
-//
-// Issue order per key/value tile j (as in FlashAttention-4 style pipelines):
+// before PV_t has read it.  Issue order per key/value tile j (as in
+// FlashAttention-4 style pipelines):
 //   PV_0(j), S_0(j+1), PV_1(j), S_1(j+1)
 // and one commit after each S_t(j+1) covers PV_t(j) as well, so when the
 // softmax of tile t sees S_t(j+1) the accumulator O_t is quiescent and P_t
-// may be overwritten.  The running maximum is in log2 units; O and l are
-// rescaled only when the maximum grew by more than 8 (a factor 256), which
-// keeps the result exact while skipping most rescales.
+// may be overwritten.
+//
+// d = 64 leaves room for P_t in columns of its own (O_t [256 + 64t, ...),
+// P_t [384 + 64t, ...)), so S_t(j+1) no longer has to wait for PV_t(j) to
+// read P_t: once P_t(j) is written the issue order is
+//   S_t(j+1), PV_t(j)
+// and the softmax gets its next scores after one product instead of two;
+// it writes P_t(j+1) once PV_t(j) has read P_t(j) (pv_done).  A 128-key
+// tile is half the tensor work there for the same softmax work, so the
+// softmax's wait for its next scores is what sets the pace.
+//
+// The running maximum is in log2 units; O and l are rescaled only when the
+// maximum grew by more than 8 (a factor 256), which keeps the result exact
+// while skipping most rescales.
 #include <cfloat>
 #include <climits>
 
@@ -60,10 +70,23 @@ struct FwdSmem {
   alignas(8) uint64_t kv_empty[kSlots];
   alignas(8) uint64_t s_full[2];
   alignas(8) uint64_t p_full[2];
+  alignas(8) uint64_t pv_done[2];  // d = 64: PV_t has read P_t (and O_t is quiescent)
   alignas(8) uint64_t o_final[2];
   alignas(8) uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
+};
+
+// Tensor-memory columns.  d = 128: S_0 [0,128) S_1 [128,256) O_0 [256,384)
+// O_1 [384,512), P_t over S_t's first 64 columns.  d = 64: S_0, S_1 as
+// before, O_0 [256,320) O_1 [320,384) and P_0 [384,448) P_1 [448,512) of
+// their own.
+template <int D>
+struct FwdTmem {
+  static constexpr bool kSepP = D == 64;
+  __host__ __device__ static constexpr uint32_t s(int t) { return 128u * t; }
+  __host__ __device__ static constexpr uint32_t o(int t) { return kSepP ? 256u + 64u * t : 256u + 128u * t; }
+  __host__ __device__ static constexpr uint32_t p(int t) { return kSepP ? 384u + 64u * t : 128u * t; }
 };
 
 struct FwdDev {
@@ -172,6 +195,7 @@ __device__ void fwd_producer(FwdSmem<D>& sm, const CUtensorMap* tm_q, const CUte
 template <int D>
 __device__ void fwd_mma(FwdSmem<D>& sm, uint32_t tmem, int nkv, bool o_preloaded, volatile int* ab, int* err) {
   using S = FwdSmem<D>;
+  using TM = FwdTmem<D>;
   constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
   constexpr uint32_t kIdO = idesc_bf16(128, D, false, true);
   const uint32_t total_uses = 2u * nkv;
@@ -181,67 +205,82 @@ __device__ void fwd_mma(FwdSmem<D>& sm, uint32_t tmem, int nkv, bool o_preloaded
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-      umma_ss_warp(tmem + 128 * t, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), kIdS, kk > 0);
+      umma_ss_warp(tmem + TM::s(t), sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), kIdS,
+                   kk > 0);
     }
   };
   auto issue_pv = [&](int t, uint32_t vslot, bool acc) {
     const uint32_t va = smem_u32(sm.kv[vslot]);
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk)  // A = P_t packed in S_t's columns: 8 per 16 keys
-      umma_ts_warp(tmem + 256 + 128 * t, tmem + 128 * t + 8 * kk, sdesc_sw128(va + kk * 2048, 16384, 1024), kIdO,
-              (acc || kk > 0) ? 1u : 0u);
+    for (int kk = 0; kk < 8; ++kk)  // A = P_t packed two bf16 per column: 8 columns per 16 keys
+      umma_ts_warp(tmem + TM::o(t), tmem + TM::p(t) + 8 * kk, sdesc_sw128(va + kk * 2048, 16384, 1024), kIdO,
+                   (acc || kk > 0) ? 1u : 0u);
   };
-  uint32_t n = 0;
-  auto wait_full = [&](uint32_t& slot, uint32_t& use_idx) -> bool {
-    slot = n % S::kSlots;
-    use_idx = n;
-    const bool r = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.kv_full[slot]), (n / S::kSlots) & 1, ab, err, kSiteFwdMma));
-    ++n;
-    return r;
+  // Load n of the producer's sequence (K_0, V_0, K_1, V_1, ...) sits in slot
+  // n % kSlots, filled for the (n / kSlots)-th time.
+  auto wait_load = [&](uint32_t n) -> bool {
+    return __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.kv_full[n % S::kSlots]), (n / S::kSlots) & 1, ab, err,
+                                             kSiteFwdMma));
   };
   // Release a slot only if the producer will refill it: every commit is
   // then awaited by someone before the CTA exits.
-  auto release = [&](uint32_t slot, uint32_t use_idx) {
-    if (use_idx + S::kSlots < total_uses) umma_commit_warp(smem_u32(&sm.kv_empty[slot]));
+  auto release = [&](uint32_t n) {
+    if (n + S::kSlots < total_uses) umma_commit_warp(smem_u32(&sm.kv_empty[n % S::kSlots]));
   };
 
+  // The loads a tile needs are awaited at the end of the previous tile, while
+  // the softmax still runs: an mbarrier wait costs this warp a few hundred
+  // cycles beside the softmax warps, which the tensor pipe should not idle
+  // through.
   bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.q_full), 0, ab, err, kSiteFwdMma));
+  if (ok) ok = wait_load(0);
   if (ok) {
-    uint32_t ks, ku;
-    ok = wait_full(ks, ku);
-    if (ok) {
-      tc_fence_after();
-      issue_s(0, ks);
-      umma_commit_warp(smem_u32(&sm.s_full[0]));
-      issue_s(1, ks);
-      umma_commit_warp(smem_u32(&sm.s_full[1]));
-      release(ks, ku);
-    }
+    tc_fence_after();
+    issue_s(0, 0);
+    umma_commit_warp(smem_u32(&sm.s_full[0]));
+    issue_s(1, 0);
+    umma_commit_warp(smem_u32(&sm.s_full[1]));
+    release(0);
   }
+  if (ok) ok = wait_load(1);
+  if (ok && nkv > 1) ok = wait_load(2);
   for (int j = 0; j < nkv && ok; ++j) {
-    uint32_t vs, vu, ks = 0, ku = 0;
-    ok = wait_full(vs, vu);
+    const uint32_t nk = 2u * (j + 1), nv = 2u * j + 1;
     const bool has_next = j + 1 < nkv;
     for (int t = 0; t < 2 && ok; ++t) {
       ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.p_full[t]), j & 1, ab, err, kSiteFwdMma));
       if (!ok) break;
       tc_fence_after();
-      issue_pv(t, vs, j > 0 || o_preloaded);
-      if (has_next) {
-        if (t == 0) {
-          ok = wait_full(ks, ku);
-          if (!ok) break;
-          tc_fence_after();
+      if constexpr (TM::kSepP) {
+        // S_t(j+1) first (the softmax's next scores), then PV_t(j)
+        if (has_next) {
+          issue_s(t, nk % S::kSlots);
+          umma_commit_warp(smem_u32(&sm.s_full[t]));
         }
-        issue_s(t, ks);
-        umma_commit_warp(smem_u32(&sm.s_full[t]));
+        issue_pv(t, nv % S::kSlots, j > 0 || o_preloaded);
+        umma_commit_warp(smem_u32(has_next ? &sm.pv_done[t] : &sm.o_final[t]));
       } else {
-        umma_commit_warp(smem_u32(&sm.o_final[t]));
+        // PV_t(j), then S_t(j+1) over P_t; the commit covers both
+        issue_pv(t, nv % S::kSlots, j > 0 || o_preloaded);
+        if (has_next) {
+          issue_s(t, nk % S::kSlots);
+          umma_commit_warp(smem_u32(&sm.s_full[t]));
+        } else {
+          umma_commit_warp(smem_u32(&sm.o_final[t]));
+        }
       }
     }
     if (!ok) break;
-    if (has_next) release(ks, ku);
-    release(vs, vu);
+    if (has_next) release(nk);
+    release(nv);
+    if (j + 2 < nkv) {  // V(j+1), K(j+2)
+      const uint32_t a = nv + 2, b = nk + 2;
+      ok = __all_sync(0xffffffffu, mbar_wait2(smem_u32(&sm.kv_full[a % S::kSlots]), (a / S::kSlots) & 1,
+                                              smem_u32(&sm.kv_full[b % S::kSlots]), (b / S::kSlots) & 1, ab, err,
+                                              kSiteFwdMma));
+    } else if (j + 1 < nkv) {
+      ok = wait_load(nv + 2);
+    }
   }
   if (!ok) {
     umma_commit_warp(smem_u32(&sm.drain));
@@ -258,9 +297,11 @@ __device__ void fwd_softmax(FwdSmem<D>& sm, uint32_t tmem, int t, const FwdDev& 
   const int row = wq * 32 + lane;
   const int qpos = q0 + 128 * t + row;        // row of the slice
   const int qseq = q_key<kStep>(p, q_rank, qpos);  // its key for the causal mask
+  using TM = FwdTmem<D>;
   const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-  const uint32_t t_s = tmem + 128 * t + lane_off;
-  const uint32_t t_o = tmem + 256 + 128 * t + lane_off;
+  const uint32_t t_s = tmem + TM::s(t) + lane_off;
+  const uint32_t t_o = tmem + TM::o(t) + lane_off;
+  const uint32_t t_p = tmem + TM::p(t) + lane_off;
   const float c = p.scale_log2;
   float m = -INFINITY, l = 0.f;
   if (kStep && p.acc_state) {
@@ -347,8 +388,28 @@ __device__ void fwd_softmax(FwdSmem<D>& sm, uint32_t tmem, int t, const FwdDev& 
       const float ms = (m == -INFINITY) ? 0.f : m;
       const float2 c2 = make_float2(c, c), nm2 = make_float2(-ms, -ms);
       float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-      // P = 2^(s c - m) in quarters; each quarter goes to tensor memory (two
-      // bf16 per column, over S_t's first 64 columns) as soon as it is packed.
+      // Rare: the row maximum grew by more than the threshold, so the O_t
+      // accumulated so far is rescaled to the new reference (O_t quiescent)
+      auto rescale_o = [&] {
+        if ((j > 0 || (kStep && p.acc_state)) && __any_sync(0xffffffffu, resc)) {
+          const float f = resc ? ex2(m_old - m) : 1.f;
+#pragma unroll
+          for (int c0 = 0; c0 < D / 32; ++c0) {
+            uint32_t r[32];
+            tmem_ld32(t_o + c0 * 32, r);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * f);
+            tmem_st32(t_o + c0 * 32, r);
+          }
+        }
+      };
+      // P in quarters; each quarter goes to tensor memory (two bf16 per
+      // column) as soon as it is packed.  d = 128: over S_t's first 64
+      // columns, and O_t is quiescent here (the commit that signalled S_t(j)
+      // covers PV_t(j-1)).  d = 64: to P_t's own columns once PV_t(j-1) has
+      // read them (which also leaves O_t quiescent), awaited after the first
+      // quarter's exponentials.  PV_t(j) is only issued after this thread
+      // arrives on p_full.
 #pragma unroll
       for (int half = 0; half < 4; ++half) {
         uint32_t pk[16];
@@ -362,24 +423,16 @@ __device__ void fwd_softmax(FwdSmem<D>& sm, uint32_t tmem, int t, const FwdDev& 
           pk[(i - 32 * half) / 2] = pack_bf16(p0, p1);
           pk[(i - 32 * half) / 2 + 1] = pack_bf16(p2, p3);
         }
-        tmem_st16_async(t_s + 16 * half, pk);
-      }
-      l += (acc0.x + acc0.y) + (acc1.x + acc1.y);
-      // Rare: the row maximum grew by more than the threshold, so the O_t
-      // accumulated so far is rescaled to the new reference.  O_t is
-      // quiescent here (the commit that signalled S_t(j) covers PV_t(j-1)),
-      // and PV_t(j) is only issued after this thread arrives on p_full.
-      if ((j > 0 || (kStep && p.acc_state)) && __any_sync(0xffffffffu, resc)) {
-        const float f = resc ? ex2(m_old - m) : 1.f;
-#pragma unroll
-        for (int c0 = 0; c0 < D / 32; ++c0) {
-          uint32_t r[32];
-          tmem_ld32(t_o + c0 * 32, r);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * f);
-          tmem_st32(t_o + c0 * 32, r);
+        if (TM::kSepP && half == 0 && j > 0) {
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.pv_done[t]), (j - 1) & 1, ab, err, kSiteFwdSoftmax));
+          if (!ok) break;
+          tc_fence_after();
         }
+        tmem_st16_async(t_p + 16 * half, pk);
       }
+      if (!ok) break;
+      l += (acc0.x + acc0.y) + (acc1.x + acc1.y);
+      rescale_o();
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(smem_u32(&sm.p_full[t]));
@@ -522,6 +575,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     for (int t = 0; t < 2; ++t) {
       mbar_init(smem_u32(&sm.s_full[t]), 1);
       mbar_init(smem_u32(&sm.p_full[t]), 128);
+      mbar_init(smem_u32(&sm.pv_done[t]), 1);
       mbar_init(smem_u32(&sm.o_final[t]), 1);
     }
     mbar_init(smem_u32(&sm.drain), 1);

@@ -81,6 +81,28 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// Two or three bounded waits whose phases are usually complete already: the
+// try-waits are issued back to back, so their latencies (a few hundred
+// cycles each beside busy warps) overlap; any phase still open is then
+// awaited one at a time.
+__device__ __forceinline__ bool mbar_wait2(uint32_t bar1, uint32_t parity1, uint32_t bar2, uint32_t parity2,
+                                           volatile int* abort_flag, int* err, int site) {
+  const bool r1 = mbar_try_wait(bar1, parity1);
+  const bool r2 = mbar_try_wait(bar2, parity2);
+  if (r1 && r2) return true;
+  return mbar_wait(bar1, parity1, abort_flag, err, site) && mbar_wait(bar2, parity2, abort_flag, err, site);
+}
+__device__ __forceinline__ bool mbar_wait3(uint32_t bar1, uint32_t parity1, uint32_t bar2, uint32_t parity2,
+                                           uint32_t bar3, uint32_t parity3, volatile int* abort_flag, int* err,
+                                           int site) {
+  const bool r1 = mbar_try_wait(bar1, parity1);
+  const bool r2 = mbar_try_wait(bar2, parity2);
+  const bool r3 = mbar_try_wait(bar3, parity3);
+  if (r1 && r2 && r3) return true;
+  return mbar_wait(bar1, parity1, abort_flag, err, site) && mbar_wait(bar2, parity2, abort_flag, err, site) &&
+         mbar_wait(bar3, parity3, abort_flag, err, site);
+}
+
 // ---------------------------------------------------------------- fences
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
