@@ -344,6 +344,25 @@ int ring_attn_bwd_rank_end(void* dq_chunk, int B, int Hq, int Hkv, int L, int d,
  * of 128); out [n_elems] bf16. */
 int ring_attn_grad_to_bf16(const float* acc, void* out, long long n_elems, float scale, cudaStream_t stream);
 
+/* Byte offset, inside a ring_attn_bwd_rank_* workspace of this shape, of
+ * the rank's fp32 dQ accumulator: B*Hq*C*d floats in the library's own
+ * tiled order, unscaled (0 if the shape is rejected, the offset is never 0
+ * otherwise).  With DistFlashAttention's schedule across GPUs (SP series
+ * section 7.2: an idle worker computes a block of a later worker's query
+ * chunk on its own keys), the helper runs that block through a workspace
+ * begun with the owner's o, dO, lse, then sends this accumulator to the
+ * owner, who adds it into its own with ring_attn_add_f32 before
+ * ring_attn_bwd_rank_end.  Both workspaces have the same shape, hence the
+ * same order. */
+size_t ring_attn_bwd_rank_dq_offset(int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal,
+                                    int schedule);
+
+/* dst[i] += src[i] for n_elems fp32 values (a multiple of 4; both 16-byte
+ * aligned device pointers; the caller owns both): partial gradients that
+ * arrive from another rank.  Errors: SHAPE, NULL, UNSUPPORTED (alignment),
+ * CUDA. */
+int ring_attn_add_f32(float* dst, const float* src, long long n_elems, cudaStream_t stream);
+
 /* Static description of a status code. */
 const char* ring_attn_strerror(int status);
 
@@ -488,7 +507,7 @@ enum {
   RING_ATTN_KERNEL_BWD_POST = 3, /* dq accumulator -> bf16 */
   RING_ATTN_KERNEL_RING_STEP = 4,  /* ring mode: one step of attention (every rank or one) */
   RING_ATTN_KERNEL_RING_MERGE = 5, /* ring mode: log-sum-exp merge */
-  RING_ATTN_KERNEL_RING_IO = 6,    /* ring mode: gather into / scatter out of chunk order */
+  RING_ATTN_KERNEL_RING_IO = 6,    /* ring mode: gather into / scatter out of chunk order, partial adds */
   RING_ATTN_KERNEL_ULYSSES_A2A = 7, /* Ulysses: all-to-all between sequence and head shards */
   RING_ATTN_KERNEL_FFN_GEMM = 8,    /* blockwise feed-forward: one of its two GEMMs */
   RING_ATTN_N_KERNELS = 9

@@ -46,6 +46,7 @@ from .capi import (  # noqa: F401
     ring_attn_fwd_step_accumulate,
     RankBackward,
     grad_to_bf16,
+    add_f32,
     ring_attn_merge,
     ring_attn_ring_fwd,
     ring_fwd_workspace_size,

@@ -91,6 +91,10 @@ def load():
     lib.ring_attn_bwd_rank_end.restype = I
     lib.ring_attn_grad_to_bf16.argtypes = [P, P, ctypes.c_longlong, ctypes.c_float, P]
     lib.ring_attn_grad_to_bf16.restype = I
+    lib.ring_attn_bwd_rank_dq_offset.argtypes = [I] * 8
+    lib.ring_attn_bwd_rank_dq_offset.restype = S
+    lib.ring_attn_add_f32.argtypes = [P, P, ctypes.c_longlong, P]
+    lib.ring_attn_add_f32.restype = I
     lib.ring_attn_merge.argtypes = [P, P, P, P, ctypes.c_longlong, I, P, P]
     lib.ring_attn_merge.restype = I
     lib.ring_attn_ring_fwd_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
@@ -355,6 +359,21 @@ class RankBackward:
         if rc != OK:
             raise RingAttnError(rc, "ring_attn_bwd_rank_step")
 
+    def dq_accumulator(self):
+        """The rank's fp32 dQ accumulator (a view into the workspace, in the
+        library's own order): what a DistFlashAttention helper sends back to
+        the owner of the query chunk."""
+        import torch
+        off = int(load().ring_attn_bwd_rank_dq_offset(*self.shape))
+        if off == 0:
+            raise RingAttnError(ERR_SHAPE, "ring_attn_bwd_rank_dq_offset")
+        B, Hq, C, d = self.dO.shape
+        return self.ws[off:off + 4 * B * Hq * C * d].view(torch.float32)
+
+    def add_dq(self, partial):
+        """Add a helper's dQ accumulator (see dq_accumulator) into this rank's."""
+        add_f32(self.dq_accumulator(), partial, stream=self.stream)
+
     def end(self, dq_chunk=None):
         import torch
         if dq_chunk is None:
@@ -376,6 +395,20 @@ def grad_to_bf16(acc, scale: float, out=None, stream=None):
     if rc != OK:
         raise RingAttnError(rc, "ring_attn_grad_to_bf16")
     return out
+
+
+def add_f32(dst, src, stream=None):
+    """In place: dst += src (contiguous fp32 CUDA tensors of equal size)."""
+    import torch
+    for t, n in ((dst, "dst"), (src, "src")):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous():
+            raise TypeError(f"{n} must be a contiguous fp32 CUDA tensor")
+    if dst.numel() != src.numel():
+        raise ValueError("dst and src differ in size")
+    rc = load().ring_attn_add_f32(_ptr(dst), _ptr(src), dst.numel(), _stream(stream))
+    if rc != OK:
+        raise RingAttnError(rc, "ring_attn_add_f32")
+    return dst
 
 
 def ring_attn_merge(o, lse, o_s, lse_s, o_out=None, stream=None):

@@ -120,6 +120,8 @@ cudaError_t launch_bwd_pre(const BwdArgs& a, long long q_slices, long long kv_sl
 cudaError_t launch_bwd_dq_post(const BwdArgs& a, long long q_slices, cudaStream_t stream);
 // out = bf16(scale * acc) for n_elems fp32 values (a multiple of 128).
 cudaError_t launch_grad_to_bf16(const float* acc, void* out, float scale, long long n_elems, cudaStream_t stream);
+// dst[0 .. n) += src[0 .. n) in fp32 (n a multiple of 4, 16-byte aligned)
+cudaError_t launch_add_f32(float* dst, const float* src, long long n, cudaStream_t stream);
 
 // Ring mode (ring_step.cu): the log-sum-exp merge of n_rows rows (in place
 // into o, lse; optional bf16 copy into o_out), and the gather of a [Z][L][d]

@@ -844,6 +844,23 @@ int ring_attn_grad_to_bf16(const float* acc, void* out, long long n_elems, float
   return e == cudaSuccess ? RING_ATTN_OK : RING_ATTN_ERR_CUDA;
 }
 
+size_t ring_attn_bwd_rank_dq_offset(int B, int Hq, int Hkv, int L, int d, int n_chunks, int causal, int schedule) {
+  if (check_ring_shape(B, Hq, Hkv, L, d, n_chunks, causal, schedule) != RING_ATTN_OK) return 0;
+  return rank_bwd_workspace(B, Hq, L / n_chunks, d).dq;
+}
+
+int ring_attn_add_f32(float* dst, const float* src, long long n_elems, cudaStream_t stream) {
+  if (n_elems < 0 || n_elems % 4 != 0) return RING_ATTN_ERR_SHAPE;
+  if (n_elems == 0) return RING_ATTN_OK;
+  if (!dst || !src) return RING_ATTN_ERR_NULL;
+  if (!aligned16(dst) || !aligned16(src)) return RING_ATTN_ERR_UNSUPPORTED;
+  LaunchTimer* t = active_timer();
+  if (t) t->mark(RING_ATTN_KERNEL_RING_IO, false, stream);
+  const cudaError_t e = launch_add_f32(dst, src, n_elems, stream);
+  if (t) t->mark(RING_ATTN_KERNEL_RING_IO, true, stream);
+  return e == cudaSuccess ? RING_ATTN_OK : RING_ATTN_ERR_CUDA;
+}
+
 void ring_attn_release(void) {
   std::lock_guard<std::mutex> lock(g_mutex);
   int cur = 0;

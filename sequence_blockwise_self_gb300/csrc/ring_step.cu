@@ -168,7 +168,29 @@ __global__ void __launch_bounds__(256) ring_scatter_grad_kernel(const float* __r
 
 unsigned blocks_for(long long n) { return static_cast<unsigned>((n + 255) / 256); }
 
+// dst[i] += src[i], four fp32 per thread (partial gradients arriving from
+// another rank: DistFlashAttention's helper blocks)
+__global__ void __launch_bounds__(256) add_f32_kernel(float4* __restrict__ dst, const float4* __restrict__ src,
+                                                      long long n4) {
+  const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= n4) return;
+  float4 a = dst[t];
+  const float4 b = src[t];
+  a.x += b.x;
+  a.y += b.y;
+  a.z += b.z;
+  a.w += b.w;
+  dst[t] = a;
+}
+
 }  // namespace
+
+cudaError_t launch_add_f32(float* dst, const float* src, long long n, cudaStream_t stream) {
+  const long long n4 = n / 4;
+  add_f32_kernel<<<blocks_for(n4), 256, 0, stream>>>(reinterpret_cast<float4*>(dst),
+                                                     reinterpret_cast<const float4*>(src), n4);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_ring_gather_rows(const float* src, float* dst, int Z, int L, int N, bool causal, int sched,
                                     cudaStream_t stream) {

@@ -1,5 +1,7 @@
 """The multi-GPU ring driver (ring_dist) on CPU ranks: gloo, world sizes 2
-to 4, one process per rank.  Each rank runs ring_attention_fwd and
+to 6, one process per rank, for the ring's chunk maps and for
+DistFlashAttention's protocol (helpers receive query chunks, return
+partial results and dQ).  Each rank runs ring_attention_fwd and
 ring_attention_bwd on its own chunk with the per-block arithmetic of the
 fp64 oracle (test infrastructure): a received key/value chunk is placed at
 its owner's positions of an otherwise zero sequence and the oracle's ring
@@ -85,6 +87,21 @@ class OracleRingOps:
     def bwd_end(self, state, dk_acc, dv_acc, d):
         return state["dq"], dk_acc, dv_acc
 
+    # DistFlashAttention's helper blocks
+    def fwd_merge(self, o_run, lse_run, o_s, lse_s):
+        o, lse = oracle.merge(o_run.numpy(), lse_run.numpy(), o_s.numpy(), lse_s.numpy())
+        o_run.copy_(torch.from_numpy(o))
+        lse_run.copy_(torch.from_numpy(lse))
+
+    def bwd_dq_partial(self, state):
+        return state["dq"]
+
+    def bwd_add_dq(self, state, partial):
+        state["dq"] += partial
+
+    def add(self, dst, src):
+        dst += src
+
 
 def _worker(rank, world, port, shape, schedule, out):
     from sequence_blockwise_self_gb300 import ring_dist
@@ -105,10 +122,14 @@ def _worker(rank, world, port, shape, schedule, out):
         dist.destroy_process_group()
 
 
-# (B, Hq, Hkv, L, d, causal), world size, schedule
+# (B, Hq, Hkv, L, d, causal), world size, schedule.  DistFlashAttention at
+# world sizes 2 (no helper), 3 and 5 (odd: every launch pairs), 4 and 6
+# (even: the middle launch pairs nobody).
 CASES = [((1, 2, 1, 24, 4, True), 2, "fold"), ((1, 2, 2, 24, 4, False), 3, "fold"),
          ((2, 4, 2, 32, 4, True), 4, "fold"), ((1, 2, 1, 24, 4, True), 3, "striped"),
-         ((1, 3, 1, 24, 4, True), 4, "contiguous")]
+         ((1, 3, 1, 24, 4, True), 4, "contiguous"), ((1, 2, 1, 16, 4, True), 2, "dfa"),
+         ((1, 2, 1, 24, 4, True), 3, "dfa"), ((2, 2, 2, 32, 4, True), 4, "dfa"),
+         ((1, 3, 1, 30, 4, True), 5, "dfa"), ((1, 2, 1, 36, 4, True), 6, "dfa")]
 
 
 @pytest.mark.parametrize("shape,world,schedule", CASES,
@@ -132,7 +153,30 @@ def test_ring_driver_over_gloo_ranks_equals_the_plain_definition(shape, world, s
             np.testing.assert_allclose(got, want[:, :, pos], rtol=0, atol=1e-10, err_msg=f"{name} rank {rank}")
 
 
-def test_ring_driver_rejects_the_distflash_schedule():
+def test_ring_driver_rejects_unknown_schedules_and_non_causal_distflash():
     from sequence_blockwise_self_gb300 import ring_dist
     with pytest.raises(ValueError):
-        ring_dist.ring_attention_fwd(None, None, None, True, schedule="dfa")
+        ring_dist.ring_attention_fwd(None, None, None, True, schedule="zigzag")
+    with pytest.raises(ValueError):
+        ring_dist.ring_attention_bwd(None, None, None, None, None, None, True, schedule="zigzag")
+
+
+def test_distflash_roles_cover_every_causal_block_once():
+    """DistFlashAttention's launches in the driver (SP series section 7.2):
+    every block (a, b <= a) runs exactly once -- on rank a at launch a - b
+    when a - b <= n/2, else on helper b at launch n - (a - b) -- and no rank
+    runs two blocks in one launch."""
+    from sequence_blockwise_self_gb300.ring_dist import _dfa_roles
+    for n in range(1, 13):
+        seen = {}
+        for t in range(n // 2 + 1):
+            for r in range(n):
+                own, helper_of, helped_by = _dfa_roles(n, r, t)
+                blocks = ([(r, r - t)] if own else []) + ([(helper_of, r)] if helper_of is not None else [])
+                assert len(blocks) <= 1, (n, t, r)
+                for blk in blocks:
+                    assert blk not in seen, (n, blk)
+                    seen[blk] = t
+                if helped_by is not None:  # the helper agrees on the pairing
+                    assert _dfa_roles(n, helped_by, t)[1] == r
+        assert set(seen) == {(a, b) for a in range(n) for b in range(a + 1)}, n

@@ -279,3 +279,20 @@ def test_rank_backward_workspace_and_arguments(lib):
     assert lib.ring_attn_grad_to_bf16(P256, P256, 100, ctypes.c_float(1.0), NUL) == capi.ERR_SHAPE
     assert lib.ring_attn_grad_to_bf16(NUL, P256, 128, ctypes.c_float(1.0), NUL) == capi.ERR_NULL
     assert lib.ring_attn_grad_to_bf16(NUL, NUL, 0, ctypes.c_float(1.0), NUL) == capi.OK
+
+
+def test_rank_backward_dq_accumulator_and_partial_adds(lib):
+    """The dQ accumulator's place in the rank workspace (DistFlashAttention's
+    helpers send it to the owner), and the fp32 add's argument checks."""
+    args = (1, 2, 1, 1024, 64, 4, 1, 3)
+    ws = lib.ring_attn_bwd_rank_workspace_size(*args)
+    off = lib.ring_attn_bwd_rank_dq_offset(*args)
+    rows = 2 * 256
+    assert off == 2 * rows * 4 and off % 256 == 0  # after the two per-row statistics
+    assert off + rows * 64 * 4 == ws                # and runs to the workspace's end
+    assert lib.ring_attn_bwd_rank_dq_offset(1, 2, 1, 1024, 64, 4, 0, 3) == 0  # rejected shape
+    assert lib.ring_attn_add_f32(P256, P256, 6, NUL) == capi.ERR_SHAPE          # not a multiple of 4
+    assert lib.ring_attn_add_f32(P256, P256, -4, NUL) == capi.ERR_SHAPE
+    assert lib.ring_attn_add_f32(NUL, P256, 8, NUL) == capi.ERR_NULL
+    assert lib.ring_attn_add_f32(ctypes.c_void_p(8), P256, 8, NUL) == capi.ERR_UNSUPPORTED
+    assert lib.ring_attn_add_f32(NUL, NUL, 0, NUL) == capi.OK                   # nothing to add
