@@ -167,3 +167,40 @@ def test_distflash_protocol_of_an_emulated_ring(case):
         check_bf16(f"dq rank {r}", f64(dq[r]), dq_ref[:, :, idx])
         check_bf16(f"dk rank {r}", f64(dk[r]), dk_ref[:, :, idx])
         check_bf16(f"dv rank {r}", f64(dv[r]), dv_ref[:, :, idx])
+
+
+def test_ring_driver_with_the_library_ops_on_one_rank():
+    """ring_dist's driver with its default ops (the library's kernels) on a
+    one-rank process group: DistFlashAttention's schedule at N = 1 needs no
+    exchange, so the driver's CUDA path -- running result, block, end;
+    rank backward, partial adds, conversion -- runs end to end on the GPU
+    and must equal the fp64 oracle."""
+    import os
+    import socket
+
+    import torch.distributed as dist
+
+    from sequence_blockwise_self_gb300 import ring_dist
+
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=0, world_size=1)
+    try:
+        B, Hq, Hkv, L, d = 1, 4, 2, 512, 128
+        q, k, v, dO = inputs.make_inputs(B, Hq, Hkv, L, d, seed=141)
+        qd, kd, vd, dOd = q.cuda(), k.cuda(), v.cuda(), dO.cuda()
+        o, lse = ring_dist.ring_attention_fwd(qd, kd, vd, True, schedule="dfa")
+        dq, dk, dv = ring_dist.ring_attention_bwd(qd, kd, vd, o, lse, dOd, True, schedule="dfa")
+        torch.cuda.synchronize()
+        assert ra.device_status()[0] == 0
+    finally:
+        dist.destroy_process_group()
+    o_ref, lse_ref = oracle.fwd(q.double(), k.double(), v.double(), True)
+    dq_ref, dk_ref, dv_ref, _, _ = oracle.bwd(q.double(), k.double(), v.double(), dO.double(), True)
+    check_bf16("o", f64(o), o_ref)
+    check_fp32("lse", f64(lse), lse_ref, TOL_LSE)
+    check_bf16("dq", f64(dq), dq_ref)
+    check_bf16("dk", f64(dk), dk_ref)
+    check_bf16("dv", f64(dv), dv_ref)
