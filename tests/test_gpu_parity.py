@@ -66,6 +66,12 @@ SMALL = [
     (1, 2, 2, 1024, 128, 8, True),
     (1, 2, 2, 128, 128, 1, True),     # a single tile
     (1, 1, 1, 2, 64, 1, True),        # degenerate: two tokens
+    # d = 64 over many key tiles (the forward's own P columns and pv_done
+    # hand-off, the backward's separate dQ columns): causal GQA and a ragged
+    # causal MHA whose last block ends mid-tile
+    (1, 8, 2, 4096, 64, 8, True),
+    (2, 4, 4, 3000, 64, 5, True),
+    (1, 4, 1, 2560, 64, 1, False),
 ]
 
 
