@@ -32,18 +32,19 @@
 //   bwd_post  dq = bf16(scale * dQ_acc); for grouped-query attention also
 //             dk = bf16(scale * dK_acc) and dv = bf16(dV_acc).
 //
-// Warp roles of bwd_main (384 threads): warp 0 TMA producer, warp 1
-// tcgen05 issuer (converged; one elected lane issues), warp 2 TMEM
-// allocator, warp 3 dQ reduce issuer, warps 4-11 two compute warpgroups.
-// Both warpgroups work on the same 128 key rows (one thread per row = TMEM
-// lane); warpgroup h takes query columns [64h, 64h+64) of S^T / dP^T,
-// dQ columns [h d/2, (h+1) d/2) in the drain, and dV (h = 0) or dK (h = 1)
-// in the epilogue.
+// Warp roles of bwd_main: warp 0 TMA producer, warp 1 tcgen05 issuer
+// (converged; one elected lane issues), warp 2 TMEM allocator, warp 3 dQ
+// reduce issuer, then the compute warpgroups: two at d = 128 (384
+// threads), four at d = 64 (640 threads; see BwdCfg).  All work on the
+// same 128 key rows (one thread per row = TMEM lane); of G groups, group h
+// takes query columns [h 128/G, (h+1) 128/G) of S^T / dP^T, dQ columns
+// [h d/G, (h+1) d/G) in the drain, and in the epilogue dV (d = 128: h = 0;
+// d = 64: h = 0, 1 by halves) or dK (the others).
 //
 // Tensor memory (fp32 columns): S^T [0,128) dP^T [128,256) dV [256,256+d)
 // dK [256+d, 256+2d); dQ at [384,448) for d = 64, and over S^T for d = 128
 // (S^T has been read by then; the next S^T waits for the dQ drain).  Packed
-// P^T of warpgroup h occupies [128+64h, 128+64h+32).
+// P^T of group h occupies the first half of its dP^T columns.
 //
 // Product order per query tile i: dP^T(i), S^T(i) | dV(i), dK(i) one
 // 16-query k-step at a time, each as soon as the compute warps have finished
@@ -73,7 +74,18 @@ namespace ra {
 
 namespace {
 
-constexpr int kBwdThreads = 384;
+// Compute warpgroups per CTA: two of 64 query columns at d = 128, four of
+// 32 at d = 64, where registers allow it and the softmax-gradient phase
+// rather than the products sets the pace (a 128 x 128 tile is half the
+// tensor work of d = 128 for the same per-element work).
+template <int D>
+struct BwdCfg {
+  static constexpr int kWG = D == 64 ? 4 : 2;        // compute warpgroups
+  static constexpr int kCols = 128 / kWG;            // query columns per warpgroup
+  static constexpr int kChunks = kCols / 16;         // 16-column chunks per warpgroup
+  static constexpr int kThreads = 128 + 128 * kWG;   // 4 role warps + the compute warpgroups
+  static constexpr int kComputeWarps = 4 * kWG;
+};
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
@@ -267,23 +279,26 @@ __device__ void bwd_mma(BwdSmem<D>& sm, uint32_t tmem, uint32_t n_total, volatil
     }
     umma_commit_warp(smem_u32(&sm.s_full));
     // dV += P^T dO and dK += dS^T Q one query k-step (16 queries) at a
-    // time, as the compute warps finish each 16-column chunk c of both
-    // halves: k-steps c (warpgroup 0's half) and 4 + c (warpgroup 1's), so
-    // the tensor core works while the softmax-gradient phase runs.
-    //   dV: A = packed P^T in tensor memory (k-step kk at column
-    //       128 + 64 (kk/4) + 8 (kk%4)), B = dO (MN-major)
+    // time, as the compute warps finish each 16-column chunk c of every
+    // warpgroup's columns: k-step kChunks h + c of warpgroup h, so the
+    // tensor core works while the softmax-gradient phase runs.
+    //   dV: A = packed P^T in tensor memory (warpgroup h's chunk c at
+    //       column 128 + kCols h + 8 c), B = dO (MN-major)
     //   dK: A = dS^T (K-major), B = Q (MN-major)
-    for (int c = 0; c < 4 && ok; ++c) {
+    using Cfg = BwdCfg<D>;
+    for (int c = 0; c < Cfg::kChunks && ok; ++c) {
       ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.chunk_ready[c]), i & 1, ab, err, kSiteBwdMma));
       if (!ok) break;
       tc_fence_after();
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int kk = 4 * h + c;
-        umma_ts_warp(t_dv, tmem + 128 + 64 * h + 8 * c, sdesc_sw128(da + kk * 2048, 16384, 1024), kIdKV,
+      for (int h = 0; h < Cfg::kWG; ++h) {
+        const int kk = Cfg::kChunks * h + c;  // 16-query k-step
+        // dS^T columns 16 kk.. : 64-column sub-tile kk / 4, bytes 32 (kk % 4)
+        const uint32_t ds_off = Cfg::kWG == 2 ? h * 16384 + c * 32 : (kk >> 2) * 16384 + (kk & 3) * 32;
+        umma_ts_warp(t_dv, tmem + 128 + Cfg::kCols * h + 8 * c, sdesc_sw128(da + kk * 2048, 16384, 1024), kIdKV,
                      (i > 0 || kk > 0) ? 1u : 0u);
-        umma_ss_warp(t_dk, sdesc_sw128(sa + h * 16384 + c * 32, 16, 1024), sdesc_sw128(qa + kk * 2048, 16384, 1024),
-                     kIdKV, (i > 0 || kk > 0) ? 1u : 0u);
+        umma_ss_warp(t_dk, sdesc_sw128(sa + ds_off, 16, 1024), sdesc_sw128(qa + kk * 2048, 16384, 1024), kIdKV,
+                     (i > 0 || kk > 0) ? 1u : 0u);
       }
     }
     if (!ok) break;
@@ -342,17 +357,19 @@ template <int D, bool kStep>
 __device__ void bwd_compute(BwdSmem<D>& sm, uint32_t tmem, const BwdDev& p, const CUtensorMap* tm_dkacc,
                             const CUtensorMap* tm_dvacc, int kv_z, int q_z, int kv_tile, int q_rank, int kv_rank,
                             const int32_t* rg, int nr, volatile int* ab, int* err) {
-  const int wg = ((threadIdx.x >> 5) - 4) >> 2;  // 0 or 1: which half of the query columns
+  using Cfg = BwdCfg<D>;
+  const int wg = ((threadIdx.x >> 5) - 4) >> 2;  // which kCols-column group of the queries
   const int wq = (threadIdx.x >> 5) & 3;         // TMEM lane quadrant
   const int lane = threadIdx.x & 31;
   const int row = wq * 32 + lane;  // key row (S^T lane) and also dQ query row
   const int kv_pos = kv_tile * 128 + row;  // row of the key/value slice
   const int kv_key = bwd_kv_key<kStep>(p, kv_rank, q_rank, kv_pos);
   const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-  const uint32_t t_s = tmem + 64 * wg + lane_off;          // this half's S^T columns
-  const uint32_t t_dp = tmem + 128 + 64 * wg + lane_off;   // this half's dP^T columns
+  const uint32_t t_s = tmem + Cfg::kCols * wg + lane_off;         // this group's S^T columns
+  const uint32_t t_dp = tmem + 128 + Cfg::kCols * wg + lane_off;  // this group's dP^T columns
   const uint32_t t_p = t_dp;                               // packed P^T over the first 32 of them
-  const uint32_t t_dq = ((D == 128) ? tmem : tmem + 384) + (D / 2) * wg + lane_off;
+  constexpr int kDqCols = D / Cfg::kWG;  // dQ columns this group drains
+  const uint32_t t_dq = ((D == 128) ? tmem : tmem + 384) + kDqCols * wg + lane_off;
   const uint32_t sa = smem_u32(sm.dsT);
   const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
   bool ok = true;
@@ -368,7 +385,7 @@ __device__ void bwd_compute(BwdSmem<D>& sm, uint32_t tmem, const BwdDev& p, cons
     // past the end; padded query rows have -lse2 = -inf, hence P = 0.
     const int first_valid_q = p.causal ? kv_key - bwd_q_key<kStep>(p, q_rank, q0) : 0;  // local query index
     const bool row_dead = kv_pos >= p.L;
-    const bool need_mask = row_dead || first_valid_q > 64 * wg;
+    const bool need_mask = row_dead || first_valid_q > Cfg::kCols * wg;
     const float* nlse2 = sm.lse2[slot];  // -lse * log2(e)
     const float* ndvec = sm.dvec[slot];  // -D
 
@@ -377,7 +394,7 @@ __device__ void bwd_compute(BwdSmem<D>& sm, uint32_t tmem, const BwdDev& p, cons
       uint32_t pk[8], dk8[8];
 #pragma unroll
       for (int x = 0; x < 16; x += 4) {
-        const int qq = 64 * wg + 16 * c + x;
+        const int qq = Cfg::kCols * wg + 16 * c + x;
         const float4 nl = *reinterpret_cast<const float4*>(nlse2 + qq);
         const float4 nd = *reinterpret_cast<const float4*>(ndvec + qq);
         const float2 a0 = __ffma2_rn(make_float2(__uint_as_float(rs[x]), __uint_as_float(rs[x + 1])), c2,
@@ -402,13 +419,15 @@ __device__ void bwd_compute(BwdSmem<D>& sm, uint32_t tmem, const BwdDev& p, cons
         dk8[x / 2] = pack_bf16(s0.x, s0.y);
         dk8[x / 2 + 1] = pack_bf16(s1.x, s1.y);
       }
-      // packed columns 8c..8c+7 of this half lie in dP^T columns 0..31 of the
-      // half, all read in chunks 0 and 1 (c <= 1 when c's own columns are
-      // written over, c's pending successor reads columns >= 16(c+1))
+      // packed columns 8c..8c+7 of this group lie in its dP^T columns
+      // 0..8 kChunks - 1, all read in the chunks before c's successor (c's
+      // own columns, 16c.., are read by the time they are written over)
       tmem_st8_async(t_p + 8 * c, pk);
-      const int ch = 2 * c;  // 16-byte chunk (8 queries) within the half's 128-byte row
-      st_shared_v4(sa + wg * 16384 + sw128_offset(row, ch), dk8[0], dk8[1], dk8[2], dk8[3]);
-      st_shared_v4(sa + wg * 16384 + sw128_offset(row, ch + 1), dk8[4], dk8[5], dk8[6], dk8[7]);
+      const int qb = Cfg::kCols * wg + 16 * c;               // the chunk's first query column
+      const uint32_t sub = sa + static_cast<uint32_t>(qb >> 6) * 16384;  // its 64-column sub-tile
+      const int ch = (qb & 63) >> 3;  // 16-byte chunk (8 queries) within the sub-tile's 128-byte row
+      st_shared_v4(sub + sw128_offset(row, ch), dk8[0], dk8[1], dk8[2], dk8[3]);
+      st_shared_v4(sub + sw128_offset(row, ch + 1), dk8[4], dk8[5], dk8[6], dk8[7]);
     };
     // chunk c of this warp's rows is in place -- P^T in tensor memory, dS^T
     // in shared memory, made visible to the tensor core's async proxy -- so
@@ -432,20 +451,25 @@ __device__ void bwd_compute(BwdSmem<D>& sm, uint32_t tmem, const BwdDev& p, cons
       signal(0);
       tmem_wait_ld(sB);
       reg_fence(pB);
-      tmem_ld16_async(t_s + 32, sA);
-      tmem_ld16_async(t_dp + 32, pA);
-      process(1, sB, pB);
-      signal(1);
-      tmem_wait_ld(sA);
-      reg_fence(pA);
-      tmem_ld16_async(t_s + 48, sB);
-      tmem_ld16_async(t_dp + 48, pB);
-      process(2, sA, pA);
-      signal(2);
-      tmem_wait_ld(sB);
-      reg_fence(pB);
-      process(3, sB, pB);
-      signal(3);
+      if constexpr (Cfg::kChunks == 4) {
+        tmem_ld16_async(t_s + 32, sA);
+        tmem_ld16_async(t_dp + 32, pA);
+        process(1, sB, pB);
+        signal(1);
+        tmem_wait_ld(sA);
+        reg_fence(pA);
+        tmem_ld16_async(t_s + 48, sB);
+        tmem_ld16_async(t_dp + 48, pB);
+        process(2, sA, pA);
+        signal(2);
+        tmem_wait_ld(sB);
+        reg_fence(pB);
+        process(3, sB, pB);
+        signal(3);
+      } else {
+        process(1, sB, pB);
+        signal(1);
+      }
     }
     // dQ drain: this thread's dQ row (a query row), this half's columns,
     // leaves tensor memory in one batched load; the columns are released at
@@ -455,24 +479,42 @@ __device__ void bwd_compute(BwdSmem<D>& sm, uint32_t tmem, const BwdDev& p, cons
     ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.dq_full), i & 1, ab, err, kSiteBwdSoftmax));
     if (!ok) break;
     tc_fence_after();
-    uint32_t d0[32], d1[32];
-    tmem_ld32_async(t_dq, d0);
-    if (D == 128) tmem_ld32_async(t_dq + 32, d1);
-    tmem_wait_ld(d0);
-    if (D == 128) reg_fence(d1);
-    tc_fence_before();
-    mbar_arrive(smem_u32(&sm.dq_free));
-    ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.qdo_read), i & 1, ab, err, kSiteBwdSoftmax));
-    if (!ok) break;
-    // staging in the accumulator's own layout: warpgroup wg's half tile in
-    // the tile's Q (wg 0) or dO (wg 1) buffer as [d/8 quads][128 rows][4]
-    const uint32_t stage = smem_u32(wg == 0 ? sm.q[slot] : sm.dO[slot]) + row * 16;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) st_shared_v4(stage + k * 2048, d0[4 * k], d0[4 * k + 1], d0[4 * k + 2], d0[4 * k + 3]);
-    if (D == 128) {
+    if constexpr (Cfg::kWG == 2) {
+      uint32_t d0[32], d1[32];
+      tmem_ld32_async(t_dq, d0);
+      if (D == 128) tmem_ld32_async(t_dq + 32, d1);
+      tmem_wait_ld(d0);
+      if (D == 128) reg_fence(d1);
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sm.dq_free));
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.qdo_read), i & 1, ab, err, kSiteBwdSoftmax));
+      if (!ok) break;
+      // staging in the accumulator's own layout: warpgroup wg's half tile in
+      // the tile's Q (wg 0) or dO (wg 1) buffer as [d/8 quads][128 rows][4]
+      const uint32_t stage = smem_u32(wg == 0 ? sm.q[slot] : sm.dO[slot]) + row * 16;
 #pragma unroll
       for (int k = 0; k < 8; ++k)
-        st_shared_v4(stage + (8 + k) * 2048, d1[4 * k], d1[4 * k + 1], d1[4 * k + 2], d1[4 * k + 3]);
+        st_shared_v4(stage + k * 2048, d0[4 * k], d0[4 * k + 1], d0[4 * k + 2], d0[4 * k + 3]);
+      if (D == 128) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          st_shared_v4(stage + (8 + k) * 2048, d1[4 * k], d1[4 * k + 1], d1[4 * k + 2], d1[4 * k + 3]);
+      }
+    } else {
+      // d = 64, four groups of 16 dQ columns: group wg's four quads of the
+      // [d/4 quads][128 rows][4] tile, quads 0..7 in the Q buffer, 8..15 in
+      // the dO buffer
+      uint32_t e[16];
+      tmem_ld16_async(t_dq, e);
+      tmem_wait_ld(e);
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sm.dq_free));
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.qdo_read), i & 1, ab, err, kSiteBwdSoftmax));
+      if (!ok) break;
+      const int quad0 = (kDqCols / 4) * wg;
+      const uint32_t stage = smem_u32(quad0 < D / 8 ? sm.q[slot] : sm.dO[slot]) + (quad0 % (D / 8)) * 2048 + row * 16;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) st_shared_v4(stage + k * 2048, e[4 * k], e[4 * k + 1], e[4 * k + 2], e[4 * k + 3]);
     }
     fence_proxy_async_smem();
     __syncwarp();
@@ -480,65 +522,107 @@ __device__ void bwd_compute(BwdSmem<D>& sm, uint32_t tmem, const BwdDev& p, cons
   }
   // Warp 3's reduce-adds have read every staged half once it joins here;
   // the dK/dV epilogue below reuses the Q and dO buffers across warps.
-  named_bar_sync(1, 288);
+  named_bar_sync(1, 128 * Cfg::kWG + 32);
   if (ok) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sm.kv_final), 0, ab, err, kSiteBwdEpilogue));
-  if (ok) {
-    // Epilogue: warpgroup 0 takes dV, warpgroup 1 takes dK.  Without grouped
-    // queries the CTA holds the whole gradient and writes bf16 (dK times
-    // scale); with them it adds its fp32 partial into the accumulator
-    // through staging boxes in the Q and dO buffers, free once kv_final
-    // arrived (every load was consumed by then).
-    tc_fence_after();
-    const uint32_t t_src = (wg == 0 ? tmem + 256 : tmem + 256 + D) + lane_off;
-    if (!p.kv_accumulate) {
-      const bool store = kv_pos < p.L;
-      const size_t base = (static_cast<size_t>(kv_z) * p.L + (store ? kv_pos : 0)) * D;
-      __nv_bfloat16* dst_row = (wg == 0 ? p.dv : p.dk) + base;
-      const float s = wg == 0 ? 1.f : p.scale;
-#pragma unroll
-      for (int c0 = 0; c0 < D / 32; c0 += 2) {
-        uint32_t r0[32], r1[32];
-        tmem_ld32_async(t_src + c0 * 32, r0);
-        tmem_ld32_async(t_src + c0 * 32 + 32, r1);
-        tmem_wait_ld(r0);
-        reg_fence(r1);
-        if (store) {
-          uint4* dst = reinterpret_cast<uint4*>(dst_row + c0 * 32);
-#pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4) {
-            const float* f = reinterpret_cast<const float*>(q4 < 4 ? r0 : r1) + (q4 & 3) * 8;
-            dst[q4] = make_uint4(pack_bf16(f[0] * s, f[1] * s), pack_bf16(f[2] * s, f[3] * s),
-                                 pack_bf16(f[4] * s, f[5] * s), pack_bf16(f[6] * s, f[7] * s));
+  if constexpr (Cfg::kWG == 2) {
+    if (ok) {
+      // Epilogue: warpgroup 0 takes dV, warpgroup 1 takes dK.  Without grouped
+      // queries the CTA holds the whole gradient and writes bf16 (dK times
+      // scale); with them it adds its fp32 partial into the accumulator
+      // through staging boxes in the Q and dO buffers, free once kv_final
+      // arrived (every load was consumed by then).
+      tc_fence_after();
+      const uint32_t t_src = (wg == 0 ? tmem + 256 : tmem + 256 + D) + lane_off;
+      if (!p.kv_accumulate) {
+        const bool store = kv_pos < p.L;
+        const size_t base = (static_cast<size_t>(kv_z) * p.L + (store ? kv_pos : 0)) * D;
+        __nv_bfloat16* dst_row = (wg == 0 ? p.dv : p.dk) + base;
+        const float s = wg == 0 ? 1.f : p.scale;
+  #pragma unroll
+        for (int c0 = 0; c0 < D / 32; c0 += 2) {
+          uint32_t r0[32], r1[32];
+          tmem_ld32_async(t_src + c0 * 32, r0);
+          tmem_ld32_async(t_src + c0 * 32 + 32, r1);
+          tmem_wait_ld(r0);
+          reg_fence(r1);
+          if (store) {
+            uint4* dst = reinterpret_cast<uint4*>(dst_row + c0 * 32);
+  #pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) {
+              const float* f = reinterpret_cast<const float*>(q4 < 4 ? r0 : r1) + (q4 & 3) * 8;
+              dst[q4] = make_uint4(pack_bf16(f[0] * s, f[1] * s), pack_bf16(f[2] * s, f[3] * s),
+                                   pack_bf16(f[4] * s, f[5] * s), pack_bf16(f[6] * s, f[7] * s));
+            }
           }
+        }
+      } else {
+        // warp e = 4 wg + wq stages its 32 rows x d fp32 (d/32 boxes of 4 KB) in
+        // half e % 2 of buffer e / 2 of {Q0, Q1, dO0, dO1}
+        const int e = 4 * wg + wq;
+        uint8_t* buf = e < 4 ? sm.q[e >> 1] : sm.dO[(e - 4) >> 1];
+        const uint32_t region = smem_u32(buf) + (e & 1) * (BwdSmem<D>::kTile / 2);
+        const CUtensorMap* tm = wg == 0 ? tm_dvacc : tm_dkacc;
+  #pragma unroll
+        for (int c0 = 0; c0 < D / 32; c0 += 2) {
+          uint32_t r0[32], r1[32];
+          tmem_ld32_async(t_src + c0 * 32, r0);
+          tmem_ld32_async(t_src + c0 * 32 + 32, r1);
+          tmem_wait_ld(r0);
+          reg_fence(r1);
+  #pragma unroll
+          for (int c8 = 0; c8 < 8; ++c8) {
+            st_shared_v4(region + c0 * 4096 + sw128_offset(lane, c8), r0[c8 * 4], r0[c8 * 4 + 1], r0[c8 * 4 + 2],
+                         r0[c8 * 4 + 3]);
+            st_shared_v4(region + (c0 + 1) * 4096 + sw128_offset(lane, c8), r1[c8 * 4], r1[c8 * 4 + 1],
+                         r1[c8 * 4 + 2], r1[c8 * 4 + 3]);
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          for (int c0 = 0; c0 < D / 32; ++c0)
+            tma_reduce_add_3d(tm, region + c0 * 4096, 32 * c0, kv_tile * 128 + wq * 32, kv_z);
+          bulk_commit_group();
+          bulk_wait_group<0>();
+        }
+        __syncwarp();
+      }
+    }
+  } else if (ok) {
+    // d = 64, four groups: groups 0, 1 take dV's columns [0,32), [32,64),
+    // groups 2, 3 dK's; with grouped queries each warp stages its 32 rows x
+    // 32 columns (one 4 KB box) in quarter e % 4 of buffer e / 4 of
+    // {Q0, Q1, dO0, dO1} and adds it into the accumulator
+    tc_fence_after();
+    const bool is_dv = wg < 2;
+    const int col0 = (wg & 1) * 32;
+    const uint32_t t_src = (is_dv ? tmem + 256 : tmem + 256 + D) + col0 + lane_off;
+    uint32_t r0[32];
+    tmem_ld32_async(t_src, r0);
+    tmem_wait_ld(r0);
+    if (!p.kv_accumulate) {
+      if (kv_pos < p.L) {
+        const float sc = is_dv ? 1.f : p.scale;
+        uint4* dst = reinterpret_cast<uint4*>((is_dv ? p.dv : p.dk) + (static_cast<size_t>(kv_z) * p.L + kv_pos) * D +
+                                              col0);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const float* f = reinterpret_cast<const float*>(r0) + q4 * 8;
+          dst[q4] = make_uint4(pack_bf16(f[0] * sc, f[1] * sc), pack_bf16(f[2] * sc, f[3] * sc),
+                               pack_bf16(f[4] * sc, f[5] * sc), pack_bf16(f[6] * sc, f[7] * sc));
         }
       }
     } else {
-      // warp e = 4 wg + wq stages its 32 rows x d fp32 (d/32 boxes of 4 KB) in
-      // half e % 2 of buffer e / 2 of {Q0, Q1, dO0, dO1}
       const int e = 4 * wg + wq;
-      uint8_t* buf = e < 4 ? sm.q[e >> 1] : sm.dO[(e - 4) >> 1];
-      const uint32_t region = smem_u32(buf) + (e & 1) * (BwdSmem<D>::kTile / 2);
-      const CUtensorMap* tm = wg == 0 ? tm_dvacc : tm_dkacc;
+      uint8_t* buf = (e >> 2) < 2 ? sm.q[e >> 2] : sm.dO[(e >> 2) - 2];
+      const uint32_t region = smem_u32(buf) + (e & 3) * 4096;
 #pragma unroll
-      for (int c0 = 0; c0 < D / 32; c0 += 2) {
-        uint32_t r0[32], r1[32];
-        tmem_ld32_async(t_src + c0 * 32, r0);
-        tmem_ld32_async(t_src + c0 * 32 + 32, r1);
-        tmem_wait_ld(r0);
-        reg_fence(r1);
-#pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
-          st_shared_v4(region + c0 * 4096 + sw128_offset(lane, c8), r0[c8 * 4], r0[c8 * 4 + 1], r0[c8 * 4 + 2],
-                       r0[c8 * 4 + 3]);
-          st_shared_v4(region + (c0 + 1) * 4096 + sw128_offset(lane, c8), r1[c8 * 4], r1[c8 * 4 + 1],
-                       r1[c8 * 4 + 2], r1[c8 * 4 + 3]);
-        }
-      }
+      for (int c8 = 0; c8 < 8; ++c8)
+        st_shared_v4(region + sw128_offset(lane, c8), r0[c8 * 4], r0[c8 * 4 + 1], r0[c8 * 4 + 2], r0[c8 * 4 + 3]);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        for (int c0 = 0; c0 < D / 32; ++c0)
-          tma_reduce_add_3d(tm, region + c0 * 4096, 32 * c0, kv_tile * 128 + wq * 32, kv_z);
+        tma_reduce_add_3d(is_dv ? tm_dvacc : tm_dkacc, region, col0, kv_tile * 128 + wq * 32, kv_z);
         bulk_commit_group();
         bulk_wait_group<0>();
       }
@@ -548,7 +632,7 @@ __device__ void bwd_compute(BwdSmem<D>& sm, uint32_t tmem, const BwdDev& p, cons
 }
 
 template <int D, bool kStep>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     ring_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                          const __grid_constant__ CUtensorMap tm_dkacc,
@@ -588,12 +672,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(smem_u32(&sm.do_empty[s]), 1);
     }
     mbar_init(smem_u32(&sm.s_full), 1);
-    for (int c = 0; c < 4; ++c) mbar_init(smem_u32(&sm.chunk_ready[c]), 8);
+    for (int c = 0; c < 4; ++c) mbar_init(smem_u32(&sm.chunk_ready[c]), BwdCfg<D>::kComputeWarps);
     mbar_init(smem_u32(&sm.dq_full), 1);
-    mbar_init(smem_u32(&sm.dq_free), 256);
+    mbar_init(smem_u32(&sm.dq_free), 32 * BwdCfg<D>::kComputeWarps);
     mbar_init(smem_u32(&sm.qdo_read), 1);
-    mbar_init(smem_u32(&sm.stage_full[0]), 8);
-    mbar_init(smem_u32(&sm.stage_full[1]), 8);
+    mbar_init(smem_u32(&sm.stage_full[0]), BwdCfg<D>::kComputeWarps);
+    mbar_init(smem_u32(&sm.stage_full[1]), BwdCfg<D>::kComputeWarps);
     mbar_init(smem_u32(&sm.kv_final), 1);
     mbar_init(smem_u32(&sm.drain), 1);
     fence_mbar_init();
@@ -624,7 +708,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else if (warp == 3) {
     if (lane == 0) bwd_dq_reducer<D>(sm, p.dq_acc, p.Lpad, q_z, rg, nr, ab, p.err);
     __syncwarp();
-    named_bar_sync(1, 288);
+    named_bar_sync(1, 128 * BwdCfg<D>::kWG + 32);
   } else if (warp >= 4) {
     bwd_compute<D, kStep>(sm, tmem, p, &tm_dkacc, &tm_dvacc, kv_z, q_z, kv_tile, q_rank, kv_rank, rg, nr, ab,
                           p.err);
@@ -782,7 +866,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, cudaStream_t stream) {
   const dim3 grid(static_cast<unsigned>(a.n_blocks) * a.B * a.Hq);
   const int kind = a.step_nt ? 4 : 2;  // profiling kinds of include/ring_attn.h: ring step / backward main
   if (a.timer) a.timer->mark(kind, false, stream);
-  kernel<<<grid, kBwdThreads, smem, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dkacc, a.tm_dvacc, p);
+  kernel<<<grid, BwdCfg<D>::kThreads, smem, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dkacc, a.tm_dvacc, p);
   e = cudaGetLastError();
   if (a.timer) a.timer->mark(kind, true, stream);
   if (e != cudaSuccess || a.step_nt) return e;  // ring steps: the driver converts the gradients
