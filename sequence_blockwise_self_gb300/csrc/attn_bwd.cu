@@ -501,11 +501,15 @@ __device__ void bwd_compute(BwdSmem<D>& sm, uint32_t tmem, const BwdDev& p, cons
           st_shared_v4(stage + (8 + k) * 2048, d1[4 * k], d1[4 * k + 1], d1[4 * k + 2], d1[4 * k + 3]);
       }
     } else {
-      // d = 64, four groups of 16 dQ columns: group wg's four quads of the
-      // [d/4 quads][128 rows][4] tile, quads 0..7 in the Q buffer, 8..15 in
-      // the dO buffer
-      uint32_t e[16];
-      tmem_ld16_async(t_dq, e);
+      // four groups of d/4 dQ columns: group wg's quads of the
+      // [d/4 quads][128 rows][4] tile, the first d/8 quads in the Q buffer,
+      // the rest in the dO buffer
+      uint32_t e[kDqCols];
+      if constexpr (kDqCols == 16) {
+        tmem_ld16_async(t_dq, e);
+      } else {
+        tmem_ld32_async(t_dq, e);
+      }
       tmem_wait_ld(e);
       tc_fence_before();
       mbar_arrive(smem_u32(&sm.dq_free));
@@ -514,7 +518,8 @@ __device__ void bwd_compute(BwdSmem<D>& sm, uint32_t tmem, const BwdDev& p, cons
       const int quad0 = (kDqCols / 4) * wg;
       const uint32_t stage = smem_u32(quad0 < D / 8 ? sm.q[slot] : sm.dO[slot]) + (quad0 % (D / 8)) * 2048 + row * 16;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) st_shared_v4(stage + k * 2048, e[4 * k], e[4 * k + 1], e[4 * k + 2], e[4 * k + 3]);
+      for (int k = 0; k < kDqCols / 4; ++k)
+        st_shared_v4(stage + k * 2048, e[4 * k], e[4 * k + 1], e[4 * k + 2], e[4 * k + 3]);
     }
     fence_proxy_async_smem();
     __syncwarp();
@@ -589,40 +594,49 @@ __device__ void bwd_compute(BwdSmem<D>& sm, uint32_t tmem, const BwdDev& p, cons
       }
     }
   } else if (ok) {
-    // d = 64, four groups: groups 0, 1 take dV's columns [0,32), [32,64),
-    // groups 2, 3 dK's; with grouped queries each warp stages its 32 rows x
-    // 32 columns (one 4 KB box) in quarter e % 4 of buffer e / 4 of
+    // four groups: groups 0, 1 take dV's columns by halves, groups 2, 3
+    // dK's; with grouped queries each warp stages its 32 rows x d/2 fp32
+    // (d/64 boxes of 4 KB) in quarter e % 4 of buffer e / 4 of
     // {Q0, Q1, dO0, dO1} and adds it into the accumulator
     tc_fence_after();
+    constexpr int kEpCols = D / 2;
     const bool is_dv = wg < 2;
-    const int col0 = (wg & 1) * 32;
+    const int col0 = (wg & 1) * kEpCols;
     const uint32_t t_src = (is_dv ? tmem + 256 : tmem + 256 + D) + col0 + lane_off;
-    uint32_t r0[32];
-    tmem_ld32_async(t_src, r0);
-    tmem_wait_ld(r0);
-    if (!p.kv_accumulate) {
-      if (kv_pos < p.L) {
-        const float sc = is_dv ? 1.f : p.scale;
-        uint4* dst = reinterpret_cast<uint4*>((is_dv ? p.dv : p.dk) + (static_cast<size_t>(kv_z) * p.L + kv_pos) * D +
-                                              col0);
+    const int e = 4 * wg + wq;
+    uint8_t* buf = (e >> 2) < 2 ? sm.q[e >> 2] : sm.dO[(e >> 2) - 2];
+    const uint32_t region = smem_u32(buf) + (e & 3) * (kEpCols / 32) * 4096;
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const float* f = reinterpret_cast<const float*>(r0) + q4 * 8;
-          dst[q4] = make_uint4(pack_bf16(f[0] * sc, f[1] * sc), pack_bf16(f[2] * sc, f[3] * sc),
-                               pack_bf16(f[4] * sc, f[5] * sc), pack_bf16(f[6] * sc, f[7] * sc));
+    for (int c0 = 0; c0 < kEpCols / 32; ++c0) {
+      uint32_t r0[32];
+      tmem_ld32_async(t_src + c0 * 32, r0);
+      tmem_wait_ld(r0);
+      if (!p.kv_accumulate) {
+        if (kv_pos < p.L) {
+          const float sc = is_dv ? 1.f : p.scale;
+          uint4* dst = reinterpret_cast<uint4*>((is_dv ? p.dv : p.dk) + (static_cast<size_t>(kv_z) * p.L + kv_pos) * D +
+                                                col0 + 32 * c0);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const float* f = reinterpret_cast<const float*>(r0) + q4 * 8;
+            dst[q4] = make_uint4(pack_bf16(f[0] * sc, f[1] * sc), pack_bf16(f[2] * sc, f[3] * sc),
+                                 pack_bf16(f[4] * sc, f[5] * sc), pack_bf16(f[6] * sc, f[7] * sc));
+          }
         }
-      }
-    } else {
-      const int e = 4 * wg + wq;
-      uint8_t* buf = (e >> 2) < 2 ? sm.q[e >> 2] : sm.dO[(e >> 2) - 2];
-      const uint32_t region = smem_u32(buf) + (e & 3) * 4096;
+      } else {
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8)
-        st_shared_v4(region + sw128_offset(lane, c8), r0[c8 * 4], r0[c8 * 4 + 1], r0[c8 * 4 + 2], r0[c8 * 4 + 3]);
+        for (int c8 = 0; c8 < 8; ++c8)
+          st_shared_v4(region + c0 * 4096 + sw128_offset(lane, c8), r0[c8 * 4], r0[c8 * 4 + 1], r0[c8 * 4 + 2],
+                       r0[c8 * 4 + 3]);
+      }
+    }
+    if (p.kv_accumulate) {
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        tma_reduce_add_3d(is_dv ? tm_dvacc : tm_dkacc, region, col0, kv_tile * 128 + wq * 32, kv_z);
+        for (int c0 = 0; c0 < kEpCols / 32; ++c0)
+          tma_reduce_add_3d(is_dv ? tm_dvacc : tm_dkacc, region + c0 * 4096, col0 + 32 * c0, kv_tile * 128 + wq * 32,
+                            kv_z);
         bulk_commit_group();
         bulk_wait_group<0>();
       }
