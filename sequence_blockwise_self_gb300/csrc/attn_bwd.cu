@@ -738,6 +738,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 // block of d floats of the fp32 dQ accumulator (whatever its layout, the
 // blocks of all rows cover it) and, for rows below kv_rows, the rows of the
 // dK and dV accumulators (grouped-query attention; null otherwise).
+// The pre-pass, HBM-bound: a bf16 row of o (and of dO) is D/8 16-byte
+// pieces, so a warp covers 32/(D/8) rows at once and takes kIter such groups,
+// all loads issued before any use so that enough bytes are in flight; the row
+// sums reduce across the row's lanes by shuffles.  Each warp then zeroes the
+// accumulator chunks of its rows (the accumulators are B*Hq*Lpad*D and
+// B*Hkv*Lpad*D contiguous floats whatever their tiling).
 template <int D>
 __global__ void __launch_bounds__(256) ring_attn_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
                                                                 const __nv_bfloat16* __restrict__ dO,
@@ -745,49 +751,58 @@ __global__ void __launch_bounds__(256) ring_attn_bwd_pre_kernel(const __nv_bfloa
                                                                 float* dvec, float* dq_acc, float* dk_acc,
                                                                 float* dv_acc, int L, int Lpad, long long n_rows,
                                                                 long long kv_rows) {
-  const long long r = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  constexpr int kLanesPerRow = D / 8;
+  constexpr int kRowsPerGroup = 32 / kLanesPerRow;
+  constexpr int kIter = 4;
+  constexpr int kRowsPerWarp = kRowsPerGroup * kIter;
+  const long long warp_id = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  if (r >= n_rows) return;
-  const long long bh = r / Lpad;
-  const int i = static_cast<int>(r % Lpad);
-  constexpr int kPer = D / 32;  // elements per lane
-  float acc = 0.f;
-  if (i < L) {
-    const size_t off = (static_cast<size_t>(bh) * L + i) * D + lane * kPer;
-    if constexpr (kPer == 4) {
-      const uint2 a = *reinterpret_cast<const uint2*>(o + off);
-      const uint2 bb = *reinterpret_cast<const uint2*>(dO + off);
-      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&bb);
+  const int sub = lane / kLanesPerRow, piece = lane % kLanesPerRow;
+  const long long r0 = warp_id * kRowsPerWarp;
+  if (r0 >= n_rows) return;
+  uint4 a[kIter], b[kIter];
 #pragma unroll
-      for (int x = 0; x < 2; ++x) {
-        const float2 fa = __bfloat1622float2(a2[x]), fb = __bfloat1622float2(b2[x]);
-        acc = fmaf(fa.x, fb.x, acc);
-        acc = fmaf(fa.y, fb.y, acc);
-      }
-    } else {
-      const uint32_t a = *reinterpret_cast<const uint32_t*>(o + off);
-      const uint32_t bb = *reinterpret_cast<const uint32_t*>(dO + off);
-      const float2 fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a));
-      const float2 fb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bb));
-      acc = fmaf(fa.x, fb.x, fa.y * fb.y);
+  for (int it = 0; it < kIter; ++it) {
+    const long long r = r0 + it * kRowsPerGroup + sub;
+    const long long bh = r / Lpad;
+    const int i = static_cast<int>(r % Lpad);
+    a[it] = b[it] = make_uint4(0u, 0u, 0u, 0u);
+    if (r < n_rows && i < L) {
+      const size_t off = (static_cast<size_t>(bh) * L + i) * D + piece * 8;
+      a[it] = *reinterpret_cast<const uint4*>(o + off);
+      b[it] = *reinterpret_cast<const uint4*>(dO + off);
     }
   }
 #pragma unroll
-  for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-  if (lane == 0) {
-    dvec[r] = (i < L) ? -acc : 0.f;
-    lse2[r] = (i < L) ? -lse[static_cast<size_t>(bh) * L + i] * kLog2e : -INFINITY;
+  for (int it = 0; it < kIter; ++it) {
+    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a[it]);
+    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b[it]);
+    float acc = 0.f;
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const float2 fa = __bfloat1622float2(a2[x]), fb = __bfloat1622float2(b2[x]);
+      acc = fmaf(fa.x, fb.x, acc);
+      acc = fmaf(fa.y, fb.y, acc);
+    }
+#pragma unroll
+    for (int s = kLanesPerRow / 2; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+    const long long r = r0 + it * kRowsPerGroup + sub;
+    if (piece == 0 && r < n_rows) {
+      const long long bh = r / Lpad;
+      const int i = static_cast<int>(r % Lpad);
+      dvec[r] = (i < L) ? -acc : 0.f;
+      lse2[r] = (i < L) ? -lse[static_cast<size_t>(bh) * L + i] * kLog2e : -INFINITY;
+    }
   }
   const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
-  float4* z = reinterpret_cast<float4*>(dq_acc + static_cast<size_t>(r) * D);
-#pragma unroll
-  for (int x = lane; x < D / 4; x += 32) z[x] = zero;
-  if (dk_acc && r < kv_rows) {
-    float4* zk = reinterpret_cast<float4*>(dk_acc + static_cast<size_t>(r) * D);
-    float4* zv = reinterpret_cast<float4*>(dv_acc + static_cast<size_t>(r) * D);
-#pragma unroll
-    for (int x = lane; x < D / 4; x += 32) {
+  const long long rows_here = min(static_cast<long long>(kRowsPerWarp), n_rows - r0);
+  float4* z = reinterpret_cast<float4*>(dq_acc + static_cast<size_t>(r0) * D);
+  for (long long x = lane; x < rows_here * (D / 4); x += 32) z[x] = zero;
+  if (dk_acc && r0 < kv_rows) {
+    const long long kv_here = min(static_cast<long long>(kRowsPerWarp), kv_rows - r0);
+    float4* zk = reinterpret_cast<float4*>(dk_acc + static_cast<size_t>(r0) * D);
+    float4* zv = reinterpret_cast<float4*>(dv_acc + static_cast<size_t>(r0) * D);
+    for (long long x = lane; x < kv_here * (D / 4); x += 32) {
       zk[x] = zero;
       zv[x] = zero;
     }
@@ -842,7 +857,9 @@ __global__ void __launch_bounds__(256) ring_attn_bwd_dq_post_kernel(const float*
 template <int D>
 cudaError_t launch_bwd_pre_d(const BwdArgs& a, long long q_slices, long long kv_slices, cudaStream_t stream) {
   const long long rows = q_slices * a.Lpad;
-  const unsigned pre_blocks = static_cast<unsigned>((rows * 32 + 255) / 256);
+  constexpr long long kRowsPerWarp = 4 * (32 / (D / 8));  // as in ring_attn_bwd_pre_kernel
+  const long long warps = (rows + kRowsPerWarp - 1) / kRowsPerWarp;
+  const unsigned pre_blocks = static_cast<unsigned>((warps * 32 + 255) / 256);
   if (a.timer) a.timer->mark(1, false, stream);
   ring_attn_bwd_pre_kernel<D><<<pre_blocks, 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dO), a.lse, a.lse2, a.Dvec,
