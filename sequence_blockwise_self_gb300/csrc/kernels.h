@@ -142,8 +142,8 @@ cudaError_t launch_ring_scatter_grad(const float* acc, void* g, float scale, boo
 
 // Ulysses / USP (ulysses.cu): the all-to-all between the N = U R sequence
 // shards [N][B][H][L/N][row] and the U head groups [U][B][H/U][L][row]
-// (to_heads) or back; row_bytes a multiple of 16 (d values of bf16) or 4
-// (one fp32).  causal with R > 1: the shards follow the ring's fold.
+// (to_heads) or back; row_bytes 128 or 256 (d = 64 or 128 values of bf16)
+// or 4 (one fp32).  causal with R > 1: the shards follow the ring's fold.
 cudaError_t launch_ulysses_a2a(const void* src, void* dst, int row_bytes, int B, int H, int U, int R, int L,
                                bool causal, bool to_heads, cudaStream_t stream);
 // Token-major [B][L][H][row] <-> head-major [B][H][L][row]; row_bytes a

@@ -21,6 +21,8 @@
 // so that the fused kernel's fold over R chunks is USP's load-balanced
 // ring.  The kernels copy 16 bytes per thread (rows of d values: 128 or
 // 256 bytes of bf16, 4 bytes of fp32 for lse) and are HBM-bound.
+#include <climits>
+
 #include "kernels.h"
 
 namespace ra {
@@ -54,18 +56,46 @@ __device__ __forceinline__ long long head_row(long long s, const UspMap& m) {
   return ((static_cast<long long>(g) * m.B + b) * m.Hn + hl) * m.L + pos;
 }
 
-// vec16 = 16-byte vectors per row; to_heads: sequence shards -> head groups.
+// kVec = 16-byte vectors per row; to_heads: sequence shards -> head groups.
+// Grid: y (and z beyond 65535) = the (n, b, h) slice of C shard rows, x =
+// runs of 4 x 256 vectors within it, so the slice's coordinates are
+// per-block constants and a thread only splits its vector index into (row,
+// vector) by a shift; its four copies are all loaded before any is stored.
+// Consecutive threads walk consecutive vectors of both layouts (a shard
+// slice's rows are consecutive positions of one head, except across the
+// fold's two pieces).
+template <int kVec>
 __global__ void __launch_bounds__(256) ulysses_a2a_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
-                                                          int vec16, UspMap m, int to_heads, long long n_vec) {
-  const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (t >= n_vec) return;
-  const int c = static_cast<int>(t % vec16);
-  const long long s = t / vec16;  // row in the shard layout
-  if (to_heads) {
-    dst[head_row(s, m) * vec16 + c] = src[s * vec16 + c];
-  } else {
-    dst[s * vec16 + c] = src[head_row(s, m) * vec16 + c];
+                                                          UspMap m, int to_heads, int slices) {
+  constexpr int kUnroll = 4;
+  const int sl = static_cast<int>(blockIdx.z) * static_cast<int>(gridDim.y) + static_cast<int>(blockIdx.y);
+  if (sl >= slices) return;
+  const int h = sl % m.H, b = (sl / m.H) % m.B, n = sl / (m.H * m.B);
+  const int g = h / m.Hn, hl = h % m.Hn;
+  const long long shard0 = static_cast<long long>(sl) * m.C;
+  const long long head0 = ((static_cast<long long>(g) * m.B + b) * m.Hn + hl) * m.L;
+  const int r = n / m.U, u = n % m.U;
+  const int c = m.fold ? m.L / (2 * m.R) : 0, piece = m.fold ? c / m.U : 0;
+  const int per_slice = m.C * kVec;
+  const int t0 = static_cast<int>(blockIdx.x) * (256 * kUnroll) + static_cast<int>(threadIdx.x);
+  uint4 v[kUnroll];
+  long long so[kUnroll], ho[kUnroll];
+#pragma unroll
+  for (int k = 0; k < kUnroll; ++k) {
+    const int t = t0 + 256 * k;
+    const int i = t / kVec, cc = t % kVec;
+    int pos;
+    if (!m.fold)
+      pos = n * m.C + i;
+    else
+      pos = i < piece ? r * c + u * piece + i : (2 * m.R - 1 - r) * c + u * piece + (i - piece);
+    so[k] = (shard0 + i) * kVec + cc;
+    ho[k] = (head0 + pos) * kVec + cc;
+    if (t < per_slice) v[k] = src[to_heads ? so[k] : ho[k]];
   }
+#pragma unroll
+  for (int k = 0; k < kUnroll; ++k)
+    if (t0 + 256 * k < per_slice) dst[to_heads ? ho[k] : so[k]] = v[k];
 }
 
 // The same permutation for one fp32 per row (lse): one value per thread.
@@ -89,14 +119,25 @@ cudaError_t launch_ulysses_a2a(const void* src, void* dst, int row_bytes, int B,
   m.C = L / (U * R);
   m.fold = causal && R > 1;
   const long long rows = static_cast<long long>(U) * R * B * H * m.C;
-  if (row_bytes % 16 == 0) {
-    const int vec16 = row_bytes / 16;
-    const long long n = rows * vec16;
-    ulysses_a2a_kernel<<<blocks_for(n), 256, 0, stream>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst),
-                                                          vec16, m, to_heads ? 1 : 0, n);
-  } else {  // one fp32 per row
+  if (row_bytes == 128 || row_bytes == 256) {  // rows of d = 64 or 128 bf16 values
+    const long long slices_ll = static_cast<long long>(U) * R * B * H;
+    const long long per_slice_ll = static_cast<long long>(m.C) * (row_bytes / 16);
+    if (slices_ll > INT_MAX || per_slice_ll > INT_MAX - 1024) return cudaErrorInvalidValue;
+    const int slices = static_cast<int>(slices_ll);
+    const int per_slice = static_cast<int>(per_slice_ll);
+    const dim3 grid(static_cast<unsigned>((per_slice + 1023) / 1024), static_cast<unsigned>(slices < 65535 ? slices : 65535),
+                    static_cast<unsigned>((slices + 65534) / 65535));
+    if (row_bytes == 256)
+      ulysses_a2a_kernel<16><<<grid, 256, 0, stream>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst), m,
+                                                       to_heads ? 1 : 0, slices);
+    else
+      ulysses_a2a_kernel<8><<<grid, 256, 0, stream>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst), m,
+                                                      to_heads ? 1 : 0, slices);
+  } else if (row_bytes == 4) {  // one fp32 per row
     ulysses_a2a_rows_kernel<<<blocks_for(rows), 256, 0, stream>>>(static_cast<const float*>(src),
                                                                   static_cast<float*>(dst), m, to_heads ? 1 : 0, rows);
+  } else {
+    return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
 }
