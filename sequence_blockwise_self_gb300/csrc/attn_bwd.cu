@@ -733,17 +733,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   if (warp == 2) tmem_dealloc(tmem, 512);
 }
 
-// One warp per row: stores -D_i = -sum_c dO_ic o_ic and -lse_i log2(e) (0 and
-// -inf for padded rows, whose probabilities are then 0), and zeroes the r-th
-// block of d floats of the fp32 dQ accumulator (whatever its layout, the
-// blocks of all rows cover it) and, for rows below kv_rows, the rows of the
-// dK and dV accumulators (grouped-query attention; null otherwise).
-// The pre-pass, HBM-bound: a bf16 row of o (and of dO) is D/8 16-byte
-// pieces, so a warp covers 32/(D/8) rows at once and takes kIter such groups,
-// all loads issued before any use so that enough bytes are in flight; the row
-// sums reduce across the row's lanes by shuffles.  Each warp then zeroes the
-// accumulator chunks of its rows (the accumulators are B*Hq*Lpad*D and
-// B*Hkv*Lpad*D contiguous floats whatever their tiling).
+// The pre-pass: per row, -D_i = -sum_c dO_ic o_ic and -lse_i log2(e) (0 and
+// -inf for padded rows, whose probabilities are then 0); and the fp32 dQ
+// accumulator zeroed, with the dK and dV accumulators for rows below
+// kv_rows (grouped-query attention; null otherwise).  HBM-bound: a bf16 row
+// of o (and of dO) is D/8 16-byte pieces, so a warp covers 32/(D/8) rows at
+// once and takes kIter such groups, all loads issued before any use so that
+// enough bytes are in flight; the row sums reduce across the row's lanes by
+// shuffles.  Each warp then zeroes the accumulator chunks of its rows (the
+// accumulators are B*Hq*Lpad*D and B*Hkv*Lpad*D contiguous floats whatever
+// their tiling, so the chunks of all rows cover them).
 template <int D>
 __global__ void __launch_bounds__(256) ring_attn_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
                                                                 const __nv_bfloat16* __restrict__ dO,
