@@ -66,6 +66,29 @@ def capi_limit():
     return 64 * 1024 * 1024
 
 
+def test_noalloc_backward_at_the_size_limit():
+    """The largest MHA problem at d = 128 the static array serves: 129,024
+    rows, whose fp32 dQ accumulator and statistics leave 16 KB of the array
+    for the launch plan; the gradients equal ring_attn_bwd's, so the upper
+    end of the array (and the plan placed after the workspace) is right."""
+    lib_build.build()
+    ra.load()
+    B, Hq, Hkv, L, d, N, causal = 1, 16, 16, 8064, 128, 3, False
+    ws = ra.bwd_workspace_size(B, Hq, Hkv, L, d, N, causal)
+    assert capi_limit() - 16384 <= ws <= capi_limit() - 1024
+    q, k, v, dO = (t.cuda() for t in inputs.make_inputs(B, Hq, Hkv, L, d, seed=530))
+    o, lse = ra.ring_attn_fwd(q, k, v, N, causal)
+    dq_r, dk_r, dv_r = ra.ring_attn_bwd(q, k, v, o, lse, dO, N, causal)
+    dq, dk, dv = (torch.full_like(x, float("nan")) for x in (q, k, v))
+    ra.ring_attn_bwd_noalloc(q, k, v, o, lse, dO, N, causal, dq, dk, dv)
+    torch.cuda.synchronize()
+    st, site = ra.device_status()
+    assert st == 0, f"device status {st} at {site:#x}"
+    _close("dq", dq, dq_r)
+    _close("dk", dk, dk_r)
+    _close("dv", dv, dv_r)
+
+
 def test_noalloc_backward_captured_in_a_cuda_graph_and_replayed():
     """A call captured into a CUDA graph (after one plain call of the same
     shape) replays the whole backward: its gradients equal ring_attn_bwd's,
