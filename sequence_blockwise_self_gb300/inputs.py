@@ -61,6 +61,33 @@ def make_inputs(B, Hq, Hkv, L, d, seed, with_grad=True):
     return q, k, v, dO
 
 
+def head_seed(seed: int, tensor: int, b: int, h: int) -> int:
+    """Seed of one (tensor, batch, head) slice for head_rows: tensor 0..3 =
+    q, k, v, dO."""
+    return int(seed) * 1_000_003 + tensor * 100_003 + b * 1_009 + h
+
+
+def head_rows(L: int, d: int, seed: int):
+    """One head's [L, d] bf16 rows ~ N(0,1) (drawn in fp32, rounded)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    return torch.randn((L, d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+
+
+def make_inputs_by_head(B, Hq, Hkv, L, d, seed, device):
+    """q, k, v, dO built one head at a time on the CPU (head_rows, seeds from
+    head_seed) straight into tensors on `device`: for problems too large to
+    draw whole in host memory; any head can be drawn again alone."""
+    out = []
+    for t, H in enumerate((Hq, Hkv, Hkv, Hq)):
+        x = torch.empty((B, H, L, d), dtype=torch.bfloat16, device=device)
+        for b in range(B):
+            for h in range(H):
+                x[b, h].copy_(head_rows(L, d, head_seed(seed, t, b, h)))
+        out.append(x)
+    return tuple(out)
+
+
 def workload_inputs(w: Workload, seed=None, with_grad=True):
     s = WORKLOAD_SEEDS.get(w.name, 0) if seed is None else seed
     return make_inputs(w.B, w.Hq, w.Hkv, w.L, w.d, s, with_grad)

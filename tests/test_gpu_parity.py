@@ -209,6 +209,36 @@ def test_workload_128k_sampled_parity():
     _sampled_parity(w, [w.n_chunks])
 
 
+def test_past_two_to_the_31_elements():
+    """Causal GQA with 136 query heads of 131072 rows at d = 128: q, o, dO and
+    dq hold 2.28e9 elements each, past 2^31 (the fp32 dQ accumulator 9.1
+    GB), so any 32-bit element index on the path would wrap.  o, lse and dq
+    on the sampled rows of heads 0, 127, 128 (whose first element is element
+    2^31) and 135 against the fp64 oracle, which draws those heads again on
+    the CPU from their own seeds."""
+    B, Hq, Hkv, L, d, N, causal = 1, 136, 8, 131072, 128, 32, True
+    assert Hq * L * d > 2 ** 31
+    seed = 2 ** 31 % 1000
+    q, k, v, dO = inputs.make_inputs_by_head(B, Hq, Hkv, L, d, seed, "cuda")
+    o, lse = ra.ring_attn_fwd(q, k, v, N, causal)
+    dq, dk, dv = ra.ring_attn_bwd(q, k, v, o, lse, dO, N, causal)
+    torch.cuda.synchronize()
+    assert_status_ok()
+    del q, k, v, dO, dk, dv
+    rows = inputs.sample_rows(L, N, causal, 64, seed)
+    ri = torch.from_numpy(rows).long().cuda()
+    G = Hq // Hkv
+    for h in (0, 127, 128, 135):
+        g = h // G
+        one = lambda t, hh: inputs.head_rows(L, d, inputs.head_seed(seed, t, 0, hh)).double().numpy()[None, None]  # noqa: E731
+        qh, kg, vg, dOh = one(0, h), one(1, g), one(2, g), one(3, h)
+        o_ref, lse_ref, _ = oracle.fwd_rows(qh, kg, vg, causal, rows)
+        dq_ref, _, _ = oracle.bwd_rows(qh, kg, vg, dOh, causal, rows, np.zeros(0, np.int32))
+        assert_close(f"o head {h}", f64(o[:, h:h + 1, ri]), o_ref)
+        assert_close(f"lse head {h}", f64(lse[:, h:h + 1, ri]), lse_ref, TOL_LSE, TOL_LSE)
+        assert_close(f"dq head {h}", f64(dq[:, h:h + 1, ri]), dq_ref)
+
+
 def test_tiny_workload_full_parity():
     w = inputs.WORKLOADS["tiny"]
     q, k, v, dO = inputs.workload_inputs(w)

@@ -1,5 +1,6 @@
 """The seeded row samplers the parity tests use (host logic, no GPU)."""
 import numpy as np
+import torch
 
 from sequence_blockwise_self_gb300 import inputs
 
@@ -30,3 +31,22 @@ def test_sample_rows_within_a_window():
 def test_sample_rows_small_range_returns_all_rows():
     assert np.array_equal(inputs.sample_rows(100, 2, False, 256, seed=0), np.arange(100))
     assert np.array_equal(inputs.sample_rows(100, 2, False, 256, seed=0, lo=60), np.arange(60, 100))
+
+
+def test_inputs_by_head_are_seeded_per_head_and_redrawable():
+    """The head-by-head generator: every (tensor, batch, head) slice has its
+    own seed, the result is reproducible, and any head drawn again alone
+    equals its slice of the whole."""
+    B, Hq, Hkv, L, d = 2, 4, 2, 64, 16
+    a = inputs.make_inputs_by_head(B, Hq, Hkv, L, d, 7, "cpu")
+    b = inputs.make_inputs_by_head(B, Hq, Hkv, L, d, 7, "cpu")
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    q, k, v, dO = a
+    assert q.shape == (B, Hq, L, d) and k.shape == (B, Hkv, L, d) and dO.shape == q.shape
+    assert torch.equal(q[1, 3], inputs.head_rows(L, d, inputs.head_seed(7, 0, 1, 3)))
+    assert torch.equal(v[0, 1], inputs.head_rows(L, d, inputs.head_seed(7, 2, 0, 1)))
+    seeds = {inputs.head_seed(7, t, bb, h) for t in range(4) for bb in range(B) for h in range(Hq)}
+    assert len(seeds) == 4 * B * Hq
+    assert not torch.equal(q[0, 0], dO[0, 0]) and not torch.equal(k[0, 0], v[0, 0])
+    assert abs(float(q.float().mean())) < 0.05 and abs(float(q.float().std()) - 1.0) < 0.05
